@@ -1,0 +1,355 @@
+"""fp64 reference definitions of the paged KV cache hot path (test infrastructure).
+
+Each function restates one step the pages describe, in the plainest form that
+reaches the defined result: the block table is resolved into a contiguous K/V,
+then textbook softmax attention runs on it.  Source keys ([AGENTIC], [NOTES],
+[LINEAGE], [ARCH]) are listed in ``oracle/__init__.py``.
+
+Storage convention (the data the CUDA path reads and writes, restated here
+independently):
+
+* a KV cache is two arrays ``k_cache``, ``v_cache`` of raw element bits with
+  shape ``[num_blocks][num_kv_heads][block_size][head_size]``;
+* a token written to flat slot ``s`` lands in physical block ``s // block_size``
+  at offset ``s % block_size``; a negative slot is a padding token;
+* query head ``h`` reads KV head ``h // (num_q_heads // num_kv_heads)``;
+* the ``q_len`` new tokens of a request are the last ``q_len`` positions of its
+  ``seq_len`` tokens; a query at position ``p`` attends keys ``0..p`` when causal.
+
+Element types are named by strings: ``"f32"``, ``"f16"``, ``"bf16"``,
+``"fp8_e4m3"``.  Arrays of bits use uint32 / uint16 / uint16 / uint8.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+DTYPE_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "fp8_e4m3": 1}
+_BITS = {"f32": np.uint32, "f16": np.uint16, "bf16": np.uint16, "fp8_e4m3": np.uint8}
+
+# Largest finite FP8 e4m3 magnitude: exponent field 15, mantissa 6 -> 1.75 * 2^8.
+E4M3_MAX = 448.0
+
+
+# --------------------------------------------------------------------------
+# Block arithmetic and byte counts
+# --------------------------------------------------------------------------
+
+def blocks_needed(num_tokens: int, block_size: int) -> int:
+    """Number of fixed-size blocks that hold ``num_tokens`` tokens.
+
+    [ARCH] Part 1, allocate_slots: the count of blocks is the token count
+    divided by the block size, rounded up (17 new tokens at block size 16 take
+    2 blocks).  Written as integer ceiling division.
+    """
+    if num_tokens < 0 or block_size <= 0:
+        raise ValueError("num_tokens must be >= 0 and block_size > 0")
+    return (num_tokens + block_size - 1) // block_size
+
+
+def bytes_per_block(block_size: int, num_kv_heads: int, head_size: int,
+                    dtype_bytes: int) -> int:
+    """Bytes one physical KV block occupies for one transformer layer.
+
+    [ARCH] Part 1, KV cache manager: 2 x block_size x num_kv_heads x head_size
+    x dtype_bytes (the 2 counts K and V).
+    """
+    return 2 * block_size * num_kv_heads * head_size * dtype_bytes
+
+
+def kv_cache_bytes(num_layers: int, dtype_bytes: int, num_kv_heads: int,
+                   head_dim: int, seq_lens) -> int:
+    """Total KV bytes of a set of requests.
+
+    [LINEAGE] "KV Cache：动态批处理把显存变成主资源", the M_KV equation:
+    M_KV = 2 * L * b * H_kv * d_h * sum_i T_i, the factor 2 counting K and V.
+    """
+    return 2 * num_layers * dtype_bytes * num_kv_heads * head_dim * int(sum(int(t) for t in seq_lens))
+
+
+# --------------------------------------------------------------------------
+# Element codecs
+# --------------------------------------------------------------------------
+
+def e4m3_value(code: int) -> float:
+    """Value of one FP8 e4m3 code, from its bit fields.
+
+    Lower-precision KV is the [NOTES] engine-argument ``--kv-cache-dtype``
+    (附录：参数速查).  Format: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa
+    bits; exponent field 0 holds subnormals m/8 * 2^-6; S.1111.111 is NaN;
+    there is no infinity.
+    """
+    code = int(code) & 0xFF
+    sign = -1.0 if code & 0x80 else 1.0
+    exp_field = (code >> 3) & 0xF
+    mant = code & 0x7
+    if exp_field == 0xF and mant == 0x7:
+        return math.nan
+    if exp_field == 0:
+        return sign * (mant / 8.0) * 2.0 ** -6
+    return sign * (1.0 + mant / 8.0) * 2.0 ** (exp_field - 7)
+
+
+def e4m3_table() -> np.ndarray:
+    """float64 value of every one of the 256 e4m3 codes."""
+    return np.array([e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+_E4M3 = e4m3_table()
+# Non-negative finite magnitudes, codes 0..126, strictly increasing.
+_E4M3_POS = _E4M3[:127]
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Round float64 values to FP8 e4m3 codes: nearest, ties to even, saturating.
+
+    For each |x| the two neighbouring representable magnitudes are found and
+    the nearer one is taken; on an exact tie the code with an even (zero)
+    least-significant mantissa bit wins.  Magnitudes at or above 448 give 448
+    (saturation to the largest finite value).  The sign is kept, so small
+    negative values give negative zero (0x80).  NaN gives 0x7F.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    flat = x.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint8)
+    for i, v in enumerate(flat):
+        if math.isnan(v):
+            out[i] = 0x7F
+            continue
+        a = abs(v)
+        if a >= E4M3_MAX:
+            code = 126
+        else:
+            hi = int(np.searchsorted(_E4M3_POS, a, side="right"))  # first magnitude > a
+            lo = hi - 1                                            # magnitude <= a
+            d_lo = a - _E4M3_POS[lo]
+            d_hi = _E4M3_POS[hi] - a
+            if d_lo < d_hi:
+                code = lo
+            elif d_hi < d_lo:
+                code = hi
+            else:
+                code = lo if lo % 2 == 0 else hi
+        out[i] = code | (0x80 if math.copysign(1.0, v) < 0 else 0)
+    return out.reshape(x.shape)
+
+
+def quantize_e4m3(x64, scale: float) -> np.ndarray:
+    """FP8 code stored for a value ``x`` with a per-tensor fp32 scale.
+
+    The stored code is the e4m3 rounding of the fp32 quotient x / scale.  The
+    quotient is formed in float64 and rounded once to float32; since float64
+    has more than 2*24+2 significand bits this equals the correctly rounded
+    float32 quotient.  The float32 is then rounded to e4m3 (``e4m3_encode``).
+    """
+    q32 = (np.asarray(x64, dtype=np.float64) / np.float64(np.float32(scale))).astype(np.float32)
+    return e4m3_encode(q32.astype(np.float64))
+
+
+def decode_bits(bits, dtype: str, scale: float = 1.0) -> np.ndarray:
+    """Exact float64 value of stored elements given as raw bits.
+
+    fp32 / fp16 widen exactly; bf16 is the upper half of an fp32 and widens
+    exactly; FP8 e4m3 is looked up from its bit fields and multiplied by the
+    per-tensor scale in float64.
+    """
+    b = np.asarray(bits)
+    if dtype == "f32":
+        return b.astype(np.uint32).view(np.float32).astype(np.float64)
+    if dtype == "f16":
+        return b.astype(np.uint16).view(np.float16).astype(np.float64)
+    if dtype == "bf16":
+        return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    if dtype == "fp8_e4m3":
+        return _E4M3[b.astype(np.uint8)] * np.float64(np.float32(scale))
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+# --------------------------------------------------------------------------
+# KV write: reshape_and_cache
+# --------------------------------------------------------------------------
+
+def reshape_and_cache(key_bits, value_bits, k_cache, v_cache, slot_mapping,
+                      block_size: int, src_dtype: str, cache_dtype: str,
+                      k_scale: float = 1.0, v_scale: float = 1.0) -> None:
+    """Write each new token's K and V into its slot of the paged cache, in place.
+
+    [NOTES] "Prefill 与 Decode": prefill stores K/V for every prompt token and
+    each decode step appends the new token's K/V.  [ARCH] Part 1, forward pass:
+    input preparation builds ``slot_mapping``, one flat slot per new token.
+    Slot s lands in block s // block_size, offset s % block_size; a negative
+    slot is padding and is skipped.  With the same element type the bits are
+    copied; with an FP8 cache each value is quantised with ``quantize_e4m3``.
+    """
+    key_bits = np.asarray(key_bits)
+    value_bits = np.asarray(value_bits)
+    for t, slot in enumerate(np.asarray(slot_mapping, dtype=np.int64)):
+        slot = int(slot)
+        if slot < 0:
+            continue
+        blk, off = slot // block_size, slot % block_size
+        if cache_dtype == src_dtype:
+            k_cache[blk, :, off, :] = key_bits[t]
+            v_cache[blk, :, off, :] = value_bits[t]
+        elif cache_dtype == "fp8_e4m3":
+            k_cache[blk, :, off, :] = quantize_e4m3(decode_bits(key_bits[t], src_dtype), k_scale)
+            v_cache[blk, :, off, :] = quantize_e4m3(decode_bits(value_bits[t], src_dtype), v_scale)
+        else:
+            raise ValueError(f"unsupported {src_dtype} -> {cache_dtype}")
+
+
+# --------------------------------------------------------------------------
+# Block-table resolution and attention
+# --------------------------------------------------------------------------
+
+def gather_kv(cache_bits, block_table_row, num_tokens: int, block_size: int,
+              dtype: str, scale: float = 1.0) -> np.ndarray:
+    """Contiguous float64 K (or V) ``[num_tokens][num_kv_heads][head_size]`` of one request.
+
+    [LINEAGE] "PagedAttention：把逻辑连续与物理连续分开": (sequence, logical
+    block) maps to a physical block; the kernel reads K/V through the block
+    table.  [AGENTIC] "統一分頁 + 共用池": physical blocks need not be
+    contiguous.  Position ``pos`` lives in physical block
+    ``block_table_row[pos // block_size]`` at offset ``pos % block_size``.
+    """
+    pos = np.arange(num_tokens, dtype=np.int64)
+    phys = np.asarray(block_table_row, dtype=np.int64)[pos // block_size]
+    off = pos % block_size
+    return decode_bits(np.asarray(cache_bits)[phys, :, off, :], dtype, scale)
+
+
+def query_positions(seq_len: int, q_len: int) -> np.ndarray:
+    """Positions of a request's new query tokens: the last ``q_len`` of ``seq_len``.
+
+    [ARCH] Part 1, forward pass: all sequences are flattened into one long
+    sequence and position indices plus a mask keep each token to its own
+    sequence; [LINEAGE] "Chunked prefill": a chunk's tokens follow the already
+    cached prefix.  Query j sits at position seq_len - q_len + j.
+    """
+    if not (1 <= q_len <= seq_len):
+        raise ValueError("need 1 <= q_len <= seq_len")
+    return np.arange(seq_len - q_len, seq_len, dtype=np.int64)
+
+
+def softmax_weights(scores) -> np.ndarray:
+    """Normalised softmax weights exp(s_i - max s) / sum_j exp(s_j - max s)."""
+    s = np.asarray(scores, dtype=np.float64)
+    w = np.exp(s - s.max())
+    return w / w.sum()
+
+
+def attend(q64, K64, V64, positions, scale: float, causal: bool = True) -> np.ndarray:
+    """Textbook softmax attention of one request's queries over its contiguous K/V.
+
+    q64 ``[n][Hq][d]``, K64 / V64 ``[T][Hkv][d]`` (float64), ``positions[n]``.
+    For query j and head h with KV head g = h // (Hq // Hkv):
+    s_t = scale * <q_j,h , k_t,g> for t = 0..p_j (or 0..T-1 when not causal),
+    out = sum_t exp(s_t - max s) v_t,g / sum_t exp(s_t - max s).
+    [AGENTIC] "Online softmax 到底在幹嘛" gives the weighted average
+    sum exp(score) * value / sum exp(score) and the max shift before exp.
+    """
+    q64 = np.asarray(q64, dtype=np.float64)
+    n, hq, d = q64.shape
+    hkv = K64.shape[1]
+    if hq % hkv:
+        raise ValueError("num_q_heads must be a multiple of num_kv_heads")
+    group = hq // hkv
+    out = np.empty((n, hq, d), dtype=np.float64)
+    for j in range(n):
+        last = int(positions[j]) if causal else K64.shape[0] - 1
+        for g in range(hkv):
+            heads = slice(g * group, (g + 1) * group)
+            k = K64[: last + 1, g, :]                       # [L][d]
+            v = V64[: last + 1, g, :]
+            s = scale * (k @ q64[j, heads, :].T)              # [L][group]
+            w = np.exp(s - s.max(axis=0, keepdims=True))
+            out[j, heads, :] = (w.T @ v) / w.sum(axis=0)[:, None]
+    return out
+
+
+def paged_varlen(q_bits, q_dtype: str, k_cache, v_cache, kv_dtype: str,
+                 block_tables, query_start_loc, seq_lens, block_size: int,
+                 scale: float, causal: bool = True, k_scale: float = 1.0,
+                 v_scale: float = 1.0, rows=None) -> np.ndarray:
+    """Attention of a flattened variable-length batch over a paged KV cache.
+
+    Request r owns query rows query_start_loc[r] .. query_start_loc[r+1]-1 and
+    has seq_lens[r] tokens of context including its new tokens.  [ARCH] Part 1
+    (flattened super-sequence; V1 mixes prefill chunks and decodes in one
+    step); [LINEAGE] "静态 batching" (per-step token budget sum q_i <= K with
+    q_i = 1 for a decode).  Returns float64 ``[total_q][Hq][d]``; when ``rows``
+    lists flattened query rows only those are computed and the rest are NaN.
+    """
+    q64 = decode_bits(q_bits, q_dtype)
+    qsl = np.asarray(query_start_loc, dtype=np.int64)
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    out = np.full(q64.shape, np.nan, dtype=np.float64)
+    wanted = None if rows is None else set(int(r) for r in rows)
+    for r in range(len(lens)):
+        lo, hi = int(qsl[r]), int(qsl[r + 1])
+        if hi <= lo:
+            continue
+        sel = [j for j in range(lo, hi) if wanted is None or j in wanted]
+        if not sel:
+            continue
+        L = int(lens[r])
+        pos = query_positions(L, hi - lo)
+        K = gather_kv(k_cache, block_tables[r], L, block_size, kv_dtype, k_scale)
+        V = gather_kv(v_cache, block_tables[r], L, block_size, kv_dtype, v_scale)
+        idx = np.array(sel, dtype=np.int64)
+        out[idx] = attend(q64[idx], K, V, pos[idx - lo], scale, causal)
+    return out
+
+
+def paged_decode(q_bits, q_dtype: str, k_cache, v_cache, kv_dtype: str,
+                 block_tables, seq_lens, block_size: int, scale: float,
+                 k_scale: float = 1.0, v_scale: float = 1.0, seqs=None) -> np.ndarray:
+    """PagedAttention decode: one new query token per sequence, at its last position.
+
+    [NOTES] "Prefill 与 Decode": the new token's Q attends the K/V of all
+    cached tokens.  This is ``paged_varlen`` with q_len = 1 for every request.
+    ``seqs`` optionally restricts the computation to some sequences (others NaN).
+    """
+    b = len(seq_lens)
+    qsl = np.arange(b + 1, dtype=np.int64)
+    return paged_varlen(q_bits, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
+                        qsl, seq_lens, block_size, scale, True, k_scale, v_scale,
+                        rows=seqs)
+
+
+# --------------------------------------------------------------------------
+# Partial softmax states and their merge (split-K / context-parallel algebra)
+# --------------------------------------------------------------------------
+
+def softmax_partial(scores, values):
+    """Partial state (m, l, acc) of one slice of keys.
+
+    m = max score, l = sum exp(s - m), acc = sum exp(s - m) * v.  [AGENTIC]
+    "Online softmax 到底在幹嘛": each part hands over a weighted sum and a
+    weight sum, after subtracting its own local maximum.
+    """
+    s = np.asarray(scores, dtype=np.float64)
+    v = np.asarray(values, dtype=np.float64)
+    m = float(s.max())
+    w = np.exp(s - m)
+    return m, float(w.sum()), w @ v
+
+
+def merge_partials(parts):
+    """Merge partial states: rescale each by exp(m_j - m) to the global max, then add.
+
+    [AGENTIC] "Online softmax 到底在幹嘛": the parts' weighted sums and weight
+    sums are added and divided once; the local maxima are brought to the global
+    maximum with a correction factor first.
+    """
+    m = max(p[0] for p in parts)
+    l = sum(p[1] * math.exp(p[0] - m) for p in parts)
+    acc = sum(np.asarray(p[2], dtype=np.float64) * math.exp(p[0] - m) for p in parts)
+    return m, l, acc
+
+
+def finalize_partial(part):
+    """Output of a (merged) partial state: acc / l."""
+    return np.asarray(part[2], dtype=np.float64) / part[1]

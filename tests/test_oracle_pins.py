@@ -1,0 +1,509 @@
+"""Pins of the fp64 oracle to facts that do not come from the oracle itself.
+
+Each ``check_*`` function measures one pin against an implementation passed in
+(the real oracle by default), so ``test_planted_mistakes_are_caught`` can feed
+deliberately broken copies and show that some pin fails for each mistake.
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ---------------------------------------------------------------- block math
+
+def test_block_count_golden():
+    for n, bs, nb in _golden_rows("block_count.txt"):
+        assert oracle.blocks_needed(int(n), int(bs)) == int(nb)
+
+
+def test_internal_waste_below_one_block():
+    # [LINEAGE] PagedAttention section: internal waste of a sequence is < P_b slots.
+    for bs in (1, 16, 32):
+        for n in range(0, 2000):
+            waste = oracle.blocks_needed(n, bs) * bs - n
+            assert 0 <= waste < bs
+
+
+@pytest.mark.parametrize("factory", [workloads.tiny,
+                                     lambda: workloads.build("x", 5, [40, 3], [1, 1], 8, 8, 128, 16, "bf16"),
+                                     lambda: workloads.build("y", 6, [70, 64], [1, 1], 32, 8, 128, 32, "fp8_e4m3")])
+def test_bytes_per_block_matches_allocated_tensors(factory):
+    b = factory()
+    per_block = (b.k_cache.nbytes + b.v_cache.nbytes) // b.num_blocks
+    assert per_block == oracle.bytes_per_block(b.block_size, b.num_kv_heads, b.head_size,
+                                               oracle.DTYPE_BYTES[b.kv_dtype])
+
+
+def test_per_block_bytes_of_the_named_configs():
+    # tiny fp32, Llama bf16 block 16, FP8 block 32: the allocations the workloads make.
+    assert oracle.bytes_per_block(16, 2, 64, 4) == 2 * 16 * 2 * 64 * 4 == 16384
+    assert np.zeros((1, 8, 16, 128), np.uint16).nbytes * 2 == oracle.bytes_per_block(16, 8, 128, 2)
+    assert np.zeros((1, 8, 32, 128), np.uint8).nbytes * 2 == oracle.bytes_per_block(32, 8, 128, 1)
+
+
+def test_byte_count_golden():
+    rows = _golden_rows("byte_counts.txt")
+    for heads, pos, dim, eb, k_only in rows[:2]:
+        total = oracle.kv_cache_bytes(1, int(eb), int(heads), int(dim), [int(pos)])
+        assert total // 2 == int(k_only)  # M_KV counts K and V; the page counts K only
+    L, hkv, d, eb, bs, budget, tokens, ttok, tmb = rows[2]
+    per_block_all_layers = int(L) * oracle.bytes_per_block(int(bs), int(hkv), int(d), int(eb))
+    assert (int(budget) // per_block_all_layers) * int(bs) == int(tokens)
+    transfer = oracle.blocks_needed(int(ttok), int(bs)) * per_block_all_layers
+    assert abs(transfer / 2**20 - float(tmb)) < 6e-4
+
+
+# ---------------------------------------------------------------- FP8 codec
+
+def test_e4m3_decode_exhaustive_vs_torch():
+    ours = oracle.e4m3_table()
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ours[ok], ref[ok])
+    assert np.isnan(ours[0x7F]) and np.isnan(ours[0xFF])
+    assert ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9
+
+
+def _encode_sweep():
+    mags = oracle.e4m3_table()[:127]
+    mids = (mags[:-1] + mags[1:]) / 2                       # exact ties
+    pts = np.concatenate([mags, mids, np.nextafter(mids, 0), np.nextafter(mids, np.inf)])
+    rng = np.random.default_rng(7)
+    pts = np.concatenate([pts, rng.uniform(0, 463.9, 4000), rng.uniform(0, 2 ** -6, 2000),
+                          np.float64(2.0) ** rng.uniform(-12, 8.8, 2000)])
+    pts = pts[pts < 464.0].astype(np.float32).astype(np.float64)  # values an fp32 quotient can take
+    return np.concatenate([pts, -pts, [0.0, -0.0]])
+
+
+def check_e4m3_encode(encode):
+    x = _encode_sweep()
+    ours = encode(x)
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return int(np.count_nonzero(ours != ref))
+
+
+def test_e4m3_encode_vs_torch_in_range():
+    assert check_e4m3_encode(oracle.e4m3_encode) == 0
+
+
+def test_e4m3_encode_saturates_and_nan():
+    codes = oracle.e4m3_encode(np.array([448.0, 463.99, 464.0, 1e6, np.inf, -1e6, -np.inf, np.nan]))
+    assert list(codes) == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE, 0x7F]
+
+
+def test_quantize_with_non_power_of_two_scale_vs_torch():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(5000).astype(np.float32)
+    scale = np.float32(0.0123)
+    ref_q = torch.from_numpy(x) / torch.tensor(scale)          # IEEE fp32 division
+    keep = (ref_q.abs() < 464).numpy()
+    ref = ref_q.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ours = oracle.quantize_e4m3(x.astype(np.float64), float(scale))
+    assert np.array_equal(ours[keep], ref[keep])
+
+
+def test_decode_bits_vs_torch_casts():
+    rng = np.random.default_rng(1)
+    x = torch.from_numpy(rng.standard_normal(1000).astype(np.float32) * 100)
+    for dt, tdt in (("f32", torch.float32), ("f16", torch.float16), ("bf16", torch.bfloat16)):
+        bits = workloads.torch_to_bits(x.to(tdt), dt)
+        assert np.array_equal(oracle.decode_bits(bits, dt), x.to(tdt).to(torch.float64).numpy())
+
+
+# ---------------------------------------------------------------- scatter
+
+def test_scatter_round_trip_and_padding():
+    b = workloads.build("s", 11, [5, 33, 16], [5, 2, 1], 4, 2, 64, 16, "bf16")
+    k0, v0 = b.k_cache.copy(), b.v_cache.copy()
+    kc, vc = b.k_cache.copy(), b.v_cache.copy()
+    slots = b.slot_mapping.copy()
+    slots[3] = -1                                           # a padding token
+    oracle.reshape_and_cache(b.key, b.value, kc, vc, slots, 16, "bf16", "bf16")
+    touched = np.zeros(kc.shape[0] * 16, bool)
+    for t, s in enumerate(slots):
+        if s < 0:
+            continue
+        touched[s] = True
+        assert np.array_equal(kc[s // 16, :, s % 16, :], b.key[t])
+        assert np.array_equal(vc[s // 16, :, s % 16, :], b.value[t])
+    # every other slot is unchanged
+    flat_k = kc.transpose(0, 2, 1, 3).reshape(-1, 2, 64)
+    flat_k0 = k0.transpose(0, 2, 1, 3).reshape(-1, 2, 64)
+    assert np.array_equal(flat_k[~touched], flat_k0[~touched])
+    assert np.array_equal(vc.transpose(0, 2, 1, 3).reshape(-1, 2, 64)[~touched],
+                          v0.transpose(0, 2, 1, 3).reshape(-1, 2, 64)[~touched])
+
+
+def test_scatter_fp8_codes_are_nearest():
+    b = workloads.build("s8", 12, [40, 7], [3, 1], 8, 2, 128, 32, "fp8_e4m3")
+    kc, vc = b.k_cache.copy(), b.v_cache.copy()
+    oracle.reshape_and_cache(b.key, b.value, kc, vc, b.slot_mapping, 32, "bf16", "fp8_e4m3",
+                             b.k_scale, b.v_scale)
+    table = oracle.e4m3_table()
+    mags = table[:127]
+    for t, s in enumerate(b.slot_mapping):
+        x = oracle.decode_bits(b.key[t], "bf16") / b.k_scale
+        got = table[kc[s // 32, :, s % 32, :]]
+        # nearest representable magnitude (brute force over the table)
+        dist = np.abs(np.abs(x)[..., None] - mags)
+        best = dist.min(axis=-1)
+        assert np.all(np.abs(np.abs(got) - np.abs(x)) <= best + 0.0)
+        assert np.all((got == 0) | (np.sign(got) == np.sign(x)))
+
+
+# ---------------------------------------------------------------- softmax merge
+
+def check_merge_golden(partial, merge, finalize):
+    rows = _golden_rows("online_softmax_merge.txt")
+    parts = []
+    err = 0.0
+    for tag, w, v, ws, wsum in rows[:2]:
+        w = [float(a) for a in w.split(",")]
+        v = [[float(a)] for a in v.split(",")]
+        m, l, acc = partial(np.log(w), v)
+        # undo the local max shift to compare with the page's un-shifted sums
+        err = max(err, abs(acc[0] * math.exp(m) - float(ws)), abs(l * math.exp(m) - float(wsum)))
+        parts.append((m, l, acc))
+    _, total_ws, total_w, result = rows[2]
+    merged = merge(parts)
+    err = max(err, abs(merged[2][0] * math.exp(merged[0]) - float(total_ws)),
+              abs(merged[1] * math.exp(merged[0]) - float(total_w)),
+              abs(finalize(merged)[0] - float(result)))
+    return err
+
+
+def test_online_softmax_merge_golden():
+    assert check_merge_golden(oracle.softmax_partial, oracle.merge_partials,
+                              oracle.finalize_partial) < 1e-9
+
+
+def test_merge_of_any_split_equals_whole():
+    rng = np.random.default_rng(5)
+    s = rng.standard_normal(300) * 4
+    v = rng.standard_normal((300, 7))
+    whole = oracle.finalize_partial(oracle.softmax_partial(s, v))
+    for cuts in ([150], [1, 2, 299], [10, 20, 30, 200]):
+        edges = [0] + cuts + [300]
+        parts = [oracle.softmax_partial(s[a:b], v[a:b]) for a, b in zip(edges[:-1], edges[1:])]
+        assert np.allclose(oracle.finalize_partial(oracle.merge_partials(parts)), whole,
+                           atol=1e-13, rtol=0)
+    assert np.allclose(whole, oracle.softmax_weights(s) @ v, atol=1e-13)
+
+
+def test_softmax_rows_sum_to_one():
+    rng = np.random.default_rng(9)
+    for n in (1, 2, 17, 1000):
+        s = rng.standard_normal(n) * 30
+        w = oracle.softmax_weights(s)
+        assert abs(w.sum() - 1.0) < 1e-12 and np.all(w >= 0)
+        assert np.allclose(oracle.softmax_weights(s + 1234.5), w, atol=1e-15)
+
+
+# ---------------------------------------------------------------- attention
+
+def _contiguous_case(seed, T, hq, hkv, d, q_len, bs=4):
+    """One request whose blocks are stored in order (identity block table), fp32."""
+    rng = np.random.default_rng(seed)
+    nb = -(-T // bs)
+    kc = rng.standard_normal((nb, hkv, bs, d)).astype(np.float32)
+    vc = rng.standard_normal((nb, hkv, bs, d)).astype(np.float32)
+    q = rng.standard_normal((q_len, hq, d)).astype(np.float32)
+    table = np.arange(nb, dtype=np.int32)[None, :]
+    return q, kc, vc, table
+
+
+def _run_varlen(attend_impl, gather_impl, q, kc, vc, table, lens, q_lens, bs, scale, causal=True):
+    """Oracle's paged_varlen with its inner steps replaceable (for planted mistakes)."""
+    qsl = np.concatenate([[0], np.cumsum(q_lens)])
+    out = np.zeros(q.shape, np.float64)
+    for r in range(len(lens)):
+        L = int(lens[r])
+        K = gather_impl(kc.view(np.uint32), table[r], L, bs, "f32")
+        V = gather_impl(vc.view(np.uint32), table[r], L, bs, "f32")
+        pos = oracle.query_positions(L, int(q_lens[r]))
+        out[qsl[r]:qsl[r + 1]] = attend_impl(q[qsl[r]:qsl[r + 1]].astype(np.float64), K, V, pos,
+                                             scale, causal)
+    return out
+
+
+def check_sdpa(attend_impl=oracle.attend, gather_impl=oracle.gather_kv):
+    """Identity placement, one request: equals torch SDPA in fp64 (GQA by repeat_interleave)."""
+    err = 0.0
+    for seed, T, hq, hkv, d, q_len in ((0, 37, 8, 2, 16, 5), (1, 9, 4, 4, 8, 1), (2, 64, 6, 3, 32, 64)):
+        q, kc, vc, table = _contiguous_case(seed, T, hq, hkv, d, q_len)
+        scale = 0.3
+        ours = _run_varlen(attend_impl, gather_impl, q, kc, vc, table, [T], [q_len], 4, scale)
+        K = torch.from_numpy(kc.transpose(1, 0, 2, 3).reshape(hkv, -1, d)[:, :T].astype(np.float64))
+        V = torch.from_numpy(vc.transpose(1, 0, 2, 3).reshape(hkv, -1, d)[:, :T].astype(np.float64))
+        K = K.repeat_interleave(hq // hkv, dim=0)
+        V = V.repeat_interleave(hq // hkv, dim=0)
+        Q = torch.from_numpy(q.astype(np.float64)).transpose(0, 1)          # [hq][q_len][d]
+        pos = torch.arange(T - q_len, T)
+        mask = torch.arange(T)[None, :] <= pos[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=mask, scale=scale)
+        err = max(err, float(np.abs(ours - ref.transpose(0, 1).numpy()).max()))
+    return err
+
+
+def test_identity_placement_equals_library_sdpa():
+    assert check_sdpa() < 1e-12
+
+
+def _brute_force(q, kc, vc, table, lens, q_lens, bs, scale, group):
+    """Pure-Python loops over lists, math.exp; tiny inputs only."""
+    out = []
+    start = 0
+    for r, (L, ql) in enumerate(zip(lens, q_lens)):
+        for j in range(ql):
+            p = L - ql + j
+            row = []
+            for h in range(q.shape[1]):
+                g = h // group
+                keys, vals = [], []
+                for t in range(p + 1):
+                    blk = int(table[r][t // bs])
+                    keys.append([float(x) for x in kc[blk, g, t % bs]])
+                    vals.append([float(x) for x in vc[blk, g, t % bs]])
+                qv = [float(x) for x in q[start + j, h]]
+                sc = [scale * sum(a * b for a, b in zip(qv, k)) for k in keys]
+                mx = max(sc)
+                w = [math.exp(s - mx) for s in sc]
+                tot = sum(w)
+                row.append([sum(w[t] * vals[t][i] for t in range(len(w))) / tot
+                            for i in range(len(qv))])
+            out.append(row)
+        start += ql
+    return np.array(out)
+
+
+def check_brute_force(attend_impl=oracle.attend, gather_impl=oracle.gather_kv):
+    rng = np.random.default_rng(21)
+    bs, hq, hkv, d = 2, 4, 2, 4
+    lens, q_lens = [5, 3, 6], [2, 1, 6]
+    nb = 12
+    kc = rng.standard_normal((nb, hkv, bs, d)).astype(np.float32)
+    vc = rng.standard_normal((nb, hkv, bs, d)).astype(np.float32)
+    perm = rng.permutation(nb).astype(np.int32)
+    table = np.full((3, 3), -1, np.int32)
+    table[0, :3], table[1, :2], table[2, :3] = perm[:3], perm[3:5], perm[5:8]
+    q = rng.standard_normal((sum(q_lens), hq, d)).astype(np.float32)
+    ours = _run_varlen(attend_impl, gather_impl, q, kc, vc, table, lens, q_lens, bs, 0.7)
+    ref = _brute_force(q, kc, vc, table, lens, q_lens, bs, 0.7, hq // hkv)
+    return float(np.abs(ours - ref).max())
+
+
+def test_brute_force_tiny():
+    assert check_brute_force() < 1e-12
+
+
+def test_closed_forms():
+    rng = np.random.default_rng(4)
+    d, hq, hkv, bs = 8, 4, 2, 4
+    # constant V -> output equals that constant row, whatever the scores
+    T = 11
+    kc = rng.standard_normal((3, hkv, bs, d)).astype(np.float32)
+    vc = np.broadcast_to(rng.standard_normal((1, hkv, 1, d)), (3, hkv, bs, d)).astype(np.float32).copy()
+    q = rng.standard_normal((1, hq, d)).astype(np.float32)
+    out = oracle.paged_decode(q.view(np.uint32), "f32", kc.view(np.uint32), vc.view(np.uint32), "f32",
+                              np.array([[2, 0, 1]], np.int32), [T], bs, 1.0)
+    for h in range(hq):
+        assert np.allclose(out[0, h], vc[0, h // 2, 0], atol=1e-14)
+    # q = 0 -> uniform weights -> mean of V over positions 0..p
+    q0 = np.zeros((1, hq, d), np.float32)
+    vc = rng.standard_normal((3, hkv, bs, d)).astype(np.float32)
+    out = oracle.paged_decode(q0.view(np.uint32), "f32", kc.view(np.uint32), vc.view(np.uint32), "f32",
+                              np.array([[2, 0, 1]], np.int32), [T], bs, 1.0)
+    V = vc[[2, 0, 1]].transpose(1, 0, 2, 3).reshape(hkv, -1, d)[:, :T].astype(np.float64)
+    for h in range(hq):
+        assert np.allclose(out[0, h], V[h // 2].mean(axis=0), atol=1e-14)
+    # seq_len 1 -> output is v_0
+    out = oracle.paged_decode(q.view(np.uint32), "f32", kc.view(np.uint32), vc.view(np.uint32), "f32",
+                              np.array([[1, -1, -1]], np.int32), [1], bs, 1.0)
+    for h in range(hq):
+        assert np.array_equal(out[0, h], vc[1, h // 2, 0].astype(np.float64))
+
+
+def check_permutation_invariance(attend_impl=oracle.attend, gather_impl=oracle.gather_kv):
+    """The same logical K/V stored under two placements gives identical outputs."""
+    rng = np.random.default_rng(8)
+    bs, hq, hkv, d = 4, 8, 2, 16
+    lens, q_lens = [13, 29, 4], [1, 3, 4]
+    need = [-(-n // bs) for n in lens]
+    logical_k = [rng.standard_normal((n, hkv, bs, d)).astype(np.float32) for n in need]
+    logical_v = [rng.standard_normal((n, hkv, bs, d)).astype(np.float32) for n in need]
+    q = rng.standard_normal((sum(q_lens), hq, d)).astype(np.float32)
+    outs = []
+    for placement_seed in (0, 1):
+        prng = np.random.default_rng(placement_seed)
+        nb = 2 * sum(need)
+        order = prng.permutation(nb) if placement_seed else np.arange(nb)
+        kc = rng.standard_normal((nb, hkv, bs, d)).astype(np.float32)   # garbage elsewhere
+        vc = rng.standard_normal((nb, hkv, bs, d)).astype(np.float32)
+        table = np.full((3, max(need)), -1, np.int32)
+        nxt = 0
+        for r, n in enumerate(need):
+            table[r, :n] = order[nxt:nxt + n]
+            kc[order[nxt:nxt + n]] = logical_k[r]
+            vc[order[nxt:nxt + n]] = logical_v[r]
+            nxt += n
+        outs.append(_run_varlen(attend_impl, gather_impl, q, kc, vc, table, lens, q_lens, bs, 0.25))
+    return float(np.abs(outs[0] - outs[1]).max())
+
+
+def test_block_permutation_invariance():
+    assert check_permutation_invariance() == 0.0
+
+
+def test_shared_prefix_blocks_equal_private_copies():
+    b = workloads.agentic(seed=5, host_cache=True, scale_lengths=1 / 2000.0)
+    fam = b.families[0]
+    parent, child = fam[0], fam[1]
+    nb = -(-int(b.seq_lens[child]) // b.block_size)
+    nshare = int(np.floor(0.96 * nb))
+    assert np.array_equal(b.block_tables[parent, :nshare], b.block_tables[child, :nshare])
+    assert not set(b.block_tables[child, nshare:nb]) & set(b.block_tables[parent, :nb])
+    # an unshared copy of the child: copy its shared blocks into fresh physical blocks
+    kc = np.concatenate([b.k_cache, b.k_cache[b.block_tables[child, :nshare]]])
+    vc = np.concatenate([b.v_cache, b.v_cache[b.block_tables[child, :nshare]]])
+    table = b.block_tables.copy()
+    table[child, :nshare] = np.arange(b.num_blocks, b.num_blocks + nshare)
+    common = dict(q_bits=b.q, q_dtype="bf16", kv_dtype="bf16", seq_lens=b.seq_lens,
+                  block_size=b.block_size, scale=b.scale, seqs=[child])
+    shared = oracle.paged_decode(k_cache=b.k_cache, v_cache=b.v_cache, block_tables=b.block_tables, **common)
+    private = oracle.paged_decode(k_cache=kc, v_cache=vc, block_tables=table, **common)
+    assert np.array_equal(shared[child], private[child])
+    # two sequences with identical (q, blocks, len) give identical outputs
+    q2 = b.q.copy()
+    q2[fam[2]] = q2[parent]
+    t2 = b.block_tables.copy()
+    t2[fam[2]] = t2[parent]
+    both = oracle.paged_decode(q2, "bf16", b.k_cache, b.v_cache, "bf16", t2, b.seq_lens, b.block_size,
+                               b.scale, seqs=[parent, fam[2]])
+    assert np.array_equal(both[parent], both[fam[2]])
+
+
+def test_chunked_prefill_equals_single_chunk():
+    """Queries of a prompt give the same output whether processed in one chunk or two."""
+    q, kc, vc, table = _contiguous_case(13, 23, 8, 2, 16, 23)
+    whole = _run_varlen(oracle.attend, oracle.gather_kv, q, kc, vc, table, [23], [23], 4, 0.2)
+    first = _run_varlen(oracle.attend, oracle.gather_kv, q[:9], kc, vc, table, [9], [9], 4, 0.2)
+    second = _run_varlen(oracle.attend, oracle.gather_kv, q[9:], kc, vc, table, [23], [14], 4, 0.2)
+    assert np.array_equal(np.concatenate([first, second]), whole)
+
+
+def test_varlen_with_single_tokens_equals_decode():
+    b = workloads.build("v", 17, [30, 1, 64], [1, 1, 1], 8, 2, 64, 16, "f16")
+    dec = oracle.paged_decode(b.q, "f16", b.k_cache, b.v_cache, "f16", b.block_tables, b.seq_lens, 16, b.scale)
+    var = oracle.paged_varlen(b.q, "f16", b.k_cache, b.v_cache, "f16", b.block_tables,
+                              b.query_start_loc, b.seq_lens, 16, b.scale)
+    assert np.array_equal(dec, var)
+
+
+def test_non_causal_attends_whole_context():
+    q, kc, vc, table = _contiguous_case(14, 12, 4, 4, 8, 3)
+    full = _run_varlen(oracle.attend, oracle.gather_kv, q, kc, vc, table, [12], [3], 4, 0.5, causal=False)
+    last = _run_varlen(oracle.attend, oracle.gather_kv, q[2:], kc, vc, table, [12], [1], 4, 0.5)
+    assert np.array_equal(full[2:], last)                 # the last query sees everything anyway
+    first_causal = _run_varlen(oracle.attend, oracle.gather_kv, q, kc, vc, table, [12], [3], 4, 0.5)
+    assert not np.allclose(full[0], first_causal[0])
+
+
+# ---------------------------------------------------------------- workloads
+
+def test_tiny_workload_shape():
+    b = workloads.tiny()
+    assert list(b.seq_lens) == [17, 64, 129, 200] and b.num_blocks == 64
+    used = [int(x) for x in b.block_tables.ravel() if x >= 0]
+    assert len(used) == 2 + 4 + 9 + 13 == len(set(used)) and max(used) < 64
+    assert b.scale == 1 / 8 and b.kv_dtype == "f32" and b.block_tables.shape[1] == 13
+
+
+def test_agentic_lengths_and_families():
+    lens = workloads.agentic_lengths(2)
+    assert np.all((lens >= 32768) & (lens <= 262144))
+    b = workloads.agentic(seed=2, host_cache=False)
+    assert b.num_seqs == 16 and [len(f) for f in b.families] == [5, 5, 5, 1]
+    for fam in b.families[:3]:
+        assert len({int(b.seq_lens[i]) for i in fam}) == 1
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+def _attend_gqa_modulo(q64, K64, V64, positions, scale, causal=True):
+    n, hq, d = q64.shape
+    hkv = K64.shape[1]
+    out = np.empty((n, hq, d))
+    for j in range(n):
+        last = int(positions[j]) if causal else K64.shape[0] - 1
+        for h in range(hq):
+            g = h % hkv                                   # wrong head map
+            s = scale * (K64[: last + 1, g] @ q64[j, h])
+            w = np.exp(s - s.max())
+            out[j, h] = w @ V64[: last + 1, g] / w.sum()
+    return out
+
+
+def _attend_off_by_one(q64, K64, V64, positions, scale, causal=True):
+    pos = np.maximum(np.asarray(positions) - 1, 0)        # drops the diagonal key
+    return oracle.attend(q64, K64, V64, pos, scale, causal)
+
+
+def _attend_no_scale(q64, K64, V64, positions, scale, causal=True):
+    return oracle.attend(q64, K64, V64, positions, 1.0, causal)
+
+
+def _gather_wrong_offset(cache_bits, row, n, bs, dtype, scale=1.0):
+    pos = np.arange(n)
+    phys = np.asarray(row, dtype=np.int64)[pos // bs]
+    off = (bs - 1) - pos % bs                             # reversed within a block
+    return oracle.decode_bits(np.asarray(cache_bits)[phys, :, off, :], dtype, scale)
+
+
+def _gather_logical_as_physical(cache_bits, row, n, bs, dtype, scale=1.0):
+    pos = np.arange(n)
+    return oracle.decode_bits(np.asarray(cache_bits)[pos // bs, :, pos % bs, :], dtype, scale)
+
+
+def _merge_no_rescale(parts):
+    return 0.0, sum(p[1] for p in parts), sum(np.asarray(p[2]) for p in parts)
+
+
+def _encode_ties_away(x):
+    x = np.asarray(x, dtype=np.float64)
+    mags = oracle.e4m3_table()[:127]
+    out = []
+    for v in x:
+        a = abs(v)
+        code = int(np.argmin(np.abs(mags - a) - 1e-30 * mags))  # ties go to the larger
+        out.append(code | (0x80 if math.copysign(1, v) < 0 else 0))
+    return np.array(out, np.uint8)
+
+
+def test_planted_mistakes_are_caught():
+    assert check_sdpa(attend_impl=_attend_gqa_modulo) > 1e-3
+    assert check_brute_force(attend_impl=_attend_off_by_one) > 1e-3
+    assert check_sdpa(attend_impl=_attend_no_scale) > 1e-3
+    assert check_brute_force(gather_impl=_gather_wrong_offset) > 1e-3
+    assert check_permutation_invariance(gather_impl=_gather_logical_as_physical) > 1e-3
+    assert check_merge_golden(oracle.softmax_partial, _merge_no_rescale, oracle.finalize_partial) > 1e-3
+    assert check_e4m3_encode(_encode_ties_away) > 0
