@@ -1,0 +1,243 @@
+/*
+ * pa.h -- C ABI of the paged KV cache attention library (libpa.so), GB300 / sm_103a.
+ *
+ * The library implements the data-parallel hot path of paged KV cache serving:
+ *   1. pa_reshape_and_cache  writes the K/V of new tokens into fixed-size physical
+ *                            blocks through a per-token slot mapping;
+ *   2. pa_decode             PagedAttention decode: one query token per sequence
+ *                            attends the sequence's whole cached context, read
+ *                            through its block table (split-K over the context
+ *                            plus a merge of the partial softmax states);
+ *   3. pa_varlen_attn        attention of a flattened variable-length batch that
+ *                            mixes chunked-prefill requests (many query tokens on
+ *                            a cached prefix, causal within the chunk) and decode
+ *                            requests (one query token).
+ *
+ * Sources, cited by key:
+ *   [AGENTIC] "宣稱省下 106 倍成本：vLLM 怎麼把 Serving 系統校準給 Agentic Workload"
+ *             (datasciocean.com, ai-concept/vllm-agentic-serving)
+ *   [NOTES]   "大模型推理优化学习笔记" (fishingrodd.cn, 2026/10/30)
+ *   [LINEAGE] "从静态批处理到状态化推理集群" (wineandchord.com,
+ *             llm/landscape/lineages/inference-serving)
+ *   [ARCH]    summary of a vLLM V1 architecture deep-dive
+ *             (ai.youdonthavefriends.com, llm/ai/deep-analysis/2026/08/08/vllm-architecture)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Memory.  Every array argument is a DEVICE pointer owned by the caller, unless
+ *   the argument says otherwise.  The library allocates nothing and keeps no
+ *   per-call state; scratch memory is the caller's `workspace`, sized by the
+ *   matching *_workspace_size() query.  This follows [LINEAGE]'s rule that
+ *   running out of memory is handled at admission, never while writing KV.
+ * Streams.  All compute calls are asynchronous on `stream` (a cudaStream_t;
+ *   NULL is the legacy default stream).  Calls on one stream run in issue order:
+ *   write the new tokens with pa_reshape_and_cache, then attend.
+ * Cache layout.  k_cache and v_cache are separate tensors of shape
+ *   [num_blocks][num_kv_heads][block_size][head_size], row-major, element type
+ *   kv_dtype.  One (block, kv head) tile of block_size x head_size elements is
+ *   contiguous.  Bytes per block per layer (K and V together) are
+ *   2 x block_size x num_kv_heads x head_size x dtype_bytes ([ARCH] Part 1,
+ *   KV cache manager).  Both tensors must start on a 16-byte boundary.
+ * Slots.  A token with flat slot s lives in physical block s / block_size at
+ *   offset s % block_size ([ARCH] Part 1, forward pass: slot_mapping).  A
+ *   negative slot marks a padding token and is skipped.
+ * Block tables.  block_tables is int32 [num_seqs][max_blocks_per_seq]; entry
+ *   [i][j] is the physical block that holds logical block j of sequence i
+ *   ([LINEAGE] "PagedAttention": (sequence, logical block) -> physical block).
+ *   Physical blocks may be in any order and may be shared by several sequences
+ *   ([AGENTIC] "統一分頁 + 共用池").  Only the first ceil(seq_len/block_size)
+ *   entries of a row are read.
+ * Heads.  num_q_heads is a multiple of num_kv_heads; query head h reads KV head
+ *   h / (num_q_heads / num_kv_heads) (grouped-query attention).
+ * Positions.  seq_lens[i] counts all tokens of sequence i INCLUDING the new
+ *   ones.  The q_len new query tokens of a request are its last q_len positions;
+ *   query j (0-based) sits at position seq_len - q_len + j and, when causal,
+ *   attends keys 0..position ([ARCH] Part 1: flattened batch, positions + mask).
+ * Numerics.  Scores and the softmax run in fp32 with a running max and sum
+ *   ([AGENTIC] "Online softmax"); the output is rounded once to q_dtype.
+ *   FP8 e4m3 caches carry one fp32 scale per tensor (k_scale, v_scale, device
+ *   pointers to one float each): stored code = e4m3(x / scale), rounded to
+ *   nearest even with saturation to +-448; value = e4m3 decode x scale.
+ * Errors.  Argument checks that need no device data return synchronously with
+ *   a status and launch nothing.  Inputs that live on the device (block-table
+ *   entries, slots, sequence lengths, query offsets) are checked by the kernels:
+ *   an out-of-range value is never dereferenced -- the access is skipped and a
+ *   bit is OR-ed into the device error word, which pa_get_error_flags() reads.
+ *   Launch failures return PA_ERR_CUDA.  No C++ exception crosses this ABI.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pa_stream_t; /* same type as cudaStream_t */
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1, /* a null pointer, a non-positive size, inconsistent shapes */
+  PA_ERR_UNSUPPORTED = 2, /* a dtype combination or shape this build does not handle */
+  PA_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or smaller than required */
+  PA_ERR_BOUNDS = 4,      /* returned by pa_get_error_flags when a device check fired */
+  PA_ERR_TIMEOUT = 5,     /* a bounded device wait gave up (see PA_ERRFLAG_TIMEOUT) */
+  PA_ERR_CUDA = 6         /* a CUDA runtime call or kernel launch failed */
+} pa_status;
+
+typedef enum pa_dtype {
+  PA_F32 = 0,
+  PA_F16 = 1,
+  PA_BF16 = 2,
+  PA_FP8_E4M3 = 3 /* cache only: stored as uint8 codes with a per-tensor fp32 scale */
+} pa_dtype;
+
+/* Bits of the device error word (pa_get_error_flags). */
+#define PA_ERRFLAG_BLOCK_TABLE 0x1u /* a block-table entry outside [0, num_blocks) */
+#define PA_ERRFLAG_SLOT 0x2u        /* a slot >= num_blocks * block_size */
+#define PA_ERRFLAG_SEQ_LEN 0x4u     /* seq_len <= 0, > max_seq_len or > max_blocks_per_seq*block_size */
+#define PA_ERRFLAG_QUERY 0x8u       /* query_start_loc decreasing, q_len > seq_len or > max_query_len */
+#define PA_ERRFLAG_TIMEOUT 0x10u    /* a bounded wait for an asynchronous copy gave up */
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* pa_status_string(pa_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t pa_version(void);
+
+/*
+ * pa_reshape_and_cache -- scatter new tokens' K and V into the paged cache.
+ * [NOTES] "Prefill 与 Decode": prefill stores K/V for every prompt token and each
+ * decode step appends the new token's K/V.  [ARCH] Part 1, forward pass: input
+ * preparation builds slot_mapping, one flat slot per new token.
+ *
+ *   key, value     [num_tokens][num_kv_heads][head_size], src_dtype, rows contiguous
+ *   k_cache, v_cache  cache tensors (layout above), cache_dtype
+ *   slot_mapping   int64 [num_tokens]; slot < 0 skips the token; a slot >=
+ *                  num_blocks*block_size is skipped and sets PA_ERRFLAG_SLOT.
+ *                  Two tokens with the same slot in one call: which one lands is
+ *                  unspecified.
+ *   cache_dtype == src_dtype copies the bits exactly.  cache_dtype == PA_FP8_E4M3
+ *   (src f32/f16/bf16) stores e4m3_rne_satfinite(float(x) / *k_scale) (resp. v),
+ *   the division being IEEE fp32 division.  k_scale / v_scale: device pointers to
+ *   one float each, used only for FP8 (may be NULL otherwise).
+ *   head_size * dtype_bytes must be a multiple of 16 bytes for both dtypes.
+ */
+pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                               const int64_t* slot_mapping, int32_t num_tokens, int32_t num_blocks,
+                               int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                               pa_dtype src_dtype, pa_dtype cache_dtype, const float* k_scale,
+                               const float* v_scale, pa_stream_t stream);
+
+/*
+ * Context tokens per split-K partition that pa_decode / pa_varlen_attn use when
+ * called with partition_size == 0.  A multiple of block_size.  Chosen from the
+ * problem size and the device's SM count (current device).
+ */
+int32_t pa_default_partition_size(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
+                                  int32_t block_size);
+
+/*
+ * Bytes of workspace pa_decode needs.  partition_size == 0 means the default
+ * (pa_default_partition_size with the current device; pass num_kv_heads through
+ * num_kv_heads).  Always >= 256: the first bytes hold internal bookkeeping.
+ */
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_size, int32_t max_seq_len, int32_t block_size,
+                                int32_t partition_size);
+
+/*
+ * pa_decode -- PagedAttention decode, one query token per sequence.
+ * [NOTES] "Prefill 与 Decode" / "Decode": the new token's Q attends the K/V of all
+ * the sequence's cached tokens (including its own, written just before);
+ * [LINEAGE] "PagedAttention": the kernel reads K/V through the block table.
+ * Long contexts are split into partitions of partition_size tokens whose partial
+ * softmax states (running max, weight sum, weighted sum) are merged afterwards
+ * with the rescale-and-add rule of [AGENTIC] "Online softmax".
+ *
+ *   out            [num_seqs][num_q_heads][head_size], q_dtype (written)
+ *   q              [num_seqs][num_q_heads][head_size], q_dtype (f32, f16 or bf16)
+ *   k_cache, v_cache  cache tensors, kv_dtype; kv_dtype == q_dtype, or PA_FP8_E4M3
+ *                  with q_dtype f16/bf16 (k_scale / v_scale then required)
+ *   block_tables   int32 [num_seqs][max_blocks_per_seq]
+ *   seq_lens       int32 [num_seqs], each in [1, max_seq_len]
+ *   max_seq_len    host-side upper bound of seq_lens (sizes the launch)
+ *   scale          softmax scale applied to q.k (e.g. 1/sqrt(head_size))
+ *   partition_size 0 for the default, else a positive multiple of block_size
+ *   workspace      device scratch of >= pa_decode_workspace_size(...) bytes,
+ *                  256-byte aligned; contents need no initialisation
+ * A sequence whose seq_len is out of range gets an all-zero output row and sets
+ * PA_ERRFLAG_SEQ_LEN.
+ */
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    int32_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                    const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                    int32_t block_size, float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
+                    const float* k_scale, const float* v_scale, int32_t partition_size,
+                    void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * Bytes of workspace pa_varlen_attn needs (>= 256).  Same partition_size rule
+ * as pa_decode_workspace_size.
+ */
+size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t total_q_tokens, int32_t max_query_len,
+                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                int32_t max_seq_len, int32_t block_size, int32_t partition_size);
+
+/*
+ * pa_varlen_attn -- attention of a flattened variable-length batch.
+ * [ARCH] Part 1: all sequences are concatenated into one long sequence with no
+ * padding, and V1 mixes decode requests and chunked-prefill requests in one
+ * step; [LINEAGE] "静态 batching" / "Chunked prefill": each step holds
+ * sum_i q_i <= K tokens, q_i = 1 for a decode, a chunk's tokens for a prefill.
+ *
+ *   out            [total_q_tokens][num_q_heads][head_size], q_dtype (written)
+ *   q              [total_q_tokens][num_q_heads][head_size], q_dtype
+ *   query_start_loc int32 [num_seqs + 1], non-decreasing, [0] = 0,
+ *                  [num_seqs] = total_q_tokens; request r owns query rows
+ *                  query_start_loc[r] .. query_start_loc[r+1]-1
+ *   seq_lens       int32 [num_seqs], context length including the new tokens;
+ *                  q_len_r <= seq_lens[r] is required
+ *   max_query_len, max_seq_len  host-side upper bounds (size the launch)
+ *   causal         1: query at position p attends keys 0..p; 0: all seq_len keys
+ *   the rest as pa_decode.  A request with q_len == 0 is skipped.
+ * pa_decode equals pa_varlen_attn with q_len = 1 for every request.
+ */
+pa_status pa_varlen_attn(void* out, const void* q, const void* k_cache, const void* v_cache,
+                         int32_t num_blocks, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* query_start_loc,
+                         const int32_t* seq_lens, int32_t num_seqs, int32_t total_q_tokens,
+                         int32_t max_query_len, int32_t max_seq_len, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                         float scale, int32_t causal, pa_dtype q_dtype, pa_dtype kv_dtype,
+                         const float* k_scale, const float* v_scale, int32_t partition_size,
+                         void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * Read the device error word of the current device (host pointer `flags`),
+ * after synchronising `stream`.  clear != 0 resets it to zero.  Returns
+ * PA_ERR_BOUNDS if any PA_ERRFLAG_* other than TIMEOUT is set, PA_ERR_TIMEOUT
+ * if only PA_ERRFLAG_TIMEOUT is set, PA_OK if none.
+ */
+pa_status pa_get_error_flags(uint32_t* flags, int32_t clear, pa_stream_t stream);
+
+/*
+ * Kernel-level tracing.  While enabled, every kernel the library launches is
+ * bracketed by CUDA events recorded on its launch stream.  pa_trace_read()
+ * synchronises those events and, for kernel kind `kind` (0 = reshape_and_cache,
+ * 1 = attention main kernel, 2 = partial merge, 3 = varlen plan,
+ * 4 = prefill tiles), returns the launch count and the summed device
+ * milliseconds since the last reset (reset != 0 clears every kind).
+ * Tracing is off by default and costs nothing when off.  Not thread-safe.
+ */
+pa_status pa_trace_enable(int32_t on);
+pa_status pa_trace_read(int32_t kind, int64_t* launches, double* total_ms, int32_t reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,204 @@
+"""Python binding of libpa.so, the paged KV cache attention library for GB300.
+
+Argument marshalling only: every function takes torch tensors, checks that they
+are contiguous CUDA tensors of the expected shapes, and passes raw device
+pointers, sizes and the current CUDA stream to the C ABI declared in
+``include/pa.h``.  All computation happens in the library's CUDA kernels; there
+is no fallback.  Importing this package raises ImportError when libpa.so has
+not been built (``python paged_kv_cache_pagedattention_gb300/build.py``).
+
+Cache tensors have shape ``[num_blocks][num_kv_heads][block_size][head_size]``;
+FP8 e4m3 caches are uint8 tensors of codes with per-tensor fp32 scales passed as
+one-element float32 CUDA tensors.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libpa.so not found at {LIB_PATH}; build it with "
+                      "`python paged_kv_cache_pagedattention_gb300/build.py`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_BOUNDS, \
+    PA_ERR_TIMEOUT, PA_ERR_CUDA = range(7)
+PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = range(4)
+PA_ERRFLAG_BLOCK_TABLE, PA_ERRFLAG_SLOT, PA_ERRFLAG_SEQ_LEN, PA_ERRFLAG_QUERY, PA_ERRFLAG_TIMEOUT = \
+    0x1, 0x2, 0x4, 0x8, 0x10
+
+# Names of the kernel kinds reported by pa_trace_read.
+TRACE_KINDS = ("reshape_and_cache", "attention", "merge", "varlen_plan", "prefill_tiles")
+
+# Every symbol include/pa.h declares, with its ctypes signature.
+_P, _I32, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+SIGNATURES = {
+    "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pa_version": (_I32, []),
+    "pa_reshape_and_cache": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32,
+                                            ctypes.c_int, ctypes.c_int, _P, _P, _P]),
+    "pa_default_partition_size": (_I32, [_I32, _I32, _I32, _I32]),
+    "pa_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
+    "pa_decode": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
+                                 _I32, _F, ctypes.c_int, ctypes.c_int, _P, _P, _I32, _P, _SZ, _P]),
+    "pa_varlen_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32]),
+    "pa_varlen_attn": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
+                                      _I32, _I32, _I32, _I32, _F, _I32, ctypes.c_int, ctypes.c_int,
+                                      _P, _P, _I32, _P, _SZ, _P]),
+    "pa_get_error_flags": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), _I32, _P]),
+    "pa_trace_enable": (ctypes.c_int, [_I32]),
+    "pa_trace_read": (ctypes.c_int, [_I32, ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_double), _I32]),
+}
+for _name, (_res, _args) in SIGNATURES.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_lib.pa_status_string(status).decode()}")
+
+
+def _check(status: int, where: str) -> None:
+    if status != PA_OK:
+        raise PAError(status, where)
+
+
+_DT = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.uint8: PA_FP8_E4M3}
+
+
+def dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported tensor dtype {t.dtype}") from None
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def pa_status_string(status: int) -> str:
+    return _lib.pa_status_string(status).decode()
+
+
+def pa_version() -> int:
+    return _lib.pa_version()
+
+
+def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, k_scale=None, v_scale=None,
+                         stream=None) -> None:
+    """Write key/value [T][Hkv][d] into the paged caches at slot_mapping (int64 [T])."""
+    nb, hkv, bs, d = k_cache.shape
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or v_cache.dtype != k_cache.dtype:
+        raise ValueError("k_cache and v_cache must match")
+    if key.dim() != 3 or tuple(key.shape[1:]) != (hkv, d) or key.shape != value.shape:
+        raise ValueError("key/value must be [num_tokens][num_kv_heads][head_size]")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != key.shape[0]:
+        raise ValueError("slot_mapping must be int64 [num_tokens]")
+    _check(_lib.pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                     _ptr(slot_mapping), key.shape[0], nb, hkv, d, bs,
+                                     dtype_code(key), dtype_code(k_cache), _ptr(k_scale), _ptr(v_scale),
+                                     _stream(stream)), "pa_reshape_and_cache")
+
+
+def pa_default_partition_size(num_seqs, num_kv_heads, max_seq_len, block_size) -> int:
+    return _lib.pa_default_partition_size(num_seqs, num_kv_heads, max_seq_len, block_size)
+
+
+def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size, max_seq_len, block_size,
+                             partition_size=0) -> int:
+    return _lib.pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size, max_seq_len,
+                                         block_size, partition_size)
+
+
+def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, scale, workspace,
+              k_scale=None, v_scale=None, partition_size=0, stream=None) -> None:
+    """PagedAttention decode; out/q [B][Hq][d], block_tables int32 [B][max_blocks], seq_lens int32 [B]."""
+    nb, hkv, bs, d = k_cache.shape
+    b, hq = q.shape[0], q.shape[1]
+    if q.dim() != 3 or q.shape[2] != d or out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("q/out must be [num_seqs][num_q_heads][head_size] of one dtype")
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or block_tables.shape[0] != b:
+        raise ValueError("block_tables must be int32 [num_seqs][max_blocks_per_seq]")
+    if seq_lens.dtype != torch.int32 or seq_lens.numel() != b:
+        raise ValueError("seq_lens must be int32 [num_seqs]")
+    _check(_lib.pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables),
+                          block_tables.shape[1], _ptr(seq_lens), b, int(max_seq_len), hq, hkv, d, bs,
+                          float(scale), dtype_code(q), dtype_code(k_cache), _ptr(k_scale), _ptr(v_scale),
+                          int(partition_size), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                          _stream(stream)), "pa_decode")
+
+
+def pa_varlen_workspace_size(num_seqs, total_q_tokens, max_query_len, num_q_heads, num_kv_heads,
+                             head_size, max_seq_len, block_size, partition_size=0) -> int:
+    return _lib.pa_varlen_workspace_size(num_seqs, total_q_tokens, max_query_len, num_q_heads,
+                                         num_kv_heads, head_size, max_seq_len, block_size, partition_size)
+
+
+def pa_varlen_attn(out, q, k_cache, v_cache, block_tables, query_start_loc, seq_lens, max_query_len,
+                   max_seq_len, scale, workspace, causal=True, k_scale=None, v_scale=None,
+                   partition_size=0, stream=None) -> None:
+    """Attention of a flattened varlen batch; out/q [T][Hq][d], query_start_loc int32 [B+1]."""
+    nb, hkv, bs, d = k_cache.shape
+    t, hq = q.shape[0], q.shape[1]
+    b = seq_lens.numel()
+    if q.dim() != 3 or q.shape[2] != d or out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("q/out must be [total_q_tokens][num_q_heads][head_size] of one dtype")
+    if query_start_loc.dtype != torch.int32 or query_start_loc.numel() != b + 1:
+        raise ValueError("query_start_loc must be int32 [num_seqs+1]")
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or block_tables.shape[0] != b:
+        raise ValueError("block_tables must be int32 [num_seqs][max_blocks_per_seq]")
+    _check(_lib.pa_varlen_attn(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables),
+                               block_tables.shape[1], _ptr(query_start_loc), _ptr(seq_lens), b, t,
+                               int(max_query_len), int(max_seq_len), hq, hkv, d, bs, float(scale),
+                               1 if causal else 0, dtype_code(q), dtype_code(k_cache), _ptr(k_scale),
+                               _ptr(v_scale), int(partition_size), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream)),
+           "pa_varlen_attn")
+
+
+def pa_get_error_flags(clear: bool = True, stream=None) -> int:
+    """Synchronise the stream and return the device error word (PA_ERRFLAG_* bits)."""
+    flags = ctypes.c_uint32(0)
+    st = _lib.pa_get_error_flags(ctypes.byref(flags), 1 if clear else 0, _stream(stream))
+    if st not in (PA_OK, PA_ERR_BOUNDS, PA_ERR_TIMEOUT):
+        _check(st, "pa_get_error_flags")
+    return int(flags.value)
+
+
+def pa_trace_enable(on: bool) -> None:
+    _check(_lib.pa_trace_enable(1 if on else 0), "pa_trace_enable")
+
+
+def pa_trace_read(kind: int, reset: bool = False):
+    """(launches, total device ms) of one kernel kind since the last reset."""
+    n = ctypes.c_int64(0)
+    ms = ctypes.c_double(0.0)
+    _check(_lib.pa_trace_read(kind, ctypes.byref(n), ctypes.byref(ms), 1 if reset else 0), "pa_trace_read")
+    return int(n.value), float(ms.value)
+
+
+def workspace_tensor(nbytes: int, device=None) -> torch.Tensor:
+    """A device byte buffer suitable as `workspace` (torch allocations are 256-byte aligned)."""
+    return torch.empty(int(nbytes), dtype=torch.uint8, device=device or "cuda")

@@ -1,0 +1,534 @@
+// The C ABI declared in include/pa.h: argument validation, workspace layout,
+// tensor-map encoding, kernel selection and launch, the device error word and
+// optional event-based kernel tracing.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <vector>
+
+#include "pa_internal.h"
+
+namespace {
+
+using pa::AttnParams;
+
+__device__ unsigned g_pa_error_word;
+
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+unsigned* error_word() {
+  static unsigned* cache[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!cache[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_pa_error_word) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<unsigned*>(ptr);
+  }
+  return cache[dev];
+}
+
+int sm_count() {
+  static int cache[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 148;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int dtype_bytes(int dt) {
+  switch (dt) {
+    case PA_F32: return 4;
+    case PA_F16: return 2;
+    case PA_BF16: return 2;
+    case PA_FP8_E4M3: return 1;
+    default: return 0;
+  }
+}
+
+// ------------------------------------------------------------------ partitions
+
+int round_up(int x, int m) { return static_cast<int>(ceil_div(x, m) * m); }
+
+int default_partition(int num_seqs, int num_kv_heads, int max_seq_len, int block_size) {
+  const long long units = (long long)(num_seqs > 0 ? num_seqs : 1) * (num_kv_heads > 0 ? num_kv_heads : 1);
+  const long long target = 32LL * sm_count();
+  int part = round_up(256, block_size);
+  const int cap = round_up(4096, block_size);
+  while (part < cap && units * ceil_div(max_seq_len, part) > target) part *= 2;
+  while (ceil_div(max_seq_len, part) > 65535) part *= 2;
+  return part;
+}
+
+int resolve_partition(int requested, int num_seqs, int num_kv_heads, int max_seq_len, int block_size) {
+  int part = requested > 0 ? requested : default_partition(num_seqs, num_kv_heads, max_seq_len, block_size);
+  while (ceil_div(max_seq_len, part) > 65535) part *= 2;
+  return part;
+}
+
+int prefill_partition(int part) { return part > 16384 ? part : 16384 / part * part; }
+
+struct DecodeLayout {
+  int part;
+  long long parts;
+  size_t ml_off, acc_off, total;
+};
+
+DecodeLayout decode_layout(int num_seqs, int hq, int d, int max_seq_len, int bs, int hkv, int requested) {
+  DecodeLayout L;
+  L.part = resolve_partition(requested, num_seqs, hkv, max_seq_len, bs);
+  L.parts = ceil_div(max_seq_len, L.part);
+  const size_t rows = (size_t)num_seqs * (size_t)L.parts;
+  L.ml_off = 256;
+  L.acc_off = L.ml_off + align256(rows * hq * sizeof(float2));
+  L.total = L.acc_off + align256(rows * hq * (size_t)d * sizeof(float));
+  return L;
+}
+
+struct VarlenLayout {
+  int part, part_pf;
+  long long parts, parts_pf, max_work;
+  size_t off_off, work_off, ml_off, acc_off, total;
+};
+
+VarlenLayout varlen_layout(int num_seqs, int total_q, int hq, int hkv, int d, int max_seq_len, int bs,
+                           int requested) {
+  VarlenLayout L;
+  L.part = resolve_partition(requested, num_seqs, hkv, max_seq_len, bs);
+  L.part_pf = prefill_partition(L.part);
+  L.parts = ceil_div(max_seq_len, L.part);
+  L.parts_pf = ceil_div(max_seq_len, L.part_pf);
+  const int group = hq / (hkv > 0 ? hkv : 1);
+  L.max_work = (ceil_div(total_q, pa::prefill_tile_tokens(group)) + num_seqs) * L.parts_pf;
+  const size_t rows = (size_t)num_seqs * (size_t)L.parts + (size_t)total_q * (size_t)L.parts_pf;
+  L.off_off = 256;
+  L.work_off = L.off_off + align256((size_t)num_seqs * sizeof(int32_t));
+  L.ml_off = L.work_off + align256((size_t)L.max_work * sizeof(int4));
+  L.acc_off = L.ml_off + align256(rows * hq * sizeof(float2));
+  L.total = L.acc_off + align256(rows * hq * (size_t)d * sizeof(float));
+  return L;
+}
+
+// ------------------------------------------------------------------ tensor maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// The cache seen as rows of 128 bytes: dim0 = one 128-byte row, dim1 = rows of all
+// heads of one block (Hkv x block_size x rows-per-token), dim2 = physical block.
+// One box is the (block, head) tile: block_size x rows-per-token rows, 128B swizzle.
+bool encode_cache_map(CUtensorMap* m, const void* base, int kv_dtype, int num_blocks, int hkv, int bs, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const int eb = dtype_bytes(kv_dtype);
+  const int row_bytes = d * eb;
+  if (row_bytes % 128) return false;
+  const int rpt = row_bytes / 128;
+  cuuint64_t dims[3] = {(cuuint64_t)(128 / eb), (cuuint64_t)hkv * bs * rpt, (cuuint64_t)num_blocks};
+  cuuint64_t strides[2] = {128, (cuuint64_t)hkv * bs * row_bytes};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / eb), (cuuint32_t)(bs * rpt), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType t = eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  return fn(m, t, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ tracing
+
+constexpr int kTraceKinds = 5;
+bool g_trace_on = false;
+struct TraceSlot {
+  int kind;
+  cudaEvent_t a, b;
+};
+std::vector<TraceSlot> g_pending;
+std::vector<cudaEvent_t> g_event_pool;
+int64_t g_launches[kTraceKinds];
+double g_ms[kTraceKinds];
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+struct TraceScope {
+  int kind;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  TraceScope(int k, cudaStream_t st) : kind(k), s(st) {
+    if (g_trace_on) {
+      a = take_event();
+      if (a) cudaEventRecord(a, s);
+    }
+  }
+  ~TraceScope() {
+    if (a) {
+      cudaEvent_t b = take_event();
+      if (b) {
+        cudaEventRecord(b, s);
+        g_pending.push_back({kind, a, b});
+      } else {
+        g_event_pool.push_back(a);
+      }
+    }
+  }
+};
+
+void collect_trace() {
+  for (const TraceSlot& t : g_pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(t.b) == cudaSuccess && cudaEventElapsedTime(&ms, t.a, t.b) == cudaSuccess) {
+      g_launches[t.kind] += 1;
+      g_ms[t.kind] += ms;
+    }
+    g_event_pool.push_back(t.a);
+    g_event_pool.push_back(t.b);
+  }
+  g_pending.clear();
+}
+
+pa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Checks shared by pa_decode and pa_varlen_attn.
+pa_status check_attention_args(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                               int32_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* seq_lens, int32_t max_seq_len, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                               pa_dtype q_dtype, pa_dtype kv_dtype, const float* k_scale,
+                               const float* v_scale, int32_t partition_size, void* workspace) {
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !workspace) return PA_ERR_INVALID_ARG;
+  if (num_blocks < 1 || max_blocks_per_seq < 1 || max_seq_len < 1 || num_q_heads < 1 || num_kv_heads < 1 ||
+      head_size < 1 || block_size < 1)
+    return PA_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
+  if (partition_size < 0 || (partition_size > 0 && partition_size % block_size)) return PA_ERR_INVALID_ARG;
+  if (q_dtype != PA_F32 && q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (kv_dtype != q_dtype && kv_dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+  if (kv_dtype == PA_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+  if (head_size > 256) return PA_ERR_UNSUPPORTED;
+  if (num_kv_heads * ((num_q_heads / num_kv_heads + 7) / 8) > 65535) return PA_ERR_UNSUPPORTED;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return PA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return PA_ERR_WORKSPACE;
+  return PA_OK;
+}
+
+AttnParams base_params(void* out, const void* q, const void* k_cache, const void* v_cache, int32_t num_blocks,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                       int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_size, int32_t block_size, float scale, const float* k_scale,
+                       const float* v_scale) {
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.err = error_word();
+  p.num_seqs = num_seqs;
+  p.num_blocks = num_blocks;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.head_size = head_size;
+  p.block_size = block_size;
+  p.group = num_q_heads / num_kv_heads;
+  p.num_head_groups = (p.group + 7) / 8;
+  p.max_seq_len = max_seq_len;
+  p.causal = 1;
+  p.scale = scale;
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG: invalid argument";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: unsupported dtype or shape";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case PA_ERR_BOUNDS: return "PA_ERR_BOUNDS: a device-side bounds check fired";
+    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: a bounded device wait gave up";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA call or kernel launch failed";
+    default: return "unknown pa_status";
+  }
+}
+
+int32_t pa_version(void) { return 100; }
+
+pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                               const int64_t* slot_mapping, int32_t num_tokens, int32_t num_blocks,
+                               int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                               pa_dtype src_dtype, pa_dtype cache_dtype, const float* k_scale,
+                               const float* v_scale, pa_stream_t stream) {
+  if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_size < 1 || block_size < 1)
+    return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+  if (src_dtype != PA_F32 && src_dtype != PA_F16 && src_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (cache_dtype != src_dtype && cache_dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+  if (cache_dtype == PA_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+  if ((head_size * dtype_bytes(src_dtype)) % 16 || (head_size * dtype_bytes(cache_dtype)) % 16)
+    return PA_ERR_UNSUPPORTED;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return PA_ERR_INVALID_ARG;
+  pa::ScatterParams p;
+  p.key = key;
+  p.value = value;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.slot_mapping = slot_mapping;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.err = error_word();
+  p.num_tokens = num_tokens;
+  p.num_blocks = num_blocks;
+  p.num_kv_heads = num_kv_heads;
+  p.head_size = head_size;
+  p.block_size = block_size;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  TraceScope t(0, s);
+  return cuda_status(pa::launch_reshape_and_cache(p, src_dtype, cache_dtype, s));
+}
+
+int32_t pa_default_partition_size(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
+                                  int32_t block_size) {
+  if (block_size < 1 || max_seq_len < 1) return 0;
+  return default_partition(num_seqs, num_kv_heads, max_seq_len, block_size);
+}
+
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_size, int32_t max_seq_len, int32_t block_size,
+                                int32_t partition_size) {
+  if (num_seqs < 1 || num_q_heads < 1 || head_size < 1 || max_seq_len < 1 || block_size < 1) return 256;
+  return decode_layout(num_seqs, num_q_heads, head_size, max_seq_len, block_size, num_kv_heads,
+                       partition_size)
+      .total;
+}
+
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, int32_t num_blocks,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                    int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                    int32_t head_size, int32_t block_size, float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
+                    const float* k_scale, const float* v_scale, int32_t partition_size, void* workspace,
+                    size_t workspace_bytes, pa_stream_t stream) {
+  if (num_seqs < 0) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  pa_status st = check_attention_args(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
+                                      seq_lens, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size,
+                                      q_dtype, kv_dtype, k_scale, v_scale, partition_size, workspace);
+  if (st != PA_OK) return st;
+  const DecodeLayout L =
+      decode_layout(num_seqs, num_q_heads, head_size, max_seq_len, block_size, num_kv_heads, partition_size);
+  if (workspace_bytes < L.total) return PA_ERR_WORKSPACE;
+  AttnParams p = base_params(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
+                             num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, scale,
+                             k_scale, v_scale);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.num_rows = num_seqs;
+  p.max_query_len = 1;
+  p.part = p.part_pf = L.part;
+  p.max_partitions = static_cast<int>(L.parts);
+  p.ws_ml = reinterpret_cast<float2*>(ws + L.ml_off);
+  p.ws_acc = reinterpret_cast<float*>(ws + L.acc_off);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (pa::decode_mma_supported(q_dtype, kv_dtype, head_size, block_size, p.group)) {
+    CUtensorMap tk, tv;
+    if (!encode_cache_map(&tk, k_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size) ||
+        !encode_cache_map(&tv, v_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size))
+      return PA_ERR_CUDA;
+    TraceScope t(1, s);
+    e = pa::launch_decode_mma(p, q_dtype, kv_dtype, static_cast<int>(L.parts), &tk, &tv, s);
+  } else {
+    TraceScope t(1, s);
+    e = pa::launch_attn_generic(p, q_dtype, kv_dtype, static_cast<int>(L.parts), -1, s);
+  }
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (L.parts > 1) {
+    TraceScope t(2, s);
+    e = pa::launch_merge(p, q_dtype, s);
+  }
+  return cuda_status(e);
+}
+
+size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t total_q_tokens, int32_t max_query_len,
+                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                int32_t max_seq_len, int32_t block_size, int32_t partition_size) {
+  (void)max_query_len;
+  if (num_seqs < 1 || total_q_tokens < 1 || num_q_heads < 1 || num_kv_heads < 1 || head_size < 1 ||
+      max_seq_len < 1 || block_size < 1)
+    return 256;
+  return varlen_layout(num_seqs, total_q_tokens, num_q_heads, num_kv_heads, head_size, max_seq_len, block_size,
+                       partition_size)
+      .total;
+}
+
+pa_status pa_varlen_attn(void* out, const void* q, const void* k_cache, const void* v_cache, int32_t num_blocks,
+                         const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* query_start_loc,
+                         const int32_t* seq_lens, int32_t num_seqs, int32_t total_q_tokens, int32_t max_query_len,
+                         int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                         int32_t block_size, float scale, int32_t causal, pa_dtype q_dtype, pa_dtype kv_dtype,
+                         const float* k_scale, const float* v_scale, int32_t partition_size, void* workspace,
+                         size_t workspace_bytes, pa_stream_t stream) {
+  if (num_seqs < 0 || total_q_tokens < 0) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_q_tokens == 0) return PA_OK;
+  if (!query_start_loc || max_query_len < 1) return PA_ERR_INVALID_ARG;
+  pa_status st = check_attention_args(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
+                                      seq_lens, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size,
+                                      q_dtype, kv_dtype, k_scale, v_scale, partition_size, workspace);
+  if (st != PA_OK) return st;
+  const VarlenLayout L = varlen_layout(num_seqs, total_q_tokens, num_q_heads, num_kv_heads, head_size,
+                                       max_seq_len, block_size, partition_size);
+  if (workspace_bytes < L.total) return PA_ERR_WORKSPACE;
+  if (L.max_work > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+  AttnParams p = base_params(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
+                             num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, scale,
+                             k_scale, v_scale);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.query_start_loc = query_start_loc;
+  p.num_rows = total_q_tokens;
+  p.max_query_len = max_query_len;
+  p.part = L.part;
+  p.part_pf = L.part_pf;
+  p.max_partitions = static_cast<int>(L.parts);
+  p.causal = causal ? 1 : 0;
+  int32_t* work_count = reinterpret_cast<int32_t*>(ws);
+  p.plan_ok = reinterpret_cast<int32_t*>(ws + 4);
+  int32_t* part_off = reinterpret_cast<int32_t*>(ws + L.off_off);
+  int4* work = reinterpret_cast<int4*>(ws + L.work_off);
+  p.part_off = part_off;
+  p.work = work;
+  p.work_count = work_count;
+  p.ws_ml = reinterpret_cast<float2*>(ws + L.ml_off);
+  p.ws_acc = reinterpret_cast<float*>(ws + L.acc_off);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  {
+    TraceScope t(3, s);
+    e = pa::launch_varlen_plan(p, part_off, work, work_count, static_cast<int>(L.max_work), s);
+  }
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  const bool fast_decode = pa::decode_mma_supported(q_dtype, kv_dtype, head_size, block_size, p.group);
+  const bool fast_prefill = pa::prefill_mma_supported(q_dtype, kv_dtype, head_size, block_size, p.group);
+  CUtensorMap tk, tv;
+  if (fast_decode || fast_prefill) {
+    if (!encode_cache_map(&tk, k_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size) ||
+        !encode_cache_map(&tv, v_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size))
+      return PA_ERR_CUDA;
+  }
+  // Single-token rows: tensor-core decode kernel, else the generic kernel.
+  // Multi-token rows: tensor-core prefill tiles, else the generic kernel.
+  const bool multi = max_query_len > 1;
+  if (!fast_decode && !(multi && fast_prefill)) {
+    TraceScope t(1, s);  // generic kernel for every row
+    e = pa::launch_attn_generic(p, q_dtype, kv_dtype, static_cast<int>(L.parts), -1, s);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  } else {
+    if (fast_decode) {
+      TraceScope t(1, s);
+      e = pa::launch_decode_mma(p, q_dtype, kv_dtype, static_cast<int>(L.parts), &tk, &tv, s);
+    } else {
+      TraceScope t(1, s);
+      e = pa::launch_attn_generic(p, q_dtype, kv_dtype, static_cast<int>(L.parts), 0, s);
+    }
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+    if (multi && fast_prefill) {
+      TraceScope t(4, s);
+      e = pa::launch_prefill_mma(p, q_dtype, kv_dtype, 2 * sm_count(), &tk, &tv, s);
+    } else if (multi) {
+      TraceScope t(1, s);
+      e = pa::launch_attn_generic(p, q_dtype, kv_dtype, static_cast<int>(L.parts_pf), 1, s);
+    }
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  if (L.parts > 1 || L.parts_pf > 1) {
+    TraceScope t(2, s);
+    e = pa::launch_merge(p, q_dtype, s);
+  }
+  return cuda_status(e);
+}
+
+pa_status pa_get_error_flags(uint32_t* flags, int32_t clear, pa_stream_t stream) {
+  if (!flags) return PA_ERR_INVALID_ARG;
+  unsigned* w = error_word();
+  if (!w) return PA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned host = 0;
+  if (cudaMemcpyAsync(&host, w, sizeof(unsigned), cudaMemcpyDeviceToHost, s) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  if (clear) {
+    if (cudaMemsetAsync(w, 0, sizeof(unsigned), s) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  }
+  *flags = host;
+  if (host & ~PA_ERRFLAG_TIMEOUT) return PA_ERR_BOUNDS;
+  if (host & PA_ERRFLAG_TIMEOUT) return PA_ERR_TIMEOUT;
+  return PA_OK;
+}
+
+pa_status pa_trace_enable(int32_t on) {
+  g_trace_on = on != 0;
+  return PA_OK;
+}
+
+pa_status pa_trace_read(int32_t kind, int64_t* launches, double* total_ms, int32_t reset) {
+  if (kind < 0 || kind >= kTraceKinds) return PA_ERR_INVALID_ARG;
+  collect_trace();
+  if (launches) *launches = g_launches[kind];
+  if (total_ms) *total_ms = g_ms[kind];
+  if (reset) {
+    for (int k = 0; k < kTraceKinds; ++k) {
+      g_launches[k] = 0;
+      g_ms[k] = 0.0;
+    }
+  }
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,470 @@
+// PagedAttention decode on tensor cores.
+//
+// One CTA handles (request, KV head, head group of <= 8 query heads, partition of
+// the context).  [NOTES] "Decode": the single new query token of a request reads
+// every cached K/V of that request; [LINEAGE] "PagedAttention": K/V are read through
+// the block table; the partitions' partial softmax states are merged afterwards by
+// the rescale-and-add rule of [AGENTIC] "Online softmax".
+//
+// Data movement.  Each (physical block, KV head) tile of K or V is contiguous in
+// HBM (block_size x head_size elements).  Each warp owns a private ring of stages;
+// its lane 0 issues one TMA bulk-tensor copy per tile (K and V) into the ring and
+// the warp waits on the stage's mbarrier.  The tensor map views the cache as rows
+// of 128 bytes and uses the 128-byte swizzle, so the ldmatrix / 16-byte shared
+// loads below are free of bank conflicts.  A stage is refilled as soon as its warp
+// has consumed it, keeping ring_depth tiles per warp in flight.
+//
+// Math.  The query heads that share a KV head are the N = 8 columns of a warp MMA
+// m16n8k16 (grouped-query reuse: every K/V element loaded serves all of them):
+//   S^T[token][head]   = K[token][:] . Q[head][:]       (M = 16 tokens, K = head dim)
+//   O^T[dim][head]    += V^T[dim][token] . P^T[token][head]  (M = 16 dims, K = 16 tokens)
+// P^T comes from the S^T accumulators through movmatrix (an in-register 8x8
+// transpose).  The softmax runs on the accumulators in fp32 with a running max per
+// head (log2 units), sums l from the same rounded P that feeds the MMA, and
+// rescales O when the max grows.  FP8 e4m3 tiles are converted to f16 exactly
+// (cvt e4m3x2 -> f16x2) in registers; the per-tensor scales are folded into the
+// score multiplier (k_scale) and the output (v_scale); q is scaled by a power of
+// two per head so that it fits f16 exactly.
+#include "pa_common.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+template <int KVDT, int HEAD, int BS>
+struct DecodeGeom {
+  static constexpr bool kFp8 = KVDT == PA_FP8_E4M3;
+  static constexpr int kElemBytes = kFp8 ? 1 : 2;
+  static constexpr int kRowBytes = HEAD * kElemBytes;  // one token of one head
+  static constexpr int kRowsPerToken = kRowBytes / 128;
+  static constexpr int kTileBytes = BS * kRowBytes;
+  static constexpr int kMTiles = BS / 16;
+  static constexpr int kKSteps = HEAD / 16;
+  static constexpr int kDTiles = HEAD / 16;
+  static constexpr int kStages = kTileBytes <= 4096 ? 3 : 2;
+  static_assert(kRowBytes % 128 == 0, "token rows must be whole 128-byte rows");
+};
+
+template <int KVDT, int HEAD, int BS, int NW>
+constexpr int decode_smem_bytes() {
+  using G = DecodeGeom<KVDT, HEAD, BS>;
+  return NW * G::kStages * 2 * G::kTileBytes + NW * G::kStages * 8 + 1024;
+}
+
+template <int QDT, int KVDT, int HEAD, int BS, int NW>
+__global__ void __launch_bounds__(NW * 32)
+    decode_mma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv) {
+  using G = DecodeGeom<KVDT, HEAD, BS>;
+  using QE = Elem<QDT>;
+  constexpr bool kFp8 = G::kFp8;
+  constexpr int MDT = kFp8 ? PA_F16 : QDT;  // element type fed to the MMA
+  constexpr int ST = G::kStages;
+  constexpr int TB = G::kTileBytes;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * ST * 2 * TB);
+  __shared__ int s_failed;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x;
+  const int kvh = blockIdx.y / p.num_head_groups;
+  const int hg = blockIdx.y % p.num_head_groups;
+  const int z = blockIdx.z;
+
+  int row = r;
+  if (p.query_start_loc != nullptr) {
+    if (plan_rejected(p)) return;
+    const int q0 = p.query_start_loc[r];
+    if (p.query_start_loc[r + 1] - q0 != 1) return;  // multi-token rows go elsewhere
+    row = q0;
+  }
+  const int seq_len = p.seq_lens[r];
+  const int h0 = kvh * p.group + hg * 8;
+  const int nh = min(8, p.group - hg * 8);
+  const bool ok = seq_len >= 1 && seq_len <= p.max_seq_len &&
+                  (long long)seq_len <= (long long)p.max_blocks_per_seq * BS;
+  typename QE::T* out = reinterpret_cast<typename QE::T*>(p.out);
+  if (!ok) {
+    if (z == 0) {
+      for (int i = threadIdx.x; i < nh * HEAD; i += NW * 32)
+        out[((long long)row * p.num_q_heads + h0 + i / HEAD) * HEAD + (i % HEAD)] = QE::from_float(0.f);
+      if (threadIdx.x == 0 && blockIdx.y == 0) flag_error(p.err, PA_ERRFLAG_SEQ_LEN);
+    }
+    return;
+  }
+  const int nblk = (seq_len + BS - 1) / BS;
+  const int pb = p.part / BS;
+  const int b0 = z * pb;
+  if (b0 >= nblk) return;
+  const int b1 = min(b0 + pb, nblk);
+  const int nparts = (nblk + pb - 1) / pb;
+
+  if (threadIdx.x == 0) {
+    s_failed = 0;
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+    for (int i = 0; i < NW * ST; ++i) mbar_init(bars + i, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int32_t* table = p.block_tables + (long long)r * p.max_blocks_per_seq;
+  const int nmine = (b1 - b0 > warp) ? (b1 - b0 - warp + NW - 1) / NW : 0;
+  uint8_t* ring = smem + warp * ST * 2 * TB;
+  uint64_t* wbars = bars + warp * ST;
+  const int tile_row0 = kvh * BS * G::kRowsPerToken;
+
+  auto issue = [&](int i) {
+    const int jb = b0 + warp + i * NW;
+    const int phys = table[jb];
+    uint64_t* bar = wbars + (i % ST);
+    if (phys < 0 || phys >= p.num_blocks) {
+      flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
+      mbar_arrive(bar);  // completes the phase with no data; the block is skipped
+    } else {
+      uint8_t* st = ring + (i % ST) * 2 * TB;
+      mbar_arrive_expect_tx(bar, 2 * TB);
+      tma_load_3d(st, &tmk, 0, tile_row0, phys, bar);
+      tma_load_3d(st + TB, &tmv, 0, tile_row0, phys, bar);
+    }
+  };
+  if (lane == 0)
+    for (int i = 0; i < min(ST, nmine); ++i) issue(i);
+
+  // ---- query fragments (B operand: k = head dim, n = query head of the group)
+  const int qn = lane >> 2, qq = lane & 3;  // B-fragment column / k-pair index
+  uint32_t qb[G::kKSteps][2];
+  float cA, cB;  // score multipliers (log2 units) of accumulator columns 2*qq, 2*qq+1
+  {
+    const float base_c = p.scale * kLog2e;
+    const typename QE::T* qrow =
+        reinterpret_cast<const typename QE::T*>(p.q) + ((long long)row * p.num_q_heads + h0 + qn) * HEAD;
+    if constexpr (!kFp8) {
+      const uint32_t* qw = reinterpret_cast<const uint32_t*>(qrow);
+#pragma unroll
+      for (int ks = 0; ks < G::kKSteps; ++ks) {
+        qb[ks][0] = qn < nh ? qw[8 * ks + qq] : 0u;
+        qb[ks][1] = qn < nh ? qw[8 * ks + 4 + qq] : 0u;
+      }
+      cA = cB = base_c;
+    } else {
+      // k-step ks, B rows (2qq, 2qq+1) <-> dims 32qq + 4ks + {0,1}; rows (2qq+8, 2qq+9) <-> +{2,3}
+      float amax = 0.f;
+      float qv[G::kKSteps][4];
+#pragma unroll
+      for (int ks = 0; ks < G::kKSteps; ++ks)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          qv[ks][e] = qn < nh ? QE::load(qrow + 32 * qq + 4 * ks + e) : 0.f;
+          amax = fmaxf(amax, fabsf(qv[ks][e]));
+        }
+      amax = warp_max_xor(amax, 1, 2);
+      int ex = 0;
+      frexpf(amax, &ex);                        // amax < 2^ex
+      int sh = 15 - ex;                         // |q| * 2^sh < 2^15, exact in f16
+      sh = max(-100, min(100, sh));
+#pragma unroll
+      for (int ks = 0; ks < G::kKSteps; ++ks) {
+        qb[ks][0] = pack2<PA_F16>(ldexpf(qv[ks][0], sh), ldexpf(qv[ks][1], sh));
+        qb[ks][1] = pack2<PA_F16>(ldexpf(qv[ks][2], sh), ldexpf(qv[ks][3], sh));
+      }
+      const float kc = base_c * (*p.k_scale);
+      const float my_c = ldexpf(kc, -sh);
+      cA = __shfl_sync(0xffffffffu, my_c, 8 * qq);      // head 2qq lives in lanes 8qq..8qq+3
+      cB = __shfl_sync(0xffffffffu, my_c, 8 * qq + 4);  // head 2qq+1
+    }
+  }
+
+  float acc[G::kDTiles][4];
+#pragma unroll
+  for (int i = 0; i < G::kDTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+  bool failed = false;
+  int consumed = 0;
+
+  for (int i = 0; i < nmine; ++i) {
+    const int s = i % ST;
+    const bool got = mbar_wait_bounded(wbars + s, (i / ST) & 1);
+    if (!__all_sync(0xffffffffu, got)) {
+      failed = true;
+      break;
+    }
+    consumed = i + 1;
+    const int jb = b0 + warp + i * NW;
+    const int phys = table[jb];
+    if (phys >= 0 && phys < p.num_blocks) {
+      const uint32_t kbase = smem_u32(ring + s * 2 * TB);
+      const uint32_t vbase = kbase + TB;
+      const int rem = seq_len - jb * BS;  // valid tokens in this block (>= BS except the tail)
+
+      // ---- S^T = K Q^T
+      float sc[G::kMTiles][4];
+#pragma unroll
+      for (int mt = 0; mt < G::kMTiles; ++mt) {
+        sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+        if constexpr (!kFp8) {
+#pragma unroll
+          for (int ks = 0; ks < G::kKSteps; ++ks) {
+            const int tok = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
+            const int chunk = 2 * ks + (lane >> 4);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(kbase + swz128(tok * G::kRowsPerToken + (chunk >> 3), chunk & 7), a0, a1, a2, a3);
+            mma_16816<MDT>(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+          }
+        } else {
+          const int tA = 16 * mt + (lane >> 2), tB = tA + 8;
+          const uint4 ka0 = *reinterpret_cast<const uint4*>(ring + s * 2 * TB + swz128(tA, 2 * qq));
+          const uint4 ka1 = *reinterpret_cast<const uint4*>(ring + s * 2 * TB + swz128(tA, 2 * qq + 1));
+          const uint4 kb0 = *reinterpret_cast<const uint4*>(ring + s * 2 * TB + swz128(tB, 2 * qq));
+          const uint4 kb1 = *reinterpret_cast<const uint4*>(ring + s * 2 * TB + swz128(tB, 2 * qq + 1));
+          const uint32_t wa[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
+          const uint32_t wb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
+#pragma unroll
+          for (int ks = 0; ks < G::kKSteps; ++ks) {
+            const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(wa[ks] & 0xffffu));
+            const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(wa[ks] >> 16));
+            const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(wb[ks] & 0xffffu));
+            const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(wb[ks] >> 16));
+            mma_16816<PA_F16>(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+          }
+        }
+      }
+
+      // ---- online softmax on the accumulators (columns 2qq, 2qq+1 = heads A, B)
+      float mxA = -INFINITY, mxB = -INFINITY;
+#pragma unroll
+      for (int mt = 0; mt < G::kMTiles; ++mt) {
+        const int t0 = 16 * mt + (lane >> 2);
+        const bool v0 = t0 < rem, v1 = t0 + 8 < rem;
+        sc[mt][0] = v0 ? sc[mt][0] * cA : -INFINITY;
+        sc[mt][1] = v0 ? sc[mt][1] * cB : -INFINITY;
+        sc[mt][2] = v1 ? sc[mt][2] * cA : -INFINITY;
+        sc[mt][3] = v1 ? sc[mt][3] * cB : -INFINITY;
+        mxA = fmaxf(mxA, fmaxf(sc[mt][0], sc[mt][2]));
+        mxB = fmaxf(mxB, fmaxf(sc[mt][1], sc[mt][3]));
+      }
+      mxA = warp_max_xor(mxA, 4, 16);
+      mxB = warp_max_xor(mxB, 4, 16);
+      const float nA = fmaxf(mA, mxA), nB = fmaxf(mB, mxB);
+      const float uA = nA == -INFINITY ? 0.f : nA, uB = nB == -INFINITY ? 0.f : nB;
+      const float alA = exp2f(mA - uA), alB = exp2f(mB - uB);
+      mA = nA;
+      mB = nB;
+      uint32_t pb[G::kMTiles][2];
+      float addA = 0.f, addB = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < G::kMTiles; ++mt) {
+        const uint32_t X = pack2<MDT>(exp2f(sc[mt][0] - uA), exp2f(sc[mt][1] - uB));
+        const uint32_t Y = pack2<MDT>(exp2f(sc[mt][2] - uA), exp2f(sc[mt][3] - uB));
+        const float2 fx = unpack2<MDT>(X), fy = unpack2<MDT>(Y);
+        addA += fx.x + fy.x;
+        addB += fx.y + fy.y;
+        pb[mt][0] = movmatrix_trans(X);
+        pb[mt][1] = movmatrix_trans(Y);
+      }
+      lA = lA * alA + addA;
+      lB = lB * alB + addB;
+#pragma unroll
+      for (int dt = 0; dt < G::kDTiles; ++dt) {
+        acc[dt][0] *= alA;
+        acc[dt][1] *= alB;
+        acc[dt][2] *= alA;
+        acc[dt][3] *= alB;
+      }
+
+      // ---- O^T += V^T P^T
+      const bool tail = rem < BS;
+#pragma unroll
+      for (int kt = 0; kt < G::kMTiles; ++kt) {
+        if constexpr (!kFp8) {
+          const int tk = 16 * kt + 2 * qq;  // tokens of this thread's A halves: tk, tk+1, tk+8, tk+9
+          const uint32_t lo0 = tk < rem ? 0xffffu : 0u, hi0 = tk + 1 < rem ? 0xffff0000u : 0u;
+          const uint32_t lo1 = tk + 8 < rem ? 0xffffu : 0u, hi1 = tk + 9 < rem ? 0xffff0000u : 0u;
+          const uint32_t m01 = lo0 | hi0, m23 = lo1 | hi1;
+#pragma unroll
+          for (int dt = 0; dt < G::kDTiles; ++dt) {
+            const int tok = 16 * kt + (lane & 7) + 8 * (lane >> 4);
+            const int chunk = 2 * dt + ((lane >> 3) & 1);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_trans(vbase + swz128(tok * G::kRowsPerToken + (chunk >> 3), chunk & 7), a0, a1, a2, a3);
+            if (tail) {
+              a0 &= m01;
+              a1 &= m01;
+              a2 &= m23;
+              a3 &= m23;
+            }
+            mma_16816<MDT>(acc[dt], a0, a1, a2, a3, pb[kt][0], pb[kt][1]);
+          }
+        } else {
+          // this thread owns dims 16*(lane>>2) .. +15 of tokens 16kt + {2qq, 2qq+1, 2qq+8, 2qq+9}
+          const int rr = lane >> 2;
+          const uint8_t* vt = ring + s * 2 * TB + TB;
+          const int tk = 16 * kt + 2 * qq;
+          uint4 v[4];
+          v[0] = *reinterpret_cast<const uint4*>(vt + swz128(tk, rr));
+          v[1] = *reinterpret_cast<const uint4*>(vt + swz128(tk + 1, rr));
+          v[2] = *reinterpret_cast<const uint4*>(vt + swz128(tk + 8, rr));
+          v[3] = *reinterpret_cast<const uint4*>(vt + swz128(tk + 9, rr));
+          if (tail) {
+            if (tk >= rem) v[0] = make_uint4(0, 0, 0, 0);
+            if (tk + 1 >= rem) v[1] = make_uint4(0, 0, 0, 0);
+            if (tk + 8 >= rem) v[2] = make_uint4(0, 0, 0, 0);
+            if (tk + 9 >= rem) v[3] = make_uint4(0, 0, 0, 0);
+          }
+          const uint32_t w0[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
+          const uint32_t w1[4] = {v[1].x, v[1].y, v[1].z, v[1].w};
+          const uint32_t w2[4] = {v[2].x, v[2].y, v[2].z, v[2].w};
+          const uint32_t w3[4] = {v[3].x, v[3].y, v[3].z, v[3].w};
+#pragma unroll
+          for (int dt = 0; dt < G::kDTiles; ++dt) {
+            const int sh = 16 * (dt & 1);
+            const uint32_t x0 = e4m3x2_to_f16x2(static_cast<uint16_t>(w0[dt >> 1] >> sh));
+            const uint32_t y0 = e4m3x2_to_f16x2(static_cast<uint16_t>(w1[dt >> 1] >> sh));
+            const uint32_t x1 = e4m3x2_to_f16x2(static_cast<uint16_t>(w2[dt >> 1] >> sh));
+            const uint32_t y1 = e4m3x2_to_f16x2(static_cast<uint16_t>(w3[dt >> 1] >> sh));
+            const uint32_t a0 = __byte_perm(x0, y0, 0x5410), a1 = __byte_perm(x0, y0, 0x7632);
+            const uint32_t a2 = __byte_perm(x1, y1, 0x5410), a3 = __byte_perm(x1, y1, 0x7632);
+            mma_16816<PA_F16>(acc[dt], a0, a1, a2, a3, pb[kt][0], pb[kt][1]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (i + ST < nmine && lane == 0) {
+      fence_proxy_async();
+      issue(i + ST);
+    }
+  }
+  if (failed) {
+    // a copy never completed: record it, give the copies still in flight a bounded
+    // chance to land, and write nothing for this CTA
+    if (lane == 0) {
+      flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+      for (int i = consumed; i < min(consumed + ST, nmine); ++i)
+        (void)mbar_wait_bounded(wbars + (i % ST), (i / ST) & 1, 100000000ull);
+    }
+    s_failed = 1;
+  }
+
+  // ---- merge the warps' states through shared memory
+  lA = warp_sum_xor(lA, 4, 16);
+  lB = warp_sum_xor(lB, 4, 16);
+  __syncthreads();
+  if (s_failed) return;
+  float* red = reinterpret_cast<float*>(smem);  // [NW][8][HEAD]
+  float* rm = red + NW * 8 * HEAD;              // [NW][8]
+  float* rl = rm + NW * 8;                      // [NW][8]
+  {
+    const int rr = lane >> 2;
+#pragma unroll
+    for (int dt = 0; dt < G::kDTiles; ++dt) {
+      const int dA = kFp8 ? 16 * rr + 2 * dt : 16 * dt + rr;
+      const int dB = kFp8 ? dA + 1 : dA + 8;
+      red[(warp * 8 + 2 * qq) * HEAD + dA] = acc[dt][0];
+      red[(warp * 8 + 2 * qq + 1) * HEAD + dA] = acc[dt][1];
+      red[(warp * 8 + 2 * qq) * HEAD + dB] = acc[dt][2];
+      red[(warp * 8 + 2 * qq + 1) * HEAD + dB] = acc[dt][3];
+    }
+    if (lane < 4) {
+      rm[warp * 8 + 2 * lane] = mA;
+      rm[warp * 8 + 2 * lane + 1] = mB;
+      rl[warp * 8 + 2 * lane] = lA;
+      rl[warp * 8 + 2 * lane + 1] = lB;
+    }
+  }
+  __syncthreads();
+  const float vscale = kFp8 ? *p.v_scale : 1.f;
+  const long long pbase = p.part_off ? (long long)p.part_off[r] : (long long)row * p.max_partitions;
+  for (int idx = threadIdx.x; idx < nh * HEAD; idx += NW * 32) {
+    const int n = idx / HEAD, dd = idx % HEAD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+      if (rl[w * 8 + n] > 0.f) M = fmaxf(M, rm[w * 8 + n]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float lw = rl[w * 8 + n];
+      if (lw > 0.f) {
+        const float f = exp2f(rm[w * 8 + n] - M);
+        L = fmaf(lw, f, L);
+        O = fmaf(red[(w * 8 + n) * HEAD + dd], f, O);
+      }
+    }
+    O *= vscale;
+    const int h = h0 + n;
+    if (nparts == 1) {
+      out[((long long)row * p.num_q_heads + h) * HEAD + dd] = QE::from_float(L > 0.f ? O / L : 0.f);
+    } else {
+      const long long pi = pbase + z;
+      p.ws_acc[(pi * p.num_q_heads + h) * HEAD + dd] = O;
+      if (dd == 0) p.ws_ml[pi * p.num_q_heads + h] = make_float2(M, L);
+    }
+  }
+}
+
+template <int QDT, int KVDT, int HEAD, int BS>
+cudaError_t launch_t(const AttnParams& p, int grid_z, const CUtensorMap* tk, const CUtensorMap* tv,
+                     cudaStream_t stream) {
+  constexpr int NW = 4;
+  constexpr int smem = decode_smem_bytes<KVDT, HEAD, BS, NW>();
+  auto kern = decode_mma_kernel<QDT, KVDT, HEAD, BS, NW>;
+  static int configured_device = -1;  // the attribute is per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  dim3 grid(p.num_seqs, p.num_kv_heads * p.num_head_groups, grid_z);
+  kern<<<grid, NW * 32, smem, stream>>>(p, *tk, *tv);
+  return cudaGetLastError();
+}
+
+template <int QDT, int KVDT>
+cudaError_t launch_shape(const AttnParams& p, int grid_z, const CUtensorMap* tk,
+                         const CUtensorMap* tv, cudaStream_t s) {
+  const int d = p.head_size, bs = p.block_size;
+  if constexpr (KVDT != PA_FP8_E4M3) {
+    if (d == 128 && bs == 16) return launch_t<QDT, KVDT, 128, 16>(p, grid_z, tk, tv, s);
+    if (d == 128 && bs == 32) return launch_t<QDT, KVDT, 128, 32>(p, grid_z, tk, tv, s);
+    if (d == 64 && bs == 16) return launch_t<QDT, KVDT, 64, 16>(p, grid_z, tk, tv, s);
+    if (d == 64 && bs == 32) return launch_t<QDT, KVDT, 64, 32>(p, grid_z, tk, tv, s);
+  } else {
+    if (d == 128 && bs == 16) return launch_t<QDT, KVDT, 128, 16>(p, grid_z, tk, tv, s);
+    if (d == 128 && bs == 32) return launch_t<QDT, KVDT, 128, 32>(p, grid_z, tk, tv, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool decode_mma_supported(int q_dtype, int kv_dtype, int head_size, int block_size, int group) {
+  (void)group;
+  const bool q16 = q_dtype == PA_BF16 || q_dtype == PA_F16;
+  if (!q16) return false;
+  if (kv_dtype == q_dtype) return (head_size == 64 || head_size == 128) && (block_size == 16 || block_size == 32);
+  if (kv_dtype == PA_FP8_E4M3) return head_size == 128 && (block_size == 16 || block_size == 32);
+  return false;
+}
+
+cudaError_t launch_decode_mma(const AttnParams& p, int q_dtype, int kv_dtype, int grid_z,
+                              const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                              cudaStream_t stream) {
+  if (q_dtype == PA_BF16 && kv_dtype == PA_BF16) return launch_shape<PA_BF16, PA_BF16>(p, grid_z, tmap_k, tmap_v, stream);
+  if (q_dtype == PA_F16 && kv_dtype == PA_F16) return launch_shape<PA_F16, PA_F16>(p, grid_z, tmap_k, tmap_v, stream);
+  if (q_dtype == PA_BF16 && kv_dtype == PA_FP8_E4M3) return launch_shape<PA_BF16, PA_FP8_E4M3>(p, grid_z, tmap_k, tmap_v, stream);
+  if (q_dtype == PA_F16 && kv_dtype == PA_FP8_E4M3) return launch_shape<PA_F16, PA_FP8_E4M3>(p, grid_z, tmap_k, tmap_v, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

@@ -1,0 +1,296 @@
+// Device-side building blocks shared by the library's kernels: element types,
+// parameter blocks, the error word, and thin inline-PTX wrappers for mbarriers,
+// TMA bulk-tensor copies, ldmatrix / movmatrix and the warp-level tensor-core MMA.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa_internal.h"
+
+namespace pa {
+
+// ---------------------------------------------------------------- elements
+
+template <int DT>
+struct Elem;
+template <>
+struct Elem<PA_F32> {
+  using T = float;
+  static constexpr int bytes = 4;
+  static __device__ __forceinline__ float load(const T* p) { return *p; }
+  static __device__ __forceinline__ T from_float(float x) { return x; }
+};
+template <>
+struct Elem<PA_F16> {
+  using T = __half;
+  static constexpr int bytes = 2;
+  static __device__ __forceinline__ float load(const T* p) { return __half2float(*p); }
+  static __device__ __forceinline__ T from_float(float x) { return __float2half_rn(x); }
+};
+template <>
+struct Elem<PA_BF16> {
+  using T = __nv_bfloat16;
+  static constexpr int bytes = 2;
+  static __device__ __forceinline__ float load(const T* p) { return __bfloat162float(*p); }
+  static __device__ __forceinline__ T from_float(float x) { return __float2bfloat16_rn(x); }
+};
+template <>
+struct Elem<PA_FP8_E4M3> {
+  using T = uint8_t;
+  static constexpr int bytes = 1;
+  static __device__ __forceinline__ float load(const T* p) {
+    __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(*p), __NV_E4M3);
+    return __half2float(__half(h));
+  }
+};
+
+__device__ __forceinline__ void flag_error(unsigned* err, unsigned bits) {
+  if (err) atomicOr(err, bits);
+}
+
+__device__ __forceinline__ int ceil_div_dev(int a, int b) { return (a + b - 1) / b; }
+
+// Index of the first partial row of query row `row`, and the partition count of
+// the row's request (see pa_internal.h, AttnParams).
+__device__ __forceinline__ long long partial_base(const AttnParams& p, int request, int row,
+                                                  int row_in_request, int parts_of_request) {
+  if (p.part_off) return (long long)p.part_off[request] + (long long)row_in_request * parts_of_request;
+  return (long long)row * p.max_partitions;
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of an mbarrier, giving up after `limit_ns` nanoseconds.
+// Returns false on timeout.  Every thread that calls it polls on its own.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// ---------------------------------------------------------------- TMA
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 3-D tiled bulk-tensor copy global -> shared, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of 128-byte row `row` inside a tile
+// written by TMA with CU_TENSOR_MAP_SWIZZLE_128B (tile base 1024-byte aligned).
+__device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk) {
+  return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+// ---------------------------------------------------------------- warp MMA
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+template <int DT>
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1);
+
+template <>
+__device__ __forceinline__ void mma_16816<PA_BF16>(float (&c)[4], uint32_t a0, uint32_t a1,
+                                                   uint32_t a2, uint32_t a3, uint32_t b0,
+                                                   uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <>
+__device__ __forceinline__ void mma_16816<PA_F16>(float (&c)[4], uint32_t a0, uint32_t a1,
+                                                  uint32_t a2, uint32_t a3, uint32_t b0,
+                                                  uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Pack two fp32 into one register of two 16-bit elements (lo = a), round to nearest.
+template <int DT>
+__device__ __forceinline__ uint32_t pack2(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack2<PA_BF16>(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<PA_F16>(float a, float b) {
+  __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// The two fp32 values of a packed pair (exact widening).
+template <int DT>
+__device__ __forceinline__ float2 unpack2(uint32_t v);
+template <>
+__device__ __forceinline__ float2 unpack2<PA_BF16>(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+template <>
+__device__ __forceinline__ float2 unpack2<PA_F16>(uint32_t v) {
+  __half2 h = *reinterpret_cast<__half2*>(&v);
+  return __half22float2(h);
+}
+
+// Two e4m3 codes (low byte first) -> two f16 in one register, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+__device__ __forceinline__ float warp_max_xor(float v, int lane_mask_lo, int lane_mask_hi) {
+  for (int m = lane_mask_lo; m <= lane_mask_hi; m <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum_xor(float v, int lane_mask_lo, int lane_mask_hi) {
+  for (int m = lane_mask_lo; m <= lane_mask_hi; m <<= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+  return v;
+}
+
+}  // namespace pa
+
+namespace pa {
+
+// Where a query row sits: its request, position, the keys it attends and the
+// split-K partitioning of those keys.
+struct RowInfo {
+  int request;
+  int q_len;
+  int j;          // row index inside its request
+  int seq_len;
+  int pos;        // position of the query token: seq_len - q_len + j
+  int kv_len;     // number of keys attended: pos + 1 (causal) or seq_len
+  int part;       // partition tokens for this request
+  int parts_req;  // partitions covering seq_len (sizes the request's partial rows)
+  int parts_row;  // partitions covering kv_len (the ones this row uses)
+  bool ok;
+};
+
+__device__ __forceinline__ RowInfo row_info(const AttnParams& p, int row) {
+  RowInfo ri;
+  if (p.query_start_loc == nullptr) {
+    ri.request = row;
+    ri.q_len = 1;
+    ri.j = 0;
+  } else {
+    int lo = 0, hi = p.num_seqs;  // first r with qsl[r+1] > row
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (p.query_start_loc[mid + 1] <= row) lo = mid + 1; else hi = mid;
+    }
+    ri.request = lo < p.num_seqs ? lo : p.num_seqs - 1;
+    const int s = p.query_start_loc[ri.request];
+    ri.q_len = p.query_start_loc[ri.request + 1] - s;
+    ri.j = row - s;
+  }
+  ri.seq_len = p.seq_lens[ri.request];
+  ri.ok = ri.seq_len >= 1 && ri.seq_len <= p.max_seq_len &&
+          (long long)ri.seq_len <= (long long)p.max_blocks_per_seq * p.block_size &&
+          ri.q_len >= 1 && ri.q_len <= ri.seq_len && ri.j >= 0 && ri.j < ri.q_len;
+  ri.pos = ri.seq_len - ri.q_len + ri.j;
+  ri.kv_len = p.causal ? ri.pos + 1 : ri.seq_len;
+  ri.part = ri.q_len == 1 ? p.part : p.part_pf;
+  ri.parts_req = ri.ok ? ceil_div_dev(ri.seq_len, ri.part) : 0;
+  ri.parts_row = ri.ok ? ceil_div_dev(ri.kv_len, ri.part) : 0;
+  return ri;
+}
+
+// Varlen launches do nothing when query_start_loc was found inconsistent (the plan
+// kernel has flagged it); this keeps every row and partial index in range.
+__device__ __forceinline__ bool plan_rejected(const AttnParams& p) {
+  return p.query_start_loc != nullptr && p.plan_ok != nullptr && *p.plan_ok == 0;
+}
+
+__device__ __forceinline__ long long row_partial_base(const AttnParams& p, const RowInfo& ri,
+                                                      int row) {
+  return partial_base(p, ri.request, row, ri.j, ri.parts_req);
+}
+
+}  // namespace pa

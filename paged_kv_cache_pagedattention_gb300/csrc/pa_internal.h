@@ -1,0 +1,90 @@
+// Internal interfaces between the C-ABI layer (api.cu) and the kernel translation
+// units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// Everything an attention kernel needs.  "Rows" are query rows: one per sequence
+// in decode mode (query_start_loc == nullptr), one per flattened query token in
+// varlen mode.
+struct AttnParams {
+  void* out;                       // [num_rows][Hq][d], q dtype
+  const void* q;                   // [num_rows][Hq][d], q dtype
+  const void* k_cache;             // [num_blocks][Hkv][bs][d]
+  const void* v_cache;
+  const int32_t* block_tables;     // [num_seqs][max_blocks_per_seq]
+  const int32_t* seq_lens;         // [num_seqs]
+  const int32_t* query_start_loc;  // [num_seqs+1] in varlen mode, nullptr in decode mode
+  const int32_t* part_off;         // varlen: first partial row of each request (plan kernel)
+  const int4* work;                // varlen: prefill tile work list (plan kernel)
+  const int32_t* work_count;       // varlen: number of entries in `work`
+  const int32_t* plan_ok;          // varlen: 1 when query_start_loc passed the plan kernel's checks
+  float* ws_acc;                   // [partial rows][Hq][d]  un-normalised weighted sums
+  float2* ws_ml;                   // [partial rows][Hq]     (running max in log2 units, weight sum)
+  const float* k_scale;            // FP8 only
+  const float* v_scale;
+  unsigned* err;                   // device error word
+  int num_seqs;
+  int num_rows;
+  int num_blocks;
+  int max_blocks_per_seq;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_size;
+  int block_size;
+  int group;            // Hq / Hkv
+  int num_head_groups;  // ceil(group / 8) for the tensor-core kernels
+  int max_seq_len;
+  int max_query_len;
+  int part;             // partition tokens for rows of single-token requests
+  int part_pf;          // partition tokens for rows of multi-token requests
+  int max_partitions;   // decode mode: partial rows reserved per query row
+  int causal;
+  float scale;          // softmax scale
+};
+
+struct ScatterParams {
+  const void* key;
+  const void* value;
+  void* k_cache;
+  void* v_cache;
+  const int64_t* slot_mapping;
+  const float* k_scale;
+  const float* v_scale;
+  unsigned* err;
+  int num_tokens;
+  int num_blocks;
+  int num_kv_heads;
+  int head_size;
+  int block_size;
+};
+
+// Tokens of query rows in one prefill tile of the tensor-core varlen kernel.
+int prefill_tile_tokens(int group);
+
+cudaError_t launch_reshape_and_cache(const ScatterParams& p, int src_dtype, int cache_dtype,
+                                     cudaStream_t stream);
+cudaError_t launch_attn_generic(const AttnParams& p, int q_dtype, int kv_dtype, int grid_z,
+                                int only_multi_token, cudaStream_t stream);
+cudaError_t launch_merge(const AttnParams& p, int q_dtype, cudaStream_t stream);
+cudaError_t launch_varlen_plan(const AttnParams& p, int32_t* part_off, int4* work,
+                               int32_t* work_count, int max_work, cudaStream_t stream);
+
+bool decode_mma_supported(int q_dtype, int kv_dtype, int head_size, int block_size, int group);
+cudaError_t launch_decode_mma(const AttnParams& p, int q_dtype, int kv_dtype, int grid_z,
+                              const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                              cudaStream_t stream);
+
+bool prefill_mma_supported(int q_dtype, int kv_dtype, int head_size, int block_size, int group);
+cudaError_t launch_prefill_mma(const AttnParams& p, int q_dtype, int kv_dtype, int num_ctas,
+                               const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                               cudaStream_t stream);
+
+}  // namespace pa

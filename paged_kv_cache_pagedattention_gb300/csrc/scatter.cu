@@ -1,0 +1,117 @@
+// reshape_and_cache: write each new token's K and V rows into its slot of the
+// paged cache.  [NOTES] "Prefill 与 Decode" (prefill stores every prompt token's
+// K/V, decode appends the new token's); [ARCH] Part 1, forward pass (slot_mapping
+// built during input preparation).  Slot s -> block s / block_size, offset
+// s % block_size; negative slots are padding.
+//
+// One thread moves one 16-byte piece of a destination row (same dtype: a straight
+// copy of 16 bytes; FP8: 16 codes quantised from 16 source elements).  Threads of a
+// warp cover consecutive pieces of consecutive rows, so both the source reads and
+// the destination writes are coalesced 16-byte accesses.
+#include "pa_common.cuh"
+
+namespace pa {
+
+namespace {
+
+__global__ void __launch_bounds__(256) scatter_copy_kernel(const ScatterParams p, int elem_bytes) {
+  const int pieces = p.head_size * elem_bytes / 16;  // per (token, head) row
+  const long long per_token = (long long)p.num_kv_heads * pieces;
+  const long long total = (long long)p.num_tokens * per_token;
+  const long long limit = (long long)p.num_blocks * p.block_size;
+  for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < total;
+       u += (long long)gridDim.x * blockDim.x) {
+    const long long t = u / per_token;
+    const int rem = static_cast<int>(u - t * per_token);
+    const int h = rem / pieces, c = rem % pieces;
+    const long long slot = p.slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= limit) {
+      flag_error(p.err, PA_ERRFLAG_SLOT);
+      continue;
+    }
+    const long long blk = slot / p.block_size, off = slot % p.block_size;
+    const long long src = (t * p.num_kv_heads + h) * pieces + c;
+    const long long dst = ((blk * p.num_kv_heads + h) * p.block_size + off) * pieces + c;
+    const uint4 kv = reinterpret_cast<const uint4*>(p.key)[src];
+    const uint4 vv = reinterpret_cast<const uint4*>(p.value)[src];
+    reinterpret_cast<uint4*>(p.k_cache)[dst] = kv;
+    reinterpret_cast<uint4*>(p.v_cache)[dst] = vv;
+  }
+}
+
+// x / scale in IEEE fp32 (correctly rounded division), then e4m3 round-to-nearest-even
+// with saturation to the largest finite value, via the CUDA conversion intrinsic.
+__device__ __forceinline__ uint8_t quant_e4m3(float x, float scale) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3));
+}
+
+template <int SRC>
+__global__ void __launch_bounds__(256) scatter_fp8_kernel(const ScatterParams p) {
+  using SE = Elem<SRC>;
+  const int pieces = p.head_size / 16;  // 16 codes per piece
+  const long long per_token = (long long)p.num_kv_heads * pieces;
+  const long long total = (long long)p.num_tokens * per_token;
+  const long long limit = (long long)p.num_blocks * p.block_size;
+  const float ks = *p.k_scale, vs = *p.v_scale;
+  for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < total;
+       u += (long long)gridDim.x * blockDim.x) {
+    const long long t = u / per_token;
+    const int rem = static_cast<int>(u - t * per_token);
+    const int h = rem / pieces, c = rem % pieces;
+    const long long slot = p.slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= limit) {
+      flag_error(p.err, PA_ERRFLAG_SLOT);
+      continue;
+    }
+    const long long blk = slot / p.block_size, off = slot % p.block_size;
+    const long long src = ((t * p.num_kv_heads + h) * p.head_size) + c * 16;
+    const long long dst = ((blk * p.num_kv_heads + h) * p.block_size + off) * p.head_size + c * 16;
+    const typename SE::T* ksrc = reinterpret_cast<const typename SE::T*>(p.key) + src;
+    const typename SE::T* vsrc = reinterpret_cast<const typename SE::T*>(p.value) + src;
+    uint32_t kw[4], vw[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t kb = 0, vb = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        kb |= static_cast<uint32_t>(quant_e4m3(SE::load(ksrc + 4 * w + b), ks)) << (8 * b);
+        vb |= static_cast<uint32_t>(quant_e4m3(SE::load(vsrc + 4 * w + b), vs)) << (8 * b);
+      }
+      kw[w] = kb;
+      vw[w] = vb;
+    }
+    reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.k_cache) + dst)[0] = make_uint4(kw[0], kw[1], kw[2], kw[3]);
+    reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.v_cache) + dst)[0] = make_uint4(vw[0], vw[1], vw[2], vw[3]);
+  }
+}
+
+int scatter_grid(long long units) {
+  long long blocks = (units + 255) / 256;
+  if (blocks > 152LL * 64) blocks = 152LL * 64;
+  return static_cast<int>(blocks < 1 ? 1 : blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_reshape_and_cache(const ScatterParams& p, int src_dtype, int cache_dtype,
+                                     cudaStream_t stream) {
+  if (p.num_tokens == 0) return cudaSuccess;
+  if (src_dtype == cache_dtype) {
+    const int eb = src_dtype == PA_F32 ? 4 : (src_dtype == PA_FP8_E4M3 ? 1 : 2);
+    const long long units = (long long)p.num_tokens * p.num_kv_heads * (p.head_size * eb / 16);
+    scatter_copy_kernel<<<scatter_grid(units), 256, 0, stream>>>(p, eb);
+    return cudaGetLastError();
+  }
+  if (cache_dtype != PA_FP8_E4M3) return cudaErrorInvalidValue;
+  const long long units = (long long)p.num_tokens * p.num_kv_heads * (p.head_size / 16);
+  const int g = scatter_grid(units);
+  if (src_dtype == PA_F32) scatter_fp8_kernel<PA_F32><<<g, 256, 0, stream>>>(p);
+  else if (src_dtype == PA_F16) scatter_fp8_kernel<PA_F16><<<g, 256, 0, stream>>>(p);
+  else if (src_dtype == PA_BF16) scatter_fp8_kernel<PA_BF16><<<g, 256, 0, stream>>>(p);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,98 @@
+"""CPU-side checks of the C ABI: the library builds, loads, and exports every
+symbol include/pa.h declares; host-only entry points behave as documented.
+No compute call is made here (there may be no GPU)."""
+
+import ctypes
+import importlib.util
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+def _lib_path():
+    spec = importlib.util.spec_from_file_location(
+        "_pa_build", os.path.join(ROOT, "paged_kv_cache_pagedattention_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()
+
+
+@pytest.fixture(scope="module")
+def pa():
+    _lib_path()
+    import paged_kv_cache_pagedattention_gb300 as lib
+    return lib
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_hot_path_calls():
+    names = declared_functions()
+    for n in ("pa_reshape_and_cache", "pa_decode", "pa_varlen_attn"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(pa):
+    lib = ctypes.CDLL(pa.LIB_PATH)
+    names = declared_functions()
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert sorted(pa.SIGNATURES) == names
+
+
+def test_status_strings_and_version(pa):
+    for s in range(7):
+        assert pa.pa_status_string(s).startswith("PA_")
+    assert pa.pa_status_string(99) == "unknown pa_status"
+    assert pa.pa_version() >= 100
+
+
+def test_workspace_sizes(pa):
+    a = pa.pa_decode_workspace_size(64, 32, 8, 128, 4096, 16)
+    assert a >= 256 and a % 256 == 0
+    # more context or more sequences never needs less workspace
+    assert pa.pa_decode_workspace_size(64, 32, 8, 128, 8192, 16, 512) >= pa.pa_decode_workspace_size(
+        64, 32, 8, 128, 4096, 16, 512)
+    assert pa.pa_decode_workspace_size(128, 32, 8, 128, 4096, 16, 512) >= pa.pa_decode_workspace_size(
+        64, 32, 8, 128, 4096, 16, 512)
+    # explicit partition: partial rows = B * ceil(max_len / part); each row Hq*(8 + 4d) bytes
+    exp = 256 + (64 * 8 * 32 * 8 + 255) // 256 * 256 + (64 * 8 * 32 * 128 * 4 + 255) // 256 * 256
+    assert pa.pa_decode_workspace_size(64, 32, 8, 128, 4096, 16, 512) == exp
+    assert pa.pa_varlen_workspace_size(132, 2176, 512, 32, 8, 128, 66048, 16) >= 256
+    assert pa.pa_decode_workspace_size(0, 32, 8, 128, 4096, 16) == 256
+
+
+def test_default_partition_is_a_block_multiple(pa):
+    for bs in (16, 32, 48):
+        for b, hkv, L in ((4, 2, 200), (64, 8, 4096), (16, 8, 262144), (256, 8, 32768), (1, 1, 10 ** 7)):
+            part = pa.pa_default_partition_size(b, hkv, L, bs)
+            assert part % bs == 0 and part >= bs
+            assert -(-L // part) <= 65535
+
+
+def test_host_validation_rejects_null_pointers_without_a_gpu(pa):
+    lib = ctypes.CDLL(pa.LIB_PATH)
+    for name, (res, args) in pa.SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    st = lib.pa_decode(None, None, None, None, 10, None, 4, None, 2, 64, 8, 2, 128, 16, 1.0, 2, 2, None, None,
+                       0, None, 0, None)
+    assert st == pa.PA_ERR_INVALID_ARG
+    st = lib.pa_varlen_attn(None, None, None, None, 10, None, 4, None, None, 2, 5, 4, 64, 8, 2, 128, 16, 1.0, 1,
+                            2, 2, None, None, 0, None, 0, None)
+    assert st == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_reshape_and_cache(None, None, None, None, None, 0, 10, 2, 128, 16, 2, 2, None, None,
+                                    None) == pa.PA_OK  # nothing to write
+    assert lib.pa_reshape_and_cache(None, None, None, None, None, 3, 10, 2, 128, 16, 2, 2, None, None,
+                                    None) == pa.PA_ERR_INVALID_ARG
+    # zero sequences: a no-op that succeeds before touching any pointer
+    assert lib.pa_decode(None, None, None, None, 10, None, 4, None, 0, 64, 8, 2, 128, 16, 1.0, 2, 2, None, None,
+                         0, None, 0, None) == pa.PA_OK
