@@ -1,0 +1,511 @@
+"""Benchmark of the paged KV cache hot path on GB300 (one JSON line on stdout).
+
+A step is one pass of the hot path over one batch: the scatter of every
+sequence's new token into the paged cache (pa_reshape_and_cache), then
+PagedAttention decode over the whole batch (pa_decode: split-K attention kernel
++ partial merge).  The default workload is the long-context agentic decode
+(batch 16 = 3 families of parent + 4 forks sharing 96% of their blocks + 1 lone
+parent, lengths log-normal around 142K tokens, 64 query / 8 KV heads, head 128,
+bf16, block 16).  Its KV working set (~2.7 GB unique) is far larger than L2, so
+consecutive steps do not hit in L2 across iterations.
+
+metric: attended KV tokens per second (sum of seq_lens per step / step time),
+whole job over all ranks.  Multi-GPU (torchrun): each rank runs its own
+independent batch (weak scaling, no collective on the data path).
+
+`--impl reference` times the fp64 CPU oracle instead (the reference arm of this
+build), on the host cores, on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import multiprocessing as mp
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attended KV tokens/sec and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
+UNIT = "tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+WORKLOADS = ("agentic", "llama", "fp8", "mixed", "tiny")
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def max_over_ranks(x: float, device) -> float:
+    """Max of a float over all ranks (identity without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank draws its own batch of the same shape (weak scaling)."""
+    return base + 7919 * rank
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+
+        self.path = tempfile.mktemp(prefix="pa_clocks_", suffix=".csv")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                if self.bus_id and not self.bus_id.endswith(parts[1].lower()[-12:]) and \
+                        not parts[1].lower().endswith(self.bus_id[-12:]):
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        smax = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def unique_kv_tokens(b) -> int:
+    """Token slots that hold data some sequence reads, shared blocks counted once."""
+    import numpy as np
+
+    valid = {}
+    for s in range(b.num_seqs):
+        n = int(b.seq_lens[s])
+        nb = -(-n // b.block_size)
+        for j in range(nb):
+            cnt = min(b.block_size, n - j * b.block_size)
+            p = int(b.block_tables[s, j])
+            if cnt > valid.get(p, 0):
+                valid[p] = cnt
+    return int(np.sum(list(valid.values()), dtype=np.int64))
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("attn_decode.cu", "pa_common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_pagedattention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary,
+    if it was captured on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"decode_mma_kernel_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_per_launch_bytes\s*=\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_hash\s*=\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != decode_source_hash():
+        return None
+    return float(m.group(1))
+
+
+# ----------------------------------------------------------------------------- workload
+
+def make_workload(name: str, seed: int, length_scale: float = 1.0):
+    import workloads
+
+    if name == "agentic":
+        return workloads.agentic(seed=seed, scale_lengths=length_scale)
+    if name == "llama":
+        return workloads.llama(seed=seed)
+    if name == "fp8":
+        return workloads.fp8(seed=seed, scale_lengths=length_scale)
+    if name == "mixed":
+        return workloads.mixed(seed=seed, scale_lengths=length_scale)
+    if name == "tiny":
+        return workloads.tiny(seed=seed)
+    raise ValueError(name)
+
+
+BASE_SEEDS = {"agentic": 2, "llama": 1, "fp8": 4, "mixed": 3, "tiny": 0}
+
+
+def algorithmic_bytes(b) -> dict:
+    """Bytes the attention must move at least (per call), and the logical total."""
+    import workloads
+
+    kv_tok = 2 * b.num_kv_heads * b.head_size * workloads.ELEM_BYTES[b.kv_dtype]
+    qb = workloads.ELEM_BYTES[b.q_dtype]
+    q_out = 2 * b.total_q * b.num_q_heads * b.head_size * qb
+    tables = sum(-(-int(n) // b.block_size) for n in b.seq_lens) * 4 + 4 * b.num_seqs
+    logical = int(sum(int(n) for n in b.seq_lens)) * kv_tok
+    unique = unique_kv_tokens(b) * kv_tok
+    return {"kv_token_bytes": kv_tok, "logical_kv": logical, "unique_kv": unique,
+            "algorithmic": unique + q_out + tables, "logical_total": logical + q_out + tables}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) arm
+
+_CPU_SAMPLE = {}
+
+
+def _cpu_worker_init(shape):
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    name, seed, length, hq, hkv, d, bs, kv = shape
+    import torch
+
+    torch.set_num_threads(1)
+    import workloads
+
+    # one sequence with the workload's head shape, dtype and block size
+    _CPU_SAMPLE["b"] = workloads.build(name + "_cpu_sample", seed, [length], [1], hq, hkv, d, bs, kv)
+
+
+def _cpu_worker_run(_):
+    import oracle
+
+    b = _CPU_SAMPLE["b"]
+    t0 = time.time()
+    oracle.paged_decode(b.q, b.q_dtype, b.k_cache, b.v_cache, b.kv_dtype, b.block_tables, b.seq_lens,
+                        b.block_size, b.scale, b.k_scale, b.v_scale)
+    t1 = time.time()
+    return t0, t1, int(b.seq_lens[0])
+
+
+class OracleSampler:
+    """The fp64 oracle timed on host cores: W worker processes (spawned, one BLAS
+    thread each), each running the oracle on one decode sequence with the
+    workload's head shape, dtype and block size (the median length, or its first
+    tokens when a time budget is given).  Rate = attended tokens / wall time."""
+
+    # oracle cost measured on one x86 core: about 3.3e5 (context token x query head)
+    # per second; sizes a sample to a time budget
+    TOKEN_HEADS_PER_CORE_SECOND = 3.3e5
+
+    def __init__(self, b, workers: int, budget_s: float | None = None):
+        self.b = b
+        self.workers = workers
+        L = int(sorted(b.seq_lens)[len(b.seq_lens) // 2])  # median-length sequence
+        self.full_length = L
+        if budget_s is not None:
+            L = min(L, max(256, int(self.TOKEN_HEADS_PER_CORE_SECOND / b.num_q_heads * budget_s)))
+        self.length = L
+        shape = (b.name, 11, L, b.num_q_heads, b.num_kv_heads, b.head_size, b.block_size, b.kv_dtype)
+        ctx = mp.get_context("spawn")
+        env_keep = os.environ.get("OPENBLAS_NUM_THREADS")
+        os.environ["OPENBLAS_NUM_THREADS"] = "1"
+        os.environ["OMP_NUM_THREADS"] = "1"
+        self.pool = ctx.Pool(workers, initializer=_cpu_worker_init, initargs=(shape,))
+        if env_keep is None:
+            os.environ.pop("OPENBLAS_NUM_THREADS", None)
+
+    def step(self):
+        res = self.pool.map(_cpu_worker_run, range(self.workers), chunksize=1)
+        t0 = min(r[0] for r in res)
+        t1 = max(r[1] for r in res)
+        tokens = sum(r[2] for r in res)
+        wall = t1 - t0
+        return tokens / wall, wall
+
+    def describe(self):
+        which = ("the batch's median length" if self.length == self.full_length else
+                 f"the first {self.length} tokens of a median-length ({self.full_length}) sequence")
+        return (f"{self.workers} processes x 1 decode sequence of {self.length} tokens ({which}), "
+                f"{self.b.num_q_heads}/{self.b.num_kv_heads} heads, head {self.b.head_size}, "
+                f"{self.b.kv_dtype}, block {self.b.block_size}, per step")
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def cpu_workers():
+    n = os.cpu_count() or 1
+    return max(1, min(8, n))
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    b = make_workload(args.workload, BASE_SEEDS[args.workload])
+    # whole run (warm-up + timed steps) sized to about two minutes of oracle time
+    sampler = OracleSampler(b, cpu_workers(), budget_s=120.0 / (args.steps + args.warmup))
+    for _ in range(args.warmup):
+        sampler.step()
+    rates, walls = [], []
+    for _ in range(args.steps):
+        r, w = sampler.step()
+        rates.append(r)
+        walls.append(w)
+    sampler.close()
+    value = statistics.median(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * statistics.median(walls),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(b, args),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": sampler.workers, "kind": "oracle",
+                         "sample": sampler.describe()},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(b, args):
+    return {"workload": b.name, "num_seqs": b.num_seqs, "total_context_tokens": int(sum(int(n) for n in b.seq_lens)),
+            "max_seq_len": b.max_seq_len, "num_q_heads": b.num_q_heads, "num_kv_heads": b.num_kv_heads,
+            "head_size": b.head_size, "block_size": b.block_size, "kv_dtype": b.kv_dtype,
+            "q_dtype": b.q_dtype, "new_tokens_per_step": b.total_q,
+            "partition_size": args.partition_size or "auto",
+            "length_scale": args.length_scale,
+            "l2": "inputs larger than L2 (KV working set >> 129 MB)" if b.name != "tiny" else "tiny (fits L2)"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    import paged_kv_cache_pagedattention_gb300 as pa
+    import workloads
+
+    b = make_workload(args.workload, rank_seed(BASE_SEEDS[args.workload], rank), args.length_scale)
+    varlen = b.max_query_len > 1
+    kc, vc = workloads.device_cache(b, dev)
+    T = workloads.bits_to_torch
+    key, val = T(b.key, b.src_dtype, dev), T(b.value, b.src_dtype, dev)
+    slots = torch.from_numpy(b.slot_mapping).to(dev)
+    q = T(b.q, b.q_dtype, dev)
+    tables = torch.from_numpy(b.block_tables).to(dev)
+    lens = torch.from_numpy(b.seq_lens).to(dev)
+    qsl = torch.from_numpy(b.query_start_loc).to(dev)
+    fp8 = b.kv_dtype == "fp8_e4m3"
+    ks = torch.tensor([b.k_scale], dtype=torch.float32, device=dev) if fp8 else None
+    vs = torch.tensor([b.v_scale], dtype=torch.float32, device=dev) if fp8 else None
+    out = torch.empty_like(q)
+    part = args.partition_size
+    if varlen:
+        wsb = pa.pa_varlen_workspace_size(b.num_seqs, b.total_q, b.max_query_len, b.num_q_heads, b.num_kv_heads,
+                                          b.head_size, b.max_seq_len, b.block_size, part)
+    else:
+        wsb = pa.pa_decode_workspace_size(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_size, b.max_seq_len,
+                                          b.block_size, part)
+    ws = pa.workspace_tensor(wsb, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(q_=q, key_=key, value_=val, slots_=slots, tables_=tables, lens_=lens, qsl_=qsl, out_=out):
+        pa.pa_reshape_and_cache(key_, value_, kc, vc, slots_, ks, vs, stream)
+        if varlen:
+            pa.pa_varlen_attn(out_, q_, kc, vc, tables_, qsl_, lens_, b.max_query_len, b.max_seq_len, b.scale, ws,
+                              True, ks, vs, part, stream)
+        else:
+            pa.pa_decode(out_, q_, kc, vc, tables_, lens_, b.max_seq_len, b.scale, ws, ks, vs, part, stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    flags = pa.pa_get_error_flags()
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x} during warm-up")
+
+    # ---- timed region: exactly K steps, CUDA events on the launching stream
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        pass
+    sampler = ClockSampler(bus) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    pa.pa_trace_read(0, reset=True)
+    pa.pa_trace_enable(True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    pa.pa_trace_enable(False)
+    ms_local = e0.elapsed_time(e1)
+    clocks = sampler.stop() if sampler else None
+    trace = {name: pa.pa_trace_read(k) for k, name in enumerate(pa.TRACE_KINDS)}
+    ms_total = max_over_ranks(ms_local, dev)
+    ms_per_step = ms_total / args.steps
+    ctx_tokens = int(sum(int(n) for n in b.seq_lens))
+    tok_s = ctx_tokens * world / (ms_per_step / 1000.0)
+    launches = sum(n for n, _ in trace.values())
+
+    # ---- roofline of the attention kernel (kind 1)
+    nbytes = algorithmic_bytes(b)
+    n_att, ms_att = trace["attention"]
+    att_ms = ms_att / max(n_att, 1)
+    achieved = nbytes["algorithmic"] / (att_ms / 1000.0) / 1e9
+    peak, peak_kind = measured_peaks()
+    traffic = profiled_traffic(args.workload)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic, "kernel": "decode_mma_kernel" if not varlen else "attention kernels",
+                "peak_source": f"{peak_kind} MEASURED_PEAKS.json hbm_gbs" if peak_kind == "measured" else "fallback",
+                "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                "algorithmic_bytes_per_launch": nbytes["algorithmic"],
+                "logical_kv_bytes_per_launch": nbytes["logical_kv"],
+                "logical_gbs": nbytes["logical_total"] / (att_ms / 1000.0) / 1e9,
+                "kernel_ms": att_ms}
+
+    # ---- end to end through the public API with host buffers (pinned), K steps
+    e2e = None
+    if not args.no_e2e:
+        hq_, hkey, hval, hslots, htab, hlens, hqsl = (t.cpu().pin_memory() for t in (q, key, val, slots, tables, lens, qsl))
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        dq, dkey, dval, dslots, dtab, dlens, dqsl = (torch.empty_like(t) for t in (q, key, val, slots, tables, lens, qsl))
+        h2d = sum(t.numel() * t.element_size() for t in (hq_, hkey, hval, hslots, htab, hlens) + ((hqsl,) if varlen else ()))
+        d2h = hout.numel() * hout.element_size()
+
+        def e2e_step():
+            for d_, h_ in ((dq, hq_), (dkey, hkey), (dval, hval), (dslots, hslots), (dtab, htab), (dlens, hlens)):
+                d_.copy_(h_, non_blocking=True)
+            if varlen:
+                dqsl.copy_(hqsl, non_blocking=True)
+            step(dq, dkey, dval, dslots, dtab, dlens, dqsl, out)
+            hout.copy_(out, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        barrier()
+        t0 = time.perf_counter()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        f1.record(stream)
+        barrier()
+        wall_ms = (time.perf_counter() - t0) * 1000.0
+        e2e_ms = max_over_ranks(max(f0.elapsed_time(f1), wall_ms), dev) / args.steps
+        e2e = {"value": ctx_tokens * world / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    flags = pa.pa_get_error_flags()
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x} during the timed region")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sampler_cpu = OracleSampler(b, cpu_workers(), budget_s=15.0)
+        rate, wall = sampler_cpu.step()
+        sampler_cpu.close()
+        cpu = {"value": rate, "unit": UNIT, "cores": sampler_cpu.workers, "kind": "oracle",
+               "sample": sampler_cpu.describe(), "wall_s": wall}
+
+    if world > 1:
+        dist.barrier()
+    if rank == 0:
+        line = {"metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16" if b.kv_dtype == "bf16" else b.kv_dtype,
+                "data": "synthetic (seeded N(0,1) values, seeded block placement)",
+                "config": workload_config(b, args),
+                "hbm_gbs": achieved, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches,
+                "launches_by_kernel": {k: v[0] for k, v in trace.items() if v[0]},
+                "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=WORKLOADS, default="agentic")
+    ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--length-scale", type=float, default=1.0,
+                    help="shrink every sequence length (profiling captures only; 1.0 = the named workload)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
