@@ -203,6 +203,9 @@ size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t total_q_tokens, int32_
  *                  q_len_r <= seq_lens[r] is required
  *   max_query_len, max_seq_len  host-side upper bounds (size the launch)
  *   causal         1: query at position p attends keys 0..p; 0: all seq_len keys
+ *   partition_size 0: defaults (single-token rows as pa_decode, rows of
+ *                  multi-token requests in partitions of >= 16384 tokens); > 0:
+ *                  that many tokens for every row
  *   the rest as pa_decode.  A request with q_len == 0 is skipped.
  * pa_decode equals pa_varlen_attn with q_len = 1 for every request.
  */

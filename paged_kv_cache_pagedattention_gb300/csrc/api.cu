@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <vector>
@@ -110,7 +111,7 @@ VarlenLayout varlen_layout(int num_seqs, int total_q, int hq, int hkv, int d, in
                            int requested) {
   VarlenLayout L;
   L.part = resolve_partition(requested, num_seqs, hkv, max_seq_len, bs);
-  L.part_pf = prefill_partition(L.part);
+  L.part_pf = requested > 0 ? L.part : prefill_partition(L.part);
   L.parts = ceil_div(max_seq_len, L.part);
   L.parts_pf = ceil_div(max_seq_len, L.part_pf);
   const int group = hq / (hkv > 0 ? hkv : 1);
@@ -144,22 +145,24 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// The cache seen as rows of 128 bytes: dim0 = one 128-byte row, dim1 = rows of all
-// heads of one block (Hkv x block_size x rows-per-token), dim2 = physical block.
-// One box is the (block, head) tile: block_size x rows-per-token rows, 128B swizzle.
+// The cache as a 4-D tensor: dim0 = 128 bytes of a token's row, dim1 = the tokens
+// of all heads of one block (Hkv x block_size, stride one row), dim2 = which
+// 128-byte piece of the row (stride 128 bytes), dim3 = physical block.  One box is
+// a whole (block, head) tile, {128 bytes, block_size, pieces, 1}; in shared memory
+// it lands piece-major ([piece][token][128 bytes]) with the 128-byte swizzle.
 bool encode_cache_map(CUtensorMap* m, const void* base, int kv_dtype, int num_blocks, int hkv, int bs, int d) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const int eb = dtype_bytes(kv_dtype);
   const int row_bytes = d * eb;
   if (row_bytes % 128) return false;
-  const int rpt = row_bytes / 128;
-  cuuint64_t dims[3] = {(cuuint64_t)(128 / eb), (cuuint64_t)hkv * bs * rpt, (cuuint64_t)num_blocks};
-  cuuint64_t strides[2] = {128, (cuuint64_t)hkv * bs * row_bytes};
-  cuuint32_t box[3] = {(cuuint32_t)(128 / eb), (cuuint32_t)(bs * rpt), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
+  const int pieces = row_bytes / 128;
+  cuuint64_t dims[4] = {(cuuint64_t)(128 / eb), (cuuint64_t)hkv * bs, (cuuint64_t)pieces, (cuuint64_t)num_blocks};
+  cuuint64_t strides[3] = {(cuuint64_t)row_bytes, 128, (cuuint64_t)hkv * bs * row_bytes};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / eb), (cuuint32_t)bs, (cuuint32_t)pieces, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType t = eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
-  return fn(m, t, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  return fn(m, t, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -251,6 +254,18 @@ pa_status check_attention_args(const void* out, const void* q, const void* k_cac
   return PA_OK;
 }
 
+// L2 prefetch distance (blocks beyond the shared-memory ring) of the tensor-core
+// kernels; PA_PREFETCH in the environment overrides the default (0 = off).
+int prefetch_distance() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("PA_PREFETCH");
+    v = e ? atoi(e) : 0;
+    if (v < 0) v = 0;
+  }
+  return v;
+}
+
 AttnParams base_params(void* out, const void* q, const void* k_cache, const void* v_cache, int32_t num_blocks,
                        const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
                        int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
@@ -278,6 +293,7 @@ AttnParams base_params(void* out, const void* q, const void* k_cache, const void
   p.num_head_groups = (p.group + 7) / 8;
   p.max_seq_len = max_seq_len;
   p.causal = 1;
+  p.prefetch = prefetch_distance();
   p.scale = scale;
   return p;
 }
@@ -480,7 +496,7 @@ pa_status pa_varlen_attn(void* out, const void* q, const void* k_cache, const vo
     if (e != cudaSuccess) return PA_ERR_CUDA;
     if (multi && fast_prefill) {
       TraceScope t(4, s);
-      e = pa::launch_prefill_mma(p, q_dtype, kv_dtype, 2 * sm_count(), &tk, &tv, s);
+      e = pa::launch_prefill_mma(p, q_dtype, kv_dtype, static_cast<int>(L.max_work), &tk, &tv, s);
     } else if (multi) {
       TraceScope t(1, s);
       e = pa::launch_attn_generic(p, q_dtype, kv_dtype, static_cast<int>(L.parts_pf), 1, s);

@@ -9,10 +9,12 @@
 // Data movement.  Each (physical block, KV head) tile of K or V is contiguous in
 // HBM (block_size x head_size elements).  Each warp owns a private ring of stages;
 // its lane 0 issues one TMA bulk-tensor copy per tile (K and V) into the ring and
-// the warp waits on the stage's mbarrier.  The tensor map views the cache as rows
-// of 128 bytes and uses the 128-byte swizzle, so the ldmatrix / 16-byte shared
-// loads below are free of bank conflicts.  A stage is refilled as soon as its warp
-// has consumed it, keeping ring_depth tiles per warp in flight.
+// the warp waits on the stage's mbarrier.  The 4-D tensor map lands a tile in
+// shared memory as head_size*elem/128 sub-tiles of [block_size tokens][128 bytes]
+// with the 128-byte swizzle, so eight consecutive tokens of one 16-byte column sit
+// in eight different bank groups: the ldmatrix / 16-byte shared loads below are
+// free of bank conflicts.  A stage is refilled as soon as its warp has consumed it;
+// optionally the same lane also asks TMA to prefetch blocks further ahead into L2.
 //
 // Math.  The query heads that share a KV head are the N = 8 columns of a warp MMA
 // m16n8k16 (grouped-query reuse: every K/V element loaded serves all of them):
@@ -42,13 +44,18 @@ struct DecodeGeom {
   static constexpr bool kFp8 = KVDT == PA_FP8_E4M3;
   static constexpr int kElemBytes = kFp8 ? 1 : 2;
   static constexpr int kRowBytes = HEAD * kElemBytes;  // one token of one head
-  static constexpr int kRowsPerToken = kRowBytes / 128;
   static constexpr int kTileBytes = BS * kRowBytes;
   static constexpr int kMTiles = BS / 16;
   static constexpr int kKSteps = HEAD / 16;
   static constexpr int kDTiles = HEAD / 16;
   static constexpr int kStages = kTileBytes <= 4096 ? 3 : 2;
+  static constexpr int kSub = kRowBytes / 128;           // 128-byte sub-tiles per tile
+  static constexpr int kSubElems = 128 / kElemBytes;     // elements per sub-tile row
   static_assert(kRowBytes % 128 == 0, "token rows must be whole 128-byte rows");
+  // byte offset of 16-byte chunk `chunk` of token `tok` inside a tile
+  static __device__ __forceinline__ uint32_t off(int tok, int chunk) {
+    return static_cast<uint32_t>((chunk >> 3) * BS * 128) + swz128(tok, chunk & 7);
+  }
 };
 
 template <int KVDT, int HEAD, int BS, int NW>
@@ -120,8 +127,16 @@ __global__ void __launch_bounds__(NW * 32)
   const int nmine = (b1 - b0 > warp) ? (b1 - b0 - warp + NW - 1) / NW : 0;
   uint8_t* ring = smem + warp * ST * 2 * TB;
   uint64_t* wbars = bars + warp * ST;
-  const int tile_row0 = kvh * BS * G::kRowsPerToken;
+  const int tile_row0 = kvh * BS;
 
+  const int pf_dist = p.prefetch > 0 ? ST + p.prefetch : 0;
+  auto prefetch = [&](int i) {
+    const int phys = table[b0 + warp + i * NW];
+    if (phys >= 0 && phys < p.num_blocks) {
+      tma_prefetch_l2_4d(&tmk, 0, tile_row0, 0, phys);
+      tma_prefetch_l2_4d(&tmv, 0, tile_row0, 0, phys);
+    }
+  };
   auto issue = [&](int i) {
     const int jb = b0 + warp + i * NW;
     const int phys = table[jb];
@@ -132,12 +147,15 @@ __global__ void __launch_bounds__(NW * 32)
     } else {
       uint8_t* st = ring + (i % ST) * 2 * TB;
       mbar_arrive_expect_tx(bar, 2 * TB);
-      tma_load_3d(st, &tmk, 0, tile_row0, phys, bar);
-      tma_load_3d(st + TB, &tmv, 0, tile_row0, phys, bar);
+      tma_load_4d(st, &tmk, 0, tile_row0, 0, phys, bar);
+      tma_load_4d(st + TB, &tmv, 0, tile_row0, 0, phys, bar);
     }
+    if (pf_dist && i + pf_dist < nmine) prefetch(i + pf_dist);
   };
-  if (lane == 0)
+  if (lane == 0) {
+    for (int i = ST; i < min(pf_dist, nmine); ++i) prefetch(i);
     for (int i = 0; i < min(ST, nmine); ++i) issue(i);
+  }
 
   // ---- query fragments (B operand: k = head dim, n = query head of the group)
   const int qn = lane >> 2, qq = lane & 3;  // B-fragment column / k-pair index
@@ -209,6 +227,7 @@ __global__ void __launch_bounds__(NW * 32)
       float sc[G::kMTiles][4];
 #pragma unroll
       for (int mt = 0; mt < G::kMTiles; ++mt) {
+        float sc2[4] = {0.f, 0.f, 0.f, 0.f};  // second, independent accumulation chain
         sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
         if constexpr (!kFp8) {
 #pragma unroll
@@ -216,8 +235,9 @@ __global__ void __launch_bounds__(NW * 32)
             const int tok = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
             const int chunk = 2 * ks + (lane >> 4);
             uint32_t a0, a1, a2, a3;
-            ldsm_x4(kbase + swz128(tok * G::kRowsPerToken + (chunk >> 3), chunk & 7), a0, a1, a2, a3);
-            mma_16816<MDT>(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+            ldsm_x4(kbase + G::off(tok, chunk), a0, a1, a2, a3);
+            if (ks & 1) mma_16816<MDT>(sc2, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+            else mma_16816<MDT>(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
           }
         } else {
           const int tA = 16 * mt + (lane >> 2), tB = tA + 8;
@@ -233,9 +253,12 @@ __global__ void __launch_bounds__(NW * 32)
             const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(wa[ks] >> 16));
             const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(wb[ks] & 0xffffu));
             const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(wb[ks] >> 16));
-            mma_16816<PA_F16>(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+            if (ks & 1) mma_16816<PA_F16>(sc2, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+            else mma_16816<PA_F16>(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
           }
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[mt][e] += sc2[e];
       }
 
       // ---- online softmax on the accumulators (columns 2qq, 2qq+1 = heads A, B)
@@ -294,7 +317,7 @@ __global__ void __launch_bounds__(NW * 32)
             const int tok = 16 * kt + (lane & 7) + 8 * (lane >> 4);
             const int chunk = 2 * dt + ((lane >> 3) & 1);
             uint32_t a0, a1, a2, a3;
-            ldsm_x4_trans(vbase + swz128(tok * G::kRowsPerToken + (chunk >> 3), chunk & 7), a0, a1, a2, a3);
+            ldsm_x4_trans(vbase + G::off(tok, chunk), a0, a1, a2, a3);
             if (tail) {
               a0 &= m01;
               a1 &= m01;

@@ -109,38 +109,75 @@ __global__ void __launch_bounds__(128)
   }
 }
 
-// One warp per (row, head): out = sum_j acc_j * 2^(m_j - M) / sum_j l_j * 2^(m_j - M).
+// One CTA per (row, head): out = sum_j acc_j * 2^(m_j - M) / sum_j l_j * 2^(m_j - M)
+// with M = max_j m_j.  The per-partition factors are computed once into shared
+// memory; then each thread owns output dimensions and streams the partials with
+// independent, coalesced loads.
+constexpr int kMergeThreads = 128;
+constexpr int kMergeChunk = 512;
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
+  v = is_max ? warp_max_xor(v, 1, 16) : warp_sum_xor(v, 1, 16);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+  __syncthreads();
+  return r;
+}
+
 template <int QDT>
-__global__ void __launch_bounds__(128) merge_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnParams p) {
   using QE = Elem<QDT>;
-  const int lane = threadIdx.x & 31;
-  const long long gw = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (gw >= (long long)p.num_rows * p.num_q_heads || plan_rejected(p)) return;
-  const int row = static_cast<int>(gw / p.num_q_heads);
-  const int head = static_cast<int>(gw % p.num_q_heads);
+  __shared__ float wts[kMergeChunk];
+  __shared__ float red[kMergeThreads / 32];
+  const long long gid = blockIdx.x;
+  const int row = static_cast<int>(gid / p.num_q_heads);
+  const int head = static_cast<int>(gid % p.num_q_heads);
+  if (row >= p.num_rows || plan_rejected(p)) return;
   const RowInfo ri = row_info(p, row);
   if (!ri.ok || ri.parts_row <= 1) return;
   const long long base = row_partial_base(p, ri, row);
   const int np = ri.parts_row;
+  const int hq = p.num_q_heads, d = p.head_size;
   float M = -INFINITY;
-  for (int j = lane; j < np; j += 32) M = fmaxf(M, p.ws_ml[(base + j) * p.num_q_heads + head].x);
-  M = warp_max_xor(M, 1, 16);
+  for (int j = threadIdx.x; j < np; j += blockDim.x) {
+    const float2 ml = p.ws_ml[(base + j) * hq + head];
+    if (ml.y > 0.f) M = fmaxf(M, ml.x);
+  }
+  M = block_reduce(M, true, red);
   float L = 0.f;
-  for (int j = lane; j < np; j += 32) {
-    const float2 ml = p.ws_ml[(base + j) * p.num_q_heads + head];
+  for (int j = threadIdx.x; j < np; j += blockDim.x) {
+    const float2 ml = p.ws_ml[(base + j) * hq + head];
     if (ml.y > 0.f) L += ml.y * exp2f(ml.x - M);
   }
-  L = warp_sum_xor(L, 1, 16);
+  L = block_reduce(L, false, red);
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  const int d = p.head_size;
-  typename QE::T* out = reinterpret_cast<typename QE::T*>(p.out) + ((long long)row * p.num_q_heads + head) * d;
-  for (int dd = lane; dd < d; dd += 32) {
-    float o = 0.f;
-    for (int j = 0; j < np; ++j) {
-      const float2 ml = p.ws_ml[(base + j) * p.num_q_heads + head];
-      if (ml.y > 0.f) o = fmaf(p.ws_acc[((base + j) * p.num_q_heads + head) * d + dd], exp2f(ml.x - M), o);
+  typename QE::T* out = reinterpret_cast<typename QE::T*>(p.out) + ((long long)row * hq + head) * d;
+  for (int d0 = 0; d0 < d; d0 += blockDim.x) {
+    const int dd = d0 + threadIdx.x;
+    float o0 = 0.f, o1 = 0.f;
+    for (int c0 = 0; c0 < np; c0 += kMergeChunk) {
+      const int n = min(kMergeChunk, np - c0);
+      __syncthreads();
+      for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        const float2 ml = p.ws_ml[(base + c0 + j) * hq + head];
+        wts[j] = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
+      }
+      __syncthreads();
+      if (dd < d) {
+        const float* src = p.ws_acc + ((base + c0) * hq + head) * d + dd;
+        const long long stride = (long long)hq * d;
+        int j = 0;
+        for (; j + 1 < n; j += 2) {
+          o0 = fmaf(src[j * stride], wts[j], o0);
+          o1 = fmaf(src[(j + 1) * stride], wts[j + 1], o1);
+        }
+        if (j < n) o0 = fmaf(src[j * stride], wts[j], o0);
+      }
     }
-    out[dd] = QE::from_float(o * inv);
+    if (dd < d) out[dd] = QE::from_float((o0 + o1) * inv);
   }
 }
 
@@ -248,8 +285,8 @@ cudaError_t launch_generic_t(const AttnParams& p, int grid_z, int only_multi, cu
 
 template <int QDT>
 cudaError_t launch_merge_t(const AttnParams& p, cudaStream_t s) {
-  const long long warps = (long long)p.num_rows * p.num_q_heads;
-  merge_kernel<QDT><<<(unsigned)((warps + 3) / 4), 128, 0, s>>>(p);
+  const long long ctas = (long long)p.num_rows * p.num_q_heads;
+  merge_kernel<QDT><<<(unsigned)ctas, kMergeThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -47,6 +47,7 @@ struct AttnParams {
   int part_pf;          // partition tokens for rows of multi-token requests
   int max_partitions;   // decode mode: partial rows reserved per query row
   int causal;
+  int prefetch;         // L2 prefetch distance of the tensor-core kernels, in blocks (0 = off)
   float scale;          // softmax scale
 };
 

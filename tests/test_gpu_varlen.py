@@ -44,6 +44,12 @@ VARLEN_CASES = [
     ("f16_bs32", "f16", 12, 4, 128, 32, [400, 33, 65], [100, 1, 65], 64, True),
     ("f32_generic", "f32", 8, 2, 64, 16, [200, 17, 64], [40, 1, 64], 48, True),
     ("fp8_mixed", "fp8_e4m3", 32, 8, 128, 32, [500, 64, 33], [70, 1, 33], 64, True),
+    ("prefill_g16_two_groups", "bf16", 32, 2, 128, 16, [300, 80], [150, 80], 64, True),
+    ("prefill_g3_padded", "bf16", 6, 2, 128, 32, [200, 45], [100, 45], 32, True),
+    ("prefill_g1_d64", "bf16", 4, 4, 64, 16, [130, 66], [70, 66], 0, True),
+    ("prefill_ragged_tiles", "bf16", 32, 8, 128, 16, [97, 33, 1000], [97, 31, 45], 48, True),
+    ("prefill_split_k_default", "bf16", 16, 4, 128, 16, [20000, 17000, 40], [100, 33, 1], 0, True),
+    ("non_causal_g8", "f16", 16, 2, 128, 16, [250, 90], [60, 90], 64, False),
 ]
 
 
