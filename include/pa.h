@@ -180,6 +180,42 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                     void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * Size of the fixed device array pa_decode_static_workspace uses as scratch:
+ * 32 MiB, held on every GPU that loads this library until the process exits.
+ */
+#define PA_STATIC_WORKSPACE_BYTES (32u << 20)
+
+/*
+ * pa_decode_static_workspace -- pa_decode without a caller-provided workspace.
+ * The serving pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory where attention runs: runtimes whose memory
+ * planner only provides the tensors it planned (inputs, outputs, KV cache) and no
+ * operator scratch, and plug-ins that must not call cudaMalloc or a caching
+ * allocator on the serving path (it can synchronise the device, or fail when the
+ * pool is exhausted).  The caller passes inputs and outputs only; the split-K
+ * partial states go to a file-scope device array of PA_STATIC_WORKSPACE_BYTES.
+ *
+ *   Arguments as pa_decode.  partition_size 0 picks the default partitioning,
+ *   coarsened (doubled) until the partial states fit the array; an explicit
+ *   partition_size is used as given.  If the partial states do not fit (many
+ *   sequences x heads), returns PA_ERR_WORKSPACE and launches nothing.
+ *   Allocates nothing: no cudaMalloc / cudaFree and no allocating library call.
+ *   The first call on a device looks up the array's device address (with that
+ *   device current); make that first call before any CUDA stream capture.
+ *   Every call on a device shares the one array and leaves its contents behind.
+ *   Nothing in it needs to start at zero (each call writes every partial it later
+ *   reads), but calls that overlap on the GPU -- on different streams, or from
+ *   different host threads -- race on it: serialise them.
+ */
+pa_status pa_decode_static_workspace(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                     int32_t num_blocks, const int32_t* block_tables,
+                                     int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                                     int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_size, int32_t block_size, float scale, pa_dtype q_dtype,
+                                     pa_dtype kv_dtype, const float* k_scale, const float* v_scale,
+                                     int32_t partition_size, pa_stream_t stream);
+
+/*
  * Bytes of workspace pa_varlen_attn needs (>= 256).  Same partition_size rule
  * as pa_decode_workspace_size.
  */

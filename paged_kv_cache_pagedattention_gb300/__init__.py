@@ -48,6 +48,8 @@ SIGNATURES = {
     "pa_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "pa_decode": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
                                  _I32, _F, ctypes.c_int, ctypes.c_int, _P, _P, _I32, _P, _SZ, _P]),
+    "pa_decode_static_workspace": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, _I32,
+                                                  _I32, _I32, _F, ctypes.c_int, ctypes.c_int, _P, _P, _I32, _P]),
     "pa_varlen_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "pa_varlen_attn": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
                                       _I32, _I32, _I32, _I32, _F, _I32, ctypes.c_int, ctypes.c_int,
@@ -148,6 +150,26 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, sca
                           float(scale), dtype_code(q), dtype_code(k_cache), _ptr(k_scale), _ptr(v_scale),
                           int(partition_size), _ptr(workspace), workspace.numel() * workspace.element_size(),
                           _stream(stream)), "pa_decode")
+
+
+def pa_decode_static_workspace(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, scale,
+                               k_scale=None, v_scale=None, partition_size=0, stream=None) -> None:
+    """pa_decode with the library's fixed scratch array instead of a workspace: for
+    callers that cannot allocate device memory where attention runs.  See pa.h."""
+    nb, hkv, bs, d = k_cache.shape
+    b, hq = q.shape[0], q.shape[1]
+    if q.dim() != 3 or q.shape[2] != d or out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("q/out must be [num_seqs][num_q_heads][head_size] of one dtype")
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or block_tables.shape[0] != b:
+        raise ValueError("block_tables must be int32 [num_seqs][max_blocks_per_seq]")
+    if seq_lens.dtype != torch.int32 or seq_lens.numel() != b:
+        raise ValueError("seq_lens must be int32 [num_seqs]")
+    _check(_lib.pa_decode_static_workspace(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), nb,
+                                           _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), b,
+                                           int(max_seq_len), hq, hkv, d, bs, float(scale), dtype_code(q),
+                                           dtype_code(k_cache), _ptr(k_scale), _ptr(v_scale),
+                                           int(partition_size), _stream(stream)),
+           "pa_decode_static_workspace")
 
 
 def pa_varlen_workspace_size(num_seqs, total_q_tokens, max_query_len, num_q_heads, num_kv_heads,
