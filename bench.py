@@ -187,10 +187,10 @@ def decode_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the attention kernel from the committed ncu summary,
-    if it was captured on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"decode_mma_kernel_{workload}.md")
+def profiled_traffic(workload: str, kernel: str = "decode_mma_kernel"):
+    """DRAM bytes per launch of a kernel from the committed ncu summary, if it was
+    captured on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -221,6 +221,45 @@ def make_workload(name: str, seed: int, length_scale: float = 1.0):
 
 
 BASE_SEEDS = {"agentic": 2, "llama": 1, "fp8": 4, "mixed": 3, "tiny": 0}
+
+
+def prefix_groups(b):
+    """Groups of consecutive sequences and the leading blocks they share (the
+    scheduler's knowledge of its forks): (group_start [G+1], shared_blocks [G]) or None."""
+    import numpy as np
+
+    if not b.families or all(len(f) == 1 for f in b.families):
+        return None
+    starts, shared = [0], []
+    for fam in b.families:
+        if fam != list(range(starts[-1], starts[-1] + len(fam))):
+            return None
+        n = min(int(b.seq_lens[i]) for i in fam)
+        common = n // b.block_size
+        for i in fam[1:]:
+            eq = b.block_tables[i, :common] == b.block_tables[fam[0], :common]
+            common = int(np.argmin(eq)) if not eq.all() else common
+        shared.append(common if len(fam) > 1 else 0)
+        starts.append(starts[-1] + len(fam))
+    return np.array(starts, np.int32), np.array(shared, np.int32)
+
+
+def shared_split_bytes(b, groups) -> dict:
+    """KV bytes read by the shared-prefix kernel (each group's prefix once) and by the
+    private-part decode kernel (each sequence's remaining tokens)."""
+    import workloads
+
+    kv_tok = 2 * b.num_kv_heads * b.head_size * workloads.ELEM_BYTES[b.kv_dtype]
+    starts, shared = groups
+    shared_tok, private_tok = 0, 0
+    for g in range(len(shared)):
+        mem = range(int(starts[g]), int(starts[g + 1]))
+        S = 0
+        if len(mem) > 1:
+            S = min([int(shared[g])] + [int(b.seq_lens[m]) // b.block_size for m in mem]) * b.block_size
+        shared_tok += S
+        private_tok += sum(int(b.seq_lens[m]) - S for m in mem)
+    return {"shared": shared_tok * kv_tok, "private": private_tok * kv_tok}
 
 
 def algorithmic_bytes(b) -> dict:
@@ -352,6 +391,8 @@ def workload_config(b, args):
             "head_size": b.head_size, "block_size": b.block_size, "kv_dtype": b.kv_dtype,
             "q_dtype": b.q_dtype, "new_tokens_per_step": b.total_q,
             "partition_size": args.partition_size or "auto",
+            "decode_api": ("pa_varlen_attn" if b.max_query_len > 1 else
+                           "pa_decode" if (args.no_shared_prefix or not b.families) else "pa_decode_shared_prefix"),
             "length_scale": args.length_scale,
             "l2": "inputs larger than L2 (KV working set >> 129 MB)" if b.name != "tiny" else "tiny (fits L2)"}
 
@@ -392,6 +433,13 @@ def run_ours(args):
     else:
         wsb = pa.pa_decode_workspace_size(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_size, b.max_seq_len,
                                           b.block_size, part)
+    groups = None if (varlen or args.no_shared_prefix) else prefix_groups(b)
+    if groups is not None:
+        wsb = pa.pa_decode_shared_prefix_workspace_size(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_size,
+                                                        b.max_seq_len, b.block_size, part)
+        gstart = torch.from_numpy(groups[0]).to(dev)
+        gshared = torch.from_numpy(groups[1]).to(dev)
+        max_group = int(max(groups[0][1:] - groups[0][:-1]))
     ws = pa.workspace_tensor(wsb, dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -400,6 +448,9 @@ def run_ours(args):
         if varlen:
             pa.pa_varlen_attn(out_, q_, kc, vc, tables_, qsl_, lens_, b.max_query_len, b.max_seq_len, b.scale, ws,
                               True, ks, vs, part, stream)
+        elif groups is not None:
+            pa.pa_decode_shared_prefix(out_, q_, kc, vc, tables_, lens_, b.max_seq_len, b.scale, ws, gstart,
+                                       gshared, max_group, ks, vs, part, stream)
         else:
             pa.pa_decode(out_, q_, kc, vc, tables_, lens_, b.max_seq_len, b.scale, ws, ks, vs, part, stream)
 
@@ -449,7 +500,29 @@ def run_ours(args):
     att_ms = ms_att / max(n_att, 1)
     peak, peak_kind = measured_peaks()
     kernel_ms = {k: (v[1] / v[0] if v[0] else 0.0) for k, v in trace.items()}
-    if not varlen:
+    if groups is not None:
+        sb = shared_split_bytes(b, groups)
+        extra = nbytes["algorithmic"] - nbytes["unique_kv"]  # q, out, block tables
+        sh_ms, pr_ms, mg_ms = kernel_ms.get("shared_prefix", 0.0), att_ms, kernel_ms.get("merge", 0.0)
+        sh_line = {"bound": "hbm", "kernel": "shared_prefix_kernel", "kernel_ms": sh_ms,
+                   "algorithmic_bytes_per_launch": sb["shared"],
+                   "achieved": sb["shared"] / (sh_ms / 1000.0) / 1e9 if sh_ms else 0.0,
+                   "traffic": profiled_traffic(args.workload, "shared_prefix_kernel")}
+        pr_line = {"bound": "hbm", "kernel": "decode_mma_kernel (private remainders)", "kernel_ms": pr_ms,
+                   "algorithmic_bytes_per_launch": sb["private"] + extra,
+                   "achieved": (sb["private"] + extra) / (pr_ms / 1000.0) / 1e9 if pr_ms else 0.0,
+                   "traffic": None}
+        for ln in (sh_line, pr_line):
+            ln.update(peak=peak, unit="GB/s", frac=ln["achieved"] / peak,
+                      peak_source=f"{peak_kind} MEASURED_PEAKS.json hbm_gbs")
+        dom, other = (sh_line, pr_line) if sh_ms >= pr_ms else (pr_line, sh_line)
+        total_ms = sh_ms + pr_ms + mg_ms
+        achieved = dom["achieved"]
+        roofline = dict(dom, secondary=other, frac_of_nominal_8tbs=achieved / NOMINAL_HBM_GBS,
+                        attention_ms=total_ms,
+                        attention_unique_gbs=nbytes["algorithmic"] / (total_ms / 1000.0) / 1e9,
+                        attention_logical_gbs=nbytes["logical_total"] / (total_ms / 1000.0) / 1e9)
+    elif not varlen:
         achieved = nbytes["algorithmic"] / (att_ms / 1000.0) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                     "traffic": profiled_traffic(args.workload), "kernel": "decode_mma_kernel",
@@ -483,6 +556,9 @@ def run_ours(args):
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         dq, dkey, dval, dslots, dtab, dlens, dqsl = (torch.empty_like(t) for t in (q, key, val, slots, tables, lens, qsl))
         h2d = sum(t.numel() * t.element_size() for t in (hq_, hkey, hval, hslots, htab, hlens) + ((hqsl,) if varlen else ()))
+        if groups is not None:
+            hgs, hgb = gstart.cpu().pin_memory(), gshared.cpu().pin_memory()
+            h2d += hgs.numel() * 4 + hgb.numel() * 4
         d2h = hout.numel() * hout.element_size()
 
         def e2e_step():
@@ -490,6 +566,9 @@ def run_ours(args):
                 d_.copy_(h_, non_blocking=True)
             if varlen:
                 dqsl.copy_(hqsl, non_blocking=True)
+            if groups is not None:
+                gstart.copy_(hgs, non_blocking=True)
+                gshared.copy_(hgb, non_blocking=True)
             step(dq, dkey, dval, dslots, dtab, dlens, dqsl, out)
             hout.copy_(out, non_blocking=True)
 
@@ -549,6 +628,8 @@ def main(argv=None):
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-shared-prefix", action="store_true",
+                    help="agentic: call pa_decode instead of pa_decode_shared_prefix")
     ap.add_argument("--length-scale", type=float, default=1.0,
                     help="shrink every sequence length (profiling captures only; 1.0 = the named workload)")
     args = ap.parse_args(argv)

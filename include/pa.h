@@ -180,6 +180,48 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                     void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * Bytes of workspace pa_decode_shared_prefix needs (>= 256); partition_size as
+ * for pa_decode_workspace_size.
+ */
+size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                              int32_t head_size, int32_t max_seq_len, int32_t block_size,
+                                              int32_t partition_size);
+
+/*
+ * pa_decode_shared_prefix -- pa_decode for batches whose sequences share prefix
+ * blocks.  [AGENTIC] "統一分頁 + 共用池": sequences that share a prefix (forked
+ * subagents, parallel samples) point at the same physical blocks through reference
+ * counts.  Same result as pa_decode; each shared (block, KV head) tile is read once
+ * per group and applied to every member's query heads, then each member's
+ * remaining (private) tokens are attended as in pa_decode and the two partial
+ * states are merged.
+ *
+ *   group_start        device int32 [num_groups + 1], non-decreasing, [0] = 0,
+ *                      [num_groups] = num_seqs: group g is the run of consecutive
+ *                      sequences group_start[g] .. group_start[g+1]-1
+ *   group_shared_blocks device int32 [num_groups]: the first that-many block-table
+ *                      entries are identical for every member of group g (clamped
+ *                      to the full blocks of the group's shortest member)
+ *   num_groups         number of groups (0: plain pa_decode)
+ *   max_group_size     host bound on the members of any group, 1..8; groups larger
+ *                      than the bound share nothing (still correct)
+ *   the rest as pa_decode; workspace >= pa_decode_shared_prefix_workspace_size(...).
+ * A member whose table disagrees with the group's first sequence on a block it is
+ * declared to share sets PA_ERRFLAG_BLOCK_TABLE and that block is skipped for the
+ * whole group.  Without a tensor-core path for the dtypes/shape (or with no groups)
+ * this is exactly pa_decode (with a workspace of the size above).
+ */
+pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                  int32_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                  int32_t block_size, float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
+                                  const float* k_scale, const float* v_scale, const int32_t* group_start,
+                                  const int32_t* group_shared_blocks, int32_t num_groups,
+                                  int32_t max_group_size, int32_t partition_size, void* workspace,
+                                  size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * Size of the fixed device array pa_decode_static_workspace uses as scratch:
  * 32 MiB, held on every GPU that loads this library until the process exits.
  */

@@ -35,7 +35,7 @@ PA_ERRFLAG_BLOCK_TABLE, PA_ERRFLAG_SLOT, PA_ERRFLAG_SEQ_LEN, PA_ERRFLAG_QUERY, P
     0x1, 0x2, 0x4, 0x8, 0x10
 
 # Names of the kernel kinds reported by pa_trace_read.
-TRACE_KINDS = ("reshape_and_cache", "attention", "merge", "varlen_plan", "prefill_tiles")
+TRACE_KINDS = ("reshape_and_cache", "attention", "merge", "varlen_plan", "prefill_tiles", "shared_prefix")
 
 # Every symbol include/pa.h declares, with its ctypes signature.
 _P, _I32, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
@@ -48,6 +48,10 @@ SIGNATURES = {
     "pa_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "pa_decode": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
                                  _I32, _F, ctypes.c_int, ctypes.c_int, _P, _P, _I32, _P, _SZ, _P]),
+    "pa_decode_shared_prefix_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
+    "pa_decode_shared_prefix": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
+                                               _I32, _F, ctypes.c_int, ctypes.c_int, _P, _P, _P, _P, _I32,
+                                               _I32, _I32, _P, _SZ, _P]),
     "pa_decode_static_workspace": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, _I32,
                                                   _I32, _I32, _F, ctypes.c_int, ctypes.c_int, _P, _P, _I32, _P]),
     "pa_varlen_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32]),
@@ -150,6 +154,36 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, sca
                           float(scale), dtype_code(q), dtype_code(k_cache), _ptr(k_scale), _ptr(v_scale),
                           int(partition_size), _ptr(workspace), workspace.numel() * workspace.element_size(),
                           _stream(stream)), "pa_decode")
+
+
+def pa_decode_shared_prefix_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size, max_seq_len,
+                                           block_size, partition_size=0) -> int:
+    return _lib.pa_decode_shared_prefix_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size,
+                                                       max_seq_len, block_size, partition_size)
+
+
+def pa_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, scale, workspace,
+                            group_start, group_shared_blocks, max_group_size, k_scale=None, v_scale=None,
+                            partition_size=0, stream=None) -> None:
+    """pa_decode where groups of consecutive sequences share leading blocks.
+
+    group_start int32 [G+1] (device), group_shared_blocks int32 [G] (device)."""
+    nb, hkv, bs, d = k_cache.shape
+    b, hq = q.shape[0], q.shape[1]
+    if q.dim() != 3 or q.shape[2] != d or out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("q/out must be [num_seqs][num_q_heads][head_size] of one dtype")
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or block_tables.shape[0] != b:
+        raise ValueError("block_tables must be int32 [num_seqs][max_blocks_per_seq]")
+    if group_start.dtype != torch.int32 or group_shared_blocks.dtype != torch.int32 or \
+            group_start.numel() != group_shared_blocks.numel() + 1:
+        raise ValueError("group_start int32 [G+1], group_shared_blocks int32 [G]")
+    _check(_lib.pa_decode_shared_prefix(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables),
+                                        block_tables.shape[1], _ptr(seq_lens), b, int(max_seq_len), hq, hkv, d,
+                                        bs, float(scale), dtype_code(q), dtype_code(k_cache), _ptr(k_scale),
+                                        _ptr(v_scale), _ptr(group_start), _ptr(group_shared_blocks),
+                                        group_shared_blocks.numel(), int(max_group_size), int(partition_size),
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream)), "pa_decode_shared_prefix")
 
 
 def pa_decode_static_workspace(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, scale,

@@ -169,7 +169,7 @@ bool encode_cache_map(CUtensorMap* m, const void* base, int kv_dtype, int num_bl
 
 // ------------------------------------------------------------------ tracing
 
-constexpr int kTraceKinds = 5;
+constexpr int kTraceKinds = 6;
 bool g_trace_on = false;
 struct TraceSlot {
   int kind;
@@ -411,6 +411,82 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
     e = pa::launch_merge(p, q_dtype, s);
   }
   return cuda_status(e);
+}
+
+size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                              int32_t head_size, int32_t max_seq_len, int32_t block_size,
+                                              int32_t partition_size) {
+  if (num_seqs < 1 || num_q_heads < 1 || head_size < 1 || max_seq_len < 1 || block_size < 1) return 256;
+  DecodeLayout L = decode_layout(num_seqs, num_q_heads, head_size, max_seq_len, block_size, num_kv_heads,
+                                 partition_size);
+  // one more partition per row: the shared prefix and the private rest both round up
+  const size_t rows = (size_t)num_seqs * (size_t)(L.parts + 1);
+  return 256 + align256(rows * num_q_heads * sizeof(float2)) +
+         align256(rows * num_q_heads * (size_t)head_size * sizeof(float));
+}
+
+pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                  int32_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                  int32_t block_size, float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
+                                  const float* k_scale, const float* v_scale, const int32_t* group_start,
+                                  const int32_t* group_shared_blocks, int32_t num_groups,
+                                  int32_t max_group_size, int32_t partition_size, void* workspace,
+                                  size_t workspace_bytes, pa_stream_t stream) {
+  if (num_seqs < 0 || num_groups < 0) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  pa_status st = check_attention_args(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
+                                      seq_lens, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size,
+                                      q_dtype, kv_dtype, k_scale, v_scale, partition_size, workspace);
+  if (st != PA_OK) return st;
+  if (num_groups > 0 && (!group_start || !group_shared_blocks)) return PA_ERR_INVALID_ARG;
+  if (max_group_size < 1 || max_group_size > 8) return PA_ERR_UNSUPPORTED;
+  const bool fast = pa::decode_mma_supported(q_dtype, kv_dtype, head_size, block_size,
+                                             num_q_heads / num_kv_heads);
+  if (!fast || num_groups == 0 || max_group_size < 2)  // nothing to share, or no tensor-core path
+    return pa_decode(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
+                     num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, scale, q_dtype,
+                     kv_dtype, k_scale, v_scale, partition_size, workspace, workspace_bytes, stream);
+  const DecodeLayout L =
+      decode_layout(num_seqs, num_q_heads, head_size, max_seq_len, block_size, num_kv_heads, partition_size);
+  const size_t rows = (size_t)num_seqs * (size_t)(L.parts + 1);
+  const size_t ml_off = 256, acc_off = ml_off + align256(rows * num_q_heads * sizeof(float2));
+  if (workspace_bytes < acc_off + align256(rows * num_q_heads * (size_t)head_size * sizeof(float)))
+    return PA_ERR_WORKSPACE;
+  AttnParams p = base_params(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
+                             num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, scale,
+                             k_scale, v_scale);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.num_rows = num_seqs;
+  p.max_query_len = 1;
+  p.part = p.part_pf = L.part;
+  p.max_partitions = static_cast<int>(L.parts + 1);
+  p.ws_ml = reinterpret_cast<float2*>(ws + ml_off);
+  p.ws_acc = reinterpret_cast<float*>(ws + acc_off);
+  p.group_start = group_start;
+  p.group_shared_blocks = group_shared_blocks;
+  p.num_groups = num_groups;
+  p.max_group_size = max_group_size;
+  p.force_partials = 1;
+  CUtensorMap tk, tv;
+  if (!encode_cache_map(&tk, k_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size) ||
+      !encode_cache_map(&tv, v_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size))
+    return PA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  {
+    TraceScope t(5, s);
+    e = pa::launch_shared_prefix(p, q_dtype, kv_dtype, static_cast<int>(L.parts), &tk, &tv, s);
+  }
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  {
+    TraceScope t(1, s);
+    e = pa::launch_decode_mma(p, q_dtype, kv_dtype, static_cast<int>(L.parts), &tk, &tv, s);
+  }
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  TraceScope t(2, s);
+  return cuda_status(pa::launch_merge(p, q_dtype, s));
 }
 
 size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t total_q_tokens, int32_t max_query_len,

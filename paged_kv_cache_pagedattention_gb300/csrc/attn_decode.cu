@@ -1,20 +1,28 @@
 // PagedAttention decode on tensor cores.
 //
-// One CTA handles (request, KV head, head group of <= 8 query heads, partition of
-// the context).  [NOTES] "Decode": the single new query token of a request reads
-// every cached K/V of that request; [LINEAGE] "PagedAttention": K/V are read through
-// the block table; the partitions' partial softmax states are merged afterwards by
-// the rescale-and-add rule of [AGENTIC] "Online softmax".
+// decode_mma_kernel: one CTA handles (request, KV head, head group of <= 8 query
+// heads, partition of the context).  [NOTES] "Decode": the single new query token
+// of a request reads every cached K/V of that request; [LINEAGE] "PagedAttention":
+// K/V are read through the block table; the partitions' partial softmax states are
+// merged afterwards by the rescale-and-add rule of [AGENTIC] "Online softmax".
+//
+// shared_prefix_kernel: one CTA handles (group of sequences whose block tables
+// share leading entries, KV head, head group, partition of the shared prefix).
+// [AGENTIC] "統一分頁 + 共用池": forked requests point at the same physical blocks;
+// here each shared (block, head) tile is loaded once and one warp per member
+// applies that member's query heads to it.  The members' private remainders run in
+// decode_mma_kernel from their first private token, and the merge combines both.
 //
 // Data movement.  Each (physical block, KV head) tile of K or V is contiguous in
-// HBM (block_size x head_size elements).  Each warp owns a private ring of stages;
-// its lane 0 issues one TMA bulk-tensor copy per tile (K and V) into the ring and
-// the warp waits on the stage's mbarrier.  The 4-D tensor map lands a tile in
-// shared memory as head_size*elem/128 sub-tiles of [block_size tokens][128 bytes]
-// with the 128-byte swizzle, so eight consecutive tokens of one 16-byte column sit
-// in eight different bank groups: the ldmatrix / 16-byte shared loads below are
-// free of bank conflicts.  A stage is refilled as soon as its warp has consumed it;
-// optionally the same lane also asks TMA to prefetch blocks further ahead into L2.
+// HBM (block_size x head_size elements).  TMA bulk-tensor copies land a tile in
+// shared memory through a 4-D tensor map as head_size*elem/128 pieces of
+// [block_size tokens][128 bytes] with the 128-byte swizzle, so eight consecutive
+// tokens of one 16-byte column sit in eight different bank groups: the ldmatrix /
+// 16-byte shared loads below are free of bank conflicts.  Copies complete on
+// mbarrier transaction counts.  In decode_mma_kernel each warp owns a private ring
+// and its lane 0 refills a stage as soon as the warp has consumed it (optionally
+// also prefetching further blocks into L2); in shared_prefix_kernel a producer
+// warp fills a CTA ring that all member warps read (full / empty mbarriers).
 //
 // Math.  The query heads that share a KV head are the N = 8 columns of a warp MMA
 // m16n8k16 (grouped-query reuse: every K/V element loaded serves all of them):
@@ -48,15 +56,234 @@ struct DecodeGeom {
   static constexpr int kMTiles = BS / 16;
   static constexpr int kKSteps = HEAD / 16;
   static constexpr int kDTiles = HEAD / 16;
-  static constexpr int kStages = kTileBytes <= 4096 ? 3 : 2;
-  static constexpr int kSub = kRowBytes / 128;           // 128-byte sub-tiles per tile
-  static constexpr int kSubElems = 128 / kElemBytes;     // elements per sub-tile row
+  static constexpr int kStages = kTileBytes <= 4096 ? 3 : 2;       // per-warp ring (decode)
+  static constexpr int kSharedStages = kTileBytes <= 4096 ? 6 : 4;  // CTA ring (shared prefix)
   static_assert(kRowBytes % 128 == 0, "token rows must be whole 128-byte rows");
   // byte offset of 16-byte chunk `chunk` of token `tok` inside a tile
   static __device__ __forceinline__ uint32_t off(int tok, int chunk) {
     return static_cast<uint32_t>((chunk >> 3) * BS * 128) + swz128(tok, chunk & 7);
   }
 };
+
+// Per-warp attention state for one query row and its <= 8 heads (columns 2qq, 2qq+1
+// of the accumulators belong to this thread: heads A and B).
+template <int HEAD>
+struct WarpState {
+  float acc[HEAD / 16][4];
+  float mA, mB, lA, lB;
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int i = 0; i < HEAD / 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    mA = mB = -INFINITY;
+    lA = lB = 0.f;
+  }
+};
+
+// B-operand fragments of the query (k = head dim, n = query head of the group) and
+// the score multipliers (log2 units) of this thread's accumulator columns.
+template <int QDT, int KVDT, int HEAD>
+__device__ __forceinline__ void load_query(const AttnParams& p, long long row, int h0, int nh,
+                                           uint32_t (&qb)[HEAD / 16][2], float& cA, float& cB) {
+  using QE = Elem<QDT>;
+  constexpr int KS = HEAD / 16;
+  const int lane = threadIdx.x & 31;
+  const int qn = lane >> 2, qq = lane & 3;
+  const float base_c = p.scale * kLog2e;
+  const typename QE::T* qrow =
+      reinterpret_cast<const typename QE::T*>(p.q) + (row * p.num_q_heads + h0 + qn) * HEAD;
+  if constexpr (KVDT != PA_FP8_E4M3) {
+    const uint32_t* qw = reinterpret_cast<const uint32_t*>(qrow);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qb[ks][0] = qn < nh ? qw[8 * ks + qq] : 0u;
+      qb[ks][1] = qn < nh ? qw[8 * ks + 4 + qq] : 0u;
+    }
+    cA = cB = base_c;
+  } else {
+    // k-step ks, B rows (2qq, 2qq+1) <-> dims 32qq + 4ks + {0,1}; rows (2qq+8, 2qq+9) <-> +{2,3}
+    float amax = 0.f;
+    float qv[KS][4];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        qv[ks][e] = qn < nh ? QE::load(qrow + 32 * qq + 4 * ks + e) : 0.f;
+        amax = fmaxf(amax, fabsf(qv[ks][e]));
+      }
+    amax = warp_max_xor(amax, 1, 2);
+    int ex = 0;
+    frexpf(amax, &ex);  // amax < 2^ex
+    int sh = 15 - ex;   // |q| * 2^sh < 2^15, exact in f16
+    sh = max(-100, min(100, sh));
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qb[ks][0] = pack2<PA_F16>(ldexpf(qv[ks][0], sh), ldexpf(qv[ks][1], sh));
+      qb[ks][1] = pack2<PA_F16>(ldexpf(qv[ks][2], sh), ldexpf(qv[ks][3], sh));
+    }
+    const float my_c = ldexpf(base_c * (*p.k_scale), -sh);
+    cA = __shfl_sync(0xffffffffu, my_c, 8 * qq);      // head 2qq lives in lanes 8qq..8qq+3
+    cB = __shfl_sync(0xffffffffu, my_c, 8 * qq + 4);  // head 2qq+1
+  }
+}
+
+// One block of block_size tokens (K tile at `tile`, V tile at `tile + tile_bytes`)
+// folded into a warp's state; `rem` tokens of the block are valid.
+template <int QDT, int KVDT, int HEAD, int BS>
+__device__ __forceinline__ void attend_block(const uint8_t* tile, int rem, const uint32_t (&qb)[HEAD / 16][2],
+                                             float cA, float cB, WarpState<HEAD>& w) {
+  using G = DecodeGeom<KVDT, HEAD, BS>;
+  constexpr bool kFp8 = G::kFp8;
+  constexpr int MDT = kFp8 ? PA_F16 : QDT;
+  constexpr int TB = G::kTileBytes;
+  const int lane = threadIdx.x & 31, qq = lane & 3;
+  const uint32_t kbase = smem_u32(tile);
+  const uint32_t vbase = kbase + TB;
+
+  // ---- S^T = K Q^T
+  float sc[G::kMTiles][4];
+#pragma unroll
+  for (int mt = 0; mt < G::kMTiles; ++mt) {
+    float sc2[4] = {0.f, 0.f, 0.f, 0.f};  // second, independent accumulation chain
+    sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+    if constexpr (!kFp8) {
+#pragma unroll
+      for (int ks = 0; ks < G::kKSteps; ++ks) {
+        const int tok = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int chunk = 2 * ks + (lane >> 4);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kbase + G::off(tok, chunk), a0, a1, a2, a3);
+        if (ks & 1) mma_16816<MDT>(sc2, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+        else mma_16816<MDT>(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+      }
+    } else {
+      const int tA = 16 * mt + (lane >> 2), tB = tA + 8;
+      const uint4 ka0 = *reinterpret_cast<const uint4*>(tile + swz128(tA, 2 * qq));
+      const uint4 ka1 = *reinterpret_cast<const uint4*>(tile + swz128(tA, 2 * qq + 1));
+      const uint4 kb0 = *reinterpret_cast<const uint4*>(tile + swz128(tB, 2 * qq));
+      const uint4 kb1 = *reinterpret_cast<const uint4*>(tile + swz128(tB, 2 * qq + 1));
+      const uint32_t wa[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
+      const uint32_t wb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
+#pragma unroll
+      for (int ks = 0; ks < G::kKSteps; ++ks) {
+        const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(wa[ks] & 0xffffu));
+        const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(wa[ks] >> 16));
+        const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(wb[ks] & 0xffffu));
+        const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(wb[ks] >> 16));
+        if (ks & 1) mma_16816<PA_F16>(sc2, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+        else mma_16816<PA_F16>(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sc[mt][e] += sc2[e];
+  }
+
+  // ---- online softmax on the accumulators (columns 2qq, 2qq+1 = heads A, B)
+  float mxA = -INFINITY, mxB = -INFINITY;
+#pragma unroll
+  for (int mt = 0; mt < G::kMTiles; ++mt) {
+    const int t0 = 16 * mt + (lane >> 2);
+    const bool v0 = t0 < rem, v1 = t0 + 8 < rem;
+    sc[mt][0] = v0 ? sc[mt][0] * cA : -INFINITY;
+    sc[mt][1] = v0 ? sc[mt][1] * cB : -INFINITY;
+    sc[mt][2] = v1 ? sc[mt][2] * cA : -INFINITY;
+    sc[mt][3] = v1 ? sc[mt][3] * cB : -INFINITY;
+    mxA = fmaxf(mxA, fmaxf(sc[mt][0], sc[mt][2]));
+    mxB = fmaxf(mxB, fmaxf(sc[mt][1], sc[mt][3]));
+  }
+  mxA = warp_max_xor(mxA, 4, 16);
+  mxB = warp_max_xor(mxB, 4, 16);
+  const float nA = fmaxf(w.mA, mxA), nB = fmaxf(w.mB, mxB);
+  const float uA = nA == -INFINITY ? 0.f : nA, uB = nB == -INFINITY ? 0.f : nB;
+  const float alA = exp2f(w.mA - uA), alB = exp2f(w.mB - uB);
+  w.mA = nA;
+  w.mB = nB;
+  uint32_t pb[G::kMTiles][2];
+  float addA = 0.f, addB = 0.f;
+#pragma unroll
+  for (int mt = 0; mt < G::kMTiles; ++mt) {
+    const uint32_t X = pack2<MDT>(exp2f(sc[mt][0] - uA), exp2f(sc[mt][1] - uB));
+    const uint32_t Y = pack2<MDT>(exp2f(sc[mt][2] - uA), exp2f(sc[mt][3] - uB));
+    const float2 fx = unpack2<MDT>(X), fy = unpack2<MDT>(Y);
+    addA += fx.x + fy.x;
+    addB += fx.y + fy.y;
+    pb[mt][0] = movmatrix_trans(X);
+    pb[mt][1] = movmatrix_trans(Y);
+  }
+  w.lA = w.lA * alA + addA;
+  w.lB = w.lB * alB + addB;
+#pragma unroll
+  for (int dt = 0; dt < G::kDTiles; ++dt) {
+    w.acc[dt][0] *= alA;
+    w.acc[dt][1] *= alB;
+    w.acc[dt][2] *= alA;
+    w.acc[dt][3] *= alB;
+  }
+
+  // ---- O^T += V^T P^T; V tokens past the valid ones are zeroed (their P is 0,
+  // their bits arbitrary)
+  const bool tail = rem < BS;
+#pragma unroll
+  for (int kt = 0; kt < G::kMTiles; ++kt) {
+    if constexpr (!kFp8) {
+      const int tk = 16 * kt + 2 * qq;  // tokens of this thread's A halves: tk, tk+1, tk+8, tk+9
+      const uint32_t m01 = (tk < rem ? 0xffffu : 0u) | (tk + 1 < rem ? 0xffff0000u : 0u);
+      const uint32_t m23 = (tk + 8 < rem ? 0xffffu : 0u) | (tk + 9 < rem ? 0xffff0000u : 0u);
+#pragma unroll
+      for (int dt = 0; dt < G::kDTiles; ++dt) {
+        const int tok = 16 * kt + (lane & 7) + 8 * (lane >> 4);
+        const int chunk = 2 * dt + ((lane >> 3) & 1);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(vbase + G::off(tok, chunk), a0, a1, a2, a3);
+        if (tail) {
+          a0 &= m01;
+          a1 &= m01;
+          a2 &= m23;
+          a3 &= m23;
+        }
+        mma_16816<MDT>(w.acc[dt], a0, a1, a2, a3, pb[kt][0], pb[kt][1]);
+      }
+    } else {
+      // this thread owns dims 16*(lane>>2) .. +15 of tokens 16kt + {2qq, 2qq+1, 2qq+8, 2qq+9}
+      const int rr = lane >> 2;
+      const uint8_t* vt = tile + TB;
+      const int tk = 16 * kt + 2 * qq;
+      uint4 v[4];
+      v[0] = *reinterpret_cast<const uint4*>(vt + swz128(tk, rr));
+      v[1] = *reinterpret_cast<const uint4*>(vt + swz128(tk + 1, rr));
+      v[2] = *reinterpret_cast<const uint4*>(vt + swz128(tk + 8, rr));
+      v[3] = *reinterpret_cast<const uint4*>(vt + swz128(tk + 9, rr));
+      if (tail) {
+        if (tk >= rem) v[0] = make_uint4(0, 0, 0, 0);
+        if (tk + 1 >= rem) v[1] = make_uint4(0, 0, 0, 0);
+        if (tk + 8 >= rem) v[2] = make_uint4(0, 0, 0, 0);
+        if (tk + 9 >= rem) v[3] = make_uint4(0, 0, 0, 0);
+      }
+      const uint32_t w0[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
+      const uint32_t w1[4] = {v[1].x, v[1].y, v[1].z, v[1].w};
+      const uint32_t w2[4] = {v[2].x, v[2].y, v[2].z, v[2].w};
+      const uint32_t w3[4] = {v[3].x, v[3].y, v[3].z, v[3].w};
+#pragma unroll
+      for (int dt = 0; dt < G::kDTiles; ++dt) {
+        const int sh = 16 * (dt & 1);
+        const uint32_t x0 = e4m3x2_to_f16x2(static_cast<uint16_t>(w0[dt >> 1] >> sh));
+        const uint32_t y0 = e4m3x2_to_f16x2(static_cast<uint16_t>(w1[dt >> 1] >> sh));
+        const uint32_t x1 = e4m3x2_to_f16x2(static_cast<uint16_t>(w2[dt >> 1] >> sh));
+        const uint32_t y1 = e4m3x2_to_f16x2(static_cast<uint16_t>(w3[dt >> 1] >> sh));
+        const uint32_t a0 = __byte_perm(x0, y0, 0x5410), a1 = __byte_perm(x0, y0, 0x7632);
+        const uint32_t a2 = __byte_perm(x1, y1, 0x5410), a3 = __byte_perm(x1, y1, 0x7632);
+        mma_16816<PA_F16>(w.acc[dt], a0, a1, a2, a3, pb[kt][0], pb[kt][1]);
+      }
+    }
+  }
+}
+
+// Output dimensions of accumulator elements 0/1 (dA) and 2/3 (dB) of d-tile dt.
+template <bool kFp8>
+__device__ __forceinline__ void acc_dims(int dt, int lane, int& dA, int& dB) {
+  const int rr = lane >> 2;
+  dA = kFp8 ? 16 * rr + 2 * dt : 16 * dt + rr;
+  dB = kFp8 ? dA + 1 : dA + 8;
+}
 
 template <int KVDT, int HEAD, int BS, int NW>
 constexpr int decode_smem_bytes() {
@@ -71,7 +298,6 @@ __global__ void __launch_bounds__(NW * 32)
   using G = DecodeGeom<KVDT, HEAD, BS>;
   using QE = Elem<QDT>;
   constexpr bool kFp8 = G::kFp8;
-  constexpr int MDT = kFp8 ? PA_F16 : QDT;  // element type fed to the MMA
   constexpr int ST = G::kStages;
   constexpr int TB = G::kTileBytes;
 
@@ -107,12 +333,16 @@ __global__ void __launch_bounds__(NW * 32)
     }
     return;
   }
+  // tokens [start, seq_len) are this kernel's; [0, start) belong to the shared-prefix kernel
+  const int start = p.query_start_loc == nullptr ? shared_prefix_tokens(p, r) : 0;
   const int nblk = (seq_len + BS - 1) / BS;
   const int pb = p.part / BS;
-  const int b0 = z * pb;
+  const int sb0 = start / BS;
+  const int b0 = sb0 + z * pb;
   if (b0 >= nblk) return;
   const int b1 = min(b0 + pb, nblk);
-  const int nparts = (nblk + pb - 1) / pb;
+  const int nparts = (nblk - sb0 + pb - 1) / pb;
+  const int shared_parts = (start + p.part - 1) / p.part;
 
   if (threadIdx.x == 0) {
     s_failed = 0;
@@ -157,54 +387,11 @@ __global__ void __launch_bounds__(NW * 32)
     for (int i = 0; i < min(ST, nmine); ++i) issue(i);
   }
 
-  // ---- query fragments (B operand: k = head dim, n = query head of the group)
-  const int qn = lane >> 2, qq = lane & 3;  // B-fragment column / k-pair index
   uint32_t qb[G::kKSteps][2];
-  float cA, cB;  // score multipliers (log2 units) of accumulator columns 2*qq, 2*qq+1
-  {
-    const float base_c = p.scale * kLog2e;
-    const typename QE::T* qrow =
-        reinterpret_cast<const typename QE::T*>(p.q) + ((long long)row * p.num_q_heads + h0 + qn) * HEAD;
-    if constexpr (!kFp8) {
-      const uint32_t* qw = reinterpret_cast<const uint32_t*>(qrow);
-#pragma unroll
-      for (int ks = 0; ks < G::kKSteps; ++ks) {
-        qb[ks][0] = qn < nh ? qw[8 * ks + qq] : 0u;
-        qb[ks][1] = qn < nh ? qw[8 * ks + 4 + qq] : 0u;
-      }
-      cA = cB = base_c;
-    } else {
-      // k-step ks, B rows (2qq, 2qq+1) <-> dims 32qq + 4ks + {0,1}; rows (2qq+8, 2qq+9) <-> +{2,3}
-      float amax = 0.f;
-      float qv[G::kKSteps][4];
-#pragma unroll
-      for (int ks = 0; ks < G::kKSteps; ++ks)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          qv[ks][e] = qn < nh ? QE::load(qrow + 32 * qq + 4 * ks + e) : 0.f;
-          amax = fmaxf(amax, fabsf(qv[ks][e]));
-        }
-      amax = warp_max_xor(amax, 1, 2);
-      int ex = 0;
-      frexpf(amax, &ex);                        // amax < 2^ex
-      int sh = 15 - ex;                         // |q| * 2^sh < 2^15, exact in f16
-      sh = max(-100, min(100, sh));
-#pragma unroll
-      for (int ks = 0; ks < G::kKSteps; ++ks) {
-        qb[ks][0] = pack2<PA_F16>(ldexpf(qv[ks][0], sh), ldexpf(qv[ks][1], sh));
-        qb[ks][1] = pack2<PA_F16>(ldexpf(qv[ks][2], sh), ldexpf(qv[ks][3], sh));
-      }
-      const float kc = base_c * (*p.k_scale);
-      const float my_c = ldexpf(kc, -sh);
-      cA = __shfl_sync(0xffffffffu, my_c, 8 * qq);      // head 2qq lives in lanes 8qq..8qq+3
-      cB = __shfl_sync(0xffffffffu, my_c, 8 * qq + 4);  // head 2qq+1
-    }
-  }
-
-  float acc[G::kDTiles][4];
-#pragma unroll
-  for (int i = 0; i < G::kDTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+  float cA, cB;
+  load_query<QDT, KVDT, HEAD>(p, row, h0, nh, qb, cA, cB);
+  WarpState<HEAD> w;
+  w.init();
   bool failed = false;
   int consumed = 0;
 
@@ -218,148 +405,8 @@ __global__ void __launch_bounds__(NW * 32)
     consumed = i + 1;
     const int jb = b0 + warp + i * NW;
     const int phys = table[jb];
-    if (phys >= 0 && phys < p.num_blocks) {
-      const uint32_t kbase = smem_u32(ring + s * 2 * TB);
-      const uint32_t vbase = kbase + TB;
-      const int rem = seq_len - jb * BS;  // valid tokens in this block (>= BS except the tail)
-
-      // ---- S^T = K Q^T
-      float sc[G::kMTiles][4];
-#pragma unroll
-      for (int mt = 0; mt < G::kMTiles; ++mt) {
-        float sc2[4] = {0.f, 0.f, 0.f, 0.f};  // second, independent accumulation chain
-        sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
-        if constexpr (!kFp8) {
-#pragma unroll
-          for (int ks = 0; ks < G::kKSteps; ++ks) {
-            const int tok = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
-            const int chunk = 2 * ks + (lane >> 4);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(kbase + G::off(tok, chunk), a0, a1, a2, a3);
-            if (ks & 1) mma_16816<MDT>(sc2, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-            else mma_16816<MDT>(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-          }
-        } else {
-          const int tA = 16 * mt + (lane >> 2), tB = tA + 8;
-          const uint4 ka0 = *reinterpret_cast<const uint4*>(ring + s * 2 * TB + swz128(tA, 2 * qq));
-          const uint4 ka1 = *reinterpret_cast<const uint4*>(ring + s * 2 * TB + swz128(tA, 2 * qq + 1));
-          const uint4 kb0 = *reinterpret_cast<const uint4*>(ring + s * 2 * TB + swz128(tB, 2 * qq));
-          const uint4 kb1 = *reinterpret_cast<const uint4*>(ring + s * 2 * TB + swz128(tB, 2 * qq + 1));
-          const uint32_t wa[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
-          const uint32_t wb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
-#pragma unroll
-          for (int ks = 0; ks < G::kKSteps; ++ks) {
-            const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(wa[ks] & 0xffffu));
-            const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(wa[ks] >> 16));
-            const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(wb[ks] & 0xffffu));
-            const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(wb[ks] >> 16));
-            if (ks & 1) mma_16816<PA_F16>(sc2, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-            else mma_16816<PA_F16>(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-          }
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sc[mt][e] += sc2[e];
-      }
-
-      // ---- online softmax on the accumulators (columns 2qq, 2qq+1 = heads A, B)
-      float mxA = -INFINITY, mxB = -INFINITY;
-#pragma unroll
-      for (int mt = 0; mt < G::kMTiles; ++mt) {
-        const int t0 = 16 * mt + (lane >> 2);
-        const bool v0 = t0 < rem, v1 = t0 + 8 < rem;
-        sc[mt][0] = v0 ? sc[mt][0] * cA : -INFINITY;
-        sc[mt][1] = v0 ? sc[mt][1] * cB : -INFINITY;
-        sc[mt][2] = v1 ? sc[mt][2] * cA : -INFINITY;
-        sc[mt][3] = v1 ? sc[mt][3] * cB : -INFINITY;
-        mxA = fmaxf(mxA, fmaxf(sc[mt][0], sc[mt][2]));
-        mxB = fmaxf(mxB, fmaxf(sc[mt][1], sc[mt][3]));
-      }
-      mxA = warp_max_xor(mxA, 4, 16);
-      mxB = warp_max_xor(mxB, 4, 16);
-      const float nA = fmaxf(mA, mxA), nB = fmaxf(mB, mxB);
-      const float uA = nA == -INFINITY ? 0.f : nA, uB = nB == -INFINITY ? 0.f : nB;
-      const float alA = exp2f(mA - uA), alB = exp2f(mB - uB);
-      mA = nA;
-      mB = nB;
-      uint32_t pb[G::kMTiles][2];
-      float addA = 0.f, addB = 0.f;
-#pragma unroll
-      for (int mt = 0; mt < G::kMTiles; ++mt) {
-        const uint32_t X = pack2<MDT>(exp2f(sc[mt][0] - uA), exp2f(sc[mt][1] - uB));
-        const uint32_t Y = pack2<MDT>(exp2f(sc[mt][2] - uA), exp2f(sc[mt][3] - uB));
-        const float2 fx = unpack2<MDT>(X), fy = unpack2<MDT>(Y);
-        addA += fx.x + fy.x;
-        addB += fx.y + fy.y;
-        pb[mt][0] = movmatrix_trans(X);
-        pb[mt][1] = movmatrix_trans(Y);
-      }
-      lA = lA * alA + addA;
-      lB = lB * alB + addB;
-#pragma unroll
-      for (int dt = 0; dt < G::kDTiles; ++dt) {
-        acc[dt][0] *= alA;
-        acc[dt][1] *= alB;
-        acc[dt][2] *= alA;
-        acc[dt][3] *= alB;
-      }
-
-      // ---- O^T += V^T P^T
-      const bool tail = rem < BS;
-#pragma unroll
-      for (int kt = 0; kt < G::kMTiles; ++kt) {
-        if constexpr (!kFp8) {
-          const int tk = 16 * kt + 2 * qq;  // tokens of this thread's A halves: tk, tk+1, tk+8, tk+9
-          const uint32_t lo0 = tk < rem ? 0xffffu : 0u, hi0 = tk + 1 < rem ? 0xffff0000u : 0u;
-          const uint32_t lo1 = tk + 8 < rem ? 0xffffu : 0u, hi1 = tk + 9 < rem ? 0xffff0000u : 0u;
-          const uint32_t m01 = lo0 | hi0, m23 = lo1 | hi1;
-#pragma unroll
-          for (int dt = 0; dt < G::kDTiles; ++dt) {
-            const int tok = 16 * kt + (lane & 7) + 8 * (lane >> 4);
-            const int chunk = 2 * dt + ((lane >> 3) & 1);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_trans(vbase + G::off(tok, chunk), a0, a1, a2, a3);
-            if (tail) {
-              a0 &= m01;
-              a1 &= m01;
-              a2 &= m23;
-              a3 &= m23;
-            }
-            mma_16816<MDT>(acc[dt], a0, a1, a2, a3, pb[kt][0], pb[kt][1]);
-          }
-        } else {
-          // this thread owns dims 16*(lane>>2) .. +15 of tokens 16kt + {2qq, 2qq+1, 2qq+8, 2qq+9}
-          const int rr = lane >> 2;
-          const uint8_t* vt = ring + s * 2 * TB + TB;
-          const int tk = 16 * kt + 2 * qq;
-          uint4 v[4];
-          v[0] = *reinterpret_cast<const uint4*>(vt + swz128(tk, rr));
-          v[1] = *reinterpret_cast<const uint4*>(vt + swz128(tk + 1, rr));
-          v[2] = *reinterpret_cast<const uint4*>(vt + swz128(tk + 8, rr));
-          v[3] = *reinterpret_cast<const uint4*>(vt + swz128(tk + 9, rr));
-          if (tail) {
-            if (tk >= rem) v[0] = make_uint4(0, 0, 0, 0);
-            if (tk + 1 >= rem) v[1] = make_uint4(0, 0, 0, 0);
-            if (tk + 8 >= rem) v[2] = make_uint4(0, 0, 0, 0);
-            if (tk + 9 >= rem) v[3] = make_uint4(0, 0, 0, 0);
-          }
-          const uint32_t w0[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
-          const uint32_t w1[4] = {v[1].x, v[1].y, v[1].z, v[1].w};
-          const uint32_t w2[4] = {v[2].x, v[2].y, v[2].z, v[2].w};
-          const uint32_t w3[4] = {v[3].x, v[3].y, v[3].z, v[3].w};
-#pragma unroll
-          for (int dt = 0; dt < G::kDTiles; ++dt) {
-            const int sh = 16 * (dt & 1);
-            const uint32_t x0 = e4m3x2_to_f16x2(static_cast<uint16_t>(w0[dt >> 1] >> sh));
-            const uint32_t y0 = e4m3x2_to_f16x2(static_cast<uint16_t>(w1[dt >> 1] >> sh));
-            const uint32_t x1 = e4m3x2_to_f16x2(static_cast<uint16_t>(w2[dt >> 1] >> sh));
-            const uint32_t y1 = e4m3x2_to_f16x2(static_cast<uint16_t>(w3[dt >> 1] >> sh));
-            const uint32_t a0 = __byte_perm(x0, y0, 0x5410), a1 = __byte_perm(x0, y0, 0x7632);
-            const uint32_t a2 = __byte_perm(x1, y1, 0x5410), a3 = __byte_perm(x1, y1, 0x7632);
-            mma_16816<PA_F16>(acc[dt], a0, a1, a2, a3, pb[kt][0], pb[kt][1]);
-          }
-        }
-      }
-    }
+    if (phys >= 0 && phys < p.num_blocks)
+      attend_block<QDT, KVDT, HEAD, BS>(ring + s * 2 * TB, seq_len - jb * BS, qb, cA, cB, w);
     __syncwarp();
     if (i + ST < nmine && lane == 0) {
       fence_proxy_async();
@@ -378,60 +425,215 @@ __global__ void __launch_bounds__(NW * 32)
   }
 
   // ---- merge the warps' states through shared memory
-  lA = warp_sum_xor(lA, 4, 16);
-  lB = warp_sum_xor(lB, 4, 16);
+  w.lA = warp_sum_xor(w.lA, 4, 16);
+  w.lB = warp_sum_xor(w.lB, 4, 16);
   __syncthreads();
   if (s_failed) return;
   float* red = reinterpret_cast<float*>(smem);  // [NW][8][HEAD]
   float* rm = red + NW * 8 * HEAD;              // [NW][8]
   float* rl = rm + NW * 8;                      // [NW][8]
   {
-    const int rr = lane >> 2;
+    const int qq = lane & 3;
 #pragma unroll
     for (int dt = 0; dt < G::kDTiles; ++dt) {
-      const int dA = kFp8 ? 16 * rr + 2 * dt : 16 * dt + rr;
-      const int dB = kFp8 ? dA + 1 : dA + 8;
-      red[(warp * 8 + 2 * qq) * HEAD + dA] = acc[dt][0];
-      red[(warp * 8 + 2 * qq + 1) * HEAD + dA] = acc[dt][1];
-      red[(warp * 8 + 2 * qq) * HEAD + dB] = acc[dt][2];
-      red[(warp * 8 + 2 * qq + 1) * HEAD + dB] = acc[dt][3];
+      int dA, dB;
+      acc_dims<kFp8>(dt, lane, dA, dB);
+      red[(warp * 8 + 2 * qq) * HEAD + dA] = w.acc[dt][0];
+      red[(warp * 8 + 2 * qq + 1) * HEAD + dA] = w.acc[dt][1];
+      red[(warp * 8 + 2 * qq) * HEAD + dB] = w.acc[dt][2];
+      red[(warp * 8 + 2 * qq + 1) * HEAD + dB] = w.acc[dt][3];
     }
     if (lane < 4) {
-      rm[warp * 8 + 2 * lane] = mA;
-      rm[warp * 8 + 2 * lane + 1] = mB;
-      rl[warp * 8 + 2 * lane] = lA;
-      rl[warp * 8 + 2 * lane + 1] = lB;
+      rm[warp * 8 + 2 * lane] = w.mA;
+      rm[warp * 8 + 2 * lane + 1] = w.mB;
+      rl[warp * 8 + 2 * lane] = w.lA;
+      rl[warp * 8 + 2 * lane + 1] = w.lB;
     }
   }
   __syncthreads();
   const float vscale = kFp8 ? *p.v_scale : 1.f;
   const long long pbase = p.part_off ? (long long)p.part_off[r] : (long long)row * p.max_partitions;
+  const bool direct = nparts == 1 && !p.force_partials;
   for (int idx = threadIdx.x; idx < nh * HEAD; idx += NW * 32) {
     const int n = idx / HEAD, dd = idx % HEAD;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NW; ++w)
-      if (rl[w * 8 + n] > 0.f) M = fmaxf(M, rm[w * 8 + n]);
+    for (int ww = 0; ww < NW; ++ww)
+      if (rl[ww * 8 + n] > 0.f) M = fmaxf(M, rm[ww * 8 + n]);
     float L = 0.f, O = 0.f;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const float lw = rl[w * 8 + n];
+    for (int ww = 0; ww < NW; ++ww) {
+      const float lw = rl[ww * 8 + n];
       if (lw > 0.f) {
-        const float f = exp2f(rm[w * 8 + n] - M);
+        const float f = exp2f(rm[ww * 8 + n] - M);
         L = fmaf(lw, f, L);
-        O = fmaf(red[(w * 8 + n) * HEAD + dd], f, O);
+        O = fmaf(red[(ww * 8 + n) * HEAD + dd], f, O);
       }
     }
     O *= vscale;
     const int h = h0 + n;
-    if (nparts == 1) {
+    if (direct) {
       out[((long long)row * p.num_q_heads + h) * HEAD + dd] = QE::from_float(L > 0.f ? O / L : 0.f);
     } else {
-      const long long pi = pbase + z;
+      const long long pi = pbase + shared_parts + z;
       p.ws_acc[(pi * p.num_q_heads + h) * HEAD + dd] = O;
       if (dd == 0) p.ws_ml[pi * p.num_q_heads + h] = make_float2(M, L);
     }
   }
+}
+
+// ------------------------------------------------------------------ shared prefix
+
+constexpr int kMaxGroup = 8;
+
+template <int KVDT, int HEAD, int BS>
+constexpr int shared_smem_bytes() {
+  using G = DecodeGeom<KVDT, HEAD, BS>;
+  return G::kSharedStages * 2 * G::kTileBytes + 2 * G::kSharedStages * 8 + 1024;
+}
+
+// grid: (group, KV head x head group, partition of the shared prefix); block: one
+// warp per group member (up to the group size bound) + one producer warp.
+template <int QDT, int KVDT, int HEAD, int BS>
+__global__ void __launch_bounds__((kMaxGroup + 1) * 32)
+    shared_prefix_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                         const __grid_constant__ CUtensorMap tmv) {
+  using G = DecodeGeom<KVDT, HEAD, BS>;
+  constexpr bool kFp8 = G::kFp8;
+  constexpr int ST = G::kSharedStages;
+  constexpr int TB = G::kTileBytes;
+
+  const int g = blockIdx.x;
+  const int kvh = blockIdx.y / p.num_head_groups, hg = blockIdx.y % p.num_head_groups;
+  const int z = blockIdx.z;
+  const int s0 = p.group_start[g], s1 = p.group_start[g + 1];
+  const int nm = s1 - s0;
+  const int nwarps = blockDim.x >> 5;
+  if (nm < 2 || nm > nwarps - 1) return;
+  const int S = group_shared_tokens(p, g, s0, s1);
+  if (S == 0) return;
+  const int nsb = S / BS, pb = p.part / BS;
+  const int b0 = z * pb;
+  if (b0 >= nsb) return;
+  const int nblocks = min(b0 + pb, nsb) - b0;
+  const int h0 = kvh * p.group + hg * 8;
+  const int nh = min(8, p.group - hg * 8);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * 2 * TB);
+  uint64_t* empty = full + ST;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+    for (int i = 0; i < ST; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, nm);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int32_t* lead = p.block_tables + (long long)s0 * p.max_blocks_per_seq;
+
+  if (warp == nm) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      for (int i = 0; i < nblocks; ++i) {
+        const int s = i % ST;
+        if (i >= ST && !mbar_wait_bounded(empty + s, ((i / ST) - 1) & 1)) {
+          flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+          break;  // the members time out on the full barrier and write nothing
+        }
+        const int jb = b0 + i;
+        const int phys = lead[jb];
+        bool same = true;  // the members' tables must name the same physical block
+        for (int m = 1; m < nm; ++m)
+          same &= p.block_tables[(long long)(s0 + m) * p.max_blocks_per_seq + jb] == phys;
+        if (!same || phys < 0 || phys >= p.num_blocks) {
+          flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
+          mbar_arrive(full + s);  // empty phase: the members skip this block
+        } else {
+          uint8_t* st = smem + s * 2 * TB;
+          mbar_arrive_expect_tx(full + s, 2 * TB);
+          tma_load_4d(st, &tmk, 0, kvh * BS, 0, phys, full + s);
+          tma_load_4d(st + TB, &tmv, 0, kvh * BS, 0, phys, full + s);
+        }
+      }
+    }
+    return;
+  }
+  if (warp > nm) return;
+
+  // ------------------------------------------------------------------ members
+  const int seq = s0 + warp;
+  uint32_t qb[G::kKSteps][2];
+  float cA, cB;
+  load_query<QDT, KVDT, HEAD>(p, seq, h0, nh, qb, cA, cB);
+  WarpState<HEAD> w;
+  w.init();
+  for (int i = 0; i < nblocks; ++i) {
+    const int s = i % ST;
+    const bool got = mbar_wait_bounded(full + s, (i / ST) & 1);
+    if (!__all_sync(0xffffffffu, got)) {
+      if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+      return;
+    }
+    const int jb = b0 + i;
+    const int phys = lead[jb];
+    bool same = true;
+    for (int m = 1; m < nm; ++m)
+      same &= p.block_tables[(long long)(s0 + m) * p.max_blocks_per_seq + jb] == phys;
+    if (same && phys >= 0 && phys < p.num_blocks)
+      attend_block<QDT, KVDT, HEAD, BS>(smem + s * 2 * TB, BS, qb, cA, cB, w);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty + s);
+  }
+
+  // ---- this member's partial state for partition z of its shared prefix
+  w.lA = warp_sum_xor(w.lA, 4, 16);
+  w.lB = warp_sum_xor(w.lB, 4, 16);
+  const float vscale = kFp8 ? *p.v_scale : 1.f;
+  const long long pi = (long long)seq * p.max_partitions + z;
+  const int qq = lane & 3;
+  const int hA = 2 * qq, hB = 2 * qq + 1;
+#pragma unroll
+  for (int dt = 0; dt < G::kDTiles; ++dt) {
+    int dA, dB;
+    acc_dims<kFp8>(dt, lane, dA, dB);
+    if (hA < nh) {
+      float* wa = p.ws_acc + (pi * p.num_q_heads + h0 + hA) * HEAD;
+      wa[dA] = w.acc[dt][0] * vscale;
+      wa[dB] = w.acc[dt][2] * vscale;
+    }
+    if (hB < nh) {
+      float* wb = p.ws_acc + (pi * p.num_q_heads + h0 + hB) * HEAD;
+      wb[dA] = w.acc[dt][1] * vscale;
+      wb[dB] = w.acc[dt][3] * vscale;
+    }
+  }
+  if (lane < 4) {
+    if (hA < nh) p.ws_ml[pi * p.num_q_heads + h0 + hA] = make_float2(w.mA, w.lA);
+    if (hB < nh) p.ws_ml[pi * p.num_q_heads + h0 + hB] = make_float2(w.mB, w.lB);
+  }
+}
+
+// Opt the kernel into `smem` bytes of dynamic shared memory, once per kernel and
+// device (one static per instantiation of this template, i.e. per kernel).
+template <auto kKernel>
+cudaError_t set_smem(int smem) {
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kKernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();  // consume it: the caller reports the failure
+      return e;
+    }
+    configured_device = dev;
+  }
+  return cudaSuccess;
 }
 
 template <int QDT, int KVDT, int HEAD, int BS>
@@ -439,33 +641,56 @@ cudaError_t launch_t(const AttnParams& p, int grid_z, const CUtensorMap* tk, con
                      cudaStream_t stream) {
   constexpr int NW = 4;
   constexpr int smem = decode_smem_bytes<KVDT, HEAD, BS, NW>();
-  auto kern = decode_mma_kernel<QDT, KVDT, HEAD, BS, NW>;
-  static int configured_device = -1;  // the attribute is per device
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
+  constexpr auto kern = decode_mma_kernel<QDT, KVDT, HEAD, BS, NW>;
+  cudaError_t e = set_smem<kern>(smem);
+  if (e != cudaSuccess) return e;
   dim3 grid(p.num_seqs, p.num_kv_heads * p.num_head_groups, grid_z);
   kern<<<grid, NW * 32, smem, stream>>>(p, *tk, *tv);
   return cudaGetLastError();
 }
 
-template <int QDT, int KVDT>
+template <int QDT, int KVDT, int HEAD, int BS>
+cudaError_t launch_shared_t(const AttnParams& p, int grid_z, const CUtensorMap* tk, const CUtensorMap* tv,
+                            cudaStream_t stream) {
+  constexpr int smem = shared_smem_bytes<KVDT, HEAD, BS>();
+  constexpr auto kern = shared_prefix_kernel<QDT, KVDT, HEAD, BS>;
+  cudaError_t e = set_smem<kern>(smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.num_groups, p.num_kv_heads * p.num_head_groups, grid_z);
+  kern<<<grid, (p.max_group_size + 1) * 32, smem, stream>>>(p, *tk, *tv);
+  return cudaGetLastError();
+}
+
+template <int QDT, int KVDT, bool kShared>
 cudaError_t launch_shape(const AttnParams& p, int grid_z, const CUtensorMap* tk,
                          const CUtensorMap* tv, cudaStream_t s) {
   const int d = p.head_size, bs = p.block_size;
+#define PA_SHAPE(D, B)                                                      \
+  if (d == D && bs == B)                                                   \
+    return kShared ? launch_shared_t<QDT, KVDT, D, B>(p, grid_z, tk, tv, s) \
+                   : launch_t<QDT, KVDT, D, B>(p, grid_z, tk, tv, s);
   if constexpr (KVDT != PA_FP8_E4M3) {
-    if (d == 128 && bs == 16) return launch_t<QDT, KVDT, 128, 16>(p, grid_z, tk, tv, s);
-    if (d == 128 && bs == 32) return launch_t<QDT, KVDT, 128, 32>(p, grid_z, tk, tv, s);
-    if (d == 64 && bs == 16) return launch_t<QDT, KVDT, 64, 16>(p, grid_z, tk, tv, s);
-    if (d == 64 && bs == 32) return launch_t<QDT, KVDT, 64, 32>(p, grid_z, tk, tv, s);
+    PA_SHAPE(128, 16)
+    PA_SHAPE(128, 32)
+    PA_SHAPE(64, 16)
+    PA_SHAPE(64, 32)
   } else {
-    if (d == 128 && bs == 16) return launch_t<QDT, KVDT, 128, 16>(p, grid_z, tk, tv, s);
-    if (d == 128 && bs == 32) return launch_t<QDT, KVDT, 128, 32>(p, grid_z, tk, tv, s);
+    PA_SHAPE(128, 16)
+    PA_SHAPE(128, 32)
   }
+#undef PA_SHAPE
+  return cudaErrorInvalidValue;
+}
+
+template <bool kShared>
+cudaError_t dispatch(const AttnParams& p, int q_dtype, int kv_dtype, int grid_z, const CUtensorMap* tk,
+                     const CUtensorMap* tv, cudaStream_t s) {
+  if (q_dtype == PA_BF16 && kv_dtype == PA_BF16) return launch_shape<PA_BF16, PA_BF16, kShared>(p, grid_z, tk, tv, s);
+  if (q_dtype == PA_F16 && kv_dtype == PA_F16) return launch_shape<PA_F16, PA_F16, kShared>(p, grid_z, tk, tv, s);
+  if (q_dtype == PA_BF16 && kv_dtype == PA_FP8_E4M3)
+    return launch_shape<PA_BF16, PA_FP8_E4M3, kShared>(p, grid_z, tk, tv, s);
+  if (q_dtype == PA_F16 && kv_dtype == PA_FP8_E4M3)
+    return launch_shape<PA_F16, PA_FP8_E4M3, kShared>(p, grid_z, tk, tv, s);
   return cudaErrorInvalidValue;
 }
 
@@ -483,11 +708,14 @@ bool decode_mma_supported(int q_dtype, int kv_dtype, int head_size, int block_si
 cudaError_t launch_decode_mma(const AttnParams& p, int q_dtype, int kv_dtype, int grid_z,
                               const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
                               cudaStream_t stream) {
-  if (q_dtype == PA_BF16 && kv_dtype == PA_BF16) return launch_shape<PA_BF16, PA_BF16>(p, grid_z, tmap_k, tmap_v, stream);
-  if (q_dtype == PA_F16 && kv_dtype == PA_F16) return launch_shape<PA_F16, PA_F16>(p, grid_z, tmap_k, tmap_v, stream);
-  if (q_dtype == PA_BF16 && kv_dtype == PA_FP8_E4M3) return launch_shape<PA_BF16, PA_FP8_E4M3>(p, grid_z, tmap_k, tmap_v, stream);
-  if (q_dtype == PA_F16 && kv_dtype == PA_FP8_E4M3) return launch_shape<PA_F16, PA_FP8_E4M3>(p, grid_z, tmap_k, tmap_v, stream);
-  return cudaErrorInvalidValue;
+  return dispatch<false>(p, q_dtype, kv_dtype, grid_z, tmap_k, tmap_v, stream);
+}
+
+cudaError_t launch_shared_prefix(const AttnParams& p, int q_dtype, int kv_dtype, int grid_z,
+                                 const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                                 cudaStream_t stream) {
+  if (p.max_group_size < 2 || p.max_group_size > kMaxGroup || p.num_groups <= 0) return cudaErrorInvalidValue;
+  return dispatch<true>(p, q_dtype, kv_dtype, grid_z, tmap_k, tmap_v, stream);
 }
 
 }  // namespace pa

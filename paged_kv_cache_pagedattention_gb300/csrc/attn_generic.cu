@@ -137,9 +137,16 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnParams p
   const int head = static_cast<int>(gid % p.num_q_heads);
   if (row >= p.num_rows || plan_rejected(p)) return;
   const RowInfo ri = row_info(p, row);
-  if (!ri.ok || ri.parts_row <= 1) return;
+  if (!ri.ok) return;
+  int np = ri.parts_row;
+  if (p.force_partials) {
+    // shared-prefix decode: partials of the shared prefix, then of the private rest
+    const int start = shared_prefix_tokens(p, row);
+    np = (start + ri.part - 1) / ri.part + (ri.seq_len - start + ri.part - 1) / ri.part;
+  } else if (np <= 1) {
+    return;  // written directly by the attention kernel
+  }
   const long long base = row_partial_base(p, ri, row);
-  const int np = ri.parts_row;
   const int hq = p.num_q_heads, d = p.head_size;
   float M = -INFINITY;
   for (int j = threadIdx.x; j < np; j += blockDim.x) {

@@ -349,7 +349,10 @@ cudaError_t launch_t(const AttnParams& p, int num_items, const CUtensorMap* tk, 
   cudaGetDevice(&dev);
   if (configured_device != dev) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();  // consume it: the caller reports the failure
+      return e;
+    }
     configured_device = dev;
   }
   dim3 grid(num_items, p.num_kv_heads * p.num_head_groups);

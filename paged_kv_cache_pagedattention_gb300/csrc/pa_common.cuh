@@ -301,6 +301,36 @@ __device__ __forceinline__ RowInfo row_info(const AttnParams& p, int row) {
   return ri;
 }
 
+// Shared-prefix decode.  Group g is the run of sequences group_start[g] ..
+// group_start[g+1]-1; its members' block tables agree on their first
+// group_shared_blocks[g] entries.  The shared length used is that count clamped so
+// every member holds that many full blocks; groups of one sequence, or larger than
+// max_group_size, share nothing.
+__device__ __forceinline__ int group_shared_tokens(const AttnParams& p, int g, int s0, int s1) {
+  if (s1 - s0 < 2 || s1 - s0 > p.max_group_size) return 0;
+  int sb = p.group_shared_blocks[g];
+  for (int m = s0; m < s1; ++m) {
+    const int len = p.seq_lens[m];
+    if (len < 1 || len > p.max_seq_len) return 0;
+    sb = min(sb, len / p.block_size);
+  }
+  return sb > 0 ? sb * p.block_size : 0;
+}
+
+// Tokens at the start of sequence `seq` processed by the shared-prefix kernel.
+__device__ __forceinline__ int shared_prefix_tokens(const AttnParams& p, int seq) {
+  if (p.group_start == nullptr || p.num_groups <= 0) return 0;
+  int lo = 0, hi = p.num_groups;  // first g with group_start[g+1] > seq
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (p.group_start[mid + 1] <= seq) lo = mid + 1; else hi = mid;
+  }
+  if (lo >= p.num_groups) return 0;
+  const int s0 = p.group_start[lo], s1 = p.group_start[lo + 1];
+  if (seq < s0 || seq >= s1) return 0;
+  return group_shared_tokens(p, lo, s0, s1);
+}
+
 // Varlen launches do nothing when query_start_loc was found inconsistent (the plan
 // kernel has flagged it); this keeps every row and partial index in range.
 __device__ __forceinline__ bool plan_rejected(const AttnParams& p) {

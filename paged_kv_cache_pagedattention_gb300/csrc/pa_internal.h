@@ -26,6 +26,8 @@ struct AttnParams {
   const int4* work;                // varlen: prefill tile work list (plan kernel)
   const int32_t* work_count;       // varlen: number of entries in `work`
   const int32_t* plan_ok;          // varlen: 1 when query_start_loc passed the plan kernel's checks
+  const int32_t* group_start;      // shared-prefix decode: [num_groups+1] runs of consecutive sequences
+  const int32_t* group_shared_blocks;  // shared-prefix decode: [num_groups] leading blocks shared in a group
   float* ws_acc;                   // [partial rows][Hq][d]  un-normalised weighted sums
   float2* ws_ml;                   // [partial rows][Hq]     (running max in log2 units, weight sum)
   const float* k_scale;            // FP8 only
@@ -47,6 +49,9 @@ struct AttnParams {
   int part_pf;          // partition tokens for rows of multi-token requests
   int max_partitions;   // decode mode: partial rows reserved per query row
   int causal;
+  int num_groups;       // shared-prefix decode: number of groups (0 = no sharing)
+  int max_group_size;   // shared-prefix decode: host bound on sequences per group (<= 8)
+  int force_partials;   // every row writes partial states and goes through the merge
   int prefetch;         // L2 prefetch distance of the tensor-core kernels, in blocks (0 = off)
   float scale;          // softmax scale
 };
@@ -82,6 +87,10 @@ bool decode_mma_supported(int q_dtype, int kv_dtype, int head_size, int block_si
 cudaError_t launch_decode_mma(const AttnParams& p, int q_dtype, int kv_dtype, int grid_z,
                               const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
                               cudaStream_t stream);
+
+cudaError_t launch_shared_prefix(const AttnParams& p, int q_dtype, int kv_dtype, int grid_z,
+                                 const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                                 cudaStream_t stream);
 
 bool prefill_mma_supported(int q_dtype, int kv_dtype, int head_size, int block_size, int group);
 cudaError_t launch_prefill_mma(const AttnParams& p, int q_dtype, int kv_dtype, int num_ctas,

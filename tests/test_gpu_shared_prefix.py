@@ -1,0 +1,109 @@
+"""GPU parity of pa_decode_shared_prefix (groups of sequences sharing prefix blocks)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from harness import DeviceBatch, compare, oracle_scatter, run_decode, run_scatter, sampled_oracle_inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def pa():
+    import paged_kv_cache_pagedattention_gb300 as lib
+    lib.pa_get_error_flags(clear=True)
+    return lib
+
+
+def family_groups(b):
+    """group_start / shared blocks of the agentic families (forks share floor(0.96 * blocks))."""
+    starts, shared = [0], []
+    for fam in b.families:
+        assert fam == list(range(starts[-1], starts[-1] + len(fam)))
+        nb = -(-int(b.seq_lens[fam[0]]) // b.block_size)
+        shared.append(int(np.floor(0.96 * nb)) if len(fam) > 1 else 0)
+        starts.append(starts[-1] + len(fam))
+    return np.array(starts, np.int32), np.array(shared, np.int32)
+
+
+def run_shared(pa, db, starts, shared, max_group=8, partition_size=0):
+    b = db.b
+    out = torch.empty_like(db.q)
+    ws = pa.workspace_tensor(pa.pa_decode_shared_prefix_workspace_size(
+        b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_size, b.max_seq_len, b.block_size, partition_size), DEV)
+    pa.pa_decode_shared_prefix(out, db.q, db.kc, db.vc, db.tables, db.lens, b.max_seq_len, b.scale, ws,
+                               torch.from_numpy(starts).to(DEV), torch.from_numpy(shared).to(DEV), max_group,
+                               db.k_scale, db.v_scale, partition_size)
+    return out
+
+
+def _parity(pa, b, starts, shared, partition_size=0, max_group=8):
+    db = DeviceBatch(b, DEV)
+    run_scatter(pa, db)
+    out = run_shared(pa, db, starts, shared, max_group, partition_size)
+    torch.cuda.synchronize()
+    assert pa.pa_get_error_flags() == 0
+    k_ref, v_ref = oracle_scatter(b)
+    ref = oracle.paged_decode(b.q, b.q_dtype, k_ref, v_ref, b.kv_dtype, b.block_tables, b.seq_lens, b.block_size,
+                              b.scale, b.k_scale, b.v_scale)
+    compare(out, ref, b.kv_dtype, where=b.name)
+    plain = run_decode(pa, db, partition_size)
+    return out, plain
+
+
+@pytest.mark.parametrize("part", [0, 32, 160])
+def test_agentic_families_scaled_down(pa, part):
+    b = workloads.agentic(seed=7, host_cache=True, scale_lengths=1 / 400.0)
+    starts, shared = family_groups(b)
+    out, plain = _parity(pa, b, starts, shared, part)
+    assert (out.double() - plain.double()).abs().max().item() < 1e-2
+
+
+def test_fp8_groups_and_clamped_share(pa):
+    # two groups of 3 declaring 5 shared blocks and one singleton; the last member of
+    # group 1 holds only 3 full blocks, so that group's shared length is clamped to 3
+    lens = [300, 300, 300, 200, 210, 100, 77]
+    shared_map = {1: (0, 5), 2: (0, 5), 4: (3, 5), 5: (3, 3)}
+    b = workloads.build("fp8grp", 21, lens, [1] * 7, 32, 8, 128, 32, "fp8_e4m3", shared=shared_map)
+    starts = np.array([0, 3, 6, 7], np.int32)
+    shared = np.array([5, 5, 0], np.int32)
+    _parity(pa, b, starts, shared, 64)
+
+
+def test_groups_larger_than_bound_share_nothing(pa):
+    b = workloads.agentic(seed=9, host_cache=True, scale_lengths=1 / 400.0)
+    starts, shared = family_groups(b)
+    out, plain = _parity(pa, b, starts, shared, 64, max_group=4)  # families of 5 exceed the bound
+    assert torch.equal(out, plain) or (out.double() - plain.double()).abs().max().item() < 1e-2
+
+
+def test_declared_share_that_is_not_shared_is_flagged(pa):
+    b = workloads.build("liar", 23, [200, 200, 64], [1] * 3, 16, 2, 128, 16, "bf16")
+    db = DeviceBatch(b, DEV)
+    starts = np.array([0, 2, 3], np.int32)
+    shared = np.array([4, 0], np.int32)  # sequences 0 and 1 share nothing in truth
+    run_shared(pa, db, starts, shared, 4, 64)
+    assert pa.pa_get_error_flags() & pa.PA_ERRFLAG_BLOCK_TABLE
+
+
+@pytest.mark.slow
+def test_agentic_full_size_sampled(pa):
+    b = workloads.agentic()
+    starts, shared = family_groups(b)
+    db = DeviceBatch(b, DEV)
+    seqs = [b.families[0][0], b.families[1][2], b.families[2][4], b.families[3][0]]
+    outs = []
+
+    def gpu():
+        run_scatter(pa, db)
+        outs.append(run_shared(pa, db, starts, shared))
+
+    k, v, tables = sampled_oracle_inputs(db, seqs, gpu)
+    assert pa.pa_get_error_flags() == 0
+    ref = oracle.paged_decode(b.q, b.q_dtype, k, v, b.kv_dtype, tables, b.seq_lens, b.block_size, b.scale,
+                              seqs=seqs)
+    compare(outs[0], ref, b.kv_dtype, rows=seqs, where="agentic shared prefix")
