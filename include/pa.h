@@ -164,7 +164,9 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t n
  *   block_tables   int32 [num_seqs][max_blocks_per_seq]
  *   seq_lens       int32 [num_seqs], each in [1, max_seq_len]
  *   max_seq_len    host-side upper bound of seq_lens (sizes the launch)
- *   scale          softmax scale applied to q.k (e.g. 1/sqrt(head_size))
+ *   scale          softmax scale applied to q.k (e.g. 1/sqrt(head_size)); positive and
+ *                  finite, else PA_ERR_INVALID_ARG (the same for every attention call).
+ *                  FP8 scales (*k_scale, *v_scale) must be positive as well.
  *   partition_size 0 for the default, else a positive multiple of block_size
  *   workspace      device scratch of >= pa_decode_workspace_size(...) bytes,
  *                  256-byte aligned; contents need no initialisation

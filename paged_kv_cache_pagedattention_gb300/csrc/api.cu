@@ -3,6 +3,7 @@
 // optional event-based kernel tracing.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -254,18 +255,6 @@ pa_status check_attention_args(const void* out, const void* q, const void* k_cac
   return PA_OK;
 }
 
-// L2 prefetch distance (blocks beyond the shared-memory ring) of the tensor-core
-// kernels; PA_PREFETCH in the environment overrides the default (0 = off).
-int prefetch_distance() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("PA_PREFETCH");
-    v = e ? atoi(e) : 0;
-    if (v < 0) v = 0;
-  }
-  return v;
-}
-
 AttnParams base_params(void* out, const void* q, const void* k_cache, const void* v_cache, int32_t num_blocks,
                        const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
                        int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
@@ -293,7 +282,6 @@ AttnParams base_params(void* out, const void* q, const void* k_cache, const void
   p.num_head_groups = (p.group + 7) / 8;
   p.max_seq_len = max_seq_len;
   p.causal = 1;
-  p.prefetch = prefetch_distance();
   p.scale = scale;
   return p;
 }
@@ -379,6 +367,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                                       seq_lens, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size,
                                       q_dtype, kv_dtype, k_scale, v_scale, partition_size, workspace);
   if (st != PA_OK) return st;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return PA_ERR_INVALID_ARG;
   const DecodeLayout L =
       decode_layout(num_seqs, num_q_heads, head_size, max_seq_len, block_size, num_kv_heads, partition_size);
   if (workspace_bytes < L.total) return PA_ERR_WORKSPACE;
@@ -440,6 +429,7 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
                                       seq_lens, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size,
                                       q_dtype, kv_dtype, k_scale, v_scale, partition_size, workspace);
   if (st != PA_OK) return st;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return PA_ERR_INVALID_ARG;
   if (num_groups > 0 && (!group_start || !group_shared_blocks)) return PA_ERR_INVALID_ARG;
   if (max_group_size < 1 || max_group_size > 8) return PA_ERR_UNSUPPORTED;
   const bool fast = pa::decode_mma_supported(q_dtype, kv_dtype, head_size, block_size,
@@ -515,6 +505,7 @@ pa_status pa_varlen_attn(void* out, const void* q, const void* k_cache, const vo
                                       seq_lens, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size,
                                       q_dtype, kv_dtype, k_scale, v_scale, partition_size, workspace);
   if (st != PA_OK) return st;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return PA_ERR_INVALID_ARG;
   const VarlenLayout L = varlen_layout(num_seqs, total_q_tokens, num_q_heads, num_kv_heads, head_size,
                                        max_seq_len, block_size, partition_size);
   if (workspace_bytes < L.total) return PA_ERR_WORKSPACE;

@@ -20,9 +20,10 @@
 // tokens of one 16-byte column sit in eight different bank groups: the ldmatrix /
 // 16-byte shared loads below are free of bank conflicts.  Copies complete on
 // mbarrier transaction counts.  In decode_mma_kernel each warp owns a private ring
-// and its lane 0 refills a stage as soon as the warp has consumed it (optionally
-// also prefetching further blocks into L2); in shared_prefix_kernel a producer
-// warp fills a CTA ring that all member warps read (full / empty mbarriers).
+// and its lane 0 refills a stage as soon as the warp has consumed it; in
+// shared_prefix_kernel a producer warp fills a CTA ring that all member warps read
+// (full / empty mbarriers).  Whether a stage holds a valid block is recorded in
+// shared memory by the issuing lane before its mbarrier arrive.
 //
 // Math.  The query heads that share a KV head are the N = 8 columns of a warp MMA
 // m16n8k16 (grouped-query reuse: every K/V element loaded serves all of them):
@@ -177,47 +178,60 @@ __device__ __forceinline__ void attend_block(const uint8_t* tile, int rem, const
     for (int e = 0; e < 4; ++e) sc[mt][e] += sc2[e];
   }
 
-  // ---- online softmax on the accumulators (columns 2qq, 2qq+1 = heads A, B)
+  // ---- online softmax on the accumulators (columns 2qq, 2qq+1 = heads A, B).
+  // Scores stay raw here; the positive multipliers cA / cB (scale * log2 e, and
+  // k_scale for FP8) are applied inside the exponent.  The running max m is kept in
+  // scaled (log2) units and is only raised when a block's max exceeds it by more
+  // than kRescaleSlack: until then P = 2^(s*c - m) <= 2^kRescaleSlack and O, l need
+  // no rescale.  The final normalisation divides by l computed with the same m, so
+  // the result is the same softmax.
+  if (rem < BS) {  // tokens past the sequence end: raw score -inf
+#pragma unroll
+    for (int mt = 0; mt < G::kMTiles; ++mt) {
+      const int t0 = 16 * mt + (lane >> 2);
+      if (t0 >= rem) sc[mt][0] = sc[mt][1] = -INFINITY;
+      if (t0 + 8 >= rem) sc[mt][2] = sc[mt][3] = -INFINITY;
+    }
+  }
   float mxA = -INFINITY, mxB = -INFINITY;
 #pragma unroll
   for (int mt = 0; mt < G::kMTiles; ++mt) {
-    const int t0 = 16 * mt + (lane >> 2);
-    const bool v0 = t0 < rem, v1 = t0 + 8 < rem;
-    sc[mt][0] = v0 ? sc[mt][0] * cA : -INFINITY;
-    sc[mt][1] = v0 ? sc[mt][1] * cB : -INFINITY;
-    sc[mt][2] = v1 ? sc[mt][2] * cA : -INFINITY;
-    sc[mt][3] = v1 ? sc[mt][3] * cB : -INFINITY;
     mxA = fmaxf(mxA, fmaxf(sc[mt][0], sc[mt][2]));
     mxB = fmaxf(mxB, fmaxf(sc[mt][1], sc[mt][3]));
   }
-  mxA = warp_max_xor(mxA, 4, 16);
-  mxB = warp_max_xor(mxB, 4, 16);
-  const float nA = fmaxf(w.mA, mxA), nB = fmaxf(w.mB, mxB);
-  const float uA = nA == -INFINITY ? 0.f : nA, uB = nB == -INFINITY ? 0.f : nB;
-  const float alA = exp2f(w.mA - uA), alB = exp2f(w.mB - uB);
-  w.mA = nA;
-  w.mB = nB;
+  mxA = warp_max_xor(mxA, 4, 16) * cA;
+  mxB = warp_max_xor(mxB, 4, 16) * cB;
+  if (__any_sync(0xffffffffu, mxA > w.mA + kRescaleSlack || mxB > w.mB + kRescaleSlack)) {
+    const float nA = fmaxf(w.mA, mxA), nB = fmaxf(w.mB, mxB);
+    const float alA = nA == -INFINITY ? 1.f : ex2_approx(w.mA - nA);
+    const float alB = nB == -INFINITY ? 1.f : ex2_approx(w.mB - nB);
+    w.mA = nA;
+    w.mB = nB;
+    w.lA *= alA;
+    w.lB *= alB;
+#pragma unroll
+    for (int dt = 0; dt < G::kDTiles; ++dt) {
+      w.acc[dt][0] *= alA;
+      w.acc[dt][1] *= alB;
+      w.acc[dt][2] *= alA;
+      w.acc[dt][3] *= alB;
+    }
+  }
+  const float uA = w.mA == -INFINITY ? 0.f : w.mA, uB = w.mB == -INFINITY ? 0.f : w.mB;
   uint32_t pb[G::kMTiles][2];
   float addA = 0.f, addB = 0.f;
 #pragma unroll
   for (int mt = 0; mt < G::kMTiles; ++mt) {
-    const uint32_t X = pack2<MDT>(exp2f(sc[mt][0] - uA), exp2f(sc[mt][1] - uB));
-    const uint32_t Y = pack2<MDT>(exp2f(sc[mt][2] - uA), exp2f(sc[mt][3] - uB));
+    const uint32_t X = pack2<MDT>(ex2_approx(fmaf(sc[mt][0], cA, -uA)), ex2_approx(fmaf(sc[mt][1], cB, -uB)));
+    const uint32_t Y = pack2<MDT>(ex2_approx(fmaf(sc[mt][2], cA, -uA)), ex2_approx(fmaf(sc[mt][3], cB, -uB)));
     const float2 fx = unpack2<MDT>(X), fy = unpack2<MDT>(Y);
     addA += fx.x + fy.x;
     addB += fx.y + fy.y;
     pb[mt][0] = movmatrix_trans(X);
     pb[mt][1] = movmatrix_trans(Y);
   }
-  w.lA = w.lA * alA + addA;
-  w.lB = w.lB * alB + addB;
-#pragma unroll
-  for (int dt = 0; dt < G::kDTiles; ++dt) {
-    w.acc[dt][0] *= alA;
-    w.acc[dt][1] *= alB;
-    w.acc[dt][2] *= alA;
-    w.acc[dt][3] *= alB;
-  }
+  w.lA += addA;
+  w.lB += addB;
 
   // ---- O^T += V^T P^T; V tokens past the valid ones are zeroed (their P is 0,
   // their bits arbitrary)
@@ -288,7 +302,7 @@ __device__ __forceinline__ void acc_dims(int dt, int lane, int& dA, int& dB) {
 template <int KVDT, int HEAD, int BS, int NW>
 constexpr int decode_smem_bytes() {
   using G = DecodeGeom<KVDT, HEAD, BS>;
-  return NW * G::kStages * 2 * G::kTileBytes + NW * G::kStages * 8 + 1024;
+  return NW * G::kStages * 2 * G::kTileBytes + NW * G::kStages * (8 + 4) + 1024;
 }
 
 template <int QDT, int KVDT, int HEAD, int BS, int NW>
@@ -304,6 +318,7 @@ __global__ void __launch_bounds__(NW * 32)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * ST * 2 * TB);
+  int* stage_ok = reinterpret_cast<int*>(bars + NW * ST);
   __shared__ int s_failed;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -357,35 +372,36 @@ __global__ void __launch_bounds__(NW * 32)
   const int nmine = (b1 - b0 > warp) ? (b1 - b0 - warp + NW - 1) / NW : 0;
   uint8_t* ring = smem + warp * ST * 2 * TB;
   uint64_t* wbars = bars + warp * ST;
+  int* wok = stage_ok + warp * ST;
   const int tile_row0 = kvh * BS;
 
-  const int pf_dist = p.prefetch > 0 ? ST + p.prefetch : 0;
-  auto prefetch = [&](int i) {
-    const int phys = table[b0 + warp + i * NW];
-    if (phys >= 0 && phys < p.num_blocks) {
-      tma_prefetch_l2_4d(&tmk, 0, tile_row0, 0, phys);
-      tma_prefetch_l2_4d(&tmv, 0, tile_row0, 0, phys);
+  // Block-table entries of this warp's blocks, 32 at a time in registers (lane l
+  // holds the entry of the warp's block index base + l); the next window is loaded
+  // one window ahead so the issuing lane never waits on a table read.
+  auto load_window = [&](int base) {
+    const int i = base + lane;
+    return i < nmine ? table[b0 + warp + i * NW] : -1;
+  };
+  int tbl = load_window(0), tbl_next = load_window(32);
+  // Lane 0 issues the copies of the warp's block index i into stage i % ST and
+  // records in shared memory whether the block is valid (read after the wait).
+  auto issue = [&](int i, int phys) {
+    if (lane == 0) {
+      const int s = i % ST;
+      const bool valid = phys >= 0 && phys < p.num_blocks;
+      wok[s] = valid;
+      if (!valid) {
+        flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
+        mbar_arrive(wbars + s);  // completes the phase with no data; the block is skipped
+      } else {
+        uint8_t* st = ring + s * 2 * TB;
+        mbar_arrive_expect_tx(wbars + s, 2 * TB);
+        tma_load_4d(st, &tmk, 0, tile_row0, 0, phys, wbars + s);
+        tma_load_4d(st + TB, &tmv, 0, tile_row0, 0, phys, wbars + s);
+      }
     }
   };
-  auto issue = [&](int i) {
-    const int jb = b0 + warp + i * NW;
-    const int phys = table[jb];
-    uint64_t* bar = wbars + (i % ST);
-    if (phys < 0 || phys >= p.num_blocks) {
-      flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
-      mbar_arrive(bar);  // completes the phase with no data; the block is skipped
-    } else {
-      uint8_t* st = ring + (i % ST) * 2 * TB;
-      mbar_arrive_expect_tx(bar, 2 * TB);
-      tma_load_4d(st, &tmk, 0, tile_row0, 0, phys, bar);
-      tma_load_4d(st + TB, &tmv, 0, tile_row0, 0, phys, bar);
-    }
-    if (pf_dist && i + pf_dist < nmine) prefetch(i + pf_dist);
-  };
-  if (lane == 0) {
-    for (int i = ST; i < min(pf_dist, nmine); ++i) prefetch(i);
-    for (int i = 0; i < min(ST, nmine); ++i) issue(i);
-  }
+  for (int i = 0; i < min(ST, nmine); ++i) issue(i, __shfl_sync(0xffffffffu, tbl, i));
 
   uint32_t qb[G::kKSteps][2];
   float cA, cB;
@@ -403,14 +419,20 @@ __global__ void __launch_bounds__(NW * 32)
       break;
     }
     consumed = i + 1;
-    const int jb = b0 + warp + i * NW;
-    const int phys = table[jb];
-    if (phys >= 0 && phys < p.num_blocks)
+    if (wok[s]) {
+      const int jb = b0 + warp + i * NW;
       attend_block<QDT, KVDT, HEAD, BS>(ring + s * 2 * TB, seq_len - jb * BS, qb, cA, cB, w);
+    }
     __syncwarp();
-    if (i + ST < nmine && lane == 0) {
-      fence_proxy_async();
-      issue(i + ST);
+    const int j = i + ST;
+    if (j < nmine) {
+      if ((j & 31) == 0) {
+        tbl = tbl_next;
+        tbl_next = load_window(j + 32);
+      }
+      const int phys = __shfl_sync(0xffffffffu, tbl, j & 31);
+      if (lane == 0) fence_proxy_async();
+      issue(j, phys);
     }
   }
   if (failed) {
@@ -489,7 +511,7 @@ constexpr int kMaxGroup = 8;
 template <int KVDT, int HEAD, int BS>
 constexpr int shared_smem_bytes() {
   using G = DecodeGeom<KVDT, HEAD, BS>;
-  return G::kSharedStages * 2 * G::kTileBytes + 2 * G::kSharedStages * 8 + 1024;
+  return G::kSharedStages * 2 * G::kTileBytes + G::kSharedStages * (8 + 8 + 4) + 1024;
 }
 
 // grid: (group, KV head x head group, partition of the shared prefix); block: one
@@ -523,6 +545,7 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32)
   uint8_t* smem = align1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * 2 * TB);
   uint64_t* empty = full + ST;
+  int* stage_ok = reinterpret_cast<int*>(empty + ST);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmk);
@@ -550,7 +573,9 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32)
         bool same = true;  // the members' tables must name the same physical block
         for (int m = 1; m < nm; ++m)
           same &= p.block_tables[(long long)(s0 + m) * p.max_blocks_per_seq + jb] == phys;
-        if (!same || phys < 0 || phys >= p.num_blocks) {
+        const bool valid = same && phys >= 0 && phys < p.num_blocks;
+        stage_ok[s] = valid;
+        if (!valid) {
           flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
           mbar_arrive(full + s);  // empty phase: the members skip this block
         } else {
@@ -579,13 +604,7 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32)
       if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
       return;
     }
-    const int jb = b0 + i;
-    const int phys = lead[jb];
-    bool same = true;
-    for (int m = 1; m < nm; ++m)
-      same &= p.block_tables[(long long)(s0 + m) * p.max_blocks_per_seq + jb] == phys;
-    if (same && phys >= 0 && phys < p.num_blocks)
-      attend_block<QDT, KVDT, HEAD, BS>(smem + s * 2 * TB, BS, qb, cA, cB, w);
+    if (stage_ok[s]) attend_block<QDT, KVDT, HEAD, BS>(smem + s * 2 * TB, BS, qb, cA, cB, w);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + s);
   }

@@ -15,8 +15,8 @@
 // Warp roles: warps 0..7 each own 16 query rows (Q fragments and the O accumulator
 // stay in registers, FlashAttention-2 style); warp 8 produces: its lane 0 walks the
 // partition's blocks through the block table and issues TMA bulk-tensor copies of
-// the K/V tiles into a ring of stages shared by the CTA (full / empty mbarriers),
-// plus L2 prefetches further ahead.  Per 16-token block and warp:
+// the K/V tiles into a ring of stages shared by the CTA (full / empty mbarriers).
+// Per 16-token block and warp:
 //   S = Q K^T   (m16n8k16, M = 16 rows, N = 8 tokens, K = head dim)
 //   online softmax per row (running max / sum, exp2, fp32), causal mask by position
 //   O += P V    (P straight from the S accumulators as the A operand)
@@ -121,14 +121,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ph = table[kb];
         return (ph >= 0 && ph < p.num_blocks) ? ph : -1;
       };
-      const int pf_dist = p.prefetch > 0 ? ST + p.prefetch : 0;
-      for (int i = 0; i < min(pf_dist, nblocks); ++i) {
-        const int ph = phys_of(kb0 + i);
-        if (ph >= 0) {
-          tma_prefetch_l2_4d(&tmk, 0, kvh * BS, 0, ph);
-          tma_prefetch_l2_4d(&tmv, 0, kvh * BS, 0, ph);
-        }
-      }
       for (int i = 0; i < nblocks; ++i) {
         const int s = i % ST;
         if (i >= ST && !mbar_wait_bounded(empty + s, ((i / ST) - 1) & 1)) {
@@ -145,13 +137,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(full + s, 2 * TB);
           tma_load_4d(st, &tmk, 0, kvh * BS, 0, ph, full + s);
           tma_load_4d(st + TB, &tmv, 0, kvh * BS, 0, ph, full + s);
-        }
-        if (pf_dist && i + pf_dist < nblocks) {
-          const int pf = phys_of(kb0 + i + pf_dist);
-          if (pf >= 0) {
-            tma_prefetch_l2_4d(&tmk, 0, kvh * BS, 0, pf);
-            tma_prefetch_l2_4d(&tmv, 0, kvh * BS, 0, pf);
-          }
         }
       }
     }

@@ -147,15 +147,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// Hint: fetch one box of a tensor into L2 (no shared-memory destination, no completion).
-__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* map, int c0, int c1, int c2,
-                                                   int c3) {
-  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-               : "memory");
-}
-
 // Byte offset of 16-byte chunk `chunk` (0..7) of 128-byte row `row` inside a tile
 // written by TMA with CU_TENSOR_MAP_SWIZZLE_128B (tile base 1024-byte aligned).
 __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk) {
@@ -242,6 +233,17 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes), __NV_E4M3);
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
+
+// 2^x with the hardware approximation (MUFU); 2^-inf = +0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Online-softmax running max: a block whose max exceeds it by at most this much
+// (log2 units) is accumulated against the stale max without rescaling.
+constexpr float kRescaleSlack = 8.0f;
 
 __device__ __forceinline__ float warp_max_xor(float v, int lane_mask_lo, int lane_mask_hi) {
   for (int m = lane_mask_lo; m <= lane_mask_hi; m <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));

@@ -52,7 +52,6 @@ struct AttnParams {
   int num_groups;       // shared-prefix decode: number of groups (0 = no sharing)
   int max_group_size;   // shared-prefix decode: host bound on sequences per group (<= 8)
   int force_partials;   // every row writes partial states and goes through the merge
-  int prefetch;         // L2 prefetch distance of the tensor-core kernels, in blocks (0 = off)
   float scale;          // softmax scale
 };
 

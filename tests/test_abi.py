@@ -96,3 +96,14 @@ def test_host_validation_rejects_null_pointers_without_a_gpu(pa):
     # zero sequences: a no-op that succeeds before touching any pointer
     assert lib.pa_decode(None, None, None, None, 10, None, 4, None, 0, 64, 8, 2, 128, 16, 1.0, 2, 2, None, None,
                          0, None, 0, None) == pa.PA_OK
+
+
+def test_non_positive_scale_rejected_without_a_gpu(pa):
+    lib = ctypes.CDLL(pa.LIB_PATH)
+    fn = lib.pa_decode
+    fn.restype, fn.argtypes = pa.SIGNATURES["pa_decode"]
+    fake = 1 << 20  # aligned, never dereferenced: the checks return first
+    for scale in (0.0, -0.125, float("inf"), float("nan")):
+        st = fn(fake, fake, fake, fake, 10, fake, 4, fake, 2, 64, 8, 2, 128, 16, scale, 2, 2, None, None, 0,
+                fake, 1 << 30, None)
+        assert st == pa.PA_ERR_INVALID_ARG, scale
