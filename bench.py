@@ -435,8 +435,9 @@ def run_ours(args):
                                           b.block_size, part)
     groups = None if (varlen or args.no_shared_prefix) else prefix_groups(b)
     if groups is not None:
-        wsb = pa.pa_decode_shared_prefix_workspace_size(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_size,
-                                                        b.max_seq_len, b.block_size, part)
+        wsb = pa.pa_decode_shared_prefix_workspace_size(b.num_seqs, len(groups[1]), b.num_q_heads,
+                                                        b.num_kv_heads, b.head_size, b.max_seq_len,
+                                                        b.block_size, part)
         gstart = torch.from_numpy(groups[0]).to(dev)
         gshared = torch.from_numpy(groups[1]).to(dev)
         max_group = int(max(groups[0][1:] - groups[0][:-1]))

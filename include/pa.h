@@ -182,12 +182,13 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                     void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
- * Bytes of workspace pa_decode_shared_prefix needs (>= 256); partition_size as
- * for pa_decode_workspace_size.
+ * Bytes of workspace pa_decode_shared_prefix needs (>= 256) for num_groups groups;
+ * partition_size as for pa_decode_workspace_size (0: the shared prefixes get their
+ * own default partition size, sized by groups x KV heads).
  */
-size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                                              int32_t head_size, int32_t max_seq_len, int32_t block_size,
-                                              int32_t partition_size);
+size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_groups, int32_t num_q_heads,
+                                              int32_t num_kv_heads, int32_t head_size, int32_t max_seq_len,
+                                              int32_t block_size, int32_t partition_size);
 
 /*
  * pa_decode_shared_prefix -- pa_decode for batches whose sequences share prefix

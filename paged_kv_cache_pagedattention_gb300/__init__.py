@@ -48,7 +48,7 @@ SIGNATURES = {
     "pa_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "pa_decode": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
                                  _I32, _F, ctypes.c_int, ctypes.c_int, _P, _P, _I32, _P, _SZ, _P]),
-    "pa_decode_shared_prefix_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
+    "pa_decode_shared_prefix_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "pa_decode_shared_prefix": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
                                                _I32, _F, ctypes.c_int, ctypes.c_int, _P, _P, _P, _P, _I32,
                                                _I32, _I32, _P, _SZ, _P]),
@@ -156,10 +156,10 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, sca
                           _stream(stream)), "pa_decode")
 
 
-def pa_decode_shared_prefix_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size, max_seq_len,
-                                           block_size, partition_size=0) -> int:
-    return _lib.pa_decode_shared_prefix_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size,
-                                                       max_seq_len, block_size, partition_size)
+def pa_decode_shared_prefix_workspace_size(num_seqs, num_groups, num_q_heads, num_kv_heads, head_size,
+                                           max_seq_len, block_size, partition_size=0) -> int:
+    return _lib.pa_decode_shared_prefix_workspace_size(num_seqs, num_groups, num_q_heads, num_kv_heads,
+                                                       head_size, max_seq_len, block_size, partition_size)
 
 
 def pa_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, scale, workspace,

@@ -126,6 +126,30 @@ VarlenLayout varlen_layout(int num_seqs, int total_q, int hq, int hkv, int d, in
   return L;
 }
 
+// Shared-prefix decode: partitions of the shared prefixes (part_shared, sized by
+// the groups x KV heads units) followed by partitions of the private rests (part).
+struct SharedLayout {
+  int part, part_shared;
+  long long parts_shared, parts_private, parts;
+  size_t ml_off, acc_off, total;
+};
+
+SharedLayout shared_layout(int num_seqs, int num_groups, int hq, int hkv, int d, int max_seq_len, int bs,
+                           int requested) {
+  SharedLayout L;
+  L.part = resolve_partition(requested, num_seqs, hkv, max_seq_len, bs);
+  L.part_shared = requested > 0 ? L.part
+                                : resolve_partition(0, num_groups > 0 ? num_groups : 1, hkv, max_seq_len, bs);
+  L.parts_shared = ceil_div(max_seq_len, L.part_shared);
+  L.parts_private = ceil_div(max_seq_len, L.part);
+  L.parts = L.parts_shared + L.parts_private;
+  const size_t rows = (size_t)num_seqs * (size_t)L.parts;
+  L.ml_off = 256;
+  L.acc_off = L.ml_off + align256(rows * hq * sizeof(float2));
+  L.total = L.acc_off + align256(rows * hq * (size_t)d * sizeof(float));
+  return L;
+}
+
 // ------------------------------------------------------------------ tensor maps
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -283,7 +307,7 @@ AttnParams base_params(void* out, const void* q, const void* k_cache, const void
   p.max_seq_len = max_seq_len;
   p.causal = 1;
   p.scale = scale;
-  return p;
+  return p;  // part / part_pf / part_shared are set by the caller
 }
 
 }  // namespace
@@ -378,6 +402,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
   p.num_rows = num_seqs;
   p.max_query_len = 1;
   p.part = p.part_pf = L.part;
+  p.part_shared = L.part;
   p.max_partitions = static_cast<int>(L.parts);
   p.ws_ml = reinterpret_cast<float2*>(ws + L.ml_off);
   p.ws_acc = reinterpret_cast<float*>(ws + L.acc_off);
@@ -402,16 +427,13 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
   return cuda_status(e);
 }
 
-size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                                              int32_t head_size, int32_t max_seq_len, int32_t block_size,
-                                              int32_t partition_size) {
+size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_groups, int32_t num_q_heads,
+                                              int32_t num_kv_heads, int32_t head_size, int32_t max_seq_len,
+                                              int32_t block_size, int32_t partition_size) {
   if (num_seqs < 1 || num_q_heads < 1 || head_size < 1 || max_seq_len < 1 || block_size < 1) return 256;
-  DecodeLayout L = decode_layout(num_seqs, num_q_heads, head_size, max_seq_len, block_size, num_kv_heads,
-                                 partition_size);
-  // one more partition per row: the shared prefix and the private rest both round up
-  const size_t rows = (size_t)num_seqs * (size_t)(L.parts + 1);
-  return 256 + align256(rows * num_q_heads * sizeof(float2)) +
-         align256(rows * num_q_heads * (size_t)head_size * sizeof(float));
+  return shared_layout(num_seqs, num_groups, num_q_heads, num_kv_heads, head_size, max_seq_len, block_size,
+                       partition_size)
+      .total;
 }
 
 pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -432,18 +454,15 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
   if (!(scale > 0.f) || !(scale < INFINITY)) return PA_ERR_INVALID_ARG;
   if (num_groups > 0 && (!group_start || !group_shared_blocks)) return PA_ERR_INVALID_ARG;
   if (max_group_size < 1 || max_group_size > 8) return PA_ERR_UNSUPPORTED;
+  const SharedLayout L = shared_layout(num_seqs, num_groups, num_q_heads, num_kv_heads, head_size, max_seq_len,
+                                       block_size, partition_size);
+  if (workspace_bytes < L.total) return PA_ERR_WORKSPACE;
   const bool fast = pa::decode_mma_supported(q_dtype, kv_dtype, head_size, block_size,
                                              num_q_heads / num_kv_heads);
   if (!fast || num_groups == 0 || max_group_size < 2)  // nothing to share, or no tensor-core path
     return pa_decode(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                      num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, scale, q_dtype,
                      kv_dtype, k_scale, v_scale, partition_size, workspace, workspace_bytes, stream);
-  const DecodeLayout L =
-      decode_layout(num_seqs, num_q_heads, head_size, max_seq_len, block_size, num_kv_heads, partition_size);
-  const size_t rows = (size_t)num_seqs * (size_t)(L.parts + 1);
-  const size_t ml_off = 256, acc_off = ml_off + align256(rows * num_q_heads * sizeof(float2));
-  if (workspace_bytes < acc_off + align256(rows * num_q_heads * (size_t)head_size * sizeof(float)))
-    return PA_ERR_WORKSPACE;
   AttnParams p = base_params(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                              num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, scale,
                              k_scale, v_scale);
@@ -451,9 +470,10 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
   p.num_rows = num_seqs;
   p.max_query_len = 1;
   p.part = p.part_pf = L.part;
-  p.max_partitions = static_cast<int>(L.parts + 1);
-  p.ws_ml = reinterpret_cast<float2*>(ws + ml_off);
-  p.ws_acc = reinterpret_cast<float*>(ws + acc_off);
+  p.part_shared = L.part_shared;
+  p.max_partitions = static_cast<int>(L.parts);
+  p.ws_ml = reinterpret_cast<float2*>(ws + L.ml_off);
+  p.ws_acc = reinterpret_cast<float*>(ws + L.acc_off);
   p.group_start = group_start;
   p.group_shared_blocks = group_shared_blocks;
   p.num_groups = num_groups;
@@ -467,12 +487,14 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
   cudaError_t e;
   {
     TraceScope t(5, s);
-    e = pa::launch_shared_prefix(p, q_dtype, kv_dtype, static_cast<int>(L.parts), &tk, &tv, s);
+    e = kv_dtype == PA_FP8_E4M3
+            ? pa::launch_shared_prefix(p, q_dtype, kv_dtype, static_cast<int>(L.parts_shared), &tk, &tv, s)
+            : pa::launch_shared_prefix_tiles(p, q_dtype, static_cast<int>(L.parts_shared), &tk, &tv, s);
   }
   if (e != cudaSuccess) return PA_ERR_CUDA;
   {
     TraceScope t(1, s);
-    e = pa::launch_decode_mma(p, q_dtype, kv_dtype, static_cast<int>(L.parts), &tk, &tv, s);
+    e = pa::launch_decode_mma(p, q_dtype, kv_dtype, static_cast<int>(L.parts_private), &tk, &tv, s);
   }
   if (e != cudaSuccess) return PA_ERR_CUDA;
   TraceScope t(2, s);
@@ -519,6 +541,7 @@ pa_status pa_varlen_attn(void* out, const void* q, const void* k_cache, const vo
   p.max_query_len = max_query_len;
   p.part = L.part;
   p.part_pf = L.part_pf;
+  p.part_shared = L.part;
   p.max_partitions = static_cast<int>(L.parts);
   p.causal = causal ? 1 : 0;
   int32_t* work_count = reinterpret_cast<int32_t*>(ws);

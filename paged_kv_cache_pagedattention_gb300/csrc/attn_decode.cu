@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(NW * 32)
   if (b0 >= nblk) return;
   const int b1 = min(b0 + pb, nblk);
   const int nparts = (nblk - sb0 + pb - 1) / pb;
-  const int shared_parts = (start + p.part - 1) / p.part;
+  const int shared_parts = start > 0 ? (start + p.part_shared - 1) / p.part_shared : 0;
 
   if (threadIdx.x == 0) {
     s_failed = 0;
@@ -534,7 +534,7 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32)
   if (nm < 2 || nm > nwarps - 1) return;
   const int S = group_shared_tokens(p, g, s0, s1);
   if (S == 0) return;
-  const int nsb = S / BS, pb = p.part / BS;
+  const int nsb = S / BS, pb = p.part_shared / BS;
   const int b0 = z * pb;
   if (b0 >= nsb) return;
   const int nblocks = min(b0 + pb, nsb) - b0;

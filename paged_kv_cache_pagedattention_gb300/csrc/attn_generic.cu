@@ -142,7 +142,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnParams p
   if (p.force_partials) {
     // shared-prefix decode: partials of the shared prefix, then of the private rest
     const int start = shared_prefix_tokens(p, row);
-    np = (start + ri.part - 1) / ri.part + (ri.seq_len - start + ri.part - 1) / ri.part;
+    np = (start > 0 ? (start + p.part_shared - 1) / p.part_shared : 0) +
+         (ri.seq_len - start + ri.part - 1) / ri.part;
   } else if (np <= 1) {
     return;  // written directly by the attention kernel
   }

@@ -56,10 +56,136 @@ struct PrefillGeom {
   }
 };
 
+// Online-softmax state of the two query rows a thread holds in an FA2 tile
+// (warp rows lane/4 and lane/4 + 8): O accumulators over the head dim, running max
+// in log2 units, running sum.
+template <int HEAD>
+struct RowState {
+  float acc[HEAD / 8][4];
+  float m[2], l[2];
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int i = 0; i < HEAD / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+  }
+};
+
+// Raw scores S = Q K^T of one block: 16 rows x block_size keys, m16n8k16 with the
+// Q rows as A (registers) and the K tile as B (ldmatrix, conflict-free layout).
+template <int QDT, int HEAD, int BS>
+__device__ __forceinline__ void fa2_scores(uint32_t kbase, const uint32_t (&qa)[HEAD / 16][4],
+                                           float (&sc)[BS / 8][4]) {
+  using G = PrefillGeom<HEAD, BS>;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int nt = 0; nt < G::kNTok; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < G::kKSteps; ++ks) {
+#pragma unroll
+    for (int np2 = 0; np2 < G::kNTok / 2; ++np2) {
+      const int mi = lane >> 3;
+      const int tok = 16 * np2 + (lane & 7) + 8 * (mi >> 1);
+      const int chunk = 2 * ks + (mi & 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(kbase + G::off(tok, chunk), b0, b1, b2, b3);
+      mma_16816<QDT>(sc[2 * np2], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+      mma_16816<QDT>(sc[2 * np2 + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+    }
+  }
+}
+
+// Softmax and O += P V for one block.  `sc` holds raw scores, -inf where masked;
+// the positive multiplier c (scale * log2 e) is applied inside the exponent.  The
+// running max is raised only when a block exceeds it by more than kRescaleSlack
+// (then O and l are rescaled); P feeds the PV MMA straight from the S registers.
+// V tokens at or past `rem` are zeroed (their P is 0, their bits arbitrary).
+template <int QDT, int HEAD, int BS>
+__device__ __forceinline__ void fa2_softmax_pv(uint32_t vbase, float (&sc)[BS / 8][4], float c, int rem,
+                                               RowState<HEAD>& st) {
+  using G = PrefillGeom<HEAD, BS>;
+  const int lane = threadIdx.x & 31;
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int nt = 0; nt < G::kNTok; ++nt) {
+    mx[0] = fmaxf(mx[0], fmaxf(sc[nt][0], sc[nt][1]));
+    mx[1] = fmaxf(mx[1], fmaxf(sc[nt][2], sc[nt][3]));
+  }
+  mx[0] = warp_max_xor(mx[0], 1, 2) * c;
+  mx[1] = warp_max_xor(mx[1], 1, 2) * c;
+  if (__any_sync(0xffffffffu, mx[0] > st.m[0] + kRescaleSlack || mx[1] > st.m[1] + kRescaleSlack)) {
+    float al[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float nm = fmaxf(st.m[h], mx[h]);
+      al[h] = nm == -INFINITY ? 1.f : ex2_approx(st.m[h] - nm);
+      st.m[h] = nm;
+      st.l[h] *= al[h];
+    }
+#pragma unroll
+    for (int dn = 0; dn < G::kNDim; ++dn) {
+      st.acc[dn][0] *= al[0];
+      st.acc[dn][1] *= al[0];
+      st.acc[dn][2] *= al[1];
+      st.acc[dn][3] *= al[1];
+    }
+  }
+  const float u0 = st.m[0] == -INFINITY ? 0.f : st.m[0], u1 = st.m[1] == -INFINITY ? 0.f : st.m[1];
+  uint32_t pa[G::kNTok][2];
+  float add0 = 0.f, add1 = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < G::kNTok; ++nt) {
+    pa[nt][0] = pack2<QDT>(ex2_approx(fmaf(sc[nt][0], c, -u0)), ex2_approx(fmaf(sc[nt][1], c, -u0)));
+    pa[nt][1] = pack2<QDT>(ex2_approx(fmaf(sc[nt][2], c, -u1)), ex2_approx(fmaf(sc[nt][3], c, -u1)));
+    const float2 f0 = unpack2<QDT>(pa[nt][0]), f1 = unpack2<QDT>(pa[nt][1]);
+    add0 += f0.x + f0.y;
+    add1 += f1.x + f1.y;
+  }
+  st.l[0] += add0;
+  st.l[1] += add1;
+#pragma unroll
+  for (int kt = 0; kt < BS / 16; ++kt) {
+    const int tk = 16 * kt + 2 * (lane & 3);
+    const bool tail = rem < 16 * kt + 16;
+    const uint32_t m01 = (tk < rem ? 0xffffu : 0u) | (tk + 1 < rem ? 0xffff0000u : 0u);
+    const uint32_t m23 = (tk + 8 < rem ? 0xffffu : 0u) | (tk + 9 < rem ? 0xffff0000u : 0u);
+#pragma unroll
+    for (int dp = 0; dp < G::kNDim / 2; ++dp) {
+      const int mi = lane >> 3;
+      const int tok = 16 * kt + (lane & 7) + 8 * (mi & 1);
+      const int chunk = 2 * dp + (mi >> 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_trans(vbase + G::off(tok, chunk), b0, b1, b2, b3);
+      if (tail) {
+        b0 &= m01;
+        b1 &= m23;
+        b2 &= m01;
+        b3 &= m23;
+      }
+      mma_16816<QDT>(st.acc[2 * dp], pa[2 * kt][0], pa[2 * kt][1], pa[2 * kt + 1][0], pa[2 * kt + 1][1], b0, b1);
+      mma_16816<QDT>(st.acc[2 * dp + 1], pa[2 * kt][0], pa[2 * kt][1], pa[2 * kt + 1][0], pa[2 * kt + 1][1], b2,
+                     b3);
+    }
+  }
+}
+
+// A-operand fragments of two query rows (zero when the row pointer is null).
+template <int HEAD>
+__device__ __forceinline__ void load_query_rows(const uint32_t* q0, const uint32_t* q1, uint32_t (&qa)[HEAD / 16][4]) {
+  const int qq = threadIdx.x & 3;
+#pragma unroll
+  for (int ks = 0; ks < HEAD / 16; ++ks) {
+    qa[ks][0] = q0 ? q0[8 * ks + qq] : 0u;
+    qa[ks][1] = q1 ? q1[8 * ks + qq] : 0u;
+    qa[ks][2] = q0 ? q0[8 * ks + 4 + qq] : 0u;
+    qa[ks][3] = q1 ? q1[8 * ks + 4 + qq] : 0u;
+  }
+}
+
 template <int HEAD, int BS>
 constexpr int prefill_smem_bytes() {
   using G = PrefillGeom<HEAD, BS>;
-  return G::kStages * 2 * G::kTileBytes + 2 * G::kStages * 8 + 1024;
+  return G::kStages * 2 * G::kTileBytes + G::kStages * (8 + 8 + 4) + 1024;
 }
 
 template <int QDT, int HEAD, int BS>
@@ -98,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = align1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * 2 * TB);
   uint64_t* empty = full + ST;
+  int* stage_ok = reinterpret_cast<int*>(empty + ST);
   __shared__ int s_failed;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -129,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const int ph = phys_of(kb0 + i);
+        stage_ok[s] = ph >= 0;
         if (ph < 0) {
           flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
           mbar_arrive(full + s);
@@ -170,20 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                               reinterpret_cast<const typename QE::T*>(p.q) +
                               ((long long)(row0 + rt[h]) * p.num_q_heads + h0 + rn[h]) * HEAD)
                         : nullptr;
-    const int qq = lane & 3;
-#pragma unroll
-    for (int ks = 0; ks < G::kKSteps; ++ks) {
-      qa[ks][0] = qw[0] ? qw[0][8 * ks + qq] : 0u;
-      qa[ks][1] = qw[1] ? qw[1][8 * ks + qq] : 0u;
-      qa[ks][2] = qw[0] ? qw[0][8 * ks + 4 + qq] : 0u;
-      qa[ks][3] = qw[1] ? qw[1][8 * ks + 4 + qq] : 0u;
-    }
+    load_query_rows<HEAD>(qw[0], qw[1], qa);
   }
   const float c = p.scale * kLog2e;
-  float acc[G::kNDim][4];
-#pragma unroll
-  for (int i = 0; i < G::kNDim; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  RowState<HEAD> st;
+  st.init();
 
   for (int i = 0; i < nblocks; ++i) {
     const int s = i % ST;
@@ -195,99 +314,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       break;
     }
-    const int kb = kb0 + i;
-    const int ph = table[kb];
-    const int kbase_tok = kb * BS;
+    const int kbase_tok = (kb0 + i) * BS;
     // skip blocks that no row of this warp can see (all keys after its last position)
-    const bool useful = warp_active && (ph >= 0 && ph < p.num_blocks) &&
-                        (!p.causal || kbase_tok <= warp_last_pos);
+    const bool useful = warp_active && stage_ok[s] && (!p.causal || kbase_tok <= warp_last_pos);
     if (useful) {
       const uint32_t kbase = smem_u32(smem + s * 2 * TB);
-      const uint32_t vbase = kbase + TB;
-      // ---- S = Q K^T over this block's tokens
       float sc[G::kNTok][4];
+      fa2_scores<QDT, HEAD, BS>(kbase, qa, sc);
+      // mask keys outside [k0, k1) of this partition, past seq_len, or after the row's
+      // position (causal); only blocks that reach such keys pay for the test
+      const bool edge = kbase_tok < k0 || kbase_tok + BS > k1 || kbase_tok + BS > seq_len ||
+                        (p.causal && kbase_tok + BS - 1 > pos0 + (16 * warp) / gp);
+      if (__any_sync(0xffffffffu, edge || !rvalid[0] || !rvalid[1])) {
 #pragma unroll
-      for (int nt = 0; nt < G::kNTok; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        for (int nt = 0; nt < G::kNTok; ++nt) {
+          const int key = kbase_tok + 8 * nt + 2 * (lane & 3);
 #pragma unroll
-      for (int ks = 0; ks < G::kKSteps; ++ks) {
-#pragma unroll
-        for (int np2 = 0; np2 < G::kNTok / 2; ++np2) {
-          const int mi = lane >> 3;
-          const int tok = 16 * np2 + (lane & 7) + 8 * (mi >> 1);
-          const int chunk = 2 * ks + (mi & 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kbase + G::off(tok, chunk), b0, b1, b2, b3);
-          mma_16816<QDT>(sc[2 * np2], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-          mma_16816<QDT>(sc[2 * np2 + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-        }
-      }
-      // ---- mask, scale, online softmax (rows h = 0: c0,c1; h = 1: c2,c3)
-      float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-      for (int nt = 0; nt < G::kNTok; ++nt) {
-        const int key = kbase_tok + 8 * nt + 2 * (lane & 3);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int h = e >> 1;
-          const int k = key + (e & 1);
-          const bool ok = rvalid[h] && k < seq_len && k >= k0 && k < k1 && (!p.causal || k <= rpos[h]);
-          sc[nt][e] = ok ? sc[nt][e] * c : -INFINITY;
-          mx[h] = fmaxf(mx[h], sc[nt][e]);
-        }
-      }
-      float alpha[2], use[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        mx[h] = warp_max_xor(mx[h], 1, 2);
-        const float nm = fmaxf(m[h], mx[h]);
-        use[h] = nm == -INFINITY ? 0.f : nm;
-        alpha[h] = exp2f(m[h] - use[h]);
-        m[h] = nm;
-      }
-      uint32_t pa[G::kNTok][2];
-      float add[2] = {0.f, 0.f};
-#pragma unroll
-      for (int nt = 0; nt < G::kNTok; ++nt) {
-        pa[nt][0] = pack2<QDT>(exp2f(sc[nt][0] - use[0]), exp2f(sc[nt][1] - use[0]));
-        pa[nt][1] = pack2<QDT>(exp2f(sc[nt][2] - use[1]), exp2f(sc[nt][3] - use[1]));
-        const float2 f0 = unpack2<QDT>(pa[nt][0]), f1 = unpack2<QDT>(pa[nt][1]);
-        add[0] += f0.x + f0.y;
-        add[1] += f1.x + f1.y;
-      }
-      l[0] = l[0] * alpha[0] + add[0];
-      l[1] = l[1] * alpha[1] + add[1];
-#pragma unroll
-      for (int dn = 0; dn < G::kNDim; ++dn) {
-        acc[dn][0] *= alpha[0];
-        acc[dn][1] *= alpha[0];
-        acc[dn][2] *= alpha[1];
-        acc[dn][3] *= alpha[1];
-      }
-      // ---- O += P V; V tokens past seq_len are zeroed (their P is 0, their bits arbitrary)
-      const int rem = seq_len - kbase_tok;
-#pragma unroll
-      for (int kt = 0; kt < BS / 16; ++kt) {
-        const int tk = 16 * kt + 2 * (lane & 3);
-        const uint32_t m01 = (tk < rem ? 0xffffu : 0u) | (tk + 1 < rem ? 0xffff0000u : 0u);
-        const uint32_t m23 = (tk + 8 < rem ? 0xffffu : 0u) | (tk + 9 < rem ? 0xffff0000u : 0u);
-        const bool tail = rem < 16 * kt + 16;
-#pragma unroll
-        for (int dp = 0; dp < G::kNDim / 2; ++dp) {
-          const int mi = lane >> 3;
-          const int tok = 16 * kt + (lane & 7) + 8 * (mi & 1);
-          const int chunk = 2 * dp + (mi >> 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_trans(vbase + G::off(tok, chunk), b0, b1, b2, b3);
-          if (tail) {
-            b0 &= m01;
-            b1 &= m23;
-            b2 &= m01;
-            b3 &= m23;
+          for (int e = 0; e < 4; ++e) {
+            const int h = e >> 1;
+            const int k = key + (e & 1);
+            const bool ok = rvalid[h] && k < seq_len && k >= k0 && k < k1 && (!p.causal || k <= rpos[h]);
+            if (!ok) sc[nt][e] = -INFINITY;
           }
-          mma_16816<QDT>(acc[2 * dp], pa[2 * kt][0], pa[2 * kt][1], pa[2 * kt + 1][0], pa[2 * kt + 1][1], b0, b1);
-          mma_16816<QDT>(acc[2 * dp + 1], pa[2 * kt][0], pa[2 * kt][1], pa[2 * kt + 1][0], pa[2 * kt + 1][1], b2, b3);
         }
       }
+      fa2_softmax_pv<QDT, HEAD, BS>(kbase + TB, sc, c, seq_len - kbase_tok, st);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + s);
@@ -297,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- epilogue: each thread writes its two rows' columns
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    l[h] = warp_sum_xor(l[h], 1, 2);
+    st.l[h] = warp_sum_xor(st.l[h], 1, 2);
     if (!rvalid[h]) continue;
     const int kv_len = p.causal ? rpos[h] + 1 : seq_len;
     const int parts_row = (kv_len + part - 1) / part;
@@ -306,11 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int head = h0 + rn[h];
     const int dcol = 2 * (lane & 3);
     if (parts_row == 1) {
-      const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
+      const float inv = st.l[h] > 0.f ? 1.f / st.l[h] : 0.f;
       typename QE::T* o = reinterpret_cast<typename QE::T*>(p.out) + ((long long)(qs + t) * p.num_q_heads + head) * HEAD;
 #pragma unroll
       for (int dn = 0; dn < G::kNDim; ++dn) {
-        const uint32_t v = pack2<QDT>(acc[dn][2 * h] * inv, acc[dn][2 * h + 1] * inv);
+        const uint32_t v = pack2<QDT>(st.acc[dn][2 * h] * inv, st.acc[dn][2 * h + 1] * inv);
         *reinterpret_cast<uint32_t*>(o + 8 * dn + dcol) = v;
       }
     } else {
@@ -318,10 +369,178 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* wa = p.ws_acc + (pi * p.num_q_heads + head) * HEAD;
 #pragma unroll
       for (int dn = 0; dn < G::kNDim; ++dn)
-        *reinterpret_cast<float2*>(wa + 8 * dn + dcol) = make_float2(acc[dn][2 * h], acc[dn][2 * h + 1]);
-      if ((lane & 3) == 0) p.ws_ml[pi * p.num_q_heads + head] = make_float2(m[h], l[h]);
+        *reinterpret_cast<float2*>(wa + 8 * dn + dcol) = make_float2(st.acc[dn][2 * h], st.acc[dn][2 * h + 1]);
+      if ((lane & 3) == 0) p.ws_ml[pi * p.num_q_heads + head] = make_float2(st.m[h], st.l[h]);
     }
   }
+}
+
+// Shared-prefix tiles.  [AGENTIC] "統一分頁 + 共用池": forked sequences point at
+// the same physical blocks.  One CTA handles (group of sequences sharing leading
+// blocks, KV head, head group, partition of the shared prefix); its query rows are
+// the (member, head) pairs of the group, member-major (row = member * GP + head),
+// so every shared K/V tile is loaded once and serves every member's heads.  All
+// shared keys precede every member's query position: no mask.  Each row writes a
+// partial state at its sequence's shared partition z; the members' private tokens
+// are attended by the decode kernel and the merge combines both.
+template <int QDT, int HEAD, int BS>
+__global__ void __launch_bounds__(kThreads, 1)
+    shared_prefix_tile_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                              const __grid_constant__ CUtensorMap tmv) {
+  using G = PrefillGeom<HEAD, BS>;
+  constexpr int ST = G::kStages;
+  constexpr int TB = G::kTileBytes;
+
+  const int g = blockIdx.x;
+  const int kvh = blockIdx.y / p.num_head_groups, hg = blockIdx.y % p.num_head_groups;
+  const int z = blockIdx.z;
+  const int s0 = p.group_start[g], s1 = p.group_start[g + 1];
+  const int nm = s1 - s0;
+  const int nwc = (int)(blockDim.x >> 5) - 1;  // consumer warps
+  int gp = 1;
+  while (gp < min(p.group, 8)) gp <<= 1;
+  if (nm < 2 || nm * gp > 16 * nwc) return;
+  const int S = group_shared_tokens(p, g, s0, s1);
+  if (S == 0) return;
+  const int pb = p.part_shared / BS, nsb = S / BS;
+  const int b0 = z * pb;
+  if (b0 >= nsb) return;
+  const int nblocks = min(b0 + pb, nsb) - b0;
+  const int h0 = kvh * p.group + hg * 8;
+  const int nh = min(8, p.group - hg * 8);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * 2 * TB);
+  uint64_t* empty = full + ST;
+  int* stage_ok = reinterpret_cast<int*>(empty + ST);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+    for (int i = 0; i < ST; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, nwc);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int32_t* lead = p.block_tables + (long long)s0 * p.max_blocks_per_seq;
+
+  if (warp == nwc) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      for (int i = 0; i < nblocks; ++i) {
+        const int s = i % ST;
+        if (i >= ST && !mbar_wait_bounded(empty + s, ((i / ST) - 1) & 1)) {
+          flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+          break;  // the consumers time out on the full barrier and write nothing
+        }
+        const int jb = b0 + i;
+        const int phys = lead[jb];
+        bool same = true;  // every member's table must name the same physical block
+        for (int m = 1; m < nm; ++m)
+          same &= p.block_tables[(long long)(s0 + m) * p.max_blocks_per_seq + jb] == phys;
+        const bool valid = same && phys >= 0 && phys < p.num_blocks;
+        stage_ok[s] = valid;
+        if (!valid) {
+          flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
+          mbar_arrive(full + s);  // empty phase: the block is skipped for the whole group
+        } else {
+          uint8_t* st = smem + s * 2 * TB;
+          mbar_arrive_expect_tx(full + s, 2 * TB);
+          tma_load_4d(st, &tmk, 0, kvh * BS, 0, phys, full + s);
+          tma_load_4d(st + TB, &tmv, 0, kvh * BS, 0, phys, full + s);
+        }
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  int rm[2], rn[2];
+  bool rvalid[2];
+  const uint32_t* qw[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int rho = 16 * warp + (lane >> 2) + 8 * h;
+    rm[h] = rho / gp;
+    rn[h] = rho % gp;
+    rvalid[h] = rm[h] < nm && rn[h] < nh;
+    qw[h] = rvalid[h] ? reinterpret_cast<const uint32_t*>(
+                            reinterpret_cast<const typename Elem<QDT>::T*>(p.q) +
+                            ((long long)(s0 + rm[h]) * p.num_q_heads + h0 + rn[h]) * HEAD)
+                      : nullptr;
+  }
+  const bool warp_active = (16 * warp) / gp < nm;
+  const bool all_valid = __all_sync(0xffffffffu, rvalid[0] && rvalid[1]);
+  uint32_t qa[G::kKSteps][4];
+  load_query_rows<HEAD>(qw[0], qw[1], qa);
+  const float c = p.scale * kLog2e;
+  RowState<HEAD> st;
+  st.init();
+  for (int i = 0; i < nblocks; ++i) {
+    const int s = i % ST;
+    const bool got = mbar_wait_bounded(full + s, (i / ST) & 1);
+    if (!__all_sync(0xffffffffu, got)) {
+      if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+      return;
+    }
+    if (warp_active && stage_ok[s]) {
+      const uint32_t kbase = smem_u32(smem + s * 2 * TB);
+      float sc[G::kNTok][4];
+      fa2_scores<QDT, HEAD, BS>(kbase, qa, sc);
+      if (!all_valid) {  // padding rows (no member / head) take no part
+#pragma unroll
+        for (int nt = 0; nt < G::kNTok; ++nt) {
+          if (!rvalid[0]) sc[nt][0] = sc[nt][1] = -INFINITY;
+          if (!rvalid[1]) sc[nt][2] = sc[nt][3] = -INFINITY;
+        }
+      }
+      fa2_softmax_pv<QDT, HEAD, BS>(kbase + TB, sc, c, BS, st);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty + s);
+  }
+
+  // ---- each valid row's partial state for shared partition z
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    st.l[h] = warp_sum_xor(st.l[h], 1, 2);
+    if (!rvalid[h]) continue;
+    const long long pi = (long long)(s0 + rm[h]) * p.max_partitions + z;
+    const int head = h0 + rn[h];
+    float* wa = p.ws_acc + (pi * p.num_q_heads + head) * HEAD;
+    const int dcol = 2 * (lane & 3);
+#pragma unroll
+    for (int dn = 0; dn < G::kNDim; ++dn)
+      *reinterpret_cast<float2*>(wa + 8 * dn + dcol) = make_float2(st.acc[dn][2 * h], st.acc[dn][2 * h + 1]);
+    if ((lane & 3) == 0) p.ws_ml[pi * p.num_q_heads + head] = make_float2(st.m[h], st.l[h]);
+  }
+}
+
+template <int QDT, int HEAD, int BS>
+cudaError_t launch_shared_t(const AttnParams& p, int grid_z, const CUtensorMap* tk, const CUtensorMap* tv,
+                            cudaStream_t stream) {
+  constexpr int smem = prefill_smem_bytes<HEAD, BS>();
+  auto kern = shared_prefix_tile_kernel<QDT, HEAD, BS>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();  // consume it: the caller reports the failure
+      return e;
+    }
+    configured_device = dev;
+  }
+  int gp = 1;
+  while (gp < (p.group < 8 ? p.group : 8)) gp <<= 1;
+  const int nwc = (p.max_group_size * gp + 15) / 16;
+  dim3 grid(p.num_groups, p.num_kv_heads * p.num_head_groups, grid_z);
+  kern<<<grid, (nwc + 1) * 32, smem, stream>>>(p, *tk, *tv);
+  return cudaGetLastError();
 }
 
 template <int QDT, int HEAD, int BS>
@@ -357,6 +576,24 @@ cudaError_t launch_shape(const AttnParams& p, int num_items, const CUtensorMap* 
 }
 
 }  // namespace
+
+cudaError_t launch_shared_prefix_tiles(const AttnParams& p, int q_dtype, int grid_z, const CUtensorMap* tk,
+                                       const CUtensorMap* tv, cudaStream_t s) {
+  const int d = p.head_size, bs = p.block_size;
+  if (p.max_group_size < 2 || p.max_group_size > 8 || p.num_groups <= 0) return cudaErrorInvalidValue;
+#define PA_SHAPE(Q, D, B) \
+  if (q_dtype == Q && d == D && bs == B) return launch_shared_t<Q, D, B>(p, grid_z, tk, tv, s);
+  PA_SHAPE(PA_BF16, 128, 16)
+  PA_SHAPE(PA_BF16, 128, 32)
+  PA_SHAPE(PA_BF16, 64, 16)
+  PA_SHAPE(PA_BF16, 64, 32)
+  PA_SHAPE(PA_F16, 128, 16)
+  PA_SHAPE(PA_F16, 128, 32)
+  PA_SHAPE(PA_F16, 64, 16)
+  PA_SHAPE(PA_F16, 64, 32)
+#undef PA_SHAPE
+  return cudaErrorInvalidValue;
+}
 
 bool prefill_mma_supported(int q_dtype, int kv_dtype, int head_size, int block_size, int group) {
   (void)group;

@@ -47,6 +47,7 @@ struct AttnParams {
   int max_query_len;
   int part;             // partition tokens for rows of single-token requests
   int part_pf;          // partition tokens for rows of multi-token requests
+  int part_shared;      // partition tokens of a group's shared prefix (shared-prefix decode)
   int max_partitions;   // decode mode: partial rows reserved per query row
   int causal;
   int num_groups;       // shared-prefix decode: number of groups (0 = no sharing)
@@ -90,6 +91,10 @@ cudaError_t launch_decode_mma(const AttnParams& p, int q_dtype, int kv_dtype, in
 cudaError_t launch_shared_prefix(const AttnParams& p, int q_dtype, int kv_dtype, int grid_z,
                                  const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
                                  cudaStream_t stream);
+
+cudaError_t launch_shared_prefix_tiles(const AttnParams& p, int q_dtype, int grid_z,
+                                       const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                                       cudaStream_t stream);
 
 bool prefill_mma_supported(int q_dtype, int kv_dtype, int head_size, int block_size, int group);
 cudaError_t launch_prefill_mma(const AttnParams& p, int q_dtype, int kv_dtype, int num_ctas,

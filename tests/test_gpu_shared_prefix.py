@@ -34,7 +34,8 @@ def run_shared(pa, db, starts, shared, max_group=8, partition_size=0):
     b = db.b
     out = torch.empty_like(db.q)
     ws = pa.workspace_tensor(pa.pa_decode_shared_prefix_workspace_size(
-        b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_size, b.max_seq_len, b.block_size, partition_size), DEV)
+        b.num_seqs, len(shared), b.num_q_heads, b.num_kv_heads, b.head_size, b.max_seq_len, b.block_size,
+        partition_size), DEV)
     pa.pa_decode_shared_prefix(out, db.q, db.kc, db.vc, db.tables, db.lens, b.max_seq_len, b.scale, ws,
                                torch.from_numpy(starts).to(DEV), torch.from_numpy(shared).to(DEV), max_group,
                                db.k_scale, db.v_scale, partition_size)
