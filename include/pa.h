@@ -213,6 +213,11 @@ size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_grou
  * declared to share sets PA_ERRFLAG_BLOCK_TABLE and that block is skipped for the
  * whole group.  Without a tensor-core path for the dtypes/shape (or with no groups)
  * this is exactly pa_decode (with a workspace of the size above).
+ * The shared-prefix and private-remainder kernels run at once: the call forks a
+ * second stream of its own (created on the device's first call, with two events;
+ * make that first call before any CUDA stream capture) and joins it back into
+ * `stream` before the merge.  Calls from several host threads are serialised
+ * around that fork / join.
  */
 pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const void* v_cache,
                                   int32_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -313,7 +318,9 @@ pa_status pa_get_error_flags(uint32_t* flags, int32_t clear, pa_stream_t stream)
  * bracketed by CUDA events recorded on its launch stream.  pa_trace_read()
  * synchronises those events and, for kernel kind `kind` (0 = reshape_and_cache,
  * 1 = attention main kernel, 2 = partial merge, 3 = varlen plan,
- * 4 = prefill tiles), returns the launch count and the summed device
+ * 4 = prefill tiles, 5 = shared-prefix tiles, 6 = the span of the shared-prefix
+ * and private-remainder kernels of pa_decode_shared_prefix), returns the launch
+ * count and the summed device
  * milliseconds since the last reset (reset != 0 clears every kind).
  * Tracing is off by default and costs nothing when off.  Not thread-safe.
  */

@@ -35,7 +35,8 @@ PA_ERRFLAG_BLOCK_TABLE, PA_ERRFLAG_SLOT, PA_ERRFLAG_SEQ_LEN, PA_ERRFLAG_QUERY, P
     0x1, 0x2, 0x4, 0x8, 0x10
 
 # Names of the kernel kinds reported by pa_trace_read.
-TRACE_KINDS = ("reshape_and_cache", "attention", "merge", "varlen_plan", "prefill_tiles", "shared_prefix")
+TRACE_KINDS = ("reshape_and_cache", "attention", "merge", "varlen_plan", "prefill_tiles", "shared_prefix",
+               "shared_span")
 
 # Every symbol include/pa.h declares, with its ctypes signature.
 _P, _I32, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float

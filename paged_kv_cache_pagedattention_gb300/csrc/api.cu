@@ -8,6 +8,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
 #include <vector>
 
 #include "pa_internal.h"
@@ -194,7 +195,7 @@ bool encode_cache_map(CUtensorMap* m, const void* base, int kv_dtype, int num_bl
 
 // ------------------------------------------------------------------ tracing
 
-constexpr int kTraceKinds = 6;
+constexpr int kTraceKinds = 7;
 bool g_trace_on = false;
 struct TraceSlot {
   int kind;
@@ -250,6 +251,35 @@ void collect_trace() {
     g_event_pool.push_back(t.b);
   }
   g_pending.clear();
+}
+
+// A second stream per device, created on first use, onto which the shared-prefix
+// decode forks its private-remainder kernel so both run at once; joined back with
+// events before the merge.  Guarded by a mutex: the fork / join pair must not
+// interleave between host threads.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool failed = false;
+};
+std::mutex g_side_mutex;
+SideStream g_side[kMaxDevices];
+
+SideStream* side_stream() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  SideStream& sd = g_side[dev];
+  if (sd.failed) return nullptr;
+  if (!sd.stream) {
+    if (cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) {
+      (void)cudaGetLastError();
+      sd.failed = true;
+      return nullptr;
+    }
+  }
+  return &sd;
 }
 
 pa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
@@ -484,17 +514,29 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
       !encode_cache_map(&tv, v_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size))
     return PA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
+  cudaError_t e = cudaSuccess;
   {
-    TraceScope t(5, s);
-    e = kv_dtype == PA_FP8_E4M3
-            ? pa::launch_shared_prefix(p, q_dtype, kv_dtype, static_cast<int>(L.parts_shared), &tk, &tv, s)
-            : pa::launch_shared_prefix_tiles(p, q_dtype, static_cast<int>(L.parts_shared), &tk, &tv, s);
-  }
-  if (e != cudaSuccess) return PA_ERR_CUDA;
-  {
-    TraceScope t(1, s);
-    e = pa::launch_decode_mma(p, q_dtype, kv_dtype, static_cast<int>(L.parts_private), &tk, &tv, s);
+    std::lock_guard<std::mutex> lock(g_side_mutex);
+    SideStream* side = side_stream();
+    TraceScope span(6, s);  // shared prefixes and private rests together
+    cudaStream_t s2 = s;
+    if (side && cudaEventRecord(side->fork, s) == cudaSuccess &&
+        cudaStreamWaitEvent(side->stream, side->fork, 0) == cudaSuccess)
+      s2 = side->stream;
+    {
+      TraceScope t(5, s);
+      e = kv_dtype == PA_FP8_E4M3
+              ? pa::launch_shared_prefix(p, q_dtype, kv_dtype, static_cast<int>(L.parts_shared), &tk, &tv, s)
+              : pa::launch_shared_prefix_tiles(p, q_dtype, static_cast<int>(L.parts_shared), &tk, &tv, s);
+    }
+    if (e == cudaSuccess) {
+      TraceScope t(1, s2);
+      e = pa::launch_decode_mma(p, q_dtype, kv_dtype, static_cast<int>(L.parts_private), &tk, &tv, s2);
+    }
+    if (s2 != s) {  // join, even after a failed launch, so the caller's stream stays ordered
+      if (cudaEventRecord(side->join, s2) != cudaSuccess || cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess)
+        e = cudaErrorUnknown;
+    }
   }
   if (e != cudaSuccess) return PA_ERR_CUDA;
   TraceScope t(2, s);

@@ -109,33 +109,32 @@ __global__ void __launch_bounds__(128)
   }
 }
 
-// One CTA per (row, head): out = sum_j acc_j * 2^(m_j - M) / sum_j l_j * 2^(m_j - M)
-// with M = max_j m_j.  The per-partition factors are computed once into shared
-// memory; then each thread owns output dimensions and streams the partials with
-// independent, coalesced loads.
+// One warp per (row, head), four per CTA: out = sum_j acc_j * 2^(m_j - M) /
+// sum_j l_j * 2^(m_j - M) with M = max_j m_j.  (M, L) come from one pass over the
+// partial states with an online combine; then each lane owns four output
+// dimensions and streams the partials with 16-byte loads, eight in flight.
 constexpr int kMergeThreads = 128;
-constexpr int kMergeChunk = 512;
 
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
-  v = is_max ? warp_max_xor(v, 1, 16) : warp_sum_xor(v, 1, 16);
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  if (lane == 0) red[wid] = v;
-  __syncthreads();
-  float r = red[0];
-  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
-  __syncthreads();
-  return r;
+__device__ __forceinline__ void combine_ml(float& m, float& l, float m2, float l2) {
+  if (l2 <= 0.f) return;
+  if (l <= 0.f) {
+    m = m2;
+    l = l2;
+    return;
+  }
+  const float nm = fmaxf(m, m2);
+  l = l * exp2f(m - nm) + l2 * exp2f(m2 - nm);
+  m = nm;
 }
 
 template <int QDT>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnParams p) {
   using QE = Elem<QDT>;
-  __shared__ float wts[kMergeChunk];
-  __shared__ float red[kMergeThreads / 32];
-  const long long gid = blockIdx.x;
-  const int row = static_cast<int>(gid / p.num_q_heads);
-  const int head = static_cast<int>(gid % p.num_q_heads);
-  if (row >= p.num_rows || plan_rejected(p)) return;
+  const int lane = threadIdx.x & 31;
+  const long long gw = (long long)blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);
+  if (gw >= (long long)p.num_rows * p.num_q_heads || plan_rejected(p)) return;
+  const int row = static_cast<int>(gw / p.num_q_heads);
+  const int head = static_cast<int>(gw % p.num_q_heads);
   const RowInfo ri = row_info(p, row);
   if (!ri.ok) return;
   int np = ri.parts_row;
@@ -149,43 +148,160 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnParams p
   }
   const long long base = row_partial_base(p, ri, row);
   const int hq = p.num_q_heads, d = p.head_size;
-  float M = -INFINITY;
-  for (int j = threadIdx.x; j < np; j += blockDim.x) {
-    const float2 ml = p.ws_ml[(base + j) * hq + head];
-    if (ml.y > 0.f) M = fmaxf(M, ml.x);
+  const float2* ml = p.ws_ml + base * hq + head;  // partial j at ml[j * hq]
+  float M = -INFINITY, L = 0.f;
+  for (int j = lane; j < np; j += 32) {
+    const float2 v = ml[(long long)j * hq];
+    combine_ml(M, L, v.x, v.y);
   }
-  M = block_reduce(M, true, red);
-  float L = 0.f;
-  for (int j = threadIdx.x; j < np; j += blockDim.x) {
-    const float2 ml = p.ws_ml[(base + j) * hq + head];
-    if (ml.y > 0.f) L += ml.y * exp2f(ml.x - M);
+  for (int o = 16; o >= 1; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, M, o), l2 = __shfl_xor_sync(0xffffffffu, L, o);
+    combine_ml(M, L, m2, l2);
   }
-  L = block_reduce(L, false, red);
   const float inv = L > 0.f ? 1.f / L : 0.f;
   typename QE::T* out = reinterpret_cast<typename QE::T*>(p.out) + ((long long)row * hq + head) * d;
-  for (int d0 = 0; d0 < d; d0 += blockDim.x) {
-    const int dd = d0 + threadIdx.x;
-    float o0 = 0.f, o1 = 0.f;
-    for (int c0 = 0; c0 < np; c0 += kMergeChunk) {
-      const int n = min(kMergeChunk, np - c0);
-      __syncthreads();
-      for (int j = threadIdx.x; j < n; j += blockDim.x) {
-        const float2 ml = p.ws_ml[(base + c0 + j) * hq + head];
-        wts[j] = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
-      }
-      __syncthreads();
-      if (dd < d) {
-        const float* src = p.ws_acc + ((base + c0) * hq + head) * d + dd;
-        const long long stride = (long long)hq * d;
-        int j = 0;
-        for (; j + 1 < n; j += 2) {
-          o0 = fmaf(src[j * stride], wts[j], o0);
-          o1 = fmaf(src[(j + 1) * stride], wts[j + 1], o1);
+  const long long stride = (long long)hq * d;  // floats between consecutive partials
+  const float* acc = p.ws_acc + (base * hq + head) * d;
+  if ((d & 3) == 0) {
+    for (int c = lane; c < (d >> 2); c += 32) {
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      int j = 0;
+      for (; j + 8 <= np; j += 8) {
+        float4 a[8];
+        float w[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float2 v = ml[(long long)(j + u) * hq];
+          w[u] = v.y > 0.f ? exp2f(v.x - M) : 0.f;
+          a[u] = reinterpret_cast<const float4*>(acc + (j + u) * stride)[c];
         }
-        if (j < n) o0 = fmaf(src[j * stride], wts[j], o0);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          o.x = fmaf(a[u].x, w[u], o.x);
+          o.y = fmaf(a[u].y, w[u], o.y);
+          o.z = fmaf(a[u].z, w[u], o.z);
+          o.w = fmaf(a[u].w, w[u], o.w);
+        }
+      }
+      for (; j < np; ++j) {
+        const float2 v = ml[(long long)j * hq];
+        const float w = v.y > 0.f ? exp2f(v.x - M) : 0.f;
+        const float4 a = reinterpret_cast<const float4*>(acc + j * stride)[c];
+        o.x = fmaf(a.x, w, o.x);
+        o.y = fmaf(a.y, w, o.y);
+        o.z = fmaf(a.z, w, o.z);
+        o.w = fmaf(a.w, w, o.w);
+      }
+      out[4 * c + 0] = QE::from_float(o.x * inv);
+      out[4 * c + 1] = QE::from_float(o.y * inv);
+      out[4 * c + 2] = QE::from_float(o.z * inv);
+      out[4 * c + 3] = QE::from_float(o.w * inv);
+    }
+  } else {
+    for (int dd = lane; dd < d; dd += 32) {
+      float o = 0.f;
+      for (int j = 0; j < np; ++j) {
+        const float2 v = ml[(long long)j * hq];
+        if (v.y > 0.f) o = fmaf(acc[j * stride + dd], exp2f(v.x - M), o);
+      }
+      out[dd] = QE::from_float(o * inv);
+    }
+  }
+}
+
+// Rows with many partials: one CTA of four warps per (row, head); the warps split
+// the partitions (each lane owning four output dimensions, four loads in flight)
+// and their sums meet in shared memory.
+template <int QDT>
+__global__ void __launch_bounds__(kMergeThreads) merge_wide_kernel(const AttnParams p) {
+  using QE = Elem<QDT>;
+  constexpr int kWarps = kMergeThreads / 32;
+  __shared__ float red_m[kWarps], red_l[kWarps];
+  __shared__ float4 red_o[kWarps][64];  // head_size <= 256
+  const long long gid = blockIdx.x;
+  const int row = static_cast<int>(gid / p.num_q_heads);
+  const int head = static_cast<int>(gid % p.num_q_heads);
+  if (row >= p.num_rows || plan_rejected(p)) return;
+  const RowInfo ri = row_info(p, row);
+  if (!ri.ok) return;
+  int np = ri.parts_row;
+  if (p.force_partials) {
+    const int start = shared_prefix_tokens(p, row);
+    np = (start > 0 ? (start + p.part_shared - 1) / p.part_shared : 0) +
+         (ri.seq_len - start + ri.part - 1) / ri.part;
+  } else if (np <= 1) {
+    return;
+  }
+  const long long base = row_partial_base(p, ri, row);
+  const int hq = p.num_q_heads, d = p.head_size, nv = d >> 2;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float2* ml = p.ws_ml + base * hq + head;
+  float M = -INFINITY, L = 0.f;
+  for (int j = threadIdx.x; j < np; j += kMergeThreads) {
+    const float2 v = ml[(long long)j * hq];
+    combine_ml(M, L, v.x, v.y);
+  }
+  for (int o = 16; o >= 1; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, M, o), l2 = __shfl_xor_sync(0xffffffffu, L, o);
+    combine_ml(M, L, m2, l2);
+  }
+  if (lane == 0) {
+    red_m[warp] = M;
+    red_l[warp] = L;
+  }
+  __syncthreads();
+  M = red_m[0];
+  L = red_l[0];
+  for (int w = 1; w < kWarps; ++w) combine_ml(M, L, red_m[w], red_l[w]);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const long long stride = (long long)hq * d;
+  const float* acc = p.ws_acc + (base * hq + head) * d;
+  for (int c = lane; c < nv; c += 32) {
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    int j = warp;
+    for (; j + 3 * kWarps < np; j += 4 * kWarps) {
+      float4 a[4];
+      float w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int jj = j + u * kWarps;
+        const float2 v = ml[(long long)jj * hq];
+        w[u] = v.y > 0.f ? exp2f(v.x - M) : 0.f;
+        a[u] = reinterpret_cast<const float4*>(acc + jj * stride)[c];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        o.x = fmaf(a[u].x, w[u], o.x);
+        o.y = fmaf(a[u].y, w[u], o.y);
+        o.z = fmaf(a[u].z, w[u], o.z);
+        o.w = fmaf(a[u].w, w[u], o.w);
       }
     }
-    if (dd < d) out[dd] = QE::from_float((o0 + o1) * inv);
+    for (; j < np; j += kWarps) {
+      const float2 v = ml[(long long)j * hq];
+      const float w = v.y > 0.f ? exp2f(v.x - M) : 0.f;
+      const float4 a = reinterpret_cast<const float4*>(acc + j * stride)[c];
+      o.x = fmaf(a.x, w, o.x);
+      o.y = fmaf(a.y, w, o.y);
+      o.z = fmaf(a.z, w, o.z);
+      o.w = fmaf(a.w, w, o.w);
+    }
+    red_o[warp][c] = o;
+  }
+  __syncthreads();
+  typename QE::T* out = reinterpret_cast<typename QE::T*>(p.out) + ((long long)row * hq + head) * d;
+  for (int c = threadIdx.x; c < nv; c += kMergeThreads) {
+    float4 o = red_o[0][c];
+    for (int w = 1; w < kWarps; ++w) {
+      o.x += red_o[w][c].x;
+      o.y += red_o[w][c].y;
+      o.z += red_o[w][c].z;
+      o.w += red_o[w][c].w;
+    }
+    out[4 * c + 0] = QE::from_float(o.x * inv);
+    out[4 * c + 1] = QE::from_float(o.y * inv);
+    out[4 * c + 2] = QE::from_float(o.z * inv);
+    out[4 * c + 3] = QE::from_float(o.w * inv);
   }
 }
 
@@ -291,10 +407,16 @@ cudaError_t launch_generic_t(const AttnParams& p, int grid_z, int only_multi, cu
   return cudaGetLastError();
 }
 
+// Rows may carry up to p.max_partitions partials: with many, four warps per row.
 template <int QDT>
 cudaError_t launch_merge_t(const AttnParams& p, cudaStream_t s) {
-  const long long ctas = (long long)p.num_rows * p.num_q_heads;
-  merge_kernel<QDT><<<(unsigned)ctas, kMergeThreads, 0, s>>>(p);
+  const long long rows = (long long)p.num_rows * p.num_q_heads;
+  if (p.max_partitions > 32 && (p.head_size & 3) == 0 && p.head_size <= 256) {
+    merge_wide_kernel<QDT><<<(unsigned)rows, kMergeThreads, 0, s>>>(p);
+  } else {
+    const long long ctas = (rows + kMergeThreads / 32 - 1) / (kMergeThreads / 32);
+    merge_kernel<QDT><<<(unsigned)ctas, kMergeThreads, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 
