@@ -180,7 +180,8 @@ def unique_kv_tokens(b) -> int:
 
 
 KERNEL_SOURCES = {"decode_mma_kernel": ("attn_decode.cu", "pa_common.cuh"),
-                  "shared_prefix_span": ("attn_decode.cu", "attn_prefill.cu", "pa_common.cuh")}
+                  "shared_prefix_span": ("attn_decode.cu", "attn_prefill.cu", "pa_common.cuh"),
+                  "prefill_tc_kernel": ("attn_prefill_tc.cu", "pa_common.cuh")}
 
 
 def decode_source_hash(kernel: str = "decode_mma_kernel") -> str:
@@ -544,8 +545,9 @@ def run_ours(args):
                        "kernel": "decode_mma_kernel (single-token rows)", "kernel_ms": att_ms,
                        "algorithmic_bytes_per_launch": vsplit["decode_bytes"], "traffic": None}
         prefill_line = {"bound": "tensor", "achieved": pf_tflops, "peak": tpeak, "unit": "TFLOP/s",
-                        "frac": pf_tflops / tpeak, "kernel": "prefill_mma_kernel (multi-token rows)",
-                        "kernel_ms": pf_ms, "algorithmic_flops_per_launch": vsplit["prefill_flops"], "traffic": None,
+                        "frac": pf_tflops / tpeak, "kernel": "prefill_tc_kernel (multi-token rows)",
+                        "kernel_ms": pf_ms, "algorithmic_flops_per_launch": vsplit["prefill_flops"],
+                        "traffic": profiled_traffic(args.workload, "prefill_tc_kernel"),
                         "peak_source": f"{tkind} MEASURED_PEAKS.json bf16_tflops_sustained"}
         roofline, other = (prefill_line, decode_line) if pf_ms >= att_ms else (decode_line, prefill_line)
         roofline = dict(roofline, secondary=other)

@@ -176,7 +176,10 @@ EncodeTiledFn encode_fn() {
 // 128-byte piece of the row (stride 128 bytes), dim3 = physical block.  One box is
 // a whole (block, head) tile, {128 bytes, block_size, pieces, 1}; in shared memory
 // it lands piece-major ([piece][token][128 bytes]) with the 128-byte swizzle.
-bool encode_cache_map(CUtensorMap* m, const void* base, int kv_dtype, int num_blocks, int hkv, int bs, int d) {
+// With `one_piece` the box is a single piece, {128 bytes, block_size, 1, 1}, so
+// the copies of consecutive blocks can be placed side by side per piece.
+bool encode_cache_map(CUtensorMap* m, const void* base, int kv_dtype, int num_blocks, int hkv, int bs, int d,
+                      bool one_piece = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const int eb = dtype_bytes(kv_dtype);
@@ -185,7 +188,7 @@ bool encode_cache_map(CUtensorMap* m, const void* base, int kv_dtype, int num_bl
   const int pieces = row_bytes / 128;
   cuuint64_t dims[4] = {(cuuint64_t)(128 / eb), (cuuint64_t)hkv * bs, (cuuint64_t)pieces, (cuuint64_t)num_blocks};
   cuuint64_t strides[3] = {(cuuint64_t)row_bytes, 128, (cuuint64_t)hkv * bs * row_bytes};
-  cuuint32_t box[4] = {(cuuint32_t)(128 / eb), (cuuint32_t)bs, (cuuint32_t)pieces, 1};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / eb), (cuuint32_t)bs, one_piece ? 1u : (cuuint32_t)pieces, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType t = eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
   return fn(m, t, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -603,11 +606,16 @@ pa_status pa_varlen_attn(void* out, const void* q, const void* k_cache, const vo
   }
   if (e != cudaSuccess) return PA_ERR_CUDA;
   const bool fast_decode = pa::decode_mma_supported(q_dtype, kv_dtype, head_size, block_size, p.group);
-  const bool fast_prefill = pa::prefill_mma_supported(q_dtype, kv_dtype, head_size, block_size, p.group);
-  CUtensorMap tk, tv;
-  if (fast_decode || fast_prefill) {
+  const bool fast_prefill = pa::prefill_tc_supported(q_dtype, kv_dtype, head_size, block_size);
+  CUtensorMap tk, tv, tk1, tv1;
+  if (fast_decode) {
     if (!encode_cache_map(&tk, k_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size) ||
         !encode_cache_map(&tv, v_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size))
+      return PA_ERR_CUDA;
+  }
+  if (fast_prefill && max_query_len > 1) {
+    if (!encode_cache_map(&tk1, k_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size, true) ||
+        !encode_cache_map(&tv1, v_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size, true))
       return PA_ERR_CUDA;
   }
   // Single-token rows: tensor-core decode kernel, else the generic kernel.
@@ -628,7 +636,7 @@ pa_status pa_varlen_attn(void* out, const void* q, const void* k_cache, const vo
     if (e != cudaSuccess) return PA_ERR_CUDA;
     if (multi && fast_prefill) {
       TraceScope t(4, s);
-      e = pa::launch_prefill_mma(p, q_dtype, kv_dtype, static_cast<int>(L.max_work), &tk, &tv, s);
+      e = pa::launch_prefill_tc(p, q_dtype, kv_dtype, static_cast<int>(L.max_work), &tk1, &tv1, s);
     } else if (multi) {
       TraceScope t(1, s);
       e = pa::launch_attn_generic(p, q_dtype, kv_dtype, static_cast<int>(L.parts_pf), 1, s);

@@ -1,0 +1,532 @@
+// Prefill (multi-token) rows of a varlen batch on the 5th-generation tensor cores:
+// tcgen05.mma with operands in shared memory and accumulators in tensor memory.
+//
+// [LINEAGE] "Chunked prefill" / [ARCH] Part 2: a prefill chunk's query tokens attend
+// the request's cached prefix and, causally, the chunk itself; [NOTES] "Prefill 与
+// Decode": this work is dense and compute-bound.
+//
+// One CTA per work item of the varlen plan (request, first query row of the tile,
+// partition of the keys) and per (KV head, group of <= 8 query heads).  The tile's
+// 128 query rows are (token, head) pairs, token-major (row = token * GP + head, GP =
+// the head group padded to a power of two); row r lives in TMEM lane r.  Keys stream
+// in chunks of 64 tokens (whole paged blocks), staged by TMA:
+//   S(i)  = Q K(i)^T    M = 128 rows, N = 64 keys, K = head dim   -> TMEM (2 buffers)
+//   P(i)  = softmax numerators of S(i), 16-bit                    -> shared memory
+//   O    += P(i) V(i)   M = 128 rows, N = head dim, K = 64 keys   -> TMEM
+// Warps 0-3 own one row per thread: they read S(i) from TMEM, keep the running max
+// (in log2 units, raised only when a chunk exceeds it by more than kRescaleSlack;
+// then O is rescaled in TMEM) and the running sum, and write P(i).  Warp 4 issues
+// the TMA copies.  Warp 5 allocates TMEM and one of its threads issues the MMAs:
+// S(i+1) is computed while the softmax of chunk i runs.  Every operand uses the
+// 128-byte swizzle; Q, K and P are K-major, V is MN-major (head dim contiguous), so
+// K and V chunks share one shared-memory layout: [64-element piece][key][128 bytes].
+#include "pa_common.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kRows = 128;   // query rows per tile = TMEM lanes
+constexpr int kChunk = 64;   // keys per chunk
+constexpr int kThreadsTc = 6 * 32;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kTmemCols = 256;  // S0 [0,64), S1 [64,128), O [128, 128 + head dim)
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Shared-memory matrix descriptor: start address, leading and stride byte offsets,
+// descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((addr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16 with fp32 accumulation: operand format 0 = f16,
+// 1 = bf16 (A and B alike); A K-major; B K-major (0) or MN-major (1).
+__device__ __forceinline__ uint32_t umma_idesc(int M, int N, uint32_t fmt, uint32_t b_mn_major) {
+  uint32_t d = 1u << 4;
+  d |= fmt << 7;
+  d |= fmt << 10;
+  d |= b_mn_major << 16;
+  d |= (uint32_t)(N >> 3) << 17;
+  d |= (uint32_t)(M >> 4) << 24;
+  return d;
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// Arrive once on `bar` when every MMA this thread has issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive TMEM columns of the warp's 32 lanes (thread i reads lane base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+template <int HEAD, int BS>
+struct TcGeom {
+  static constexpr int kPieces = HEAD / 64;                 // 128-byte pieces of a row
+  static constexpr int kBlocks = kChunk / BS;               // paged blocks per chunk
+  static constexpr int kStages = HEAD == 128 ? 4 : 6;       // K/V ring depth, chunks
+  static constexpr int kPiece = kChunk * 128;               // one piece of a chunk (64 keys)
+  static constexpr int kKvBytes = kPieces * kPiece;         // K (or V) of one chunk
+  static constexpr int kStageBytes = 2 * kKvBytes;          // K then V
+  static constexpr int kQPiece = kRows * 128;
+  static constexpr int kQBytes = kPieces * kQPiece;
+  static constexpr int kPBytes = kRows * 128;               // 64 keys x 2 bytes per row
+  static constexpr int kBlockTx = kPieces * BS * 128;       // bytes of one (block, head) tile
+  static constexpr int kBarOff = kQBytes + kStages * kStageBytes + kPBytes;
+  // full[S], empty[S], s_full[2], p_full, o_done, mma_fin; then the TMEM address
+  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kSmem = 1024 + kBarOff + 8 * kNumBars + 16;
+  static_assert(kBlocks * BS == kChunk, "block size must divide the chunk");
+  static_assert(HEAD + 128 <= kTmemCols, "O must fit beside the two S buffers");
+};
+
+template <int QDT, int HEAD, int BS>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv) {
+  using G = TcGeom<HEAD, BS>;
+  using QE = Elem<QDT>;
+  constexpr int ST = G::kStages;
+  constexpr int NB = G::kBlocks;
+
+  if (plan_rejected(p) || (int)blockIdx.x >= *p.work_count) return;
+  const int4 item = p.work[blockIdx.x];
+  const int r = item.x, row0 = item.y, z = item.z;
+  const int kvh = blockIdx.y / p.num_head_groups, hg = blockIdx.y % p.num_head_groups;
+  const int h0 = kvh * p.group + hg * 8;
+  const int nh = min(8, p.group - hg * 8);
+  int gp = 1;
+  while (gp < min(p.group, 8)) gp <<= 1;
+  const int tile_tokens = kRows / gp;
+  const int qs = p.query_start_loc[r];
+  const int q_len = p.query_start_loc[r + 1] - qs;
+  const int seq_len = p.seq_lens[r];
+  const int t0 = row0 - qs;                             // first token of the tile in its request
+  const int ntok = min(tile_tokens, q_len - t0);        // tokens in this tile
+  const int pos0 = seq_len - q_len + t0;                // position of the tile's first token
+  const int kv_end = p.causal ? pos0 + ntok : seq_len;  // keys the tile's last row attends
+  const int part = p.part_pf;
+  const int parts_req = (seq_len + part - 1) / part;
+  const int k0 = z * part, k1 = min(k0 + part, kv_end);
+  const int nch = k1 > k0 ? (k1 - k0 + kChunk - 1) / kChunk : 0;
+  const int kb_first = k0 / BS;
+  // keys held by the blocks a chunk loads end at the last block that reaches k1; V
+  // rows past them (or past seq_len) are zeroed before they meet P
+  const int kv_loaded_end = min(seq_len, (k1 + BS - 1) / BS * BS);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sQ = smem;
+  uint8_t* sKV = sQ + G::kQBytes;
+  uint8_t* sP = sKV + ST * G::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::kBarOff);
+  uint64_t* empty = full + ST;
+  uint64_t* s_full = empty + ST;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_done = p_full + 1;
+  uint64_t* mma_fin = o_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_fin + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+
+  // ---- set-up: barriers, the Q tile (zero rows for padding), TMEM
+  if (tid == 0) {
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+    for (int i = 0; i < ST; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_full + 1, 1);
+    mbar_init(p_full, kRows);
+    mbar_init(o_done, 1);
+    mbar_init(mma_fin, 1);
+    fence_mbar_init();
+  }
+  const int row_tok = tid / gp, row_head = tid % gp;
+  const bool row_valid = tid < kRows && row_tok < ntok && row_head < nh;
+  const int row_pos = pos0 + row_tok;
+  if (tid < kRows) {
+    const uint4* src = row_valid ? reinterpret_cast<const uint4*>(
+                                       reinterpret_cast<const typename QE::T*>(p.q) +
+                                       ((long long)(row0 + row_tok) * p.num_q_heads + h0 + row_head) * HEAD)
+                                 : nullptr;
+#pragma unroll
+    for (int c = 0; c < HEAD / 8; ++c) {
+      const uint4 v = src ? src[c] : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sQ + (c >> 3) * G::kQPiece + swz128(tid, c & 7)) = v;
+    }
+  }
+  fence_proxy_async();
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tO = tmem + 128;
+  const int32_t* table = p.block_tables + (long long)r * p.max_blocks_per_seq;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < nch; ++i) {
+        const int s = i % ST;
+        if (i >= ST && !mbar_wait_bounded(empty + s, ((i / ST) - 1) & 1)) {
+          flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+          break;
+        }
+        int phys[NB];
+        int nvalid = 0;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const int kb = kb_first + i * NB + b;
+          phys[b] = -1;
+          if (kb * BS < k1) {
+            const int ph = table[kb];
+            if (ph >= 0 && ph < p.num_blocks) {
+              phys[b] = ph;
+              ++nvalid;
+            } else {
+              flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
+            }
+          }
+        }
+        uint8_t* sk = sKV + s * G::kStageBytes;
+        uint8_t* sv = sk + G::kKvBytes;
+        if (nvalid == 0) {
+          mbar_arrive(full + s);
+        } else {
+          mbar_arrive_expect_tx(full + s, (uint32_t)(nvalid * 2 * G::kBlockTx));
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            if (phys[b] < 0) continue;
+#pragma unroll
+            for (int pc = 0; pc < G::kPieces; ++pc) {
+              tma_load_4d(sk + pc * G::kPiece + b * BS * 128, &tmk, 0, kvh * BS, pc, phys[b], full + s);
+              tma_load_4d(sv + pc * G::kPiece + b * BS * 128, &tmv, 0, kvh * BS, pc, phys[b], full + s);
+            }
+          }
+        }
+        issued = i + 1;
+      }
+      // every copy lands before the CTA can leave
+      for (int j = max(0, issued - ST); j < issued; ++j)
+        if (!mbar_wait_bounded(full + j % ST, (j / ST) & 1)) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t fmt = QDT == PA_BF16 ? 1u : 0u;
+      const uint32_t id_s = umma_idesc(kRows, kChunk, fmt, 0);
+      const uint32_t id_o = umma_idesc(kRows, HEAD, fmt, 1);
+      const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP);
+      auto issue_s = [&](int i) {
+        const uint32_t k_addr = smem_u32(sKV + (i % ST) * G::kStageBytes);
+#pragma unroll
+        for (int ks = 0; ks < HEAD / 16; ++ks) {
+          const uint32_t off = (ks & 3) * 32;  // 16 elements along the 128-byte row
+          const uint64_t a = umma_desc(q_addr + (ks >> 2) * G::kQPiece + off, 16, 1024);
+          const uint64_t b = umma_desc(k_addr + (ks >> 2) * G::kPiece + off, 16, 1024);
+          umma(tmem + (i & 1) * 64, a, b, id_s, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(s_full + (i & 1));
+      };
+      bool ok = true;
+      if (nch > 0) {
+        ok = mbar_wait_bounded(full, 0);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+        }
+      }
+      for (int i = 0; ok && i < nch; ++i) {
+        if (i + 1 < nch) {
+          if (!mbar_wait_bounded(full + (i + 1) % ST, ((i + 1) / ST) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(i + 1);
+        }
+        if (!mbar_wait_bounded(p_full, i & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sKV + (i % ST) * G::kStageBytes + G::kKvBytes);
+#pragma unroll
+        for (int ks = 0; ks < kChunk / 16; ++ks) {
+          const uint64_t a = umma_desc(p_addr + ks * 32, 16, 1024);
+          const uint64_t b = umma_desc(v_addr + ks * 2048, G::kPiece, 1024);
+          umma(tO, a, b, id_o, (i > 0 || ks > 0) ? 1u : 0u);
+        }
+        umma_commit(o_done);
+        umma_commit(empty + i % ST);
+      }
+      if (!ok) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+      // every MMA completes before TMEM is released
+      umma_commit(mma_fin);
+      if (!mbar_wait_bounded(mma_fin, 0)) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps 0-3
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float c = p.scale * kLog2e;
+    const int row_limit = p.causal ? min(k1, row_pos + 1) : k1;  // this row attends keys < row_limit
+    float m = -INFINITY, l = 0.f;
+    bool fail = false;
+    for (int i = 0; i < nch; ++i) {
+      const int base = k0 + i * kChunk;
+      const bool got = mbar_wait_bounded(s_full + (i & 1), (i >> 1) & 1);
+      if (!__all_sync(0xffffffffu, got)) {
+        fail = true;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[kChunk];
+      tmem_ld32(tmem + (i & 1) * 64 + lane_base, sr);
+      tmem_ld32(tmem + (i & 1) * 64 + 32 + lane_base, sr + 32);
+      tmem_wait_ld();
+      float sc[kChunk];
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) sc[j] = __uint_as_float(sr[j]);
+      const int rem = row_limit - base;  // keys of this chunk the row attends: [0, rem)
+      if (rem < kChunk) {
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j)
+          if (j >= rem) sc[j] = -INFINITY;
+      }
+      float mx = sc[0];
+#pragma unroll
+      for (int j = 1; j < kChunk; ++j) mx = fmaxf(mx, sc[j]);
+      mx *= c;
+      const bool need = mx > m + kRescaleSlack;
+      float al = 1.f;
+      if (need) {
+        const float nm = fmaxf(m, mx);
+        al = ex2_approx(m - nm);  // 0 while the row had no key yet
+        m = nm;
+        l *= al;
+      }
+      const float u = m == -INFINITY ? 0.f : m;
+      uint32_t pk[kChunk / 2];
+      float add = 0.f;
+#pragma unroll
+      for (int j = 0; j < kChunk / 2; ++j) {
+        const float e0 = ex2_approx(fmaf(sc[2 * j], c, -u));
+        const float e1 = ex2_approx(fmaf(sc[2 * j + 1], c, -u));
+        add += e0 + e1;
+        pk[j] = pack2<QDT>(e0, e1);
+      }
+      l += add;
+      // PV(i-1) has completed: O may be rescaled and P overwritten
+      if (i > 0) {
+        const bool done = mbar_wait_bounded(o_done, (i - 1) & 1);
+        if (!__all_sync(0xffffffffu, done)) {
+          fail = true;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+          for (int cb = 0; cb < HEAD; cb += 32) {
+            uint32_t o[32];
+            tmem_ld32(tO + cb + lane_base, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * al);
+            tmem_st32(tO + cb + lane_base, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      // V rows past the loaded keys (ragged partition end, sequence end) may hold any
+      // bits; their P is 0, so they are zeroed to keep 0 * V finite.  Each thread's
+      // stores precede its own arrival on p_full, which the PV MMA waits for.
+      if (base + kChunk > kv_loaded_end) {
+        const bool landed = mbar_wait_bounded(full + i % ST, (i / ST) & 1);
+        const int vrem = kv_loaded_end - base;
+        if (landed && tid < G::kPieces * kChunk) {
+          const int key = tid % kChunk, pc = tid / kChunk;
+          if (key >= vrem) {
+            uint4* d = reinterpret_cast<uint4*>(sKV + (i % ST) * G::kStageBytes + G::kKvBytes + pc * G::kPiece +
+                                                key * 128);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) d[q] = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc)
+        *reinterpret_cast<uint4*>(sP + swz128(tid, cc)) =
+            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (!fail && nch > 0) {
+      const bool done = mbar_wait_bounded(o_done, (nch - 1) & 1);
+      fail = !__all_sync(0xffffffffu, done);
+      tc_fence_after();
+    }
+    if (fail) {
+      if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+    } else {
+      // ---- epilogue: thread = row; direct output when the row needs one partition,
+      // else its partial state (unnormalised O, max in log2 units, sum)
+      const int kv_len = p.causal ? row_pos + 1 : seq_len;
+      const int parts_row = (kv_len + part - 1) / part;
+      const bool write = row_valid && z < parts_row;
+      const bool direct = parts_row == 1;
+      const int t = t0 + row_tok;
+      const int head = h0 + row_head;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const long long pi = (long long)p.part_off[r] + (long long)t * parts_req + z;
+      typename QE::T* o_row = reinterpret_cast<typename QE::T*>(p.out) + ((long long)(qs + t) * p.num_q_heads + head) * HEAD;
+      float* w_row = p.ws_acc + (pi * p.num_q_heads + head) * HEAD;
+#pragma unroll 1
+      for (int cb = 0; cb < HEAD; cb += 32) {
+        uint32_t o[32];
+        if (nch > 0) {
+          tmem_ld32(tO + cb + lane_base, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = 0u;
+        }
+        if (!write) continue;
+        if (direct) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 v;
+            v.x = pack2<QDT>(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+            v.y = pack2<QDT>(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+            v.z = pack2<QDT>(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+            v.w = pack2<QDT>(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+            *reinterpret_cast<uint4*>(o_row + cb + 8 * q) = v;
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(w_row + cb + 4 * q) =
+                make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]), __uint_as_float(o[4 * q + 2]),
+                            __uint_as_float(o[4 * q + 3]));
+        }
+      }
+      if (write && !direct) p.ws_ml[pi * p.num_q_heads + head] = make_float2(m, l);
+    }
+  }
+
+  // ---- teardown: TMEM is released once every warp is done with it
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+template <int QDT, int HEAD, int BS>
+cudaError_t launch_tc_t(const AttnParams& p, int num_items, const CUtensorMap* tk, const CUtensorMap* tv,
+                        cudaStream_t stream) {
+  constexpr int smem = TcGeom<HEAD, BS>::kSmem;
+  auto kern = prefill_tc_kernel<QDT, HEAD, BS>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();  // consume it: the caller reports the failure
+      return e;
+    }
+    configured_device = dev;
+  }
+  dim3 grid(num_items, p.num_kv_heads * p.num_head_groups);
+  kern<<<grid, kThreadsTc, smem, stream>>>(p, *tk, *tv);
+  return cudaGetLastError();
+}
+
+template <int QDT>
+cudaError_t launch_tc_shape(const AttnParams& p, int num_items, const CUtensorMap* tk, const CUtensorMap* tv,
+                            cudaStream_t s) {
+  const int d = p.head_size, bs = p.block_size;
+  if (d == 128 && bs == 16) return launch_tc_t<QDT, 128, 16>(p, num_items, tk, tv, s);
+  if (d == 128 && bs == 32) return launch_tc_t<QDT, 128, 32>(p, num_items, tk, tv, s);
+  if (d == 128 && bs == 64) return launch_tc_t<QDT, 128, 64>(p, num_items, tk, tv, s);
+  if (d == 64 && bs == 16) return launch_tc_t<QDT, 64, 16>(p, num_items, tk, tv, s);
+  if (d == 64 && bs == 32) return launch_tc_t<QDT, 64, 32>(p, num_items, tk, tv, s);
+  if (d == 64 && bs == 64) return launch_tc_t<QDT, 64, 64>(p, num_items, tk, tv, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool prefill_tc_supported(int q_dtype, int kv_dtype, int head_size, int block_size) {
+  if (!(q_dtype == PA_BF16 || q_dtype == PA_F16) || kv_dtype != q_dtype) return false;
+  return (head_size == 64 || head_size == 128) && (block_size == 16 || block_size == 32 || block_size == 64);
+}
+
+cudaError_t launch_prefill_tc(const AttnParams& p, int q_dtype, int kv_dtype, int num_items,
+                              const CUtensorMap* tmap_k, const CUtensorMap* tmap_v, cudaStream_t stream) {
+  if (num_items <= 0) return cudaSuccess;
+  if (kv_dtype != q_dtype) return cudaErrorInvalidValue;
+  if (q_dtype == PA_BF16) return launch_tc_shape<PA_BF16>(p, num_items, tmap_k, tmap_v, stream);
+  if (q_dtype == PA_F16) return launch_tc_shape<PA_F16>(p, num_items, tmap_k, tmap_v, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

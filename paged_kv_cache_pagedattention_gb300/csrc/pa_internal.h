@@ -96,9 +96,9 @@ cudaError_t launch_shared_prefix_tiles(const AttnParams& p, int q_dtype, int gri
                                        const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
                                        cudaStream_t stream);
 
-bool prefill_mma_supported(int q_dtype, int kv_dtype, int head_size, int block_size, int group);
-cudaError_t launch_prefill_mma(const AttnParams& p, int q_dtype, int kv_dtype, int num_ctas,
-                               const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
-                               cudaStream_t stream);
+// tcgen05 prefill tiles (TMEM accumulators); the tensor maps have one-piece boxes.
+bool prefill_tc_supported(int q_dtype, int kv_dtype, int head_size, int block_size);
+cudaError_t launch_prefill_tc(const AttnParams& p, int q_dtype, int kv_dtype, int num_items,
+                              const CUtensorMap* tmap_k, const CUtensorMap* tmap_v, cudaStream_t stream);
 
 }  // namespace pa

@@ -50,6 +50,9 @@ VARLEN_CASES = [
     ("prefill_ragged_tiles", "bf16", 32, 8, 128, 16, [97, 33, 1000], [97, 31, 45], 48, True),
     ("prefill_split_k_default", "bf16", 16, 4, 128, 16, [20000, 17000, 40], [100, 33, 1], 0, True),
     ("non_causal_g8", "f16", 16, 2, 128, 16, [250, 90], [60, 90], 64, False),
+    ("prefill_bs64", "bf16", 16, 4, 128, 64, [300, 129, 64], [150, 129, 1], 128, True),
+    ("prefill_bs64_d64_f16", "f16", 8, 2, 64, 64, [513, 70], [200, 70], 0, True),
+    ("prefill_part_not_chunk_multiple", "bf16", 8, 2, 128, 32, [1000, 161], [230, 161], 96, True),
 ]
 
 
