@@ -607,17 +607,17 @@ pa_status pa_varlen_attn(void* out, const void* q, const void* k_cache, const vo
   if (e != cudaSuccess) return PA_ERR_CUDA;
   const bool fast_decode = pa::decode_mma_supported(q_dtype, kv_dtype, head_size, block_size, p.group);
   const bool fast_prefill = pa::prefill_tc_supported(q_dtype, kv_dtype, head_size, block_size);
-  CUtensorMap tk, tv, tk1, tv1;
-  if (fast_decode) {
+  // whole-tile boxes for K and V; the prefill tiles copy K one piece at a time
+  CUtensorMap tk, tv, tk1;
+  const bool prefill_tiles = fast_prefill && max_query_len > 1;
+  if (fast_decode || prefill_tiles) {
     if (!encode_cache_map(&tk, k_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size) ||
         !encode_cache_map(&tv, v_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size))
       return PA_ERR_CUDA;
   }
-  if (fast_prefill && max_query_len > 1) {
-    if (!encode_cache_map(&tk1, k_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size, true) ||
-        !encode_cache_map(&tv1, v_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size, true))
-      return PA_ERR_CUDA;
-  }
+  if (prefill_tiles &&
+      !encode_cache_map(&tk1, k_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size, true))
+    return PA_ERR_CUDA;
   // Single-token rows: tensor-core decode kernel, else the generic kernel.
   // Multi-token rows: tensor-core prefill tiles, else the generic kernel.
   const bool multi = max_query_len > 1;
@@ -636,7 +636,7 @@ pa_status pa_varlen_attn(void* out, const void* q, const void* k_cache, const vo
     if (e != cudaSuccess) return PA_ERR_CUDA;
     if (multi && fast_prefill) {
       TraceScope t(4, s);
-      e = pa::launch_prefill_tc(p, q_dtype, kv_dtype, static_cast<int>(L.max_work), &tk1, &tv1, s);
+      e = pa::launch_prefill_tc(p, q_dtype, kv_dtype, static_cast<int>(L.max_work), &tk1, &tv, s);
     } else if (multi) {
       TraceScope t(1, s);
       e = pa::launch_attn_generic(p, q_dtype, kv_dtype, static_cast<int>(L.parts_pf), 1, s);

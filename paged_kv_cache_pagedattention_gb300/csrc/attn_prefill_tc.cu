@@ -10,16 +10,22 @@
 // 128 query rows are (token, head) pairs, token-major (row = token * GP + head, GP =
 // the head group padded to a power of two); row r lives in TMEM lane r.  Keys stream
 // in chunks of 64 tokens (whole paged blocks), staged by TMA:
-//   S(i)  = Q K(i)^T    M = 128 rows, N = 64 keys, K = head dim   -> TMEM (2 buffers)
-//   P(i)  = softmax numerators of S(i), 16-bit                    -> shared memory
-//   O    += P(i) V(i)   M = 128 rows, N = head dim, K = 64 keys   -> TMEM
+//   S(i)  = Q K(i)^T    M = 128 rows, N = 64 keys, K = head dim   -> TMEM (3 buffers)
+//   P(i)  = softmax numerators of S(i), 16-bit, written over S(i) -> TMEM
+//   O    += P(i) V(i)   M = 128 rows, N = head dim, K = 64 keys   -> TMEM (A from TMEM)
 // Warps 0-3 own one row per thread: they read S(i) from TMEM, keep the running max
 // (in log2 units, raised only when a chunk exceeds it by more than kRescaleSlack;
-// then O is rescaled in TMEM) and the running sum, and write P(i).  Warp 4 issues
-// the TMA copies.  Warp 5 allocates TMEM and one of its threads issues the MMAs:
-// S(i+1) is computed while the softmax of chunk i runs.  Every operand uses the
-// 128-byte swizzle; Q, K and P are K-major, V is MN-major (head dim contiguous), so
-// K and V chunks share one shared-memory layout: [64-element piece][key][128 bytes].
+// then O is rescaled in TMEM) and the running sum, and write P(i) back into the
+// first 32 columns of S(i)'s buffer (two 16-bit values per column).  Warp 4 loads:
+// its lanes read the block table a window at a time and each lane issues one TMA
+// copy of the chunk.  Warp 5 allocates TMEM and issues the MMAs from one elected
+// lane, in the order S(0) S(1) S(2) PV(0) S(3) PV(1) ...; the tensor core runs
+// them in issue order, so S(i+3) never overwrites P(i) before PV(i) has read it,
+// and the softmax of chunk i overlaps PV(i-1) and S(i+2).
+// Shared memory: Q and each K chunk are K-major, [64-element piece][row][128 bytes];
+// V is MN-major (head dim contiguous) and kept as the cache lays it out per block,
+// [block][piece][token][128 bytes], one TMA box per block; every operand uses the
+// 128-byte swizzle.
 #include "pa_common.cuh"
 
 namespace pa {
@@ -32,7 +38,9 @@ constexpr int kChunk = 64;   // keys per chunk
 constexpr int kThreadsTc = 6 * 32;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kTmemCols = 256;  // S0 [0,64), S1 [64,128), O [128, 128 + head dim)
+constexpr int kSBufs = 3;         // S / P buffers in TMEM, 64 columns each
+constexpr int kOCol = 256;        // O: columns [256, 256 + head dim)
+constexpr int kTmemCols = 512;
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -69,11 +77,58 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
       : "memory");
 }
 
+// D (+)= A B with A read from TMEM (rows in lanes, two 16-bit values per column).
+__device__ __forceinline__ void umma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 // Arrive once on `bar` when every MMA this thread has issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
+}
+
+// One lane of the (converged) warp: issues the single-thread tcgen05 operations while
+// their operands stay warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// Packed fp32 pairs (Blackwell f32x2 arithmetic) and the three-input maximum.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -109,21 +164,29 @@ template <int HEAD, int BS>
 struct TcGeom {
   static constexpr int kPieces = HEAD / 64;                 // 128-byte pieces of a row
   static constexpr int kBlocks = kChunk / BS;               // paged blocks per chunk
-  static constexpr int kStages = HEAD == 128 ? 4 : 6;       // K/V ring depth, chunks
-  static constexpr int kPiece = kChunk * 128;               // one piece of a chunk (64 keys)
+  static constexpr int kStages = HEAD == 128 ? 5 : 8;       // K/V ring depth, chunks
+  static constexpr int kPiece = kChunk * 128;               // one K piece of a chunk (64 keys)
   static constexpr int kKvBytes = kPieces * kPiece;         // K (or V) of one chunk
   static constexpr int kStageBytes = 2 * kKvBytes;          // K then V
+  static constexpr int kBlockTx = kPieces * BS * 128;       // bytes of one (block, head) tile
   static constexpr int kQPiece = kRows * 128;
   static constexpr int kQBytes = kPieces * kQPiece;
-  static constexpr int kPBytes = kRows * 128;               // 64 keys x 2 bytes per row
-  static constexpr int kBlockTx = kPieces * BS * 128;       // bytes of one (block, head) tile
-  static constexpr int kBarOff = kQBytes + kStages * kStageBytes + kPBytes;
-  // full[S], empty[S], s_full[2], p_full, o_done, mma_fin; then the TMEM address
-  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kBarOff = kQBytes + kStages * kStageBytes;
+  // full[S], empty[S], s_full[3], p_full[3], o_done[2], mma_fin; then the TMEM address
+  static constexpr int kNumBars = 2 * kStages + 2 * kSBufs + 3;
   static constexpr int kSmem = 1024 + kBarOff + 8 * kNumBars + 16;
+  static constexpr int kCopies = kBlocks * kPieces + kBlocks;  // TMA copies of a chunk
   static_assert(kBlocks * BS == kChunk, "block size must divide the chunk");
-  static_assert(HEAD + 128 <= kTmemCols, "O must fit beside the two S buffers");
+  static_assert(kCopies <= 32, "one copy per producer lane");
+  static_assert(kSBufs * 64 <= kOCol && kOCol + HEAD <= kTmemCols, "TMEM columns");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
 };
+
+// Byte offset, inside a chunk's V, of key `key`'s row in piece `pc`.
+template <int HEAD, int BS>
+__device__ __forceinline__ uint32_t v_row_off(int key, int pc) {
+  return (uint32_t)((key / BS) * TcGeom<HEAD, BS>::kBlockTx + pc * BS * 128 + (key % BS) * 128);
+}
 
 template <int QDT, int HEAD, int BS>
 __global__ void __launch_bounds__(kThreadsTc, 1)
@@ -163,13 +226,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sQ = smem;
   uint8_t* sKV = sQ + G::kQBytes;
-  uint8_t* sP = sKV + ST * G::kStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::kBarOff);
   uint64_t* empty = full + ST;
+  // Per S/P buffer b: s_full[b] when S(i) is in TMEM, p_full[b] when P(i) is (i % 3
+  // == b, phase i / 3).  One barrier per buffer keeps every waiter within one phase
+  // of its barrier: chunk i + 3 cannot start before PV(i) was issued.
   uint64_t* s_full = empty + ST;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 1;
-  uint64_t* mma_fin = o_done + 1;
+  uint64_t* p_full = s_full + kSBufs;
+  uint64_t* o_done = p_full + kSBufs;   // [2]: PV(i) completes phase i / 2 of o_done[i & 1]
+  uint64_t* mma_fin = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_fin + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -183,10 +248,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       mbar_init(full + i, 1);
       mbar_init(empty + i, 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(s_full + 1, 1);
-    mbar_init(p_full, kRows);
+    for (int i = 0; i < kSBufs; ++i) {
+      mbar_init(s_full + i, 1);
+      mbar_init(p_full + i, kRows);
+    }
     mbar_init(o_done, 1);
+    mbar_init(o_done + 1, 1);
     mbar_init(mma_fin, 1);
     fence_mbar_init();
   }
@@ -215,112 +282,131 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tO = tmem + 128;
+  const uint32_t tO = tmem + kOCol;
   const int32_t* table = p.block_tables + (long long)r * p.max_blocks_per_seq;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < nch; ++i) {
-        const int s = i % ST;
-        if (i >= ST && !mbar_wait_bounded(empty + s, ((i / ST) - 1) & 1)) {
-          flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-          break;
-        }
-        int phys[NB];
-        int nvalid = 0;
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          const int kb = kb_first + i * NB + b;
-          phys[b] = -1;
-          if (kb * BS < k1) {
-            const int ph = table[kb];
-            if (ph >= 0 && ph < p.num_blocks) {
-              phys[b] = ph;
-              ++nvalid;
-            } else {
-              flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
-            }
-          }
-        }
-        uint8_t* sk = sKV + s * G::kStageBytes;
-        uint8_t* sv = sk + G::kKvBytes;
-        if (nvalid == 0) {
-          mbar_arrive(full + s);
-        } else {
-          mbar_arrive_expect_tx(full + s, (uint32_t)(nvalid * 2 * G::kBlockTx));
-#pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            if (phys[b] < 0) continue;
-#pragma unroll
-            for (int pc = 0; pc < G::kPieces; ++pc) {
-              tma_load_4d(sk + pc * G::kPiece + b * BS * 128, &tmk, 0, kvh * BS, pc, phys[b], full + s);
-              tma_load_4d(sv + pc * G::kPiece + b * BS * 128, &tmv, 0, kvh * BS, pc, phys[b], full + s);
-            }
-          }
-        }
-        issued = i + 1;
+    // Lane j holds block table entry kb_first + 32 w + j of window w; the next window
+    // is prefetched.  Per chunk, lanes [0, NB * pieces) copy one K piece of one block
+    // each and the next NB lanes one whole V block each.
+    const int kb_end = (k1 + BS - 1) / BS;  // blocks [kb_first, kb_end) are loaded
+    auto load_window = [&](int w) {
+      const int kb = kb_first + 32 * w + lane;
+      return kb < kb_end ? table[kb] : -1;
+    };
+    int my_b = -1, my_pc = 0;
+    bool my_v = false;
+    if (lane < NB * G::kPieces) {
+      my_b = lane / G::kPieces;
+      my_pc = lane % G::kPieces;
+    } else if (lane < G::kCopies) {
+      my_b = lane - NB * G::kPieces;
+      my_v = true;
+    }
+    int cur_w = 0;
+    int win = load_window(0);
+    int win_next = load_window(1);
+    int issued = 0;
+    for (int i = 0; i < nch; ++i) {
+      const int s = i % ST;
+      if (i >= ST && !__all_sync(0xffffffffu, mbar_wait_bounded(empty + s, ((i / ST) - 1) & 1))) {
+        if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+        break;
       }
-      // every copy lands before the CTA can leave
+      const int w = (i * NB) >> 5;  // NB divides 32: a chunk's blocks share one window
+      if (w != cur_w) {
+        win = win_next;
+        win_next = load_window(w + 1);
+        cur_w = w;
+      }
+      const int e = __shfl_sync(0xffffffffu, win, (i * NB + (my_b < 0 ? 0 : my_b)) & 31);
+      const int kb = kb_first + i * NB + my_b;
+      const bool in_range = my_b >= 0 && kb < kb_end;
+      const bool ok_b = in_range && e >= 0 && e < p.num_blocks;
+      if (my_v && in_range && !ok_b) flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
+      const int nvalid = __popc(__ballot_sync(0xffffffffu, my_v && ok_b));
+      if (lane == 0) {
+        if (nvalid == 0) mbar_arrive(full + s);
+        else mbar_arrive_expect_tx(full + s, (uint32_t)(nvalid * 2 * G::kBlockTx));
+      }
+      __syncwarp();
+      if (ok_b) {
+        uint8_t* sk = sKV + s * G::kStageBytes;
+        if (my_v) tma_load_4d(sk + G::kKvBytes + my_b * G::kBlockTx, &tmv, 0, kvh * BS, 0, e, full + s);
+        else tma_load_4d(sk + my_pc * G::kPiece + my_b * BS * 128, &tmk, 0, kvh * BS, my_pc, e, full + s);
+      }
+      issued = i + 1;
+    }
+    // every copy lands before the CTA can leave
+    if (lane == 0)
       for (int j = max(0, issued - ST); j < issued; ++j)
         if (!mbar_wait_bounded(full + j % ST, (j / ST) & 1)) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-    }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t fmt = QDT == PA_BF16 ? 1u : 0u;
-      const uint32_t id_s = umma_idesc(kRows, kChunk, fmt, 0);
-      const uint32_t id_o = umma_idesc(kRows, HEAD, fmt, 1);
-      const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP);
-      auto issue_s = [&](int i) {
-        const uint32_t k_addr = smem_u32(sKV + (i % ST) * G::kStageBytes);
+    // The whole warp follows the schedule (descriptors stay warp-uniform); one
+    // elected lane issues each group of MMAs and its commit.
+    const uint32_t fmt = QDT == PA_BF16 ? 1u : 0u;
+    const uint32_t id_s = umma_idesc(kRows, kChunk, fmt, 0);
+    const uint32_t id_o = umma_idesc(kRows, HEAD, fmt, 1);
+    // descriptor start addresses count 16-byte units: offsets are added pre-shifted
+    const uint64_t qd0 = umma_desc(smem_u32(sQ), 16, 1024);
+    const uint64_t kd0 = umma_desc(smem_u32(sKV), 16, 1024);
+    const uint64_t vd0 = umma_desc(smem_u32(sKV) + G::kKvBytes, BS * 128, 1024);
+    auto issue_s = [&](int j) {
+      const uint64_t kd = kd0 + (uint64_t)(((j % ST) * G::kStageBytes) >> 4);
+      const uint32_t d = tmem + (j % kSBufs) * 64;
+      if (elect_one()) {
 #pragma unroll
         for (int ks = 0; ks < HEAD / 16; ++ks) {
-          const uint32_t off = (ks & 3) * 32;  // 16 elements along the 128-byte row
-          const uint64_t a = umma_desc(q_addr + (ks >> 2) * G::kQPiece + off, 16, 1024);
-          const uint64_t b = umma_desc(k_addr + (ks >> 2) * G::kPiece + off, 16, 1024);
-          umma(tmem + (i & 1) * 64, a, b, id_s, ks > 0 ? 1u : 0u);
+          const uint32_t qo = ((ks >> 2) * G::kQPiece + (ks & 3) * 32) >> 4;
+          const uint32_t ko = ((ks >> 2) * G::kPiece + (ks & 3) * 32) >> 4;
+          umma(d, qd0 + qo, kd + ko, id_s, ks > 0 ? 1u : 0u);
         }
-        umma_commit(s_full + (i & 1));
-      };
-      bool ok = true;
-      if (nch > 0) {
-        ok = mbar_wait_bounded(full, 0);
-        if (ok) {
-          tc_fence_after();
-          issue_s(0);
-        }
+        umma_commit(s_full + j % kSBufs);
       }
-      for (int i = 0; ok && i < nch; ++i) {
-        if (i + 1 < nch) {
-          if (!mbar_wait_bounded(full + (i + 1) % ST, ((i + 1) / ST) & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_s(i + 1);
-        }
-        if (!mbar_wait_bounded(p_full, i & 1)) {
+      __syncwarp();
+    };
+    bool ok = true;
+    for (int j = 0; ok && j < kSBufs - 1 && j < nch; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(full + j % ST, (j / ST) & 1));
+      if (ok) {
+        tc_fence_after();
+        issue_s(j);
+      }
+    }
+    for (int i = 0; ok && i < nch; ++i) {
+      const int j = i + kSBufs - 1;  // S runs kSBufs - 1 chunks ahead of PV
+      if (j < nch) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(full + j % ST, (j / ST) & 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t v_addr = smem_u32(sKV + (i % ST) * G::kStageBytes + G::kKvBytes);
+        issue_s(j);
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(p_full + i % kSBufs, (i / kSBufs) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t vd = vd0 + (uint64_t)(((i % ST) * G::kStageBytes) >> 4);
+      const uint32_t pt = tmem + (i % kSBufs) * 64;
+      if (elect_one()) {
 #pragma unroll
-        for (int ks = 0; ks < kChunk / 16; ++ks) {
-          const uint64_t a = umma_desc(p_addr + ks * 32, 16, 1024);
-          const uint64_t b = umma_desc(v_addr + ks * 2048, G::kPiece, 1024);
-          umma(tO, a, b, id_o, (i > 0 || ks > 0) ? 1u : 0u);
-        }
-        umma_commit(o_done);
+        for (int ks = 0; ks < kChunk / 16; ++ks)
+          umma_tmem_a(tO, pt + ks * 8, vd + (uint64_t)(v_row_off<HEAD, BS>(16 * ks, 0) >> 4), id_o,
+                      (i > 0 || ks > 0) ? 1u : 0u);
+        umma_commit(o_done + (i & 1));
         umma_commit(empty + i % ST);
       }
-      if (!ok) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-      // every MMA completes before TMEM is released
-      umma_commit(mma_fin);
-      if (!mbar_wait_bounded(mma_fin, 0)) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+      __syncwarp();
     }
+    if (!ok && lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+    // every MMA completes before TMEM is released
+    if (elect_one()) umma_commit(mma_fin);
+    __syncwarp();
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(mma_fin, 0)) && lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
   } else {
     // ------------------------------------------------------------ softmax warps 0-3
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
@@ -330,15 +416,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     bool fail = false;
     for (int i = 0; i < nch; ++i) {
       const int base = k0 + i * kChunk;
-      const bool got = mbar_wait_bounded(s_full + (i & 1), (i >> 1) & 1);
+      const uint32_t tS = tmem + (i % kSBufs) * 64;
+      const bool got = mbar_wait_bounded(s_full + i % kSBufs, (i / kSBufs) & 1);
       if (!__all_sync(0xffffffffu, got)) {
         fail = true;
         break;
       }
       tc_fence_after();
       uint32_t sr[kChunk];
-      tmem_ld32(tmem + (i & 1) * 64 + lane_base, sr);
-      tmem_ld32(tmem + (i & 1) * 64 + 32 + lane_base, sr + 32);
+      tmem_ld32(tS + lane_base, sr);
+      tmem_ld32(tS + 32 + lane_base, sr + 32);
       tmem_wait_ld();
       float sc[kChunk];
 #pragma unroll
@@ -349,10 +436,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         for (int j = 0; j < kChunk; ++j)
           if (j >= rem) sc[j] = -INFINITY;
       }
-      float mx = sc[0];
+      // row maximum: eight independent chains of three-input maxima
+      float mq[8];
 #pragma unroll
-      for (int j = 1; j < kChunk; ++j) mx = fmaxf(mx, sc[j]);
-      mx *= c;
+      for (int q = 0; q < 8; ++q) {
+        float t = max3(sc[8 * q], sc[8 * q + 1], sc[8 * q + 2]);
+        t = max3(t, sc[8 * q + 3], sc[8 * q + 4]);
+        t = max3(t, sc[8 * q + 5], sc[8 * q + 6]);
+        mq[q] = fmaxf(t, sc[8 * q + 7]);
+      }
+      const float mx = max3(max3(mq[0], mq[1], mq[2]), max3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7])) * c;
       const bool need = mx > m + kRescaleSlack;
       float al = 1.f;
       if (need) {
@@ -362,37 +455,39 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         l *= al;
       }
       const float u = m == -INFINITY ? 0.f : m;
+      // p = 2^(s c - u) on pairs of keys; the row sum in four packed accumulators
+      const uint64_t c2 = f2_pack(c, c), nu2 = f2_pack(-u, -u);
       uint32_t pk[kChunk / 2];
-      float add = 0.f;
+      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int j = 0; j < kChunk / 2; ++j) {
-        const float e0 = ex2_approx(fmaf(sc[2 * j], c, -u));
-        const float e1 = ex2_approx(fmaf(sc[2 * j + 1], c, -u));
-        add += e0 + e1;
+        const float2 x = f2_unpack(f2_fma(f2_pack(sc[2 * j], sc[2 * j + 1]), c2, nu2));
+        const float e0 = ex2_approx(x.x), e1 = ex2_approx(x.y);
+        acc2[j & 3] = f2_add(acc2[j & 3], f2_pack(e0, e1));
         pk[j] = pack2<QDT>(e0, e1);
       }
-      l += add;
-      // PV(i-1) has completed: O may be rescaled and P overwritten
-      if (i > 0) {
-        const bool done = mbar_wait_bounded(o_done, (i - 1) & 1);
+      const float2 lsum = f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])));
+      l += lsum.x + lsum.y;
+      // O is rescaled only once PV(i-1) has completed
+      if (__any_sync(0xffffffffu, need) && i > 0) {
+        const bool done = mbar_wait_bounded(o_done + ((i - 1) & 1), ((i - 1) >> 1) & 1);
         if (!__all_sync(0xffffffffu, done)) {
           fail = true;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-          for (int cb = 0; cb < HEAD; cb += 32) {
-            uint32_t o[32];
-            tmem_ld32(tO + cb + lane_base, o);
-            tmem_wait_ld();
+        for (int cb = 0; cb < HEAD; cb += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + cb + lane_base, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * al);
-            tmem_st32(tO + cb + lane_base, o);
-          }
-          tmem_wait_st();
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * al);
+          tmem_st32(tO + cb + lane_base, o);
         }
       }
+      // P(i) over the first half of S(i)'s columns
+      tmem_st32(tS + lane_base, pk);
       // V rows past the loaded keys (ragged partition end, sequence end) may hold any
       // bits; their P is 0, so they are zeroed to keep 0 * V finite.  Each thread's
       // stores precede its own arrival on p_full, which the PV MMA waits for.
@@ -402,23 +497,30 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         if (landed && tid < G::kPieces * kChunk) {
           const int key = tid % kChunk, pc = tid / kChunk;
           if (key >= vrem) {
-            uint4* d = reinterpret_cast<uint4*>(sKV + (i % ST) * G::kStageBytes + G::kKvBytes + pc * G::kPiece +
-                                                key * 128);
+            uint4* d = reinterpret_cast<uint4*>(sKV + (i % ST) * G::kStageBytes + G::kKvBytes +
+                                                v_row_off<HEAD, BS>(key, pc));
 #pragma unroll
             for (int q = 0; q < 8; ++q) d[q] = make_uint4(0, 0, 0, 0);
           }
         }
+        fence_proxy_async();
       }
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-        *reinterpret_cast<uint4*>(sP + swz128(tid, cc)) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      fence_proxy_async();
+      tmem_wait_st();
+      // Observe PV(i-2) (phase (i-2)/2 of o_done[i & 1]): every phase of both o_done
+      // barriers is waited for in order and never more than one phase late, so the
+      // parity waits stay unambiguous.
+      if (i >= 2) {
+        const bool done = mbar_wait_bounded(o_done + (i & 1), ((i - 2) >> 1) & 1);
+        if (!__all_sync(0xffffffffu, done)) {
+          fail = true;
+          break;
+        }
+      }
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(p_full + i % kSBufs);
     }
     if (!fail && nch > 0) {
-      const bool done = mbar_wait_bounded(o_done, (nch - 1) & 1);
+      const bool done = mbar_wait_bounded(o_done + ((nch - 1) & 1), ((nch - 1) >> 1) & 1);
       fail = !__all_sync(0xffffffffu, done);
       tc_fence_after();
     }

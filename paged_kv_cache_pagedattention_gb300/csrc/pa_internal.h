@@ -96,7 +96,8 @@ cudaError_t launch_shared_prefix_tiles(const AttnParams& p, int q_dtype, int gri
                                        const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
                                        cudaStream_t stream);
 
-// tcgen05 prefill tiles (TMEM accumulators); the tensor maps have one-piece boxes.
+// tcgen05 prefill tiles (TMEM accumulators); tmap_k has one-piece boxes, tmap_v
+// whole (block, head) tiles.
 bool prefill_tc_supported(int q_dtype, int kv_dtype, int head_size, int block_size);
 cudaError_t launch_prefill_tc(const AttnParams& p, int q_dtype, int kv_dtype, int num_items,
                               const CUtensorMap* tmap_k, const CUtensorMap* tmap_v, cudaStream_t stream);
