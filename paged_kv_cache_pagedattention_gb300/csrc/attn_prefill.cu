@@ -1,6 +1,5 @@
 // FlashAttention-2 style tiles on the warp-level tensor-core MMA (m16n8k16) for the
-// shared prefixes of sequence groups, and the tile shape shared with the tcgen05
-// prefill kernel.
+// shared prefixes of sequence groups.
 //
 // [AGENTIC] "統一分頁 + 共用池": forked sequences point at the same physical blocks,
 // so the rows that read one shared block are gathered into one tile and the block
@@ -16,14 +15,6 @@
 #include "pa_common.cuh"
 
 namespace pa {
-
-// Query tokens of a 128-row prefill tile: rows are (token, head) pairs with the
-// head group padded to a power of two, at most 8 heads per tile.
-int prefill_tile_tokens(int group) {
-  int g8 = 1;
-  while (g8 < group && g8 < 8) g8 <<= 1;
-  return 128 / g8;
-}
 
 namespace {
 

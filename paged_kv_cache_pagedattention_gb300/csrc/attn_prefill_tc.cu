@@ -17,8 +17,8 @@
 // (in log2 units, raised only when a chunk exceeds it by more than kRescaleSlack;
 // then O is rescaled in TMEM) and the running sum, and write P(i) back into the
 // first 32 columns of S(i)'s buffer (two 16-bit values per column).  Warp 4 loads:
-// its lanes read the block table a window at a time and each lane issues one TMA
-// copy of the chunk.  Warp 5 allocates TMEM and issues the MMAs from one elected
+// its lanes read the block table a window at a time and one elected lane issues
+// the chunk's TMA copies.  Warp 5 allocates TMEM and issues the MMAs from one elected
 // lane, in the order S(0) S(1) S(2) PV(0) S(3) PV(1) ...; the tensor core runs
 // them in issue order, so S(i+3) never overwrites P(i) before PV(i) has read it,
 // and the softmax of chunk i overlaps PV(i-1) and S(i+2).
@@ -33,14 +33,16 @@ namespace pa {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kRows = 128;   // query rows per tile = TMEM lanes
-constexpr int kChunk = 64;   // keys per chunk
-constexpr int kThreadsTc = 6 * 32;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kSBufs = 3;         // S / P buffers in TMEM, 64 columns each
-constexpr int kOCol = 256;        // O: columns [256, 256 + head dim)
-constexpr int kTmemCols = 512;
+constexpr int kRows = 128;        // query rows per tile = TMEM lanes
+constexpr int kTiles = 2;         // tiles per CTA, sharing every K/V chunk
+constexpr int kChunk = 64;        // keys per chunk
+constexpr int kThreadsTc = (4 * kTiles + 2) * 32;
+constexpr int kProducerWarp = 4 * kTiles;
+constexpr int kMmaWarp = 4 * kTiles + 1;
+constexpr int kSBufs = 2;         // S / P buffers per tile, 64 TMEM columns each
+constexpr int kOCol = 128;        // a tile's O: columns [128, 128 + head dim) of its 256
+constexpr int kTileCols = 256;
+constexpr int kTmemCols = kTiles * kTileCols;
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -164,21 +166,19 @@ template <int HEAD, int BS>
 struct TcGeom {
   static constexpr int kPieces = HEAD / 64;                 // 128-byte pieces of a row
   static constexpr int kBlocks = kChunk / BS;               // paged blocks per chunk
-  static constexpr int kStages = HEAD == 128 ? 5 : 8;       // K/V ring depth, chunks
+  static constexpr int kStages = HEAD == 128 ? 4 : 8;       // K/V ring depth, chunks
   static constexpr int kPiece = kChunk * 128;               // one K piece of a chunk (64 keys)
   static constexpr int kKvBytes = kPieces * kPiece;         // K (or V) of one chunk
   static constexpr int kStageBytes = 2 * kKvBytes;          // K then V
   static constexpr int kBlockTx = kPieces * BS * 128;       // bytes of one (block, head) tile
   static constexpr int kQPiece = kRows * 128;
-  static constexpr int kQBytes = kPieces * kQPiece;
-  static constexpr int kBarOff = kQBytes + kStages * kStageBytes;
-  // full[S], empty[S], s_full[3], p_full[3], o_done[2], mma_fin; then the TMEM address
-  static constexpr int kNumBars = 2 * kStages + 2 * kSBufs + 3;
+  static constexpr int kQTile = kPieces * kQPiece;
+  static constexpr int kBarOff = kTiles * kQTile + kStages * kStageBytes;
+  // full[S], empty[S]; per tile s_full[2], p_full[2], o_done[2]; mma_fin; TMEM address
+  static constexpr int kNumBars = 2 * kStages + 3 * kSBufs * kTiles + 1;
   static constexpr int kSmem = 1024 + kBarOff + 8 * kNumBars + 16;
-  static constexpr int kCopies = kBlocks * kPieces + kBlocks;  // TMA copies of a chunk
   static_assert(kBlocks * BS == kChunk, "block size must divide the chunk");
-  static_assert(kCopies <= 32, "one copy per producer lane");
-  static_assert(kSBufs * 64 <= kOCol && kOCol + HEAD <= kTmemCols, "TMEM columns");
+  static_assert(kSBufs * 64 <= kOCol && kOCol + HEAD <= kTileCols, "TMEM columns");
   static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
@@ -205,42 +205,56 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int nh = min(8, p.group - hg * 8);
   int gp = 1;
   while (gp < min(p.group, 8)) gp <<= 1;
-  const int tile_tokens = kRows / gp;
+  const int tile_tokens = kRows / gp;                   // query tokens of one 128-row tile
   const int qs = p.query_start_loc[r];
   const int q_len = p.query_start_loc[r + 1] - qs;
   const int seq_len = p.seq_lens[r];
-  const int t0 = row0 - qs;                             // first token of the tile in its request
-  const int ntok = min(tile_tokens, q_len - t0);        // tokens in this tile
-  const int pos0 = seq_len - q_len + t0;                // position of the tile's first token
-  const int kv_end = p.causal ? pos0 + ntok : seq_len;  // keys the tile's last row attends
+  const int t0 = row0 - qs;                             // first token of the CTA in its request
+  const int ntok = min(kTiles * tile_tokens, q_len - t0);
+  const int pos0 = seq_len - q_len + t0;                // position of the CTA's first token
   const int part = p.part_pf;
   const int parts_req = (seq_len + part - 1) / part;
-  const int k0 = z * part, k1 = min(k0 + part, kv_end);
-  const int nch = k1 > k0 ? (k1 - k0 + kChunk - 1) / kChunk : 0;
+  const int k0 = z * part;
+  // keys [k0, k1) of this partition that some row of tile t attends -> its chunks
+  auto tile_chunks = [&](int t) {
+    const int nt = min(ntok, (t + 1) * tile_tokens) - t * tile_tokens;
+    if (nt <= 0) return 0;
+    const int k1t = min(k0 + part, p.causal ? pos0 + t * tile_tokens + nt : seq_len);
+    return k1t > k0 ? (k1t - k0 + kChunk - 1) / kChunk : 0;
+  };
+  static_assert(kTiles == 2, "two tiles per CTA");
+  const int nch_t[kTiles] = {tile_chunks(0), tile_chunks(1)};
+  const int k1 = min(k0 + part, p.causal ? pos0 + ntok : seq_len);
+  const int nch = k1 > k0 ? (k1 - k0 + kChunk - 1) / kChunk : 0;  // = the largest nch_t
   const int kb_first = k0 / BS;
   // keys held by the blocks a chunk loads end at the last block that reaches k1; V
-  // rows past them (or past seq_len) are zeroed before they meet P
+  // rows past them (or past seq_len) are zeroed before they meet P.  Only the last
+  // chunk can hold such rows; the last tile that reads it zeroes them.
   const int kv_loaded_end = min(seq_len, (k1 + BS - 1) / BS * BS);
+  const bool tail_chunk = nch > 0 && k0 + nch * kChunk > kv_loaded_end;
+  const int zero_tile = nch_t[kTiles - 1] == nch ? kTiles - 1 : 0;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* sQ = smem;
-  uint8_t* sKV = sQ + G::kQBytes;
+  uint8_t* sQ = smem;                                   // [tile][piece][row][128 bytes]
+  uint8_t* sKV = sQ + kTiles * G::kQTile;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::kBarOff);
   uint64_t* empty = full + ST;
-  // Per S/P buffer b: s_full[b] when S(i) is in TMEM, p_full[b] when P(i) is (i % 3
-  // == b, phase i / 3).  One barrier per buffer keeps every waiter within one phase
-  // of its barrier: chunk i + 3 cannot start before PV(i) was issued.
-  uint64_t* s_full = empty + ST;
-  uint64_t* p_full = s_full + kSBufs;
-  uint64_t* o_done = p_full + kSBufs;   // [2]: PV(i) completes phase i / 2 of o_done[i & 1]
-  uint64_t* mma_fin = o_done + 2;
+  // Per tile t and buffer b (chunk i uses b = i % 2, phase i / 2): s_full when S(i)
+  // is in TMEM, p_full when P(i) is, o_done when PV(i) has completed.  The next use
+  // of a buffer's barrier always follows its waiter's observation of the previous
+  // phase (S(i+2) is issued after PV(i), PV(i) after p_full(i)), so no waiter can
+  // fall two phases behind.
+  uint64_t* s_full = empty + ST;                        // [tile][2]
+  uint64_t* p_full = s_full + kTiles * kSBufs;
+  uint64_t* o_done = p_full + kTiles * kSBufs;
+  uint64_t* mma_fin = o_done + kTiles * kSBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_fin + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
 
-  // ---- set-up: barriers, the Q tile (zero rows for padding), TMEM
+  // ---- set-up: barriers, the Q tiles (zero rows for padding), TMEM
   if (tid == 0) {
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
@@ -248,27 +262,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       mbar_init(full + i, 1);
       mbar_init(empty + i, 1);
     }
-    for (int i = 0; i < kSBufs; ++i) {
+    for (int i = 0; i < kTiles * kSBufs; ++i) {
       mbar_init(s_full + i, 1);
       mbar_init(p_full + i, kRows);
+      mbar_init(o_done + i, 1);
     }
-    mbar_init(o_done, 1);
-    mbar_init(o_done + 1, 1);
     mbar_init(mma_fin, 1);
     fence_mbar_init();
   }
+  // CTA row R = token * gp + head; tile R / 128, TMEM lane R % 128
   const int row_tok = tid / gp, row_head = tid % gp;
-  const bool row_valid = tid < kRows && row_tok < ntok && row_head < nh;
+  const bool row_valid = tid < kTiles * kRows && row_tok < ntok && row_head < nh;
   const int row_pos = pos0 + row_tok;
-  if (tid < kRows) {
+  if (tid < kTiles * kRows) {
     const uint4* src = row_valid ? reinterpret_cast<const uint4*>(
                                        reinterpret_cast<const typename QE::T*>(p.q) +
                                        ((long long)(row0 + row_tok) * p.num_q_heads + h0 + row_head) * HEAD)
                                  : nullptr;
+    uint8_t* dst = sQ + (tid / kRows) * G::kQTile;
 #pragma unroll
     for (int c = 0; c < HEAD / 8; ++c) {
       const uint4 v = src ? src[c] : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(sQ + (c >> 3) * G::kQPiece + swz128(tid, c & 7)) = v;
+      *reinterpret_cast<uint4*>(dst + (c >> 3) * G::kQPiece + swz128(tid % kRows, c & 7)) = v;
     }
   }
   fence_proxy_async();
@@ -282,28 +297,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tO = tmem + kOCol;
   const int32_t* table = p.block_tables + (long long)r * p.max_blocks_per_seq;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     // Lane j holds block table entry kb_first + 32 w + j of window w; the next window
-    // is prefetched.  Per chunk, lanes [0, NB * pieces) copy one K piece of one block
-    // each and the next NB lanes one whole V block each.
+    // is prefetched.  One elected lane issues a chunk's copies: K one piece of one
+    // block at a time, V one whole block at a time.
     const int kb_end = (k1 + BS - 1) / BS;  // blocks [kb_first, kb_end) are loaded
     auto load_window = [&](int w) {
       const int kb = kb_first + 32 * w + lane;
       return kb < kb_end ? table[kb] : -1;
     };
-    int my_b = -1, my_pc = 0;
-    bool my_v = false;
-    if (lane < NB * G::kPieces) {
-      my_b = lane / G::kPieces;
-      my_pc = lane % G::kPieces;
-    } else if (lane < G::kCopies) {
-      my_b = lane - NB * G::kPieces;
-      my_v = true;
-    }
     int cur_w = 0;
     int win = load_window(0);
     int win_next = load_window(1);
@@ -320,22 +325,34 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         win_next = load_window(w + 1);
         cur_w = w;
       }
-      const int e = __shfl_sync(0xffffffffu, win, (i * NB + (my_b < 0 ? 0 : my_b)) & 31);
-      const int kb = kb_first + i * NB + my_b;
-      const bool in_range = my_b >= 0 && kb < kb_end;
-      const bool ok_b = in_range && e >= 0 && e < p.num_blocks;
-      if (my_v && in_range && !ok_b) flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
-      const int nvalid = __popc(__ballot_sync(0xffffffffu, my_v && ok_b));
-      if (lane == 0) {
-        if (nvalid == 0) mbar_arrive(full + s);
-        else mbar_arrive_expect_tx(full + s, (uint32_t)(nvalid * 2 * G::kBlockTx));
+      int phys[NB];
+      int nvalid = 0;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        const int e = __shfl_sync(0xffffffffu, win, (i * NB + b) & 31);
+        const bool in_range = kb_first + i * NB + b < kb_end;
+        const bool ok_b = in_range && e >= 0 && e < p.num_blocks;
+        if (in_range && !ok_b && lane == 0) flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
+        phys[b] = ok_b ? e : -1;
+        nvalid += ok_b;
+      }
+      if (elect_one()) {
+        uint8_t* sk = sKV + s * G::kStageBytes;
+        if (nvalid == 0) {
+          mbar_arrive(full + s);
+        } else {
+          mbar_arrive_expect_tx(full + s, (uint32_t)(nvalid * 2 * G::kBlockTx));
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            if (phys[b] < 0) continue;
+#pragma unroll
+            for (int pc = 0; pc < G::kPieces; ++pc)
+              tma_load_4d(sk + pc * G::kPiece + b * BS * 128, &tmk, 0, kvh * BS, pc, phys[b], full + s);
+            tma_load_4d(sk + G::kKvBytes + b * G::kBlockTx, &tmv, 0, kvh * BS, 0, phys[b], full + s);
+          }
+        }
       }
       __syncwarp();
-      if (ok_b) {
-        uint8_t* sk = sKV + s * G::kStageBytes;
-        if (my_v) tma_load_4d(sk + G::kKvBytes + my_b * G::kBlockTx, &tmv, 0, kvh * BS, 0, e, full + s);
-        else tma_load_4d(sk + my_pc * G::kPiece + my_b * BS * 128, &tmk, 0, kvh * BS, my_pc, e, full + s);
-      }
       issued = i + 1;
     }
     // every copy lands before the CTA can leave
@@ -345,7 +362,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp follows the schedule (descriptors stay warp-uniform); one
-    // elected lane issues each group of MMAs and its commit.
+    // elected lane issues each group of MMAs and its commit.  Per chunk i and tile:
+    // PV(i) as soon as P(i) is in TMEM, then S(i+2) into the buffer PV(i) frees.
     const uint32_t fmt = QDT == PA_BF16 ? 1u : 0u;
     const uint32_t id_s = umma_idesc(kRows, kChunk, fmt, 0);
     const uint32_t id_o = umma_idesc(kRows, HEAD, fmt, 1);
@@ -353,71 +371,87 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const uint64_t qd0 = umma_desc(smem_u32(sQ), 16, 1024);
     const uint64_t kd0 = umma_desc(smem_u32(sKV), 16, 1024);
     const uint64_t vd0 = umma_desc(smem_u32(sKV) + G::kKvBytes, BS * 128, 1024);
-    auto issue_s = [&](int j) {
+    auto issue_s = [&](int t, int j) {
+      const uint64_t qd = qd0 + (uint64_t)((t * G::kQTile) >> 4);
       const uint64_t kd = kd0 + (uint64_t)(((j % ST) * G::kStageBytes) >> 4);
-      const uint32_t d = tmem + (j % kSBufs) * 64;
+      const uint32_t d = tmem + t * kTileCols + (j % kSBufs) * 64;
       if (elect_one()) {
 #pragma unroll
         for (int ks = 0; ks < HEAD / 16; ++ks) {
           const uint32_t qo = ((ks >> 2) * G::kQPiece + (ks & 3) * 32) >> 4;
           const uint32_t ko = ((ks >> 2) * G::kPiece + (ks & 3) * 32) >> 4;
-          umma(d, qd0 + qo, kd + ko, id_s, ks > 0 ? 1u : 0u);
+          umma(d, qd + qo, kd + ko, id_s, ks > 0 ? 1u : 0u);
         }
-        umma_commit(s_full + j % kSBufs);
+        umma_commit(s_full + t * kSBufs + j % kSBufs);
       }
       __syncwarp();
     };
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
+    };
     bool ok = true;
-    for (int j = 0; ok && j < kSBufs - 1 && j < nch; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(full + j % ST, (j / ST) & 1));
-      if (ok) {
-        tc_fence_after();
-        issue_s(j);
-      }
+    for (int j = 0; ok && j < kSBufs && j < nch; ++j) {
+      ok = wait_all(full + j % ST, (j / ST) & 1);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int t = 0; t < kTiles; ++t)
+        if (j < nch_t[t]) issue_s(t, j);
     }
     for (int i = 0; ok && i < nch; ++i) {
-      const int j = i + kSBufs - 1;  // S runs kSBufs - 1 chunks ahead of PV
-      if (j < nch) {
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(full + j % ST, (j / ST) & 1))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_s(j);
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(p_full + i % kSBufs, (i / kSBufs) & 1))) {
-        ok = false;
+      // a tail chunk's V is read only after its zeroing tile has written P(i)
+      if (tail_chunk && i == nch - 1 &&
+          !(ok = wait_all(p_full + zero_tile * kSBufs + i % kSBufs, (i / kSBufs) & 1)))
         break;
-      }
-      tc_fence_after();
-      const uint64_t vd = vd0 + (uint64_t)(((i % ST) * G::kStageBytes) >> 4);
-      const uint32_t pt = tmem + (i % kSBufs) * 64;
-      if (elect_one()) {
 #pragma unroll
-        for (int ks = 0; ks < kChunk / 16; ++ks)
-          umma_tmem_a(tO, pt + ks * 8, vd + (uint64_t)(v_row_off<HEAD, BS>(16 * ks, 0) >> 4), id_o,
-                      (i > 0 || ks > 0) ? 1u : 0u);
-        umma_commit(o_done + (i & 1));
-        umma_commit(empty + i % ST);
+      for (int t = 0; t < kTiles; ++t) {
+        if (i >= nch_t[t]) continue;
+        if (!(ok = wait_all(p_full + t * kSBufs + i % kSBufs, (i / kSBufs) & 1))) break;
+        tc_fence_after();
+        const uint64_t vd = vd0 + (uint64_t)(((i % ST) * G::kStageBytes) >> 4);
+        const uint32_t pt = tmem + t * kTileCols + (i % kSBufs) * 64;
+        const bool last_reader = t == kTiles - 1 || i >= nch_t[kTiles - 1];
+        if (elect_one()) {
+#pragma unroll
+          for (int ks = 0; ks < kChunk / 16; ++ks)
+            umma_tmem_a(tmem + t * kTileCols + kOCol, pt + ks * 8,
+                        vd + (uint64_t)(v_row_off<HEAD, BS>(16 * ks, 0) >> 4), id_o, (i > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(o_done + t * kSBufs + i % kSBufs);
+          if (last_reader) umma_commit(empty + i % ST);
+        }
+        __syncwarp();
+        const int j = i + kSBufs;
+        if (j < nch_t[t]) {
+          if (!(ok = wait_all(full + j % ST, (j / ST) & 1))) break;
+          tc_fence_after();
+          issue_s(t, j);
+        }
       }
-      __syncwarp();
     }
     if (!ok && lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
     // every MMA completes before TMEM is released
     if (elect_one()) umma_commit(mma_fin);
     __syncwarp();
-    if (!__all_sync(0xffffffffu, mbar_wait_bounded(mma_fin, 0)) && lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+    if (!wait_all(mma_fin, 0) && lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
   } else {
-    // ------------------------------------------------------------ softmax warps 0-3
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // ------------------------------------------------------------ softmax warps
+    // Warps 4t .. 4t+3 serve tile t; thread = TMEM lane = row of the tile.
+    const int t = warp >> 2;
+    const int my_nch = t == 0 ? nch_t[0] : nch_t[1];
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tT = tmem + t * kTileCols;
+    const uint32_t tO = tT + kOCol;
+    uint64_t* my_s_full = s_full + t * kSBufs;
+    uint64_t* my_p_full = p_full + t * kSBufs;
+    uint64_t* my_o_done = o_done + t * kSBufs;
     const float c = p.scale * kLog2e;
     const int row_limit = p.causal ? min(k1, row_pos + 1) : k1;  // this row attends keys < row_limit
     float m = -INFINITY, l = 0.f;
     bool fail = false;
-    for (int i = 0; i < nch; ++i) {
+    for (int i = 0; i < my_nch; ++i) {
       const int base = k0 + i * kChunk;
-      const uint32_t tS = tmem + (i % kSBufs) * 64;
-      const bool got = mbar_wait_bounded(s_full + i % kSBufs, (i / kSBufs) & 1);
+      const uint32_t tS = tT + (i % kSBufs) * 64;
+      const bool got = mbar_wait_bounded(my_s_full + i % kSBufs, (i / kSBufs) & 1);
       if (!__all_sync(0xffffffffu, got)) {
         fail = true;
         break;
@@ -440,10 +474,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       float mq[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        float t = max3(sc[8 * q], sc[8 * q + 1], sc[8 * q + 2]);
-        t = max3(t, sc[8 * q + 3], sc[8 * q + 4]);
-        t = max3(t, sc[8 * q + 5], sc[8 * q + 6]);
-        mq[q] = fmaxf(t, sc[8 * q + 7]);
+        float x = max3(sc[8 * q], sc[8 * q + 1], sc[8 * q + 2]);
+        x = max3(x, sc[8 * q + 3], sc[8 * q + 4]);
+        x = max3(x, sc[8 * q + 5], sc[8 * q + 6]);
+        mq[q] = fmaxf(x, sc[8 * q + 7]);
       }
       const float mx = max3(max3(mq[0], mq[1], mq[2]), max3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7])) * c;
       const bool need = mx > m + kRescaleSlack;
@@ -470,7 +504,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       l += lsum.x + lsum.y;
       // O is rescaled only once PV(i-1) has completed
       if (__any_sync(0xffffffffu, need) && i > 0) {
-        const bool done = mbar_wait_bounded(o_done + ((i - 1) & 1), ((i - 1) >> 1) & 1);
+        const bool done = mbar_wait_bounded(my_o_done + (i - 1) % kSBufs, ((i - 1) / kSBufs) & 1);
         if (!__all_sync(0xffffffffu, done)) {
           fail = true;
           break;
@@ -488,14 +522,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       // P(i) over the first half of S(i)'s columns
       tmem_st32(tS + lane_base, pk);
-      // V rows past the loaded keys (ragged partition end, sequence end) may hold any
-      // bits; their P is 0, so they are zeroed to keep 0 * V finite.  Each thread's
-      // stores precede its own arrival on p_full, which the PV MMA waits for.
-      if (base + kChunk > kv_loaded_end) {
+      // V rows past the loaded keys may hold any bits; their P is 0, so they are
+      // zeroed to keep 0 * V finite.  Each thread's stores precede its own arrival
+      // on p_full, which every PV of this chunk waits for.
+      if (tail_chunk && t == zero_tile && i == nch - 1) {
         const bool landed = mbar_wait_bounded(full + i % ST, (i / ST) & 1);
         const int vrem = kv_loaded_end - base;
-        if (landed && tid < G::kPieces * kChunk) {
-          const int key = tid % kChunk, pc = tid / kChunk;
+        const int rr = tid % kRows;
+        if (landed && rr < G::kPieces * kChunk) {
+          const int key = rr % kChunk, pc = rr / kChunk;
           if (key >= vrem) {
             uint4* d = reinterpret_cast<uint4*>(sKV + (i % ST) * G::kStageBytes + G::kKvBytes +
                                                 v_row_off<HEAD, BS>(key, pc));
@@ -506,21 +541,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         fence_proxy_async();
       }
       tmem_wait_st();
-      // Observe PV(i-2) (phase (i-2)/2 of o_done[i & 1]): every phase of both o_done
-      // barriers is waited for in order and never more than one phase late, so the
-      // parity waits stay unambiguous.
-      if (i >= 2) {
-        const bool done = mbar_wait_bounded(o_done + (i & 1), ((i - 2) >> 1) & 1);
+      // Observe PV(i-2): every phase of both o_done barriers is waited for in order
+      // and never more than one phase late, so the parity waits stay unambiguous.
+      if (i >= kSBufs) {
+        const bool done = mbar_wait_bounded(my_o_done + i % kSBufs, ((i - kSBufs) / kSBufs) & 1);
         if (!__all_sync(0xffffffffu, done)) {
           fail = true;
           break;
         }
       }
       tc_fence_before();
-      mbar_arrive(p_full + i % kSBufs);
+      mbar_arrive(my_p_full + i % kSBufs);
     }
-    if (!fail && nch > 0) {
-      const bool done = mbar_wait_bounded(o_done + ((nch - 1) & 1), ((nch - 1) >> 1) & 1);
+    if (!fail && my_nch > 0) {
+      const bool done = mbar_wait_bounded(my_o_done + (my_nch - 1) % kSBufs, ((my_nch - 1) / kSBufs) & 1);
       fail = !__all_sync(0xffffffffu, done);
       tc_fence_after();
     }
@@ -533,16 +567,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int parts_row = (kv_len + part - 1) / part;
       const bool write = row_valid && z < parts_row;
       const bool direct = parts_row == 1;
-      const int t = t0 + row_tok;
+      const int tq = t0 + row_tok;
       const int head = h0 + row_head;
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const long long pi = (long long)p.part_off[r] + (long long)t * parts_req + z;
-      typename QE::T* o_row = reinterpret_cast<typename QE::T*>(p.out) + ((long long)(qs + t) * p.num_q_heads + head) * HEAD;
+      const long long pi = (long long)p.part_off[r] + (long long)tq * parts_req + z;
+      typename QE::T* o_row =
+          reinterpret_cast<typename QE::T*>(p.out) + ((long long)(qs + tq) * p.num_q_heads + head) * HEAD;
       float* w_row = p.ws_acc + (pi * p.num_q_heads + head) * HEAD;
 #pragma unroll 1
       for (int cb = 0; cb < HEAD; cb += 32) {
         uint32_t o[32];
-        if (nch > 0) {
+        if (my_nch > 0) {
           tmem_ld32(tO + cb + lane_base, o);
           tmem_wait_ld();
         } else {
@@ -616,6 +651,14 @@ cudaError_t launch_tc_shape(const AttnParams& p, int num_items, const CUtensorMa
 }
 
 }  // namespace
+
+// Query tokens of one prefill CTA: two 128-row tiles whose rows are (token, head)
+// pairs, the head group padded to a power of two, at most 8 heads per tile.
+int prefill_tile_tokens(int group) {
+  int g8 = 1;
+  while (g8 < group && g8 < 8) g8 <<= 1;
+  return kTiles * kRows / g8;
+}
 
 bool prefill_tc_supported(int q_dtype, int kv_dtype, int head_size, int block_size) {
   if (!(q_dtype == PA_BF16 || q_dtype == PA_F16) || kv_dtype != q_dtype) return false;

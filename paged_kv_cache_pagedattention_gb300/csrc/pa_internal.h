@@ -72,7 +72,7 @@ struct ScatterParams {
   int block_size;
 };
 
-// Tokens of query rows in one prefill tile of the tensor-core varlen kernel.
+// Query tokens handled by one CTA of the tcgen05 prefill kernel.
 int prefill_tile_tokens(int group);
 
 cudaError_t launch_reshape_and_cache(const ScatterParams& p, int src_dtype, int cache_dtype,
