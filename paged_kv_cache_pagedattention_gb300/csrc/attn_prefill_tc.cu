@@ -5,23 +5,26 @@
 // the request's cached prefix and, causally, the chunk itself; [NOTES] "Prefill 与
 // Decode": this work is dense and compute-bound.
 //
-// One CTA per work item of the varlen plan (request, first query row of the tile,
-// partition of the keys) and per (KV head, group of <= 8 query heads).  The tile's
-// 128 query rows are (token, head) pairs, token-major (row = token * GP + head, GP =
-// the head group padded to a power of two); row r lives in TMEM lane r.  Keys stream
-// in chunks of 64 tokens (whole paged blocks), staged by TMA:
-//   S(i)  = Q K(i)^T    M = 128 rows, N = 64 keys, K = head dim   -> TMEM (3 buffers)
+// One CTA per work item of the varlen plan (request, first query row, partition of
+// the keys) and per (KV head, group of <= 8 query heads).  Its 256 query rows are
+// (token, head) pairs, token-major (row = token * GP + head, GP = the head group
+// padded to a power of two), split into two tiles of 128 rows; row r of a tile lives
+// in TMEM lane r.  Keys stream in chunks of 64 tokens (whole paged blocks) staged by
+// TMA, and every chunk serves both tiles.  Per tile and chunk i:
+//   S(i)  = Q K(i)^T    M = 128 rows, N = 64 keys, K = head dim   -> TMEM (2 buffers)
 //   P(i)  = softmax numerators of S(i), 16-bit, written over S(i) -> TMEM
 //   O    += P(i) V(i)   M = 128 rows, N = head dim, K = 64 keys   -> TMEM (A from TMEM)
-// Warps 0-3 own one row per thread: they read S(i) from TMEM, keep the running max
-// (in log2 units, raised only when a chunk exceeds it by more than kRescaleSlack;
-// then O is rescaled in TMEM) and the running sum, and write P(i) back into the
-// first 32 columns of S(i)'s buffer (two 16-bit values per column).  Warp 4 loads:
-// its lanes read the block table a window at a time and one elected lane issues
-// the chunk's TMA copies.  Warp 5 allocates TMEM and issues the MMAs from one elected
-// lane, in the order S(0) S(1) S(2) PV(0) S(3) PV(1) ...; the tensor core runs
-// them in issue order, so S(i+3) never overwrites P(i) before PV(i) has read it,
-// and the softmax of chunk i overlaps PV(i-1) and S(i+2).
+// Warps:
+//   0-3, 4-7  softmax of tile 0, tile 1: one row per thread; read S(i) from TMEM,
+//             keep the running max (log2 units, raised only when a chunk exceeds it
+//             by more than kRescaleSlack; then O is rescaled in TMEM) and sum, write
+//             P(i) over the first 32 columns of S(i)'s buffer (two values a column);
+//   8, 9      TMA producers of K (one piece of one block per copy) and V (one block
+//             per copy), from a block-table window read by their lanes;
+//   10, 11    MMA issuers of tile 0, tile 1 (warp 10 also owns TMEM): PV(i) once
+//             P(i) is written, then S(i+2) into the buffer PV(i) frees.  A thread's
+//             MMAs run in issue order, so S(i+2) never overwrites P(i) before PV(i)
+//             has read it; the softmax of chunk i+1 overlaps PV(i) and S(i+2).
 // Shared memory: Q and each K chunk are K-major, [64-element piece][row][128 bytes];
 // V is MN-major (head dim contiguous) and kept as the cache lays it out per block,
 // [block][piece][token][128 bytes], one TMA box per block; every operand uses the
@@ -36,9 +39,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kRows = 128;        // query rows per tile = TMEM lanes
 constexpr int kTiles = 2;         // tiles per CTA, sharing every K/V chunk
 constexpr int kChunk = 64;        // keys per chunk
-constexpr int kThreadsTc = (4 * kTiles + 2) * 32;
-constexpr int kProducerWarp = 4 * kTiles;
-constexpr int kMmaWarp = 4 * kTiles + 1;
+constexpr int kProducerWarp = 4 * kTiles;  // K copies; the next warp issues the V copies
+constexpr int kMmaWarp = 4 * kTiles + 2;   // one MMA warp per tile; the first owns TMEM
+constexpr int kThreadsTc = (kMmaWarp + kTiles) * 32;
 constexpr int kSBufs = 2;         // S / P buffers per tile, 64 TMEM columns each
 constexpr int kOCol = 128;        // a tile's O: columns [128, 128 + head dim) of its 256
 constexpr int kTileCols = 256;
@@ -259,15 +262,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
     for (int i = 0; i < ST; ++i) {
-      mbar_init(full + i, 1);
-      mbar_init(empty + i, 1);
+      mbar_init(full + i, 2);        // the K and the V producer
+      mbar_init(empty + i, kTiles);  // every tile's MMA warp
     }
     for (int i = 0; i < kTiles * kSBufs; ++i) {
       mbar_init(s_full + i, 1);
       mbar_init(p_full + i, kRows);
       mbar_init(o_done + i, 1);
     }
-    mbar_init(mma_fin, 1);
+    mbar_init(mma_fin, kTiles);
     fence_mbar_init();
   }
   // CTA row R = token * gp + head; tile R / 128, TMEM lane R % 128
@@ -299,11 +302,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const uint32_t tmem = *tmem_slot;
   const int32_t* table = p.block_tables + (long long)r * p.max_blocks_per_seq;
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == kProducerWarp || warp == kProducerWarp + 1) {
+    // ------------------------------------------------------------ TMA producers
     // Lane j holds block table entry kb_first + 32 w + j of window w; the next window
-    // is prefetched.  One elected lane issues a chunk's copies: K one piece of one
-    // block at a time, V one whole block at a time.
+    // is prefetched.  An elected lane of the first warp copies a chunk's K one piece
+    // of one block at a time; the second warp's copies V one whole block at a time.
+    // Each arrives once per chunk on full with its own byte count.
+    const bool is_v = warp != kProducerWarp;
     const int kb_end = (k1 + BS - 1) / BS;  // blocks [kb_first, kb_end) are loaded
     auto load_window = [&](int w) {
       const int kb = kb_first + 32 * w + lane;
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int e = __shfl_sync(0xffffffffu, win, (i * NB + b) & 31);
         const bool in_range = kb_first + i * NB + b < kb_end;
         const bool ok_b = in_range && e >= 0 && e < p.num_blocks;
-        if (in_range && !ok_b && lane == 0) flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
+        if (in_range && !ok_b && lane == 0 && !is_v) flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
         phys[b] = ok_b ? e : -1;
         nvalid += ok_b;
       }
@@ -341,14 +346,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         if (nvalid == 0) {
           mbar_arrive(full + s);
         } else {
-          mbar_arrive_expect_tx(full + s, (uint32_t)(nvalid * 2 * G::kBlockTx));
+          mbar_arrive_expect_tx(full + s, (uint32_t)(nvalid * G::kBlockTx));
 #pragma unroll
           for (int b = 0; b < NB; ++b) {
             if (phys[b] < 0) continue;
+            if (is_v) {
+              tma_load_4d(sk + G::kKvBytes + b * G::kBlockTx, &tmv, 0, kvh * BS, 0, phys[b], full + s);
+            } else {
 #pragma unroll
-            for (int pc = 0; pc < G::kPieces; ++pc)
-              tma_load_4d(sk + pc * G::kPiece + b * BS * 128, &tmk, 0, kvh * BS, pc, phys[b], full + s);
-            tma_load_4d(sk + G::kKvBytes + b * G::kBlockTx, &tmv, 0, kvh * BS, 0, phys[b], full + s);
+              for (int pc = 0; pc < G::kPieces; ++pc)
+                tma_load_4d(sk + pc * G::kPiece + b * BS * 128, &tmk, 0, kvh * BS, pc, phys[b], full + s);
+            }
           }
         }
       }
@@ -359,22 +367,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (lane == 0)
       for (int j = max(0, issued - ST); j < issued; ++j)
         if (!mbar_wait_bounded(full + j % ST, (j / ST) & 1)) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp follows the schedule (descriptors stay warp-uniform); one
-    // elected lane issues each group of MMAs and its commit.  Per chunk i and tile:
-    // PV(i) as soon as P(i) is in TMEM, then S(i+2) into the buffer PV(i) frees.
+  } else if (warp >= kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    // One warp per tile follows that tile's schedule (descriptors stay
+    // warp-uniform); an elected lane issues each group of MMAs and its commit.  Per
+    // chunk i: PV(i) as soon as P(i) is in TMEM, then S(i+2) into the buffer PV(i)
+    // frees.  The two tiles' streams run independently on the tensor core.
+    const int t = warp - kMmaWarp;
+    const int my_nch = t == 0 ? nch_t[0] : nch_t[1];
     const uint32_t fmt = QDT == PA_BF16 ? 1u : 0u;
     const uint32_t id_s = umma_idesc(kRows, kChunk, fmt, 0);
     const uint32_t id_o = umma_idesc(kRows, HEAD, fmt, 1);
     // descriptor start addresses count 16-byte units: offsets are added pre-shifted
-    const uint64_t qd0 = umma_desc(smem_u32(sQ), 16, 1024);
+    const uint64_t qd = umma_desc(smem_u32(sQ) + t * G::kQTile, 16, 1024);
     const uint64_t kd0 = umma_desc(smem_u32(sKV), 16, 1024);
     const uint64_t vd0 = umma_desc(smem_u32(sKV) + G::kKvBytes, BS * 128, 1024);
-    auto issue_s = [&](int t, int j) {
-      const uint64_t qd = qd0 + (uint64_t)((t * G::kQTile) >> 4);
+    const uint32_t tT = tmem + t * kTileCols;
+    uint64_t* my_p_full = p_full + t * kSBufs;
+    auto issue_s = [&](int j) {
       const uint64_t kd = kd0 + (uint64_t)(((j % ST) * G::kStageBytes) >> 4);
-      const uint32_t d = tmem + t * kTileCols + (j % kSBufs) * 64;
+      const uint32_t d = tT + (j % kSBufs) * 64;
       if (elect_one()) {
 #pragma unroll
         for (int ks = 0; ks < HEAD / 16; ++ks) {
@@ -390,46 +402,47 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
     };
     bool ok = true;
-    for (int j = 0; ok && j < kSBufs && j < nch; ++j) {
+    for (int j = 0; ok && j < kSBufs && j < my_nch; ++j) {
       ok = wait_all(full + j % ST, (j / ST) & 1);
       if (!ok) break;
       tc_fence_after();
-#pragma unroll
-      for (int t = 0; t < kTiles; ++t)
-        if (j < nch_t[t]) issue_s(t, j);
+      issue_s(j);
     }
     for (int i = 0; ok && i < nch; ++i) {
+      if (i >= my_nch) {
+        // This tile does not read chunk i.  It still releases the stage once, after
+        // the chunk has landed (so it never arrives twice within one phase).
+        if (!(ok = wait_all(full + i % ST, (i / ST) & 1))) break;
+        if (elect_one()) mbar_arrive(empty + i % ST);
+        __syncwarp();
+        continue;
+      }
       // a tail chunk's V is read only after its zeroing tile has written P(i)
-      if (tail_chunk && i == nch - 1 &&
+      if (tail_chunk && i == nch - 1 && t != zero_tile &&
           !(ok = wait_all(p_full + zero_tile * kSBufs + i % kSBufs, (i / kSBufs) & 1)))
         break;
+      if (!(ok = wait_all(my_p_full + i % kSBufs, (i / kSBufs) & 1))) break;
+      tc_fence_after();
+      const uint64_t vd = vd0 + (uint64_t)(((i % ST) * G::kStageBytes) >> 4);
+      const uint32_t pt = tT + (i % kSBufs) * 64;
+      if (elect_one()) {
 #pragma unroll
-      for (int t = 0; t < kTiles; ++t) {
-        if (i >= nch_t[t]) continue;
-        if (!(ok = wait_all(p_full + t * kSBufs + i % kSBufs, (i / kSBufs) & 1))) break;
+        for (int ks = 0; ks < kChunk / 16; ++ks)
+          umma_tmem_a(tT + kOCol, pt + ks * 8, vd + (uint64_t)(v_row_off<HEAD, BS>(16 * ks, 0) >> 4), id_o,
+                      (i > 0 || ks > 0) ? 1u : 0u);
+        umma_commit(o_done + t * kSBufs + i % kSBufs);
+        umma_commit(empty + i % ST);
+      }
+      __syncwarp();
+      const int j = i + kSBufs;
+      if (j < my_nch) {
+        if (!(ok = wait_all(full + j % ST, (j / ST) & 1))) break;
         tc_fence_after();
-        const uint64_t vd = vd0 + (uint64_t)(((i % ST) * G::kStageBytes) >> 4);
-        const uint32_t pt = tmem + t * kTileCols + (i % kSBufs) * 64;
-        const bool last_reader = t == kTiles - 1 || i >= nch_t[kTiles - 1];
-        if (elect_one()) {
-#pragma unroll
-          for (int ks = 0; ks < kChunk / 16; ++ks)
-            umma_tmem_a(tmem + t * kTileCols + kOCol, pt + ks * 8,
-                        vd + (uint64_t)(v_row_off<HEAD, BS>(16 * ks, 0) >> 4), id_o, (i > 0 || ks > 0) ? 1u : 0u);
-          umma_commit(o_done + t * kSBufs + i % kSBufs);
-          if (last_reader) umma_commit(empty + i % ST);
-        }
-        __syncwarp();
-        const int j = i + kSBufs;
-        if (j < nch_t[t]) {
-          if (!(ok = wait_all(full + j % ST, (j / ST) & 1))) break;
-          tc_fence_after();
-          issue_s(t, j);
-        }
+        issue_s(j);
       }
     }
     if (!ok && lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-    // every MMA completes before TMEM is released
+    // every MMA of both tiles completes before TMEM is released
     if (elect_one()) umma_commit(mma_fin);
     __syncwarp();
     if (!wait_all(mma_fin, 0) && lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
