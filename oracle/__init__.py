@@ -33,6 +33,7 @@ from .paged_attention import (  # noqa: F401
     attend,
     blocks_needed,
     bytes_per_block,
+    copy_blocks,
     decode_bits,
     e4m3_encode,
     e4m3_value,

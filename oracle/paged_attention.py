@@ -201,6 +201,35 @@ def reshape_and_cache(key_bits, value_bits, k_cache, v_cache, slot_mapping,
 
 
 # --------------------------------------------------------------------------
+# Copy-on-write block copy
+# --------------------------------------------------------------------------
+
+def copy_blocks(k_cache, v_cache, block_mapping) -> list:
+    """Copy whole physical blocks, K and V, in place: ``cache[dst] = cache[src]``.
+
+    [AGENTIC] "統一分頁 + 共用池" (reference counting + copy-on-write): forked
+    sequences point their block tables at the same physical blocks and a block
+    is duplicated only when shared content must change.  [LINEAGE] "Prefix
+    reuse": a shared block that is not yet full must be copied before either
+    branch writes its next token into it, or one branch would overwrite the
+    other's history.  ``block_mapping`` is ``[num_pairs][2]`` (src, dst); a pair
+    with an index outside ``[0, num_blocks)`` is skipped.  The caller keeps every
+    dst distinct and never also a src, so the pairs are independent.  Returns the
+    indices of the skipped pairs.
+    """
+    num_blocks = k_cache.shape[0]
+    skipped = []
+    for i, (src, dst) in enumerate(np.asarray(block_mapping, dtype=np.int64).reshape(-1, 2)):
+        src, dst = int(src), int(dst)
+        if not (0 <= src < num_blocks and 0 <= dst < num_blocks):
+            skipped.append(i)
+            continue
+        k_cache[dst] = k_cache[src].copy()
+        v_cache[dst] = v_cache[src].copy()
+    return skipped
+
+
+# --------------------------------------------------------------------------
 # Block-table resolution and attention
 # --------------------------------------------------------------------------
 

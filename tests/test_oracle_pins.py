@@ -402,6 +402,72 @@ def test_shared_prefix_blocks_equal_private_copies():
     assert np.array_equal(both[parent], both[fam[2]])
 
 
+# ---------------------------------------------------------------- copy-on-write
+
+def test_copy_blocks_copies_whole_blocks_and_nothing_else():
+    rng = np.random.default_rng(31)
+    kc = rng.integers(0, 2 ** 16, size=(12, 2, 16, 64), dtype=np.uint16)
+    vc = rng.integers(0, 2 ** 16, size=(12, 2, 16, 64), dtype=np.uint16)
+    k0, v0 = kc.copy(), vc.copy()
+    pairs = np.array([[3, 7], [0, 11], [5, 5], [2, 12], [-1, 4]], np.int64)
+    assert oracle.copy_blocks(kc, vc, pairs) == [3, 4]      # out-of-range pairs skipped
+    for src, dst in ((3, 7), (0, 11), (5, 5)):
+        assert np.array_equal(kc[dst], k0[src]) and np.array_equal(vc[dst], v0[src])
+    rest = [b for b in range(12) if b not in (7, 11)]
+    assert np.array_equal(kc[rest], k0[rest]) and np.array_equal(vc[rest], v0[rest])
+    assert oracle.copy_blocks(kc, vc, np.zeros((0, 2), np.int64)) == []
+
+
+def _fork_appends(cow: bool):
+    """A parent of 40 tokens (block 16: the third block holds 8) and a fork sharing all
+    three blocks each append a different token at position 40.  Returns the paged
+    decode of both and, for each, SDPA on its own dense history (fp64, torch)."""
+    rng = np.random.default_rng(32)
+    bs, hkv, hq, d, L, nb = 16, 2, 4, 32, 40, 8
+    hist_k = rng.standard_normal((L, hkv, d)).astype(np.float32)
+    hist_v = rng.standard_normal((L, hkv, d)).astype(np.float32)
+    new_k = rng.standard_normal((2, hkv, d)).astype(np.float32)    # parent's, fork's
+    new_v = rng.standard_normal((2, hkv, d)).astype(np.float32)
+    q = rng.standard_normal((2, hq, d)).astype(np.float32)
+    kc = np.zeros((nb, hkv, bs, d), np.uint32)
+    vc = np.zeros((nb, hkv, bs, d), np.uint32)
+    table = np.array([[4, 1, 6, 0], [4, 1, 6, 0]], np.int32)
+    slots = np.array([table[0, t // bs] * bs + t % bs for t in range(L)], np.int64)
+    oracle.reshape_and_cache(hist_k.view(np.uint32), hist_v.view(np.uint32), kc, vc, slots, bs, "f32", "f32")
+    if cow:   # the fork takes a private copy of the shared, not yet full tail block
+        assert oracle.copy_blocks(kc, vc, [[6, 7]]) == []
+        table[1, 2] = 7
+    for r in (0, 1):
+        slot = [table[r, L // bs] * bs + L % bs]
+        oracle.reshape_and_cache(new_k[r:r + 1].view(np.uint32), new_v[r:r + 1].view(np.uint32), kc, vc,
+                                 slot, bs, "f32", "f32")
+    scale = 0.3
+    out = oracle.paged_decode(q.view(np.uint32), "f32", kc, vc, "f32", table, [L + 1, L + 1], bs, scale)
+    refs = []
+    for r in (0, 1):
+        K = torch.from_numpy(np.concatenate([hist_k, new_k[r:r + 1]])).double()    # [L+1][hkv][d]
+        V = torch.from_numpy(np.concatenate([hist_v, new_v[r:r + 1]])).double()
+        K = K.permute(1, 0, 2).repeat_interleave(hq // hkv, dim=0)                 # [hq][L+1][d]
+        V = V.permute(1, 0, 2).repeat_interleave(hq // hkv, dim=0)
+        qq = torch.from_numpy(q[r]).double()[:, None, :]                           # [hq][1][d]
+        refs.append(torch.nn.functional.scaled_dot_product_attention(qq, K, V, scale=scale)[:, 0, :].numpy())
+    return out, refs
+
+
+def test_copy_on_write_keeps_each_branch_history():
+    out, (ref_parent, ref_fork) = _fork_appends(cow=True)
+    assert np.abs(out[0] - ref_parent).max() < 1e-12
+    assert np.abs(out[1] - ref_fork).max() < 1e-12
+
+
+def test_without_copy_on_write_the_fork_overwrites_the_parent():
+    # [LINEAGE] "Prefix reuse": skipping the copy lets the later writer replace the
+    # other branch's token in the shared tail block.
+    out, (ref_parent, ref_fork) = _fork_appends(cow=False)
+    assert np.abs(out[0] - ref_parent).max() > 1e-3
+    assert np.abs(out[1] - ref_fork).max() < 1e-12
+
+
 def test_chunked_prefill_equals_single_chunk():
     """Queries of a prompt give the same output whether processed in one chunk or two."""
     q, kc, vc, table = _contiguous_case(13, 23, 8, 2, 16, 23)
