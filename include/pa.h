@@ -3,7 +3,8 @@
  *
  * The library implements the data-parallel hot path of paged KV cache serving:
  *   1. pa_reshape_and_cache  writes the K/V of new tokens into fixed-size physical
- *                            blocks through a per-token slot mapping;
+ *                            blocks through a per-token slot mapping
+ *                            (pa_copy_blocks duplicates blocks for copy-on-write);
  *   2. pa_decode             PagedAttention decode: one query token per sequence
  *                            attends the sequence's whole cached context, read
  *                            through its block table (split-K over the context
@@ -130,6 +131,32 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
                                int32_t num_kv_heads, int32_t head_size, int32_t block_size,
                                pa_dtype src_dtype, pa_dtype cache_dtype, const float* k_scale,
                                const float* v_scale, pa_stream_t stream);
+
+/*
+ * pa_copy_blocks -- copy whole physical blocks of the paged cache (copy-on-write).
+ * [AGENTIC] "統一分頁 + 共用池": with reference counting and copy-on-write, forked
+ * sequences' block tables point at the same physical blocks, and a block is
+ * duplicated only when shared content has to change.  [LINEAGE] "Prefix reuse":
+ * a shared block that is not yet full must be copied before either branch writes
+ * its next token into it; otherwise one branch overwrites the other's history.
+ * The caller (which owns the reference counts) picks the destination block, calls
+ * this, points the writing branch's block table at the copy, then writes.
+ *
+ *   k_cache, v_cache  cache tensors (layout above), cache_dtype (any pa_dtype;
+ *                  only its size matters: the bytes are copied exactly)
+ *   block_mapping  int64 [num_pairs][2], pairs (src, dst): block dst of both
+ *                  tensors becomes a copy of block src (all KV heads, all
+ *                  block_size slots).  A pair with src or dst outside
+ *                  [0, num_blocks) is skipped and sets PA_ERRFLAG_BLOCK_TABLE;
+ *                  src == dst is a no-op.  Destinations must be distinct and no
+ *                  destination may also be a source in the same call (otherwise
+ *                  the result is unspecified).
+ *   head_size * dtype_bytes must be a multiple of 16; both tensors 16-byte aligned.
+ * num_pairs == 0 returns PA_OK and launches nothing.
+ */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping, int32_t num_pairs,
+                         int32_t num_blocks, int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                         pa_dtype cache_dtype, pa_stream_t stream);
 
 /*
  * Context tokens per split-K partition that pa_decode / pa_varlen_attn use when
@@ -319,9 +346,9 @@ pa_status pa_get_error_flags(uint32_t* flags, int32_t clear, pa_stream_t stream)
  * synchronises those events and, for kernel kind `kind` (0 = reshape_and_cache,
  * 1 = attention main kernel, 2 = partial merge, 3 = varlen plan,
  * 4 = prefill tiles, 5 = shared-prefix tiles, 6 = the span of the shared-prefix
- * and private-remainder kernels of pa_decode_shared_prefix), returns the launch
- * count and the summed device
- * milliseconds since the last reset (reset != 0 clears every kind).
+ * and private-remainder kernels of pa_decode_shared_prefix, 7 = copy_blocks),
+ * returns the launch count and the summed device milliseconds since the last
+ * reset (reset != 0 clears every kind).
  * Tracing is off by default and costs nothing when off.  Not thread-safe.
  */
 pa_status pa_trace_enable(int32_t on);

@@ -36,7 +36,7 @@ PA_ERRFLAG_BLOCK_TABLE, PA_ERRFLAG_SLOT, PA_ERRFLAG_SEQ_LEN, PA_ERRFLAG_QUERY, P
 
 # Names of the kernel kinds reported by pa_trace_read.
 TRACE_KINDS = ("reshape_and_cache", "attention", "merge", "varlen_plan", "prefill_tiles", "shared_prefix",
-               "shared_span")
+               "shared_span", "copy_blocks")
 
 # Every symbol include/pa.h declares, with its ctypes signature.
 _P, _I32, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
@@ -45,6 +45,7 @@ SIGNATURES = {
     "pa_version": (_I32, []),
     "pa_reshape_and_cache": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32,
                                             ctypes.c_int, ctypes.c_int, _P, _P, _P]),
+    "pa_copy_blocks": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, ctypes.c_int, _P]),
     "pa_default_partition_size": (_I32, [_I32, _I32, _I32, _I32]),
     "pa_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "pa_decode": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
@@ -127,6 +128,20 @@ def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, k_scale=Non
                                      _ptr(slot_mapping), key.shape[0], nb, hkv, d, bs,
                                      dtype_code(key), dtype_code(k_cache), _ptr(k_scale), _ptr(v_scale),
                                      _stream(stream)), "pa_reshape_and_cache")
+
+
+def pa_copy_blocks(k_cache, v_cache, block_mapping, stream=None) -> None:
+    """Copy whole physical blocks: block_mapping is int64 [num_pairs][2] of (src, dst)."""
+    nb, hkv, bs, d = k_cache.shape
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or v_cache.dtype != k_cache.dtype:
+        raise ValueError("k_cache and v_cache must match")
+    if block_mapping.dtype != torch.int64 or block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
+        raise ValueError("block_mapping must be int64 [num_pairs][2]")
+    if not block_mapping.is_contiguous():
+        raise ValueError("block_mapping must be contiguous")
+    n = block_mapping.shape[0]
+    _check(_lib.pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_mapping) if n else None, n, nb, hkv, d,
+                               bs, dtype_code(k_cache), _stream(stream)), "pa_copy_blocks")
 
 
 def pa_default_partition_size(num_seqs, num_kv_heads, max_seq_len, block_size) -> int:

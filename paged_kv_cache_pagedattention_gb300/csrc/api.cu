@@ -207,7 +207,7 @@ bool encode_cache_map(CUtensorMap* m, const void* base, int kv_dtype, int num_bl
 
 // ------------------------------------------------------------------ tracing
 
-constexpr int kTraceKinds = 7;
+constexpr int kTraceKinds = 8;
 bool g_trace_on = false;
 struct TraceSlot {
   int kind;
@@ -404,6 +404,30 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   TraceScope t(0, s);
   return cuda_status(pa::launch_reshape_and_cache(p, src_dtype, cache_dtype, s));
+}
+
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping, int32_t num_pairs,
+                         int32_t num_blocks, int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                         pa_dtype cache_dtype, pa_stream_t stream) {
+  if (num_pairs < 0 || num_blocks < 1 || num_kv_heads < 1 || head_size < 1 || block_size < 1)
+    return PA_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !block_mapping) return PA_ERR_INVALID_ARG;
+  const int eb = dtype_bytes(cache_dtype);
+  if (eb == 0) return PA_ERR_UNSUPPORTED;
+  if ((head_size * eb) % 16) return PA_ERR_UNSUPPORTED;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return PA_ERR_INVALID_ARG;
+  pa::CopyParams p;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_mapping = block_mapping;
+  p.err = error_word();
+  p.num_pairs = num_pairs;
+  p.num_blocks = num_blocks;
+  p.block_bytes = (long long)num_kv_heads * block_size * head_size * eb;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  TraceScope t(7, s);
+  return cuda_status(pa::launch_copy_blocks(p, s));
 }
 
 int32_t pa_default_partition_size(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,

@@ -72,6 +72,18 @@ struct ScatterParams {
   int block_size;
 };
 
+struct CopyParams {
+  void* k_cache;
+  void* v_cache;
+  const int64_t* block_mapping;  // [num_pairs][2] (src, dst)
+  unsigned* err;
+  int num_pairs;
+  int num_blocks;
+  long long block_bytes;         // bytes of one block of one cache tensor
+};
+
+cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
+
 // Query tokens handled by one CTA of the tcgen05 prefill kernel.
 int prefill_tile_tokens(int group);
 

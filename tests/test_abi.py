@@ -107,3 +107,16 @@ def test_non_positive_scale_rejected_without_a_gpu(pa):
         st = fn(fake, fake, fake, fake, 10, fake, 4, fake, 2, 64, 8, 2, 128, 16, scale, 2, 2, None, None, 0,
                 fake, 1 << 30, None)
         assert st == pa.PA_ERR_INVALID_ARG, scale
+
+
+def test_copy_blocks_host_validation_without_a_gpu(pa):
+    lib = ctypes.CDLL(pa.LIB_PATH)
+    fn = lib.pa_copy_blocks
+    fn.restype, fn.argtypes = pa.SIGNATURES["pa_copy_blocks"]
+    assert fn(None, None, None, 0, 10, 2, 128, 16, pa.PA_BF16, None) == pa.PA_OK      # nothing to copy
+    assert fn(None, None, None, 3, 10, 2, 128, 16, pa.PA_BF16, None) == pa.PA_ERR_INVALID_ARG
+    assert fn(None, None, None, -1, 10, 2, 128, 16, pa.PA_BF16, None) == pa.PA_ERR_INVALID_ARG
+    fake = 1 << 20  # aligned, never dereferenced: the checks return first
+    assert fn(fake, fake, fake, 3, 10, 2, 128, 16, 7, None) == pa.PA_ERR_UNSUPPORTED   # unknown dtype
+    assert fn(fake, fake, fake, 3, 10, 2, 4, 16, pa.PA_F16, None) == pa.PA_ERR_UNSUPPORTED  # 8-byte rows
+    assert fn(fake + 8, fake, fake, 3, 10, 2, 128, 16, pa.PA_BF16, None) == pa.PA_ERR_INVALID_ARG
