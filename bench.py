@@ -622,6 +622,109 @@ def run_ours(args):
     return 0
 
 
+def run_copy_blocks(args):
+    """Copy-on-write block copy measured alone: a Llama-sized bf16 pool (18,432
+    blocks of 8 KV heads x 16 slots x 128 dims) and 4,096 disjoint (src, dst) pairs
+    per step, two pair sets alternating (each step moves 537 MB: > L2)."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_pagedattention_gb300 as pa
+
+    rank, local_rank, world = dist_env()
+    if world > 1 and rank != 0:
+        return 0  # one GPU's kernel; further ranks would only repeat it
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    nb, hkv, bs, d, npairs = 18432, 8, 16, 128, 4096
+    g = torch.Generator(device=dev).manual_seed(11)
+    kc = torch.randn(nb, hkv, bs, d, device=dev, generator=g).to(torch.bfloat16)
+    vc = torch.randn(nb, hkv, bs, d, device=dev, generator=g).to(torch.bfloat16)
+    rng = np.random.default_rng(12)
+    maps = []
+    for _ in range(2):
+        perm = rng.permutation(nb)
+        maps.append(np.stack([perm[:npairs], perm[npairs:2 * npairs]], 1).astype(np.int64))
+    dmaps = [torch.from_numpy(m).to(dev) for m in maps]
+    stream = torch.cuda.current_stream(dev)
+    block_bytes = hkv * bs * d * 2
+    moved = 2 * 2 * block_bytes * npairs  # K and V, each read once and written once
+    for i in range(args.warmup):
+        pa.pa_copy_blocks(kc, vc, dmaps[i % 2], stream)
+    torch.cuda.synchronize(dev)
+    if pa.pa_get_error_flags():
+        raise RuntimeError("device error flags during warm-up")
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        pass
+    sampler = ClockSampler(bus)
+    sampler.start()
+    pa.pa_trace_read(0, reset=True)
+    pa.pa_trace_enable(True)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        pa.pa_copy_blocks(kc, vc, dmaps[i % 2], stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    pa.pa_trace_enable(False)
+    clocks = sampler.stop()
+    n_copy, ms_copy = pa.pa_trace_read(7)
+    ms_per_step = e0.elapsed_time(e1) / args.steps
+    gbs = moved / (ms_per_step / 1e3) / 1e9
+    peak, peak_kind = measured_peaks()
+    kern_ms = ms_copy / n_copy if n_copy else ms_per_step
+    achieved = moved / (kern_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": None, "kernel": "copy_blocks_kernel", "kernel_ms": kern_ms,
+                "algorithmic_bytes_per_launch": moved, "peak_source": f"{peak_kind} MEASURED_PEAKS.json hbm_gbs"}
+    e2e = None
+    if not args.no_e2e:
+        hmaps = [torch.from_numpy(m).pin_memory() for m in maps]
+        dmap = torch.empty_like(dmaps[0])
+        hflags = torch.empty(1, dtype=torch.int32).pin_memory()
+        torch.cuda.synchronize(dev)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            dmap.copy_(hmaps[i % 2], non_blocking=True)
+            pa.pa_copy_blocks(kc, vc, dmap, stream)
+            hflags.copy_(dmap[0, :1].to(torch.int32), non_blocking=True)  # completion read-back
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = t0.elapsed_time(t1) / args.steps
+        e2e = {"value": moved / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": maps[0].nbytes,
+               "d2h_bytes_per_step": 4, "ms_per_step": e2e_ms}
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+
+        # the oracle copying 64 pairs of host blocks of the same shape
+        kh = np.random.default_rng(13).integers(0, 2 ** 16, size=(256, hkv, bs, d), dtype=np.uint16)
+        vh = kh.copy()
+        pairs = np.stack([np.arange(64), np.arange(64, 128)], 1)
+        t = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t < 2.0:
+            oracle.copy_blocks(kh, vh, pairs)
+            reps += 1
+        dt = time.perf_counter() - t
+        cpu = {"value": reps * 64 * 4 * block_bytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{reps} x 64 block pairs (8 x 16 x 128 bf16) in 2 s"}
+    line = {"metric": "copy-on-write block copy: HBM GB/s (bytes read + written)", "value": gbs, "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "replicas only", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) cache, seeded disjoint pairs)",
+            "config": {"workload": "copy_blocks", "num_blocks": nb, "num_kv_heads": hkv, "block_size": bs,
+                       "head_size": d, "pairs_per_step": npairs, "l2": "537 MB moved per step (> L2)"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_copy, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -634,6 +737,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-shared-prefix", action="store_true",
                     help="agentic: call pa_decode instead of pa_decode_shared_prefix")
+    ap.add_argument("--op", choices=("attention", "copy_blocks"), default="attention",
+                    help="copy_blocks: time the copy-on-write block copy alone")
     ap.add_argument("--length-scale", type=float, default=1.0,
                     help="shrink every sequence length (profiling captures only; 1.0 = the named workload)")
     args = ap.parse_args(argv)
@@ -641,6 +746,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.op == "copy_blocks":
+        return run_copy_blocks(args)
     return run_ours(args)
 
 
