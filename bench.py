@@ -448,9 +448,9 @@ def run_ours(args):
         gshared = torch.from_numpy(groups[1]).to(dev)
         max_group = int(max(groups[0][1:] - groups[0][:-1]))
     ws = pa.workspace_tensor(wsb, dev)
-    stream = torch.cuda.current_stream(dev)
 
     def step(q_=q, key_=key, value_=val, slots_=slots, tables_=tables, lens_=lens, qsl_=qsl, out_=out):
+        stream = torch.cuda.current_stream(dev)  # the capture stream while a graph is recorded
         pa.pa_reshape_and_cache(key_, value_, kc, vc, slots_, ks, vs, stream)
         if varlen:
             pa.pa_varlen_attn(out_, q_, kc, vc, tables_, qsl_, lens_, b.max_query_len, b.max_seq_len, b.scale, ws,
@@ -482,6 +482,7 @@ def run_ours(args):
     sampler = ClockSampler(bus) if rank == 0 else None
     if sampler:
         sampler.start()
+    stream = torch.cuda.current_stream(dev)
     pa.pa_trace_read(0, reset=True)
     pa.pa_trace_enable(True)
     barrier()
@@ -492,11 +493,27 @@ def run_ours(args):
     e1.record(stream)
     barrier()
     pa.pa_trace_enable(False)
-    ms_local = e0.elapsed_time(e1)
-    clocks = sampler.stop() if sampler else None
+    ms_eager = max_over_ranks(e0.elapsed_time(e1), dev) / args.steps
     trace = {name: pa.pa_trace_read(k) for k, name in enumerate(pa.TRACE_KINDS)}
-    ms_total = max_over_ranks(ms_local, dev)
-    ms_per_step = ms_total / args.steps
+    ms_graph = None
+    if not args.no_graph:
+        # The same step captured once into a CUDA graph (the library's calls neither
+        # synchronise nor allocate) and replayed: K replays timed with CUDA events.
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(3):
+            graph.replay()
+        barrier()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        g1.record(stream)
+        barrier()
+        ms_graph = max_over_ranks(g0.elapsed_time(g1), dev) / args.steps
+    clocks = sampler.stop() if sampler else None
+    ms_per_step = ms_graph if ms_graph is not None else ms_eager
     ctx_tokens = int(sum(int(n) for n in b.seq_lens))
     tok_s = ctx_tokens * world / (ms_per_step / 1000.0)
     launches = sum(n for n, _ in trace.values())
@@ -612,6 +629,8 @@ def run_ours(args):
                 "data": "synthetic (seeded N(0,1) values, seeded block placement)",
                 "config": workload_config(b, args),
                 "hbm_gbs": achieved, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "step_launch": "cuda_graph_replay" if ms_graph is not None else "eager",
+                "ms_per_step_eager": ms_eager,
                 "gpu_launches": launches,
                 "launches_by_kernel": {k: v[0] for k, v in trace.items() if v[0]},
                 "kernel_ms_by_kind": {k: v for k, v in kernel_ms.items() if v},
@@ -735,6 +754,8 @@ def main(argv=None):
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager launches instead of replaying the step captured in a CUDA graph")
     ap.add_argument("--no-shared-prefix", action="store_true",
                     help="agentic: call pa_decode instead of pa_decode_shared_prefix")
     ap.add_argument("--op", choices=("attention", "copy_blocks"), default="attention",
