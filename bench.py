@@ -38,7 +38,7 @@ METRIC = "attended KV tokens/sec and achieved HBM GB/s (fraction of GB300 peak),
 UNIT = "tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-WORKLOADS = ("agentic", "llama", "fp8", "mixed", "tiny")
+WORKLOADS = ("agentic", "llama", "fp8", "mixed", "mixed_fp8", "tiny")
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -221,12 +221,14 @@ def make_workload(name: str, seed: int, length_scale: float = 1.0):
         return workloads.fp8(seed=seed, scale_lengths=length_scale)
     if name == "mixed":
         return workloads.mixed(seed=seed, scale_lengths=length_scale)
+    if name == "mixed_fp8":
+        return workloads.mixed_fp8(seed=seed, scale_lengths=length_scale)
     if name == "tiny":
         return workloads.tiny(seed=seed)
     raise ValueError(name)
 
 
-BASE_SEEDS = {"agentic": 2, "llama": 1, "fp8": 4, "mixed": 3, "tiny": 0}
+BASE_SEEDS = {"agentic": 2, "llama": 1, "fp8": 4, "mixed": 3, "mixed_fp8": 3, "tiny": 0}
 
 
 def prefix_groups(b):

@@ -41,7 +41,10 @@ constexpr int kTiles = 2;         // tiles per CTA, sharing every K/V chunk
 constexpr int kChunk = 64;        // keys per chunk
 constexpr int kProducerWarp = 4 * kTiles;  // K copies; the next warp issues the V copies
 constexpr int kMmaWarp = 4 * kTiles + 2;   // one MMA warp per tile; the first owns TMEM
-constexpr int kThreadsTc = (kMmaWarp + kTiles) * 32;
+constexpr int kConvWarp = kMmaWarp + kTiles;  // FP8 caches: four warps widen K/V to f16
+constexpr int kConvThreads = 128;
+template <bool F8>
+constexpr int threads_tc() { return (kConvWarp + (F8 ? kConvThreads / 32 : 0)) * 32; }
 constexpr int kSBufs = 2;         // S / P buffers per tile, 64 TMEM columns each
 constexpr int kOCol = 128;        // a tile's O: columns [128, 128 + head dim) of its 256
 constexpr int kTileCols = 256;
@@ -165,37 +168,46 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-template <int HEAD, int BS>
+template <int HEAD, int BS, bool F8 = false>
 struct TcGeom {
-  static constexpr int kPieces = HEAD / 64;                 // 128-byte pieces of a row
+  static constexpr int kPieces = HEAD / 64;                 // 128-byte pieces of an f16 row
   static constexpr int kBlocks = kChunk / BS;               // paged blocks per chunk
-  static constexpr int kStages = HEAD == 128 ? 4 : 8;       // K/V ring depth, chunks
+  static constexpr int kStages = F8 ? 3 : (HEAD == 128 ? 4 : 8);  // f16 K/V ring depth, chunks
   static constexpr int kPiece = kChunk * 128;               // one K piece of a chunk (64 keys)
   static constexpr int kKvBytes = kPieces * kPiece;         // K (or V) of one chunk
   static constexpr int kStageBytes = 2 * kKvBytes;          // K then V
   static constexpr int kBlockTx = kPieces * BS * 128;       // bytes of one (block, head) tile
   static constexpr int kQPiece = kRows * 128;
   static constexpr int kQTile = kPieces * kQPiece;
-  static constexpr int kBarOff = kTiles * kQTile + kStages * kStageBytes;
-  // full[S], empty[S]; per tile s_full[2], p_full[2], o_done[2]; mma_fin; TMEM address
-  static constexpr int kNumBars = 2 * kStages + 3 * kSBufs * kTiles + 1;
+  // FP8 caches: the copies land in a staging ring, [K | V][block][token][head-dim bytes]
+  static constexpr int kStgStages = F8 ? 3 : 0;
+  static constexpr int kStgBlock = BS * HEAD;               // FP8 bytes of one (block, head) tile
+  static constexpr int kStgKv = kChunk * HEAD;
+  static constexpr int kStgOff = kTiles * kQTile + kStages * kStageBytes;
+  static constexpr int kBarOff = kStgOff + kStgStages * 2 * kStgKv;
+  // full[S], empty[S]; per tile s_full[2], p_full[2], o_done[2]; mma_fin;
+  // stg_full[SG], stg_empty[SG]; the TMEM address
+  static constexpr int kNumBars = 2 * kStages + 3 * kSBufs * kTiles + 1 + 2 * kStgStages;
   static constexpr int kSmem = 1024 + kBarOff + 8 * kNumBars + 16;
   static_assert(kBlocks * BS == kChunk, "block size must divide the chunk");
   static_assert(kSBufs * 64 <= kOCol && kOCol + HEAD <= kTileCols, "TMEM columns");
   static_assert(kSmem <= 227 * 1024, "shared memory");
+  static_assert(!F8 || HEAD == 128, "FP8 rows are one 128-byte piece");
 };
 
 // Byte offset, inside a chunk's V, of key `key`'s row in piece `pc`.
 template <int HEAD, int BS>
 __device__ __forceinline__ uint32_t v_row_off(int key, int pc) {
-  return (uint32_t)((key / BS) * TcGeom<HEAD, BS>::kBlockTx + pc * BS * 128 + (key % BS) * 128);
+  return (uint32_t)((key / BS) * (HEAD / 64) * BS * 128 + pc * BS * 128 + (key % BS) * 128);
 }
 
-template <int QDT, int HEAD, int BS>
-__global__ void __launch_bounds__(kThreadsTc, 1)
+template <int QDT, int KVDT, int HEAD, int BS>
+__global__ void __launch_bounds__(threads_tc<KVDT == PA_FP8_E4M3>(), 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv) {
-  using G = TcGeom<HEAD, BS>;
+  constexpr bool kF8 = KVDT == PA_FP8_E4M3;
+  constexpr int ODT = kF8 ? PA_F16 : QDT;  // MMA operand type (FP8 K/V are widened to f16)
+  using G = TcGeom<HEAD, BS, kF8>;
   using QE = Elem<QDT>;
   constexpr int ST = G::kStages;
   constexpr int NB = G::kBlocks;
@@ -252,7 +264,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   uint64_t* p_full = s_full + kTiles * kSBufs;
   uint64_t* o_done = p_full + kTiles * kSBufs;
   uint64_t* mma_fin = o_done + kTiles * kSBufs;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_fin + 1);
+  // FP8: stg_full when a chunk's codes have landed in staging, stg_empty when the
+  // converters have widened them (the f16 `full` is then arrived by the converters)
+  uint64_t* stg_full = mma_fin + 1;
+  uint64_t* stg_empty = stg_full + G::kStgStages;
+  uint8_t* sStg = smem + G::kStgOff;                    // [stage][K | V][block][token][bytes]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stg_empty + G::kStgStages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
@@ -262,8 +279,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
     for (int i = 0; i < ST; ++i) {
-      mbar_init(full + i, 2);        // the K and the V producer
-      mbar_init(empty + i, kTiles);  // every tile's MMA warp
+      mbar_init(full + i, kF8 ? kConvThreads : 2);  // the converters, or the K and V producers
+      mbar_init(empty + i, kTiles);                 // every tile's MMA warp
+    }
+    for (int i = 0; i < G::kStgStages; ++i) {
+      mbar_init(stg_full + i, 2);
+      mbar_init(stg_empty + i, kConvThreads);
     }
     for (int i = 0; i < kTiles * kSBufs; ++i) {
       mbar_init(s_full + i, 1);
@@ -277,16 +298,48 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int row_tok = tid / gp, row_head = tid % gp;
   const bool row_valid = tid < kTiles * kRows && row_tok < ntok && row_head < nh;
   const int row_pos = pos0 + row_tok;
+  // FP8 caches: the row is scaled by 2^q_shift so that f16 holds it exactly (max |q|
+  // below 2^15); the softmax multiplier takes 2^-q_shift back
+  int q_shift = 0;
   if (tid < kTiles * kRows) {
     const uint4* src = row_valid ? reinterpret_cast<const uint4*>(
                                        reinterpret_cast<const typename QE::T*>(p.q) +
                                        ((long long)(row0 + row_tok) * p.num_q_heads + h0 + row_head) * HEAD)
                                  : nullptr;
     uint8_t* dst = sQ + (tid / kRows) * G::kQTile;
+    if constexpr (!kF8) {
 #pragma unroll
-    for (int c = 0; c < HEAD / 8; ++c) {
-      const uint4 v = src ? src[c] : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(dst + (c >> 3) * G::kQPiece + swz128(tid % kRows, c & 7)) = v;
+      for (int c = 0; c < HEAD / 8; ++c) {
+        const uint4 v = src ? src[c] : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(dst + (c >> 3) * G::kQPiece + swz128(tid % kRows, c & 7)) = v;
+      }
+    } else {
+      float amax = 0.f;
+      for (int c = 0; c < HEAD / 8 && src; ++c) {
+        const uint4 v = src[c];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = unpack2<QDT>(w[e]);
+          amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+      }
+      int ex = 0;
+      frexpf(amax, &ex);  // amax < 2^ex
+      q_shift = max(-100, min(100, 15 - ex));
+#pragma unroll 4
+      for (int c = 0; c < HEAD / 8; ++c) {
+        const uint4 v = src ? src[c] : make_uint4(0, 0, 0, 0);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t h[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = unpack2<QDT>(w[e]);
+          h[e] = pack2<PA_F16>(ldexpf(f.x, q_shift), ldexpf(f.y, q_shift));
+        }
+        *reinterpret_cast<uint4*>(dst + (c >> 3) * G::kQPiece + swz128(tid % kRows, c & 7)) =
+            make_uint4(h[0], h[1], h[2], h[3]);
+      }
     }
   }
   fence_proxy_async();
@@ -307,7 +360,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // Lane j holds block table entry kb_first + 32 w + j of window w; the next window
     // is prefetched.  An elected lane of the first warp copies a chunk's K one piece
     // of one block at a time; the second warp's copies V one whole block at a time.
-    // Each arrives once per chunk on full with its own byte count.
+    // Each arrives once per chunk on full with its own byte count.  With an FP8 cache
+    // both copy whole (block, head) tiles of codes into the staging ring instead.
+    constexpr int RS = kF8 ? G::kStgStages : ST;
+    uint64_t* rfull = kF8 ? stg_full : full;
+    uint64_t* rempty = kF8 ? stg_empty : empty;
     const bool is_v = warp != kProducerWarp;
     const int kb_end = (k1 + BS - 1) / BS;  // blocks [kb_first, kb_end) are loaded
     auto load_window = [&](int w) {
@@ -319,8 +376,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     int win_next = load_window(1);
     int issued = 0;
     for (int i = 0; i < nch; ++i) {
-      const int s = i % ST;
-      if (i >= ST && !__all_sync(0xffffffffu, mbar_wait_bounded(empty + s, ((i / ST) - 1) & 1))) {
+      const int s = i % RS;
+      if (i >= RS && !__all_sync(0xffffffffu, mbar_wait_bounded(rempty + s, ((i / RS) - 1) & 1))) {
         if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
         break;
       }
@@ -341,7 +398,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         phys[b] = ok_b ? e : -1;
         nvalid += ok_b;
       }
-      if (elect_one()) {
+      if (kF8 && elect_one()) {
+        uint8_t* sg = sStg + s * 2 * G::kStgKv + (is_v ? G::kStgKv : 0);
+        if (nvalid == 0) {
+          mbar_arrive(rfull + s);
+        } else {
+          mbar_arrive_expect_tx(rfull + s, (uint32_t)(nvalid * G::kStgBlock));
+#pragma unroll
+          for (int b = 0; b < NB; ++b)
+            if (phys[b] >= 0) tma_load_4d(sg + b * G::kStgBlock, is_v ? &tmv : &tmk, 0, kvh * BS, 0, phys[b], rfull + s);
+        }
+      } else if (!kF8 && elect_one()) {
         uint8_t* sk = sKV + s * G::kStageBytes;
         if (nvalid == 0) {
           mbar_arrive(full + s);
@@ -365,9 +432,53 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     // every copy lands before the CTA can leave
     if (lane == 0)
-      for (int j = max(0, issued - ST); j < issued; ++j)
-        if (!mbar_wait_bounded(full + j % ST, (j / ST) & 1)) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-  } else if (warp >= kMmaWarp) {
+      for (int j = max(0, issued - RS); j < issued; ++j)
+        if (!mbar_wait_bounded(rfull + j % RS, (j / RS) & 1)) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+  } else if (kF8 && warp >= kConvWarp) {
+    // ------------------------------------------------------------ FP8 converters
+    // Chunk i: wait for its codes in staging and for its f16 stage to be free, widen
+    // every code to f16 exactly (e4m3 values are all f16 values; the scales are
+    // applied later) into the K-major K layout and the per-block V layout, release
+    // the staging slot and mark the f16 stage full.  Unit u of a chunk is one 16-byte
+    // group of codes: tensor u / 512, key (u % 512) / 8, group u % 8 (elements
+    // 16 g .. 16 g + 15 = two 8-element f16 chunks of piece g / 4).
+    if constexpr (kF8) {
+    const int ct = tid - kConvWarp * 32;
+    for (int i = 0; i < nch; ++i) {
+      const int s = i % ST, ss = i % G::kStgStages;
+      bool ok = mbar_wait_bounded(stg_full + ss, (i / G::kStgStages) & 1);
+      if (i >= ST) ok = ok && mbar_wait_bounded(empty + s, ((i / ST) - 1) & 1);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+        break;
+      }
+      const uint8_t* sg = sStg + ss * 2 * G::kStgKv;
+      uint8_t* sk = sKV + s * G::kStageBytes;
+#pragma unroll 2
+      for (int u = ct; u < 2 * kChunk * 8; u += kConvThreads) {
+        const int tensor = u / (kChunk * 8), key = (u % (kChunk * 8)) >> 3, g = u & 7;
+        const int blk = key / BS, tok = key % BS;
+        const uint4 codes = *reinterpret_cast<const uint4*>(sg + tensor * G::kStgKv + blk * G::kStgBlock +
+                                                            swz128(tok, g));
+        const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+        uint32_t h[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          h[2 * e] = e4m3x2_to_f16x2(static_cast<uint16_t>(cw[e] & 0xffffu));
+          h[2 * e + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(cw[e] >> 16));
+        }
+        const int pc = g >> 2, cc = (2 * g) & 7;
+        uint8_t* row = tensor == 0 ? sk + pc * G::kPiece + key * 128
+                                   : sk + G::kKvBytes + blk * G::kBlockTx + pc * BS * 128 + tok * 128;
+        *reinterpret_cast<uint4*>(row + ((cc ^ (key & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (key & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+      }
+      fence_proxy_async();  // generic-proxy writes, read next by the tensor core
+      mbar_arrive(stg_empty + ss);
+      mbar_arrive(full + s);
+    }
+    }
+  } else if (warp >= kMmaWarp && warp < kConvWarp) {
     // ------------------------------------------------------------ MMA issuers
     // One warp per tile follows that tile's schedule (descriptors stay
     // warp-uniform); an elected lane issues each group of MMAs and its commit.  Per
@@ -375,7 +486,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // frees.  The two tiles' streams run independently on the tensor core.
     const int t = warp - kMmaWarp;
     const int my_nch = t == 0 ? nch_t[0] : nch_t[1];
-    const uint32_t fmt = QDT == PA_BF16 ? 1u : 0u;
+    const uint32_t fmt = ODT == PA_BF16 ? 1u : 0u;
     const uint32_t id_s = umma_idesc(kRows, kChunk, fmt, 0);
     const uint32_t id_o = umma_idesc(kRows, HEAD, fmt, 1);
     // descriptor start addresses count 16-byte units: offsets are added pre-shifted
@@ -457,7 +568,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     uint64_t* my_s_full = s_full + t * kSBufs;
     uint64_t* my_p_full = p_full + t * kSBufs;
     uint64_t* my_o_done = o_done + t * kSBufs;
-    const float c = p.scale * kLog2e;
+    // score multiplier in log2 units; FP8: the K scale and the row's f16 shift too
+    const float c = kF8 ? ldexpf(p.scale * kLog2e * (*p.k_scale), -q_shift) : p.scale * kLog2e;
+    const float out_scale = kF8 ? *p.v_scale : 1.f;
     const int row_limit = p.causal ? min(k1, row_pos + 1) : k1;  // this row attends keys < row_limit
     float m = -INFINITY, l = 0.f;
     bool fail = false;
@@ -511,7 +624,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const float2 x = f2_unpack(f2_fma(f2_pack(sc[2 * j], sc[2 * j + 1]), c2, nu2));
         const float e0 = ex2_approx(x.x), e1 = ex2_approx(x.y);
         acc2[j & 3] = f2_add(acc2[j & 3], f2_pack(e0, e1));
-        pk[j] = pack2<QDT>(e0, e1);
+        pk[j] = pack2<ODT>(e0, e1);
       }
       const float2 lsum = f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])));
       l += lsum.x + lsum.y;
@@ -582,7 +695,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const bool direct = parts_row == 1;
       const int tq = t0 + row_tok;
       const int head = h0 + row_head;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? out_scale / l : 0.f;
       const long long pi = (long long)p.part_off[r] + (long long)tq * parts_req + z;
       typename QE::T* o_row =
           reinterpret_cast<typename QE::T*>(p.out) + ((long long)(qs + tq) * p.num_q_heads + head) * HEAD;
@@ -612,8 +725,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             *reinterpret_cast<float4*>(w_row + cb + 4 * q) =
-                make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]), __uint_as_float(o[4 * q + 2]),
-                            __uint_as_float(o[4 * q + 3]));
+                make_float4(__uint_as_float(o[4 * q]) * out_scale, __uint_as_float(o[4 * q + 1]) * out_scale,
+                            __uint_as_float(o[4 * q + 2]) * out_scale, __uint_as_float(o[4 * q + 3]) * out_scale);
         }
       }
       if (write && !direct) p.ws_ml[pi * p.num_q_heads + head] = make_float2(m, l);
@@ -629,11 +742,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   }
 }
 
-template <int QDT, int HEAD, int BS>
+template <int QDT, int KVDT, int HEAD, int BS>
 cudaError_t launch_tc_t(const AttnParams& p, int num_items, const CUtensorMap* tk, const CUtensorMap* tv,
                         cudaStream_t stream) {
-  constexpr int smem = TcGeom<HEAD, BS>::kSmem;
-  auto kern = prefill_tc_kernel<QDT, HEAD, BS>;
+  constexpr bool kF8 = KVDT == PA_FP8_E4M3;
+  constexpr int smem = TcGeom<HEAD, BS, kF8>::kSmem;
+  auto kern = prefill_tc_kernel<QDT, KVDT, HEAD, BS>;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -646,20 +760,22 @@ cudaError_t launch_tc_t(const AttnParams& p, int num_items, const CUtensorMap* t
     configured_device = dev;
   }
   dim3 grid(num_items, p.num_kv_heads * p.num_head_groups);
-  kern<<<grid, kThreadsTc, smem, stream>>>(p, *tk, *tv);
+  kern<<<grid, threads_tc<kF8>(), smem, stream>>>(p, *tk, *tv);
   return cudaGetLastError();
 }
 
-template <int QDT>
+template <int QDT, int KVDT>
 cudaError_t launch_tc_shape(const AttnParams& p, int num_items, const CUtensorMap* tk, const CUtensorMap* tv,
                             cudaStream_t s) {
   const int d = p.head_size, bs = p.block_size;
-  if (d == 128 && bs == 16) return launch_tc_t<QDT, 128, 16>(p, num_items, tk, tv, s);
-  if (d == 128 && bs == 32) return launch_tc_t<QDT, 128, 32>(p, num_items, tk, tv, s);
-  if (d == 128 && bs == 64) return launch_tc_t<QDT, 128, 64>(p, num_items, tk, tv, s);
-  if (d == 64 && bs == 16) return launch_tc_t<QDT, 64, 16>(p, num_items, tk, tv, s);
-  if (d == 64 && bs == 32) return launch_tc_t<QDT, 64, 32>(p, num_items, tk, tv, s);
-  if (d == 64 && bs == 64) return launch_tc_t<QDT, 64, 64>(p, num_items, tk, tv, s);
+  if (d == 128 && bs == 16) return launch_tc_t<QDT, KVDT, 128, 16>(p, num_items, tk, tv, s);
+  if (d == 128 && bs == 32) return launch_tc_t<QDT, KVDT, 128, 32>(p, num_items, tk, tv, s);
+  if (d == 128 && bs == 64) return launch_tc_t<QDT, KVDT, 128, 64>(p, num_items, tk, tv, s);
+  if constexpr (KVDT != PA_FP8_E4M3) {
+    if (d == 64 && bs == 16) return launch_tc_t<QDT, KVDT, 64, 16>(p, num_items, tk, tv, s);
+    if (d == 64 && bs == 32) return launch_tc_t<QDT, KVDT, 64, 32>(p, num_items, tk, tv, s);
+    if (d == 64 && bs == 64) return launch_tc_t<QDT, KVDT, 64, 64>(p, num_items, tk, tv, s);
+  }
   return cudaErrorInvalidValue;
 }
 
@@ -674,16 +790,23 @@ int prefill_tile_tokens(int group) {
 }
 
 bool prefill_tc_supported(int q_dtype, int kv_dtype, int head_size, int block_size) {
-  if (!(q_dtype == PA_BF16 || q_dtype == PA_F16) || kv_dtype != q_dtype) return false;
-  return (head_size == 64 || head_size == 128) && (block_size == 16 || block_size == 32 || block_size == 64);
+  if (!(q_dtype == PA_BF16 || q_dtype == PA_F16)) return false;
+  if (!(block_size == 16 || block_size == 32 || block_size == 64)) return false;
+  if (kv_dtype == PA_FP8_E4M3) return head_size == 128;  // one 128-byte row of codes
+  return kv_dtype == q_dtype && (head_size == 64 || head_size == 128);
 }
 
 cudaError_t launch_prefill_tc(const AttnParams& p, int q_dtype, int kv_dtype, int num_items,
                               const CUtensorMap* tmap_k, const CUtensorMap* tmap_v, cudaStream_t stream) {
   if (num_items <= 0) return cudaSuccess;
+  if (kv_dtype == PA_FP8_E4M3) {
+    if (q_dtype == PA_BF16) return launch_tc_shape<PA_BF16, PA_FP8_E4M3>(p, num_items, tmap_k, tmap_v, stream);
+    if (q_dtype == PA_F16) return launch_tc_shape<PA_F16, PA_FP8_E4M3>(p, num_items, tmap_k, tmap_v, stream);
+    return cudaErrorInvalidValue;
+  }
   if (kv_dtype != q_dtype) return cudaErrorInvalidValue;
-  if (q_dtype == PA_BF16) return launch_tc_shape<PA_BF16>(p, num_items, tmap_k, tmap_v, stream);
-  if (q_dtype == PA_F16) return launch_tc_shape<PA_F16>(p, num_items, tmap_k, tmap_v, stream);
+  if (q_dtype == PA_BF16) return launch_tc_shape<PA_BF16, PA_BF16>(p, num_items, tmap_k, tmap_v, stream);
+  if (q_dtype == PA_F16) return launch_tc_shape<PA_F16, PA_F16>(p, num_items, tmap_k, tmap_v, stream);
   return cudaErrorInvalidValue;
 }
 

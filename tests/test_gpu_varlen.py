@@ -53,6 +53,9 @@ VARLEN_CASES = [
     ("prefill_bs64", "bf16", 16, 4, 128, 64, [300, 129, 64], [150, 129, 1], 128, True),
     ("prefill_bs64_d64_f16", "f16", 8, 2, 64, 64, [513, 70], [200, 70], 0, True),
     ("prefill_part_not_chunk_multiple", "bf16", 8, 2, 128, 32, [1000, 161], [230, 161], 96, True),
+    ("fp8_prefill_split_default", "fp8_e4m3", 32, 8, 128, 16, [20000, 3000, 40], [300, 129, 1], 0, True),
+    ("fp8_prefill_ragged_part48", "fp8_e4m3", 32, 8, 128, 16, [97, 33, 1000], [97, 31, 45], 48, True),
+    ("fp8_prefill_noncausal_bs64", "fp8_e4m3", 16, 2, 128, 64, [250, 90], [60, 90], 64, False),
 ]
 
 
@@ -61,6 +64,12 @@ def test_varlen_parity(pa, case):
     name, kv, hq, hkv, d, bs, lens, q_lens, part, causal = case
     b = workloads.build(name, 300 + len(name), lens, q_lens, hq, hkv, d, bs, kv, causal=causal)
     _varlen_parity(pa, b, part, causal)
+
+
+def test_fp8_prefill_with_f16_queries(pa):
+    b = workloads.build("fp8_f16q_pf", 71, [700, 37, 300], [64, 1, 300], 32, 8, 128, 32, "fp8_e4m3",
+                        q_dtype="f16", src_dtype="f16")
+    _varlen_parity(pa, b, 64, True)
 
 
 def test_varlen_single_tokens_equals_decode(pa):

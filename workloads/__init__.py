@@ -287,7 +287,7 @@ def agentic(seed: int = 2, host_cache: bool = False, scale_lengths: float = 1.0)
 
 
 def mixed(seed: int = 3, host_cache: bool = False, scale_lengths: float = 1.0,
-          chunk: int = 512, n_prefill: int = 4, n_decode: int = 128) -> PagedBatch:
+          chunk: int = 512, n_prefill: int = 4, n_decode: int = 128, kv_dtype: str = "bf16") -> PagedBatch:
     """Flattened chunked-prefill + decode step; prefill requests first."""
     rng = np.random.Generator(np.random.PCG64(seed + 3000))
     prefix = rng.integers(8192, 65536, size=n_prefill, endpoint=True)
@@ -297,8 +297,16 @@ def mixed(seed: int = 3, host_cache: bool = False, scale_lengths: float = 1.0,
         ctx = np.maximum(np.round(ctx * scale_lengths).astype(np.int64), 1)
     lens = [int(p) + chunk for p in prefix] + [int(c) for c in ctx]
     q_lens = [chunk] * n_prefill + [1] * n_decode
-    return build("mixed_chunked_prefill_decode", seed, lens, q_lens, 32, 8, 128, 16, "bf16",
-                 host_cache=host_cache)
+    if kv_dtype == "bf16":
+        return build("mixed_chunked_prefill_decode", seed, lens, q_lens, 32, 8, 128, 16, "bf16",
+                     host_cache=host_cache)
+    return build("mixed_chunked_prefill_decode_" + kv_dtype, seed, lens, q_lens, 32, 8, 128, 16, kv_dtype,
+                 q_dtype="bf16", src_dtype="bf16", host_cache=host_cache)
+
+
+def mixed_fp8(seed: int = 3, host_cache: bool = False, scale_lengths: float = 1.0) -> PagedBatch:
+    """The mixed step with an FP8 e4m3 cache (per-tensor scales 2^-6)."""
+    return mixed(seed, host_cache, scale_lengths, kv_dtype="fp8_e4m3")
 
 
 def fp8(seed: int = 4, host_cache: bool = False, batch: int = 256,
@@ -311,7 +319,7 @@ def fp8(seed: int = 4, host_cache: bool = False, batch: int = 256,
                  q_dtype="bf16", src_dtype="bf16", host_cache=host_cache)
 
 
-NAMED = {"tiny": tiny, "llama": llama, "agentic": agentic, "mixed": mixed, "fp8": fp8}
+NAMED = {"tiny": tiny, "llama": llama, "agentic": agentic, "mixed": mixed, "fp8": fp8, "mixed_fp8": mixed_fp8}
 
 
 # --------------------------------------------------------------------------
