@@ -234,7 +234,7 @@ def copy_blocks(k_cache, v_cache, block_mapping) -> list:
 # --------------------------------------------------------------------------
 
 def gather_kv(cache_bits, block_table_row, num_tokens: int, block_size: int,
-              dtype: str, scale: float = 1.0) -> np.ndarray:
+              dtype: str, scale: float = 1.0, first: int = 0) -> np.ndarray:
     """Contiguous float64 K (or V) ``[num_tokens][num_kv_heads][head_size]`` of one request.
 
     [LINEAGE] "PagedAttention：把逻辑连续与物理连续分开": (sequence, logical
@@ -242,8 +242,9 @@ def gather_kv(cache_bits, block_table_row, num_tokens: int, block_size: int,
     table.  [AGENTIC] "統一分頁 + 共用池": physical blocks need not be
     contiguous.  Position ``pos`` lives in physical block
     ``block_table_row[pos // block_size]`` at offset ``pos % block_size``.
+    Positions ``first .. num_tokens-1`` are gathered (row 0 = position ``first``).
     """
-    pos = np.arange(num_tokens, dtype=np.int64)
+    pos = np.arange(first, num_tokens, dtype=np.int64)
     phys = np.asarray(block_table_row, dtype=np.int64)[pos // block_size]
     off = pos % block_size
     return decode_bits(np.asarray(cache_bits)[phys, :, off, :], dtype, scale)
@@ -269,7 +270,8 @@ def softmax_weights(scores) -> np.ndarray:
     return w / w.sum()
 
 
-def attend(q64, K64, V64, positions, scale: float, causal: bool = True) -> np.ndarray:
+def attend(q64, K64, V64, positions, scale: float, causal: bool = True, window: int = 0,
+           key_offset: int = 0) -> np.ndarray:
     """Textbook softmax attention of one request's queries over its contiguous K/V.
 
     q64 ``[n][Hq][d]``, K64 / V64 ``[T][Hkv][d]`` (float64), ``positions[n]``.
@@ -278,6 +280,10 @@ def attend(q64, K64, V64, positions, scale: float, causal: bool = True) -> np.nd
     out = sum_t exp(s_t - max s) v_t,g / sum_t exp(s_t - max s).
     [AGENTIC] "Online softmax 到底在幹嘛" gives the weighted average
     sum exp(score) * value / sum exp(score) and the max shift before exp.
+    With ``window`` W > 0 (causal only) query j attends t = max(0, p_j - W + 1)
+    .. p_j: [AGENTIC] "為什麼需要「分頁」記憶體管理", sliding-window attention
+    only looks at the most recent fixed range.  Row 0 of K64 / V64 holds
+    position ``key_offset``.
     """
     q64 = np.asarray(q64, dtype=np.float64)
     n, hq, d = q64.shape
@@ -286,12 +292,17 @@ def attend(q64, K64, V64, positions, scale: float, causal: bool = True) -> np.nd
         raise ValueError("num_q_heads must be a multiple of num_kv_heads")
     group = hq // hkv
     out = np.empty((n, hq, d), dtype=np.float64)
+    if window and not causal:
+        raise ValueError("a sliding window needs causal attention")
     for j in range(n):
-        last = int(positions[j]) if causal else K64.shape[0] - 1
+        last = int(positions[j]) if causal else key_offset + K64.shape[0] - 1
+        first = max(0, last - window + 1) if window else 0
+        if first < key_offset:
+            raise ValueError("keys before key_offset are needed")
         for g in range(hkv):
             heads = slice(g * group, (g + 1) * group)
-            k = K64[: last + 1, g, :]                       # [L][d]
-            v = V64[: last + 1, g, :]
+            k = K64[first - key_offset: last - key_offset + 1, g, :]     # [L][d]
+            v = V64[first - key_offset: last - key_offset + 1, g, :]
             s = scale * (k @ q64[j, heads, :].T)              # [L][group]
             w = np.exp(s - s.max(axis=0, keepdims=True))
             out[j, heads, :] = (w.T @ v) / w.sum(axis=0)[:, None]
@@ -301,7 +312,7 @@ def attend(q64, K64, V64, positions, scale: float, causal: bool = True) -> np.nd
 def paged_varlen(q_bits, q_dtype: str, k_cache, v_cache, kv_dtype: str,
                  block_tables, query_start_loc, seq_lens, block_size: int,
                  scale: float, causal: bool = True, k_scale: float = 1.0,
-                 v_scale: float = 1.0, rows=None) -> np.ndarray:
+                 v_scale: float = 1.0, rows=None, window: int = 0) -> np.ndarray:
     """Attention of a flattened variable-length batch over a paged KV cache.
 
     Request r owns query rows query_start_loc[r] .. query_start_loc[r+1]-1 and
@@ -310,6 +321,9 @@ def paged_varlen(q_bits, q_dtype: str, k_cache, v_cache, kv_dtype: str,
     step); [LINEAGE] "静态 batching" (per-step token budget sum q_i <= K with
     q_i = 1 for a decode).  Returns float64 ``[total_q][Hq][d]``; when ``rows``
     lists flattened query rows only those are computed and the rest are NaN.
+    With a sliding ``window`` only positions some query of the request attends
+    are read through the block table: entries of blocks that lie wholly before
+    the first query's window may be released (any value).
     """
     q64 = decode_bits(q_bits, q_dtype)
     qsl = np.asarray(query_start_loc, dtype=np.int64)
@@ -325,16 +339,17 @@ def paged_varlen(q_bits, q_dtype: str, k_cache, v_cache, kv_dtype: str,
             continue
         L = int(lens[r])
         pos = query_positions(L, hi - lo)
-        K = gather_kv(k_cache, block_tables[r], L, block_size, kv_dtype, k_scale)
-        V = gather_kv(v_cache, block_tables[r], L, block_size, kv_dtype, v_scale)
+        first = max(0, int(pos[0]) - window + 1) if window else 0
+        K = gather_kv(k_cache, block_tables[r], L, block_size, kv_dtype, k_scale, first)
+        V = gather_kv(v_cache, block_tables[r], L, block_size, kv_dtype, v_scale, first)
         idx = np.array(sel, dtype=np.int64)
-        out[idx] = attend(q64[idx], K, V, pos[idx - lo], scale, causal)
+        out[idx] = attend(q64[idx], K, V, pos[idx - lo], scale, causal, window, first)
     return out
 
 
 def paged_decode(q_bits, q_dtype: str, k_cache, v_cache, kv_dtype: str,
                  block_tables, seq_lens, block_size: int, scale: float,
-                 k_scale: float = 1.0, v_scale: float = 1.0, seqs=None) -> np.ndarray:
+                 k_scale: float = 1.0, v_scale: float = 1.0, seqs=None, window: int = 0) -> np.ndarray:
     """PagedAttention decode: one new query token per sequence, at its last position.
 
     [NOTES] "Prefill 与 Decode": the new token's Q attends the K/V of all
@@ -345,7 +360,7 @@ def paged_decode(q_bits, q_dtype: str, k_cache, v_cache, kv_dtype: str,
     qsl = np.arange(b + 1, dtype=np.int64)
     return paged_varlen(q_bits, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
                         qsl, seq_lens, block_size, scale, True, k_scale, v_scale,
-                        rows=seqs)
+                        rows=seqs, window=window)
 
 
 # --------------------------------------------------------------------------

@@ -468,6 +468,68 @@ def test_without_copy_on_write_the_fork_overwrites_the_parent():
     assert np.abs(out[1] - ref_fork).max() < 1e-12
 
 
+# ---------------------------------------------------------------- sliding window
+
+def _windowed_batch(seed=33):
+    return workloads.build("win", seed, [300, 37, 129, 1000], [40, 1, 129, 7], 8, 2, 64, 16, "f32")
+
+
+def _varlen(b, window, tables=None):
+    return oracle.paged_varlen(b.q, b.q_dtype, b.k_cache, b.v_cache, b.kv_dtype,
+                               b.block_tables if tables is None else tables, b.query_start_loc, b.seq_lens,
+                               b.block_size, b.scale, True, window=window)
+
+
+def test_window_covering_the_context_is_full_attention():
+    b = _windowed_batch()
+    assert np.array_equal(_varlen(b, 0), _varlen(b, 5000))
+
+
+def test_window_of_one_returns_the_own_value():
+    b = _windowed_batch()
+    out = _varlen(b, 1)
+    group = b.num_q_heads // b.num_kv_heads
+    for r in range(b.num_seqs):
+        q0, q1, L = int(b.query_start_loc[r]), int(b.query_start_loc[r + 1]), int(b.seq_lens[r])
+        for j in range(q0, q1):
+            pos = L - (q1 - q0) + (j - q0)
+            blk, off = int(b.block_tables[r, pos // 16]), pos % 16
+            v = oracle.decode_bits(b.v_cache[blk, :, off, :], "f32")      # [Hkv][d]
+            assert np.array_equal(out[j], np.repeat(v, group, axis=0))
+
+
+def test_window_matches_sdpa_with_a_band_mask():
+    # identity placement, one request with a 300-token prefix and 40 new tokens, window 100
+    b = workloads.build("winsdpa", 34, [340], [40], 8, 2, 64, 16, "f32")
+    W = 100
+    out = _varlen(b, W)
+    L, n = 340, 40
+    K = torch.from_numpy(oracle.gather_kv(b.k_cache, b.block_tables[0], L, 16, "f32"))
+    V = torch.from_numpy(oracle.gather_kv(b.v_cache, b.block_tables[0], L, 16, "f32"))
+    q = torch.from_numpy(oracle.decode_bits(b.q, "f32"))                    # [n][Hq][d]
+    pos = torch.arange(L - n, L)[:, None]
+    keys = torch.arange(L)[None, :]
+    band = (keys <= pos) & (keys > pos - W)                                  # [n][L]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        q.permute(1, 0, 2), K.permute(1, 0, 2).repeat_interleave(4, 0), V.permute(1, 0, 2).repeat_interleave(4, 0),
+        attn_mask=band, scale=b.scale).permute(1, 0, 2).numpy()
+    assert np.abs(out - ref).max() < 1e-12
+
+
+def test_released_blocks_before_the_window_are_never_read():
+    # [AGENTIC] "為什麼需要「分頁」記憶體管理": blocks that leave the window are
+    # reclaimed at once; their table entries may then hold anything.
+    b = _windowed_batch()
+    W = 64
+    tables = b.block_tables.copy()
+    for r in range(b.num_seqs):
+        q_len = int(b.query_start_loc[r + 1] - b.query_start_loc[r])
+        first = max(0, int(b.seq_lens[r]) - q_len - W + 1)
+        tables[r, : first // 16] = -1
+    assert (tables == -1).sum() > 0
+    assert np.array_equal(_varlen(b, W), _varlen(b, W, tables))
+
+
 def test_chunked_prefill_equals_single_chunk():
     """Queries of a prompt give the same output whether processed in one chunk or two."""
     q, kc, vc, table = _contiguous_case(13, 23, 8, 2, 16, 23)
