@@ -270,16 +270,24 @@ def shared_split_bytes(b, groups) -> dict:
     return {"shared": shared_tok * kv_tok, "private": private_tok * kv_tok}
 
 
-def algorithmic_bytes(b) -> dict:
-    """Bytes the attention must move at least (per call), and the logical total."""
+def window_tokens(b, window: int) -> list:
+    """Keys each decode sequence attends: all of them, or the last `window`."""
+    return [min(int(n), window) if window > 0 else int(n) for n in b.seq_lens]
+
+
+def algorithmic_bytes(b, window: int = 0) -> dict:
+    """Bytes the attention must move at least (per call), and the logical total.
+    With a sliding window (decode) only the window's keys and block-table entries."""
     import workloads
 
     kv_tok = 2 * b.num_kv_heads * b.head_size * workloads.ELEM_BYTES[b.kv_dtype]
     qb = workloads.ELEM_BYTES[b.q_dtype]
     q_out = 2 * b.total_q * b.num_q_heads * b.head_size * qb
-    tables = sum(-(-int(n) // b.block_size) for n in b.seq_lens) * 4 + 4 * b.num_seqs
-    logical = int(sum(int(n) for n in b.seq_lens)) * kv_tok
-    unique = unique_kv_tokens(b) * kv_tok
+    bs = b.block_size
+    spans = [int(n) - (max(0, int(n) - window) // bs * bs if window > 0 else 0) for n in b.seq_lens]
+    tables = sum(-(-sp // bs) for sp in spans) * 4 + 4 * b.num_seqs
+    logical = int(sum(window_tokens(b, window))) * kv_tok
+    unique = logical if window > 0 else unique_kv_tokens(b) * kv_tok
     return {"kv_token_bytes": kv_tok, "logical_kv": logical, "unique_kv": unique,
             "algorithmic": unique + q_out + tables, "logical_total": logical + q_out + tables}
 
@@ -402,6 +410,7 @@ def workload_config(b, args):
             "decode_api": ("pa_varlen_attn" if b.max_query_len > 1 else
                            "pa_decode" if (args.no_shared_prefix or not b.families) else "pa_decode_shared_prefix"),
             "length_scale": args.length_scale,
+            "sliding_window": args.window or None,
             "l2": "inputs larger than L2 (KV working set >> 129 MB)" if b.name != "tiny" else "tiny (fits L2)"}
 
 
@@ -441,7 +450,9 @@ def run_ours(args):
     else:
         wsb = pa.pa_decode_workspace_size(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_size, b.max_seq_len,
                                           b.block_size, part)
-    groups = None if (varlen or args.no_shared_prefix) else prefix_groups(b)
+    if args.window and varlen:
+        raise SystemExit("--window applies to the decode workloads (llama, fp8, agentic)")
+    groups = None if (varlen or args.no_shared_prefix or args.window) else prefix_groups(b)
     if groups is not None:
         wsb = pa.pa_decode_shared_prefix_workspace_size(b.num_seqs, len(groups[1]), b.num_q_heads,
                                                         b.num_kv_heads, b.head_size, b.max_seq_len,
@@ -461,7 +472,8 @@ def run_ours(args):
             pa.pa_decode_shared_prefix(out_, q_, kc, vc, tables_, lens_, b.max_seq_len, b.scale, ws, gstart,
                                        gshared, max_group, ks, vs, part, stream)
         else:
-            pa.pa_decode(out_, q_, kc, vc, tables_, lens_, b.max_seq_len, b.scale, ws, ks, vs, part, stream)
+            pa.pa_decode(out_, q_, kc, vc, tables_, lens_, b.max_seq_len, b.scale, ws, ks, vs, part, stream,
+                         window=args.window)
 
     def barrier():
         if world > 1:
@@ -516,12 +528,12 @@ def run_ours(args):
         ms_graph = max_over_ranks(g0.elapsed_time(g1), dev) / args.steps
     clocks = sampler.stop() if sampler else None
     ms_per_step = ms_graph if ms_graph is not None else ms_eager
-    ctx_tokens = int(sum(int(n) for n in b.seq_lens))
+    ctx_tokens = int(sum(window_tokens(b, args.window)))
     tok_s = ctx_tokens * world / (ms_per_step / 1000.0)
     launches = sum(n for n, _ in trace.values())
 
     # ---- roofline of the dominant kernel
-    nbytes = algorithmic_bytes(b)
+    nbytes = algorithmic_bytes(b, args.window)
     n_att, ms_att = trace["attention"]
     att_ms = ms_att / max(n_att, 1)
     peak, peak_kind = measured_peaks()
@@ -615,7 +627,7 @@ def run_ours(args):
         raise RuntimeError(f"device error flags {flags:#x} during the timed region")
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.window:
         sampler_cpu = OracleSampler(b, cpu_workers(), budget_s=15.0)
         rate, wall = sampler_cpu.step()
         sampler_cpu.close()
@@ -758,6 +770,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches instead of replaying the step captured in a CUDA graph")
+    ap.add_argument("--window", type=int, default=0,
+                    help="decode workloads: sliding-window attention over the last W keys (pa_decode_windowed)")
     ap.add_argument("--no-shared-prefix", action="store_true",
                     help="agentic: call pa_decode instead of pa_decode_shared_prefix")
     ap.add_argument("--op", choices=("attention", "copy_blocks"), default="attention",

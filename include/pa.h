@@ -209,6 +209,26 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                     void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_decode_windowed -- pa_decode with sliding-window attention.
+ * [AGENTIC] "為什麼需要「分頁」記憶體管理": sliding-window attention only looks at
+ * the most recent fixed range, and blocks that leave it are reclaimed at once
+ * into the shared pool.  The query of sequence i (at position seq_lens[i] - 1)
+ * attends keys seq_lens[i] - window .. seq_lens[i] - 1 (all of them when the
+ * sequence is shorter).  Entries of blocks that lie wholly before the window may
+ * hold anything (released blocks): they are never read and never checked.
+ * window == 0 is pa_decode; window < 0 is PA_ERR_INVALID_ARG.  The workspace size
+ * is pa_decode_workspace_size(...) as for pa_decode; other arguments as pa_decode.
+ */
+pa_status pa_decode_windowed(void* out, const void* q, const void* k_cache, const void* v_cache,
+                             int32_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                             int32_t block_size, float scale, int32_t window, pa_dtype q_dtype,
+                             pa_dtype kv_dtype, const float* k_scale, const float* v_scale,
+                             int32_t partition_size, void* workspace, size_t workspace_bytes,
+                             pa_stream_t stream);
+
+/*
  * Bytes of workspace pa_decode_shared_prefix needs (>= 256) for num_groups groups;
  * partition_size as for pa_decode_workspace_size (0: the shared prefixes get their
  * own default partition size, sized by groups x KV heads).
@@ -331,6 +351,25 @@ pa_status pa_varlen_attn(void* out, const void* q, const void* k_cache, const vo
                          float scale, int32_t causal, pa_dtype q_dtype, pa_dtype kv_dtype,
                          const float* k_scale, const float* v_scale, int32_t partition_size,
                          void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_varlen_attn_windowed -- pa_varlen_attn with sliding-window attention
+ * (causal only; window > 0 with causal == 0 is PA_ERR_UNSUPPORTED).  Query j of a
+ * request (position p = seq_len - q_len + j) attends keys max(0, p - window + 1)
+ * .. p.  Entries of blocks wholly before the window of the request's first query
+ * may hold anything (released blocks): they are never read.  window == 0 is
+ * pa_varlen_attn; the workspace is sized by pa_varlen_workspace_size as for it.
+ */
+pa_status pa_varlen_attn_windowed(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                  int32_t num_blocks, const int32_t* block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t* query_start_loc,
+                                  const int32_t* seq_lens, int32_t num_seqs, int32_t total_q_tokens,
+                                  int32_t max_query_len, int32_t max_seq_len, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                  float scale, int32_t window, int32_t causal, pa_dtype q_dtype,
+                                  pa_dtype kv_dtype, const float* k_scale, const float* v_scale,
+                                  int32_t partition_size, void* workspace, size_t workspace_bytes,
+                                  pa_stream_t stream);
 
 /*
  * Read the device error word of the current device (host pointer `flags`),

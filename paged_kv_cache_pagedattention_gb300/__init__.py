@@ -50,6 +50,8 @@ SIGNATURES = {
     "pa_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "pa_decode": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
                                  _I32, _F, ctypes.c_int, ctypes.c_int, _P, _P, _I32, _P, _SZ, _P]),
+    "pa_decode_windowed": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
+                                          _I32, _F, _I32, ctypes.c_int, ctypes.c_int, _P, _P, _I32, _P, _SZ, _P]),
     "pa_decode_shared_prefix_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "pa_decode_shared_prefix": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
                                                _I32, _F, ctypes.c_int, ctypes.c_int, _P, _P, _P, _P, _I32,
@@ -60,6 +62,9 @@ SIGNATURES = {
     "pa_varlen_attn": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
                                       _I32, _I32, _I32, _I32, _F, _I32, ctypes.c_int, ctypes.c_int,
                                       _P, _P, _I32, _P, _SZ, _P]),
+    "pa_varlen_attn_windowed": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
+                                               _I32, _I32, _I32, _I32, _F, _I32, _I32, ctypes.c_int, ctypes.c_int,
+                                               _P, _P, _I32, _P, _SZ, _P]),
     "pa_get_error_flags": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), _I32, _P]),
     "pa_trace_enable": (ctypes.c_int, [_I32]),
     "pa_trace_read": (ctypes.c_int, [_I32, ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_double), _I32]),
@@ -155,8 +160,9 @@ def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size, max
 
 
 def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, scale, workspace,
-              k_scale=None, v_scale=None, partition_size=0, stream=None) -> None:
-    """PagedAttention decode; out/q [B][Hq][d], block_tables int32 [B][max_blocks], seq_lens int32 [B]."""
+              k_scale=None, v_scale=None, partition_size=0, stream=None, window=0) -> None:
+    """PagedAttention decode; out/q [B][Hq][d], block_tables int32 [B][max_blocks], seq_lens int32 [B].
+    window > 0: sliding-window attention (pa_decode_windowed)."""
     nb, hkv, bs, d = k_cache.shape
     b, hq = q.shape[0], q.shape[1]
     if q.dim() != 3 or q.shape[2] != d or out.shape != q.shape or out.dtype != q.dtype:
@@ -165,11 +171,11 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, sca
         raise ValueError("block_tables must be int32 [num_seqs][max_blocks_per_seq]")
     if seq_lens.dtype != torch.int32 or seq_lens.numel() != b:
         raise ValueError("seq_lens must be int32 [num_seqs]")
-    _check(_lib.pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables),
-                          block_tables.shape[1], _ptr(seq_lens), b, int(max_seq_len), hq, hkv, d, bs,
-                          float(scale), dtype_code(q), dtype_code(k_cache), _ptr(k_scale), _ptr(v_scale),
-                          int(partition_size), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                          _stream(stream)), "pa_decode")
+    _check(_lib.pa_decode_windowed(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables),
+                                   block_tables.shape[1], _ptr(seq_lens), b, int(max_seq_len), hq, hkv, d, bs,
+                                   float(scale), int(window), dtype_code(q), dtype_code(k_cache), _ptr(k_scale),
+                                   _ptr(v_scale), int(partition_size), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)), "pa_decode")
 
 
 def pa_decode_shared_prefix_workspace_size(num_seqs, num_groups, num_q_heads, num_kv_heads, head_size,
@@ -230,8 +236,9 @@ def pa_varlen_workspace_size(num_seqs, total_q_tokens, max_query_len, num_q_head
 
 def pa_varlen_attn(out, q, k_cache, v_cache, block_tables, query_start_loc, seq_lens, max_query_len,
                    max_seq_len, scale, workspace, causal=True, k_scale=None, v_scale=None,
-                   partition_size=0, stream=None) -> None:
-    """Attention of a flattened varlen batch; out/q [T][Hq][d], query_start_loc int32 [B+1]."""
+                   partition_size=0, stream=None, window=0) -> None:
+    """Attention of a flattened varlen batch; out/q [T][Hq][d], query_start_loc int32 [B+1].
+    window > 0: sliding-window attention (pa_varlen_attn_windowed)."""
     nb, hkv, bs, d = k_cache.shape
     t, hq = q.shape[0], q.shape[1]
     b = seq_lens.numel()
@@ -241,9 +248,9 @@ def pa_varlen_attn(out, q, k_cache, v_cache, block_tables, query_start_loc, seq_
         raise ValueError("query_start_loc must be int32 [num_seqs+1]")
     if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or block_tables.shape[0] != b:
         raise ValueError("block_tables must be int32 [num_seqs][max_blocks_per_seq]")
-    _check(_lib.pa_varlen_attn(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables),
+    _check(_lib.pa_varlen_attn_windowed(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables),
                                block_tables.shape[1], _ptr(query_start_loc), _ptr(seq_lens), b, t,
-                               int(max_query_len), int(max_seq_len), hq, hkv, d, bs, float(scale),
+                               int(max_query_len), int(max_seq_len), hq, hkv, d, bs, float(scale), int(window),
                                1 if causal else 0, dtype_code(q), dtype_code(k_cache), _ptr(k_scale),
                                _ptr(v_scale), int(partition_size), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream)),

@@ -8,6 +8,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -86,6 +87,14 @@ int resolve_partition(int requested, int num_seqs, int num_kv_heads, int max_seq
   int part = requested > 0 ? requested : default_partition(num_seqs, num_kv_heads, max_seq_len, block_size);
   while (ceil_div(max_seq_len, part) > 65535) part *= 2;
   return part;
+}
+
+// Partitions a row can use under a sliding window: its keys span at most
+// window + q_len - 1 positions from a block-aligned origin.
+int window_partitions(long long parts, int window, int max_query_len, int block_size, int part) {
+  if (window <= 0) return static_cast<int>(parts);
+  const long long span = (long long)window + max_query_len - 1 + block_size - 1;
+  return static_cast<int>(std::min<long long>(parts, ceil_div(span, part)));
 }
 
 int prefill_partition(int part) { return part > 16384 ? part : 16384 / part * part; }
@@ -451,7 +460,18 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                     int32_t head_size, int32_t block_size, float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
                     const float* k_scale, const float* v_scale, int32_t partition_size, void* workspace,
                     size_t workspace_bytes, pa_stream_t stream) {
-  if (num_seqs < 0) return PA_ERR_INVALID_ARG;
+  return pa_decode_windowed(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
+                            num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, scale, 0,
+                            q_dtype, kv_dtype, k_scale, v_scale, partition_size, workspace, workspace_bytes, stream);
+}
+
+pa_status pa_decode_windowed(void* out, const void* q, const void* k_cache, const void* v_cache, int32_t num_blocks,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                             int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                             int32_t head_size, int32_t block_size, float scale, int32_t window,
+                             pa_dtype q_dtype, pa_dtype kv_dtype, const float* k_scale, const float* v_scale,
+                             int32_t partition_size, void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  if (num_seqs < 0 || window < 0) return PA_ERR_INVALID_ARG;
   if (num_seqs == 0) return PA_OK;
   pa_status st = check_attention_args(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
                                       seq_lens, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size,
@@ -470,8 +490,10 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
   p.part = p.part_pf = L.part;
   p.part_shared = L.part;
   p.max_partitions = static_cast<int>(L.parts);
+  p.window = window;
   p.ws_ml = reinterpret_cast<float2*>(ws + L.ml_off);
   p.ws_acc = reinterpret_cast<float*>(ws + L.acc_off);
+  const int grid_z = window_partitions(L.parts, window, 1, block_size, L.part);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (pa::decode_mma_supported(q_dtype, kv_dtype, head_size, block_size, p.group)) {
@@ -480,10 +502,10 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
         !encode_cache_map(&tv, v_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size))
       return PA_ERR_CUDA;
     TraceScope t(1, s);
-    e = pa::launch_decode_mma(p, q_dtype, kv_dtype, static_cast<int>(L.parts), &tk, &tv, s);
+    e = pa::launch_decode_mma(p, q_dtype, kv_dtype, grid_z, &tk, &tv, s);
   } else {
     TraceScope t(1, s);
-    e = pa::launch_attn_generic(p, q_dtype, kv_dtype, static_cast<int>(L.parts), -1, s);
+    e = pa::launch_attn_generic(p, q_dtype, kv_dtype, grid_z, -1, s);
   }
   if (e != cudaSuccess) return PA_ERR_CUDA;
   if (L.parts > 1) {
@@ -598,7 +620,22 @@ pa_status pa_varlen_attn(void* out, const void* q, const void* k_cache, const vo
                          int32_t block_size, float scale, int32_t causal, pa_dtype q_dtype, pa_dtype kv_dtype,
                          const float* k_scale, const float* v_scale, int32_t partition_size, void* workspace,
                          size_t workspace_bytes, pa_stream_t stream) {
-  if (num_seqs < 0 || total_q_tokens < 0) return PA_ERR_INVALID_ARG;
+  return pa_varlen_attn_windowed(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
+                                 query_start_loc, seq_lens, num_seqs, total_q_tokens, max_query_len, max_seq_len,
+                                 num_q_heads, num_kv_heads, head_size, block_size, scale, 0, causal, q_dtype,
+                                 kv_dtype, k_scale, v_scale, partition_size, workspace, workspace_bytes, stream);
+}
+
+pa_status pa_varlen_attn_windowed(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                  int32_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* query_start_loc, const int32_t* seq_lens, int32_t num_seqs,
+                                  int32_t total_q_tokens, int32_t max_query_len, int32_t max_seq_len,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                  float scale, int32_t window, int32_t causal, pa_dtype q_dtype, pa_dtype kv_dtype,
+                                  const float* k_scale, const float* v_scale, int32_t partition_size,
+                                  void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  if (num_seqs < 0 || total_q_tokens < 0 || window < 0) return PA_ERR_INVALID_ARG;
+  if (window > 0 && !causal) return PA_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q_tokens == 0) return PA_OK;
   if (!query_start_loc || max_query_len < 1) return PA_ERR_INVALID_ARG;
   pa_status st = check_attention_args(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
@@ -622,6 +659,10 @@ pa_status pa_varlen_attn(void* out, const void* q, const void* k_cache, const vo
   p.part_shared = L.part;
   p.max_partitions = static_cast<int>(L.parts);
   p.causal = causal ? 1 : 0;
+  p.window = window;
+  const int grid_dec = window_partitions(L.parts, window, 1, block_size, L.part);
+  const int grid_all = window_partitions(L.parts, window, max_query_len, block_size, L.part);
+  const int grid_pf = window_partitions(L.parts_pf, window, max_query_len, block_size, L.part_pf);
   int32_t* work_count = reinterpret_cast<int32_t*>(ws);
   p.plan_ok = reinterpret_cast<int32_t*>(ws + 4);
   int32_t* part_off = reinterpret_cast<int32_t*>(ws + L.off_off);
@@ -656,15 +697,15 @@ pa_status pa_varlen_attn(void* out, const void* q, const void* k_cache, const vo
   const bool multi = max_query_len > 1;
   if (!fast_decode && !(multi && fast_prefill)) {
     TraceScope t(1, s);  // generic kernel for every row
-    e = pa::launch_attn_generic(p, q_dtype, kv_dtype, static_cast<int>(L.parts), -1, s);
+    e = pa::launch_attn_generic(p, q_dtype, kv_dtype, std::max(grid_all, grid_pf), -1, s);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   } else {
     if (fast_decode) {
       TraceScope t(1, s);
-      e = pa::launch_decode_mma(p, q_dtype, kv_dtype, static_cast<int>(L.parts), &tk, &tv, s);
+      e = pa::launch_decode_mma(p, q_dtype, kv_dtype, grid_dec, &tk, &tv, s);
     } else {
       TraceScope t(1, s);
-      e = pa::launch_attn_generic(p, q_dtype, kv_dtype, static_cast<int>(L.parts), 0, s);
+      e = pa::launch_attn_generic(p, q_dtype, kv_dtype, grid_dec, 0, s);
     }
     if (e != cudaSuccess) return PA_ERR_CUDA;
     if (multi && fast_prefill) {
@@ -672,7 +713,7 @@ pa_status pa_varlen_attn(void* out, const void* q, const void* k_cache, const vo
       e = pa::launch_prefill_tc(p, q_dtype, kv_dtype, static_cast<int>(L.max_work), &tk1, &tv, s);
     } else if (multi) {
       TraceScope t(1, s);
-      e = pa::launch_attn_generic(p, q_dtype, kv_dtype, static_cast<int>(L.parts_pf), 1, s);
+      e = pa::launch_attn_generic(p, q_dtype, kv_dtype, grid_pf, 1, s);
     }
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }

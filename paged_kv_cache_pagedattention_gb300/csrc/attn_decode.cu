@@ -128,9 +128,11 @@ __device__ __forceinline__ void load_query(const AttnParams& p, long long row, i
 }
 
 // One block of block_size tokens (K tile at `tile`, V tile at `tile + tile_bytes`)
-// folded into a warp's state; `rem` tokens of the block are valid.
+// folded into a warp's state; tokens lo .. rem-1 of the block are attended (lo > 0
+// only in the block where a sliding window starts; the tokens before it are older
+// cached tokens, finite, so only their scores are masked).
 template <int QDT, int KVDT, int HEAD, int BS>
-__device__ __forceinline__ void attend_block(const uint8_t* tile, int rem, const uint32_t (&qb)[HEAD / 16][2],
+__device__ __forceinline__ void attend_block(const uint8_t* tile, int rem, int lo, const uint32_t (&qb)[HEAD / 16][2],
                                              float cA, float cB, WarpState<HEAD>& w) {
   using G = DecodeGeom<KVDT, HEAD, BS>;
   constexpr bool kFp8 = G::kFp8;
@@ -185,12 +187,12 @@ __device__ __forceinline__ void attend_block(const uint8_t* tile, int rem, const
   // than kRescaleSlack: until then P = 2^(s*c - m) <= 2^kRescaleSlack and O, l need
   // no rescale.  The final normalisation divides by l computed with the same m, so
   // the result is the same softmax.
-  if (rem < BS) {  // tokens past the sequence end: raw score -inf
+  if (rem < BS || lo > 0) {  // tokens past the sequence end or before the window: -inf
 #pragma unroll
     for (int mt = 0; mt < G::kMTiles; ++mt) {
       const int t0 = 16 * mt + (lane >> 2);
-      if (t0 >= rem) sc[mt][0] = sc[mt][1] = -INFINITY;
-      if (t0 + 8 >= rem) sc[mt][2] = sc[mt][3] = -INFINITY;
+      if (t0 >= rem || t0 < lo) sc[mt][0] = sc[mt][1] = -INFINITY;
+      if (t0 + 8 >= rem || t0 + 8 < lo) sc[mt][2] = sc[mt][3] = -INFINITY;
     }
   }
   float mxA = -INFINITY, mxB = -INFINITY;
@@ -348,8 +350,10 @@ __global__ void __launch_bounds__(NW * 32)
     }
     return;
   }
-  // tokens [start, seq_len) are this kernel's; [0, start) belong to the shared-prefix kernel
-  const int start = p.query_start_loc == nullptr ? shared_prefix_tokens(p, r) : 0;
+  // tokens [start, seq_len) are this kernel's; [0, start) belong to the shared-prefix
+  // kernel, or lie before the sliding window's origin block (never read)
+  const int shared_start = p.query_start_loc == nullptr ? shared_prefix_tokens(p, r) : 0;
+  const int start = max(shared_start, window_origin(p, seq_len, 1));
   const int nblk = (seq_len + BS - 1) / BS;
   const int pb = p.part / BS;
   const int sb0 = start / BS;
@@ -357,7 +361,8 @@ __global__ void __launch_bounds__(NW * 32)
   if (b0 >= nblk) return;
   const int b1 = min(b0 + pb, nblk);
   const int nparts = (nblk - sb0 + pb - 1) / pb;
-  const int shared_parts = start > 0 ? (start + p.part_shared - 1) / p.part_shared : 0;
+  // this row's partials follow those of its shared prefix (none under a window)
+  const int shared_parts = shared_start > 0 ? (shared_start + p.part_shared - 1) / p.part_shared : 0;
 
   if (threadIdx.x == 0) {
     s_failed = 0;
@@ -421,7 +426,9 @@ __global__ void __launch_bounds__(NW * 32)
     consumed = i + 1;
     if (wok[s]) {
       const int jb = b0 + warp + i * NW;
-      attend_block<QDT, KVDT, HEAD, BS>(ring + s * 2 * TB, seq_len - jb * BS, qb, cA, cB, w);
+      // first key attended (sliding window), relative to the block
+      const int lo = p.window > 0 ? seq_len - p.window - jb * BS : 0;
+      attend_block<QDT, KVDT, HEAD, BS>(ring + s * 2 * TB, seq_len - jb * BS, lo, qb, cA, cB, w);
     }
     __syncwarp();
     const int j = i + ST;
@@ -604,7 +611,7 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32)
       if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
       return;
     }
-    if (stage_ok[s]) attend_block<QDT, KVDT, HEAD, BS>(smem + s * 2 * TB, BS, qb, cA, cB, w);
+    if (stage_ok[s]) attend_block<QDT, KVDT, HEAD, BS>(smem + s * 2 * TB, BS, 0, qb, cA, cB, w);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + s);
   }

@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(128)
   if (z >= ri.parts_row) return;
 
   const int kvh = head / p.group;
-  const int t0 = z * ri.part;
+  const int t0 = ri.origin + z * ri.part;  // partition z of the row's keys
   const int t1 = min(t0 + ri.part, ri.kv_len);
   float kscale = 1.f, vscale = 1.f;
   if (KVDT == PA_FP8_E4M3) {
@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(128)
   const typename KE::T* vc = reinterpret_cast<const typename KE::T*>(p.v_cache);
   const int32_t* table = p.block_tables + (long long)ri.request * p.max_blocks_per_seq;
   float m = -INFINITY, l = 0.f;
-  for (int t = t0; t < t1; ++t) {
+  for (int t = max(t0, ri.lo); t < t1; ++t) {  // keys before the window are not read
     const int phys = table[t / p.block_size];
     if (phys < 0 || phys >= p.num_blocks) {
       if (lane == 0) flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
@@ -339,13 +339,14 @@ __global__ void __launch_bounds__(1024)
                                                    ? PA_ERRFLAG_QUERY : PA_ERRFLAG_SEQ_LEN);
       if (ok && q_len > 0 && seq_len >= 1) {
         part = q_len == 1 ? p.part : p.part_pf;
-        parts = ceil_div_dev(seq_len, part);
+        const int origin = window_origin(p, seq_len, q_len);
+        parts = ceil_div_dev(seq_len - origin, part);
         if (q_len > 1) {
           // tiles of tile_tokens query tokens; a tile needs the partitions up to its last key
           for (int t0 = 0; t0 < q_len; t0 += tile_tokens) {
             const int last = min(t0 + tile_tokens, q_len) - 1;
             const int kv = p.causal ? seq_len - q_len + last + 1 : seq_len;
-            items += ceil_div_dev(kv, part);
+            items += ceil_div_dev(kv - origin, part);
           }
         }
       }
@@ -377,10 +378,11 @@ __global__ void __launch_bounds__(1024)
       if (items) {
         int k = ex1;
         const int row0 = p.query_start_loc[r];
+        const int origin = window_origin(p, seq_len, q_len);
         for (int t0 = 0; t0 < q_len; t0 += tile_tokens) {
           const int last = min(t0 + tile_tokens, q_len) - 1;
           const int kv = p.causal ? seq_len - q_len + last + 1 : seq_len;
-          const int np = ceil_div_dev(kv, part);
+          const int np = ceil_div_dev(kv - origin, part);
           for (int z = 0; z < np; ++z, ++k)
             if (k < max_work) work[k] = make_int4(r, row0 + t0, z, 0);
         }

@@ -228,25 +228,30 @@ __global__ void __launch_bounds__(threads_tc<KVDT == PA_FP8_E4M3>(), 1)
   const int ntok = min(kTiles * tile_tokens, q_len - t0);
   const int pos0 = seq_len - q_len + t0;                // position of the CTA's first token
   const int part = p.part_pf;
-  const int parts_req = (seq_len + part - 1) / part;
-  const int k0 = z * part;
-  // keys [k0, k1) of this partition that some row of tile t attends -> its chunks
+  // partitions count from the request's origin (0, or the block where the first
+  // query's sliding window starts)
+  const int origin = window_origin(p, seq_len, q_len);
+  const int parts_req = (seq_len - origin + part - 1) / part;
+  const int k0 = origin + z * part;
+  // chunks start at the block holding the first key the CTA's first row attends
+  const int klo = p.window > 0 ? max(k0, max(0, pos0 - p.window + 1) / BS * BS) : k0;
+  // keys [klo, k1) of this partition that some row of tile t attends -> its chunks
   auto tile_chunks = [&](int t) {
     const int nt = min(ntok, (t + 1) * tile_tokens) - t * tile_tokens;
     if (nt <= 0) return 0;
     const int k1t = min(k0 + part, p.causal ? pos0 + t * tile_tokens + nt : seq_len);
-    return k1t > k0 ? (k1t - k0 + kChunk - 1) / kChunk : 0;
+    return k1t > klo ? (k1t - klo + kChunk - 1) / kChunk : 0;
   };
   static_assert(kTiles == 2, "two tiles per CTA");
   const int nch_t[kTiles] = {tile_chunks(0), tile_chunks(1)};
   const int k1 = min(k0 + part, p.causal ? pos0 + ntok : seq_len);
-  const int nch = k1 > k0 ? (k1 - k0 + kChunk - 1) / kChunk : 0;  // = the largest nch_t
-  const int kb_first = k0 / BS;
+  const int nch = k1 > klo ? (k1 - klo + kChunk - 1) / kChunk : 0;  // = the largest nch_t
+  const int kb_first = klo / BS;
   // keys held by the blocks a chunk loads end at the last block that reaches k1; V
   // rows past them (or past seq_len) are zeroed before they meet P.  Only the last
   // chunk can hold such rows; the last tile that reads it zeroes them.
   const int kv_loaded_end = min(seq_len, (k1 + BS - 1) / BS * BS);
-  const bool tail_chunk = nch > 0 && k0 + nch * kChunk > kv_loaded_end;
+  const bool tail_chunk = nch > 0 && klo + nch * kChunk > kv_loaded_end;
   const int zero_tile = nch_t[kTiles - 1] == nch ? kTiles - 1 : 0;
 
   extern __shared__ uint8_t smem_raw[];
@@ -572,10 +577,11 @@ __global__ void __launch_bounds__(threads_tc<KVDT == PA_FP8_E4M3>(), 1)
     const float c = kF8 ? ldexpf(p.scale * kLog2e * (*p.k_scale), -q_shift) : p.scale * kLog2e;
     const float out_scale = kF8 ? *p.v_scale : 1.f;
     const int row_limit = p.causal ? min(k1, row_pos + 1) : k1;  // this row attends keys < row_limit
+    const int row_lo = p.window > 0 ? max(0, row_pos - p.window + 1) : 0;  // ... and keys >= row_lo
     float m = -INFINITY, l = 0.f;
     bool fail = false;
     for (int i = 0; i < my_nch; ++i) {
-      const int base = k0 + i * kChunk;
+      const int base = klo + i * kChunk;
       const uint32_t tS = tT + (i % kSBufs) * 64;
       const bool got = mbar_wait_bounded(my_s_full + i % kSBufs, (i / kSBufs) & 1);
       if (!__all_sync(0xffffffffu, got)) {
@@ -590,11 +596,12 @@ __global__ void __launch_bounds__(threads_tc<KVDT == PA_FP8_E4M3>(), 1)
       float sc[kChunk];
 #pragma unroll
       for (int j = 0; j < kChunk; ++j) sc[j] = __uint_as_float(sr[j]);
-      const int rem = row_limit - base;  // keys of this chunk the row attends: [0, rem)
-      if (rem < kChunk) {
+      const int rem = row_limit - base;  // keys of this chunk the row attends: [lo_rem, rem)
+      const int lo_rem = row_lo - base;
+      if (rem < kChunk || lo_rem > 0) {
 #pragma unroll
         for (int j = 0; j < kChunk; ++j)
-          if (j >= rem) sc[j] = -INFINITY;
+          if (j >= rem || j < lo_rem) sc[j] = -INFINITY;
       }
       // row maximum: eight independent chains of three-input maxima
       float mq[8];
@@ -690,7 +697,7 @@ __global__ void __launch_bounds__(threads_tc<KVDT == PA_FP8_E4M3>(), 1)
       // ---- epilogue: thread = row; direct output when the row needs one partition,
       // else its partial state (unnormalised O, max in log2 units, sum)
       const int kv_len = p.causal ? row_pos + 1 : seq_len;
-      const int parts_row = (kv_len + part - 1) / part;
+      const int parts_row = (kv_len - origin + part - 1) / part;
       const bool write = row_valid && z < parts_row;
       const bool direct = parts_row == 1;
       const int tq = t0 + row_tok;

@@ -259,6 +259,16 @@ __device__ __forceinline__ float warp_sum_xor(float v, int lane_mask_lo, int lan
 
 namespace pa {
 
+// Sliding window ([AGENTIC] "為什麼需要「分頁」記憶體管理": only the most recent
+// fixed range is attended; blocks that leave it are reclaimed).  A request's
+// split-K partitions start at its origin: the block holding the first key its
+// first query attends.  Blocks before the origin are never read.
+__device__ __forceinline__ int window_origin(const AttnParams& p, int seq_len, int q_len) {
+  if (p.window <= 0) return 0;
+  const int first = max(0, seq_len - q_len - p.window + 1);
+  return first / p.block_size * p.block_size;
+}
+
 // Where a query row sits: its request, position, the keys it attends and the
 // split-K partitioning of those keys.
 struct RowInfo {
@@ -267,10 +277,12 @@ struct RowInfo {
   int j;          // row index inside its request
   int seq_len;
   int pos;        // position of the query token: seq_len - q_len + j
-  int kv_len;     // number of keys attended: pos + 1 (causal) or seq_len
+  int kv_len;     // keys attended end here: pos + 1 (causal) or seq_len
+  int lo;         // first key attended (sliding window), else 0
+  int origin;     // first key of the request's partition 0 (block aligned)
   int part;       // partition tokens for this request
-  int parts_req;  // partitions covering seq_len (sizes the request's partial rows)
-  int parts_row;  // partitions covering kv_len (the ones this row uses)
+  int parts_req;  // partitions covering origin .. seq_len (sizes the request's partial rows)
+  int parts_row;  // partitions covering origin .. kv_len (the ones this row uses)
   bool ok;
 };
 
@@ -297,9 +309,11 @@ __device__ __forceinline__ RowInfo row_info(const AttnParams& p, int row) {
           ri.q_len >= 1 && ri.q_len <= ri.seq_len && ri.j >= 0 && ri.j < ri.q_len;
   ri.pos = ri.seq_len - ri.q_len + ri.j;
   ri.kv_len = p.causal ? ri.pos + 1 : ri.seq_len;
+  ri.lo = p.window > 0 ? max(0, ri.pos - p.window + 1) : 0;
+  ri.origin = window_origin(p, ri.seq_len, ri.q_len);
   ri.part = ri.q_len == 1 ? p.part : p.part_pf;
-  ri.parts_req = ri.ok ? ceil_div_dev(ri.seq_len, ri.part) : 0;
-  ri.parts_row = ri.ok ? ceil_div_dev(ri.kv_len, ri.part) : 0;
+  ri.parts_req = ri.ok ? ceil_div_dev(ri.seq_len - ri.origin, ri.part) : 0;
+  ri.parts_row = ri.ok ? ceil_div_dev(ri.kv_len - ri.origin, ri.part) : 0;
   return ri;
 }
 

@@ -50,6 +50,7 @@ struct AttnParams {
   int part_shared;      // partition tokens of a group's shared prefix (shared-prefix decode)
   int max_partitions;   // decode mode: partial rows reserved per query row
   int causal;
+  int window;           // sliding window: a query at position p attends keys > p - window (0 = all)
   int num_groups;       // shared-prefix decode: number of groups (0 = no sharing)
   int max_group_size;   // shared-prefix decode: host bound on sequences per group (<= 8)
   int force_partials;   // every row writes partial states and goes through the merge
