@@ -30,6 +30,7 @@ invariants, an independent library routine or brute force.  No function is
 from .paged_attention import (  # noqa: F401
     DTYPE_BYTES,
     E4M3_MAX,
+    E5M2_MAX,
     attend,
     blocks_needed,
     bytes_per_block,
@@ -38,6 +39,9 @@ from .paged_attention import (  # noqa: F401
     e4m3_encode,
     e4m3_value,
     e4m3_table,
+    e5m2_encode,
+    e5m2_table,
+    e5m2_value,
     finalize_partial,
     gather_kv,
     kv_cache_bytes,
@@ -45,6 +49,7 @@ from .paged_attention import (  # noqa: F401
     paged_decode,
     paged_varlen,
     quantize_e4m3,
+    quantize_e5m2,
     reshape_and_cache,
     softmax_partial,
     softmax_weights,

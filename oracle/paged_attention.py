@@ -26,11 +26,13 @@ import math
 
 import numpy as np
 
-DTYPE_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "fp8_e4m3": 1}
-_BITS = {"f32": np.uint32, "f16": np.uint16, "bf16": np.uint16, "fp8_e4m3": np.uint8}
+DTYPE_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "fp8_e4m3": 1, "fp8_e5m2": 1}
+_BITS = {"f32": np.uint32, "f16": np.uint16, "bf16": np.uint16, "fp8_e4m3": np.uint8, "fp8_e5m2": np.uint8}
 
 # Largest finite FP8 e4m3 magnitude: exponent field 15, mantissa 6 -> 1.75 * 2^8.
 E4M3_MAX = 448.0
+# Largest finite FP8 e5m2 magnitude: exponent field 30, mantissa 3 -> 1.75 * 2^15.
+E5M2_MAX = 57344.0
 
 
 # --------------------------------------------------------------------------
@@ -102,6 +104,35 @@ _E4M3 = e4m3_table()
 _E4M3_POS = _E4M3[:127]
 
 
+def _fp8_encode(x, pos_mags: np.ndarray, vmax: float) -> np.ndarray:
+    """Nearest FP8 code, ties to even, saturating at ``vmax``; ``pos_mags`` are the
+    non-negative finite magnitudes in code order (strictly increasing)."""
+    x = np.asarray(x, dtype=np.float64)
+    flat = x.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint8)
+    top = len(pos_mags) - 1
+    for i, v in enumerate(flat):
+        if math.isnan(v):
+            out[i] = 0x7F
+            continue
+        a = abs(v)
+        if a >= vmax:
+            code = top
+        else:
+            hi = int(np.searchsorted(pos_mags, a, side="right"))  # first magnitude > a
+            lo = hi - 1                                           # magnitude <= a
+            d_lo = a - pos_mags[lo]
+            d_hi = pos_mags[hi] - a
+            if d_lo < d_hi:
+                code = lo
+            elif d_hi < d_lo:
+                code = hi
+            else:
+                code = lo if lo % 2 == 0 else hi
+        out[i] = code | (0x80 if math.copysign(1.0, v) < 0 else 0)
+    return out.reshape(x.shape)
+
+
 def e4m3_encode(x) -> np.ndarray:
     """Round float64 values to FP8 e4m3 codes: nearest, ties to even, saturating.
 
@@ -111,29 +142,41 @@ def e4m3_encode(x) -> np.ndarray:
     (saturation to the largest finite value).  The sign is kept, so small
     negative values give negative zero (0x80).  NaN gives 0x7F.
     """
-    x = np.asarray(x, dtype=np.float64)
-    flat = x.reshape(-1)
-    out = np.empty(flat.shape, dtype=np.uint8)
-    for i, v in enumerate(flat):
-        if math.isnan(v):
-            out[i] = 0x7F
-            continue
-        a = abs(v)
-        if a >= E4M3_MAX:
-            code = 126
-        else:
-            hi = int(np.searchsorted(_E4M3_POS, a, side="right"))  # first magnitude > a
-            lo = hi - 1                                            # magnitude <= a
-            d_lo = a - _E4M3_POS[lo]
-            d_hi = _E4M3_POS[hi] - a
-            if d_lo < d_hi:
-                code = lo
-            elif d_hi < d_lo:
-                code = hi
-            else:
-                code = lo if lo % 2 == 0 else hi
-        out[i] = code | (0x80 if math.copysign(1.0, v) < 0 else 0)
-    return out.reshape(x.shape)
+    return _fp8_encode(x, _E4M3_POS, E4M3_MAX)
+
+
+def e5m2_value(code: int) -> float:
+    """Value of one FP8 e5m2 code, from its bit fields.
+
+    The second FP8 cache format of the [NOTES] ``--kv-cache-dtype`` knob: 1 sign
+    bit, 5 exponent bits (bias 15), 2 mantissa bits; exponent field 0 holds
+    subnormals m/4 * 2^-14; exponent field 31 is infinity (mantissa 0) or NaN.
+    """
+    code = int(code) & 0xFF
+    sign = -1.0 if code & 0x80 else 1.0
+    exp_field = (code >> 2) & 0x1F
+    mant = code & 0x3
+    if exp_field == 0x1F:
+        return sign * math.inf if mant == 0 else math.nan
+    if exp_field == 0:
+        return sign * (mant / 4.0) * 2.0 ** -14
+    return sign * (1.0 + mant / 4.0) * 2.0 ** (exp_field - 15)
+
+
+def e5m2_table() -> np.ndarray:
+    """float64 value of every one of the 256 e5m2 codes."""
+    return np.array([e5m2_value(c) for c in range(256)], dtype=np.float64)
+
+
+_E5M2 = e5m2_table()
+# Non-negative finite magnitudes, codes 0..123 (0x7B = 57344), strictly increasing.
+_E5M2_POS = _E5M2[:124]
+
+
+def e5m2_encode(x) -> np.ndarray:
+    """Round float64 values to FP8 e5m2 codes: nearest, ties to even, saturating
+    to +-57344 (no infinity is produced); NaN gives 0x7F."""
+    return _fp8_encode(x, _E5M2_POS, E5M2_MAX)
 
 
 def quantize_e4m3(x64, scale: float) -> np.ndarray:
@@ -146,6 +189,12 @@ def quantize_e4m3(x64, scale: float) -> np.ndarray:
     """
     q32 = (np.asarray(x64, dtype=np.float64) / np.float64(np.float32(scale))).astype(np.float32)
     return e4m3_encode(q32.astype(np.float64))
+
+
+def quantize_e5m2(x64, scale: float) -> np.ndarray:
+    """As ``quantize_e4m3`` for the e5m2 format: e5m2 rounding of the fp32 quotient."""
+    q32 = (np.asarray(x64, dtype=np.float64) / np.float64(np.float32(scale))).astype(np.float32)
+    return e5m2_encode(q32.astype(np.float64))
 
 
 def decode_bits(bits, dtype: str, scale: float = 1.0) -> np.ndarray:
@@ -164,6 +213,8 @@ def decode_bits(bits, dtype: str, scale: float = 1.0) -> np.ndarray:
         return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
     if dtype == "fp8_e4m3":
         return _E4M3[b.astype(np.uint8)] * np.float64(np.float32(scale))
+    if dtype == "fp8_e5m2":
+        return _E5M2[b.astype(np.uint8)] * np.float64(np.float32(scale))
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
@@ -193,9 +244,10 @@ def reshape_and_cache(key_bits, value_bits, k_cache, v_cache, slot_mapping,
         if cache_dtype == src_dtype:
             k_cache[blk, :, off, :] = key_bits[t]
             v_cache[blk, :, off, :] = value_bits[t]
-        elif cache_dtype == "fp8_e4m3":
-            k_cache[blk, :, off, :] = quantize_e4m3(decode_bits(key_bits[t], src_dtype), k_scale)
-            v_cache[blk, :, off, :] = quantize_e4m3(decode_bits(value_bits[t], src_dtype), v_scale)
+        elif cache_dtype in ("fp8_e4m3", "fp8_e5m2"):
+            quant = quantize_e4m3 if cache_dtype == "fp8_e4m3" else quantize_e5m2
+            k_cache[blk, :, off, :] = quant(decode_bits(key_bits[t], src_dtype), k_scale)
+            v_cache[blk, :, off, :] = quant(decode_bits(value_bits[t], src_dtype), v_scale)
         else:
             raise ValueError(f"unsupported {src_dtype} -> {cache_dtype}")
 

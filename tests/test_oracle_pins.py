@@ -111,6 +111,32 @@ def test_e4m3_encode_saturates_and_nan():
     assert list(codes) == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE, 0x7F]
 
 
+def test_e5m2_decode_exhaustive_vs_torch():
+    ours = oracle.e5m2_table()
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e5m2).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ours[ok], ref[ok])
+    assert ours[0x7B] == 57344.0 and ours[0x01] == 2.0 ** -16 and ours[0x7C] == np.inf
+
+
+def test_e5m2_encode_vs_torch_in_range():
+    mags = oracle.e5m2_table()[:124]
+    mids = (mags[:-1] + mags[1:]) / 2                       # exact ties
+    rng = np.random.default_rng(8)
+    pts = np.concatenate([mags, mids, np.nextafter(mids, 0), np.nextafter(mids, np.inf),
+                          rng.uniform(0, 57000, 4000), np.float64(2.0) ** rng.uniform(-18, 15.7, 4000)])
+    pts = pts[pts < 57344.0].astype(np.float32).astype(np.float64)
+    x = np.concatenate([pts, -pts, [0.0, -0.0]])
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.count_nonzero(oracle.e5m2_encode(x) != ref) == 0
+
+
+def test_e5m2_encode_saturates_and_nan():
+    codes = oracle.e5m2_encode(np.array([57344.0, 61439.0, 61440.0, 1e9, np.inf, -1e9, -np.inf, np.nan]))
+    assert list(codes) == [0x7B, 0x7B, 0x7B, 0x7B, 0x7B, 0xFB, 0xFB, 0x7F]
+
+
 def test_quantize_with_non_power_of_two_scale_vs_torch():
     rng = np.random.default_rng(3)
     x = rng.standard_normal(5000).astype(np.float32)
