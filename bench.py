@@ -38,7 +38,7 @@ METRIC = "attended KV tokens/sec and achieved HBM GB/s (fraction of GB300 peak),
 UNIT = "tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-WORKLOADS = ("agentic", "llama", "fp8", "mixed", "mixed_fp8", "tiny")
+WORKLOADS = ("agentic", "llama", "fp8", "fp8_e5m2", "mixed", "mixed_fp8", "tiny")
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -221,6 +221,8 @@ def make_workload(name: str, seed: int, length_scale: float = 1.0):
         return workloads.fp8(seed=seed, scale_lengths=length_scale)
     if name == "mixed":
         return workloads.mixed(seed=seed, scale_lengths=length_scale)
+    if name == "fp8_e5m2":
+        return workloads.fp8_e5m2(seed=seed, scale_lengths=length_scale)
     if name == "mixed_fp8":
         return workloads.mixed_fp8(seed=seed, scale_lengths=length_scale)
     if name == "tiny":
@@ -228,7 +230,7 @@ def make_workload(name: str, seed: int, length_scale: float = 1.0):
     raise ValueError(name)
 
 
-BASE_SEEDS = {"agentic": 2, "llama": 1, "fp8": 4, "mixed": 3, "mixed_fp8": 3, "tiny": 0}
+BASE_SEEDS = {"agentic": 2, "llama": 1, "fp8": 4, "fp8_e5m2": 4, "mixed": 3, "mixed_fp8": 3, "tiny": 0}
 
 
 def prefix_groups(b):
@@ -439,7 +441,7 @@ def run_ours(args):
     tables = torch.from_numpy(b.block_tables).to(dev)
     lens = torch.from_numpy(b.seq_lens).to(dev)
     qsl = torch.from_numpy(b.query_start_loc).to(dev)
-    fp8 = b.kv_dtype == "fp8_e4m3"
+    fp8 = b.kv_dtype in workloads.FP8
     ks = torch.tensor([b.k_scale], dtype=torch.float32, device=dev) if fp8 else None
     vs = torch.tensor([b.v_scale], dtype=torch.float32, device=dev) if fp8 else None
     out = torch.empty_like(q)

@@ -92,7 +92,8 @@ typedef enum pa_dtype {
   PA_F32 = 0,
   PA_F16 = 1,
   PA_BF16 = 2,
-  PA_FP8_E4M3 = 3 /* cache only: stored as uint8 codes with a per-tensor fp32 scale */
+  PA_FP8_E4M3 = 3, /* cache only: stored as uint8 codes with a per-tensor fp32 scale */
+  PA_FP8_E5M2 = 4  /* cache only: as PA_FP8_E4M3, 5 exponent and 2 mantissa bits */
 } pa_dtype;
 
 /* Bits of the device error word (pa_get_error_flags). */
@@ -121,7 +122,8 @@ int32_t pa_version(void);
  *                  Two tokens with the same slot in one call: which one lands is
  *                  unspecified.
  *   cache_dtype == src_dtype copies the bits exactly.  cache_dtype == PA_FP8_E4M3
- *   (src f32/f16/bf16) stores e4m3_rne_satfinite(float(x) / *k_scale) (resp. v),
+ *   or PA_FP8_E5M2 (src f32/f16/bf16) stores fp8_rne_satfinite(float(x) / *k_scale)
+ *   (resp. v; saturation at +-448 for e4m3, +-57344 for e5m2),
  *   the division being IEEE fp32 division.  k_scale / v_scale: device pointers to
  *   one float each, used only for FP8 (may be NULL otherwise).
  *   head_size * dtype_bytes must be a multiple of 16 bytes for both dtypes.
@@ -186,7 +188,7 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t n
  *
  *   out            [num_seqs][num_q_heads][head_size], q_dtype (written)
  *   q              [num_seqs][num_q_heads][head_size], q_dtype (f32, f16 or bf16)
- *   k_cache, v_cache  cache tensors, kv_dtype; kv_dtype == q_dtype, or PA_FP8_E4M3
+ *   k_cache, v_cache  cache tensors, kv_dtype; kv_dtype == q_dtype, or PA_FP8_E4M3 / E5M2
  *                  with q_dtype f16/bf16 (k_scale / v_scale then required)
  *   block_tables   int32 [num_seqs][max_blocks_per_seq]
  *   seq_lens       int32 [num_seqs], each in [1, max_seq_len]

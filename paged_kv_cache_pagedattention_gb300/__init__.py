@@ -30,7 +30,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_BOUNDS, \
     PA_ERR_TIMEOUT, PA_ERR_CUDA = range(7)
-PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = range(4)
+PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3, PA_FP8_E5M2 = range(5)
 PA_ERRFLAG_BLOCK_TABLE, PA_ERRFLAG_SLOT, PA_ERRFLAG_SEQ_LEN, PA_ERRFLAG_QUERY, PA_ERRFLAG_TIMEOUT = \
     0x1, 0x2, 0x4, 0x8, 0x10
 
@@ -86,7 +86,9 @@ def _check(status: int, where: str) -> None:
         raise PAError(status, where)
 
 
-_DT = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.uint8: PA_FP8_E4M3}
+# FP8 caches: uint8 codes are e4m3; torch's float8 dtypes name their format
+_DT = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.uint8: PA_FP8_E4M3,
+       torch.float8_e4m3fn: PA_FP8_E4M3, torch.float8_e5m2: PA_FP8_E5M2}
 
 
 def dtype_code(t: torch.Tensor) -> int:

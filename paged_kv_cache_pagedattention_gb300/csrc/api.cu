@@ -61,6 +61,7 @@ int dtype_bytes(int dt) {
     case PA_F16: return 2;
     case PA_BF16: return 2;
     case PA_FP8_E4M3: return 1;
+    case PA_FP8_E5M2: return 1;
     default: return 0;
   }
 }
@@ -321,8 +322,9 @@ pa_status check_attention_args(const void* out, const void* q, const void* k_cac
   if (num_q_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
   if (partition_size < 0 || (partition_size > 0 && partition_size % block_size)) return PA_ERR_INVALID_ARG;
   if (q_dtype != PA_F32 && q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-  if (kv_dtype != q_dtype && kv_dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
-  if (kv_dtype == PA_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+  const bool kv_fp8 = kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_FP8_E5M2;
+  if (kv_dtype != q_dtype && !kv_fp8) return PA_ERR_UNSUPPORTED;
+  if (kv_fp8 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
   if (head_size > 256) return PA_ERR_UNSUPPORTED;
   if (num_kv_heads * ((num_q_heads / num_kv_heads + 7) / 8) > 65535) return PA_ERR_UNSUPPORTED;
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return PA_ERR_INVALID_ARG;
@@ -390,8 +392,9 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
   if (num_tokens == 0) return PA_OK;
   if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
   if (src_dtype != PA_F32 && src_dtype != PA_F16 && src_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-  if (cache_dtype != src_dtype && cache_dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
-  if (cache_dtype == PA_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+  const bool cache_fp8 = cache_dtype == PA_FP8_E4M3 || cache_dtype == PA_FP8_E5M2;
+  if (cache_dtype != src_dtype && !cache_fp8) return PA_ERR_UNSUPPORTED;
+  if (cache_fp8 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
   if ((head_size * dtype_bytes(src_dtype)) % 16 || (head_size * dtype_bytes(cache_dtype)) % 16)
     return PA_ERR_UNSUPPORTED;
   if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
@@ -583,7 +586,7 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
       s2 = side->stream;
     {
       TraceScope t(5, s);
-      e = kv_dtype == PA_FP8_E4M3
+      e = (kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_FP8_E5M2)
               ? pa::launch_shared_prefix(p, q_dtype, kv_dtype, static_cast<int>(L.parts_shared), &tk, &tv, s)
               : pa::launch_shared_prefix_tiles(p, q_dtype, static_cast<int>(L.parts_shared), &tk, &tv, s);
     }

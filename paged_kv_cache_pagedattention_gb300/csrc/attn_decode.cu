@@ -50,7 +50,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 
 template <int KVDT, int HEAD, int BS>
 struct DecodeGeom {
-  static constexpr bool kFp8 = KVDT == PA_FP8_E4M3;
+  static constexpr bool kFp8 = is_fp8<KVDT>();
   static constexpr int kElemBytes = kFp8 ? 1 : 2;
   static constexpr int kRowBytes = HEAD * kElemBytes;  // one token of one head
   static constexpr int kTileBytes = BS * kRowBytes;
@@ -92,7 +92,7 @@ __device__ __forceinline__ void load_query(const AttnParams& p, long long row, i
   const float base_c = p.scale * kLog2e;
   const typename QE::T* qrow =
       reinterpret_cast<const typename QE::T*>(p.q) + (row * p.num_q_heads + h0 + qn) * HEAD;
-  if constexpr (KVDT != PA_FP8_E4M3) {
+  if constexpr (!is_fp8<KVDT>()) {
     const uint32_t* qw = reinterpret_cast<const uint32_t*>(qrow);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
@@ -168,10 +168,10 @@ __device__ __forceinline__ void attend_block(const uint8_t* tile, int rem, int l
       const uint32_t wb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
 #pragma unroll
       for (int ks = 0; ks < G::kKSteps; ++ks) {
-        const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(wa[ks] & 0xffffu));
-        const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(wa[ks] >> 16));
-        const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(wb[ks] & 0xffffu));
-        const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(wb[ks] >> 16));
+        const uint32_t a0 = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(wa[ks] & 0xffffu));
+        const uint32_t a2 = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(wa[ks] >> 16));
+        const uint32_t a1 = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(wb[ks] & 0xffffu));
+        const uint32_t a3 = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(wb[ks] >> 16));
         if (ks & 1) mma_16816<PA_F16>(sc2, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
         else mma_16816<PA_F16>(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
       }
@@ -281,10 +281,10 @@ __device__ __forceinline__ void attend_block(const uint8_t* tile, int rem, int l
 #pragma unroll
       for (int dt = 0; dt < G::kDTiles; ++dt) {
         const int sh = 16 * (dt & 1);
-        const uint32_t x0 = e4m3x2_to_f16x2(static_cast<uint16_t>(w0[dt >> 1] >> sh));
-        const uint32_t y0 = e4m3x2_to_f16x2(static_cast<uint16_t>(w1[dt >> 1] >> sh));
-        const uint32_t x1 = e4m3x2_to_f16x2(static_cast<uint16_t>(w2[dt >> 1] >> sh));
-        const uint32_t y1 = e4m3x2_to_f16x2(static_cast<uint16_t>(w3[dt >> 1] >> sh));
+        const uint32_t x0 = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(w0[dt >> 1] >> sh));
+        const uint32_t y0 = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(w1[dt >> 1] >> sh));
+        const uint32_t x1 = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(w2[dt >> 1] >> sh));
+        const uint32_t y1 = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(w3[dt >> 1] >> sh));
         const uint32_t a0 = __byte_perm(x0, y0, 0x5410), a1 = __byte_perm(x0, y0, 0x7632);
         const uint32_t a2 = __byte_perm(x1, y1, 0x5410), a3 = __byte_perm(x1, y1, 0x7632);
         mma_16816<PA_F16>(w.acc[dt], a0, a1, a2, a3, pb[kt][0], pb[kt][1]);
@@ -695,7 +695,7 @@ cudaError_t launch_shape(const AttnParams& p, int grid_z, const CUtensorMap* tk,
   if (d == D && bs == B)                                                   \
     return kShared ? launch_shared_t<QDT, KVDT, D, B>(p, grid_z, tk, tv, s) \
                    : launch_t<QDT, KVDT, D, B>(p, grid_z, tk, tv, s);
-  if constexpr (KVDT != PA_FP8_E4M3) {
+  if constexpr (!is_fp8<KVDT>()) {
     PA_SHAPE(128, 16)
     PA_SHAPE(128, 32)
     PA_SHAPE(64, 16)
@@ -717,6 +717,10 @@ cudaError_t dispatch(const AttnParams& p, int q_dtype, int kv_dtype, int grid_z,
     return launch_shape<PA_BF16, PA_FP8_E4M3, kShared>(p, grid_z, tk, tv, s);
   if (q_dtype == PA_F16 && kv_dtype == PA_FP8_E4M3)
     return launch_shape<PA_F16, PA_FP8_E4M3, kShared>(p, grid_z, tk, tv, s);
+  if (q_dtype == PA_BF16 && kv_dtype == PA_FP8_E5M2)
+    return launch_shape<PA_BF16, PA_FP8_E5M2, kShared>(p, grid_z, tk, tv, s);
+  if (q_dtype == PA_F16 && kv_dtype == PA_FP8_E5M2)
+    return launch_shape<PA_F16, PA_FP8_E5M2, kShared>(p, grid_z, tk, tv, s);
   return cudaErrorInvalidValue;
 }
 
@@ -727,7 +731,8 @@ bool decode_mma_supported(int q_dtype, int kv_dtype, int head_size, int block_si
   const bool q16 = q_dtype == PA_BF16 || q_dtype == PA_F16;
   if (!q16) return false;
   if (kv_dtype == q_dtype) return (head_size == 64 || head_size == 128) && (block_size == 16 || block_size == 32);
-  if (kv_dtype == PA_FP8_E4M3) return head_size == 128 && (block_size == 16 || block_size == 32);
+  if (kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_FP8_E5M2)
+    return head_size == 128 && (block_size == 16 || block_size == 32);
   return false;
 }
 

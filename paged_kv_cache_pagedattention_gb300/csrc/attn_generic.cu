@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(128)
   const int t0 = ri.origin + z * ri.part;  // partition z of the row's keys
   const int t1 = min(t0 + ri.part, ri.kv_len);
   float kscale = 1.f, vscale = 1.f;
-  if (KVDT == PA_FP8_E4M3) {
+  if (is_fp8<KVDT>()) {
     kscale = *p.k_scale;
     vscale = *p.v_scale;
   }
@@ -435,6 +435,9 @@ cudaError_t launch_attn_generic(const AttnParams& p, int q_dtype, int kv_dtype, 
   PA_GEN(PA_F16, PA_FP8_E4M3)
   PA_GEN(PA_BF16, PA_FP8_E4M3)
   PA_GEN(PA_F32, PA_FP8_E4M3)
+  PA_GEN(PA_F16, PA_FP8_E5M2)
+  PA_GEN(PA_BF16, PA_FP8_E5M2)
+  PA_GEN(PA_F32, PA_FP8_E5M2)
 #undef PA_GEN
   return cudaErrorInvalidValue;
 }

@@ -202,10 +202,10 @@ __device__ __forceinline__ uint32_t v_row_off(int key, int pc) {
 }
 
 template <int QDT, int KVDT, int HEAD, int BS>
-__global__ void __launch_bounds__(threads_tc<KVDT == PA_FP8_E4M3>(), 1)
+__global__ void __launch_bounds__(threads_tc<is_fp8<KVDT>()>(), 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv) {
-  constexpr bool kF8 = KVDT == PA_FP8_E4M3;
+  constexpr bool kF8 = is_fp8<KVDT>();
   constexpr int ODT = kF8 ? PA_F16 : QDT;  // MMA operand type (FP8 K/V are widened to f16)
   using G = TcGeom<HEAD, BS, kF8>;
   using QE = Elem<QDT>;
@@ -469,8 +469,8 @@ __global__ void __launch_bounds__(threads_tc<KVDT == PA_FP8_E4M3>(), 1)
         uint32_t h[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          h[2 * e] = e4m3x2_to_f16x2(static_cast<uint16_t>(cw[e] & 0xffffu));
-          h[2 * e + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(cw[e] >> 16));
+          h[2 * e] = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(cw[e] & 0xffffu));
+          h[2 * e + 1] = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(cw[e] >> 16));
         }
         const int pc = g >> 2, cc = (2 * g) & 7;
         uint8_t* row = tensor == 0 ? sk + pc * G::kPiece + key * 128
@@ -752,7 +752,7 @@ __global__ void __launch_bounds__(threads_tc<KVDT == PA_FP8_E4M3>(), 1)
 template <int QDT, int KVDT, int HEAD, int BS>
 cudaError_t launch_tc_t(const AttnParams& p, int num_items, const CUtensorMap* tk, const CUtensorMap* tv,
                         cudaStream_t stream) {
-  constexpr bool kF8 = KVDT == PA_FP8_E4M3;
+  constexpr bool kF8 = is_fp8<KVDT>();
   constexpr int smem = TcGeom<HEAD, BS, kF8>::kSmem;
   auto kern = prefill_tc_kernel<QDT, KVDT, HEAD, BS>;
   static int configured_device = -1;
@@ -778,7 +778,7 @@ cudaError_t launch_tc_shape(const AttnParams& p, int num_items, const CUtensorMa
   if (d == 128 && bs == 16) return launch_tc_t<QDT, KVDT, 128, 16>(p, num_items, tk, tv, s);
   if (d == 128 && bs == 32) return launch_tc_t<QDT, KVDT, 128, 32>(p, num_items, tk, tv, s);
   if (d == 128 && bs == 64) return launch_tc_t<QDT, KVDT, 128, 64>(p, num_items, tk, tv, s);
-  if constexpr (KVDT != PA_FP8_E4M3) {
+  if constexpr (!is_fp8<KVDT>()) {
     if (d == 64 && bs == 16) return launch_tc_t<QDT, KVDT, 64, 16>(p, num_items, tk, tv, s);
     if (d == 64 && bs == 32) return launch_tc_t<QDT, KVDT, 64, 32>(p, num_items, tk, tv, s);
     if (d == 64 && bs == 64) return launch_tc_t<QDT, KVDT, 64, 64>(p, num_items, tk, tv, s);
@@ -799,7 +799,7 @@ int prefill_tile_tokens(int group) {
 bool prefill_tc_supported(int q_dtype, int kv_dtype, int head_size, int block_size) {
   if (!(q_dtype == PA_BF16 || q_dtype == PA_F16)) return false;
   if (!(block_size == 16 || block_size == 32 || block_size == 64)) return false;
-  if (kv_dtype == PA_FP8_E4M3) return head_size == 128;  // one 128-byte row of codes
+  if (kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_FP8_E5M2) return head_size == 128;  // one 128-byte row of codes
   return kv_dtype == q_dtype && (head_size == 64 || head_size == 128);
 }
 
@@ -809,6 +809,11 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int q_dtype, int kv_dtype, in
   if (kv_dtype == PA_FP8_E4M3) {
     if (q_dtype == PA_BF16) return launch_tc_shape<PA_BF16, PA_FP8_E4M3>(p, num_items, tmap_k, tmap_v, stream);
     if (q_dtype == PA_F16) return launch_tc_shape<PA_F16, PA_FP8_E4M3>(p, num_items, tmap_k, tmap_v, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (kv_dtype == PA_FP8_E5M2) {
+    if (q_dtype == PA_BF16) return launch_tc_shape<PA_BF16, PA_FP8_E5M2>(p, num_items, tmap_k, tmap_v, stream);
+    if (q_dtype == PA_F16) return launch_tc_shape<PA_F16, PA_FP8_E5M2>(p, num_items, tmap_k, tmap_v, stream);
     return cudaErrorInvalidValue;
   }
   if (kv_dtype != q_dtype) return cudaErrorInvalidValue;

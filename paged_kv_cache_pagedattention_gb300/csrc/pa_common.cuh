@@ -48,6 +48,19 @@ struct Elem<PA_FP8_E4M3> {
     return __half2float(__half(h));
   }
 };
+template <>
+struct Elem<PA_FP8_E5M2> {
+  using T = uint8_t;
+  static constexpr int bytes = 1;
+  static __device__ __forceinline__ float load(const T* p) {
+    __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(*p), __NV_E5M2);
+    return __half2float(__half(h));
+  }
+};
+
+// FP8 cache formats (codes with a per-tensor scale).
+template <int DT>
+constexpr bool is_fp8() { return DT == PA_FP8_E4M3 || DT == PA_FP8_E5M2; }
 
 __device__ __forceinline__ void flag_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);
@@ -228,9 +241,12 @@ __device__ __forceinline__ float2 unpack2<PA_F16>(uint32_t v) {
   return __half22float2(h);
 }
 
-// Two e4m3 codes (low byte first) -> two f16 in one register, exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes), __NV_E4M3);
+// Two FP8 codes (low byte first) -> two f16 in one register, exact (every e4m3 and
+// every finite e5m2 value is an f16 value).
+template <int DT>
+__device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint16_t codes) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes),
+                                             DT == PA_FP8_E5M2 ? __NV_E5M2 : __NV_E4M3);
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 

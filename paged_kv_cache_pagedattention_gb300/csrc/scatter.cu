@@ -40,13 +40,16 @@ __global__ void __launch_bounds__(256) scatter_copy_kernel(const ScatterParams p
   }
 }
 
-// x / scale in IEEE fp32 (correctly rounded division), then e4m3 round-to-nearest-even
-// with saturation to the largest finite value, via the CUDA conversion intrinsic.
-__device__ __forceinline__ uint8_t quant_e4m3(float x, float scale) {
-  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3));
+// x / scale in IEEE fp32 (correctly rounded division), then FP8 (e4m3 or e5m2)
+// round-to-nearest-even with saturation to the largest finite value, via the CUDA
+// conversion intrinsic.
+template <int CDT>
+__device__ __forceinline__ uint8_t quant_fp8(float x, float scale) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE,
+                                                    CDT == PA_FP8_E5M2 ? __NV_E5M2 : __NV_E4M3));
 }
 
-template <int SRC>
+template <int SRC, int CDT>
 __global__ void __launch_bounds__(256) scatter_fp8_kernel(const ScatterParams p) {
   using SE = Elem<SRC>;
   const int pieces = p.head_size / 16;  // 16 codes per piece
@@ -76,8 +79,8 @@ __global__ void __launch_bounds__(256) scatter_fp8_kernel(const ScatterParams p)
       uint32_t kb = 0, vb = 0;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        kb |= static_cast<uint32_t>(quant_e4m3(SE::load(ksrc + 4 * w + b), ks)) << (8 * b);
-        vb |= static_cast<uint32_t>(quant_e4m3(SE::load(vsrc + 4 * w + b), vs)) << (8 * b);
+        kb |= static_cast<uint32_t>(quant_fp8<CDT>(SE::load(ksrc + 4 * w + b), ks)) << (8 * b);
+        vb |= static_cast<uint32_t>(quant_fp8<CDT>(SE::load(vsrc + 4 * w + b), vs)) << (8 * b);
       }
       kw[w] = kb;
       vw[w] = vb;
@@ -99,18 +102,23 @@ cudaError_t launch_reshape_and_cache(const ScatterParams& p, int src_dtype, int 
                                      cudaStream_t stream) {
   if (p.num_tokens == 0) return cudaSuccess;
   if (src_dtype == cache_dtype) {
-    const int eb = src_dtype == PA_F32 ? 4 : (src_dtype == PA_FP8_E4M3 ? 1 : 2);
+    const int eb = src_dtype == PA_F32 ? 4 : (src_dtype == PA_F16 || src_dtype == PA_BF16 ? 2 : 1);
     const long long units = (long long)p.num_tokens * p.num_kv_heads * (p.head_size * eb / 16);
     scatter_copy_kernel<<<scatter_grid(units), 256, 0, stream>>>(p, eb);
     return cudaGetLastError();
   }
-  if (cache_dtype != PA_FP8_E4M3) return cudaErrorInvalidValue;
+  if (cache_dtype != PA_FP8_E4M3 && cache_dtype != PA_FP8_E5M2) return cudaErrorInvalidValue;
   const long long units = (long long)p.num_tokens * p.num_kv_heads * (p.head_size / 16);
   const int g = scatter_grid(units);
-  if (src_dtype == PA_F32) scatter_fp8_kernel<PA_F32><<<g, 256, 0, stream>>>(p);
-  else if (src_dtype == PA_F16) scatter_fp8_kernel<PA_F16><<<g, 256, 0, stream>>>(p);
-  else if (src_dtype == PA_BF16) scatter_fp8_kernel<PA_BF16><<<g, 256, 0, stream>>>(p);
+  const bool e5 = cache_dtype == PA_FP8_E5M2;
+#define PA_Q(S) \
+  e5 ? (scatter_fp8_kernel<S, PA_FP8_E5M2><<<g, 256, 0, stream>>>(p), 0) \
+     : (scatter_fp8_kernel<S, PA_FP8_E4M3><<<g, 256, 0, stream>>>(p), 0)
+  if (src_dtype == PA_F32) PA_Q(PA_F32);
+  else if (src_dtype == PA_F16) PA_Q(PA_F16);
+  else if (src_dtype == PA_BF16) PA_Q(PA_BF16);
   else return cudaErrorInvalidValue;
+#undef PA_Q
   return cudaGetLastError();
 }
 

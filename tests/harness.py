@@ -16,7 +16,7 @@ TOL_FP8 = {"max": 5e-2, "mean": 1e-3}
 
 
 def tol_for(kv_dtype):
-    return TOL_FP8 if kv_dtype == "fp8_e4m3" else TOL
+    return TOL_FP8 if kv_dtype in workloads.FP8 else TOL
 
 
 class DeviceBatch:
@@ -33,7 +33,7 @@ class DeviceBatch:
         self.tables = torch.from_numpy(b.block_tables).to(dev)
         self.lens = torch.from_numpy(b.seq_lens).to(dev)
         self.qsl = torch.from_numpy(b.query_start_loc).to(dev)
-        fp8 = b.kv_dtype == "fp8_e4m3"
+        fp8 = b.kv_dtype in workloads.FP8
         self.k_scale = torch.tensor([b.k_scale], dtype=torch.float32, device=dev) if fp8 else None
         self.v_scale = torch.tensor([b.v_scale], dtype=torch.float32, device=dev) if fp8 else None
 

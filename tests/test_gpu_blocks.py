@@ -11,7 +11,7 @@ from harness import compare
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
-_BITS = {"bf16": np.uint16, "f16": np.uint16, "f32": np.uint32, "fp8_e4m3": np.uint8}
+_BITS = {"bf16": np.uint16, "f16": np.uint16, "f32": np.uint32, "fp8_e4m3": np.uint8, "fp8_e5m2": np.uint8}
 
 
 @pytest.fixture(scope="module")
@@ -29,7 +29,8 @@ def _pairs(rng, nb, n, extra=()):
 
 
 @pytest.mark.parametrize("dtype,shape", [("bf16", (64, 8, 16, 128)), ("fp8_e4m3", (48, 8, 32, 128)),
-                                         ("f32", (20, 2, 16, 64)), ("f16", (30, 3, 32, 64))])
+                                         ("f32", (20, 2, 16, 64)), ("f16", (30, 3, 32, 64)),
+                                         ("fp8_e5m2", (40, 8, 16, 128))])
 def test_copy_blocks_bit_exact(pa, dtype, shape):
     rng = np.random.default_rng(41)
     hi = np.iinfo(_BITS[dtype]).max
@@ -84,7 +85,7 @@ def test_copy_on_write_fork_on_device(pa, kv):
 
     kc = workloads.bits_to_torch(b.k_cache, kv, DEV)
     vc = workloads.bits_to_torch(b.v_cache, kv, DEV)
-    fp8 = kv == "fp8_e4m3"
+    fp8 = kv in workloads.FP8
     ks = torch.tensor([b.k_scale], dtype=torch.float32, device=DEV) if fp8 else None
     vs = torch.tensor([b.v_scale], dtype=torch.float32, device=DEV) if fp8 else None
     pa.pa_copy_blocks(kc, vc, torch.from_numpy(pairs).to(DEV))

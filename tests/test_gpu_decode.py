@@ -62,13 +62,16 @@ CASES = [
     ("fp8_g4_bs32", "fp8_e4m3", 32, 8, 128, 32, RAGGED, 64),
     ("fp8_g8_bs16", "fp8_e4m3", 16, 2, 128, 16, RAGGED, 0),
     ("fp8_f16q", "fp8_e4m3", 8, 2, 128, 32, RAGGED, 32),
+    ("fp8e5m2_g4_bs32", "fp8_e5m2", 32, 8, 128, 32, RAGGED, 64),
+    ("fp8e5m2_g8_bs16", "fp8_e5m2", 16, 2, 128, 16, RAGGED, 0),
+    ("fp8e5m2_f32q_generic", "fp8_e5m2", 8, 2, 128, 16, RAGGED, 48),
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_decode_parity(pa, case):
     name, kv, hq, hkv, d, bs, lens, part = case
-    q_dtype = "f16" if name == "fp8_f16q" else None
+    q_dtype = {"fp8_f16q": "f16", "fp8e5m2_f32q_generic": "f32"}.get(name)
     b = workloads.build(name, 100 + len(name), lens, [1] * len(lens), hq, hkv, d, bs, kv, q_dtype=q_dtype,
                         src_dtype=q_dtype)
     _full_parity(pa, b, part)
@@ -92,6 +95,27 @@ def test_fp8_scatter_matches_cuda_conversion(pa):
         pa.pa_reshape_and_cache(key, key, kc, vc, slots, sc, sc)
         got = kc[:, 0, 3, :].cpu().numpy().reshape(-1)
         ref = oracle.quantize_e4m3(x.astype(np.float64), scale)
+        assert np.array_equal(got, ref), f"scale {scale}: {np.count_nonzero(got != ref)} codes differ"
+
+
+def test_fp8_e5m2_scatter_matches_cuda_conversion(pa):
+    """e5m2 quantisation of ties, subnormals and out-of-range values: oracle == CUDA's conversion."""
+    mags = oracle.e5m2_table()[:124]
+    vals = np.concatenate([mags, (mags[:-1] + mags[1:]) / 2, [61440.0, 1e9, 60000.0, 2.0 ** -18, 3e-6]])
+    vals = np.concatenate([vals, -vals]).astype(np.float32)
+    n = -(-vals.size // 128) * 128
+    x = np.zeros(n, np.float32)
+    x[: vals.size] = vals
+    tokens = n // 128
+    for scale in (1.0, 0.37):
+        key = torch.from_numpy(x.reshape(tokens, 1, 128)).to(DEV)
+        kc = torch.zeros((tokens, 1, 16, 128), dtype=torch.float8_e5m2, device=DEV)
+        vc = torch.zeros_like(kc)
+        slots = torch.arange(tokens, dtype=torch.int64, device=DEV) * 16 + 3
+        sc = torch.tensor([scale], dtype=torch.float32, device=DEV)
+        pa.pa_reshape_and_cache(key, key, kc, vc, slots, sc, sc)
+        got = kc[:, 0, 3, :].view(torch.uint8).cpu().numpy().reshape(-1)
+        ref = oracle.quantize_e5m2(x.astype(np.float64), scale)
         assert np.array_equal(got, ref), f"scale {scale}: {np.count_nonzero(got != ref)} codes differ"
 
 

@@ -56,6 +56,7 @@ VARLEN_CASES = [
     ("fp8_prefill_split_default", "fp8_e4m3", 32, 8, 128, 16, [20000, 3000, 40], [300, 129, 1], 0, True),
     ("fp8_prefill_ragged_part48", "fp8_e4m3", 32, 8, 128, 16, [97, 33, 1000], [97, 31, 45], 48, True),
     ("fp8_prefill_noncausal_bs64", "fp8_e4m3", 16, 2, 128, 64, [250, 90], [60, 90], 64, False),
+    ("fp8e5m2_prefill_mixed", "fp8_e5m2", 32, 8, 128, 16, [2000, 33, 700, 1], [300, 1, 64, 1], 0, True),
 ]
 
 

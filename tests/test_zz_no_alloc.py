@@ -54,7 +54,7 @@ def _call_static(fn, pa, db, partition_size=0):
 
 
 def _check_close(a, b, kv_dtype):
-    tol = TOL_FP8 if kv_dtype == "fp8_e4m3" else TOL
+    tol = TOL_FP8 if kv_dtype in workloads.FP8 else TOL
     err = (a.double() - b.double()).abs()
     assert torch.isfinite(a.double()).all()
     assert err.max().item() <= tol["max"] and err.mean().item() <= tol["mean"], (err.max().item(), err.mean().item())

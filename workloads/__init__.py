@@ -33,8 +33,11 @@ from typing import Optional
 
 import numpy as np
 
-ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "fp8_e4m3": 1}
-BITS_NP = {"f32": np.uint32, "f16": np.uint16, "bf16": np.uint16, "fp8_e4m3": np.uint8}
+ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "fp8_e4m3": 1, "fp8_e5m2": 1}
+BITS_NP = {"f32": np.uint32, "f16": np.uint16, "bf16": np.uint16, "fp8_e4m3": np.uint8, "fp8_e5m2": np.uint8}
+FP8 = ("fp8_e4m3", "fp8_e5m2")
+# largest finite magnitude of each FP8 format: torch's casts do not saturate
+FP8_MAX = {"fp8_e4m3": 448.0, "fp8_e5m2": 57344.0}
 
 
 @dataclasses.dataclass
@@ -94,8 +97,8 @@ class PagedBatch:
 def normal_bits(rng: np.random.Generator, shape, dtype: str, scale: float = 1.0) -> np.ndarray:
     """N(0,1) fp32 values cast to ``dtype`` (torch casts), returned as raw bits.
 
-    For FP8 the value stored is x / scale cast by torch to float8_e4m3fn after
-    clamping to +-448 (torch's cast does not saturate).
+    For FP8 the value stored is x / scale cast by torch to float8_e4m3fn (e5m2)
+    after clamping to +-448 (+-57344): torch's casts do not saturate.
     """
     import torch
 
@@ -112,8 +115,9 @@ def _cast_bits(x, dtype: str, scale: float = 1.0) -> np.ndarray:
         return x.to(torch.float16).contiguous().view(torch.int16).numpy().view(np.uint16)
     if dtype == "bf16":
         return x.to(torch.bfloat16).contiguous().view(torch.int16).numpy().view(np.uint16)
-    if dtype == "fp8_e4m3":
-        y = (x.to(torch.float32) / scale).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    if dtype in FP8:
+        m = FP8_MAX[dtype]
+        y = (x.to(torch.float32) / scale).clamp(-m, m).to(torch_dtype(dtype))
         return y.contiguous().view(torch.uint8).numpy()
     raise ValueError(dtype)
 
@@ -122,11 +126,12 @@ def torch_dtype(dtype: str):
     import torch
 
     return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
-            "fp8_e4m3": torch.uint8}[dtype]
+            "fp8_e4m3": torch.float8_e4m3fn, "fp8_e5m2": torch.float8_e5m2}[dtype]
 
 
 def bits_to_torch(bits: np.ndarray, dtype: str, device=None):
-    """Raw bits -> torch tensor of the element type (FP8 stays uint8)."""
+    """Raw bits -> torch tensor of the element type (FP8 e4m3 as uint8 codes, e5m2 as
+    torch.float8_e5m2 so the format travels with the tensor)."""
     import torch
 
     t = torch.from_numpy(np.ascontiguousarray(bits))
@@ -136,6 +141,8 @@ def bits_to_torch(bits: np.ndarray, dtype: str, device=None):
         t = t.view(torch.int16).view(torch_dtype(dtype))
     elif dtype == "fp8_e4m3":
         t = t.view(torch.uint8)
+    elif dtype == "fp8_e5m2":
+        t = t.view(torch.uint8).view(torch.float8_e5m2)
     if device is not None:
         t = t.to(device)
     return t
@@ -204,7 +211,7 @@ def build(name, seed, seq_lens, q_lens, num_q_heads, num_kv_heads, head_size,
     rng = np.random.Generator(np.random.PCG64(seed))
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     q_lens = np.asarray(q_lens, dtype=np.int32)
-    q_dtype = q_dtype or ("bf16" if kv_dtype == "fp8_e4m3" else kv_dtype)
+    q_dtype = q_dtype or ("bf16" if kv_dtype in FP8 else kv_dtype)
     src_dtype = src_dtype or q_dtype
     if scale is None:
         scale = 1.0 / float(np.sqrt(head_size))
@@ -216,7 +223,7 @@ def build(name, seed, seq_lens, q_lens, num_q_heads, num_kv_heads, head_size,
     q = normal_bits(rng, (tq, num_q_heads, head_size), q_dtype)
     key = normal_bits(rng, (tq, num_kv_heads, head_size), src_dtype)
     value = normal_bits(rng, (tq, num_kv_heads, head_size), src_dtype)
-    is_fp8 = kv_dtype == "fp8_e4m3"
+    is_fp8 = kv_dtype in FP8
     ks = vs = fp8_scale if is_fp8 else 1.0
     k_cache = v_cache = None
     cache_seed = int(rng.integers(0, 2**31 - 1))
@@ -310,16 +317,22 @@ def mixed_fp8(seed: int = 3, host_cache: bool = False, scale_lengths: float = 1.
 
 
 def fp8(seed: int = 4, host_cache: bool = False, batch: int = 256,
-        scale_lengths: float = 1.0) -> PagedBatch:
+        scale_lengths: float = 1.0, kv_dtype: str = "fp8_e4m3") -> PagedBatch:
     rng = np.random.Generator(np.random.PCG64(seed + 4000))
     lens = rng.integers(1024, 32768, size=batch, endpoint=True)
     if scale_lengths != 1.0:
         lens = np.maximum(np.round(lens * scale_lengths).astype(np.int64), 1)
-    return build("fp8_kv_decode", seed, lens, [1] * batch, 32, 8, 128, 32, "fp8_e4m3",
+    name = "fp8_kv_decode" if kv_dtype == "fp8_e4m3" else "fp8_e5m2_kv_decode"
+    return build(name, seed, lens, [1] * batch, 32, 8, 128, 32, kv_dtype,
                  q_dtype="bf16", src_dtype="bf16", host_cache=host_cache)
 
 
-NAMED = {"tiny": tiny, "llama": llama, "agentic": agentic, "mixed": mixed, "fp8": fp8, "mixed_fp8": mixed_fp8}
+def fp8_e5m2(seed: int = 4, host_cache: bool = False, scale_lengths: float = 1.0) -> PagedBatch:
+    """The FP8 decode workload with an e5m2 cache."""
+    return fp8(seed, host_cache, scale_lengths=scale_lengths, kv_dtype="fp8_e5m2")
+
+
+NAMED = {"tiny": tiny, "llama": llama, "agentic": agentic, "mixed": mixed, "fp8": fp8, "mixed_fp8": mixed_fp8, "fp8_e5m2": fp8_e5m2}
 
 
 # --------------------------------------------------------------------------
@@ -340,7 +353,9 @@ def device_cache(batch: PagedBatch, device, chunk_elems: int = 1 << 28):
     if batch.k_cache is not None:
         return (bits_to_torch(batch.k_cache, batch.kv_dtype, device),
                 bits_to_torch(batch.v_cache, batch.kv_dtype, device))
-    tdt = torch_dtype(batch.kv_dtype)
+    tdt = torch_dtype(batch.kv_dtype) if batch.kv_dtype != "fp8_e4m3" else torch.uint8
+    if batch.kv_dtype == "fp8_e5m2":
+        tdt = torch.float8_e5m2
     gen = torch.Generator(device=device)
     gen.manual_seed(batch.cache_seed)
     caches = []
@@ -352,6 +367,8 @@ def device_cache(batch: PagedBatch, device, chunk_elems: int = 1 << 28):
             x = torch.randn(hi - lo, generator=gen, device=device, dtype=torch.float32)
             if batch.kv_dtype == "fp8_e4m3":
                 flat[lo:hi] = (x / sc).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+            elif batch.kv_dtype == "fp8_e5m2":
+                flat[lo:hi] = (x / sc).clamp_(-57344.0, 57344.0).to(torch.float8_e5m2)
             else:
                 flat[lo:hi] = x.to(tdt)
             del x
