@@ -179,21 +179,28 @@ def e5m2_encode(x) -> np.ndarray:
     return _fp8_encode(x, _E5M2_POS, E5M2_MAX)
 
 
-def quantize_e4m3(x64, scale: float) -> np.ndarray:
-    """FP8 code stored for a value ``x`` with a per-tensor fp32 scale.
+def _scale64(scale) -> np.ndarray:
+    """An fp32 scale (a scalar, or one per KV head: shape [Hkv] becomes [Hkv][1] so it
+    broadcasts over [..][Hkv][d] element arrays) as float64."""
+    s = np.asarray(scale, dtype=np.float32).astype(np.float64)
+    return s.reshape(-1, 1) if s.ndim == 1 else s
+
+
+def quantize_e4m3(x64, scale) -> np.ndarray:
+    """FP8 code stored for a value ``x`` with an fp32 scale (per tensor, or per KV head).
 
     The stored code is the e4m3 rounding of the fp32 quotient x / scale.  The
     quotient is formed in float64 and rounded once to float32; since float64
     has more than 2*24+2 significand bits this equals the correctly rounded
     float32 quotient.  The float32 is then rounded to e4m3 (``e4m3_encode``).
     """
-    q32 = (np.asarray(x64, dtype=np.float64) / np.float64(np.float32(scale))).astype(np.float32)
+    q32 = (np.asarray(x64, dtype=np.float64) / _scale64(scale)).astype(np.float32)
     return e4m3_encode(q32.astype(np.float64))
 
 
-def quantize_e5m2(x64, scale: float) -> np.ndarray:
+def quantize_e5m2(x64, scale) -> np.ndarray:
     """As ``quantize_e4m3`` for the e5m2 format: e5m2 rounding of the fp32 quotient."""
-    q32 = (np.asarray(x64, dtype=np.float64) / np.float64(np.float32(scale))).astype(np.float32)
+    q32 = (np.asarray(x64, dtype=np.float64) / _scale64(scale)).astype(np.float32)
     return e5m2_encode(q32.astype(np.float64))
 
 
@@ -201,8 +208,8 @@ def decode_bits(bits, dtype: str, scale: float = 1.0) -> np.ndarray:
     """Exact float64 value of stored elements given as raw bits.
 
     fp32 / fp16 widen exactly; bf16 is the upper half of an fp32 and widens
-    exactly; FP8 e4m3 is looked up from its bit fields and multiplied by the
-    per-tensor scale in float64.
+    exactly; FP8 e4m3 / e5m2 is looked up from its bit fields and multiplied by
+    the scale in float64 (per tensor, or per KV head for [..][Hkv][d] arrays).
     """
     b = np.asarray(bits)
     if dtype == "f32":
@@ -212,9 +219,9 @@ def decode_bits(bits, dtype: str, scale: float = 1.0) -> np.ndarray:
     if dtype == "bf16":
         return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
     if dtype == "fp8_e4m3":
-        return _E4M3[b.astype(np.uint8)] * np.float64(np.float32(scale))
+        return _E4M3[b.astype(np.uint8)] * _scale64(scale)
     if dtype == "fp8_e5m2":
-        return _E5M2[b.astype(np.uint8)] * np.float64(np.float32(scale))
+        return _E5M2[b.astype(np.uint8)] * _scale64(scale)
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
@@ -224,7 +231,7 @@ def decode_bits(bits, dtype: str, scale: float = 1.0) -> np.ndarray:
 
 def reshape_and_cache(key_bits, value_bits, k_cache, v_cache, slot_mapping,
                       block_size: int, src_dtype: str, cache_dtype: str,
-                      k_scale: float = 1.0, v_scale: float = 1.0) -> None:
+                      k_scale=1.0, v_scale=1.0) -> None:
     """Write each new token's K and V into its slot of the paged cache, in place.
 
     [NOTES] "Prefill 与 Decode": prefill stores K/V for every prompt token and
@@ -232,7 +239,9 @@ def reshape_and_cache(key_bits, value_bits, k_cache, v_cache, slot_mapping,
     input preparation builds ``slot_mapping``, one flat slot per new token.
     Slot s lands in block s // block_size, offset s % block_size; a negative
     slot is padding and is skipped.  With the same element type the bits are
-    copied; with an FP8 cache each value is quantised with ``quantize_e4m3``.
+    copied; with an FP8 cache each value is quantised (``quantize_e4m3`` /
+    ``quantize_e5m2``) with the tensor's scale, or its KV head's when the scales
+    are given one per head.
     """
     key_bits = np.asarray(key_bits)
     value_bits = np.asarray(value_bits)

@@ -148,6 +148,28 @@ def test_quantize_with_non_power_of_two_scale_vs_torch():
     assert np.array_equal(ours[keep], ref[keep])
 
 
+@pytest.mark.parametrize("kv", ["fp8_e4m3", "fp8_e5m2"])
+def test_per_head_scales(kv):
+    """One scale per KV head: equal scales reproduce the per-tensor result, and each
+    head of a per-head run equals a one-head run with that head's scale."""
+    b = workloads.build("phs", 35, [300, 37, 129], [1, 1, 1], 8, 4, 128, 16, "bf16")
+    x64 = oracle.decode_bits(b.k_cache, "bf16")                         # [nb][Hkv][bs][d]
+    x64 = x64.transpose(0, 2, 1, 3)                                     # [nb][bs][Hkv][d]
+    quant = oracle.quantize_e4m3 if kv == "fp8_e4m3" else oracle.quantize_e5m2
+    scales = np.array([2.0 ** -6, 0.011, 2.0 ** -3, 0.37], np.float32)
+    kc = quant(x64, scales).transpose(0, 2, 1, 3).copy()
+    vc = quant(-x64, scales[::-1].copy()).transpose(0, 2, 1, 3).copy()
+    same = quant(x64, np.full(4, scales[0], np.float32)).transpose(0, 2, 1, 3)
+    assert np.array_equal(same, quant(x64, scales[0]).transpose(0, 2, 1, 3))
+    out = oracle.paged_decode(b.q, "bf16", kc, vc, kv, b.block_tables, b.seq_lens, 16, b.scale,
+                              scales, scales[::-1].copy())
+    for h in range(4):
+        one = oracle.paged_decode(b.q[:, 2 * h: 2 * h + 2], "bf16", kc[:, h: h + 1], vc[:, h: h + 1], kv,
+                                  b.block_tables, b.seq_lens, 16, b.scale, float(scales[h]),
+                                  float(scales[::-1][h]))
+        assert np.array_equal(out[:, 2 * h: 2 * h + 2], one)
+
+
 def test_decode_bits_vs_torch_casts():
     rng = np.random.default_rng(1)
     x = torch.from_numpy(rng.standard_normal(1000).astype(np.float32) * 100)
