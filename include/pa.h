@@ -56,9 +56,10 @@
  *   attends keys 0..position ([ARCH] Part 1: flattened batch, positions + mask).
  * Numerics.  Scores and the softmax run in fp32 with a running max and sum
  *   ([AGENTIC] "Online softmax"); the output is rounded once to q_dtype.
- *   FP8 e4m3 caches carry one fp32 scale per tensor (k_scale, v_scale, device
- *   pointers to one float each): stored code = e4m3(x / scale), rounded to
- *   nearest even with saturation to +-448; value = e4m3 decode x scale.
+ *   FP8 caches carry fp32 scales (k_scale, v_scale: device pointers to one float
+ *   each, or to num_kv_heads floats with the *_PER_HEAD formats, KV head h using
+ *   [h]): stored code = fp8(x / scale), rounded to nearest even with saturation to
+ *   +-448 (e4m3) or +-57344 (e5m2); value = fp8 decode x scale.
  * Errors.  Argument checks that need no device data return synchronously with
  *   a status and launch nothing.  Inputs that live on the device (block-table
  *   entries, slots, sequence lengths, query offsets) are checked by the kernels:
@@ -93,7 +94,9 @@ typedef enum pa_dtype {
   PA_F16 = 1,
   PA_BF16 = 2,
   PA_FP8_E4M3 = 3, /* cache only: stored as uint8 codes with a per-tensor fp32 scale */
-  PA_FP8_E5M2 = 4  /* cache only: as PA_FP8_E4M3, 5 exponent and 2 mantissa bits */
+  PA_FP8_E5M2 = 4, /* cache only: as PA_FP8_E4M3, 5 exponent and 2 mantissa bits */
+  PA_FP8_E4M3_PER_HEAD = 5, /* as PA_FP8_E4M3 with one scale per KV head: k_scale and */
+  PA_FP8_E5M2_PER_HEAD = 6  /* v_scale point to num_kv_heads floats (head h: [h]) */
 } pa_dtype;
 
 /* Bits of the device error word (pa_get_error_flags). */

@@ -30,7 +30,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_BOUNDS, \
     PA_ERR_TIMEOUT, PA_ERR_CUDA = range(7)
-PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3, PA_FP8_E5M2 = range(5)
+PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3, PA_FP8_E5M2, PA_FP8_E4M3_PER_HEAD, PA_FP8_E5M2_PER_HEAD = range(7)
 PA_ERRFLAG_BLOCK_TABLE, PA_ERRFLAG_SLOT, PA_ERRFLAG_SEQ_LEN, PA_ERRFLAG_QUERY, PA_ERRFLAG_TIMEOUT = \
     0x1, 0x2, 0x4, 0x8, 0x10
 
@@ -98,6 +98,17 @@ def dtype_code(t: torch.Tensor) -> int:
         raise TypeError(f"unsupported tensor dtype {t.dtype}") from None
 
 
+def kv_code(cache: torch.Tensor, k_scale=None) -> int:
+    """Cache dtype code; FP8 scales holding more than one value (one per KV head,
+    cache [num_blocks][num_kv_heads][block_size][head_size]) select the per-head format."""
+    code = dtype_code(cache)
+    if code in (PA_FP8_E4M3, PA_FP8_E5M2) and k_scale is not None and k_scale.numel() > 1:
+        if k_scale.numel() != cache.shape[1]:
+            raise ValueError("FP8 scales: one per tensor or one per KV head")
+        return PA_FP8_E4M3_PER_HEAD if code == PA_FP8_E4M3 else PA_FP8_E5M2_PER_HEAD
+    return code
+
+
 def _ptr(t) -> int | None:
     if t is None:
         return None
@@ -133,7 +144,7 @@ def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, k_scale=Non
         raise ValueError("slot_mapping must be int64 [num_tokens]")
     _check(_lib.pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
                                      _ptr(slot_mapping), key.shape[0], nb, hkv, d, bs,
-                                     dtype_code(key), dtype_code(k_cache), _ptr(k_scale), _ptr(v_scale),
+                                     dtype_code(key), kv_code(k_cache, k_scale), _ptr(k_scale), _ptr(v_scale),
                                      _stream(stream)), "pa_reshape_and_cache")
 
 
@@ -175,7 +186,7 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, sca
         raise ValueError("seq_lens must be int32 [num_seqs]")
     _check(_lib.pa_decode_windowed(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables),
                                    block_tables.shape[1], _ptr(seq_lens), b, int(max_seq_len), hq, hkv, d, bs,
-                                   float(scale), int(window), dtype_code(q), dtype_code(k_cache), _ptr(k_scale),
+                                   float(scale), int(window), dtype_code(q), kv_code(k_cache, k_scale), _ptr(k_scale),
                                    _ptr(v_scale), int(partition_size), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream)), "pa_decode")
 
@@ -203,7 +214,7 @@ def pa_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, seq_lens, ma
         raise ValueError("group_start int32 [G+1], group_shared_blocks int32 [G]")
     _check(_lib.pa_decode_shared_prefix(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables),
                                         block_tables.shape[1], _ptr(seq_lens), b, int(max_seq_len), hq, hkv, d,
-                                        bs, float(scale), dtype_code(q), dtype_code(k_cache), _ptr(k_scale),
+                                        bs, float(scale), dtype_code(q), kv_code(k_cache, k_scale), _ptr(k_scale),
                                         _ptr(v_scale), _ptr(group_start), _ptr(group_shared_blocks),
                                         group_shared_blocks.numel(), int(max_group_size), int(partition_size),
                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -225,7 +236,7 @@ def pa_decode_static_workspace(out, q, k_cache, v_cache, block_tables, seq_lens,
     _check(_lib.pa_decode_static_workspace(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), nb,
                                            _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), b,
                                            int(max_seq_len), hq, hkv, d, bs, float(scale), dtype_code(q),
-                                           dtype_code(k_cache), _ptr(k_scale), _ptr(v_scale),
+                                           kv_code(k_cache, k_scale), _ptr(k_scale), _ptr(v_scale),
                                            int(partition_size), _stream(stream)),
            "pa_decode_static_workspace")
 
@@ -253,7 +264,7 @@ def pa_varlen_attn(out, q, k_cache, v_cache, block_tables, query_start_loc, seq_
     _check(_lib.pa_varlen_attn_windowed(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables),
                                block_tables.shape[1], _ptr(query_start_loc), _ptr(seq_lens), b, t,
                                int(max_query_len), int(max_seq_len), hq, hkv, d, bs, float(scale), int(window),
-                               1 if causal else 0, dtype_code(q), dtype_code(k_cache), _ptr(k_scale),
+                               1 if causal else 0, dtype_code(q), kv_code(k_cache, k_scale), _ptr(k_scale),
                                _ptr(v_scale), int(partition_size), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream)),
            "pa_varlen_attn")

@@ -62,9 +62,20 @@ int dtype_bytes(int dt) {
     case PA_BF16: return 2;
     case PA_FP8_E4M3: return 1;
     case PA_FP8_E5M2: return 1;
+    case PA_FP8_E4M3_PER_HEAD: return 1;
+    case PA_FP8_E5M2_PER_HEAD: return 1;
     default: return 0;
   }
 }
+
+// FP8 formats with one scale per KV head are the base format with a scale stride
+// of 1 (the kernels read the scale of KV head h at scale[h * stride]).
+pa_dtype base_dtype(pa_dtype dt) {
+  if (dt == PA_FP8_E4M3_PER_HEAD) return PA_FP8_E4M3;
+  if (dt == PA_FP8_E5M2_PER_HEAD) return PA_FP8_E5M2;
+  return dt;
+}
+int scale_stride_of(pa_dtype dt) { return dt == PA_FP8_E4M3_PER_HEAD || dt == PA_FP8_E5M2_PER_HEAD ? 1 : 0; }
 
 // ------------------------------------------------------------------ partitions
 
@@ -387,6 +398,8 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
                                int32_t num_kv_heads, int32_t head_size, int32_t block_size,
                                pa_dtype src_dtype, pa_dtype cache_dtype, const float* k_scale,
                                const float* v_scale, pa_stream_t stream) {
+  const int scale_stride = scale_stride_of(cache_dtype);
+  cache_dtype = base_dtype(cache_dtype);
   if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_size < 1 || block_size < 1)
     return PA_ERR_INVALID_ARG;
   if (num_tokens == 0) return PA_OK;
@@ -400,6 +413,7 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
   if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
     return PA_ERR_INVALID_ARG;
   pa::ScatterParams p;
+  p.scale_stride = scale_stride;
   p.key = key;
   p.value = value;
   p.k_cache = k_cache;
@@ -474,6 +488,8 @@ pa_status pa_decode_windowed(void* out, const void* q, const void* k_cache, cons
                              int32_t head_size, int32_t block_size, float scale, int32_t window,
                              pa_dtype q_dtype, pa_dtype kv_dtype, const float* k_scale, const float* v_scale,
                              int32_t partition_size, void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  const int scale_stride = scale_stride_of(kv_dtype);
+  kv_dtype = base_dtype(kv_dtype);
   if (num_seqs < 0 || window < 0) return PA_ERR_INVALID_ARG;
   if (num_seqs == 0) return PA_OK;
   pa_status st = check_attention_args(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
@@ -487,6 +503,7 @@ pa_status pa_decode_windowed(void* out, const void* q, const void* k_cache, cons
   AttnParams p = base_params(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                              num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, scale,
                              k_scale, v_scale);
+  p.scale_stride = scale_stride;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.num_rows = num_seqs;
   p.max_query_len = 1;
@@ -536,6 +553,8 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
                                   const int32_t* group_shared_blocks, int32_t num_groups,
                                   int32_t max_group_size, int32_t partition_size, void* workspace,
                                   size_t workspace_bytes, pa_stream_t stream) {
+  const int scale_stride = scale_stride_of(kv_dtype);
+  kv_dtype = base_dtype(kv_dtype);
   if (num_seqs < 0 || num_groups < 0) return PA_ERR_INVALID_ARG;
   if (num_seqs == 0) return PA_OK;
   pa_status st = check_attention_args(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
@@ -557,6 +576,7 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
   AttnParams p = base_params(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                              num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, scale,
                              k_scale, v_scale);
+  p.scale_stride = scale_stride;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.num_rows = num_seqs;
   p.max_query_len = 1;
@@ -637,6 +657,8 @@ pa_status pa_varlen_attn_windowed(void* out, const void* q, const void* k_cache,
                                   float scale, int32_t window, int32_t causal, pa_dtype q_dtype, pa_dtype kv_dtype,
                                   const float* k_scale, const float* v_scale, int32_t partition_size,
                                   void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  const int scale_stride = scale_stride_of(kv_dtype);
+  kv_dtype = base_dtype(kv_dtype);
   if (num_seqs < 0 || total_q_tokens < 0 || window < 0) return PA_ERR_INVALID_ARG;
   if (window > 0 && !causal) return PA_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q_tokens == 0) return PA_OK;
@@ -653,6 +675,7 @@ pa_status pa_varlen_attn_windowed(void* out, const void* q, const void* k_cache,
   AttnParams p = base_params(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                              num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, scale,
                              k_scale, v_scale);
+  p.scale_stride = scale_stride;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.query_start_loc = query_start_loc;
   p.num_rows = total_q_tokens;

@@ -121,7 +121,7 @@ __device__ __forceinline__ void load_query(const AttnParams& p, long long row, i
       qb[ks][0] = pack2<PA_F16>(ldexpf(qv[ks][0], sh), ldexpf(qv[ks][1], sh));
       qb[ks][1] = pack2<PA_F16>(ldexpf(qv[ks][2], sh), ldexpf(qv[ks][3], sh));
     }
-    const float my_c = ldexpf(base_c * (*p.k_scale), -sh);
+    const float my_c = ldexpf(base_c * p.k_scale[(h0 / p.group) * p.scale_stride], -sh);
     cA = __shfl_sync(0xffffffffu, my_c, 8 * qq);      // head 2qq lives in lanes 8qq..8qq+3
     cB = __shfl_sync(0xffffffffu, my_c, 8 * qq + 4);  // head 2qq+1
   }
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(NW * 32)
     }
   }
   __syncthreads();
-  const float vscale = kFp8 ? *p.v_scale : 1.f;
+  const float vscale = kFp8 ? p.v_scale[kvh * p.scale_stride] : 1.f;
   const long long pbase = p.part_off ? (long long)p.part_off[r] : (long long)row * p.max_partitions;
   const bool direct = nparts == 1 && !p.force_partials;
   for (int idx = threadIdx.x; idx < nh * HEAD; idx += NW * 32) {
@@ -619,7 +619,7 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32)
   // ---- this member's partial state for partition z of its shared prefix
   w.lA = warp_sum_xor(w.lA, 4, 16);
   w.lB = warp_sum_xor(w.lB, 4, 16);
-  const float vscale = kFp8 ? *p.v_scale : 1.f;
+  const float vscale = kFp8 ? p.v_scale[kvh * p.scale_stride] : 1.f;
   const long long pi = (long long)seq * p.max_partitions + z;
   const int qq = lane & 3;
   const int hA = 2 * qq, hB = 2 * qq + 1;

@@ -45,8 +45,8 @@ __global__ void __launch_bounds__(128)
   const int t1 = min(t0 + ri.part, ri.kv_len);
   float kscale = 1.f, vscale = 1.f;
   if (is_fp8<KVDT>()) {
-    kscale = *p.k_scale;
-    vscale = *p.v_scale;
+    kscale = p.k_scale[kvh * p.scale_stride];
+    vscale = p.v_scale[kvh * p.scale_stride];
   }
   const float c = p.scale * kscale * kLog2e;
 

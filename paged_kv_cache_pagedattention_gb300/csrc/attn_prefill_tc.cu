@@ -574,8 +574,8 @@ __global__ void __launch_bounds__(threads_tc<is_fp8<KVDT>()>(), 1)
     uint64_t* my_p_full = p_full + t * kSBufs;
     uint64_t* my_o_done = o_done + t * kSBufs;
     // score multiplier in log2 units; FP8: the K scale and the row's f16 shift too
-    const float c = kF8 ? ldexpf(p.scale * kLog2e * (*p.k_scale), -q_shift) : p.scale * kLog2e;
-    const float out_scale = kF8 ? *p.v_scale : 1.f;
+    const float c = kF8 ? ldexpf(p.scale * kLog2e * p.k_scale[kvh * p.scale_stride], -q_shift) : p.scale * kLog2e;
+    const float out_scale = kF8 ? p.v_scale[kvh * p.scale_stride] : 1.f;
     const int row_limit = p.causal ? min(k1, row_pos + 1) : k1;  // this row attends keys < row_limit
     const int row_lo = p.window > 0 ? max(0, row_pos - p.window + 1) : 0;  // ... and keys >= row_lo
     float m = -INFINITY, l = 0.f;

@@ -30,8 +30,9 @@ struct AttnParams {
   const int32_t* group_shared_blocks;  // shared-prefix decode: [num_groups] leading blocks shared in a group
   float* ws_acc;                   // [partial rows][Hq][d]  un-normalised weighted sums
   float2* ws_ml;                   // [partial rows][Hq]     (running max in log2 units, weight sum)
-  const float* k_scale;            // FP8 only
+  const float* k_scale;            // FP8 only: scale of KV head h at k_scale[h * scale_stride]
   const float* v_scale;
+  int scale_stride;                // 0: one scale per tensor, 1: one per KV head
   unsigned* err;                   // device error word
   int num_seqs;
   int num_rows;
@@ -63,8 +64,9 @@ struct ScatterParams {
   void* k_cache;
   void* v_cache;
   const int64_t* slot_mapping;
-  const float* k_scale;
+  const float* k_scale;  // FP8 only: scale of KV head h at k_scale[h * scale_stride]
   const float* v_scale;
+  int scale_stride;
   unsigned* err;
   int num_tokens;
   int num_blocks;

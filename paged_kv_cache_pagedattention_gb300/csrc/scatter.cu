@@ -56,7 +56,6 @@ __global__ void __launch_bounds__(256) scatter_fp8_kernel(const ScatterParams p)
   const long long per_token = (long long)p.num_kv_heads * pieces;
   const long long total = (long long)p.num_tokens * per_token;
   const long long limit = (long long)p.num_blocks * p.block_size;
-  const float ks = *p.k_scale, vs = *p.v_scale;
   for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < total;
        u += (long long)gridDim.x * blockDim.x) {
     const long long t = u / per_token;
@@ -68,6 +67,7 @@ __global__ void __launch_bounds__(256) scatter_fp8_kernel(const ScatterParams p)
       flag_error(p.err, PA_ERRFLAG_SLOT);
       continue;
     }
+    const float ks = p.k_scale[h * p.scale_stride], vs = p.v_scale[h * p.scale_stride];
     const long long blk = slot / p.block_size, off = slot % p.block_size;
     const long long src = ((t * p.num_kv_heads + h) * p.head_size) + c * 16;
     const long long dst = ((blk * p.num_kv_heads + h) * p.block_size + off) * p.head_size + c * 16;

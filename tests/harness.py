@@ -34,8 +34,9 @@ class DeviceBatch:
         self.lens = torch.from_numpy(b.seq_lens).to(dev)
         self.qsl = torch.from_numpy(b.query_start_loc).to(dev)
         fp8 = b.kv_dtype in workloads.FP8
-        self.k_scale = torch.tensor([b.k_scale], dtype=torch.float32, device=dev) if fp8 else None
-        self.v_scale = torch.tensor([b.v_scale], dtype=torch.float32, device=dev) if fp8 else None
+        # one scale per tensor, or one per KV head
+        self.k_scale = torch.tensor(np.atleast_1d(b.k_scale), dtype=torch.float32, device=dev) if fp8 else None
+        self.v_scale = torch.tensor(np.atleast_1d(b.v_scale), dtype=torch.float32, device=dev) if fp8 else None
 
 
 def run_scatter(pa, db: DeviceBatch):

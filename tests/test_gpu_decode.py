@@ -237,3 +237,15 @@ def test_agentic_full_size_sampled(pa):
 def test_fp8_full_size_sampled(pa):
     b = workloads.fp8()
     _sampled_full_size(pa, b, [0, 100, 255])
+
+
+PER_HEAD = [0.011, 2.0 ** -6, 0.3, 2.0 ** -2, 0.05, 1.0, 2.0 ** -9, 0.0071]
+
+
+@pytest.mark.parametrize("kv,q_dtype", [("fp8_e4m3", None), ("fp8_e5m2", None), ("fp8_e4m3", "f32")])
+def test_per_head_fp8_scales(pa, kv, q_dtype):
+    """One scale per KV head (scatter codes and decode) on the tensor-core and generic paths."""
+    b = workloads.build("phs_" + kv, 131, RAGGED, [1] * len(RAGGED), 32, 8, 128, 32, kv, q_dtype=q_dtype,
+                        src_dtype=q_dtype, fp8_scale=PER_HEAD)
+    assert np.ndim(b.k_scale) == 1
+    _full_parity(pa, b, 64)

@@ -64,13 +64,14 @@ def test_agentic_families_scaled_down(pa, part):
     assert (out.double() - plain.double()).abs().max().item() < 1e-2
 
 
-@pytest.mark.parametrize("kv", ["fp8_e4m3", "fp8_e5m2"])
-def test_fp8_groups_and_clamped_share(pa, kv):
+@pytest.mark.parametrize("kv,per_head", [("fp8_e4m3", False), ("fp8_e5m2", False), ("fp8_e4m3", True)])
+def test_fp8_groups_and_clamped_share(pa, kv, per_head):
     # two groups of 3 declaring 5 shared blocks and one singleton; the last member of
     # group 1 holds only 3 full blocks, so that group's shared length is clamped to 3
     lens = [300, 300, 300, 200, 210, 100, 77]
     shared_map = {1: (0, 5), 2: (0, 5), 4: (3, 5), 5: (3, 3)}
-    b = workloads.build("fp8grp", 21, lens, [1] * 7, 32, 8, 128, 32, kv, shared=shared_map)
+    scales = [0.011, 2.0 ** -6, 0.3, 2.0 ** -2, 0.05, 1.0, 2.0 ** -9, 0.0071] if per_head else 2.0 ** -6
+    b = workloads.build("fp8grp", 21, lens, [1] * 7, 32, 8, 128, 32, kv, shared=shared_map, fp8_scale=scales)
     starts = np.array([0, 3, 6, 7], np.int32)
     shared = np.array([5, 5, 0], np.int32)
     _parity(pa, b, starts, shared, 64)

@@ -120,3 +120,11 @@ def test_mixed_full_size_sampled(pa):
     ref = oracle.paged_varlen(b.q, b.q_dtype, k, v, b.kv_dtype, tables, b.query_start_loc, b.seq_lens,
                               b.block_size, b.scale, True, rows=rows)
     compare(outs[0], ref, b.kv_dtype, rows=sorted(set(rows)), where="mixed full size")
+
+
+@pytest.mark.parametrize("kv", ["fp8_e4m3", "fp8_e5m2"])
+def test_fp8_prefill_per_head_scales(pa, kv):
+    scales = [0.011, 2.0 ** -6, 0.3, 2.0 ** -2, 0.05, 1.0, 2.0 ** -9, 0.0071]
+    b = workloads.build("phs_pf_" + kv, 72, [700, 37, 300, 1], [64, 1, 300, 1], 32, 8, 128, 16, kv,
+                        fp8_scale=scales)
+    _varlen_parity(pa, b, 0, True)

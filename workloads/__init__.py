@@ -117,7 +117,10 @@ def _cast_bits(x, dtype: str, scale: float = 1.0) -> np.ndarray:
         return x.to(torch.bfloat16).contiguous().view(torch.int16).numpy().view(np.uint16)
     if dtype in FP8:
         m = FP8_MAX[dtype]
-        y = (x.to(torch.float32) / scale).clamp(-m, m).to(torch_dtype(dtype))
+        sc = torch.as_tensor(np.asarray(scale, dtype=np.float32))
+        if sc.dim() == 1:  # one scale per KV head of a [blocks][heads][slots][dim] cache
+            sc = sc.view(1, -1, 1, 1)
+        y = (x.to(torch.float32) / sc).clamp(-m, m).to(torch_dtype(dtype))
         return y.contiguous().view(torch.uint8).numpy()
     raise ValueError(dtype)
 
@@ -225,6 +228,10 @@ def build(name, seed, seq_lens, q_lens, num_q_heads, num_kv_heads, head_size,
     value = normal_bits(rng, (tq, num_kv_heads, head_size), src_dtype)
     is_fp8 = kv_dtype in FP8
     ks = vs = fp8_scale if is_fp8 else 1.0
+    if is_fp8 and np.ndim(fp8_scale):  # one scale per KV head
+        ks = np.asarray(fp8_scale, dtype=np.float32)
+        vs = ks[::-1].copy()
+        assert ks.shape == (num_kv_heads,)
     k_cache = v_cache = None
     cache_seed = int(rng.integers(0, 2**31 - 1))
     if host_cache:
@@ -235,7 +242,8 @@ def build(name, seed, seq_lens, q_lens, num_q_heads, num_kv_heads, head_size,
     return PagedBatch(name=name, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                       head_size=head_size, block_size=block_size, num_blocks=nb,
                       q_dtype=q_dtype, kv_dtype=kv_dtype, src_dtype=src_dtype,
-                      scale=float(scale), k_scale=float(ks), v_scale=float(vs),
+                      scale=float(scale), k_scale=ks if np.ndim(ks) else float(ks),
+                      v_scale=vs if np.ndim(vs) else float(vs),
                       causal=causal, seq_lens=seq_lens, query_start_loc=qsl,
                       block_tables=table, slot_mapping=slots, q=q, key=key, value=value,
                       k_cache=k_cache, v_cache=v_cache, cache_seed=cache_seed,
