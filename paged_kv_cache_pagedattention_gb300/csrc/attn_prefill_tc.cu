@@ -442,13 +442,16 @@ __global__ void __launch_bounds__(threads_tc<is_fp8<KVDT>()>(), 1)
   } else if (kF8 && warp >= kConvWarp) {
     // ------------------------------------------------------------ FP8 converters
     // Chunk i: wait for its codes in staging and for its f16 stage to be free, widen
-    // every code to f16 exactly (e4m3 values are all f16 values; the scales are
-    // applied later) into the K-major K layout and the per-block V layout, release
-    // the staging slot and mark the f16 stage full.  Unit u of a chunk is one 16-byte
-    // group of codes: tensor u / 512, key (u % 512) / 8, group u % 8 (elements
-    // 16 g .. 16 g + 15 = two 8-element f16 chunks of piece g / 4).
+    // every code to f16 exactly (every e4m3 value and every finite e5m2 value is an
+    // f16 value; the scales are applied later) into the K-major K layout and the
+    // per-block V layout, release the staging slot and mark the f16 stage full.
+    // Thread t owns one row: K row t (t < 64) or V row t - 64.  Reading group g of
+    // a row and writing its two f16 chunks touch eight different 16-byte bank groups
+    // across any eight consecutive rows, so neither side has bank conflicts.
     if constexpr (kF8) {
     const int ct = tid - kConvWarp * 32;
+    const int tensor = ct / kChunk, key = ct % kChunk;
+    const int blk = key / BS, tok = key % BS, sw = key & 7;  // tok & 7 == key & 7
     for (int i = 0; i < nch; ++i) {
       const int s = i % ST, ss = i % G::kStgStages;
       bool ok = mbar_wait_bounded(stg_full + ss, (i / G::kStgStages) & 1);
@@ -457,14 +460,13 @@ __global__ void __launch_bounds__(threads_tc<is_fp8<KVDT>()>(), 1)
         if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
         break;
       }
-      const uint8_t* sg = sStg + ss * 2 * G::kStgKv;
+      const uint8_t* srow = sStg + ss * 2 * G::kStgKv + tensor * G::kStgKv + blk * G::kStgBlock + tok * 128;
       uint8_t* sk = sKV + s * G::kStageBytes;
-#pragma unroll 2
-      for (int u = ct; u < 2 * kChunk * 8; u += kConvThreads) {
-        const int tensor = u / (kChunk * 8), key = (u % (kChunk * 8)) >> 3, g = u & 7;
-        const int blk = key / BS, tok = key % BS;
-        const uint4 codes = *reinterpret_cast<const uint4*>(sg + tensor * G::kStgKv + blk * G::kStgBlock +
-                                                            swz128(tok, g));
+      uint8_t* drow = tensor == 0 ? sk + key * 128 : sk + G::kKvBytes + blk * G::kBlockTx + tok * 128;
+      const int piece_stride = tensor == 0 ? G::kPiece : BS * 128;
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {  // codes 16 g .. 16 g + 15 -> f16 chunks 2g, 2g+1 (mod 8) of piece g / 4
+        const uint4 codes = *reinterpret_cast<const uint4*>(srow + ((g ^ sw) << 4));
         const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
         uint32_t h[8];
 #pragma unroll
@@ -472,11 +474,10 @@ __global__ void __launch_bounds__(threads_tc<is_fp8<KVDT>()>(), 1)
           h[2 * e] = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(cw[e] & 0xffffu));
           h[2 * e + 1] = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(cw[e] >> 16));
         }
-        const int pc = g >> 2, cc = (2 * g) & 7;
-        uint8_t* row = tensor == 0 ? sk + pc * G::kPiece + key * 128
-                                   : sk + G::kKvBytes + blk * G::kBlockTx + pc * BS * 128 + tok * 128;
-        *reinterpret_cast<uint4*>(row + ((cc ^ (key & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (key & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+        uint8_t* row = drow + (g >> 2) * piece_stride;
+        const int cc = (2 * g) & 7;
+        *reinterpret_cast<uint4*>(row + ((cc ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(row + (((cc + 1) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
       }
       fence_proxy_async();  // generic-proxy writes, read next by the tensor core
       mbar_arrive(stg_empty + ss);
