@@ -9,7 +9,7 @@ helpers.  The only thing both sides consume is the seeded input generator in
 
 Everything is computed in float64 with numpy; stored cache elements are decoded
 from their raw bits exactly (fp32 / fp16 / bf16 widen exactly, FP8 e4m3 is
-decoded from its bit fields).
+decoded from its bit fields, NVFP4 from its E2M1 codes and E4M3 block scales).
 
 Sources cited by key in the docstrings of this package:
 
@@ -18,6 +18,8 @@ Sources cited by key in the docstrings of this package:
 [NOTES]    "大模型推理优化学习笔记" (fishingrodd.cn, 2026/10/30).
 [LINEAGE]  "从静态批处理到状态化推理集群" (wineandchord.com,
            llm/landscape/lineages/inference-serving).
+[DSV41]    vLLM x DeepSeek-V4.1-Flash agentic throughput write-up (yaoyouai.cn,
+           news/405/vllm-deepseek-v41-flash-agentic-throughput-5x).
 [ARCH]     summary of a vLLM V1 architecture deep-dive
            (ai.youdonthavefriends.com, llm/ai/deep-analysis/2026/08/08/vllm-architecture).
 
@@ -29,6 +31,7 @@ invariants, an independent library routine or brute force.  No function is
 
 from .paged_attention import (  # noqa: F401
     DTYPE_BYTES,
+    E2M1_MAX,
     E4M3_MAX,
     E5M2_MAX,
     attend,
@@ -36,6 +39,9 @@ from .paged_attention import (  # noqa: F401
     bytes_per_block,
     copy_blocks,
     decode_bits,
+    e2m1_encode,
+    e2m1_table,
+    e2m1_value,
     e4m3_encode,
     e4m3_value,
     e4m3_table,
@@ -46,6 +52,11 @@ from .paged_attention import (  # noqa: F401
     gather_kv,
     kv_cache_bytes,
     merge_partials,
+    NVFP4_GROUP,
+    nvfp4_pack,
+    nvfp4_quantize_row,
+    nvfp4_rows,
+    nvfp4_tile_bytes,
     paged_decode,
     paged_varlen,
     quantize_e4m3,

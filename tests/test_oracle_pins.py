@@ -219,6 +219,209 @@ def test_scatter_fp8_codes_are_nearest():
         assert np.all((got == 0) | (np.sign(got) == np.sign(x)))
 
 
+# ---------------------------------------------------------------- NVFP4
+
+_E2M1_MAGS = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _e4m3_torch(codes):
+    """E4M3 code -> value through torch's float8_e4m3fn (pinned independently)."""
+    return torch.from_numpy(np.asarray(codes, np.uint8)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e2m1_values_are_the_two_bit_significand_floats():
+    """E2M1 magnitudes are 0 and the multiples of 0.5 up to 6 whose significand has
+    at most two bits (odd part 1 or 3), found by enumeration; negative codes are the
+    sign-flipped magnitudes; every value is exact in E4M3 (torch's cast)."""
+    mags = [0.0]
+    for k in range(1, 13):
+        odd = k
+        while odd % 2 == 0:
+            odd //= 2
+        if odd in (1, 3):
+            mags.append(k / 2)
+    assert mags == _E2M1_MAGS
+    t = oracle.e2m1_table()
+    assert list(t[:8]) == mags
+    assert np.array_equal(t[8:], -t[:8]) and all(math.copysign(1.0, v) < 0 for v in t[8:])
+    tt = torch.tensor(t, dtype=torch.float32)
+    assert torch.equal(tt.to(torch.float8_e4m3fn).to(torch.float32), tt)
+
+
+def check_e2m1_encode(encode):
+    """Brute force over y = k/32 in [-8, 8] and -0: the code is a nearest E2M1 value,
+    an exact tie goes to the code with mantissa bit 0, |y| >= 6 saturates, the sign
+    bit follows y.  Returns the number of violations."""
+    ys = np.concatenate([np.arange(-256, 257) / 32.0, [-0.0]])
+    codes = np.asarray(encode(ys))
+    bad = 0
+    for y, c in zip(ys, codes):
+        a = abs(float(y))
+        dist = [abs(a - m) for m in _E2M1_MAGS]
+        near = [i for i, dd in enumerate(dist) if dd == min(dist)]
+        want = near[0] if len(near) == 1 else [i for i in near if i % 2 == 0][0]
+        if a >= 6.0:
+            want = 7
+        want |= 0x8 if math.copysign(1.0, float(y)) < 0 else 0
+        bad += int(c) != want
+    return bad
+
+
+def test_e2m1_encode_nearest_even_saturating():
+    assert check_e2m1_encode(oracle.e2m1_encode) == 0
+    assert oracle.e2m1_encode([np.nan])[0] == 0x7
+
+
+def check_nvfp4_round_trip(quantize):
+    """Rows made of E2M1 values x normal E4M3 block scales x a power-of-two tensor
+    scale, with one +-6 in every group (so the group maximum fixes its block scale
+    exactly), are stored back as exactly those codes and scales.  Returns the
+    number of mismatching codes."""
+    rng = np.random.default_rng(5)
+    bad = 0
+    for _ in range(40):
+        st = float(2.0 ** int(rng.integers(-8, 3)))
+        d = 64
+        sb = rng.integers(0x08, 0x77, size=d // 16).astype(np.uint8)       # normal E4M3 codes
+        codes = rng.integers(0, 16, size=d).astype(np.uint8)
+        for g in range(d // 16):
+            codes[g * 16 + int(rng.integers(16))] = int(rng.choice([0x7, 0xF]))
+        vals = np.array([(-1.0 if c & 8 else 1.0) * _E2M1_MAGS[c & 7] for c in codes])
+        x = vals * np.repeat(_e4m3_torch(sb), 16) * st
+        got_c, got_s = quantize(x, st)
+        bad += int(np.sum(np.asarray(got_s) != sb)) + int(np.sum(np.asarray(got_c) != codes))
+    return bad
+
+
+def test_nvfp4_exact_rows_round_trip():
+    assert check_nvfp4_round_trip(oracle.nvfp4_quantize_row) == 0
+
+
+def test_nvfp4_quantisation_error_bound():
+    """N(0,1) rows, tensor scale 0.0123: each block scale is the E4M3 rounding of
+    amax / (6 s) (relative error <= 2^-4 for normal values), and each element's error
+    is at most half the E2M1 spacing at its scaled magnitude, saturation included."""
+    rng = np.random.default_rng(6)
+    st = np.float32(0.0123)
+    for _ in range(30):
+        x = rng.standard_normal(128).astype(np.float32).astype(np.float64)
+        codes, scales = oracle.nvfp4_quantize_row(x, float(st))
+        b = _e4m3_torch(scales)
+        for g in range(8):
+            q = np.max(np.abs(x[g * 16:(g + 1) * 16])) / (6.0 * float(st))
+            assert abs(b[g] - q) <= q * 2.0 ** -4 * 1.0001
+            unit = float(st) * b[g]
+            for i in range(g * 16, (g + 1) * 16):
+                c = int(codes[i])
+                deq = (-1.0 if c & 8 else 1.0) * _E2M1_MAGS[c & 7] * unit
+                y = abs(x[i]) / unit
+                half_gap = 0.25 if y < 2 else 0.5 if y < 4 else 1.0
+                assert abs(deq - x[i]) <= half_gap * unit * 1.0001
+
+
+def test_nvfp4_zero_and_vanishing_groups():
+    st = 1.0
+    x = np.zeros(32)
+    x[16:] = 1e-6                     # amax / 6 rounds to E4M3 zero
+    codes, scales = oracle.nvfp4_quantize_row(x, st)
+    assert np.all(codes == 0) and np.all(scales == 0)
+    x[16] = 6.0 * 448.0 * 4           # beyond the largest block scale: saturates
+    codes, scales = oracle.nvfp4_quantize_row(x, st)
+    assert scales[1] == 0x7E and (codes[16] & 7) == 7
+    assert np.all(codes[17:] == 0)
+
+
+def test_nvfp4_power_of_two_rescaling_keeps_codes():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal(128)
+    c0, s0 = oracle.nvfp4_quantize_row(x, 0.0123)
+    c1, s1 = oracle.nvfp4_quantize_row(x * 8.0, 0.0123 * 8.0)
+    assert np.array_equal(c0, c1) and np.array_equal(s0, s1)
+
+
+def test_nvfp4_is_about_45_percent_smaller_than_fp8():
+    # [DSV41] "三、第二招": the NVFP4 KV format is 45% smaller than the FP8 KV cache.
+    fp8_tile = 16 * 128 * oracle.DTYPE_BYTES["fp8_e4m3"]
+    saving = 1.0 - oracle.nvfp4_tile_bytes(16, 128) / fp8_tile
+    assert saving == 0.4375 and abs(saving - 0.45) < 0.02
+
+
+def _golden_nvfp4_tile():
+    """A tile of block 2, head 32, built byte by byte from the layout: code rows
+    (16 bytes each, element 2i in the low nibble of byte i), then scale rows (2
+    bytes each).  Expected values with tensor scale 0.5, worked by hand."""
+    tile = np.zeros(36, np.uint8)
+    tile[0], tile[1] = 0x21, 0xF7          # row 0: 0.5, 1.0, 6, -6, then zeros
+    tile[16] = 0x3A                        # row 1: -1.0, 1.5, then 0.5 everywhere
+    tile[17:32] = 0x11
+    tile[32:36] = [0x38, 0x40, 0x30, 0x3C]  # scales 1.0, 2.0 | 0.5, 1.5
+    want = np.zeros((2, 32))
+    want[0, :4] = [0.25, 0.5, 3.0, -3.0]
+    want[1, 0], want[1, 1] = -0.25, 0.375
+    want[1, 2:16] = 0.125
+    want[1, 16:] = 0.375
+    return tile, want
+
+
+def check_nvfp4_rows_golden(rows_impl):
+    tile, want = _golden_nvfp4_tile()
+    cache = np.zeros((3, 1, 36), np.uint8)
+    cache[2, 0] = tile
+    got = rows_impl(cache, [2, 2], [0, 1], 2, 0.5)[:, 0, :]
+    return float(np.abs(got - want).max())
+
+
+def test_nvfp4_rows_golden_tile():
+    assert check_nvfp4_rows_golden(oracle.nvfp4_rows) == 0.0
+
+
+def test_nvfp4_scatter_writes_the_quantised_row_in_its_tile():
+    b = workloads.build("s4", 13, [40, 7], [3, 1], 8, 2, 128, 16, "nvfp4")
+    kc, vc = b.k_cache.copy(), b.v_cache.copy()
+    k0 = kc.copy()
+    oracle.reshape_and_cache(b.key, b.value, kc, vc, b.slot_mapping, 16, "bf16", "nvfp4", b.k_scale, b.v_scale)
+    for t, s in enumerate(b.slot_mapping):
+        got = oracle.nvfp4_rows(kc, [s // 16], [s % 16], 16, b.k_scale)[0]
+        for h in range(2):
+            codes, scales = oracle.nvfp4_quantize_row(oracle.decode_bits(b.key[t, h], "bf16"), b.k_scale)
+            vals = np.array([(-1.0 if c & 8 else 1.0) * _E2M1_MAGS[c & 7] for c in codes])
+            assert np.array_equal(got[h], vals * np.repeat(_e4m3_torch(scales), 16) * b.k_scale)
+    # bytes of other slots are untouched
+    written = set(int(s) for s in b.slot_mapping)
+    for blk in range(kc.shape[0]):
+        for off in range(16):
+            if blk * 16 + off in written:
+                continue
+            assert np.array_equal(kc[blk, :, off * 64:(off + 1) * 64], k0[blk, :, off * 64:(off + 1) * 64])
+            assert np.array_equal(kc[blk, :, 1024 + off * 8:1024 + (off + 1) * 8],
+                                  k0[blk, :, 1024 + off * 8:1024 + (off + 1) * 8])
+
+
+def test_nvfp4_attention_is_placement_invariant_and_matches_sdpa():
+    """Decode over an NVFP4 cache: the same logical blocks under a second placement
+    give identical outputs, and both equal torch SDPA on the dequantised rows."""
+    b = workloads.build("p4", 14, [70, 33, 16], [1, 1, 1], 8, 2, 128, 16, "nvfp4")
+    out = oracle.paged_decode(b.q, "bf16", b.k_cache, b.v_cache, "nvfp4", b.block_tables, b.seq_lens, 16,
+                              b.scale, b.k_scale, b.v_scale)
+    perm = np.random.default_rng(3).permutation(b.num_blocks)
+    inv = np.argsort(perm)
+    kc2, vc2 = b.k_cache[perm], b.v_cache[perm]               # new block i holds old block perm[i]
+    tables2 = np.where(b.block_tables >= 0, inv[np.maximum(b.block_tables, 0)], -1).astype(np.int32)
+    out2 = oracle.paged_decode(b.q, "bf16", kc2, vc2, "nvfp4", tables2, b.seq_lens, 16, b.scale, b.k_scale,
+                               b.v_scale)
+    assert np.array_equal(out, out2)
+    q64 = oracle.decode_bits(b.q, "bf16")
+    for r, n in enumerate(b.seq_lens):
+        pos = np.arange(n)
+        phys = b.block_tables[r][pos // 16]
+        K = torch.from_numpy(oracle.nvfp4_rows(b.k_cache, phys, pos % 16, 16, b.k_scale))   # [n][2][d]
+        V = torch.from_numpy(oracle.nvfp4_rows(b.v_cache, phys, pos % 16, 16, b.v_scale))
+        q = torch.from_numpy(q64[r]).view(2, 4, 1, 128)                                    # [Hkv][G][1][d]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q, K.permute(1, 0, 2)[:, None], V.permute(1, 0, 2)[:, None], scale=b.scale)
+        assert np.allclose(out[r], ref.reshape(8, 128).numpy(), rtol=0, atol=1e-12)
+
+
 # ---------------------------------------------------------------- softmax merge
 
 def check_merge_golden(partial, merge, finalize):
@@ -675,7 +878,32 @@ def _encode_ties_away(x):
     return np.array(out, np.uint8)
 
 
+def _e2m1_ties_away(x):
+    out = []
+    for v in np.asarray(x, dtype=np.float64):
+        a = min(abs(v), 6.0)
+        code = int(np.argmin(np.abs(np.array(_E2M1_MAGS) - a) - 1e-30 * np.array(_E2M1_MAGS)))
+        out.append(code | (0x8 if math.copysign(1, v) < 0 else 0))
+    return np.array(out, np.uint8)
+
+
+def _nvfp4_amax_over_four(x64, scale):
+    # a plausible slip: block scale from amax / 4 instead of amax / 6
+    return oracle.nvfp4_quantize_row(np.asarray(x64) * 1.5, scale)
+
+
+def _nvfp4_rows_nibbles_swapped(cache, phys, off, bs, scale=1.0):
+    c = np.asarray(cache).copy()
+    d = c.shape[2] * 16 // (9 * bs)
+    codes = c[:, :, :bs * d // 2]
+    c[:, :, :bs * d // 2] = (codes >> 4) | ((codes & 0xF) << 4)
+    return oracle.nvfp4_rows(c, phys, off, bs, scale)
+
+
 def test_planted_mistakes_are_caught():
+    assert check_e2m1_encode(_e2m1_ties_away) > 0
+    assert check_nvfp4_round_trip(_nvfp4_amax_over_four) > 0
+    assert check_nvfp4_rows_golden(_nvfp4_rows_nibbles_swapped) > 0
     assert check_sdpa(attend_impl=_attend_gqa_modulo) > 1e-3
     assert check_brute_force(attend_impl=_attend_off_by_one) > 1e-3
     assert check_sdpa(attend_impl=_attend_no_scale) > 1e-3

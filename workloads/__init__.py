@@ -24,6 +24,17 @@ Workloads (shapes and distributions from the serving pages' workloads):
               32/8 heads, d 128, bf16, block 16; 2,176 new tokens.
 * ``fp8``     batch 256, lengths U[1024, 32768], 32/8 heads, d 128, FP8 e4m3
               K/V with per-tensor scale 2^-6, bf16 q/out, block 32.
+* ``nvfp4``   the ``fp8`` decode shapes with an NVFP4 cache (4-bit E2M1 codes,
+              one E4M3 scale per 16 elements, per-tensor fp32 scale 0.375).
+
+NVFP4 caches are ``[num_blocks][num_kv_heads][tile_bytes]`` bytes: a (block, KV
+head) tile holds block_size rows of head_size/2 code bytes, then block_size rows
+of head_size/16 block-scale bytes.  Their history is drawn as random bits, not
+quantised from values (this module has no quantiser): uniform E2M1 codes, and
+block-scale codes uniform over the E4M3 codes 0x20..0x47 (values 0.125 .. 3.75),
+so that code x block scale x 0.375 spans about +-8 with a mean magnitude near
+0.6.  New tokens' keys and values are N(0,1) as for every other cache type; the
+scatter under test quantises them.
 """
 
 from __future__ import annotations
@@ -34,8 +45,11 @@ from typing import Optional
 import numpy as np
 
 ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "fp8_e4m3": 1, "fp8_e5m2": 1}
-BITS_NP = {"f32": np.uint32, "f16": np.uint16, "bf16": np.uint16, "fp8_e4m3": np.uint8, "fp8_e5m2": np.uint8}
+BITS_NP = {"f32": np.uint32, "f16": np.uint16, "bf16": np.uint16, "fp8_e4m3": np.uint8, "fp8_e5m2": np.uint8,
+           "nvfp4": np.uint8}
 FP8 = ("fp8_e4m3", "fp8_e5m2")
+NVFP4 = "nvfp4"
+SCALED = FP8 + (NVFP4,)  # cache types that carry fp32 scales
 # largest finite magnitude of each FP8 format: torch's casts do not saturate
 FP8_MAX = {"fp8_e4m3": 448.0, "fp8_e5m2": 57344.0}
 
@@ -125,6 +139,20 @@ def _cast_bits(x, dtype: str, scale: float = 1.0) -> np.ndarray:
     raise ValueError(dtype)
 
 
+def nvfp4_tile_bytes(block_size: int, head_size: int) -> int:
+    """Storage size of one (block, KV head) tile of an NVFP4 cache."""
+    return block_size * head_size // 2 + block_size * head_size // 16
+
+
+def nvfp4_random_cache(rng: np.random.Generator, num_blocks: int, num_kv_heads: int, block_size: int,
+                       head_size: int) -> np.ndarray:
+    """Random NVFP4 cache bytes: uniform code bytes, block-scale codes in 0x20..0x47."""
+    codes = rng.integers(0, 256, size=(num_blocks, num_kv_heads, block_size * head_size // 2), dtype=np.uint8)
+    scales = rng.integers(0x20, 0x48, size=(num_blocks, num_kv_heads, block_size * head_size // 16),
+                          dtype=np.uint8)
+    return np.concatenate([codes, scales], axis=2)
+
+
 def torch_dtype(dtype: str):
     import torch
 
@@ -142,7 +170,7 @@ def bits_to_torch(bits: np.ndarray, dtype: str, device=None):
         t = t.view(torch.int32).view(torch.float32)
     elif dtype in ("f16", "bf16"):
         t = t.view(torch.int16).view(torch_dtype(dtype))
-    elif dtype == "fp8_e4m3":
+    elif dtype in ("fp8_e4m3", "nvfp4"):
         t = t.view(torch.uint8)
     elif dtype == "fp8_e5m2":
         t = t.view(torch.uint8).view(torch.float8_e5m2)
@@ -209,12 +237,15 @@ def _slots_for(table, seq_lens, q_lens, block_size):
 def build(name, seed, seq_lens, q_lens, num_q_heads, num_kv_heads, head_size,
           block_size, kv_dtype, q_dtype=None, src_dtype=None, scale=None,
           fp8_scale=2.0 ** -6, pool_factor=2.0, min_pool=0, shared=None,
-          host_cache=True, causal=True, families=None) -> PagedBatch:
-    """Generic builder: lengths, placement, slots, q / new K,V and (optionally) cache bits."""
+          host_cache=True, causal=True, families=None, nvfp4_scale=0.375) -> PagedBatch:
+    """Generic builder: lengths, placement, slots, q / new K,V and (optionally) cache bits.
+
+    ``fp8_scale`` (FP8) / ``nvfp4_scale`` (NVFP4) is the caches' fp32 scale: a float,
+    or one value per KV head (K uses them in order, V reversed)."""
     rng = np.random.Generator(np.random.PCG64(seed))
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     q_lens = np.asarray(q_lens, dtype=np.int32)
-    q_dtype = q_dtype or ("bf16" if kv_dtype in FP8 else kv_dtype)
+    q_dtype = q_dtype or ("bf16" if kv_dtype in SCALED else kv_dtype)
     src_dtype = src_dtype or q_dtype
     if scale is None:
         scale = 1.0 / float(np.sqrt(head_size))
@@ -226,19 +257,23 @@ def build(name, seed, seq_lens, q_lens, num_q_heads, num_kv_heads, head_size,
     q = normal_bits(rng, (tq, num_q_heads, head_size), q_dtype)
     key = normal_bits(rng, (tq, num_kv_heads, head_size), src_dtype)
     value = normal_bits(rng, (tq, num_kv_heads, head_size), src_dtype)
-    is_fp8 = kv_dtype in FP8
-    ks = vs = fp8_scale if is_fp8 else 1.0
-    if is_fp8 and np.ndim(fp8_scale):  # one scale per KV head
-        ks = np.asarray(fp8_scale, dtype=np.float32)
+    sc = fp8_scale if kv_dtype in FP8 else nvfp4_scale if kv_dtype == NVFP4 else 1.0
+    ks = vs = sc
+    if kv_dtype in SCALED and np.ndim(sc):  # one scale per KV head
+        ks = np.asarray(sc, dtype=np.float32)
         vs = ks[::-1].copy()
         assert ks.shape == (num_kv_heads,)
     k_cache = v_cache = None
     cache_seed = int(rng.integers(0, 2**31 - 1))
     if host_cache:
-        shape = (nb, num_kv_heads, block_size, head_size)
         crng = np.random.Generator(np.random.PCG64(cache_seed))
-        k_cache = normal_bits(crng, shape, kv_dtype, ks)
-        v_cache = normal_bits(crng, shape, kv_dtype, vs)
+        if kv_dtype == NVFP4:
+            k_cache = nvfp4_random_cache(crng, nb, num_kv_heads, block_size, head_size)
+            v_cache = nvfp4_random_cache(crng, nb, num_kv_heads, block_size, head_size)
+        else:
+            shape = (nb, num_kv_heads, block_size, head_size)
+            k_cache = normal_bits(crng, shape, kv_dtype, ks)
+            v_cache = normal_bits(crng, shape, kv_dtype, vs)
     return PagedBatch(name=name, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                       head_size=head_size, block_size=block_size, num_blocks=nb,
                       q_dtype=q_dtype, kv_dtype=kv_dtype, src_dtype=src_dtype,
@@ -330,7 +365,7 @@ def fp8(seed: int = 4, host_cache: bool = False, batch: int = 256,
     lens = rng.integers(1024, 32768, size=batch, endpoint=True)
     if scale_lengths != 1.0:
         lens = np.maximum(np.round(lens * scale_lengths).astype(np.int64), 1)
-    name = "fp8_kv_decode" if kv_dtype == "fp8_e4m3" else "fp8_e5m2_kv_decode"
+    name = {"fp8_e4m3": "fp8_kv_decode", "fp8_e5m2": "fp8_e5m2_kv_decode", NVFP4: "nvfp4_kv_decode"}[kv_dtype]
     return build(name, seed, lens, [1] * batch, 32, 8, 128, 32, kv_dtype,
                  q_dtype="bf16", src_dtype="bf16", host_cache=host_cache)
 
@@ -340,7 +375,13 @@ def fp8_e5m2(seed: int = 4, host_cache: bool = False, scale_lengths: float = 1.0
     return fp8(seed, host_cache, scale_lengths=scale_lengths, kv_dtype="fp8_e5m2")
 
 
-NAMED = {"tiny": tiny, "llama": llama, "agentic": agentic, "mixed": mixed, "fp8": fp8, "mixed_fp8": mixed_fp8, "fp8_e5m2": fp8_e5m2}
+def nvfp4(seed: int = 4, host_cache: bool = False, scale_lengths: float = 1.0) -> PagedBatch:
+    """The FP8 decode shapes with an NVFP4 cache."""
+    return fp8(seed, host_cache, scale_lengths=scale_lengths, kv_dtype=NVFP4)
+
+
+NAMED = {"tiny": tiny, "llama": llama, "agentic": agentic, "mixed": mixed, "fp8": fp8, "mixed_fp8": mixed_fp8,
+         "fp8_e5m2": fp8_e5m2, "nvfp4": nvfp4}
 
 
 # --------------------------------------------------------------------------
@@ -361,6 +402,24 @@ def device_cache(batch: PagedBatch, device, chunk_elems: int = 1 << 28):
     if batch.k_cache is not None:
         return (bits_to_torch(batch.k_cache, batch.kv_dtype, device),
                 bits_to_torch(batch.v_cache, batch.kv_dtype, device))
+    if batch.kv_dtype == NVFP4:
+        # uniform code bytes, block-scale bytes in 0x20..0x47 (as nvfp4_random_cache)
+        gen = torch.Generator(device=device)
+        gen.manual_seed(batch.cache_seed)
+        ncode = batch.block_size * batch.head_size // 2
+        tile = nvfp4_tile_bytes(batch.block_size, batch.head_size)
+        caches = []
+        for _ in range(2):
+            c = torch.empty((batch.num_blocks, batch.num_kv_heads, tile), dtype=torch.uint8, device=device)
+            step = max(1, chunk_elems // (batch.num_kv_heads * tile))
+            for lo in range(0, batch.num_blocks, step):
+                hi = min(lo + step, batch.num_blocks)
+                c[lo:hi, :, :ncode] = torch.randint(0, 256, (hi - lo, batch.num_kv_heads, ncode), generator=gen,
+                                                    device=device, dtype=torch.int32).to(torch.uint8)
+                c[lo:hi, :, ncode:] = torch.randint(0x20, 0x48, (hi - lo, batch.num_kv_heads, tile - ncode),
+                                                    generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
+            caches.append(c)
+        return caches[0], caches[1]
     tdt = torch_dtype(batch.kv_dtype) if batch.kv_dtype != "fp8_e4m3" else torch.uint8
     if batch.kv_dtype == "fp8_e5m2":
         tdt = torch.float8_e5m2
