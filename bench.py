@@ -38,7 +38,7 @@ METRIC = "attended KV tokens/sec and achieved HBM GB/s (fraction of GB300 peak),
 UNIT = "tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-WORKLOADS = ("agentic", "llama", "fp8", "fp8_e5m2", "mixed", "mixed_fp8", "tiny")
+WORKLOADS = ("agentic", "llama", "fp8", "fp8_e5m2", "nvfp4", "mixed", "mixed_fp8", "tiny")
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -225,12 +225,14 @@ def make_workload(name: str, seed: int, length_scale: float = 1.0):
         return workloads.fp8_e5m2(seed=seed, scale_lengths=length_scale)
     if name == "mixed_fp8":
         return workloads.mixed_fp8(seed=seed, scale_lengths=length_scale)
+    if name == "nvfp4":
+        return workloads.nvfp4(seed=seed, scale_lengths=length_scale)
     if name == "tiny":
         return workloads.tiny(seed=seed)
     raise ValueError(name)
 
 
-BASE_SEEDS = {"agentic": 2, "llama": 1, "fp8": 4, "fp8_e5m2": 4, "mixed": 3, "mixed_fp8": 3, "tiny": 0}
+BASE_SEEDS = {"agentic": 2, "llama": 1, "fp8": 4, "fp8_e5m2": 4, "nvfp4": 4, "mixed": 3, "mixed_fp8": 3, "tiny": 0}
 
 
 def prefix_groups(b):
@@ -441,9 +443,9 @@ def run_ours(args):
     tables = torch.from_numpy(b.block_tables).to(dev)
     lens = torch.from_numpy(b.seq_lens).to(dev)
     qsl = torch.from_numpy(b.query_start_loc).to(dev)
-    fp8 = b.kv_dtype in workloads.FP8
-    ks = torch.tensor([b.k_scale], dtype=torch.float32, device=dev) if fp8 else None
-    vs = torch.tensor([b.v_scale], dtype=torch.float32, device=dev) if fp8 else None
+    scaled = b.kv_dtype in workloads.SCALED
+    ks = torch.tensor([b.k_scale], dtype=torch.float32, device=dev) if scaled else None
+    vs = torch.tensor([b.v_scale], dtype=torch.float32, device=dev) if scaled else None
     out = torch.empty_like(q)
     part = args.partition_size
     if varlen:

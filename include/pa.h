@@ -39,6 +39,17 @@
  *   contiguous.  Bytes per block per layer (K and V together) are
  *   2 x block_size x num_kv_heads x head_size x dtype_bytes ([ARCH] Part 1,
  *   KV cache manager).  Both tensors must start on a 16-byte boundary.
+ * NVFP4 caches.  [DSV41] "三、第二招：把能合的内核全合成一个" names an NVFP4 KV
+ *   format 45% smaller than FP8; read as NVIDIA's NVFP4: 4-bit E2M1 elements (1 sign,
+ *   2 exponent bits with bias 1, 1 mantissa bit: +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}), one
+ *   E4M3 block scale per 16 consecutive elements of a token's head vector, and the
+ *   fp32 scale k_scale / v_scale.  Shape [num_blocks][num_kv_heads][tile_bytes]
+ *   bytes, tile_bytes = 9 x block_size x head_size / 16: a tile holds block_size
+ *   code rows of head_size/2 bytes (element 2i in the low nibble of byte i,
+ *   element 2i+1 in the high nibble), then block_size scale rows of head_size/16
+ *   bytes.  head_size must be a multiple of 16 and block_size x head_size a
+ *   multiple of 256 (whole 16-byte tiles).  Element value = E2M1(code) x
+ *   E4M3(block scale) x scale.
  * Slots.  A token with flat slot s lives in physical block s / block_size at
  *   offset s % block_size ([ARCH] Part 1, forward pass: slot_mapping).  A
  *   negative slot marks a padding token and is skipped.
@@ -59,7 +70,8 @@
  *   FP8 caches carry fp32 scales (k_scale, v_scale: device pointers to one float
  *   each, or to num_kv_heads floats with the *_PER_HEAD formats, KV head h using
  *   [h]): stored code = fp8(x / scale), rounded to nearest even with saturation to
- *   +-448 (e4m3) or +-57344 (e5m2); value = fp8 decode x scale.
+ *   +-448 (e4m3) or +-57344 (e5m2); value = fp8 decode x scale.  NVFP4 caches
+ *   (PA_NVFP4, PA_NVFP4_PER_HEAD) carry the same fp32 scales; see pa_reshape_and_cache.
  * Errors.  Argument checks that need no device data return synchronously with
  *   a status and launch nothing.  Inputs that live on the device (block-table
  *   entries, slots, sequence lengths, query offsets) are checked by the kernels:
@@ -96,7 +108,9 @@ typedef enum pa_dtype {
   PA_FP8_E4M3 = 3, /* cache only: stored as uint8 codes with a per-tensor fp32 scale */
   PA_FP8_E5M2 = 4, /* cache only: as PA_FP8_E4M3, 5 exponent and 2 mantissa bits */
   PA_FP8_E4M3_PER_HEAD = 5, /* as PA_FP8_E4M3 with one scale per KV head: k_scale and */
-  PA_FP8_E5M2_PER_HEAD = 6  /* v_scale point to num_kv_heads floats (head h: [h]) */
+  PA_FP8_E5M2_PER_HEAD = 6, /* v_scale point to num_kv_heads floats (head h: [h]) */
+  PA_NVFP4 = 7,             /* cache only: E2M1 codes + E4M3 block scales + fp32 scale */
+  PA_NVFP4_PER_HEAD = 8     /* as PA_NVFP4 with one fp32 scale per KV head */
 } pa_dtype;
 
 /* Bits of the device error word (pa_get_error_flags). */
@@ -128,8 +142,16 @@ int32_t pa_version(void);
  *   or PA_FP8_E5M2 (src f32/f16/bf16) stores fp8_rne_satfinite(float(x) / *k_scale)
  *   (resp. v; saturation at +-448 for e4m3, +-57344 for e5m2),
  *   the division being IEEE fp32 division.  k_scale / v_scale: device pointers to
- *   one float each, used only for FP8 (may be NULL otherwise).
- *   head_size * dtype_bytes must be a multiple of 16 bytes for both dtypes.
+ *   one float each, used only for FP8 and NVFP4 (may be NULL otherwise).
+ *   cache_dtype == PA_NVFP4 (src f32/f16/bf16): for each group of 16 consecutive
+ *   elements of a (token, head) row with largest magnitude a, with s = *k_scale
+ *   (resp. v) and every product / quotient one IEEE fp32 operation: the block
+ *   scale is e4m3_rne_satfinite(a / (6 s)), of value b; each element x is stored as
+ *   e2m1_rne_satfinite(x / (s b)) (ties to the even code, saturating at +-6, the
+ *   sign kept, so small negatives give code 0x8); a group with b == 0 stores zero
+ *   codes.  Non-finite inputs give unspecified codes.
+ *   head_size * dtype_bytes must be a multiple of 16 bytes for both dtypes (NVFP4:
+ *   the tile rule of the cache layout above).
  */
 pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
                                const int64_t* slot_mapping, int32_t num_tokens, int32_t num_blocks,
@@ -148,7 +170,8 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
  * this, points the writing branch's block table at the copy, then writes.
  *
  *   k_cache, v_cache  cache tensors (layout above), cache_dtype (any pa_dtype;
- *                  only its size matters: the bytes are copied exactly)
+ *                  only its size matters: the bytes are copied exactly; an NVFP4
+ *                  block is num_kv_heads tiles of codes and block scales)
  *   block_mapping  int64 [num_pairs][2], pairs (src, dst): block dst of both
  *                  tensors becomes a copy of block src (all KV heads, all
  *                  block_size slots).  A pair with src or dst outside
@@ -191,8 +214,8 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t n
  *
  *   out            [num_seqs][num_q_heads][head_size], q_dtype (written)
  *   q              [num_seqs][num_q_heads][head_size], q_dtype (f32, f16 or bf16)
- *   k_cache, v_cache  cache tensors, kv_dtype; kv_dtype == q_dtype, or PA_FP8_E4M3 / E5M2
- *                  with q_dtype f16/bf16 (k_scale / v_scale then required)
+ *   k_cache, v_cache  cache tensors, kv_dtype; kv_dtype == q_dtype, or an FP8 / NVFP4
+ *                  format with q_dtype f16/bf16 (k_scale / v_scale then required)
  *   block_tables   int32 [num_seqs][max_blocks_per_seq]
  *   seq_lens       int32 [num_seqs], each in [1, max_seq_len]
  *   max_seq_len    host-side upper bound of seq_lens (sizes the launch)

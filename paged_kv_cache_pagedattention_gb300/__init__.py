@@ -9,7 +9,10 @@ not been built (``python paged_kv_cache_pagedattention_gb300/build.py``).
 
 Cache tensors have shape ``[num_blocks][num_kv_heads][block_size][head_size]``;
 FP8 e4m3 caches are uint8 tensors of codes with per-tensor fp32 scales passed as
-one-element float32 CUDA tensors.
+one-element float32 CUDA tensors (one value per KV head selects per-head scales).
+NVFP4 caches are 3-D uint8 tensors ``[num_blocks][num_kv_heads][tile_bytes]``,
+``tile_bytes = 9 * block_size * head_size / 16`` (codes, then block scales; see
+``include/pa.h``); their head size is taken from the query or key tensor.
 """
 
 from __future__ import annotations
@@ -30,7 +33,8 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_BOUNDS, \
     PA_ERR_TIMEOUT, PA_ERR_CUDA = range(7)
-PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3, PA_FP8_E5M2, PA_FP8_E4M3_PER_HEAD, PA_FP8_E5M2_PER_HEAD = range(7)
+PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3, PA_FP8_E5M2, PA_FP8_E4M3_PER_HEAD, PA_FP8_E5M2_PER_HEAD, PA_NVFP4, \
+    PA_NVFP4_PER_HEAD = range(9)
 PA_ERRFLAG_BLOCK_TABLE, PA_ERRFLAG_SLOT, PA_ERRFLAG_SEQ_LEN, PA_ERRFLAG_QUERY, PA_ERRFLAG_TIMEOUT = \
     0x1, 0x2, 0x4, 0x8, 0x10
 
@@ -98,15 +102,36 @@ def dtype_code(t: torch.Tensor) -> int:
         raise TypeError(f"unsupported tensor dtype {t.dtype}") from None
 
 
+def is_nvfp4(cache: torch.Tensor) -> bool:
+    """NVFP4 caches are the 3-D uint8 tensors [num_blocks][num_kv_heads][tile_bytes]."""
+    return cache.dim() == 3 and cache.dtype == torch.uint8
+
+
 def kv_code(cache: torch.Tensor, k_scale=None) -> int:
-    """Cache dtype code; FP8 scales holding more than one value (one per KV head,
-    cache [num_blocks][num_kv_heads][block_size][head_size]) select the per-head format."""
-    code = dtype_code(cache)
-    if code in (PA_FP8_E4M3, PA_FP8_E5M2) and k_scale is not None and k_scale.numel() > 1:
+    """Cache dtype code; scales holding more than one value (one per KV head, the
+    cache's dimension 1) select the per-head format."""
+    code = PA_NVFP4 if is_nvfp4(cache) else dtype_code(cache)
+    if code in (PA_FP8_E4M3, PA_FP8_E5M2, PA_NVFP4) and k_scale is not None and k_scale.numel() > 1:
         if k_scale.numel() != cache.shape[1]:
-            raise ValueError("FP8 scales: one per tensor or one per KV head")
-        return PA_FP8_E4M3_PER_HEAD if code == PA_FP8_E4M3 else PA_FP8_E5M2_PER_HEAD
+            raise ValueError("scales: one per tensor or one per KV head")
+        return {PA_FP8_E4M3: PA_FP8_E4M3_PER_HEAD, PA_FP8_E5M2: PA_FP8_E5M2_PER_HEAD,
+                PA_NVFP4: PA_NVFP4_PER_HEAD}[code]
     return code
+
+
+def cache_geometry(k_cache: torch.Tensor, v_cache: torch.Tensor, head_size: int):
+    """(num_blocks, num_kv_heads, block_size, head_size) of a K/V cache pair; the
+    head size of an NVFP4 cache comes from the caller's query or key tensor."""
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or v_cache.dtype != k_cache.dtype:
+        raise ValueError("k_cache and v_cache must match")
+    if is_nvfp4(k_cache):
+        nb, hkv, tile = k_cache.shape
+        if head_size < 1 or (16 * tile) % (9 * head_size):
+            raise ValueError("NVFP4 cache: tile_bytes must be 9 * block_size * head_size / 16")
+        return nb, hkv, 16 * tile // (9 * head_size), head_size
+    if k_cache.dim() != 4:
+        raise ValueError("cache must be [num_blocks][num_kv_heads][block_size][head_size]")
+    return tuple(k_cache.shape)
 
 
 def _ptr(t) -> int | None:
@@ -135,9 +160,7 @@ def pa_version() -> int:
 def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, k_scale=None, v_scale=None,
                          stream=None) -> None:
     """Write key/value [T][Hkv][d] into the paged caches at slot_mapping (int64 [T])."""
-    nb, hkv, bs, d = k_cache.shape
-    if tuple(v_cache.shape) != tuple(k_cache.shape) or v_cache.dtype != k_cache.dtype:
-        raise ValueError("k_cache and v_cache must match")
+    nb, hkv, bs, d = cache_geometry(k_cache, v_cache, key.shape[-1])
     if key.dim() != 3 or tuple(key.shape[1:]) != (hkv, d) or key.shape != value.shape:
         raise ValueError("key/value must be [num_tokens][num_kv_heads][head_size]")
     if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != key.shape[0]:
@@ -150,16 +173,19 @@ def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, k_scale=Non
 
 def pa_copy_blocks(k_cache, v_cache, block_mapping, stream=None) -> None:
     """Copy whole physical blocks: block_mapping is int64 [num_pairs][2] of (src, dst)."""
-    nb, hkv, bs, d = k_cache.shape
-    if tuple(v_cache.shape) != tuple(k_cache.shape) or v_cache.dtype != k_cache.dtype:
-        raise ValueError("k_cache and v_cache must match")
+    if is_nvfp4(k_cache):
+        # only the tile size matters for a copy: any (block_size, head_size) with
+        # 9 * block_size * head_size / 16 == tile_bytes names it
+        nb, hkv, bs, d = cache_geometry(k_cache, v_cache, k_cache.shape[2] // 9)
+    else:
+        nb, hkv, bs, d = cache_geometry(k_cache, v_cache, 0)
     if block_mapping.dtype != torch.int64 or block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
         raise ValueError("block_mapping must be int64 [num_pairs][2]")
     if not block_mapping.is_contiguous():
         raise ValueError("block_mapping must be contiguous")
     n = block_mapping.shape[0]
     _check(_lib.pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_mapping) if n else None, n, nb, hkv, d,
-                               bs, dtype_code(k_cache), _stream(stream)), "pa_copy_blocks")
+                               bs, kv_code(k_cache), _stream(stream)), "pa_copy_blocks")
 
 
 def pa_default_partition_size(num_seqs, num_kv_heads, max_seq_len, block_size) -> int:
@@ -176,7 +202,7 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, sca
               k_scale=None, v_scale=None, partition_size=0, stream=None, window=0) -> None:
     """PagedAttention decode; out/q [B][Hq][d], block_tables int32 [B][max_blocks], seq_lens int32 [B].
     window > 0: sliding-window attention (pa_decode_windowed)."""
-    nb, hkv, bs, d = k_cache.shape
+    nb, hkv, bs, d = cache_geometry(k_cache, v_cache, q.shape[-1])
     b, hq = q.shape[0], q.shape[1]
     if q.dim() != 3 or q.shape[2] != d or out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("q/out must be [num_seqs][num_q_heads][head_size] of one dtype")
@@ -203,7 +229,7 @@ def pa_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, seq_lens, ma
     """pa_decode where groups of consecutive sequences share leading blocks.
 
     group_start int32 [G+1] (device), group_shared_blocks int32 [G] (device)."""
-    nb, hkv, bs, d = k_cache.shape
+    nb, hkv, bs, d = cache_geometry(k_cache, v_cache, q.shape[-1])
     b, hq = q.shape[0], q.shape[1]
     if q.dim() != 3 or q.shape[2] != d or out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("q/out must be [num_seqs][num_q_heads][head_size] of one dtype")
@@ -225,7 +251,7 @@ def pa_decode_static_workspace(out, q, k_cache, v_cache, block_tables, seq_lens,
                                k_scale=None, v_scale=None, partition_size=0, stream=None) -> None:
     """pa_decode with the library's fixed scratch array instead of a workspace: for
     callers that cannot allocate device memory where attention runs.  See pa.h."""
-    nb, hkv, bs, d = k_cache.shape
+    nb, hkv, bs, d = cache_geometry(k_cache, v_cache, q.shape[-1])
     b, hq = q.shape[0], q.shape[1]
     if q.dim() != 3 or q.shape[2] != d or out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("q/out must be [num_seqs][num_q_heads][head_size] of one dtype")
@@ -252,7 +278,7 @@ def pa_varlen_attn(out, q, k_cache, v_cache, block_tables, query_start_loc, seq_
                    partition_size=0, stream=None, window=0) -> None:
     """Attention of a flattened varlen batch; out/q [T][Hq][d], query_start_loc int32 [B+1].
     window > 0: sliding-window attention (pa_varlen_attn_windowed)."""
-    nb, hkv, bs, d = k_cache.shape
+    nb, hkv, bs, d = cache_geometry(k_cache, v_cache, q.shape[-1])
     t, hq = q.shape[0], q.shape[1]
     b = seq_lens.numel()
     if q.dim() != 3 or q.shape[2] != d or out.shape != q.shape or out.dtype != q.dtype:

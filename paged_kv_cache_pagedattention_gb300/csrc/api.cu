@@ -68,14 +68,31 @@ int dtype_bytes(int dt) {
   }
 }
 
-// FP8 formats with one scale per KV head are the base format with a scale stride
-// of 1 (the kernels read the scale of KV head h at scale[h * stride]).
+// Scaled formats with one scale per KV head are the base format with a scale
+// stride of 1 (the kernels read the scale of KV head h at scale[h * stride]).
 pa_dtype base_dtype(pa_dtype dt) {
   if (dt == PA_FP8_E4M3_PER_HEAD) return PA_FP8_E4M3;
   if (dt == PA_FP8_E5M2_PER_HEAD) return PA_FP8_E5M2;
+  if (dt == PA_NVFP4_PER_HEAD) return PA_NVFP4;
   return dt;
 }
-int scale_stride_of(pa_dtype dt) { return dt == PA_FP8_E4M3_PER_HEAD || dt == PA_FP8_E5M2_PER_HEAD ? 1 : 0; }
+int scale_stride_of(pa_dtype dt) {
+  return dt == PA_FP8_E4M3_PER_HEAD || dt == PA_FP8_E5M2_PER_HEAD || dt == PA_NVFP4_PER_HEAD ? 1 : 0;
+}
+
+// Cache formats (after base_dtype) whose values carry fp32 scales.
+bool scaled_dtype(pa_dtype dt) { return dt == PA_FP8_E4M3 || dt == PA_FP8_E5M2 || dt == PA_NVFP4; }
+
+// NVFP4 tiles: whole 16-element groups per row and whole 16-byte pieces per tile.
+bool nvfp4_shape_ok(int head_size, int block_size) {
+  return head_size % 16 == 0 && ((long long)block_size * head_size) % 256 == 0;
+}
+
+// Bytes of one (block, KV head) tile of a cache.
+long long tile_bytes(pa_dtype dt, int block_size, int head_size) {
+  if (dt == PA_NVFP4) return pa::nvfp4_tile_bytes(block_size, head_size);
+  return (long long)block_size * head_size * dtype_bytes(dt);
+}
 
 // ------------------------------------------------------------------ partitions
 
@@ -226,6 +243,19 @@ bool encode_cache_map(CUtensorMap* m, const void* base, int kv_dtype, int num_bl
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor maps of the K and V caches for the tensor-core kernels.  NVFP4 tiles are
+// moved with 1-D bulk copies; their maps are zeroed and never read.
+bool cache_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k_cache, const void* v_cache, int kv_dtype,
+                int num_blocks, int hkv, int bs, int d) {
+  if (kv_dtype == PA_NVFP4) {
+    memset(tk, 0, sizeof(*tk));
+    memset(tv, 0, sizeof(*tv));
+    return true;
+  }
+  return encode_cache_map(tk, k_cache, kv_dtype, num_blocks, hkv, bs, d) &&
+         encode_cache_map(tv, v_cache, kv_dtype, num_blocks, hkv, bs, d);
+}
+
 // ------------------------------------------------------------------ tracing
 
 constexpr int kTraceKinds = 8;
@@ -333,9 +363,10 @@ pa_status check_attention_args(const void* out, const void* q, const void* k_cac
   if (num_q_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
   if (partition_size < 0 || (partition_size > 0 && partition_size % block_size)) return PA_ERR_INVALID_ARG;
   if (q_dtype != PA_F32 && q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-  const bool kv_fp8 = kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_FP8_E5M2;
-  if (kv_dtype != q_dtype && !kv_fp8) return PA_ERR_UNSUPPORTED;
-  if (kv_fp8 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+  const bool kv_scaled = scaled_dtype(kv_dtype);
+  if (kv_dtype != q_dtype && !kv_scaled) return PA_ERR_UNSUPPORTED;
+  if (kv_scaled && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+  if (kv_dtype == PA_NVFP4 && !nvfp4_shape_ok(head_size, block_size)) return PA_ERR_UNSUPPORTED;
   if (head_size > 256) return PA_ERR_UNSUPPORTED;
   if (num_kv_heads * ((num_q_heads / num_kv_heads + 7) / 8) > 65535) return PA_ERR_UNSUPPORTED;
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return PA_ERR_INVALID_ARG;
@@ -405,10 +436,11 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
   if (num_tokens == 0) return PA_OK;
   if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
   if (src_dtype != PA_F32 && src_dtype != PA_F16 && src_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-  const bool cache_fp8 = cache_dtype == PA_FP8_E4M3 || cache_dtype == PA_FP8_E5M2;
-  if (cache_dtype != src_dtype && !cache_fp8) return PA_ERR_UNSUPPORTED;
-  if (cache_fp8 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
-  if ((head_size * dtype_bytes(src_dtype)) % 16 || (head_size * dtype_bytes(cache_dtype)) % 16)
+  const bool cache_scaled = scaled_dtype(cache_dtype);
+  if (cache_dtype != src_dtype && !cache_scaled) return PA_ERR_UNSUPPORTED;
+  if (cache_scaled && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+  if ((head_size * dtype_bytes(src_dtype)) % 16) return PA_ERR_UNSUPPORTED;
+  if (cache_dtype == PA_NVFP4 ? !nvfp4_shape_ok(head_size, block_size) : (head_size * dtype_bytes(cache_dtype)) % 16)
     return PA_ERR_UNSUPPORTED;
   if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
     return PA_ERR_INVALID_ARG;
@@ -439,9 +471,14 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapp
     return PA_ERR_INVALID_ARG;
   if (num_pairs == 0) return PA_OK;
   if (!k_cache || !v_cache || !block_mapping) return PA_ERR_INVALID_ARG;
-  const int eb = dtype_bytes(cache_dtype);
-  if (eb == 0) return PA_ERR_UNSUPPORTED;
-  if ((head_size * eb) % 16) return PA_ERR_UNSUPPORTED;
+  cache_dtype = base_dtype(cache_dtype);
+  if (cache_dtype == PA_NVFP4) {
+    if (!nvfp4_shape_ok(head_size, block_size)) return PA_ERR_UNSUPPORTED;
+  } else {
+    const int eb = dtype_bytes(cache_dtype);
+    if (eb == 0) return PA_ERR_UNSUPPORTED;
+    if ((head_size * eb) % 16) return PA_ERR_UNSUPPORTED;
+  }
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return PA_ERR_INVALID_ARG;
   pa::CopyParams p;
   p.k_cache = k_cache;
@@ -450,7 +487,7 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapp
   p.err = error_word();
   p.num_pairs = num_pairs;
   p.num_blocks = num_blocks;
-  p.block_bytes = (long long)num_kv_heads * block_size * head_size * eb;
+  p.block_bytes = (long long)num_kv_heads * tile_bytes(cache_dtype, block_size, head_size);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   TraceScope t(7, s);
   return cuda_status(pa::launch_copy_blocks(p, s));
@@ -518,8 +555,7 @@ pa_status pa_decode_windowed(void* out, const void* q, const void* k_cache, cons
   cudaError_t e;
   if (pa::decode_mma_supported(q_dtype, kv_dtype, head_size, block_size, p.group)) {
     CUtensorMap tk, tv;
-    if (!encode_cache_map(&tk, k_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size) ||
-        !encode_cache_map(&tv, v_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size))
+    if (!cache_maps(&tk, &tv, k_cache, v_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size))
       return PA_ERR_CUDA;
     TraceScope t(1, s);
     e = pa::launch_decode_mma(p, q_dtype, kv_dtype, grid_z, &tk, &tv, s);
@@ -591,8 +627,7 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
   p.max_group_size = max_group_size;
   p.force_partials = 1;
   CUtensorMap tk, tv;
-  if (!encode_cache_map(&tk, k_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size) ||
-      !encode_cache_map(&tv, v_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size))
+  if (!cache_maps(&tk, &tv, k_cache, v_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size))
     return PA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
@@ -606,7 +641,7 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
       s2 = side->stream;
     {
       TraceScope t(5, s);
-      e = (kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_FP8_E5M2)
+      e = scaled_dtype(kv_dtype)
               ? pa::launch_shared_prefix(p, q_dtype, kv_dtype, static_cast<int>(L.parts_shared), &tk, &tv, s)
               : pa::launch_shared_prefix_tiles(p, q_dtype, static_cast<int>(L.parts_shared), &tk, &tv, s);
     }
@@ -711,8 +746,7 @@ pa_status pa_varlen_attn_windowed(void* out, const void* q, const void* k_cache,
   CUtensorMap tk, tv, tk1;
   const bool prefill_tiles = fast_prefill && max_query_len > 1;
   if (fast_decode || prefill_tiles) {
-    if (!encode_cache_map(&tk, k_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size) ||
-        !encode_cache_map(&tv, v_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size))
+    if (!cache_maps(&tk, &tv, k_cache, v_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size))
       return PA_ERR_CUDA;
   }
   if (prefill_tiles &&

@@ -32,10 +32,13 @@
 // P^T comes from the S^T accumulators through movmatrix (an in-register 8x8
 // transpose).  The softmax runs on the accumulators in fp32 with a running max per
 // head (log2 units), sums l from the same rounded P that feeds the MMA, and
-// rescales O when the max grows.  FP8 e4m3 tiles are converted to f16 exactly
-// (cvt e4m3x2 -> f16x2) in registers; the per-tensor scales are folded into the
-// score multiplier (k_scale) and the output (v_scale); q is scaled by a power of
-// two per head so that it fits f16 exactly.
+// rescales O when the max grows.  FP8 tiles are converted to f16 exactly (cvt
+// e4m3x2 / e5m2x2 -> f16x2) in registers; NVFP4 tiles (E2M1 codes + E4M3 block
+// scales, copied whole with one 1-D bulk copy each) are converted code pair by code
+// pair (cvt e2m1x2 -> f16x2) and multiplied by their block scale in f16, which is
+// exact (at most 6 significant bits, magnitudes within f16's normal range).  The
+// fp32 scales are folded into the score multiplier (k_scale) and the output
+// (v_scale); q is scaled by a power of two per head so that it fits f16 exactly.
 #include "pa_common.cuh"
 
 namespace pa {
@@ -51,15 +54,20 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 template <int KVDT, int HEAD, int BS>
 struct DecodeGeom {
   static constexpr bool kFp8 = is_fp8<KVDT>();
+  static constexpr bool kFp4 = is_nvfp4<KVDT>();
+  static constexpr bool kScaled = kFp8 || kFp4;  // f16 MMAs on converted codes
   static constexpr int kElemBytes = kFp8 ? 1 : 2;
-  static constexpr int kRowBytes = HEAD * kElemBytes;  // one token of one head
-  static constexpr int kTileBytes = BS * kRowBytes;
+  // code bytes of one token of one head; NVFP4 block scales follow the code rows
+  static constexpr int kRowBytes = kFp4 ? HEAD / 2 : HEAD * kElemBytes;
+  static constexpr int kCodeBytes = BS * kRowBytes;
+  static constexpr int kTileBytes = kFp4 ? nvfp4_tile_bytes(BS, HEAD) : kCodeBytes;
   static constexpr int kMTiles = BS / 16;
   static constexpr int kKSteps = HEAD / 16;
   static constexpr int kDTiles = HEAD / 16;
-  static constexpr int kStages = kTileBytes <= 4096 ? 3 : 2;       // per-warp ring (decode)
-  static constexpr int kSharedStages = kTileBytes <= 4096 ? 6 : 4;  // CTA ring (shared prefix)
-  static_assert(kRowBytes % 128 == 0, "token rows must be whole 128-byte rows");
+  static constexpr int kStages = kFp4 ? 4 : kTileBytes <= 4096 ? 3 : 2;  // per-warp ring (decode)
+  static constexpr int kSharedStages = kTileBytes <= 4096 ? 6 : 4;       // CTA ring (shared prefix)
+  static_assert(kFp4 ? HEAD == 128 : kRowBytes % 128 == 0, "token rows must be whole 128-byte rows");
+  static_assert(kTileBytes % 16 == 0, "tiles are whole 16-byte pieces");
   // byte offset of 16-byte chunk `chunk` of token `tok` inside a tile
   static __device__ __forceinline__ uint32_t off(int tok, int chunk) {
     return static_cast<uint32_t>((chunk >> 3) * BS * 128) + swz128(tok, chunk & 7);
@@ -92,7 +100,7 @@ __device__ __forceinline__ void load_query(const AttnParams& p, long long row, i
   const float base_c = p.scale * kLog2e;
   const typename QE::T* qrow =
       reinterpret_cast<const typename QE::T*>(p.q) + (row * p.num_q_heads + h0 + qn) * HEAD;
-  if constexpr (!is_fp8<KVDT>()) {
+  if constexpr (!is_scaled<KVDT>()) {
     const uint32_t* qw = reinterpret_cast<const uint32_t*>(qrow);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
@@ -136,7 +144,8 @@ __device__ __forceinline__ void attend_block(const uint8_t* tile, int rem, int l
                                              float cA, float cB, WarpState<HEAD>& w) {
   using G = DecodeGeom<KVDT, HEAD, BS>;
   constexpr bool kFp8 = G::kFp8;
-  constexpr int MDT = kFp8 ? PA_F16 : QDT;
+  constexpr bool kFp4 = G::kFp4;
+  constexpr int MDT = G::kScaled ? PA_F16 : QDT;
   constexpr int TB = G::kTileBytes;
   const int lane = threadIdx.x & 31, qq = lane & 3;
   const uint32_t kbase = smem_u32(tile);
@@ -148,7 +157,36 @@ __device__ __forceinline__ void attend_block(const uint8_t* tile, int rem, int l
   for (int mt = 0; mt < G::kMTiles; ++mt) {
     float sc2[4] = {0.f, 0.f, 0.f, 0.f};  // second, independent accumulation chain
     sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
-    if constexpr (!kFp8) {
+    if constexpr (kFp4) {
+      // rows tA, tB; this thread's 32 dims 32qq .. 32qq+31 are 16 code bytes (k-step ks:
+      // bytes 2ks, 2ks+1 = dims 32qq + 4ks + 0..3) and block scales 2qq (ks < 4), 2qq+1
+      const int tA = 16 * mt + (lane >> 2), tB = tA + 8;
+      const uint4 ka = *reinterpret_cast<const uint4*>(tile + tA * G::kRowBytes + 16 * qq);
+      const uint4 kb = *reinterpret_cast<const uint4*>(tile + tB * G::kRowBytes + 16 * qq);
+      const uint32_t sa = fp8x2_to_f16x2<PA_FP8_E4M3>(
+          *reinterpret_cast<const uint16_t*>(tile + G::kCodeBytes + tA * (HEAD / 16) + 2 * qq));
+      const uint32_t sb = fp8x2_to_f16x2<PA_FP8_E4M3>(
+          *reinterpret_cast<const uint16_t*>(tile + G::kCodeBytes + tB * (HEAD / 16) + 2 * qq));
+      const uint32_t sa0 = __byte_perm(sa, 0, 0x1010), sa1 = __byte_perm(sa, 0, 0x3232);
+      const uint32_t sb0 = __byte_perm(sb, 0, 0x1010), sb1 = __byte_perm(sb, 0, 0x3232);
+      const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w};
+      const uint32_t wb[4] = {kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+      for (int wi = 0; wi < 4; ++wi) {  // word wi: bytes 4wi .. 4wi+3 = k-steps 2wi, 2wi+1
+        uint32_t fa[4], fb[4];
+        fp4x8_to_f16x2x4(wa[wi], fa);
+        fp4x8_to_f16x2x4(wb[wi], fb);
+        const uint32_t scA = wi < 2 ? sa0 : sa1, scB = wi < 2 ? sb0 : sb1;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int ks = 2 * wi + h;
+          const uint32_t a0 = hmul2_u32(fa[2 * h], scA), a2 = hmul2_u32(fa[2 * h + 1], scA);
+          const uint32_t a1 = hmul2_u32(fb[2 * h], scB), a3 = hmul2_u32(fb[2 * h + 1], scB);
+          if (h) mma_16816<PA_F16>(sc2, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+          else mma_16816<PA_F16>(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+        }
+      }
+    } else if constexpr (!kFp8) {
 #pragma unroll
       for (int ks = 0; ks < G::kKSteps; ++ks) {
         const int tok = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
@@ -168,10 +206,9 @@ __device__ __forceinline__ void attend_block(const uint8_t* tile, int rem, int l
       const uint32_t wb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
 #pragma unroll
       for (int ks = 0; ks < G::kKSteps; ++ks) {
-        const uint32_t a0 = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(wa[ks] & 0xffffu));
-        const uint32_t a2 = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(wa[ks] >> 16));
-        const uint32_t a1 = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(wb[ks] & 0xffffu));
-        const uint32_t a3 = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(wb[ks] >> 16));
+        uint32_t a0, a1, a2, a3;
+        fp8x4_to_f16x2x2<KVDT>(wa[ks], a0, a2);
+        fp8x4_to_f16x2x2<KVDT>(wb[ks], a1, a3);
         if (ks & 1) mma_16816<PA_F16>(sc2, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
         else mma_16816<PA_F16>(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
       }
@@ -240,7 +277,53 @@ __device__ __forceinline__ void attend_block(const uint8_t* tile, int rem, int l
   const bool tail = rem < BS;
 #pragma unroll
   for (int kt = 0; kt < G::kMTiles; ++kt) {
-    if constexpr (!kFp8) {
+    if constexpr (kFp4) {
+      // this thread owns dims 16*(lane>>2) .. +15 (one block-scale group) of tokens
+      // 16kt + {2qq, 2qq+1, 2qq+8, 2qq+9}: 8 code bytes per token.  Odd quads read the
+      // second token of each pair first, so that one load instruction touches rows
+      // 0, 3, 4, 7 (or 1, 2, 5, 6) of eight: two 64-byte rows per 128-byte bank line.
+      const int rr = lane >> 2;
+      const uint8_t* vt = tile + TB;
+      const int tk = 16 * kt + 2 * qq;
+      const int odd = qq & 1;
+      uint2 v0 = *reinterpret_cast<const uint2*>(vt + (tk + odd) * G::kRowBytes + 8 * rr);
+      uint2 v1 = *reinterpret_cast<const uint2*>(vt + (tk + 1 - odd) * G::kRowBytes + 8 * rr);
+      uint2 v2 = *reinterpret_cast<const uint2*>(vt + (tk + 8 + odd) * G::kRowBytes + 8 * rr);
+      uint2 v3 = *reinterpret_cast<const uint2*>(vt + (tk + 9 - odd) * G::kRowBytes + 8 * rr);
+      const uint8_t* vs = vt + G::kCodeBytes + rr;
+      uint32_t s01 = vs[tk * (HEAD / 16)] | (static_cast<uint32_t>(vs[(tk + 1) * (HEAD / 16)]) << 8);
+      uint32_t s89 = vs[(tk + 8) * (HEAD / 16)] | (static_cast<uint32_t>(vs[(tk + 9) * (HEAD / 16)]) << 8);
+      if (tail) {  // tokens past the end: zero codes and zero scales
+        if (tk + odd >= rem) v0 = make_uint2(0, 0);
+        if (tk + 1 - odd >= rem) v1 = make_uint2(0, 0);
+        if (tk + 8 + odd >= rem) v2 = make_uint2(0, 0);
+        if (tk + 9 - odd >= rem) v3 = make_uint2(0, 0);
+        if (tk >= rem) s01 &= 0xff00u;
+        if (tk + 1 >= rem) s01 &= 0x00ffu;
+        if (tk + 8 >= rem) s89 &= 0xff00u;
+        if (tk + 9 >= rem) s89 &= 0x00ffu;
+      }
+      const uint32_t f01 = fp8x2_to_f16x2<PA_FP8_E4M3>(static_cast<uint16_t>(s01));  // (token tk, tk+1)
+      const uint32_t f89 = fp8x2_to_f16x2<PA_FP8_E4M3>(static_cast<uint16_t>(s89));
+      // (first-read, second-read) -> (token tk, token tk+1) halves
+      const uint32_t sel_lo = odd ? 0x1054u : 0x5410u, sel_hi = odd ? 0x3276u : 0x7632u;
+#pragma unroll
+      for (int wi = 0; wi < 2; ++wi) {  // word wi of each token: bytes 4wi .. 4wi+3 = d-tiles 4wi ..
+        uint32_t x0[4], y0[4], x1[4], y1[4];
+        fp4x8_to_f16x2x4(wi ? v0.y : v0.x, x0);
+        fp4x8_to_f16x2x4(wi ? v1.y : v1.x, y0);
+        fp4x8_to_f16x2x4(wi ? v2.y : v2.x, x1);
+        fp4x8_to_f16x2x4(wi ? v3.y : v3.x, y1);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t a0 = hmul2_u32(__byte_perm(x0[j], y0[j], sel_lo), f01);
+          const uint32_t a1 = hmul2_u32(__byte_perm(x0[j], y0[j], sel_hi), f01);
+          const uint32_t a2 = hmul2_u32(__byte_perm(x1[j], y1[j], sel_lo), f89);
+          const uint32_t a3 = hmul2_u32(__byte_perm(x1[j], y1[j], sel_hi), f89);
+          mma_16816<PA_F16>(w.acc[4 * wi + j], a0, a1, a2, a3, pb[kt][0], pb[kt][1]);
+        }
+      }
+    } else if constexpr (!kFp8) {
       const int tk = 16 * kt + 2 * qq;  // tokens of this thread's A halves: tk, tk+1, tk+8, tk+9
       const uint32_t m01 = (tk < rem ? 0xffffu : 0u) | (tk + 1 < rem ? 0xffff0000u : 0u);
       const uint32_t m23 = (tk + 8 < rem ? 0xffffu : 0u) | (tk + 9 < rem ? 0xffff0000u : 0u);
@@ -279,26 +362,45 @@ __device__ __forceinline__ void attend_block(const uint8_t* tile, int rem, int l
       const uint32_t w2[4] = {v[2].x, v[2].y, v[2].z, v[2].w};
       const uint32_t w3[4] = {v[3].x, v[3].y, v[3].z, v[3].w};
 #pragma unroll
-      for (int dt = 0; dt < G::kDTiles; ++dt) {
-        const int sh = 16 * (dt & 1);
-        const uint32_t x0 = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(w0[dt >> 1] >> sh));
-        const uint32_t y0 = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(w1[dt >> 1] >> sh));
-        const uint32_t x1 = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(w2[dt >> 1] >> sh));
-        const uint32_t y1 = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(w3[dt >> 1] >> sh));
-        const uint32_t a0 = __byte_perm(x0, y0, 0x5410), a1 = __byte_perm(x0, y0, 0x7632);
-        const uint32_t a2 = __byte_perm(x1, y1, 0x5410), a3 = __byte_perm(x1, y1, 0x7632);
-        mma_16816<PA_F16>(w.acc[dt], a0, a1, a2, a3, pb[kt][0], pb[kt][1]);
+      for (int k = 0; k < 4; ++k) {  // word k: dims 16rr + 4k .. +3 = d-tiles 2k, 2k+1
+        // byte-interleave the token pairs: 16-bit halves = (token t, token t+1) of one dim
+        uint32_t c01[4], c89[4];
+        fp8x4_to_f16x2x2<KVDT>(__byte_perm(w0[k], w1[k], 0x5140), c01[0], c01[1]);
+        fp8x4_to_f16x2x2<KVDT>(__byte_perm(w0[k], w1[k], 0x7362), c01[2], c01[3]);
+        fp8x4_to_f16x2x2<KVDT>(__byte_perm(w2[k], w3[k], 0x5140), c89[0], c89[1]);
+        fp8x4_to_f16x2x2<KVDT>(__byte_perm(w2[k], w3[k], 0x7362), c89[2], c89[3]);
+        mma_16816<PA_F16>(w.acc[2 * k], c01[0], c01[1], c89[0], c89[1], pb[kt][0], pb[kt][1]);
+        mma_16816<PA_F16>(w.acc[2 * k + 1], c01[2], c01[3], c89[2], c89[3], pb[kt][0], pb[kt][1]);
       }
     }
   }
 }
 
 // Output dimensions of accumulator elements 0/1 (dA) and 2/3 (dB) of d-tile dt.
-template <bool kFp8>
+template <bool kScaled>
 __device__ __forceinline__ void acc_dims(int dt, int lane, int& dA, int& dB) {
   const int rr = lane >> 2;
-  dA = kFp8 ? 16 * rr + 2 * dt : 16 * dt + rr;
-  dB = kFp8 ? dA + 1 : dA + 8;
+  dA = kScaled ? 16 * rr + 2 * dt : 16 * dt + rr;
+  dB = kScaled ? dA + 1 : dA + 8;
+}
+
+// Copies of the K and V tiles of (physical block phys, KV head kvh) into st and
+// st + tile bytes, completing on `bar`: tensor-map copies landing as swizzled
+// 128-byte pieces, or for NVFP4 one 1-D bulk copy per tile (read as laid out).
+template <int KVDT, int HEAD, int BS>
+__device__ __forceinline__ void load_kv_tiles(uint8_t* st, const AttnParams& p, const CUtensorMap* tmk,
+                                              const CUtensorMap* tmv, int kvh, int phys, uint64_t* bar) {
+  using G = DecodeGeom<KVDT, HEAD, BS>;
+  constexpr int TB = G::kTileBytes;
+  mbar_arrive_expect_tx(bar, 2 * TB);
+  if constexpr (G::kFp4) {
+    const long long off = ((long long)phys * p.num_kv_heads + kvh) * TB;
+    bulk_load(st, static_cast<const uint8_t*>(p.k_cache) + off, TB, bar);
+    bulk_load(st + TB, static_cast<const uint8_t*>(p.v_cache) + off, TB, bar);
+  } else {
+    tma_load_4d(st, tmk, 0, kvh * BS, 0, phys, bar);
+    tma_load_4d(st + TB, tmv, 0, kvh * BS, 0, phys, bar);
+  }
 }
 
 template <int KVDT, int HEAD, int BS, int NW>
@@ -313,7 +415,6 @@ __global__ void __launch_bounds__(NW * 32)
                       const __grid_constant__ CUtensorMap tmv) {
   using G = DecodeGeom<KVDT, HEAD, BS>;
   using QE = Elem<QDT>;
-  constexpr bool kFp8 = G::kFp8;
   constexpr int ST = G::kStages;
   constexpr int TB = G::kTileBytes;
 
@@ -366,8 +467,10 @@ __global__ void __launch_bounds__(NW * 32)
 
   if (threadIdx.x == 0) {
     s_failed = 0;
-    tma_prefetch_desc(&tmk);
-    tma_prefetch_desc(&tmv);
+    if constexpr (!G::kFp4) {
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+    }
     for (int i = 0; i < NW * ST; ++i) mbar_init(bars + i, 1);
     fence_mbar_init();
   }
@@ -378,7 +481,6 @@ __global__ void __launch_bounds__(NW * 32)
   uint8_t* ring = smem + warp * ST * 2 * TB;
   uint64_t* wbars = bars + warp * ST;
   int* wok = stage_ok + warp * ST;
-  const int tile_row0 = kvh * BS;
 
   // Block-table entries of this warp's blocks, 32 at a time in registers (lane l
   // holds the entry of the warp's block index base + l); the next window is loaded
@@ -399,10 +501,7 @@ __global__ void __launch_bounds__(NW * 32)
         flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
         mbar_arrive(wbars + s);  // completes the phase with no data; the block is skipped
       } else {
-        uint8_t* st = ring + s * 2 * TB;
-        mbar_arrive_expect_tx(wbars + s, 2 * TB);
-        tma_load_4d(st, &tmk, 0, tile_row0, 0, phys, wbars + s);
-        tma_load_4d(st + TB, &tmv, 0, tile_row0, 0, phys, wbars + s);
+        load_kv_tiles<KVDT, HEAD, BS>(ring + s * 2 * TB, p, &tmk, &tmv, kvh, phys, wbars + s);
       }
     }
   };
@@ -466,7 +565,7 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
     for (int dt = 0; dt < G::kDTiles; ++dt) {
       int dA, dB;
-      acc_dims<kFp8>(dt, lane, dA, dB);
+      acc_dims<G::kScaled>(dt, lane, dA, dB);
       red[(warp * 8 + 2 * qq) * HEAD + dA] = w.acc[dt][0];
       red[(warp * 8 + 2 * qq + 1) * HEAD + dA] = w.acc[dt][1];
       red[(warp * 8 + 2 * qq) * HEAD + dB] = w.acc[dt][2];
@@ -480,7 +579,7 @@ __global__ void __launch_bounds__(NW * 32)
     }
   }
   __syncthreads();
-  const float vscale = kFp8 ? p.v_scale[kvh * p.scale_stride] : 1.f;
+  const float vscale = G::kScaled ? p.v_scale[kvh * p.scale_stride] : 1.f;
   const long long pbase = p.part_off ? (long long)p.part_off[r] : (long long)row * p.max_partitions;
   const bool direct = nparts == 1 && !p.force_partials;
   for (int idx = threadIdx.x; idx < nh * HEAD; idx += NW * 32) {
@@ -528,7 +627,6 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32)
     shared_prefix_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv) {
   using G = DecodeGeom<KVDT, HEAD, BS>;
-  constexpr bool kFp8 = G::kFp8;
   constexpr int ST = G::kSharedStages;
   constexpr int TB = G::kTileBytes;
 
@@ -555,8 +653,10 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32)
   int* stage_ok = reinterpret_cast<int*>(empty + ST);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    tma_prefetch_desc(&tmk);
-    tma_prefetch_desc(&tmv);
+    if constexpr (!G::kFp4) {
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+    }
     for (int i = 0; i < ST; ++i) {
       mbar_init(full + i, 1);
       mbar_init(empty + i, nm);
@@ -586,10 +686,7 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32)
           flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
           mbar_arrive(full + s);  // empty phase: the members skip this block
         } else {
-          uint8_t* st = smem + s * 2 * TB;
-          mbar_arrive_expect_tx(full + s, 2 * TB);
-          tma_load_4d(st, &tmk, 0, kvh * BS, 0, phys, full + s);
-          tma_load_4d(st + TB, &tmv, 0, kvh * BS, 0, phys, full + s);
+          load_kv_tiles<KVDT, HEAD, BS>(smem + s * 2 * TB, p, &tmk, &tmv, kvh, phys, full + s);
         }
       }
     }
@@ -619,14 +716,14 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32)
   // ---- this member's partial state for partition z of its shared prefix
   w.lA = warp_sum_xor(w.lA, 4, 16);
   w.lB = warp_sum_xor(w.lB, 4, 16);
-  const float vscale = kFp8 ? p.v_scale[kvh * p.scale_stride] : 1.f;
+  const float vscale = G::kScaled ? p.v_scale[kvh * p.scale_stride] : 1.f;
   const long long pi = (long long)seq * p.max_partitions + z;
   const int qq = lane & 3;
   const int hA = 2 * qq, hB = 2 * qq + 1;
 #pragma unroll
   for (int dt = 0; dt < G::kDTiles; ++dt) {
     int dA, dB;
-    acc_dims<kFp8>(dt, lane, dA, dB);
+    acc_dims<G::kScaled>(dt, lane, dA, dB);
     if (hA < nh) {
       float* wa = p.ws_acc + (pi * p.num_q_heads + h0 + hA) * HEAD;
       wa[dA] = w.acc[dt][0] * vscale;
@@ -695,7 +792,7 @@ cudaError_t launch_shape(const AttnParams& p, int grid_z, const CUtensorMap* tk,
   if (d == D && bs == B)                                                   \
     return kShared ? launch_shared_t<QDT, KVDT, D, B>(p, grid_z, tk, tv, s) \
                    : launch_t<QDT, KVDT, D, B>(p, grid_z, tk, tv, s);
-  if constexpr (!is_fp8<KVDT>()) {
+  if constexpr (!is_scaled<KVDT>()) {
     PA_SHAPE(128, 16)
     PA_SHAPE(128, 32)
     PA_SHAPE(64, 16)
@@ -721,6 +818,8 @@ cudaError_t dispatch(const AttnParams& p, int q_dtype, int kv_dtype, int grid_z,
     return launch_shape<PA_BF16, PA_FP8_E5M2, kShared>(p, grid_z, tk, tv, s);
   if (q_dtype == PA_F16 && kv_dtype == PA_FP8_E5M2)
     return launch_shape<PA_F16, PA_FP8_E5M2, kShared>(p, grid_z, tk, tv, s);
+  if (q_dtype == PA_BF16 && kv_dtype == PA_NVFP4) return launch_shape<PA_BF16, PA_NVFP4, kShared>(p, grid_z, tk, tv, s);
+  if (q_dtype == PA_F16 && kv_dtype == PA_NVFP4) return launch_shape<PA_F16, PA_NVFP4, kShared>(p, grid_z, tk, tv, s);
   return cudaErrorInvalidValue;
 }
 
@@ -731,7 +830,7 @@ bool decode_mma_supported(int q_dtype, int kv_dtype, int head_size, int block_si
   const bool q16 = q_dtype == PA_BF16 || q_dtype == PA_F16;
   if (!q16) return false;
   if (kv_dtype == q_dtype) return (head_size == 64 || head_size == 128) && (block_size == 16 || block_size == 32);
-  if (kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_FP8_E5M2)
+  if (kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_FP8_E5M2 || kv_dtype == PA_NVFP4)
     return head_size == 128 && (block_size == 16 || block_size == 32);
   return false;
 }

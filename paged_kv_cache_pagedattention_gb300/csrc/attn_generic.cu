@@ -17,11 +17,22 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kGenericMaxPerLane = 8;  // head_size <= 256
 
+// Stored value (without the fp32 scale) of element dd of token row `off` of cache
+// tile `tile` (= physical block x Hkv + KV head).
+template <int KVDT>
+__device__ __forceinline__ float kv_elem(const void* cache, long long tile, int bs, int d, int off, int dd) {
+  if constexpr (is_nvfp4<KVDT>()) {
+    return nvfp4_elem(static_cast<const uint8_t*>(cache) + tile * nvfp4_tile_bytes(bs, d), bs, d, off, dd);
+  } else {
+    using KE = Elem<KVDT>;
+    return KE::load(static_cast<const typename KE::T*>(cache) + (tile * bs + off) * d + dd);
+  }
+}
+
 template <int QDT, int KVDT>
 __global__ void __launch_bounds__(128)
     attn_generic_kernel(const AttnParams p, int only_multi_token) {
   using QE = Elem<QDT>;
-  using KE = Elem<KVDT>;
   const int lane = threadIdx.x & 31;
   const int head = blockIdx.y * 4 + (threadIdx.x >> 5);
   const int row = blockIdx.x;
@@ -44,7 +55,7 @@ __global__ void __launch_bounds__(128)
   const int t0 = ri.origin + z * ri.part;  // partition z of the row's keys
   const int t1 = min(t0 + ri.part, ri.kv_len);
   float kscale = 1.f, vscale = 1.f;
-  if (is_fp8<KVDT>()) {
+  if (is_scaled<KVDT>()) {
     kscale = p.k_scale[kvh * p.scale_stride];
     vscale = p.v_scale[kvh * p.scale_stride];
   }
@@ -59,8 +70,6 @@ __global__ void __launch_bounds__(128)
     qv[i] = dd < d ? QE::load(qrow + dd) : 0.f;
     acc[i] = 0.f;
   }
-  const typename KE::T* kc = reinterpret_cast<const typename KE::T*>(p.k_cache);
-  const typename KE::T* vc = reinterpret_cast<const typename KE::T*>(p.v_cache);
   const int32_t* table = p.block_tables + (long long)ri.request * p.max_blocks_per_seq;
   float m = -INFINITY, l = 0.f;
   for (int t = max(t0, ri.lo); t < t1; ++t) {  // keys before the window are not read
@@ -69,13 +78,13 @@ __global__ void __launch_bounds__(128)
       if (lane == 0) flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
       continue;
     }
-    const long long base =
-        (((long long)phys * p.num_kv_heads + kvh) * p.block_size + (t % p.block_size)) * d;
+    const long long tile = (long long)phys * p.num_kv_heads + kvh;
+    const int off = t % p.block_size;
     float dot = 0.f;
 #pragma unroll
     for (int i = 0; i < kGenericMaxPerLane; ++i) {
       const int dd = lane + 32 * i;
-      if (dd < d) dot = fmaf(qv[i], KE::load(kc + base + dd), dot);
+      if (dd < d) dot = fmaf(qv[i], kv_elem<KVDT>(p.k_cache, tile, p.block_size, d, off, dd), dot);
     }
     dot = warp_sum_xor(dot, 1, 16);
     const float s = dot * c;
@@ -86,7 +95,7 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int i = 0; i < kGenericMaxPerLane; ++i) {
       const int dd = lane + 32 * i;
-      if (dd < d) acc[i] = fmaf(w, KE::load(vc + base + dd), acc[i] * alpha);
+      if (dd < d) acc[i] = fmaf(w, kv_elem<KVDT>(p.v_cache, tile, p.block_size, d, off, dd), acc[i] * alpha);
     }
     m = m_new;
   }
@@ -438,6 +447,9 @@ cudaError_t launch_attn_generic(const AttnParams& p, int q_dtype, int kv_dtype, 
   PA_GEN(PA_F16, PA_FP8_E5M2)
   PA_GEN(PA_BF16, PA_FP8_E5M2)
   PA_GEN(PA_F32, PA_FP8_E5M2)
+  PA_GEN(PA_F16, PA_NVFP4)
+  PA_GEN(PA_BF16, PA_NVFP4)
+  PA_GEN(PA_F32, PA_NVFP4)
 #undef PA_GEN
   return cudaErrorInvalidValue;
 }

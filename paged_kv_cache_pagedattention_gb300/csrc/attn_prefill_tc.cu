@@ -470,10 +470,7 @@ __global__ void __launch_bounds__(threads_tc<is_fp8<KVDT>()>(), 1)
         const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
         uint32_t h[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          h[2 * e] = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(cw[e] & 0xffffu));
-          h[2 * e + 1] = fp8x2_to_f16x2<KVDT>(static_cast<uint16_t>(cw[e] >> 16));
-        }
+        for (int e = 0; e < 4; ++e) fp8x4_to_f16x2x2<KVDT>(cw[e], h[2 * e], h[2 * e + 1]);
         uint8_t* row = drow + (g >> 2) * piece_stride;
         const int cc = (2 * g) & 7;
         *reinterpret_cast<uint4*>(row + ((cc ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -61,6 +62,14 @@ struct Elem<PA_FP8_E5M2> {
 // FP8 cache formats (codes with a per-tensor scale).
 template <int DT>
 constexpr bool is_fp8() { return DT == PA_FP8_E4M3 || DT == PA_FP8_E5M2; }
+// NVFP4 cache format: per (block, KV head) tile, block_size rows of head/2 bytes of
+// E2M1 codes (element 2i in the low nibble of byte i), then block_size rows of
+// head/16 E4M3 block scales; values carry the fp32 scale as FP8 does.
+template <int DT>
+constexpr bool is_nvfp4() { return DT == PA_NVFP4; }
+// Cache formats whose values carry an fp32 scale (k_scale / v_scale).
+template <int DT>
+constexpr bool is_scaled() { return is_fp8<DT>() || is_nvfp4<DT>(); }
 
 __device__ __forceinline__ void flag_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);
@@ -248,6 +257,66 @@ __device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint16_t codes) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes),
                                              DT == PA_FP8_E5M2 ? __NV_E5M2 : __NV_E4M3);
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// Four FP8 codes (one 32-bit word) -> two f16 pairs: bytes 0, 1 -> lo, bytes 2, 3 ->
+// hi; exact.  The word is split into its 16-bit halves by the conversion's operand
+// unpack, not by shifts and masks.
+template <int DT>
+__device__ __forceinline__ void fp8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if constexpr (DT == PA_FP8_E5M2)
+    asm("{\n\t.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "cvt.rn.f16x2.e5m2x2 %0, h0;\n\tcvt.rn.f16x2.e5m2x2 %1, h1;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+  else
+    asm("{\n\t.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, h0;\n\tcvt.rn.f16x2.e4m3x2 %1, h1;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+// Eight E2M1 codes (one 32-bit word; byte j holds codes 2j in its low nibble and
+// 2j+1 in its high nibble) -> four f16 pairs r[j], exact (every E2M1 value is an
+// f16 value).
+__device__ __forceinline__ void fp4x8_to_f16x2x4(uint32_t w, uint32_t (&r)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(w));
+}
+
+// Elementwise product of two f16 pairs, rounded to nearest.
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Value of one stored element (without the fp32 scale) of a NVFP4 tile: code
+// element `dim` of token row `tok`, times its block scale.
+__device__ __forceinline__ float nvfp4_elem(const uint8_t* tile, int block_size, int head, int tok, int dim) {
+  const uint32_t byte = tile[tok * (head / 2) + (dim >> 1)];
+  const uint32_t sc = tile[block_size * head / 2 + tok * (head / 16) + (dim >> 4)];
+  const __half2_raw c = __nv_cvt_fp4x2_to_halfraw2(static_cast<__nv_fp4x2_storage_t>(byte), __NV_E2M1);
+  __half_raw v;
+  v.x = (dim & 1) ? c.y : c.x;
+  const __half_raw b = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sc), __NV_E4M3);
+  return __half2float(__half(v)) * __half2float(__half(b));
+}
+
+// 1-D bulk copy global -> shared of `bytes` bytes (a multiple of 16, both addresses
+// 16-byte aligned), completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // 2^x with the hardware approximation (MUFU); 2^-inf = +0.

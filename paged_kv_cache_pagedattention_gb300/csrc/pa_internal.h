@@ -11,13 +11,19 @@
 
 namespace pa {
 
+// Bytes of one (block, KV head) tile of an NVFP4 cache: block_size rows of head/2
+// bytes of E2M1 codes, then block_size rows of head/16 E4M3 block scales.
+__host__ __device__ constexpr int nvfp4_tile_bytes(int block_size, int head) {
+  return block_size * head / 2 + block_size * head / 16;
+}
+
 // Everything an attention kernel needs.  "Rows" are query rows: one per sequence
 // in decode mode (query_start_loc == nullptr), one per flattened query token in
 // varlen mode.
 struct AttnParams {
   void* out;                       // [num_rows][Hq][d], q dtype
   const void* q;                   // [num_rows][Hq][d], q dtype
-  const void* k_cache;             // [num_blocks][Hkv][bs][d]
+  const void* k_cache;             // [num_blocks][Hkv][bs][d] (NVFP4: [num_blocks][Hkv][tile bytes])
   const void* v_cache;
   const int32_t* block_tables;     // [num_seqs][max_blocks_per_seq]
   const int32_t* seq_lens;         // [num_seqs]
@@ -30,7 +36,7 @@ struct AttnParams {
   const int32_t* group_shared_blocks;  // shared-prefix decode: [num_groups] leading blocks shared in a group
   float* ws_acc;                   // [partial rows][Hq][d]  un-normalised weighted sums
   float2* ws_ml;                   // [partial rows][Hq]     (running max in log2 units, weight sum)
-  const float* k_scale;            // FP8 only: scale of KV head h at k_scale[h * scale_stride]
+  const float* k_scale;            // FP8 / NVFP4: scale of KV head h at k_scale[h * scale_stride]
   const float* v_scale;
   int scale_stride;                // 0: one scale per tensor, 1: one per KV head
   unsigned* err;                   // device error word
@@ -64,7 +70,7 @@ struct ScatterParams {
   void* k_cache;
   void* v_cache;
   const int64_t* slot_mapping;
-  const float* k_scale;  // FP8 only: scale of KV head h at k_scale[h * scale_stride]
+  const float* k_scale;  // FP8 / NVFP4: scale of KV head h at k_scale[h * scale_stride]
   const float* v_scale;
   int scale_stride;
   unsigned* err;

@@ -5,9 +5,10 @@
 // s % block_size; negative slots are padding.
 //
 // One thread moves one 16-byte piece of a destination row (same dtype: a straight
-// copy of 16 bytes; FP8: 16 codes quantised from 16 source elements).  Threads of a
-// warp cover consecutive pieces of consecutive rows, so both the source reads and
-// the destination writes are coalesced 16-byte accesses.
+// copy of 16 bytes; FP8: 16 codes quantised from 16 source elements; NVFP4: 16
+// elements into 8 code bytes and one block-scale byte).  Threads of a warp cover
+// consecutive pieces of consecutive rows, so the source reads and the destination
+// writes are coalesced.
 #include "pa_common.cuh"
 
 namespace pa {
@@ -90,6 +91,84 @@ __global__ void __launch_bounds__(256) scatter_fp8_kernel(const ScatterParams p)
   }
 }
 
+// E2M1 code of y: round to nearest with ties to the even code, saturating at 6,
+// sign kept.  The magnitude code counts the midpoints between neighbouring E2M1
+// magnitudes (0, 0.5, 1, 1.5, 2, 3, 4, 6) that |y| lies above; at a midpoint the
+// comparison is strict or not so that the tie lands on the even code.
+__device__ __forceinline__ uint32_t e2m1_code(float y) {
+  const float a = fabsf(y);
+  const uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) +
+                     (a > 5.0f);
+  return c | (signbit(y) ? 8u : 0u);
+}
+
+// NVFP4 quantisation of one group of 16 source elements with fp32 scale s: block
+// scale code e4m3(amax / (6 s)), codes e2m1(x / (s b)) packed low nibble first;
+// zero codes when the block scale is zero.
+template <int SRC>
+__device__ __forceinline__ void quant_nvfp4_group(const typename Elem<SRC>::T* src, float s, uint2& codes,
+                                                  uint8_t& scale) {
+  float x[16];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    x[i] = Elem<SRC>::load(src + i);
+    amax = fmaxf(amax, fabsf(x[i]));
+  }
+  const float q = __fdiv_rn(amax, __fmul_rn(6.0f, s));
+  scale = static_cast<uint8_t>(__nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3));
+  const float b = __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(scale), __NV_E4M3)));
+  uint32_t w[2] = {0u, 0u};
+  if (b != 0.f) {
+    const float den = __fmul_rn(s, b);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i >> 3] |= e2m1_code(__fdiv_rn(x[i], den)) << (4 * (i & 7));
+  }
+  codes = make_uint2(w[0], w[1]);
+}
+
+// One thread per group of 16 elements of a (token, head) row, K and V; consecutive
+// threads cover consecutive groups of a row, so the 8-byte code stores and the
+// scale bytes of a row are written side by side.
+template <int SRC>
+__global__ void __launch_bounds__(256) scatter_nvfp4_kernel(const ScatterParams p) {
+  using SE = Elem<SRC>;
+  const int d = p.head_size, bs = p.block_size;
+  const int groups = d / 16;
+  const long long per_token = (long long)p.num_kv_heads * groups;
+  const long long total = (long long)p.num_tokens * per_token;
+  const long long limit = (long long)p.num_blocks * bs;
+  const long long tile = nvfp4_tile_bytes(bs, d);
+  for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < total;
+       u += (long long)gridDim.x * blockDim.x) {
+    const long long t = u / per_token;
+    const int rem = static_cast<int>(u - t * per_token);
+    const int h = rem / groups, g = rem % groups;
+    const long long slot = p.slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= limit) {
+      flag_error(p.err, PA_ERRFLAG_SLOT);
+      continue;
+    }
+    const long long blk = slot / bs;
+    const int off = static_cast<int>(slot % bs);
+    const long long src = (t * p.num_kv_heads + h) * d + g * 16;
+    const long long tbase = (blk * p.num_kv_heads + h) * tile;
+    const long long code_at = tbase + off * (d / 2) + g * 8;
+    const long long scale_at = tbase + (long long)bs * (d / 2) + off * (d / 16) + g;
+    uint2 codes;
+    uint8_t sc;
+    quant_nvfp4_group<SRC>(reinterpret_cast<const typename SE::T*>(p.key) + src, p.k_scale[h * p.scale_stride],
+                           codes, sc);
+    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.k_cache) + code_at) = codes;
+    static_cast<uint8_t*>(p.k_cache)[scale_at] = sc;
+    quant_nvfp4_group<SRC>(reinterpret_cast<const typename SE::T*>(p.value) + src, p.v_scale[h * p.scale_stride],
+                           codes, sc);
+    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.v_cache) + code_at) = codes;
+    static_cast<uint8_t*>(p.v_cache)[scale_at] = sc;
+  }
+}
+
 int scatter_grid(long long units) {
   long long blocks = (units + 255) / 256;
   if (blocks > 152LL * 64) blocks = 152LL * 64;
@@ -105,6 +184,15 @@ cudaError_t launch_reshape_and_cache(const ScatterParams& p, int src_dtype, int 
     const int eb = src_dtype == PA_F32 ? 4 : (src_dtype == PA_F16 || src_dtype == PA_BF16 ? 2 : 1);
     const long long units = (long long)p.num_tokens * p.num_kv_heads * (p.head_size * eb / 16);
     scatter_copy_kernel<<<scatter_grid(units), 256, 0, stream>>>(p, eb);
+    return cudaGetLastError();
+  }
+  if (cache_dtype == PA_NVFP4) {
+    const long long units = (long long)p.num_tokens * p.num_kv_heads * (p.head_size / 16);
+    const int g = scatter_grid(units);
+    if (src_dtype == PA_F32) scatter_nvfp4_kernel<PA_F32><<<g, 256, 0, stream>>>(p);
+    else if (src_dtype == PA_F16) scatter_nvfp4_kernel<PA_F16><<<g, 256, 0, stream>>>(p);
+    else if (src_dtype == PA_BF16) scatter_nvfp4_kernel<PA_BF16><<<g, 256, 0, stream>>>(p);
+    else return cudaErrorInvalidValue;
     return cudaGetLastError();
   }
   if (cache_dtype != PA_FP8_E4M3 && cache_dtype != PA_FP8_E5M2) return cudaErrorInvalidValue;

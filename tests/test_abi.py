@@ -117,6 +117,29 @@ def test_copy_blocks_host_validation_without_a_gpu(pa):
     assert fn(None, None, None, 3, 10, 2, 128, 16, pa.PA_BF16, None) == pa.PA_ERR_INVALID_ARG
     assert fn(None, None, None, -1, 10, 2, 128, 16, pa.PA_BF16, None) == pa.PA_ERR_INVALID_ARG
     fake = 1 << 20  # aligned, never dereferenced: the checks return first
-    assert fn(fake, fake, fake, 3, 10, 2, 128, 16, 7, None) == pa.PA_ERR_UNSUPPORTED   # unknown dtype
+    assert fn(fake, fake, fake, 3, 10, 2, 128, 16, 99, None) == pa.PA_ERR_UNSUPPORTED  # unknown dtype
+    # NVFP4 tiles must be whole 16-byte pieces: block 8 x head 16 is 72 bytes
+    assert fn(fake, fake, fake, 3, 10, 2, 16, 8, pa.PA_NVFP4, None) == pa.PA_ERR_UNSUPPORTED
     assert fn(fake, fake, fake, 3, 10, 2, 4, 16, pa.PA_F16, None) == pa.PA_ERR_UNSUPPORTED  # 8-byte rows
     assert fn(fake + 8, fake, fake, 3, 10, 2, 128, 16, pa.PA_BF16, None) == pa.PA_ERR_INVALID_ARG
+
+
+def test_nvfp4_host_validation_without_a_gpu(pa):
+    """NVFP4 caches need their fp32 scales and whole tiles (head a multiple of 16,
+    block x head a multiple of 256): checked before anything is launched."""
+    lib = ctypes.CDLL(pa.LIB_PATH)
+    fn = lib.pa_decode
+    fn.restype, fn.argtypes = pa.SIGNATURES["pa_decode"]
+    fake = 1 << 20
+    st = fn(fake, fake, fake, fake, 10, fake, 4, fake, 2, 64, 8, 2, 128, 16, 0.1, pa.PA_BF16, pa.PA_NVFP4,
+            None, None, 0, fake, 1 << 30, None)
+    assert st == pa.PA_ERR_INVALID_ARG                                   # scales missing
+    st = fn(fake, fake, fake, fake, 10, fake, 4, fake, 2, 64, 8, 2, 24, 16, 0.1, pa.PA_BF16, pa.PA_NVFP4,
+            fake, fake, 0, fake, 1 << 30, None)
+    assert st == pa.PA_ERR_UNSUPPORTED                                   # head 24: partial groups
+    rc = lib.pa_reshape_and_cache
+    rc.restype, rc.argtypes = pa.SIGNATURES["pa_reshape_and_cache"]
+    assert rc(fake, fake, fake, fake, fake, 3, 10, 2, 16, 8, pa.PA_BF16, pa.PA_NVFP4, fake, fake,
+              None) == pa.PA_ERR_UNSUPPORTED                             # 72-byte tiles
+    assert rc(fake, fake, fake, fake, fake, 3, 10, 2, 128, 16, pa.PA_BF16, pa.PA_NVFP4_PER_HEAD, None, None,
+              None) == pa.PA_ERR_INVALID_ARG                             # scales missing

@@ -44,7 +44,8 @@ from typing import Optional
 
 import numpy as np
 
-ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "fp8_e4m3": 1, "fp8_e5m2": 1}
+# bytes per stored element; NVFP4: half a byte of code plus a sixteenth of a scale byte
+ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "fp8_e4m3": 1, "fp8_e5m2": 1, "nvfp4": 0.5625}
 BITS_NP = {"f32": np.uint32, "f16": np.uint16, "bf16": np.uint16, "fp8_e4m3": np.uint8, "fp8_e5m2": np.uint8,
            "nvfp4": np.uint8}
 FP8 = ("fp8_e4m3", "fp8_e5m2")
