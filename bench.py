@@ -38,7 +38,7 @@ METRIC = "attended KV tokens/sec and achieved HBM GB/s (fraction of GB300 peak),
 UNIT = "tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-WORKLOADS = ("agentic", "llama", "fp8", "fp8_e5m2", "nvfp4", "mixed", "mixed_fp8", "tiny")
+WORKLOADS = ("agentic", "llama", "fp8", "fp8_e5m2", "nvfp4", "mixed", "mixed_fp8", "mixed_nvfp4", "tiny")
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -227,12 +227,14 @@ def make_workload(name: str, seed: int, length_scale: float = 1.0):
         return workloads.mixed_fp8(seed=seed, scale_lengths=length_scale)
     if name == "nvfp4":
         return workloads.nvfp4(seed=seed, scale_lengths=length_scale)
+    if name == "mixed_nvfp4":
+        return workloads.mixed_nvfp4(seed=seed, scale_lengths=length_scale)
     if name == "tiny":
         return workloads.tiny(seed=seed)
     raise ValueError(name)
 
 
-BASE_SEEDS = {"agentic": 2, "llama": 1, "fp8": 4, "fp8_e5m2": 4, "nvfp4": 4, "mixed": 3, "mixed_fp8": 3, "tiny": 0}
+BASE_SEEDS = {"agentic": 2, "llama": 1, "fp8": 4, "fp8_e5m2": 4, "nvfp4": 4, "mixed": 3, "mixed_fp8": 3, "mixed_nvfp4": 3, "tiny": 0}
 
 
 def prefix_groups(b):

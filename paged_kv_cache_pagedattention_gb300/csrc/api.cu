@@ -749,9 +749,12 @@ pa_status pa_varlen_attn_windowed(void* out, const void* q, const void* k_cache,
     if (!cache_maps(&tk, &tv, k_cache, v_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size))
       return PA_ERR_CUDA;
   }
-  if (prefill_tiles &&
-      !encode_cache_map(&tk1, k_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size, true))
+  if (prefill_tiles && kv_dtype == PA_NVFP4) {
+    memset(&tk1, 0, sizeof(tk1));  // NVFP4 tiles move with 1-D bulk copies
+  } else if (prefill_tiles &&
+             !encode_cache_map(&tk1, k_cache, kv_dtype, num_blocks, num_kv_heads, block_size, head_size, true)) {
     return PA_ERR_CUDA;
+  }
   // Single-token rows: tensor-core decode kernel, else the generic kernel.
   // Multi-token rows: tensor-core prefill tiles, else the generic kernel.
   const bool multi = max_query_len > 1;

@@ -25,6 +25,9 @@
 //             P(i) is written, then S(i+2) into the buffer PV(i) frees.  A thread's
 //             MMAs run in issue order, so S(i+2) never overwrites P(i) before PV(i)
 //             has read it; the softmax of chunk i+1 overlaps PV(i) and S(i+2).
+// FP8 and NVFP4 caches: the producers copy whole (block, head) tiles of codes into a
+// staging ring (NVFP4 with 1-D bulk copies, tiles as laid out in HBM) and four
+// converter warps widen them to f16 in the layouts below.
 // Shared memory: Q and each K chunk are K-major, [64-element piece][row][128 bytes];
 // V is MN-major (head dim contiguous) and kept as the cache lays it out per block,
 // [block][piece][token][128 bytes], one TMA box per block; every operand uses the
@@ -168,7 +171,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-template <int HEAD, int BS, bool F8 = false>
+template <int HEAD, int BS, bool F8 = false, bool F4 = false>
 struct TcGeom {
   static constexpr int kPieces = HEAD / 64;                 // 128-byte pieces of an f16 row
   static constexpr int kBlocks = kChunk / BS;               // paged blocks per chunk
@@ -179,10 +182,11 @@ struct TcGeom {
   static constexpr int kBlockTx = kPieces * BS * 128;       // bytes of one (block, head) tile
   static constexpr int kQPiece = kRows * 128;
   static constexpr int kQTile = kPieces * kQPiece;
-  // FP8 caches: the copies land in a staging ring, [K | V][block][token][head-dim bytes]
+  // FP8 / NVFP4 caches: the copies land in a staging ring, [K | V][block][tile bytes]
+  // (FP8: [token][head-dim bytes]; NVFP4: code rows, then block-scale rows)
   static constexpr int kStgStages = F8 ? 3 : 0;
-  static constexpr int kStgBlock = BS * HEAD;               // FP8 bytes of one (block, head) tile
-  static constexpr int kStgKv = kChunk * HEAD;
+  static constexpr int kStgBlock = F4 ? nvfp4_tile_bytes(BS, HEAD) : BS * HEAD;  // one (block, head) tile
+  static constexpr int kStgKv = kBlocks * kStgBlock;
   static constexpr int kStgOff = kTiles * kQTile + kStages * kStageBytes;
   static constexpr int kBarOff = kStgOff + kStgStages * 2 * kStgKv;
   // full[S], empty[S]; per tile s_full[2], p_full[2], o_done[2]; mma_fin;
@@ -193,6 +197,7 @@ struct TcGeom {
   static_assert(kSBufs * 64 <= kOCol && kOCol + HEAD <= kTileCols, "TMEM columns");
   static_assert(kSmem <= 227 * 1024, "shared memory");
   static_assert(!F8 || HEAD == 128, "FP8 rows are one 128-byte piece");
+  static_assert(kStgBlock % 16 == 0, "staged tiles are whole 16-byte pieces");
 };
 
 // Byte offset, inside a chunk's V, of key `key`'s row in piece `pc`.
@@ -202,12 +207,13 @@ __device__ __forceinline__ uint32_t v_row_off(int key, int pc) {
 }
 
 template <int QDT, int KVDT, int HEAD, int BS>
-__global__ void __launch_bounds__(threads_tc<is_fp8<KVDT>()>(), 1)
+__global__ void __launch_bounds__(threads_tc<is_scaled<KVDT>()>(), 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv) {
-  constexpr bool kF8 = is_fp8<KVDT>();
-  constexpr int ODT = kF8 ? PA_F16 : QDT;  // MMA operand type (FP8 K/V are widened to f16)
-  using G = TcGeom<HEAD, BS, kF8>;
+  constexpr bool kCvt = is_scaled<KVDT>();  // codes staged, then widened to f16
+  constexpr bool kFp4 = is_nvfp4<KVDT>();
+  constexpr int ODT = kCvt ? PA_F16 : QDT;  // MMA operand type (FP8 K/V are widened to f16)
+  using G = TcGeom<HEAD, BS, kCvt, kFp4>;
   using QE = Elem<QDT>;
   constexpr int ST = G::kStages;
   constexpr int NB = G::kBlocks;
@@ -281,10 +287,12 @@ __global__ void __launch_bounds__(threads_tc<is_fp8<KVDT>()>(), 1)
 
   // ---- set-up: barriers, the Q tiles (zero rows for padding), TMEM
   if (tid == 0) {
-    tma_prefetch_desc(&tmk);
-    tma_prefetch_desc(&tmv);
+    if constexpr (!kFp4) {
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+    }
     for (int i = 0; i < ST; ++i) {
-      mbar_init(full + i, kF8 ? kConvThreads : 2);  // the converters, or the K and V producers
+      mbar_init(full + i, kCvt ? kConvThreads : 2);  // the converters, or the K and V producers
       mbar_init(empty + i, kTiles);                 // every tile's MMA warp
     }
     for (int i = 0; i < G::kStgStages; ++i) {
@@ -312,7 +320,7 @@ __global__ void __launch_bounds__(threads_tc<is_fp8<KVDT>()>(), 1)
                                        ((long long)(row0 + row_tok) * p.num_q_heads + h0 + row_head) * HEAD)
                                  : nullptr;
     uint8_t* dst = sQ + (tid / kRows) * G::kQTile;
-    if constexpr (!kF8) {
+    if constexpr (!kCvt) {
 #pragma unroll
       for (int c = 0; c < HEAD / 8; ++c) {
         const uint4 v = src ? src[c] : make_uint4(0, 0, 0, 0);
@@ -367,9 +375,9 @@ __global__ void __launch_bounds__(threads_tc<is_fp8<KVDT>()>(), 1)
     // of one block at a time; the second warp's copies V one whole block at a time.
     // Each arrives once per chunk on full with its own byte count.  With an FP8 cache
     // both copy whole (block, head) tiles of codes into the staging ring instead.
-    constexpr int RS = kF8 ? G::kStgStages : ST;
-    uint64_t* rfull = kF8 ? stg_full : full;
-    uint64_t* rempty = kF8 ? stg_empty : empty;
+    constexpr int RS = kCvt ? G::kStgStages : ST;
+    uint64_t* rfull = kCvt ? stg_full : full;
+    uint64_t* rempty = kCvt ? stg_empty : empty;
     const bool is_v = warp != kProducerWarp;
     const int kb_end = (k1 + BS - 1) / BS;  // blocks [kb_first, kb_end) are loaded
     auto load_window = [&](int w) {
@@ -403,17 +411,25 @@ __global__ void __launch_bounds__(threads_tc<is_fp8<KVDT>()>(), 1)
         phys[b] = ok_b ? e : -1;
         nvalid += ok_b;
       }
-      if (kF8 && elect_one()) {
+      if (kCvt && elect_one()) {
         uint8_t* sg = sStg + s * 2 * G::kStgKv + (is_v ? G::kStgKv : 0);
         if (nvalid == 0) {
           mbar_arrive(rfull + s);
         } else {
           mbar_arrive_expect_tx(rfull + s, (uint32_t)(nvalid * G::kStgBlock));
 #pragma unroll
-          for (int b = 0; b < NB; ++b)
-            if (phys[b] >= 0) tma_load_4d(sg + b * G::kStgBlock, is_v ? &tmv : &tmk, 0, kvh * BS, 0, phys[b], rfull + s);
+          for (int b = 0; b < NB; ++b) {
+            if (phys[b] < 0) continue;
+            if constexpr (kFp4) {  // a whole tile, as laid out in HBM
+              const void* src = static_cast<const uint8_t*>(is_v ? p.v_cache : p.k_cache) +
+                                ((long long)phys[b] * p.num_kv_heads + kvh) * G::kStgBlock;
+              bulk_load(sg + b * G::kStgBlock, src, G::kStgBlock, rfull + s);
+            } else {
+              tma_load_4d(sg + b * G::kStgBlock, is_v ? &tmv : &tmk, 0, kvh * BS, 0, phys[b], rfull + s);
+            }
+          }
         }
-      } else if (!kF8 && elect_one()) {
+      } else if (!kCvt && elect_one()) {
         uint8_t* sk = sKV + s * G::kStageBytes;
         if (nvalid == 0) {
           mbar_arrive(full + s);
@@ -439,16 +455,18 @@ __global__ void __launch_bounds__(threads_tc<is_fp8<KVDT>()>(), 1)
     if (lane == 0)
       for (int j = max(0, issued - RS); j < issued; ++j)
         if (!mbar_wait_bounded(rfull + j % RS, (j / RS) & 1)) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-  } else if (kF8 && warp >= kConvWarp) {
-    // ------------------------------------------------------------ FP8 converters
+  } else if (kCvt && warp >= kConvWarp) {
+    // ------------------------------------------------------------ FP8 / NVFP4 converters
     // Chunk i: wait for its codes in staging and for its f16 stage to be free, widen
     // every code to f16 exactly (every e4m3 value and every finite e5m2 value is an
-    // f16 value; the scales are applied later) into the K-major K layout and the
-    // per-block V layout, release the staging slot and mark the f16 stage full.
+    // f16 value; NVFP4: E2M1 value x E4M3 block scale, at most 6 significant bits
+    // and within f16's normal range; the fp32 scales are applied later) into the
+    // K-major K layout and the per-block V layout, release the staging slot and mark
+    // the f16 stage full.
     // Thread t owns one row: K row t (t < 64) or V row t - 64.  Reading group g of
     // a row and writing its two f16 chunks touch eight different 16-byte bank groups
     // across any eight consecutive rows, so neither side has bank conflicts.
-    if constexpr (kF8) {
+    if constexpr (kCvt) {
     const int ct = tid - kConvWarp * 32;
     const int tensor = ct / kChunk, key = ct % kChunk;
     const int blk = key / BS, tok = key % BS, sw = key & 7;  // tok & 7 == key & 7
@@ -460,21 +478,56 @@ __global__ void __launch_bounds__(threads_tc<is_fp8<KVDT>()>(), 1)
         if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
         break;
       }
-      const uint8_t* srow = sStg + ss * 2 * G::kStgKv + tensor * G::kStgKv + blk * G::kStgBlock + tok * 128;
+      const uint8_t* stile = sStg + ss * 2 * G::kStgKv + tensor * G::kStgKv + blk * G::kStgBlock;
       uint8_t* sk = sKV + s * G::kStageBytes;
       uint8_t* drow = tensor == 0 ? sk + key * 128 : sk + G::kKvBytes + blk * G::kBlockTx + tok * 128;
       const int piece_stride = tensor == 0 ? G::kPiece : BS * 128;
+      if constexpr (kFp4) {
+        // a 64-byte code row and its 8 block scales; the row's four 16-byte chunks are
+        // read in an order rotated by row pair, so a warp's reads spread over the bank
+        // line (64-byte rows) and its writes stay on distinct banks (rows differ in
+        // their swizzle)
+        const uint8_t* crow = stile + tok * (HEAD / 2);
+        const uint2 sc8 = *reinterpret_cast<const uint2*>(stile + BS * (HEAD / 2) + tok * (HEAD / 16));
+        const uint64_t sc64 = (static_cast<uint64_t>(sc8.y) << 32) | sc8.x;
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {  // codes 16 g .. 16 g + 15 -> f16 chunks 2g, 2g+1 (mod 8) of piece g / 4
-        const uint4 codes = *reinterpret_cast<const uint4*>(srow + ((g ^ sw) << 4));
-        const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
-        uint32_t h[8];
+        for (int c = 0; c < 4; ++c) {
+          const int cc = (c + (key >> 1)) & 3;  // chunk: groups 2cc, 2cc+1 = dims 32cc .. 32cc+31
+          const uint4 codes = *reinterpret_cast<const uint4*>(crow + 16 * cc);
+          const uint32_t sp = fp8x2_to_f16x2<PA_FP8_E4M3>(static_cast<uint16_t>(sc64 >> (16 * cc)));
+          const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) fp8x4_to_f16x2x2<KVDT>(cw[e], h[2 * e], h[2 * e + 1]);
-        uint8_t* row = drow + (g >> 2) * piece_stride;
-        const int cc = (2 * g) & 7;
-        *reinterpret_cast<uint4*>(row + ((cc ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(row + (((cc + 1) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+          for (int hh = 0; hh < 2; ++hh) {  // group g = 2cc + hh: codes 16 g .. 16 g + 15
+            const int g = 2 * cc + hh;
+            const uint32_t sg = __byte_perm(sp, 0, hh ? 0x3232 : 0x1010);
+            uint32_t lo[4], hi[4];
+            fp4x8_to_f16x2x4(cw[2 * hh], lo);
+            fp4x8_to_f16x2x4(cw[2 * hh + 1], hi);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              lo[e] = hmul2_u32(lo[e], sg);
+              hi[e] = hmul2_u32(hi[e], sg);
+            }
+            uint8_t* row = drow + (g >> 2) * piece_stride;
+            const int ch = (2 * g) & 7;
+            *reinterpret_cast<uint4*>(row + ((ch ^ sw) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4*>(row + (((ch + 1) ^ sw) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          }
+        }
+      } else {
+        const uint8_t* srow = stile + tok * 128;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {  // codes 16 g .. 16 g + 15 -> f16 chunks 2g, 2g+1 (mod 8) of piece g / 4
+          const uint4 codes = *reinterpret_cast<const uint4*>(srow + ((g ^ sw) << 4));
+          const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+          uint32_t h[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) fp8x4_to_f16x2x2<KVDT>(cw[e], h[2 * e], h[2 * e + 1]);
+          uint8_t* row = drow + (g >> 2) * piece_stride;
+          const int cc = (2 * g) & 7;
+          *reinterpret_cast<uint4*>(row + ((cc ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4*>(row + (((cc + 1) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+        }
       }
       fence_proxy_async();  // generic-proxy writes, read next by the tensor core
       mbar_arrive(stg_empty + ss);
@@ -572,8 +625,8 @@ __global__ void __launch_bounds__(threads_tc<is_fp8<KVDT>()>(), 1)
     uint64_t* my_p_full = p_full + t * kSBufs;
     uint64_t* my_o_done = o_done + t * kSBufs;
     // score multiplier in log2 units; FP8: the K scale and the row's f16 shift too
-    const float c = kF8 ? ldexpf(p.scale * kLog2e * p.k_scale[kvh * p.scale_stride], -q_shift) : p.scale * kLog2e;
-    const float out_scale = kF8 ? p.v_scale[kvh * p.scale_stride] : 1.f;
+    const float c = kCvt ? ldexpf(p.scale * kLog2e * p.k_scale[kvh * p.scale_stride], -q_shift) : p.scale * kLog2e;
+    const float out_scale = kCvt ? p.v_scale[kvh * p.scale_stride] : 1.f;
     const int row_limit = p.causal ? min(k1, row_pos + 1) : k1;  // this row attends keys < row_limit
     const int row_lo = p.window > 0 ? max(0, row_pos - p.window + 1) : 0;  // ... and keys >= row_lo
     float m = -INFINITY, l = 0.f;
@@ -750,8 +803,8 @@ __global__ void __launch_bounds__(threads_tc<is_fp8<KVDT>()>(), 1)
 template <int QDT, int KVDT, int HEAD, int BS>
 cudaError_t launch_tc_t(const AttnParams& p, int num_items, const CUtensorMap* tk, const CUtensorMap* tv,
                         cudaStream_t stream) {
-  constexpr bool kF8 = is_fp8<KVDT>();
-  constexpr int smem = TcGeom<HEAD, BS, kF8>::kSmem;
+  constexpr bool kCvt = is_scaled<KVDT>();
+  constexpr int smem = TcGeom<HEAD, BS, kCvt, is_nvfp4<KVDT>()>::kSmem;
   auto kern = prefill_tc_kernel<QDT, KVDT, HEAD, BS>;
   static int configured_device = -1;
   int dev = 0;
@@ -765,7 +818,7 @@ cudaError_t launch_tc_t(const AttnParams& p, int num_items, const CUtensorMap* t
     configured_device = dev;
   }
   dim3 grid(num_items, p.num_kv_heads * p.num_head_groups);
-  kern<<<grid, threads_tc<kF8>(), smem, stream>>>(p, *tk, *tv);
+  kern<<<grid, threads_tc<kCvt>(), smem, stream>>>(p, *tk, *tv);
   return cudaGetLastError();
 }
 
@@ -776,7 +829,7 @@ cudaError_t launch_tc_shape(const AttnParams& p, int num_items, const CUtensorMa
   if (d == 128 && bs == 16) return launch_tc_t<QDT, KVDT, 128, 16>(p, num_items, tk, tv, s);
   if (d == 128 && bs == 32) return launch_tc_t<QDT, KVDT, 128, 32>(p, num_items, tk, tv, s);
   if (d == 128 && bs == 64) return launch_tc_t<QDT, KVDT, 128, 64>(p, num_items, tk, tv, s);
-  if constexpr (!is_fp8<KVDT>()) {
+  if constexpr (!is_scaled<KVDT>()) {
     if (d == 64 && bs == 16) return launch_tc_t<QDT, KVDT, 64, 16>(p, num_items, tk, tv, s);
     if (d == 64 && bs == 32) return launch_tc_t<QDT, KVDT, 64, 32>(p, num_items, tk, tv, s);
     if (d == 64 && bs == 64) return launch_tc_t<QDT, KVDT, 64, 64>(p, num_items, tk, tv, s);
@@ -797,7 +850,8 @@ int prefill_tile_tokens(int group) {
 bool prefill_tc_supported(int q_dtype, int kv_dtype, int head_size, int block_size) {
   if (!(q_dtype == PA_BF16 || q_dtype == PA_F16)) return false;
   if (!(block_size == 16 || block_size == 32 || block_size == 64)) return false;
-  if (kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_FP8_E5M2) return head_size == 128;  // one 128-byte row of codes
+  if (kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_FP8_E5M2 || kv_dtype == PA_NVFP4)
+    return head_size == 128;  // converted rows are one 128-byte piece of codes (FP8) / 64 bytes (NVFP4)
   return kv_dtype == q_dtype && (head_size == 64 || head_size == 128);
 }
 
@@ -812,6 +866,11 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int q_dtype, int kv_dtype, in
   if (kv_dtype == PA_FP8_E5M2) {
     if (q_dtype == PA_BF16) return launch_tc_shape<PA_BF16, PA_FP8_E5M2>(p, num_items, tmap_k, tmap_v, stream);
     if (q_dtype == PA_F16) return launch_tc_shape<PA_F16, PA_FP8_E5M2>(p, num_items, tmap_k, tmap_v, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (kv_dtype == PA_NVFP4) {
+    if (q_dtype == PA_BF16) return launch_tc_shape<PA_BF16, PA_NVFP4>(p, num_items, tmap_k, tmap_v, stream);
+    if (q_dtype == PA_F16) return launch_tc_shape<PA_F16, PA_NVFP4>(p, num_items, tmap_k, tmap_v, stream);
     return cudaErrorInvalidValue;
   }
   if (kv_dtype != q_dtype) return cudaErrorInvalidValue;

@@ -123,16 +123,50 @@ def test_sliding_window(pa, window, part):
     _full_parity(pa, b, part, window)
 
 
-def test_varlen_mixed_step(pa):
-    b = workloads.build("nvfp4_mixed", 351, [700, 37, 1, 300, 900], [64, 1, 1, 300, 17], 32, 8, 128, 16, "nvfp4")
+VARLEN = [
+    # (name, Hq, Hkv, bs, lens, q_lens, partition, causal, q dtype) -- multi-token rows on the
+    # tcgen05 prefill tiles (NVFP4 tiles staged by bulk copies, widened by the converters)
+    ("mixed_bs16_split64", 32, 8, 16, [700, 37, 1, 300, 900], [64, 1, 1, 300, 17], 64, True, None),
+    ("bs32_default", 32, 8, 32, [2000, 33, 700], [300, 1, 64], 0, True, None),
+    ("bs64_g8_f16q", 16, 2, 64, [1500, 513], [257, 200], 0, True, "f16"),
+    ("non_causal_bs16", 8, 2, 16, [400, 90], [130, 17], 96, False, None),
+]
+
+
+@pytest.mark.parametrize("case", VARLEN, ids=[c[0] for c in VARLEN])
+def test_varlen_parity(pa, case):
+    name, hq, hkv, bs, lens, q_lens, part, causal, q_dtype = case
+    b = workloads.build("nvfp4_v_" + name, 351 + len(name), lens, q_lens, hq, hkv, 128, bs, "nvfp4",
+                        q_dtype=q_dtype, src_dtype=q_dtype, causal=causal)
     db = DeviceBatch(b, DEV)
     run_scatter(pa, db)
-    out = run_varlen(pa, db, 64)
+    out = run_varlen(pa, db, part, causal)
     assert pa.pa_get_error_flags() == 0
     k_ref, v_ref = oracle_scatter(b)
     ref = oracle.paged_varlen(b.q, b.q_dtype, k_ref, v_ref, "nvfp4", b.block_tables, b.query_start_loc,
-                              b.seq_lens, 16, b.scale, True, b.k_scale, b.v_scale)
-    compare(out, ref, "nvfp4", where="nvfp4 varlen")
+                              b.seq_lens, bs, b.scale, causal, b.k_scale, b.v_scale)
+    compare(out, ref, "nvfp4", where="nvfp4 varlen " + name)
+
+
+def test_varlen_window_and_per_head_scales(pa):
+    b = workloads.build("nvfp4_vw", 391, [2000, 33, 700], [300, 1, 64], 32, 8, 128, 16, "nvfp4",
+                        nvfp4_scale=PER_HEAD)
+    db = DeviceBatch(b, DEV)
+    run_scatter(pa, db)
+    tables = b.block_tables.copy()
+    for r in range(b.num_seqs):   # blocks wholly before the window: released
+        q_len = int(b.query_start_loc[r + 1] - b.query_start_loc[r])
+        tables[r, : max(0, int(b.seq_lens[r]) - q_len - 200 + 1) // 16] = -1
+    out = torch.empty_like(db.q)
+    ws = pa.workspace_tensor(pa.pa_varlen_workspace_size(b.num_seqs, b.total_q, b.max_query_len, 32, 8, 128,
+                                                         b.max_seq_len, 16, 0), DEV)
+    pa.pa_varlen_attn(out, db.q, db.kc, db.vc, torch.from_numpy(tables).to(DEV), db.qsl, db.lens, b.max_query_len,
+                      b.max_seq_len, b.scale, ws, True, db.k_scale, db.v_scale, 0, window=200)
+    assert pa.pa_get_error_flags() == 0
+    k_ref, v_ref = oracle_scatter(b)
+    ref = oracle.paged_varlen(b.q, b.q_dtype, k_ref, v_ref, "nvfp4", tables, b.query_start_loc, b.seq_lens, 16,
+                              b.scale, True, b.k_scale, b.v_scale, window=200)
+    compare(out, ref, "nvfp4", where="nvfp4 varlen window per-head")
 
 
 def test_shared_prefix_groups(pa):

@@ -355,6 +355,11 @@ def mixed(seed: int = 3, host_cache: bool = False, scale_lengths: float = 1.0,
                  q_dtype="bf16", src_dtype="bf16", host_cache=host_cache)
 
 
+def mixed_nvfp4(seed: int = 3, host_cache: bool = False, scale_lengths: float = 1.0) -> PagedBatch:
+    """The mixed step with an NVFP4 cache (tensor scale 0.375)."""
+    return mixed(seed, host_cache, scale_lengths, kv_dtype=NVFP4)
+
+
 def mixed_fp8(seed: int = 3, host_cache: bool = False, scale_lengths: float = 1.0) -> PagedBatch:
     """The mixed step with an FP8 e4m3 cache (per-tensor scales 2^-6)."""
     return mixed(seed, host_cache, scale_lengths, kv_dtype="fp8_e4m3")
@@ -382,7 +387,7 @@ def nvfp4(seed: int = 4, host_cache: bool = False, scale_lengths: float = 1.0) -
 
 
 NAMED = {"tiny": tiny, "llama": llama, "agentic": agentic, "mixed": mixed, "fp8": fp8, "mixed_fp8": mixed_fp8,
-         "fp8_e5m2": fp8_e5m2, "nvfp4": nvfp4}
+         "fp8_e5m2": fp8_e5m2, "nvfp4": nvfp4, "mixed_nvfp4": mixed_nvfp4}
 
 
 # --------------------------------------------------------------------------
