@@ -639,7 +639,7 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32)
   const int s0 = p.group_start[g], s1 = p.group_start[g + 1];
   const int nm = s1 - s0;
   const int nwarps = blockDim.x >> 5;
-  if (nm < 2 || nm > nwarps - 1) return;
+  if (s0 < 0 || s1 > p.num_seqs || nm < 2 || nm > nwarps - 1) return;
   const int S = group_shared_tokens(p, g, s0, s1);
   if (S == 0) return;
   const int nsb = S / BS, pb = p.part_shared / BS;

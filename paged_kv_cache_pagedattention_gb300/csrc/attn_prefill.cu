@@ -30,7 +30,6 @@ template <int HEAD, int BS>
 struct PrefillGeom {
   static constexpr int kRowBytes = HEAD * 2;
   static constexpr int kTileBytes = BS * kRowBytes;
-  static constexpr int kSub = kRowBytes / 128;
   static constexpr int kStages = kTileBytes <= 4096 ? 8 : 5;
   static constexpr int kKSteps = HEAD / 16;  // QK k-steps over the head dim
   static constexpr int kNTok = BS / 8;       // QK n-tiles over tokens

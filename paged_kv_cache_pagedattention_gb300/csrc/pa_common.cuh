@@ -408,7 +408,7 @@ __device__ __forceinline__ RowInfo row_info(const AttnParams& p, int row) {
 // every member holds that many full blocks; groups of one sequence, or larger than
 // max_group_size, share nothing.
 __device__ __forceinline__ int group_shared_tokens(const AttnParams& p, int g, int s0, int s1) {
-  if (s1 - s0 < 2 || s1 - s0 > p.max_group_size) return 0;
+  if (s0 < 0 || s1 > p.num_seqs || s1 - s0 < 2 || s1 - s0 > p.max_group_size) return 0;
   int sb = p.group_shared_blocks[g];
   for (int m = s0; m < s1; ++m) {
     const int len = p.seq_lens[m];
