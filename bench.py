@@ -580,7 +580,8 @@ def run_ours(args):
         tpeak, tkind = measured_bf16_sustained()
         decode_line = {"bound": "hbm", "achieved": dec_gbs, "peak": peak, "unit": "GB/s", "frac": dec_gbs / peak,
                        "kernel": "decode_mma_kernel (single-token rows)", "kernel_ms": att_ms,
-                       "algorithmic_bytes_per_launch": vsplit["decode_bytes"], "traffic": None}
+                       "algorithmic_bytes_per_launch": vsplit["decode_bytes"],
+                       "traffic": profiled_traffic(args.workload, "decode_mma_kernel")}
         prefill_line = {"bound": "tensor", "achieved": pf_tflops, "peak": tpeak, "unit": "TFLOP/s",
                         "frac": pf_tflops / tpeak, "kernel": "prefill_tc_kernel (multi-token rows)",
                         "kernel_ms": pf_ms, "algorithmic_flops_per_launch": vsplit["prefill_flops"],
