@@ -1,6 +1,8 @@
 // Portable kernels of the attention path:
 //  * attn_generic_kernel -- one warp per (query row, query head, partition), plain
-//    fp32 FMAs; serves fp32 caches and every shape the tensor-core kernels do not;
+//    fp32 FMAs, 32 keys per step (a lane per key for the scores, a lane per head
+//    dimension for the weighted sum); serves fp32 caches and every shape the
+//    tensor-core kernels do not;
 //  * merge_kernel -- combines the split-K partial states of a row into its output
 //    (rescale each partial by exp2(m_j - m) to the common maximum, add, divide);
 //  * varlen_plan_kernel -- validates query_start_loc and lays out, per request,
@@ -17,15 +19,37 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kGenericMaxPerLane = 8;  // head_size <= 256
 
-// Stored value (without the fp32 scale) of element dd of token row `off` of cache
-// tile `tile` (= physical block x Hkv + KV head).
+// A token row of a cache tile (= physical block x Hkv + KV head): the address of its
+// first element (NVFP4: of its code row) and, for NVFP4, of its block-scale row.
+struct KvRow {
+  const uint8_t* row;
+  const uint8_t* scales;
+};
+
 template <int KVDT>
-__device__ __forceinline__ float kv_elem(const void* cache, long long tile, int bs, int d, int off, int dd) {
+__device__ __forceinline__ KvRow kv_row(const void* cache, long long tile, int bs, int d, int off) {
+  const uint8_t* base = static_cast<const uint8_t*>(cache);
   if constexpr (is_nvfp4<KVDT>()) {
-    return nvfp4_elem(static_cast<const uint8_t*>(cache) + tile * nvfp4_tile_bytes(bs, d), bs, d, off, dd);
+    const uint8_t* t = base + tile * nvfp4_tile_bytes(bs, d);
+    return {t + off * (d / 2), t + bs * (d / 2) + off * (d / 16)};
+  } else {
+    return {base + ((tile * bs + off) * d) * Elem<KVDT>::bytes, nullptr};
+  }
+}
+
+// Stored value (without the fp32 scale) of element dd of a token row.
+template <int KVDT>
+__device__ __forceinline__ float kv_elem(const KvRow& r, int dd) {
+  if constexpr (is_nvfp4<KVDT>()) {
+    const uint32_t byte = r.row[dd >> 1];
+    const __half2_raw c = __nv_cvt_fp4x2_to_halfraw2(static_cast<__nv_fp4x2_storage_t>(byte), __NV_E2M1);
+    __half_raw v;
+    v.x = (dd & 1) ? c.y : c.x;
+    const __half_raw b = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(r.scales[dd >> 4]), __NV_E4M3);
+    return __half2float(__half(v)) * __half2float(__half(b));
   } else {
     using KE = Elem<KVDT>;
-    return KE::load(static_cast<const typename KE::T*>(cache) + (tile * bs + off) * d + dd);
+    return KE::load(reinterpret_cast<const typename KE::T*>(r.row) + dd);
   }
 }
 
@@ -61,41 +85,72 @@ __global__ void __launch_bounds__(128)
   }
   const float c = p.scale * kscale * kLog2e;
 
+  // The warp's query row in shared memory (every lane reads all of it below).
+  __shared__ float sq[4][kGenericMaxPerLane * 32];
+  float* q_s = sq[threadIdx.x >> 5];
   const typename QE::T* qrow =
       reinterpret_cast<const typename QE::T*>(p.q) + ((long long)row * p.num_q_heads + head) * d;
-  float qv[kGenericMaxPerLane], acc[kGenericMaxPerLane];
+  for (int dd = lane; dd < d; dd += 32) q_s[dd] = QE::load(qrow + dd);
+  __syncwarp();
+  float acc[kGenericMaxPerLane];
 #pragma unroll
-  for (int i = 0; i < kGenericMaxPerLane; ++i) {
-    const int dd = lane + 32 * i;
-    qv[i] = dd < d ? QE::load(qrow + dd) : 0.f;
-    acc[i] = 0.f;
-  }
+  for (int i = 0; i < kGenericMaxPerLane; ++i) acc[i] = 0.f;
   const int32_t* table = p.block_tables + (long long)ri.request * p.max_blocks_per_seq;
   float m = -INFINITY, l = 0.f;
-  for (int t = max(t0, ri.lo); t < t1; ++t) {  // keys before the window are not read
-    const int phys = table[t / p.block_size];
-    if (phys < 0 || phys >= p.num_blocks) {
-      if (lane == 0) flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
-      continue;
-    }
-    const long long tile = (long long)phys * p.num_kv_heads + kvh;
-    const int off = t % p.block_size;
-    float dot = 0.f;
+  // 32 keys at a time (keys before the window are not read): lane j scores key tb + j
+  // on its own, so the warp reduces once per 32 keys; then lane i accumulates
+  // dimensions i, i + 32, ... of the 32 weighted V rows (coalesced row reads).
+  for (int tb = max(t0, ri.lo); tb < t1; tb += 32) {
+    const int tt = tb + lane;
+    float sj = -INFINITY;
+    long long tile = -1;
+    if (tt < t1) {
+      const int phys = table[tt / p.block_size];
+      if (phys < 0 || phys >= p.num_blocks) {
+        flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
+      } else {
+        tile = (long long)phys * p.num_kv_heads + kvh;
+        const KvRow kr = kv_row<KVDT>(p.k_cache, tile, p.block_size, d, tt % p.block_size);
+        // eight independent loads in flight, four accumulation chains
+        float dot[4] = {0.f, 0.f, 0.f, 0.f};
+        int dd = 0;
+        for (; dd + 8 <= d; dd += 8) {
+          float kv[8];
 #pragma unroll
-    for (int i = 0; i < kGenericMaxPerLane; ++i) {
-      const int dd = lane + 32 * i;
-      if (dd < d) dot = fmaf(qv[i], kv_elem<KVDT>(p.k_cache, tile, p.block_size, d, off, dd), dot);
-    }
-    dot = warp_sum_xor(dot, 1, 16);
-    const float s = dot * c;
-    const float m_new = fmaxf(m, s);
-    const float alpha = exp2f(m - m_new);  // m == -inf on the first key -> 0
-    const float w = exp2f(s - m_new);
-    l = l * alpha + w;
+          for (int e = 0; e < 8; ++e) kv[e] = kv_elem<KVDT>(kr, dd + e);
 #pragma unroll
-    for (int i = 0; i < kGenericMaxPerLane; ++i) {
-      const int dd = lane + 32 * i;
-      if (dd < d) acc[i] = fmaf(w, kv_elem<KVDT>(p.v_cache, tile, p.block_size, d, off, dd), acc[i] * alpha);
+          for (int e = 0; e < 8; ++e) dot[e & 3] = fmaf(q_s[dd + e], kv[e], dot[e & 3]);
+        }
+        for (; dd < d; ++dd) dot[0] = fmaf(q_s[dd], kv_elem<KVDT>(kr, dd), dot[0]);
+        sj = ((dot[0] + dot[1]) + (dot[2] + dot[3])) * c;
+      }
+    }
+    const float m_new = fmaxf(m, warp_max_xor(sj, 1, 16));
+    if (m_new == -INFINITY) continue;  // no attended key in this group of 32
+    const float alpha = exp2f(m - m_new);  // m == -inf before the first key -> 0
+    const float pj = exp2f(sj - m_new);
+    l = l * alpha + warp_sum_xor(pj, 1, 16);
+#pragma unroll
+    for (int i = 0; i < kGenericMaxPerLane; ++i) acc[i] *= alpha;
+    const int n = min(32, t1 - tb);
+#pragma unroll 4
+    // lane j's V row, handed to every lane in turn
+    const KvRow my_v = tile >= 0 ? kv_row<KVDT>(p.v_cache, tile, p.block_size, d, tt % p.block_size)
+                                 : KvRow{nullptr, nullptr};
+    for (int j = 0; j < n; ++j) {
+      const float pv = __shfl_sync(0xffffffffu, pj, j);
+      KvRow vr;
+      vr.row = reinterpret_cast<const uint8_t*>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(my_v.row), j));
+      if (vr.row == nullptr) continue;  // unreadable block (flagged above): no weight, not read
+      if constexpr (is_nvfp4<KVDT>())
+        vr.scales = reinterpret_cast<const uint8_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(my_v.scales), j));
+#pragma unroll
+      for (int i = 0; i < kGenericMaxPerLane; ++i) {
+        const int dd = lane + 32 * i;
+        if (dd < d) acc[i] = fmaf(pv, kv_elem<KVDT>(vr, dd), acc[i]);
+      }
     }
     m = m_new;
   }

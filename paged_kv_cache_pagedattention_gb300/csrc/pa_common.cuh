@@ -297,18 +297,6 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   return d;
 }
 
-// Value of one stored element (without the fp32 scale) of a NVFP4 tile: code
-// element `dim` of token row `tok`, times its block scale.
-__device__ __forceinline__ float nvfp4_elem(const uint8_t* tile, int block_size, int head, int tok, int dim) {
-  const uint32_t byte = tile[tok * (head / 2) + (dim >> 1)];
-  const uint32_t sc = tile[block_size * head / 2 + tok * (head / 16) + (dim >> 4)];
-  const __half2_raw c = __nv_cvt_fp4x2_to_halfraw2(static_cast<__nv_fp4x2_storage_t>(byte), __NV_E2M1);
-  __half_raw v;
-  v.x = (dim & 1) ? c.y : c.x;
-  const __half_raw b = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sc), __NV_E4M3);
-  return __half2float(__half(v)) * __half2float(__half(b));
-}
-
 // 1-D bulk copy global -> shared of `bytes` bytes (a multiple of 16, both addresses
 // 16-byte aligned), completion counted on `bar`.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
