@@ -565,7 +565,8 @@ def run_ours(args):
     elif not varlen:
         achieved = nbytes["algorithmic"] / (att_ms / 1000.0) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                    "traffic": profiled_traffic(args.workload), "kernel": "decode_mma_kernel",
+                    "traffic": profiled_traffic(args.workload),
+                    "kernel": "decode_mma_kernel" if b.kv_dtype != "f32" else "attn_generic_kernel",
                     "peak_source": f"{peak_kind} MEASURED_PEAKS.json hbm_gbs",
                     "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
                     "algorithmic_bytes_per_launch": nbytes["algorithmic"],
