@@ -183,9 +183,13 @@ SharedLayout shared_layout(int num_seqs, int num_groups, int hq, int hkv, int d,
                            int requested) {
   SharedLayout L;
   L.part = resolve_partition(requested, num_seqs, hkv, max_seq_len, bs);
-  // The shared-prefix tiles carry a whole group per CTA: ~8 CTAs per SM keep the grid
-  // busy, and coarser partitions halve the shared partials the merge reads (measured
-  // on the agentic forks: 0.442 -> 0.413 ms per step against 32 per SM).
+  // The shared-prefix tiles carry a whole group per CTA: ~8 partitions' worth of work
+  // items per SM (the persistent tile kernel takes them in turn), and coarser
+  // partitions halve the shared partials the merge reads (measured on the agentic
+  // forks: 0.442 -> 0.413 ms per step against 32 per SM).  Fixed partitions that fit
+  // the resident CTAs in exactly one wave were faster on that workload (8192 tokens:
+  // span 0.355 against 0.364 ms) but fall off a cliff when the wave is missed by a few
+  // items (6144: 0.452 ms), and the host cannot tell which groups share nothing.
   L.part_shared = requested > 0
                       ? L.part
                       : resolve_partition(default_partition(num_groups > 0 ? num_groups : 1, hkv, max_seq_len, bs, 8),

@@ -12,6 +12,8 @@
 //   O += P V    (P straight from the S accumulators as the A operand)
 // Rows write partial states (unnormalised O, max, sum) that the merge combines with
 // the members' private remainders.
+#include <algorithm>
+
 #include "pa_common.cuh"
 
 namespace pa {
@@ -172,38 +174,57 @@ constexpr int prefill_smem_bytes() {
 }
 
 // Shared-prefix tiles.  [AGENTIC] "統一分頁 + 共用池": forked sequences point at
-// the same physical blocks.  One CTA handles (group of sequences sharing leading
+// the same physical blocks.  A work item is (group of sequences sharing leading
 // blocks, KV head, head group, partition of the shared prefix); its query rows are
 // the (member, head) pairs of the group, member-major (row = member * GP + head),
 // so every shared K/V tile is loaded once and serves every member's heads.  All
 // shared keys precede every member's query position: no mask.  Each row writes a
 // partial state at its sequence's shared partition z; the members' private tokens
 // are attended by the decode kernel and the merge combines both.
+//
+// The grid is persistent: as many CTAs as fit on the GPU at once, each taking work
+// items blockIdx.x, blockIdx.x + gridDim.x, ... (items of groups that share nothing,
+// or past a group's shared length, are skipped by every warp alike).  The ring's
+// stage and phase run on across items, so the producer streams the next item's
+// blocks while the consumers finish the current one.
 template <int QDT, int HEAD, int BS>
 __global__ void __launch_bounds__(kThreads, 1)
     shared_prefix_tile_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
-                              const __grid_constant__ CUtensorMap tmv) {
+                              const __grid_constant__ CUtensorMap tmv, int parts) {
   using G = PrefillGeom<HEAD, BS>;
   constexpr int ST = G::kStages;
   constexpr int TB = G::kTileBytes;
 
-  const int g = blockIdx.x;
-  const int kvh = blockIdx.y / p.num_head_groups, hg = blockIdx.y % p.num_head_groups;
-  const int z = blockIdx.z;
-  const int s0 = p.group_start[g], s1 = p.group_start[g + 1];
-  const int nm = s1 - s0;
   const int nwc = (int)(blockDim.x >> 5) - 1;  // consumer warps
   int gp = 1;
   while (gp < min(p.group, 8)) gp <<= 1;
-  if (nm < 2 || nm * gp > 16 * nwc) return;
-  const int S = group_shared_tokens(p, g, s0, s1);
-  if (S == 0) return;
-  const int pb = p.part_shared / BS, nsb = S / BS;
-  const int b0 = z * pb;
-  if (b0 >= nsb) return;
-  const int nblocks = min(b0 + pb, nsb) - b0;
-  const int h0 = kvh * p.group + hg * 8;
-  const int nh = min(8, p.group - hg * 8);
+  const int ny = p.num_kv_heads * p.num_head_groups;
+  const long long total = (long long)p.num_groups * ny * parts;
+  // Item `it` -> its group's first sequence s0, members nm, KV head, first query head,
+  // heads, partition and blocks; false when the item has no work.
+  struct Item {
+    int s0, nm, kvh, h0, nh, z, b0, nblocks;
+  };
+  auto decode_item = [&](long long it, Item& w) -> bool {
+    w.z = (int)(it % parts);
+    const long long gy = it / parts;
+    const int y = (int)(gy % ny), g = (int)(gy / ny);
+    w.kvh = y / p.num_head_groups;
+    const int hg = y % p.num_head_groups;
+    w.s0 = p.group_start[g];
+    const int s1 = p.group_start[g + 1];
+    w.nm = s1 - w.s0;
+    if (w.nm < 2 || w.nm * gp > 16 * nwc) return false;
+    const int S = group_shared_tokens(p, g, w.s0, s1);
+    if (S == 0) return false;
+    const int pb = p.part_shared / BS, nsb = S / BS;
+    w.b0 = w.z * pb;
+    if (w.b0 >= nsb) return false;
+    w.nblocks = min(w.b0 + pb, nsb) - w.b0;
+    w.h0 = w.kvh * p.group + hg * 8;
+    w.nh = min(8, p.group - hg * 8);
+    return true;
+  };
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -221,32 +242,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   __syncthreads();
-  const int32_t* lead = p.block_tables + (long long)s0 * p.max_blocks_per_seq;
 
   if (warp == nwc) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      for (int i = 0; i < nblocks; ++i) {
-        const int s = i % ST;
-        if (i >= ST && !mbar_wait_bounded(empty + s, ((i / ST) - 1) & 1)) {
-          flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-          break;  // the consumers time out on the full barrier and write nothing
-        }
-        const int jb = b0 + i;
-        const int phys = lead[jb];
-        bool same = true;  // every member's table must name the same physical block
-        for (int m = 1; m < nm; ++m)
-          same &= p.block_tables[(long long)(s0 + m) * p.max_blocks_per_seq + jb] == phys;
-        const bool valid = same && phys >= 0 && phys < p.num_blocks;
-        stage_ok[s] = valid;
-        if (!valid) {
-          flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
-          mbar_arrive(full + s);  // empty phase: the block is skipped for the whole group
-        } else {
-          uint8_t* st = smem + s * 2 * TB;
-          mbar_arrive_expect_tx(full + s, 2 * TB);
-          tma_load_4d(st, &tmk, 0, kvh * BS, 0, phys, full + s);
-          tma_load_4d(st + TB, &tmv, 0, kvh * BS, 0, phys, full + s);
+      long long gi = 0;  // blocks issued so far, over all items
+      for (long long it = blockIdx.x; it < total; it += gridDim.x) {
+        Item w;
+        if (!decode_item(it, w)) continue;
+        const int32_t* lead = p.block_tables + (long long)w.s0 * p.max_blocks_per_seq;
+        for (int i = 0; i < w.nblocks; ++i, ++gi) {
+          const int s = (int)(gi % ST);
+          if (gi >= ST && !mbar_wait_bounded(empty + s, (uint32_t)((gi / ST) - 1) & 1)) {
+            flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+            return;  // the consumers time out on the full barrier and write nothing
+          }
+          const int jb = w.b0 + i;
+          const int phys = lead[jb];
+          bool same = true;  // every member's table must name the same physical block
+          for (int m = 1; m < w.nm; ++m)
+            same &= p.block_tables[(long long)(w.s0 + m) * p.max_blocks_per_seq + jb] == phys;
+          const bool valid = same && phys >= 0 && phys < p.num_blocks;
+          stage_ok[s] = valid;
+          if (!valid) {
+            flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
+            mbar_arrive(full + s);  // empty phase: the block is skipped for the whole group
+          } else {
+            uint8_t* st = smem + s * 2 * TB;
+            mbar_arrive_expect_tx(full + s, 2 * TB);
+            tma_load_4d(st, &tmk, 0, w.kvh * BS, 0, phys, full + s);
+            tma_load_4d(st + TB, &tmv, 0, w.kvh * BS, 0, phys, full + s);
+          }
         }
       }
     }
@@ -254,64 +280,69 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ------------------------------------------------------------------ consumers
-  int rm[2], rn[2];
-  bool rvalid[2];
-  const uint32_t* qw[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int rho = 16 * warp + (lane >> 2) + 8 * h;
-    rm[h] = rho / gp;
-    rn[h] = rho % gp;
-    rvalid[h] = rm[h] < nm && rn[h] < nh;
-    qw[h] = rvalid[h] ? reinterpret_cast<const uint32_t*>(
-                            reinterpret_cast<const typename Elem<QDT>::T*>(p.q) +
-                            ((long long)(s0 + rm[h]) * p.num_q_heads + h0 + rn[h]) * HEAD)
-                      : nullptr;
-  }
-  const bool warp_active = (16 * warp) / gp < nm;
-  const bool all_valid = __all_sync(0xffffffffu, rvalid[0] && rvalid[1]);
-  uint32_t qa[G::kKSteps][4];
-  load_query_rows<HEAD>(qw[0], qw[1], qa);
   const float c = p.scale * kLog2e;
-  RowState<HEAD> st;
-  st.init();
-  for (int i = 0; i < nblocks; ++i) {
-    const int s = i % ST;
-    const bool got = mbar_wait_bounded(full + s, (i / ST) & 1);
-    if (!__all_sync(0xffffffffu, got)) {
-      if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-      return;
-    }
-    if (warp_active && stage_ok[s]) {
-      const uint32_t kbase = smem_u32(smem + s * 2 * TB);
-      float sc[G::kNTok][4];
-      fa2_scores<QDT, HEAD, BS>(kbase, qa, sc);
-      if (!all_valid) {  // padding rows (no member / head) take no part
+  long long gi = 0;  // blocks consumed so far, over all items
+  for (long long it = blockIdx.x; it < total; it += gridDim.x) {
+    Item w;
+    if (!decode_item(it, w)) continue;
+    int rm[2], rn[2];
+    bool rvalid[2];
+    const uint32_t* qw[2];
 #pragma unroll
-        for (int nt = 0; nt < G::kNTok; ++nt) {
-          if (!rvalid[0]) sc[nt][0] = sc[nt][1] = -INFINITY;
-          if (!rvalid[1]) sc[nt][2] = sc[nt][3] = -INFINITY;
-        }
+    for (int h = 0; h < 2; ++h) {
+      const int rho = 16 * warp + (lane >> 2) + 8 * h;
+      rm[h] = rho / gp;
+      rn[h] = rho % gp;
+      rvalid[h] = rm[h] < w.nm && rn[h] < w.nh;
+      qw[h] = rvalid[h] ? reinterpret_cast<const uint32_t*>(
+                              reinterpret_cast<const typename Elem<QDT>::T*>(p.q) +
+                              ((long long)(w.s0 + rm[h]) * p.num_q_heads + w.h0 + rn[h]) * HEAD)
+                        : nullptr;
+    }
+    const bool warp_active = (16 * warp) / gp < w.nm;
+    const bool all_valid = __all_sync(0xffffffffu, rvalid[0] && rvalid[1]);
+    uint32_t qa[G::kKSteps][4];
+    load_query_rows<HEAD>(qw[0], qw[1], qa);
+    RowState<HEAD> st;
+    st.init();
+    for (int i = 0; i < w.nblocks; ++i, ++gi) {
+      const int s = (int)(gi % ST);
+      const bool got = mbar_wait_bounded(full + s, (uint32_t)(gi / ST) & 1);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+        return;
       }
-      fa2_softmax_pv<QDT, HEAD, BS>(kbase + TB, sc, c, BS, st);
+      if (warp_active && stage_ok[s]) {
+        const uint32_t kbase = smem_u32(smem + s * 2 * TB);
+        float sc[G::kNTok][4];
+        fa2_scores<QDT, HEAD, BS>(kbase, qa, sc);
+        if (!all_valid) {  // padding rows (no member / head) take no part
+#pragma unroll
+          for (int nt = 0; nt < G::kNTok; ++nt) {
+            if (!rvalid[0]) sc[nt][0] = sc[nt][1] = -INFINITY;
+            if (!rvalid[1]) sc[nt][2] = sc[nt][3] = -INFINITY;
+          }
+        }
+        fa2_softmax_pv<QDT, HEAD, BS>(kbase + TB, sc, c, BS, st);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty + s);
-  }
 
-  // ---- each valid row's partial state for shared partition z
+    // ---- each valid row's partial state for shared partition z
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    st.l[h] = warp_sum_xor(st.l[h], 1, 2);
-    if (!rvalid[h]) continue;
-    const long long pi = (long long)(s0 + rm[h]) * p.max_partitions + z;
-    const int head = h0 + rn[h];
-    float* wa = p.ws_acc + (pi * p.num_q_heads + head) * HEAD;
-    const int dcol = 2 * (lane & 3);
+    for (int h = 0; h < 2; ++h) {
+      st.l[h] = warp_sum_xor(st.l[h], 1, 2);
+      if (!rvalid[h]) continue;
+      const long long pi = (long long)(w.s0 + rm[h]) * p.max_partitions + w.z;
+      const int head = w.h0 + rn[h];
+      float* wa = p.ws_acc + (pi * p.num_q_heads + head) * HEAD;
+      const int dcol = 2 * (lane & 3);
 #pragma unroll
-    for (int dn = 0; dn < G::kNDim; ++dn)
-      *reinterpret_cast<float2*>(wa + 8 * dn + dcol) = make_float2(st.acc[dn][2 * h], st.acc[dn][2 * h + 1]);
-    if ((lane & 3) == 0) p.ws_ml[pi * p.num_q_heads + head] = make_float2(st.m[h], st.l[h]);
+      for (int dn = 0; dn < G::kNDim; ++dn)
+        *reinterpret_cast<float2*>(wa + 8 * dn + dcol) = make_float2(st.acc[dn][2 * h], st.acc[dn][2 * h + 1]);
+      if ((lane & 3) == 0) p.ws_ml[pi * p.num_q_heads + head] = make_float2(st.m[h], st.l[h]);
+    }
   }
 }
 
@@ -321,6 +352,8 @@ cudaError_t launch_shared_t(const AttnParams& p, int grid_z, const CUtensorMap* 
   constexpr int smem = prefill_smem_bytes<HEAD, BS>();
   auto kern = shared_prefix_tile_kernel<QDT, HEAD, BS>;
   static int configured_device = -1;
+  static int resident = 0;  // CTAs of this kernel per SM at the block size used
+  static int resident_threads = 0;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
@@ -330,12 +363,27 @@ cudaError_t launch_shared_t(const AttnParams& p, int grid_z, const CUtensorMap* 
       return e;
     }
     configured_device = dev;
+    resident_threads = 0;
   }
   int gp = 1;
   while (gp < (p.group < 8 ? p.group : 8)) gp <<= 1;
   const int nwc = (p.max_group_size * gp + 15) / 16;
-  dim3 grid(p.num_groups, p.num_kv_heads * p.num_head_groups, grid_z);
-  kern<<<grid, (nwc + 1) * 32, smem, stream>>>(p, *tk, *tv);
+  const int threads = (nwc + 1) * 32;
+  if (resident_threads != threads) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess || n < 1) {
+      (void)cudaGetLastError();
+      n = 1;
+    }
+    resident = n;
+    resident_threads = threads;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
+  const long long items = (long long)p.num_groups * p.num_kv_heads * p.num_head_groups * grid_z;
+  const long long grid = std::min<long long>(items, (long long)resident * sms);
+  if (grid <= 0) return cudaSuccess;
+  kern<<<static_cast<unsigned>(grid), threads, smem, stream>>>(p, *tk, *tv, grid_z);
   return cudaGetLastError();
 }
 
