@@ -110,3 +110,26 @@ def test_agentic_full_size_sampled(pa):
     ref = oracle.paged_decode(b.q, b.q_dtype, k, v, b.kv_dtype, tables, b.seq_lens, b.block_size, b.scale,
                               seqs=seqs)
     compare(outs[0], ref, b.kv_dtype, rows=seqs, where="agentic shared prefix")
+
+
+@pytest.mark.parametrize("part", [32, 0])
+def test_many_groups_more_items_than_ctas(pa, part):
+    """40 groups of 1-4 sequences with random lengths and shares: with 32-token
+    partitions there are far more (group, KV head, partition) items than resident
+    CTAs, so each CTA of the shared tiles runs many items of different sizes in turn
+    (and skips the items of singleton groups and past each group's share)."""
+    rng = np.random.default_rng(77)
+    lens, shared_map, starts, shared = [], {}, [0], []
+    for _ in range(40):
+        size = int(rng.integers(1, 5))
+        base = len(lens)
+        L = int(rng.integers(50, 400))
+        nsh = int(rng.integers(0, L // 16 + 1))
+        for m in range(size):
+            lens.append(L + int(rng.integers(0, 40)) if m else L)
+            if m:
+                shared_map[base + m] = (base, nsh)
+        starts.append(len(lens))
+        shared.append(nsh if size > 1 else 0)
+    b = workloads.build("many_groups", 79, lens, [1] * len(lens), 16, 4, 128, 16, "bf16", shared=shared_map)
+    _parity(pa, b, np.array(starts, np.int32), np.array(shared, np.int32), part, max_group=4)
