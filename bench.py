@@ -180,6 +180,7 @@ def unique_kv_tokens(b) -> int:
 
 
 KERNEL_SOURCES = {"decode_mma_kernel": ("attn_decode.cu", "pa_common.cuh"),
+                  "varlen_span": ("attn_decode.cu", "attn_prefill_tc.cu", "pa_common.cuh"),
                   "shared_prefix_span": ("attn_decode.cu", "attn_prefill.cu", "pa_common.cuh"),
                   "prefill_tc_kernel": ("attn_prefill_tc.cu", "pa_common.cuh")}
 
@@ -574,23 +575,37 @@ def run_ours(args):
                     "logical_gbs": nbytes["logical_total"] / (att_ms / 1000.0) / 1e9,
                     "kernel_ms": att_ms}
     else:
+        # the single-token rows (HBM-bound decode kernel) and the multi-token rows
+        # (tensor-bound prefill tiles) run concurrently: their fork -> join span is the
+        # unit, measured against HBM for all the bytes both must move, and against the
+        # tensor peak for the prefill FLOPs
         vsplit = varlen_split(b)
-        dec_gbs = vsplit["decode_bytes"] / (att_ms / 1000.0) / 1e9 if att_ms else 0.0
-        pf_ms = kernel_ms.get("prefill_tiles", 0.0)
-        pf_tflops = vsplit["prefill_flops"] / (pf_ms / 1000.0) / 1e12 if pf_ms else 0.0
+        span_ms = kernel_ms.get("varlen_span", 0.0)
+        qb = workloads.ELEM_BYTES[b.q_dtype]
+        pf_rows = int(sum(int(b.query_start_loc[r + 1] - b.query_start_loc[r]) for r in range(b.num_seqs)
+                          if int(b.query_start_loc[r + 1] - b.query_start_loc[r]) > 1))
+        span_bytes = vsplit["decode_bytes"] + vsplit["prefill_kv_bytes"] + 2 * pf_rows * b.num_q_heads * b.head_size * qb
+        achieved = span_bytes / (span_ms / 1000.0) / 1e9 if span_ms else 0.0
+        pf_tflops = vsplit["prefill_flops"] / (span_ms / 1000.0) / 1e12 if span_ms else 0.0
         tpeak, tkind = measured_bf16_sustained()
-        decode_line = {"bound": "hbm", "achieved": dec_gbs, "peak": peak, "unit": "GB/s", "frac": dec_gbs / peak,
-                       "kernel": "decode_mma_kernel (single-token rows)", "kernel_ms": att_ms,
-                       "algorithmic_bytes_per_launch": vsplit["decode_bytes"],
-                       "traffic": profiled_traffic(args.workload, "decode_mma_kernel")}
-        prefill_line = {"bound": "tensor", "achieved": pf_tflops, "peak": tpeak, "unit": "TFLOP/s",
-                        "frac": pf_tflops / tpeak, "kernel": "prefill_tc_kernel (multi-token rows)",
-                        "kernel_ms": pf_ms, "algorithmic_flops_per_launch": vsplit["prefill_flops"],
-                        "traffic": profiled_traffic(args.workload, "prefill_tc_kernel"),
-                        "peak_source": f"{tkind} MEASURED_PEAKS.json bf16_tflops_sustained"}
-        roofline, other = (prefill_line, decode_line) if pf_ms >= att_ms else (decode_line, prefill_line)
-        roofline = dict(roofline, secondary=other)
-        achieved = dec_gbs
+        kernel_name = "decode_mma_kernel || prefill_tc_kernel (one fork-join span)"
+        overlapped = {"decode_mma_kernel": att_ms, "prefill_tc_kernel": kernel_ms.get("prefill_tiles", 0.0)}
+        hbm_line = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                    "traffic": profiled_traffic(args.workload, "varlen_span"), "kernel": kernel_name,
+                    "peak_source": f"{peak_kind} MEASURED_PEAKS.json hbm_gbs",
+                    "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                    "algorithmic_bytes_per_launch": span_bytes, "kernel_ms": span_ms,
+                    "overlapped_kernel_ms": overlapped}
+        tensor_line = {"bound": "tensor", "achieved": pf_tflops, "peak": tpeak, "unit": "TFLOP/s",
+                       "frac": pf_tflops / tpeak, "kernel": kernel_name, "kernel_ms": span_ms,
+                       "algorithmic_flops_per_launch": vsplit["prefill_flops"],
+                       "traffic": profiled_traffic(args.workload, "varlen_span"),
+                       "peak_source": f"{tkind} MEASURED_PEAKS.json bf16_tflops_sustained",
+                       "overlapped_kernel_ms": overlapped}
+        # the binding resource: the larger of the two lower bounds on the span
+        roofline, other = ((hbm_line, tensor_line) if hbm_line["frac"] >= tensor_line["frac"]
+                           else (tensor_line, hbm_line))
+        roofline = dict(roofline, secondary={k: v for k, v in other.items() if k != "overlapped_kernel_ms"})
 
     # ---- end to end through the public API with host buffers (pinned), K steps
     e2e = None

@@ -413,7 +413,9 @@ pa_status pa_get_error_flags(uint32_t* flags, int32_t clear, pa_stream_t stream)
  * synchronises those events and, for kernel kind `kind` (0 = reshape_and_cache,
  * 1 = attention main kernel, 2 = partial merge, 3 = varlen plan,
  * 4 = prefill tiles, 5 = shared-prefix tiles, 6 = the span of the shared-prefix
- * and private-remainder kernels of pa_decode_shared_prefix, 7 = copy_blocks),
+ * and private-remainder kernels of pa_decode_shared_prefix, 7 = copy_blocks,
+ * 8 = the span of the single-token-row and multi-token-row kernels of
+ * pa_varlen_attn, which run concurrently on two streams),
  * returns the launch count and the summed device milliseconds since the last
  * reset (reset != 0 clears every kind).
  * Tracing is off by default and costs nothing when off.  Not thread-safe.

@@ -40,7 +40,7 @@ PA_ERRFLAG_BLOCK_TABLE, PA_ERRFLAG_SLOT, PA_ERRFLAG_SEQ_LEN, PA_ERRFLAG_QUERY, P
 
 # Names of the kernel kinds reported by pa_trace_read.
 TRACE_KINDS = ("reshape_and_cache", "attention", "merge", "varlen_plan", "prefill_tiles", "shared_prefix",
-               "shared_span", "copy_blocks")
+               "shared_span", "copy_blocks", "varlen_span")
 
 # Every symbol include/pa.h declares, with its ctypes signature.
 _P, _I32, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float

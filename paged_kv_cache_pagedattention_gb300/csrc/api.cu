@@ -264,7 +264,7 @@ bool cache_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k_cache, const voi
 
 // ------------------------------------------------------------------ tracing
 
-constexpr int kTraceKinds = 8;
+constexpr int kTraceKinds = 9;
 bool g_trace_on = false;
 struct TraceSlot {
   int kind;
@@ -769,20 +769,35 @@ pa_status pa_varlen_attn_windowed(void* out, const void* q, const void* k_cache,
     e = pa::launch_attn_generic(p, q_dtype, kv_dtype, std::max(grid_all, grid_pf), -1, s);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   } else {
-    if (fast_decode) {
-      TraceScope t(1, s);
-      e = pa::launch_decode_mma(p, q_dtype, kv_dtype, grid_dec, &tk, &tv, s);
-    } else {
-      TraceScope t(1, s);
-      e = pa::launch_attn_generic(p, q_dtype, kv_dtype, grid_dec, 0, s);
-    }
-    if (e != cudaSuccess) return PA_ERR_CUDA;
+    // The decode rows (HBM-bound) and the prefill tiles (tensor-bound) touch disjoint
+    // rows and partial slots: the tiles run on the side stream, concurrently, and are
+    // joined back before the merge.
+    std::lock_guard<std::mutex> lock(g_side_mutex);
+    SideStream* side = multi ? side_stream() : nullptr;
+    TraceScope span(8, s);  // decode rows and prefill tiles together
+    cudaStream_t s2 = s;
+    if (side && cudaEventRecord(side->fork, s) == cudaSuccess &&
+        cudaStreamWaitEvent(side->stream, side->fork, 0) == cudaSuccess)
+      s2 = side->stream;
     if (multi && fast_prefill) {
-      TraceScope t(4, s);
-      e = pa::launch_prefill_tc(p, q_dtype, kv_dtype, static_cast<int>(L.max_work), &tk1, &tv, s);
+      TraceScope t(4, s2);
+      e = pa::launch_prefill_tc(p, q_dtype, kv_dtype, static_cast<int>(L.max_work), &tk1, &tv, s2);
     } else if (multi) {
-      TraceScope t(1, s);
-      e = pa::launch_attn_generic(p, q_dtype, kv_dtype, grid_pf, 1, s);
+      TraceScope t(1, s2);
+      e = pa::launch_attn_generic(p, q_dtype, kv_dtype, grid_pf, 1, s2);
+    }
+    if (e == cudaSuccess) {
+      if (fast_decode) {
+        TraceScope t(1, s);
+        e = pa::launch_decode_mma(p, q_dtype, kv_dtype, grid_dec, &tk, &tv, s);
+      } else {
+        TraceScope t(1, s);
+        e = pa::launch_attn_generic(p, q_dtype, kv_dtype, grid_dec, 0, s);
+      }
+    }
+    if (s2 != s) {  // join, even after a failed launch, so the caller's stream stays ordered
+      if (cudaEventRecord(side->join, s2) != cudaSuccess || cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess)
+        e = cudaErrorUnknown;
     }
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
