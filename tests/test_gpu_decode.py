@@ -239,6 +239,12 @@ def test_fp8_full_size_sampled(pa):
     _sampled_full_size(pa, b, [0, 100, 255])
 
 
+@pytest.mark.slow
+def test_fp8_e5m2_full_size_sampled(pa):
+    b = workloads.fp8_e5m2()
+    _sampled_full_size(pa, b, [1, 128, 254])
+
+
 PER_HEAD = [0.011, 2.0 ** -6, 0.3, 2.0 ** -2, 0.05, 1.0, 2.0 ** -9, 0.0071]
 
 

@@ -98,8 +98,9 @@ def test_bad_query_start_loc_flagged(pa):
 
 
 @pytest.mark.slow
-def test_mixed_full_size_sampled(pa):
-    b = workloads.mixed()
+@pytest.mark.parametrize("kind", ["mixed", "mixed_fp8", "mixed_nvfp4"])
+def test_mixed_full_size_sampled(pa, kind):
+    b = workloads.NAMED[kind]()
     db = DeviceBatch(b, DEV)
     qsl = b.query_start_loc
     rng = np.random.default_rng(0)
@@ -118,8 +119,8 @@ def test_mixed_full_size_sampled(pa):
     k, v, tables = sampled_oracle_inputs(db, seqs, gpu)
     assert pa.pa_get_error_flags() == 0
     ref = oracle.paged_varlen(b.q, b.q_dtype, k, v, b.kv_dtype, tables, b.query_start_loc, b.seq_lens,
-                              b.block_size, b.scale, True, rows=rows)
-    compare(outs[0], ref, b.kv_dtype, rows=sorted(set(rows)), where="mixed full size")
+                              b.block_size, b.scale, True, b.k_scale, b.v_scale, rows=rows)
+    compare(outs[0], ref, b.kv_dtype, rows=sorted(set(rows)), where=b.name + " full size")
 
 
 @pytest.mark.parametrize("kv", ["fp8_e4m3", "fp8_e5m2"])
