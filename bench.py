@@ -537,7 +537,8 @@ def run_ours(args):
     ms_per_step = ms_graph if ms_graph is not None else ms_eager
     ctx_tokens = int(sum(window_tokens(b, args.window)))
     tok_s = ctx_tokens * world / (ms_per_step / 1000.0)
-    launches = sum(n for n, _ in trace.values())
+    # kernel launches: every traced kind but the fork-join spans (which wrap launches)
+    launches = sum(n for name, (n, _) in trace.items() if not name.endswith("_span"))
 
     # ---- roofline of the dominant kernel
     nbytes = algorithmic_bytes(b, args.window)
@@ -669,7 +670,7 @@ def run_ours(args):
                 "step_launch": "cuda_graph_replay" if ms_graph is not None else "eager",
                 "ms_per_step_eager": ms_eager,
                 "gpu_launches": launches,
-                "launches_by_kernel": {k: v[0] for k, v in trace.items() if v[0]},
+                "launches_by_kernel": {k: v[0] for k, v in trace.items() if v[0] and not k.endswith("_span")},
                 "kernel_ms_by_kind": {k: v for k, v in kernel_ms.items() if v},
                 "clocks": clocks}
         print(json.dumps(line), flush=True)

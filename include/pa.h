@@ -369,6 +369,11 @@ size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t total_q_tokens, int32_
  *                  that many tokens for every row
  *   the rest as pa_decode.  A request with q_len == 0 is skipped.
  * pa_decode equals pa_varlen_attn with q_len = 1 for every request.
+ * The single-token rows and the multi-token rows' tiles run concurrently: the
+ * call forks a library-owned side stream from `stream` with events and joins it
+ * back before its last kernel, so the call stays ordered on `stream` (and can be
+ * captured into a CUDA graph).  The tiles are claimed through a counter in the
+ * workspace, which the call's own plan kernel resets.
  */
 pa_status pa_varlen_attn(void* out, const void* q, const void* k_cache, const void* v_cache,
                          int32_t num_blocks, const int32_t* block_tables,
@@ -412,7 +417,8 @@ pa_status pa_get_error_flags(uint32_t* flags, int32_t clear, pa_stream_t stream)
  * bracketed by CUDA events recorded on its launch stream.  pa_trace_read()
  * synchronises those events and, for kernel kind `kind` (0 = reshape_and_cache,
  * 1 = attention main kernel, 2 = partial merge, 3 = varlen plan,
- * 4 = prefill tiles, 5 = shared-prefix tiles, 6 = the span of the shared-prefix
+ * 4 = prefill tiles (two launches per pa_varlen_attn call when single-token rows
+ * run beside them), 5 = shared-prefix tiles, 6 = the span of the shared-prefix
  * and private-remainder kernels of pa_decode_shared_prefix, 7 = copy_blocks,
  * 8 = the span of the single-token-row and multi-token-row kernels of
  * pa_varlen_attn, which run concurrently on two streams),

@@ -21,6 +21,10 @@ using pa::AttnParams;
 __device__ unsigned g_pa_error_word;
 
 constexpr int kMaxDevices = 64;
+// Share of the SMs the prefill tiles' first (side-stream) grid holds while the decode
+// rows of a varlen step run beside it.
+constexpr int kPrefillShareNum = 2;
+constexpr int kPrefillShareDen = 3;
 
 int current_device() {
   int dev = 0;
@@ -712,11 +716,12 @@ pa_status pa_varlen_attn_windowed(void* out, const void* q, const void* k_cache,
   const VarlenLayout L = varlen_layout(num_seqs, total_q_tokens, num_q_heads, num_kv_heads, head_size,
                                        max_seq_len, block_size, partition_size);
   if (workspace_bytes < L.total) return PA_ERR_WORKSPACE;
-  if (L.max_work > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   AttnParams p = base_params(out, q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                              num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, scale,
                              k_scale, v_scale);
   p.scale_stride = scale_stride;
+  // prefill tiles are claimed by index over (work item, KV head group)
+  if (L.max_work * p.num_kv_heads * p.num_head_groups > (1LL << 30)) return PA_ERR_UNSUPPORTED;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.query_start_loc = query_start_loc;
   p.num_rows = total_q_tokens;
@@ -732,6 +737,8 @@ pa_status pa_varlen_attn_windowed(void* out, const void* q, const void* k_cache,
   const int grid_pf = window_partitions(L.parts_pf, window, max_query_len, block_size, L.part_pf);
   int32_t* work_count = reinterpret_cast<int32_t*>(ws);
   p.plan_ok = reinterpret_cast<int32_t*>(ws + 4);
+  p.work_claim = reinterpret_cast<int32_t*>(ws + 8);
+  p.work_full = reinterpret_cast<int32_t*>(ws + 12);
   int32_t* part_off = reinterpret_cast<int32_t*>(ws + L.off_off);
   int4* work = reinterpret_cast<int4*>(ws + L.work_off);
   p.part_off = part_off;
@@ -770,8 +777,14 @@ pa_status pa_varlen_attn_windowed(void* out, const void* q, const void* k_cache,
     if (e != cudaSuccess) return PA_ERR_CUDA;
   } else {
     // The decode rows (HBM-bound) and the prefill tiles (tensor-bound) touch disjoint
-    // rows and partial slots: the tiles run on the side stream, concurrently, and are
-    // joined back before the merge.
+    // rows and partial slots, so they run concurrently: the tiles on the caller's
+    // stream, right behind the plan, so that their CTAs are resident first; the decode
+    // rows on the side stream, joined back before the merge.  The tiles' persistent
+    // grid then holds about two thirds of the SMs (one CTA per SM) and the decode rows
+    // keep the rest: HBM stays near its copy rate from ~80 free SMs on (an SM-holding
+    // probe measured 6.9 of 7.1 TB/s).  A second grid over every SM follows the decode
+    // rows and claims whatever tiles are left, so SMs the decode rows free up go to the
+    // tiles; if the tiles finish first, the decode grid spreads over every SM.
     std::lock_guard<std::mutex> lock(g_side_mutex);
     SideStream* side = multi ? side_stream() : nullptr;
     TraceScope span(8, s);  // decode rows and prefill tiles together
@@ -779,21 +792,24 @@ pa_status pa_varlen_attn_windowed(void* out, const void* q, const void* k_cache,
     if (side && cudaEventRecord(side->fork, s) == cudaSuccess &&
         cudaStreamWaitEvent(side->stream, side->fork, 0) == cudaSuccess)
       s2 = side->stream;
+    const int sms = sm_count();
+    const bool split = multi && fast_prefill && s2 != s;
     if (multi && fast_prefill) {
-      TraceScope t(4, s2);
-      e = pa::launch_prefill_tc(p, q_dtype, kv_dtype, static_cast<int>(L.max_work), &tk1, &tv, s2);
+      TraceScope t(4, s);
+      const int ctas = split ? std::max(1, (sms * kPrefillShareNum) / kPrefillShareDen) : sms;
+      e = pa::launch_prefill_tc(p, q_dtype, kv_dtype, static_cast<int>(L.max_work), ctas, &tk1, &tv, s);
     } else if (multi) {
-      TraceScope t(1, s2);
-      e = pa::launch_attn_generic(p, q_dtype, kv_dtype, grid_pf, 1, s2);
+      TraceScope t(1, s);
+      e = pa::launch_attn_generic(p, q_dtype, kv_dtype, grid_pf, 1, s);
     }
     if (e == cudaSuccess) {
-      if (fast_decode) {
-        TraceScope t(1, s);
-        e = pa::launch_decode_mma(p, q_dtype, kv_dtype, grid_dec, &tk, &tv, s);
-      } else {
-        TraceScope t(1, s);
-        e = pa::launch_attn_generic(p, q_dtype, kv_dtype, grid_dec, 0, s);
-      }
+      TraceScope t(1, s2);
+      e = fast_decode ? pa::launch_decode_mma(p, q_dtype, kv_dtype, grid_dec, &tk, &tv, s2)
+                      : pa::launch_attn_generic(p, q_dtype, kv_dtype, grid_dec, 0, s2);
+    }
+    if (e == cudaSuccess && split) {  // the tiles still unclaimed
+      TraceScope t(4, s2);
+      e = pa::launch_prefill_tc(p, q_dtype, kv_dtype, static_cast<int>(L.max_work), sms, &tk1, &tv, s2);
     }
     if (s2 != s) {  // join, even after a failed launch, so the caller's stream stays ordered
       if (cudaEventRecord(side->join, s2) != cudaSuccess || cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess)

@@ -369,99 +369,145 @@ __global__ void __launch_bounds__(kMergeThreads) merge_wide_kernel(const AttnPar
   }
 }
 
+// One request's plan: where its partial rows go and which prefill tiles it needs.  A
+// row tile of tile_tokens query tokens needs the partitions up to its last key; all
+// but the last of them span a whole partition.
+struct RequestPlan {
+  int q_len, seq_len, part, origin, parts;
+  int full_tiles;  // prefill tiles over a whole partition
+  int last_tiles;  // prefill tiles over a row tile's last partition
+  bool ok;
+};
+
+__device__ int tile_partitions(const AttnParams& p, const RequestPlan& rp, int t0, int tile_tokens) {
+  const int last = min(t0 + tile_tokens, rp.q_len) - 1;
+  const int kv = p.causal ? rp.seq_len - rp.q_len + last + 1 : rp.seq_len;
+  return ceil_div_dev(kv - rp.origin, rp.part);
+}
+
+__device__ RequestPlan plan_request(const AttnParams& p, int r, int tile_tokens) {
+  RequestPlan rp;
+  rp.q_len = p.query_start_loc[r + 1] - p.query_start_loc[r];
+  rp.seq_len = p.seq_lens[r];
+  rp.part = p.part;
+  rp.origin = 0;
+  rp.parts = 0;
+  rp.full_tiles = 0;
+  rp.last_tiles = 0;
+  rp.ok = rp.q_len >= 0 && rp.q_len <= p.max_query_len && rp.q_len <= rp.seq_len &&
+          rp.seq_len <= p.max_seq_len && (long long)rp.seq_len <= (long long)p.max_blocks_per_seq * p.block_size;
+  if (rp.ok && rp.q_len > 0 && rp.seq_len >= 1) {
+    rp.part = rp.q_len == 1 ? p.part : p.part_pf;
+    rp.origin = window_origin(p, rp.seq_len, rp.q_len);
+    rp.parts = ceil_div_dev(rp.seq_len - rp.origin, rp.part);
+    if (rp.q_len > 1) {
+      for (int t0 = 0; t0 < rp.q_len; t0 += tile_tokens) {
+        const int np = tile_partitions(p, rp, t0, tile_tokens);
+        if (np > 0) {
+          rp.full_tiles += np - 1;
+          rp.last_tiles += 1;
+        }
+      }
+    }
+  }
+  return rp;
+}
+
 // Single CTA.  For each request: validates its query range and computes
 //   part_off[r] = sum over earlier requests of q_len * ceil(seq_len / part_r),
-// the index of its first partial row, and appends its prefill tiles (requests
-// with q_len > 1) to the work list as (request, first query row, partition, 0).
+// the index of its first partial row, and lists its prefill tiles (requests with
+// q_len > 1) as (request, first query row, partition, 0): first every tile over a
+// whole partition (work_full of them), then each row tile's last, shorter one, so
+// that the persistent tile grids claim the long tiles first and the short ones fill
+// the tail.
 __global__ void __launch_bounds__(1024)
     varlen_plan_kernel(const AttnParams p, int32_t* part_off, int4* work, int32_t* work_count,
                        int32_t* plan_ok, int max_work, int tile_tokens) {
-  __shared__ int warp_tot[2][32];
-  __shared__ int carry[2];
-  __shared__ int bad;
+  __shared__ int warp_tot[3][32];
+  __shared__ int carry[3];
+  __shared__ int bad, full_total;
   const int tid = threadIdx.x;
   const int lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
   if (tid == 0) {
-    carry[0] = 0;
-    carry[1] = 0;
+    carry[0] = carry[1] = carry[2] = 0;
+    full_total = 0;
     const int q0 = p.query_start_loc[0], qn = p.query_start_loc[p.num_seqs];
     bad = (q0 != 0 || qn != p.num_rows) ? 1 : 0;
   }
   __syncthreads();
+  // pass 1: the number of whole-partition tiles, after which the last tiles start
   for (int base = 0; base < p.num_seqs; base += blockDim.x) {
     const int r = base + tid;
-    int parts = 0, items = 0;
-    int q_len = 0, seq_len = 0, part = p.part;
+    int nf = r < p.num_seqs ? plan_request(p, r, tile_tokens).full_tiles : 0;
+    for (int o = 16; o > 0; o >>= 1) nf += __shfl_xor_sync(0xffffffffu, nf, o);
+    if (lane == 0 && nf) atomicAdd(&full_total, nf);
+  }
+  __syncthreads();
+  // pass 2: exclusive scans of (partial rows, whole-partition tiles, last tiles)
+  for (int base = 0; base < p.num_seqs; base += blockDim.x) {
+    const int r = base + tid;
+    RequestPlan rp;
+    rp.q_len = 0;
+    rp.parts = 0;
+    rp.full_tiles = 0;
+    rp.last_tiles = 0;
     if (r < p.num_seqs) {
-      q_len = p.query_start_loc[r + 1] - p.query_start_loc[r];
-      if (q_len < 0) atomicOr(&bad, 1);
-      seq_len = p.seq_lens[r];
-      const bool ok = q_len >= 0 && q_len <= p.max_query_len && q_len <= seq_len &&
-                      seq_len <= p.max_seq_len &&
-                      (long long)seq_len <= (long long)p.max_blocks_per_seq * p.block_size;
-      if (!ok && q_len != 0) flag_error(p.err, q_len < 0 || q_len > p.max_query_len || q_len > seq_len
-                                                   ? PA_ERRFLAG_QUERY : PA_ERRFLAG_SEQ_LEN);
-      if (ok && q_len > 0 && seq_len >= 1) {
-        part = q_len == 1 ? p.part : p.part_pf;
-        const int origin = window_origin(p, seq_len, q_len);
-        parts = ceil_div_dev(seq_len - origin, part);
-        if (q_len > 1) {
-          // tiles of tile_tokens query tokens; a tile needs the partitions up to its last key
-          for (int t0 = 0; t0 < q_len; t0 += tile_tokens) {
-            const int last = min(t0 + tile_tokens, q_len) - 1;
-            const int kv = p.causal ? seq_len - q_len + last + 1 : seq_len;
-            items += ceil_div_dev(kv - origin, part);
+      rp = plan_request(p, r, tile_tokens);
+      if (rp.q_len < 0) atomicOr(&bad, 1);
+      if (!rp.ok && rp.q_len != 0)
+        flag_error(p.err, rp.q_len < 0 || rp.q_len > p.max_query_len || rp.q_len > rp.seq_len
+                              ? PA_ERRFLAG_QUERY : PA_ERRFLAG_SEQ_LEN);
+    }
+    const int v[3] = {rp.q_len > 0 ? rp.q_len * rp.parts : 0, rp.full_tiles, rp.last_tiles};
+    int sc[3] = {v[0], v[1], v[2]};
+    for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        const int a = __shfl_up_sync(0xffffffffu, sc[k], o);
+        if (lane >= o) sc[k] += a;
+      }
+    }
+    if (lane == 31)
+      for (int k = 0; k < 3; ++k) warp_tot[k][wid] = sc[k];
+    __syncthreads();
+    if (wid == 0) {
+      for (int k = 0; k < 3; ++k) {
+        int a = lane < nw ? warp_tot[k][lane] : 0;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int x = __shfl_up_sync(0xffffffffu, a, o);
+          if (lane >= o) a += x;
+        }
+        warp_tot[k][lane] = a;
+      }
+    }
+    __syncthreads();
+    int ex[3];
+    for (int k = 0; k < 3; ++k) ex[k] = carry[k] + (wid ? warp_tot[k][wid - 1] : 0) + sc[k] - v[k];
+    if (r < p.num_seqs) {
+      part_off[r] = ex[0];
+      if (rp.full_tiles + rp.last_tiles) {
+        int kf = ex[1], kl = full_total + ex[2];
+        const int row0 = p.query_start_loc[r];
+        for (int t0 = 0; t0 < rp.q_len; t0 += tile_tokens) {
+          const int np = tile_partitions(p, rp, t0, tile_tokens);
+          for (int z = 0; z < np; ++z) {
+            const int k = z + 1 < np ? kf++ : kl++;
+            if (k < max_work) work[k] = make_int4(r, row0 + t0, z, 0);
           }
         }
       }
     }
-    int v0 = q_len > 0 ? q_len * parts : 0;
-    int v1 = items;
-    // block-wide exclusive scans of v0 and v1
-    int s0 = v0, s1 = v1;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int a = __shfl_up_sync(0xffffffffu, s0, o), b = __shfl_up_sync(0xffffffffu, s1, o);
-      if (lane >= o) { s0 += a; s1 += b; }
-    }
-    if (lane == 31) { warp_tot[0][wid] = s0; warp_tot[1][wid] = s1; }
     __syncthreads();
-    if (wid == 0) {
-      int a = lane < nw ? warp_tot[0][lane] : 0, b = lane < nw ? warp_tot[1][lane] : 0;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int x = __shfl_up_sync(0xffffffffu, a, o), y = __shfl_up_sync(0xffffffffu, b, o);
-        if (lane >= o) { a += x; b += y; }
-      }
-      warp_tot[0][lane] = a;
-      warp_tot[1][lane] = b;
-    }
-    __syncthreads();
-    const int ex0 = carry[0] + (wid ? warp_tot[0][wid - 1] : 0) + s0 - v0;
-    const int ex1 = carry[1] + (wid ? warp_tot[1][wid - 1] : 0) + s1 - v1;
-    if (r < p.num_seqs) {
-      part_off[r] = ex0;
-      if (items) {
-        int k = ex1;
-        const int row0 = p.query_start_loc[r];
-        const int origin = window_origin(p, seq_len, q_len);
-        for (int t0 = 0; t0 < q_len; t0 += tile_tokens) {
-          const int last = min(t0 + tile_tokens, q_len) - 1;
-          const int kv = p.causal ? seq_len - q_len + last + 1 : seq_len;
-          const int np = ceil_div_dev(kv - origin, part);
-          for (int z = 0; z < np; ++z, ++k)
-            if (k < max_work) work[k] = make_int4(r, row0 + t0, z, 0);
-        }
-      }
-    }
-    __syncthreads();
-    if (tid == 0) {
-      carry[0] += warp_tot[0][nw - 1];
-      carry[1] += warp_tot[1][nw - 1];
-    }
+    if (tid == 0)
+      for (int k = 0; k < 3; ++k) carry[k] += warp_tot[k][nw - 1];
     __syncthreads();
   }
   if (tid == 0) {
-    *work_count = bad ? 0 : min(carry[1], max_work);
+    const int count = bad ? 0 : min(full_total + carry[2], max_work);
+    *work_count = count;
+    if (p.work_full) *p.work_full = min(full_total, count);
     *plan_ok = bad ? 0 : 1;
+    if (p.work_claim) *p.work_claim = 0;
     if (bad) flag_error(p.err, PA_ERRFLAG_QUERY);
   }
 }

@@ -32,6 +32,8 @@
 // V is MN-major (head dim contiguous) and kept as the cache lays it out per block,
 // [block][piece][token][128 bytes], one TMA box per block; every operand uses the
 // 128-byte swizzle.
+#include <algorithm>
+
 #include "pa_common.cuh"
 
 namespace pa {
@@ -218,47 +220,17 @@ __global__ void __launch_bounds__(threads_tc<is_scaled<KVDT>()>(), 1)
   constexpr int ST = G::kStages;
   constexpr int NB = G::kBlocks;
 
-  if (plan_rejected(p) || (int)blockIdx.x >= *p.work_count) return;
-  const int4 item = p.work[blockIdx.x];
-  const int r = item.x, row0 = item.y, z = item.z;
-  const int kvh = blockIdx.y / p.num_head_groups, hg = blockIdx.y % p.num_head_groups;
-  const int h0 = kvh * p.group + hg * 8;
-  const int nh = min(8, p.group - hg * 8);
-  int gp = 1;
-  while (gp < min(p.group, 8)) gp <<= 1;
-  const int tile_tokens = kRows / gp;                   // query tokens of one 128-row tile
-  const int qs = p.query_start_loc[r];
-  const int q_len = p.query_start_loc[r + 1] - qs;
-  const int seq_len = p.seq_lens[r];
-  const int t0 = row0 - qs;                             // first token of the CTA in its request
-  const int ntok = min(kTiles * tile_tokens, q_len - t0);
-  const int pos0 = seq_len - q_len + t0;                // position of the CTA's first token
-  const int part = p.part_pf;
-  // partitions count from the request's origin (0, or the block where the first
-  // query's sliding window starts)
-  const int origin = window_origin(p, seq_len, q_len);
-  const int parts_req = (seq_len - origin + part - 1) / part;
-  const int k0 = origin + z * part;
-  // chunks start at the block holding the first key the CTA's first row attends
-  const int klo = p.window > 0 ? max(k0, max(0, pos0 - p.window + 1) / BS * BS) : k0;
-  // keys [klo, k1) of this partition that some row of tile t attends -> its chunks
-  auto tile_chunks = [&](int t) {
-    const int nt = min(ntok, (t + 1) * tile_tokens) - t * tile_tokens;
-    if (nt <= 0) return 0;
-    const int k1t = min(k0 + part, p.causal ? pos0 + t * tile_tokens + nt : seq_len);
-    return k1t > klo ? (k1t - klo + kChunk - 1) / kChunk : 0;
-  };
-  static_assert(kTiles == 2, "two tiles per CTA");
-  const int nch_t[kTiles] = {tile_chunks(0), tile_chunks(1)};
-  const int k1 = min(k0 + part, p.causal ? pos0 + ntok : seq_len);
-  const int nch = k1 > klo ? (k1 - klo + kChunk - 1) / kChunk : 0;  // = the largest nch_t
-  const int kb_first = klo / BS;
-  // keys held by the blocks a chunk loads end at the last block that reaches k1; V
-  // rows past them (or past seq_len) are zeroed before they meet P.  Only the last
-  // chunk can hold such rows; the last tile that reads it zeroes them.
-  const int kv_loaded_end = min(seq_len, (k1 + BS - 1) / BS * BS);
-  const bool tail_chunk = nch > 0 && klo + nch * kChunk > kv_loaded_end;
-  const int zero_tile = nch_t[kTiles - 1] == nch ? kTiles - 1 : 0;
+  if (plan_rejected(p)) return;
+  // Persistent: each CTA claims (work item, KV head group) tiles from a counter the
+  // plan kernel zeroes, so launches of any size share one list.  Claims run over the
+  // whole-partition items first, then over the rest (each row tile's last, shorter
+  // partition); within each class the item runs fastest, so the row tiles that read
+  // one partition of one KV head are in flight together and share it through L2.
+  const int nwork = *p.work_count;
+  const int nfull = *p.work_full;
+  const int ny = p.num_kv_heads * p.num_head_groups;
+  const int total = nwork * ny;
+  const int total_full = nfull * ny;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -285,7 +257,12 @@ __global__ void __launch_bounds__(threads_tc<is_scaled<KVDT>()>(), 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
 
-  // ---- set-up: barriers, the Q tiles (zero rows for padding), TMEM
+  __shared__ int s_next, s_abort;  // the next claimed tile; set when a wait gave up
+  constexpr int RS = kCvt ? G::kStgStages : ST;  // the copy ring: staged codes, or the f16 stages
+  uint64_t* rfull = kCvt ? stg_full : full;
+  uint64_t* rempty = kCvt ? stg_empty : empty;
+
+  // ---- set-up: barriers, the first claim, TMEM
   if (tid == 0) {
     if constexpr (!kFp4) {
       tma_prefetch_desc(&tmk);
@@ -306,503 +283,579 @@ __global__ void __launch_bounds__(threads_tc<is_scaled<KVDT>()>(), 1)
     }
     mbar_init(mma_fin, kTiles);
     fence_mbar_init();
+    s_next = atomicAdd(p.work_claim, 1);
+    s_abort = 0;
   }
-  // CTA row R = token * gp + head; tile R / 128, TMEM lane R % 128
-  const int row_tok = tid / gp, row_head = tid % gp;
-  const bool row_valid = tid < kTiles * kRows && row_tok < ntok && row_head < nh;
-  const int row_pos = pos0 + row_tok;
-  // FP8 caches: the row is scaled by 2^q_shift so that f16 holds it exactly (max |q|
-  // below 2^15); the softmax multiplier takes 2^-q_shift back
-  int q_shift = 0;
-  if (tid < kTiles * kRows) {
-    const uint4* src = row_valid ? reinterpret_cast<const uint4*>(
-                                       reinterpret_cast<const typename QE::T*>(p.q) +
-                                       ((long long)(row0 + row_tok) * p.num_q_heads + h0 + row_head) * HEAD)
-                                 : nullptr;
-    uint8_t* dst = sQ + (tid / kRows) * G::kQTile;
-    if constexpr (!kCvt) {
-#pragma unroll
-      for (int c = 0; c < HEAD / 8; ++c) {
-        const uint4 v = src ? src[c] : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(dst + (c >> 3) * G::kQPiece + swz128(tid % kRows, c & 7)) = v;
-      }
-    } else {
-      float amax = 0.f;
-      for (int c = 0; c < HEAD / 8 && src; ++c) {
-        const uint4 v = src[c];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = unpack2<QDT>(w[e]);
-          amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-        }
-      }
-      int ex = 0;
-      frexpf(amax, &ex);  // amax < 2^ex
-      q_shift = max(-100, min(100, 15 - ex));
-#pragma unroll 4
-      for (int c = 0; c < HEAD / 8; ++c) {
-        const uint4 v = src ? src[c] : make_uint4(0, 0, 0, 0);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t h[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = unpack2<QDT>(w[e]);
-          h[e] = pack2<PA_F16>(ldexpf(f.x, q_shift), ldexpf(f.y, q_shift));
-        }
-        *reinterpret_cast<uint4*>(dst + (c >> 3) * G::kQPiece + swz128(tid % kRows, c & 7)) =
-            make_uint4(h[0], h[1], h[2], h[3]);
-      }
-    }
-  }
-  fence_proxy_async();
+  __syncthreads();
+  int L = s_next;
+  if (L >= total) return;
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const int32_t* table = p.block_tables + (long long)r * p.max_blocks_per_seq;
-
-  if (warp == kProducerWarp || warp == kProducerWarp + 1) {
-    // ------------------------------------------------------------ TMA producers
-    // Lane j holds block table entry kb_first + 32 w + j of window w; the next window
-    // is prefetched.  An elected lane of the first warp copies a chunk's K one piece
-    // of one block at a time; the second warp's copies V one whole block at a time.
-    // Each arrives once per chunk on full with its own byte count.  With an FP8 cache
-    // both copy whole (block, head) tiles of codes into the staging ring instead.
-    constexpr int RS = kCvt ? G::kStgStages : ST;
-    uint64_t* rfull = kCvt ? stg_full : full;
-    uint64_t* rempty = kCvt ? stg_empty : empty;
-    const bool is_v = warp != kProducerWarp;
-    const int kb_end = (k1 + BS - 1) / BS;  // blocks [kb_first, kb_end) are loaded
-    auto load_window = [&](int w) {
-      const int kb = kb_first + 32 * w + lane;
-      return kb < kb_end ? table[kb] : -1;
+  int gch = 0;             // ring chunks of earlier tiles: stages and phases run on
+  int tch0 = 0, tch1 = 0;  // each tile's chunks of earlier tiles: its S / P / O phases run on
+  int g_issued = 0;        // producers: ring chunks issued so far
+  for (;;) {
+    const int lc = L < total_full ? L : L - total_full;  // index within the claim's class
+    const int nc = L < total_full ? nfull : nwork - nfull;
+    const int x = (L < total_full ? 0 : nfull) + lc % nc, y = lc / nc;
+    const int4 item = p.work[x];
+    const int r = item.x, row0 = item.y, z = item.z;
+    const int kvh = y / p.num_head_groups, hg = y % p.num_head_groups;
+    const int h0 = kvh * p.group + hg * 8;
+    const int nh = min(8, p.group - hg * 8);
+    int gp = 1;
+    while (gp < min(p.group, 8)) gp <<= 1;
+    const int tile_tokens = kRows / gp;                   // query tokens of one 128-row tile
+    const int qs = p.query_start_loc[r];
+    const int q_len = p.query_start_loc[r + 1] - qs;
+    const int seq_len = p.seq_lens[r];
+    const int t0 = row0 - qs;                             // first token of the CTA in its request
+    const int ntok = min(kTiles * tile_tokens, q_len - t0);
+    const int pos0 = seq_len - q_len + t0;                // position of the CTA's first token
+    const int part = p.part_pf;
+    // partitions count from the request's origin (0, or the block where the first
+    // query's sliding window starts)
+    const int origin = window_origin(p, seq_len, q_len);
+    const int parts_req = (seq_len - origin + part - 1) / part;
+    const int k0 = origin + z * part;
+    // chunks start at the block holding the first key the CTA's first row attends
+    const int klo = p.window > 0 ? max(k0, max(0, pos0 - p.window + 1) / BS * BS) : k0;
+    // keys [klo, k1) of this partition that some row of tile t attends -> its chunks
+    auto tile_chunks = [&](int t) {
+      const int nt = min(ntok, (t + 1) * tile_tokens) - t * tile_tokens;
+      if (nt <= 0) return 0;
+      const int k1t = min(k0 + part, p.causal ? pos0 + t * tile_tokens + nt : seq_len);
+      return k1t > klo ? (k1t - klo + kChunk - 1) / kChunk : 0;
     };
-    int cur_w = 0;
-    int win = load_window(0);
-    int win_next = load_window(1);
-    int issued = 0;
-    for (int i = 0; i < nch; ++i) {
-      const int s = i % RS;
-      if (i >= RS && !__all_sync(0xffffffffu, mbar_wait_bounded(rempty + s, ((i / RS) - 1) & 1))) {
-        if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-        break;
-      }
-      const int w = (i * NB) >> 5;  // NB divides 32: a chunk's blocks share one window
-      if (w != cur_w) {
-        win = win_next;
-        win_next = load_window(w + 1);
-        cur_w = w;
-      }
-      int phys[NB];
-      int nvalid = 0;
+    static_assert(kTiles == 2, "two tiles per CTA");
+    const int nch_t[kTiles] = {tile_chunks(0), tile_chunks(1)};
+    const int k1 = min(k0 + part, p.causal ? pos0 + ntok : seq_len);
+    const int nch = k1 > klo ? (k1 - klo + kChunk - 1) / kChunk : 0;  // = the largest nch_t
+    const int kb_first = klo / BS;
+    // keys held by the blocks a chunk loads end at the last block that reaches k1; V
+    // rows past them (or past seq_len) are zeroed before they meet P.  Only the last
+    // chunk can hold such rows; the last tile that reads it zeroes them.
+    const int kv_loaded_end = min(seq_len, (k1 + BS - 1) / BS * BS);
+    const bool tail_chunk = nch > 0 && klo + nch * kChunk > kv_loaded_end;
+    const int zero_tile = nch_t[kTiles - 1] == nch ? kTiles - 1 : 0;
+
+    // CTA row R = token * gp + head; tile R / 128, TMEM lane R % 128
+    const int row_tok = tid / gp, row_head = tid % gp;
+    const bool row_valid = tid < kTiles * kRows && row_tok < ntok && row_head < nh;
+    const int row_pos = pos0 + row_tok;
+    // FP8 caches: the row is scaled by 2^q_shift so that f16 holds it exactly (max |q|
+    // below 2^15); the softmax multiplier takes 2^-q_shift back
+    int q_shift = 0;
+    if (tid < kTiles * kRows) {
+      const uint4* src = row_valid ? reinterpret_cast<const uint4*>(
+                                         reinterpret_cast<const typename QE::T*>(p.q) +
+                                         ((long long)(row0 + row_tok) * p.num_q_heads + h0 + row_head) * HEAD)
+                                   : nullptr;
+      uint8_t* dst = sQ + (tid / kRows) * G::kQTile;
+      if constexpr (!kCvt) {
 #pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        const int e = __shfl_sync(0xffffffffu, win, (i * NB + b) & 31);
-        const bool in_range = kb_first + i * NB + b < kb_end;
-        const bool ok_b = in_range && e >= 0 && e < p.num_blocks;
-        if (in_range && !ok_b && lane == 0 && !is_v) flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
-        phys[b] = ok_b ? e : -1;
-        nvalid += ok_b;
-      }
-      if (kCvt && elect_one()) {
-        uint8_t* sg = sStg + s * 2 * G::kStgKv + (is_v ? G::kStgKv : 0);
-        if (nvalid == 0) {
-          mbar_arrive(rfull + s);
-        } else {
-          mbar_arrive_expect_tx(rfull + s, (uint32_t)(nvalid * G::kStgBlock));
-#pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            if (phys[b] < 0) continue;
-            if constexpr (kFp4) {  // a whole tile, as laid out in HBM
-              const void* src = static_cast<const uint8_t*>(is_v ? p.v_cache : p.k_cache) +
-                                ((long long)phys[b] * p.num_kv_heads + kvh) * G::kStgBlock;
-              bulk_load(sg + b * G::kStgBlock, src, G::kStgBlock, rfull + s);
-            } else {
-              tma_load_4d(sg + b * G::kStgBlock, is_v ? &tmv : &tmk, 0, kvh * BS, 0, phys[b], rfull + s);
-            }
-          }
-        }
-      } else if (!kCvt && elect_one()) {
-        uint8_t* sk = sKV + s * G::kStageBytes;
-        if (nvalid == 0) {
-          mbar_arrive(full + s);
-        } else {
-          mbar_arrive_expect_tx(full + s, (uint32_t)(nvalid * G::kBlockTx));
-#pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            if (phys[b] < 0) continue;
-            if (is_v) {
-              tma_load_4d(sk + G::kKvBytes + b * G::kBlockTx, &tmv, 0, kvh * BS, 0, phys[b], full + s);
-            } else {
-#pragma unroll
-              for (int pc = 0; pc < G::kPieces; ++pc)
-                tma_load_4d(sk + pc * G::kPiece + b * BS * 128, &tmk, 0, kvh * BS, pc, phys[b], full + s);
-            }
-          }
-        }
-      }
-      __syncwarp();
-      issued = i + 1;
-    }
-    // every copy lands before the CTA can leave
-    if (lane == 0)
-      for (int j = max(0, issued - RS); j < issued; ++j)
-        if (!mbar_wait_bounded(rfull + j % RS, (j / RS) & 1)) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-  } else if (kCvt && warp >= kConvWarp) {
-    // ------------------------------------------------------------ FP8 / NVFP4 converters
-    // Chunk i: wait for its codes in staging and for its f16 stage to be free, widen
-    // every code to f16 exactly (every e4m3 value and every finite e5m2 value is an
-    // f16 value; NVFP4: E2M1 value x E4M3 block scale, at most 6 significant bits
-    // and within f16's normal range; the fp32 scales are applied later) into the
-    // K-major K layout and the per-block V layout, release the staging slot and mark
-    // the f16 stage full.
-    // Thread t owns one row: K row t (t < 64) or V row t - 64.  Reading group g of
-    // a row and writing its two f16 chunks touch eight different 16-byte bank groups
-    // across any eight consecutive rows, so neither side has bank conflicts.
-    if constexpr (kCvt) {
-    const int ct = tid - kConvWarp * 32;
-    const int tensor = ct / kChunk, key = ct % kChunk;
-    const int blk = key / BS, tok = key % BS, sw = key & 7;  // tok & 7 == key & 7
-    for (int i = 0; i < nch; ++i) {
-      const int s = i % ST, ss = i % G::kStgStages;
-      bool ok = mbar_wait_bounded(stg_full + ss, (i / G::kStgStages) & 1);
-      if (i >= ST) ok = ok && mbar_wait_bounded(empty + s, ((i / ST) - 1) & 1);
-      if (!__all_sync(0xffffffffu, ok)) {
-        if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-        break;
-      }
-      const uint8_t* stile = sStg + ss * 2 * G::kStgKv + tensor * G::kStgKv + blk * G::kStgBlock;
-      uint8_t* sk = sKV + s * G::kStageBytes;
-      uint8_t* drow = tensor == 0 ? sk + key * 128 : sk + G::kKvBytes + blk * G::kBlockTx + tok * 128;
-      const int piece_stride = tensor == 0 ? G::kPiece : BS * 128;
-      if constexpr (kFp4) {
-        // a 64-byte code row and its 8 block scales; the row's four 16-byte chunks are
-        // read in an order rotated by row pair, so a warp's reads spread over the bank
-        // line (64-byte rows) and its writes stay on distinct banks (rows differ in
-        // their swizzle)
-        const uint8_t* crow = stile + tok * (HEAD / 2);
-        const uint2 sc8 = *reinterpret_cast<const uint2*>(stile + BS * (HEAD / 2) + tok * (HEAD / 16));
-        const uint64_t sc64 = (static_cast<uint64_t>(sc8.y) << 32) | sc8.x;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int cc = (c + (key >> 1)) & 3;  // chunk: groups 2cc, 2cc+1 = dims 32cc .. 32cc+31
-          const uint4 codes = *reinterpret_cast<const uint4*>(crow + 16 * cc);
-          const uint32_t sp = fp8x2_to_f16x2<PA_FP8_E4M3>(static_cast<uint16_t>(sc64 >> (16 * cc)));
-          const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {  // group g = 2cc + hh: codes 16 g .. 16 g + 15
-            const int g = 2 * cc + hh;
-            const uint32_t sg = __byte_perm(sp, 0, hh ? 0x3232 : 0x1010);
-            uint32_t lo[4], hi[4];
-            fp4x8_to_f16x2x4(cw[2 * hh], lo);
-            fp4x8_to_f16x2x4(cw[2 * hh + 1], hi);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              lo[e] = hmul2_u32(lo[e], sg);
-              hi[e] = hmul2_u32(hi[e], sg);
-            }
-            uint8_t* row = drow + (g >> 2) * piece_stride;
-            const int ch = (2 * g) & 7;
-            *reinterpret_cast<uint4*>(row + ((ch ^ sw) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            *reinterpret_cast<uint4*>(row + (((ch + 1) ^ sw) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          }
+        for (int c = 0; c < HEAD / 8; ++c) {
+          const uint4 v = src ? src[c] : make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(dst + (c >> 3) * G::kQPiece + swz128(tid % kRows, c & 7)) = v;
         }
       } else {
-        const uint8_t* srow = stile + tok * 128;
+        float amax = 0.f;
+        for (int c = 0; c < HEAD / 8 && src; ++c) {
+          const uint4 v = src[c];
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {  // codes 16 g .. 16 g + 15 -> f16 chunks 2g, 2g+1 (mod 8) of piece g / 4
-          const uint4 codes = *reinterpret_cast<const uint4*>(srow + ((g ^ sw) << 4));
-          const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
-          uint32_t h[8];
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = unpack2<QDT>(w[e]);
+            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+          }
+        }
+        int ex = 0;
+        frexpf(amax, &ex);  // amax < 2^ex
+        q_shift = max(-100, min(100, 15 - ex));
+#pragma unroll 4
+        for (int c = 0; c < HEAD / 8; ++c) {
+          const uint4 v = src ? src[c] : make_uint4(0, 0, 0, 0);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          uint32_t h[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) fp8x4_to_f16x2x2<KVDT>(cw[e], h[2 * e], h[2 * e + 1]);
-          uint8_t* row = drow + (g >> 2) * piece_stride;
-          const int cc = (2 * g) & 7;
-          *reinterpret_cast<uint4*>(row + ((cc ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-          *reinterpret_cast<uint4*>(row + (((cc + 1) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = unpack2<QDT>(w[e]);
+            h[e] = pack2<PA_F16>(ldexpf(f.x, q_shift), ldexpf(f.y, q_shift));
+          }
+          *reinterpret_cast<uint4*>(dst + (c >> 3) * G::kQPiece + swz128(tid % kRows, c & 7)) =
+              make_uint4(h[0], h[1], h[2], h[3]);
         }
       }
-      fence_proxy_async();  // generic-proxy writes, read next by the tensor core
-      mbar_arrive(stg_empty + ss);
-      mbar_arrive(full + s);
     }
-    }
-  } else if (warp >= kMmaWarp && warp < kConvWarp) {
-    // ------------------------------------------------------------ MMA issuers
-    // One warp per tile follows that tile's schedule (descriptors stay
-    // warp-uniform); an elected lane issues each group of MMAs and its commit.  Per
-    // chunk i: PV(i) as soon as P(i) is in TMEM, then S(i+2) into the buffer PV(i)
-    // frees.  The two tiles' streams run independently on the tensor core.
-    const int t = warp - kMmaWarp;
-    const int my_nch = t == 0 ? nch_t[0] : nch_t[1];
-    const uint32_t fmt = ODT == PA_BF16 ? 1u : 0u;
-    const uint32_t id_s = umma_idesc(kRows, kChunk, fmt, 0);
-    const uint32_t id_o = umma_idesc(kRows, HEAD, fmt, 1);
-    // descriptor start addresses count 16-byte units: offsets are added pre-shifted
-    const uint64_t qd = umma_desc(smem_u32(sQ) + t * G::kQTile, 16, 1024);
-    const uint64_t kd0 = umma_desc(smem_u32(sKV), 16, 1024);
-    const uint64_t vd0 = umma_desc(smem_u32(sKV) + G::kKvBytes, BS * 128, 1024);
-    const uint32_t tT = tmem + t * kTileCols;
-    uint64_t* my_p_full = p_full + t * kSBufs;
-    auto issue_s = [&](int j) {
-      const uint64_t kd = kd0 + (uint64_t)(((j % ST) * G::kStageBytes) >> 4);
-      const uint32_t d = tT + (j % kSBufs) * 64;
-      if (elect_one()) {
-#pragma unroll
-        for (int ks = 0; ks < HEAD / 16; ++ks) {
-          const uint32_t qo = ((ks >> 2) * G::kQPiece + (ks & 3) * 32) >> 4;
-          const uint32_t ko = ((ks >> 2) * G::kPiece + (ks & 3) * 32) >> 4;
-          umma(d, qd + qo, kd + ko, id_s, ks > 0 ? 1u : 0u);
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();  // the Q tiles are in place; every role of the previous tile is done
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int32_t* table = p.block_tables + (long long)r * p.max_blocks_per_seq;
+
+    if (warp == kProducerWarp || warp == kProducerWarp + 1) {
+      // ------------------------------------------------------------ TMA producers
+      // Lane j holds block table entry kb_first + 32 w + j of window w; the next window
+      // is prefetched.  An elected lane of the first warp copies a chunk's K one piece
+      // of one block at a time; the second warp's copies V one whole block at a time.
+      // Each arrives once per chunk on full with its own byte count.  With an FP8 cache
+      // both copy whole (block, head) tiles of codes into the staging ring instead.
+      const bool is_v = warp != kProducerWarp;
+      const int kb_end = (k1 + BS - 1) / BS;  // blocks [kb_first, kb_end) are loaded
+      auto load_window = [&](int w) {
+        const int kb = kb_first + 32 * w + lane;
+        return kb < kb_end ? table[kb] : -1;
+      };
+      int cur_w = 0;
+      int win = load_window(0);
+      int win_next = load_window(1);
+      for (int i = 0; i < nch; ++i) {
+        const int g = gch + i;  // the chunk's place in the ring, counted across work items
+        const int s = g % RS;
+        if (g >= RS && !__all_sync(0xffffffffu, mbar_wait_bounded(rempty + s, ((g / RS) - 1) & 1))) {
+          if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+          s_abort = 1;
+          break;
         }
-        umma_commit(s_full + t * kSBufs + j % kSBufs);
-      }
-      __syncwarp();
-    };
-    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-      return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
-    };
-    bool ok = true;
-    for (int j = 0; ok && j < kSBufs && j < my_nch; ++j) {
-      ok = wait_all(full + j % ST, (j / ST) & 1);
-      if (!ok) break;
-      tc_fence_after();
-      issue_s(j);
-    }
-    for (int i = 0; ok && i < nch; ++i) {
-      if (i >= my_nch) {
-        // This tile does not read chunk i.  It still releases the stage once, after
-        // the chunk has landed (so it never arrives twice within one phase).
-        if (!(ok = wait_all(full + i % ST, (i / ST) & 1))) break;
-        if (elect_one()) mbar_arrive(empty + i % ST);
+        const int w = (i * NB) >> 5;  // NB divides 32: a chunk's blocks share one window
+        if (w != cur_w) {
+          win = win_next;
+          win_next = load_window(w + 1);
+          cur_w = w;
+        }
+        int phys[NB];
+        int nvalid = 0;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const int e = __shfl_sync(0xffffffffu, win, (i * NB + b) & 31);
+          const bool in_range = kb_first + i * NB + b < kb_end;
+          const bool ok_b = in_range && e >= 0 && e < p.num_blocks;
+          if (in_range && !ok_b && lane == 0 && !is_v) flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
+          phys[b] = ok_b ? e : -1;
+          nvalid += ok_b;
+        }
+        if (kCvt && elect_one()) {
+          uint8_t* sg = sStg + s * 2 * G::kStgKv + (is_v ? G::kStgKv : 0);
+          if (nvalid == 0) {
+            mbar_arrive(rfull + s);
+          } else {
+            mbar_arrive_expect_tx(rfull + s, (uint32_t)(nvalid * G::kStgBlock));
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+              if (phys[b] < 0) continue;
+              if constexpr (kFp4) {  // a whole tile, as laid out in HBM
+                const void* src = static_cast<const uint8_t*>(is_v ? p.v_cache : p.k_cache) +
+                                  ((long long)phys[b] * p.num_kv_heads + kvh) * G::kStgBlock;
+                bulk_load(sg + b * G::kStgBlock, src, G::kStgBlock, rfull + s);
+              } else {
+                tma_load_4d(sg + b * G::kStgBlock, is_v ? &tmv : &tmk, 0, kvh * BS, 0, phys[b], rfull + s);
+              }
+            }
+          }
+        } else if (!kCvt && elect_one()) {
+          uint8_t* sk = sKV + s * G::kStageBytes;
+          if (nvalid == 0) {
+            mbar_arrive(full + s);
+          } else {
+            mbar_arrive_expect_tx(full + s, (uint32_t)(nvalid * G::kBlockTx));
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+              if (phys[b] < 0) continue;
+              if (is_v) {
+                tma_load_4d(sk + G::kKvBytes + b * G::kBlockTx, &tmv, 0, kvh * BS, 0, phys[b], full + s);
+              } else {
+#pragma unroll
+                for (int pc = 0; pc < G::kPieces; ++pc)
+                  tma_load_4d(sk + pc * G::kPiece + b * BS * 128, &tmk, 0, kvh * BS, pc, phys[b], full + s);
+              }
+            }
+          }
+        }
         __syncwarp();
-        continue;
+        g_issued = g + 1;
       }
-      // a tail chunk's V is read only after its zeroing tile has written P(i)
-      if (tail_chunk && i == nch - 1 && t != zero_tile &&
-          !(ok = wait_all(p_full + zero_tile * kSBufs + i % kSBufs, (i / kSBufs) & 1)))
-        break;
-      if (!(ok = wait_all(my_p_full + i % kSBufs, (i / kSBufs) & 1))) break;
-      tc_fence_after();
-      const uint64_t vd = vd0 + (uint64_t)(((i % ST) * G::kStageBytes) >> 4);
-      const uint32_t pt = tT + (i % kSBufs) * 64;
-      if (elect_one()) {
+    } else if (kCvt && warp >= kConvWarp) {
+      // ------------------------------------------------------------ FP8 / NVFP4 converters
+      // Chunk i: wait for its codes in staging and for its f16 stage to be free, widen
+      // every code to f16 exactly (every e4m3 value and every finite e5m2 value is an
+      // f16 value; NVFP4: E2M1 value x E4M3 block scale, at most 6 significant bits
+      // and within f16's normal range; the fp32 scales are applied later) into the
+      // K-major K layout and the per-block V layout, release the staging slot and mark
+      // the f16 stage full.
+      // Thread t owns one row: K row t (t < 64) or V row t - 64.  Reading group g of
+      // a row and writing its two f16 chunks touch eight different 16-byte bank groups
+      // across any eight consecutive rows, so neither side has bank conflicts.
+      if constexpr (kCvt) {
+      const int ct = tid - kConvWarp * 32;
+      const int tensor = ct / kChunk, key = ct % kChunk;
+      const int blk = key / BS, tok = key % BS, sw = key & 7;  // tok & 7 == key & 7
+      for (int i = 0; i < nch; ++i) {
+        const int g = gch + i;
+        const int s = g % ST, ss = g % G::kStgStages;
+        bool ok = mbar_wait_bounded(stg_full + ss, (g / G::kStgStages) & 1);
+        if (g >= ST) ok = ok && mbar_wait_bounded(empty + s, ((g / ST) - 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+          s_abort = 1;
+          break;
+        }
+        const uint8_t* stile = sStg + ss * 2 * G::kStgKv + tensor * G::kStgKv + blk * G::kStgBlock;
+        uint8_t* sk = sKV + s * G::kStageBytes;
+        uint8_t* drow = tensor == 0 ? sk + key * 128 : sk + G::kKvBytes + blk * G::kBlockTx + tok * 128;
+        const int piece_stride = tensor == 0 ? G::kPiece : BS * 128;
+        if constexpr (kFp4) {
+          // a 64-byte code row and its 8 block scales; the row's four 16-byte chunks are
+          // read in an order rotated by row pair, so a warp's reads spread over the bank
+          // line (64-byte rows) and its writes stay on distinct banks (rows differ in
+          // their swizzle)
+          const uint8_t* crow = stile + tok * (HEAD / 2);
+          const uint2 sc8 = *reinterpret_cast<const uint2*>(stile + BS * (HEAD / 2) + tok * (HEAD / 16));
+          const uint64_t sc64 = (static_cast<uint64_t>(sc8.y) << 32) | sc8.x;
 #pragma unroll
-        for (int ks = 0; ks < kChunk / 16; ++ks)
-          umma_tmem_a(tT + kOCol, pt + ks * 8, vd + (uint64_t)(v_row_off<HEAD, BS>(16 * ks, 0) >> 4), id_o,
-                      (i > 0 || ks > 0) ? 1u : 0u);
-        umma_commit(o_done + t * kSBufs + i % kSBufs);
-        umma_commit(empty + i % ST);
+          for (int c = 0; c < 4; ++c) {
+            const int cc = (c + (key >> 1)) & 3;  // chunk: groups 2cc, 2cc+1 = dims 32cc .. 32cc+31
+            const uint4 codes = *reinterpret_cast<const uint4*>(crow + 16 * cc);
+            const uint32_t sp = fp8x2_to_f16x2<PA_FP8_E4M3>(static_cast<uint16_t>(sc64 >> (16 * cc)));
+            const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {  // group g = 2cc + hh: codes 16 g .. 16 g + 15
+              const int g = 2 * cc + hh;
+              const uint32_t sg = __byte_perm(sp, 0, hh ? 0x3232 : 0x1010);
+              uint32_t lo[4], hi[4];
+              fp4x8_to_f16x2x4(cw[2 * hh], lo);
+              fp4x8_to_f16x2x4(cw[2 * hh + 1], hi);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                lo[e] = hmul2_u32(lo[e], sg);
+                hi[e] = hmul2_u32(hi[e], sg);
+              }
+              uint8_t* row = drow + (g >> 2) * piece_stride;
+              const int ch = (2 * g) & 7;
+              *reinterpret_cast<uint4*>(row + ((ch ^ sw) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+              *reinterpret_cast<uint4*>(row + (((ch + 1) ^ sw) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            }
+          }
+        } else {
+          const uint8_t* srow = stile + tok * 128;
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {  // codes 16 g .. 16 g + 15 -> f16 chunks 2g, 2g+1 (mod 8) of piece g / 4
+            const uint4 codes = *reinterpret_cast<const uint4*>(srow + ((g ^ sw) << 4));
+            const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+            uint32_t h[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) fp8x4_to_f16x2x2<KVDT>(cw[e], h[2 * e], h[2 * e + 1]);
+            uint8_t* row = drow + (g >> 2) * piece_stride;
+            const int cc = (2 * g) & 7;
+            *reinterpret_cast<uint4*>(row + ((cc ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(row + (((cc + 1) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+          }
+        }
+        fence_proxy_async();  // generic-proxy writes, read next by the tensor core
+        mbar_arrive(stg_empty + ss);
+        mbar_arrive(full + s);
       }
-      __syncwarp();
-      const int j = i + kSBufs;
-      if (j < my_nch) {
-        if (!(ok = wait_all(full + j % ST, (j / ST) & 1))) break;
+      }
+    } else if (warp >= kMmaWarp && warp < kConvWarp) {
+      // ------------------------------------------------------------ MMA issuers
+      // One warp per tile follows that tile's schedule (descriptors stay
+      // warp-uniform); an elected lane issues each group of MMAs and its commit.  Per
+      // chunk i: PV(i) as soon as P(i) is in TMEM, then S(i+2) into the buffer PV(i)
+      // frees.  The two tiles' streams run independently on the tensor core.
+      const int t = warp - kMmaWarp;
+      const int my_nch = t == 0 ? nch_t[0] : nch_t[1];
+      const int tc = t == 0 ? tch0 : tch1;  // this tile's S / P / O sequence runs on across items
+      const uint32_t fmt = ODT == PA_BF16 ? 1u : 0u;
+      const uint32_t id_s = umma_idesc(kRows, kChunk, fmt, 0);
+      const uint32_t id_o = umma_idesc(kRows, HEAD, fmt, 1);
+      // descriptor start addresses count 16-byte units: offsets are added pre-shifted
+      const uint64_t qd = umma_desc(smem_u32(sQ) + t * G::kQTile, 16, 1024);
+      const uint64_t kd0 = umma_desc(smem_u32(sKV), 16, 1024);
+      const uint64_t vd0 = umma_desc(smem_u32(sKV) + G::kKvBytes, BS * 128, 1024);
+      const uint32_t tT = tmem + t * kTileCols;
+      uint64_t* my_p_full = p_full + t * kSBufs;
+      auto issue_s = [&](int j) {
+        const uint64_t kd = kd0 + (uint64_t)((((gch + j) % ST) * G::kStageBytes) >> 4);
+        const uint32_t d = tT + ((tc + j) % kSBufs) * 64;
+        if (elect_one()) {
+#pragma unroll
+          for (int ks = 0; ks < HEAD / 16; ++ks) {
+            const uint32_t qo = ((ks >> 2) * G::kQPiece + (ks & 3) * 32) >> 4;
+            const uint32_t ko = ((ks >> 2) * G::kPiece + (ks & 3) * 32) >> 4;
+            umma(d, qd + qo, kd + ko, id_s, ks > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full + t * kSBufs + (tc + j) % kSBufs);
+        }
+        __syncwarp();
+      };
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
+      };
+      bool ok = true;
+      for (int j = 0; ok && j < kSBufs && j < my_nch; ++j) {
+        ok = wait_all(full + (gch + j) % ST, ((gch + j) / ST) & 1);
+        if (!ok) break;
         tc_fence_after();
         issue_s(j);
       }
-    }
-    if (!ok && lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-    // every MMA of both tiles completes before TMEM is released
-    if (elect_one()) umma_commit(mma_fin);
-    __syncwarp();
-    if (!wait_all(mma_fin, 0) && lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-  } else {
-    // ------------------------------------------------------------ softmax warps
-    // Warps 4t .. 4t+3 serve tile t; thread = TMEM lane = row of the tile.
-    const int t = warp >> 2;
-    const int my_nch = t == 0 ? nch_t[0] : nch_t[1];
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tT = tmem + t * kTileCols;
-    const uint32_t tO = tT + kOCol;
-    uint64_t* my_s_full = s_full + t * kSBufs;
-    uint64_t* my_p_full = p_full + t * kSBufs;
-    uint64_t* my_o_done = o_done + t * kSBufs;
-    // score multiplier in log2 units; FP8: the K scale and the row's f16 shift too
-    const float c = kCvt ? ldexpf(p.scale * kLog2e * p.k_scale[kvh * p.scale_stride], -q_shift) : p.scale * kLog2e;
-    const float out_scale = kCvt ? p.v_scale[kvh * p.scale_stride] : 1.f;
-    const int row_limit = p.causal ? min(k1, row_pos + 1) : k1;  // this row attends keys < row_limit
-    const int row_lo = p.window > 0 ? max(0, row_pos - p.window + 1) : 0;  // ... and keys >= row_lo
-    float m = -INFINITY, l = 0.f;
-    bool fail = false;
-    for (int i = 0; i < my_nch; ++i) {
-      const int base = klo + i * kChunk;
-      const uint32_t tS = tT + (i % kSBufs) * 64;
-      const bool got = mbar_wait_bounded(my_s_full + i % kSBufs, (i / kSBufs) & 1);
-      if (!__all_sync(0xffffffffu, got)) {
-        fail = true;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[kChunk];
-      tmem_ld32(tS + lane_base, sr);
-      tmem_ld32(tS + 32 + lane_base, sr + 32);
-      tmem_wait_ld();
-      float sc[kChunk];
+      for (int i = 0; ok && i < nch; ++i) {
+        const int g = gch + i, ci = tc + i;
+        if (i >= my_nch) {
+          // This tile does not read chunk i.  It still releases the stage once, after
+          // the chunk has landed (so it never arrives twice within one phase).
+          if (!(ok = wait_all(full + g % ST, (g / ST) & 1))) break;
+          if (elect_one()) mbar_arrive(empty + g % ST);
+          __syncwarp();
+          continue;
+        }
+        // a tail chunk's V is read only after its zeroing tile has written P(i)
+        const int cz = (zero_tile == 0 ? tch0 : tch1) + i;
+        if (tail_chunk && i == nch - 1 && t != zero_tile &&
+            !(ok = wait_all(p_full + zero_tile * kSBufs + cz % kSBufs, (cz / kSBufs) & 1)))
+          break;
+        if (!(ok = wait_all(my_p_full + ci % kSBufs, (ci / kSBufs) & 1))) break;
+        tc_fence_after();
+        const uint64_t vd = vd0 + (uint64_t)(((g % ST) * G::kStageBytes) >> 4);
+        const uint32_t pt = tT + (ci % kSBufs) * 64;
+        if (elect_one()) {
 #pragma unroll
-      for (int j = 0; j < kChunk; ++j) sc[j] = __uint_as_float(sr[j]);
-      const int rem = row_limit - base;  // keys of this chunk the row attends: [lo_rem, rem)
-      const int lo_rem = row_lo - base;
-      if (rem < kChunk || lo_rem > 0) {
-#pragma unroll
-        for (int j = 0; j < kChunk; ++j)
-          if (j >= rem || j < lo_rem) sc[j] = -INFINITY;
+          for (int ks = 0; ks < kChunk / 16; ++ks)
+            umma_tmem_a(tT + kOCol, pt + ks * 8, vd + (uint64_t)(v_row_off<HEAD, BS>(16 * ks, 0) >> 4), id_o,
+                        (i > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(o_done + t * kSBufs + ci % kSBufs);
+          umma_commit(empty + g % ST);
+        }
+        __syncwarp();
+        const int j = i + kSBufs;
+        if (j < my_nch) {
+          if (!(ok = wait_all(full + (gch + j) % ST, ((gch + j) / ST) & 1))) break;
+          tc_fence_after();
+          issue_s(j);
+        }
       }
-      // row maximum: eight independent chains of three-input maxima
-      float mq[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float x = max3(sc[8 * q], sc[8 * q + 1], sc[8 * q + 2]);
-        x = max3(x, sc[8 * q + 3], sc[8 * q + 4]);
-        x = max3(x, sc[8 * q + 5], sc[8 * q + 6]);
-        mq[q] = fmaxf(x, sc[8 * q + 7]);
+      if (!ok) {
+        if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+        s_abort = 1;
       }
-      const float mx = max3(max3(mq[0], mq[1], mq[2]), max3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7])) * c;
-      const bool need = mx > m + kRescaleSlack;
-      float al = 1.f;
-      if (need) {
-        const float nm = fmaxf(m, mx);
-        al = ex2_approx(m - nm);  // 0 while the row had no key yet
-        m = nm;
-        l *= al;
-      }
-      const float u = m == -INFINITY ? 0.f : m;
-      // p = 2^(s c - u) on pairs of keys; the row sum in four packed accumulators
-      const uint64_t c2 = f2_pack(c, c), nu2 = f2_pack(-u, -u);
-      uint32_t pk[kChunk / 2];
-      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-      for (int j = 0; j < kChunk / 2; ++j) {
-        const float2 x = f2_unpack(f2_fma(f2_pack(sc[2 * j], sc[2 * j + 1]), c2, nu2));
-        const float e0 = ex2_approx(x.x), e1 = ex2_approx(x.y);
-        acc2[j & 3] = f2_add(acc2[j & 3], f2_pack(e0, e1));
-        pk[j] = pack2<ODT>(e0, e1);
-      }
-      const float2 lsum = f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])));
-      l += lsum.x + lsum.y;
-      // O is rescaled only once PV(i-1) has completed
-      if (__any_sync(0xffffffffu, need) && i > 0) {
-        const bool done = mbar_wait_bounded(my_o_done + (i - 1) % kSBufs, ((i - 1) / kSBufs) & 1);
-        if (!__all_sync(0xffffffffu, done)) {
+    } else {
+      // ------------------------------------------------------------ softmax warps
+      // Warps 4t .. 4t+3 serve tile t; thread = TMEM lane = row of the tile.
+      const int t = warp >> 2;
+      const int my_nch = t == 0 ? nch_t[0] : nch_t[1];
+      const int tc = t == 0 ? tch0 : tch1;
+      const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+      const uint32_t tT = tmem + t * kTileCols;
+      const uint32_t tO = tT + kOCol;
+      uint64_t* my_s_full = s_full + t * kSBufs;
+      uint64_t* my_p_full = p_full + t * kSBufs;
+      uint64_t* my_o_done = o_done + t * kSBufs;
+      // score multiplier in log2 units; FP8: the K scale and the row's f16 shift too
+      const float c = kCvt ? ldexpf(p.scale * kLog2e * p.k_scale[kvh * p.scale_stride], -q_shift) : p.scale * kLog2e;
+      const float out_scale = kCvt ? p.v_scale[kvh * p.scale_stride] : 1.f;
+      const int row_limit = p.causal ? min(k1, row_pos + 1) : k1;  // this row attends keys < row_limit
+      const int row_lo = p.window > 0 ? max(0, row_pos - p.window + 1) : 0;  // ... and keys >= row_lo
+      float m = -INFINITY, l = 0.f;
+      bool fail = false;
+      for (int i = 0; i < my_nch; ++i) {
+        const int base = klo + i * kChunk;
+        const int ci = tc + i, g = gch + i;
+        const uint32_t tS = tT + (ci % kSBufs) * 64;
+        const bool got = mbar_wait_bounded(my_s_full + ci % kSBufs, (ci / kSBufs) & 1);
+        if (!__all_sync(0xffffffffu, got)) {
           fail = true;
           break;
         }
         tc_fence_after();
+        uint32_t sr[kChunk];
+        tmem_ld32(tS + lane_base, sr);
+        tmem_ld32(tS + 32 + lane_base, sr + 32);
+        tmem_wait_ld();
+        float sc[kChunk];
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) sc[j] = __uint_as_float(sr[j]);
+        const int rem = row_limit - base;  // keys of this chunk the row attends: [lo_rem, rem)
+        const int lo_rem = row_lo - base;
+        if (rem < kChunk || lo_rem > 0) {
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j)
+            if (j >= rem || j < lo_rem) sc[j] = -INFINITY;
+        }
+        // row maximum: eight independent chains of three-input maxima
+        float mq[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float x = max3(sc[8 * q], sc[8 * q + 1], sc[8 * q + 2]);
+          x = max3(x, sc[8 * q + 3], sc[8 * q + 4]);
+          x = max3(x, sc[8 * q + 5], sc[8 * q + 6]);
+          mq[q] = fmaxf(x, sc[8 * q + 7]);
+        }
+        const float mx = max3(max3(mq[0], mq[1], mq[2]), max3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7])) * c;
+        const bool need = mx > m + kRescaleSlack;
+        float al = 1.f;
+        if (need) {
+          const float nm = fmaxf(m, mx);
+          al = ex2_approx(m - nm);  // 0 while the row had no key yet
+          m = nm;
+          l *= al;
+        }
+        const float u = m == -INFINITY ? 0.f : m;
+        // p = 2^(s c - u) on pairs of keys; the row sum in four packed accumulators
+        const uint64_t c2 = f2_pack(c, c), nu2 = f2_pack(-u, -u);
+        uint32_t pk[kChunk / 2];
+        uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int j = 0; j < kChunk / 2; ++j) {
+          const float2 x = f2_unpack(f2_fma(f2_pack(sc[2 * j], sc[2 * j + 1]), c2, nu2));
+          const float e0 = ex2_approx(x.x), e1 = ex2_approx(x.y);
+          acc2[j & 3] = f2_add(acc2[j & 3], f2_pack(e0, e1));
+          pk[j] = pack2<ODT>(e0, e1);
+        }
+        const float2 lsum = f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])));
+        l += lsum.x + lsum.y;
+        // O is rescaled only once PV(i-1) has completed
+        if (__any_sync(0xffffffffu, need) && i > 0) {
+          const bool done = mbar_wait_bounded(my_o_done + (ci - 1) % kSBufs, ((ci - 1) / kSBufs) & 1);
+          if (!__all_sync(0xffffffffu, done)) {
+            fail = true;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int cb = 0; cb < HEAD; cb += 32) {
+            uint32_t o[32];
+            tmem_ld32(tO + cb + lane_base, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * al);
+            tmem_st32(tO + cb + lane_base, o);
+          }
+        }
+        // P(i) over the first half of S(i)'s columns
+        tmem_st32(tS + lane_base, pk);
+        // V rows past the loaded keys may hold any bits; their P is 0, so they are
+        // zeroed to keep 0 * V finite.  Each thread's stores precede its own arrival
+        // on p_full, which every PV of this chunk waits for.
+        if (tail_chunk && t == zero_tile && i == nch - 1) {
+          const bool landed = mbar_wait_bounded(full + g % ST, (g / ST) & 1);
+          const int vrem = kv_loaded_end - base;
+          const int rr = tid % kRows;
+          if (landed && rr < G::kPieces * kChunk) {
+            const int key = rr % kChunk, pc = rr / kChunk;
+            if (key >= vrem) {
+              uint4* d = reinterpret_cast<uint4*>(sKV + (g % ST) * G::kStageBytes + G::kKvBytes +
+                                                  v_row_off<HEAD, BS>(key, pc));
+#pragma unroll
+              for (int q = 0; q < 8; ++q) d[q] = make_uint4(0, 0, 0, 0);
+            }
+          }
+          fence_proxy_async();
+        }
+        tmem_wait_st();
+        // Observe PV(i-2): every phase of both o_done barriers is waited for in order
+        // and never more than one phase late, so the parity waits stay unambiguous.
+        if (i >= kSBufs) {
+          const bool done = mbar_wait_bounded(my_o_done + ci % kSBufs, ((ci - kSBufs) / kSBufs) & 1);
+          if (!__all_sync(0xffffffffu, done)) {
+            fail = true;
+            break;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(my_p_full + ci % kSBufs);
+      }
+      if (!fail && my_nch > 0) {
+        const int cl = tc + my_nch - 1;
+        const bool done = mbar_wait_bounded(my_o_done + cl % kSBufs, (cl / kSBufs) & 1);
+        fail = !__all_sync(0xffffffffu, done);
+        tc_fence_after();
+      }
+      if (fail) {
+        if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+        s_abort = 1;
+      } else {
+        // ---- epilogue: thread = row; direct output when the row needs one partition,
+        // else its partial state (unnormalised O, max in log2 units, sum)
+        const int kv_len = p.causal ? row_pos + 1 : seq_len;
+        const int parts_row = (kv_len - origin + part - 1) / part;
+        const bool write = row_valid && z < parts_row;
+        const bool direct = parts_row == 1;
+        const int tq = t0 + row_tok;
+        const int head = h0 + row_head;
+        const float inv = l > 0.f ? out_scale / l : 0.f;
+        const long long pi = (long long)p.part_off[r] + (long long)tq * parts_req + z;
+        typename QE::T* o_row =
+            reinterpret_cast<typename QE::T*>(p.out) + ((long long)(qs + tq) * p.num_q_heads + head) * HEAD;
+        float* w_row = p.ws_acc + (pi * p.num_q_heads + head) * HEAD;
 #pragma unroll 1
         for (int cb = 0; cb < HEAD; cb += 32) {
           uint32_t o[32];
-          tmem_ld32(tO + cb + lane_base, o);
-          tmem_wait_ld();
+          if (my_nch > 0) {
+            tmem_ld32(tO + cb + lane_base, o);
+            tmem_wait_ld();
+          } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * al);
-          tmem_st32(tO + cb + lane_base, o);
-        }
-      }
-      // P(i) over the first half of S(i)'s columns
-      tmem_st32(tS + lane_base, pk);
-      // V rows past the loaded keys may hold any bits; their P is 0, so they are
-      // zeroed to keep 0 * V finite.  Each thread's stores precede its own arrival
-      // on p_full, which every PV of this chunk waits for.
-      if (tail_chunk && t == zero_tile && i == nch - 1) {
-        const bool landed = mbar_wait_bounded(full + i % ST, (i / ST) & 1);
-        const int vrem = kv_loaded_end - base;
-        const int rr = tid % kRows;
-        if (landed && rr < G::kPieces * kChunk) {
-          const int key = rr % kChunk, pc = rr / kChunk;
-          if (key >= vrem) {
-            uint4* d = reinterpret_cast<uint4*>(sKV + (i % ST) * G::kStageBytes + G::kKvBytes +
-                                                v_row_off<HEAD, BS>(key, pc));
+            for (int j = 0; j < 32; ++j) o[j] = 0u;
+          }
+          if (!write) continue;
+          if (direct) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) d[q] = make_uint4(0, 0, 0, 0);
+            for (int q = 0; q < 4; ++q) {
+              uint4 v;
+              v.x = pack2<QDT>(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+              v.y = pack2<QDT>(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+              v.z = pack2<QDT>(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+              v.w = pack2<QDT>(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+              *reinterpret_cast<uint4*>(o_row + cb + 8 * q) = v;
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<float4*>(w_row + cb + 4 * q) =
+                  make_float4(__uint_as_float(o[4 * q]) * out_scale, __uint_as_float(o[4 * q + 1]) * out_scale,
+                              __uint_as_float(o[4 * q + 2]) * out_scale, __uint_as_float(o[4 * q + 3]) * out_scale);
           }
         }
-        fence_proxy_async();
+        if (write && !direct) p.ws_ml[pi * p.num_q_heads + head] = make_float2(m, l);
       }
-      tmem_wait_st();
-      // Observe PV(i-2): every phase of both o_done barriers is waited for in order
-      // and never more than one phase late, so the parity waits stay unambiguous.
-      if (i >= kSBufs) {
-        const bool done = mbar_wait_bounded(my_o_done + i % kSBufs, ((i - kSBufs) / kSBufs) & 1);
-        if (!__all_sync(0xffffffffu, done)) {
-          fail = true;
-          break;
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(my_p_full + i % kSBufs);
     }
-    if (!fail && my_nch > 0) {
-      const bool done = mbar_wait_bounded(my_o_done + (my_nch - 1) % kSBufs, ((my_nch - 1) / kSBufs) & 1);
-      fail = !__all_sync(0xffffffffu, done);
-      tc_fence_after();
-    }
-    if (fail) {
-      if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-    } else {
-      // ---- epilogue: thread = row; direct output when the row needs one partition,
-      // else its partial state (unnormalised O, max in log2 units, sum)
-      const int kv_len = p.causal ? row_pos + 1 : seq_len;
-      const int parts_row = (kv_len - origin + part - 1) / part;
-      const bool write = row_valid && z < parts_row;
-      const bool direct = parts_row == 1;
-      const int tq = t0 + row_tok;
-      const int head = h0 + row_head;
-      const float inv = l > 0.f ? out_scale / l : 0.f;
-      const long long pi = (long long)p.part_off[r] + (long long)tq * parts_req + z;
-      typename QE::T* o_row =
-          reinterpret_cast<typename QE::T*>(p.out) + ((long long)(qs + tq) * p.num_q_heads + head) * HEAD;
-      float* w_row = p.ws_acc + (pi * p.num_q_heads + head) * HEAD;
-#pragma unroll 1
-      for (int cb = 0; cb < HEAD; cb += 32) {
-        uint32_t o[32];
-        if (my_nch > 0) {
-          tmem_ld32(tO + cb + lane_base, o);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = 0u;
-        }
-        if (!write) continue;
-        if (direct) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 v;
-            v.x = pack2<QDT>(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-            v.y = pack2<QDT>(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-            v.z = pack2<QDT>(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-            v.w = pack2<QDT>(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-            *reinterpret_cast<uint4*>(o_row + cb + 8 * q) = v;
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(w_row + cb + 4 * q) =
-                make_float4(__uint_as_float(o[4 * q]) * out_scale, __uint_as_float(o[4 * q + 1]) * out_scale,
-                            __uint_as_float(o[4 * q + 2]) * out_scale, __uint_as_float(o[4 * q + 3]) * out_scale);
-        }
-      }
-      if (write && !direct) p.ws_ml[pi * p.num_q_heads + head] = make_float2(m, l);
-    }
+
+    gch += nch;
+    tch0 += nch_t[0];
+    tch1 += nch_t[1];
+    if (tid == 0) s_next = atomicAdd(p.work_claim, 1);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    L = s_next;
+    if (L >= total || s_abort) break;
   }
 
-  // ---- teardown: TMEM is released once every warp is done with it
+  // ---- teardown: every MMA completes and every copy lands before TMEM is released
+  // and the CTA leaves
+  if (warp >= kMmaWarp && warp < kConvWarp) {
+    if (elect_one()) umma_commit(mma_fin);
+    __syncwarp();
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(mma_fin, 0)) && lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+  } else if ((warp == kProducerWarp || warp == kProducerWarp + 1) && lane == 0) {
+    for (int j = max(0, g_issued - RS); j < g_issued; ++j)
+      if (!mbar_wait_bounded(rfull + j % RS, (j / RS) & 1)) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
 }
 
 template <int QDT, int KVDT, int HEAD, int BS>
-cudaError_t launch_tc_t(const AttnParams& p, int num_items, const CUtensorMap* tk, const CUtensorMap* tv,
-                        cudaStream_t stream) {
+cudaError_t launch_tc_t(const AttnParams& p, int num_items, int max_ctas, const CUtensorMap* tk,
+                        const CUtensorMap* tv, cudaStream_t stream) {
   constexpr bool kCvt = is_scaled<KVDT>();
   constexpr int smem = TcGeom<HEAD, BS, kCvt, is_nvfp4<KVDT>()>::kSmem;
   auto kern = prefill_tc_kernel<QDT, KVDT, HEAD, BS>;
@@ -817,22 +870,23 @@ cudaError_t launch_tc_t(const AttnParams& p, int num_items, const CUtensorMap* t
     }
     configured_device = dev;
   }
-  dim3 grid(num_items, p.num_kv_heads * p.num_head_groups);
+  const long long tiles = (long long)num_items * p.num_kv_heads * p.num_head_groups;
+  const int grid = static_cast<int>(std::min<long long>(tiles, std::max(1, max_ctas)));
   kern<<<grid, threads_tc<kCvt>(), smem, stream>>>(p, *tk, *tv);
   return cudaGetLastError();
 }
 
 template <int QDT, int KVDT>
-cudaError_t launch_tc_shape(const AttnParams& p, int num_items, const CUtensorMap* tk, const CUtensorMap* tv,
-                            cudaStream_t s) {
+cudaError_t launch_tc_shape(const AttnParams& p, int num_items, int max_ctas, const CUtensorMap* tk,
+                            const CUtensorMap* tv, cudaStream_t s) {
   const int d = p.head_size, bs = p.block_size;
-  if (d == 128 && bs == 16) return launch_tc_t<QDT, KVDT, 128, 16>(p, num_items, tk, tv, s);
-  if (d == 128 && bs == 32) return launch_tc_t<QDT, KVDT, 128, 32>(p, num_items, tk, tv, s);
-  if (d == 128 && bs == 64) return launch_tc_t<QDT, KVDT, 128, 64>(p, num_items, tk, tv, s);
+  if (d == 128 && bs == 16) return launch_tc_t<QDT, KVDT, 128, 16>(p, num_items, max_ctas, tk, tv, s);
+  if (d == 128 && bs == 32) return launch_tc_t<QDT, KVDT, 128, 32>(p, num_items, max_ctas, tk, tv, s);
+  if (d == 128 && bs == 64) return launch_tc_t<QDT, KVDT, 128, 64>(p, num_items, max_ctas, tk, tv, s);
   if constexpr (!is_scaled<KVDT>()) {
-    if (d == 64 && bs == 16) return launch_tc_t<QDT, KVDT, 64, 16>(p, num_items, tk, tv, s);
-    if (d == 64 && bs == 32) return launch_tc_t<QDT, KVDT, 64, 32>(p, num_items, tk, tv, s);
-    if (d == 64 && bs == 64) return launch_tc_t<QDT, KVDT, 64, 64>(p, num_items, tk, tv, s);
+    if (d == 64 && bs == 16) return launch_tc_t<QDT, KVDT, 64, 16>(p, num_items, max_ctas, tk, tv, s);
+    if (d == 64 && bs == 32) return launch_tc_t<QDT, KVDT, 64, 32>(p, num_items, max_ctas, tk, tv, s);
+    if (d == 64 && bs == 64) return launch_tc_t<QDT, KVDT, 64, 64>(p, num_items, max_ctas, tk, tv, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -855,27 +909,27 @@ bool prefill_tc_supported(int q_dtype, int kv_dtype, int head_size, int block_si
   return kv_dtype == q_dtype && (head_size == 64 || head_size == 128);
 }
 
-cudaError_t launch_prefill_tc(const AttnParams& p, int q_dtype, int kv_dtype, int num_items,
+cudaError_t launch_prefill_tc(const AttnParams& p, int q_dtype, int kv_dtype, int num_items, int max_ctas,
                               const CUtensorMap* tmap_k, const CUtensorMap* tmap_v, cudaStream_t stream) {
   if (num_items <= 0) return cudaSuccess;
   if (kv_dtype == PA_FP8_E4M3) {
-    if (q_dtype == PA_BF16) return launch_tc_shape<PA_BF16, PA_FP8_E4M3>(p, num_items, tmap_k, tmap_v, stream);
-    if (q_dtype == PA_F16) return launch_tc_shape<PA_F16, PA_FP8_E4M3>(p, num_items, tmap_k, tmap_v, stream);
+    if (q_dtype == PA_BF16) return launch_tc_shape<PA_BF16, PA_FP8_E4M3>(p, num_items, max_ctas, tmap_k, tmap_v, stream);
+    if (q_dtype == PA_F16) return launch_tc_shape<PA_F16, PA_FP8_E4M3>(p, num_items, max_ctas, tmap_k, tmap_v, stream);
     return cudaErrorInvalidValue;
   }
   if (kv_dtype == PA_FP8_E5M2) {
-    if (q_dtype == PA_BF16) return launch_tc_shape<PA_BF16, PA_FP8_E5M2>(p, num_items, tmap_k, tmap_v, stream);
-    if (q_dtype == PA_F16) return launch_tc_shape<PA_F16, PA_FP8_E5M2>(p, num_items, tmap_k, tmap_v, stream);
+    if (q_dtype == PA_BF16) return launch_tc_shape<PA_BF16, PA_FP8_E5M2>(p, num_items, max_ctas, tmap_k, tmap_v, stream);
+    if (q_dtype == PA_F16) return launch_tc_shape<PA_F16, PA_FP8_E5M2>(p, num_items, max_ctas, tmap_k, tmap_v, stream);
     return cudaErrorInvalidValue;
   }
   if (kv_dtype == PA_NVFP4) {
-    if (q_dtype == PA_BF16) return launch_tc_shape<PA_BF16, PA_NVFP4>(p, num_items, tmap_k, tmap_v, stream);
-    if (q_dtype == PA_F16) return launch_tc_shape<PA_F16, PA_NVFP4>(p, num_items, tmap_k, tmap_v, stream);
+    if (q_dtype == PA_BF16) return launch_tc_shape<PA_BF16, PA_NVFP4>(p, num_items, max_ctas, tmap_k, tmap_v, stream);
+    if (q_dtype == PA_F16) return launch_tc_shape<PA_F16, PA_NVFP4>(p, num_items, max_ctas, tmap_k, tmap_v, stream);
     return cudaErrorInvalidValue;
   }
   if (kv_dtype != q_dtype) return cudaErrorInvalidValue;
-  if (q_dtype == PA_BF16) return launch_tc_shape<PA_BF16, PA_BF16>(p, num_items, tmap_k, tmap_v, stream);
-  if (q_dtype == PA_F16) return launch_tc_shape<PA_F16, PA_F16>(p, num_items, tmap_k, tmap_v, stream);
+  if (q_dtype == PA_BF16) return launch_tc_shape<PA_BF16, PA_BF16>(p, num_items, max_ctas, tmap_k, tmap_v, stream);
+  if (q_dtype == PA_F16) return launch_tc_shape<PA_F16, PA_F16>(p, num_items, max_ctas, tmap_k, tmap_v, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -32,6 +32,8 @@ struct AttnParams {
   const int4* work;                // varlen: prefill tile work list (plan kernel)
   const int32_t* work_count;       // varlen: number of entries in `work`
   const int32_t* plan_ok;          // varlen: 1 when query_start_loc passed the plan kernel's checks
+  int32_t* work_claim;             // varlen: prefill tiles claimed so far (zeroed by the plan kernel)
+  int32_t* work_full;              // varlen: leading entries of `work` that span a whole partition
   const int32_t* group_start;      // shared-prefix decode: [num_groups+1] runs of consecutive sequences
   const int32_t* group_shared_blocks;  // shared-prefix decode: [num_groups] leading blocks shared in a group
   float* ws_acc;                   // [partial rows][Hq][d]  un-normalised weighted sums
@@ -118,9 +120,11 @@ cudaError_t launch_shared_prefix_tiles(const AttnParams& p, int q_dtype, int gri
                                        cudaStream_t stream);
 
 // tcgen05 prefill tiles (TMEM accumulators); tmap_k has one-piece boxes, tmap_v
-// whole (block, head) tiles.
+// whole (block, head) tiles.  A persistent grid of at most max_ctas CTAs (one per SM)
+// claims (work item, KV head group) tiles through p.work_claim; several launches may
+// share one plan's list, each tile going to whichever CTA claims it first.
 bool prefill_tc_supported(int q_dtype, int kv_dtype, int head_size, int block_size);
-cudaError_t launch_prefill_tc(const AttnParams& p, int q_dtype, int kv_dtype, int num_items,
+cudaError_t launch_prefill_tc(const AttnParams& p, int q_dtype, int kv_dtype, int num_items, int max_ctas,
                               const CUtensorMap* tmap_k, const CUtensorMap* tmap_v, cudaStream_t stream);
 
 }  // namespace pa
