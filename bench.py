@@ -590,7 +590,9 @@ def run_ours(args):
         pf_tflops = vsplit["prefill_flops"] / (span_ms / 1000.0) / 1e12 if span_ms else 0.0
         tpeak, tkind = measured_bf16_sustained()
         kernel_name = "decode_mma_kernel || prefill_tc_kernel (one fork-join span)"
-        overlapped = {"decode_mma_kernel": att_ms, "prefill_tc_kernel": kernel_ms.get("prefill_tiles", 0.0)}
+        # per step: the prefill tiles launch twice when decode rows run beside them
+        n_span = max(trace["varlen_span"][0], 1)
+        overlapped = {"decode_mma_kernel": att_ms, "prefill_tc_kernel": trace["prefill_tiles"][1] / n_span}
         hbm_line = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                     "traffic": profiled_traffic(args.workload, "varlen_span"), "kernel": kernel_name,
                     "peak_source": f"{peak_kind} MEASURED_PEAKS.json hbm_gbs",
