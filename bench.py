@@ -13,8 +13,8 @@ metric: attended KV tokens per second (sum of seq_lens per step / step time),
 whole job over all ranks.  Multi-GPU (torchrun): each rank runs its own
 independent batch (weak scaling, no collective on the data path).
 
-`--impl reference` times the fp64 CPU oracle instead (the reference arm of this
-build), on the host cores, on a bounded sample of the same workload.
+`--impl reference` times the fp64 CPU oracle instead (the reference arm), on the
+host cores, on a bounded sample of the same workload.
 """
 
 from __future__ import annotations

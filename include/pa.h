@@ -94,7 +94,7 @@ typedef struct CUstream_st* pa_stream_t; /* same type as cudaStream_t */
 typedef enum pa_status {
   PA_OK = 0,
   PA_ERR_INVALID_ARG = 1, /* a null pointer, a non-positive size, inconsistent shapes */
-  PA_ERR_UNSUPPORTED = 2, /* a dtype combination or shape this build does not handle */
+  PA_ERR_UNSUPPORTED = 2, /* a dtype combination or shape the library does not handle */
   PA_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or smaller than required */
   PA_ERR_BOUNDS = 4,      /* returned by pa_get_error_flags when a device check fired */
   PA_ERR_TIMEOUT = 5,     /* a bounded device wait gave up (see PA_ERRFLAG_TIMEOUT) */
