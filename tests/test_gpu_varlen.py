@@ -57,6 +57,10 @@ VARLEN_CASES = [
     ("fp8_prefill_ragged_part48", "fp8_e4m3", 32, 8, 128, 16, [97, 33, 1000], [97, 31, 45], 48, True),
     ("fp8_prefill_noncausal_bs64", "fp8_e4m3", 16, 2, 128, 64, [250, 90], [60, 90], 64, False),
     ("fp8e5m2_prefill_mixed", "fp8_e5m2", 32, 8, 128, 16, [2000, 33, 700, 1], [300, 1, 64, 1], 0, True),
+    # more (item, KV head) tiles than the first persistent grid has CTAs, beside decode rows
+    ("mha_g1_many_tiles", "bf16", 8, 8, 128, 16, [1000, 700, 600, 520, 800, 900, 515, 640, 300, 1],
+     [512, 512, 512, 512, 512, 512, 512, 512, 1, 1], 0, True),
+    ("g2_f16_bs32", "f16", 8, 4, 128, 32, [513, 90, 1200], [257, 90, 1], 64, True),
 ]
 
 
