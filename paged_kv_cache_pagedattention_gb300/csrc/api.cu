@@ -21,8 +21,8 @@ using pa::AttnParams;
 __device__ unsigned g_pa_error_word;
 
 constexpr int kMaxDevices = 64;
-// Share of the SMs the prefill tiles' first (side-stream) grid holds while the decode
-// rows of a varlen step run beside it.
+// Share of the SMs the prefill tiles' first grid (on the caller's stream) holds while
+// the decode rows of a varlen step run beside it on the side stream.
 constexpr int kPrefillShareNum = 2;
 constexpr int kPrefillShareDen = 3;
 

@@ -5,8 +5,10 @@
 // the request's cached prefix and, causally, the chunk itself; [NOTES] "Prefill 与
 // Decode": this work is dense and compute-bound.
 //
-// One CTA per work item of the varlen plan (request, first query row, partition of
-// the keys) and per (KV head, group of <= 8 query heads).  Its 256 query rows are
+// A persistent grid (one CTA per SM) whose CTAs claim tiles in turn from a counter: a
+// tile is a work item of the varlen plan (request, first query row, partition of the
+// keys) for one (KV head, group of <= 8 query heads); the K/V ring's stages and every
+// barrier's phase run on from one tile to the next.  A tile's 256 query rows are
 // (token, head) pairs, token-major (row = token * GP + head, GP = the head group
 // padded to a power of two), split into two tiles of 128 rows; row r of a tile lives
 // in TMEM lane r.  Keys stream in chunks of 64 tokens (whole paged blocks) staged by
