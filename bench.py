@@ -299,6 +299,26 @@ def algorithmic_bytes(b, window: int = 0) -> dict:
             "algorithmic": unique + q_out + tables, "logical_total": logical + q_out + tables}
 
 
+def qk_pairs(b, window: int = 0) -> int:
+    """(query token, key token) pairs the attention scores per call: request r's query j
+    sits at position p = seq_len - q_len + j and attends keys 0..p when causal (the
+    last `window` of them with a sliding window), all seq_len keys otherwise."""
+    import numpy as np
+
+    qsl = np.asarray(b.query_start_loc, dtype=np.int64)
+    total = 0
+    for r, n in enumerate(b.seq_lens):
+        n, q = int(n), int(qsl[r + 1] - qsl[r])
+        if q <= 0:
+            continue
+        if not b.causal:
+            total += q * n
+            continue
+        keys = np.arange(n - q, n, dtype=np.int64) + 1
+        total += int(np.minimum(keys, window).sum() if window > 0 else keys.sum())
+    return total
+
+
 # ----------------------------------------------------------------------------- oracle (CPU) arm
 
 _CPU_SAMPLE = {}
@@ -537,6 +557,7 @@ def run_ours(args):
     ms_per_step = ms_graph if ms_graph is not None else ms_eager
     ctx_tokens = int(sum(window_tokens(b, args.window)))
     tok_s = ctx_tokens * world / (ms_per_step / 1000.0)
+    qk = qk_pairs(b, args.window)
     # kernel launches: every traced kind but the fork-join spans (which wrap launches)
     launches = sum(n for name, (n, _) in trace.items() if not name.endswith("_span"))
 
@@ -668,7 +689,9 @@ def run_ours(args):
                 "vs_baseline": None, "dtype": "bf16" if b.kv_dtype == "bf16" else b.kv_dtype,
                 "data": "synthetic (seeded N(0,1) values, seeded block placement)",
                 "config": workload_config(b, args),
-                "hbm_gbs": achieved, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "hbm_gbs": achieved,
+                "qk_pairs_per_step": qk, "qk_pairs_per_s": qk * world / (ms_per_step / 1000.0),
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "step_launch": "cuda_graph_replay" if ms_graph is not None else "eager",
                 "ms_per_step_eager": ms_eager,
                 "gpu_launches": launches,
