@@ -489,15 +489,17 @@ def run_ours(args):
         max_group = int(max(groups[0][1:] - groups[0][:-1]))
     ws = pa.workspace_tensor(wsb, dev)
 
-    def step(q_=q, key_=key, value_=val, slots_=slots, tables_=tables, lens_=lens, qsl_=qsl, out_=out):
+    def step(q_=q, key_=key, value_=val, slots_=slots, tables_=tables, lens_=lens, qsl_=qsl, out_=out,
+             gstart_=None, gshared_=None):
         stream = torch.cuda.current_stream(dev)  # the capture stream while a graph is recorded
         pa.pa_reshape_and_cache(key_, value_, kc, vc, slots_, ks, vs, stream)
         if varlen:
             pa.pa_varlen_attn(out_, q_, kc, vc, tables_, qsl_, lens_, b.max_query_len, b.max_seq_len, b.scale, ws,
                               True, ks, vs, part, stream)
         elif groups is not None:
-            pa.pa_decode_shared_prefix(out_, q_, kc, vc, tables_, lens_, b.max_seq_len, b.scale, ws, gstart,
-                                       gshared, max_group, ks, vs, part, stream)
+            pa.pa_decode_shared_prefix(out_, q_, kc, vc, tables_, lens_, b.max_seq_len, b.scale, ws,
+                                       gstart if gstart_ is None else gstart_,
+                                       gshared if gshared_ is None else gshared_, max_group, ks, vs, part, stream)
         else:
             pa.pa_decode(out_, q_, kc, vc, tables_, lens_, b.max_seq_len, b.scale, ws, ks, vs, part, stream,
                          window=args.window)
@@ -631,43 +633,75 @@ def run_ours(args):
                            else (tensor_line, hbm_line))
         roofline = dict(roofline, secondary={k: v for k, v in other.items() if k != "overlapped_kernel_ms"})
 
-    # ---- end to end through the public API with host buffers (pinned), K steps
+    # ---- end to end through the public API with host buffers (pinned), K steps.
+    # Every input of a step (q, new K/V, slots, block tables, lengths, query_start_loc,
+    # prefix groups) sits in one pinned host buffer, each at a 256-byte aligned offset,
+    # and moves with one host-to-device copy; the output comes back with one
+    # device-to-host copy.  The copies and the library calls are captured together
+    # and replayed as one CUDA graph per step (eager launches with --no-graph).
     e2e = None
     if not args.no_e2e:
-        hq_, hkey, hval, hslots, htab, hlens, hqsl = (t.cpu().pin_memory() for t in (q, key, val, slots, tables, lens, qsl))
-        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        dq, dkey, dval, dslots, dtab, dlens, dqsl = (torch.empty_like(t) for t in (q, key, val, slots, tables, lens, qsl))
-        h2d = sum(t.numel() * t.element_size() for t in (hq_, hkey, hval, hslots, htab, hlens) + ((hqsl,) if varlen else ()))
+        srcs = [q, key, val, slots, tables, lens] + ([qsl] if varlen else [])
         if groups is not None:
-            hgs, hgb = gstart.cpu().pin_memory(), gshared.cpu().pin_memory()
-            h2d += hgs.numel() * 4 + hgb.numel() * 4
+            srcs += [gstart, gshared]
+        offs, total = [], 0
+        for t in srcs:
+            offs.append(total)
+            total += -(-t.numel() * t.element_size() // 256) * 256
+        hbuf = torch.empty(total, dtype=torch.uint8).pin_memory()
+        dbuf = torch.empty(total, dtype=torch.uint8, device=dev)
+
+        def carve(buf, t, o):
+            return buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+
+        for t, o in zip(srcs, offs):
+            carve(hbuf, t, o).copy_(t)
+        dv = [carve(dbuf, t, o) for t, o in zip(srcs, offs)]
+        dq, dkey, dval, dslots, dtab, dlens = dv[:6]
+        dqsl = dv[6] if varlen else qsl
+        dgs, dgb = (dv[-2], dv[-1]) if groups is not None else (None, None)
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = total
         d2h = hout.numel() * hout.element_size()
 
         def e2e_step():
-            for d_, h_ in ((dq, hq_), (dkey, hkey), (dval, hval), (dslots, hslots), (dtab, htab), (dlens, hlens)):
-                d_.copy_(h_, non_blocking=True)
-            if varlen:
-                dqsl.copy_(hqsl, non_blocking=True)
-            if groups is not None:
-                gstart.copy_(hgs, non_blocking=True)
-                gshared.copy_(hgb, non_blocking=True)
-            step(dq, dkey, dval, dslots, dtab, dlens, dqsl, out)
+            dbuf.copy_(hbuf, non_blocking=True)
+            step(dq, dkey, dval, dslots, dtab, dlens, dqsl, out, dgs, dgb)
             hout.copy_(out, non_blocking=True)
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+        run_e2e, e2e_launch, capture_error = e2e_step, "eager", None
+        if not args.no_graph:
+            try:
+                e2e_graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(e2e_graph):
+                    e2e_step()
+                run_e2e, e2e_launch = e2e_graph.replay, "cuda_graph_replay"
+            except RuntimeError as ex:  # time the eager step instead, and say why
+                capture_error = str(ex).splitlines()[0][:200]
+                torch.cuda.synchronize(dev)
+        for _ in range(max(3, args.warmup)):
+            run_e2e()
         barrier()
         t0 = time.perf_counter()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record(stream)
         for _ in range(args.steps):
-            e2e_step()
+            run_e2e()
         f1.record(stream)
         barrier()
         wall_ms = (time.perf_counter() - t0) * 1000.0
         e2e_ms = max_over_ranks(max(f0.elapsed_time(f1), wall_ms), dev) / args.steps
+        # the copied inputs are the device-resident ones: the output read back must equal
+        # the device-resident step's
+        torch.cuda.synchronize(dev)
+        step()
+        torch.cuda.synchronize(dev)
+        same = bool(torch.equal(hout, out.cpu()))
         e2e = {"value": ctx_tokens * world / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "copies_per_step": {"h2d": 1, "d2h": 1},
+               "step_launch": e2e_launch, "output_equals_device_step": same}
+        if capture_error:
+            e2e["capture_error"] = capture_error
 
     flags = pa.pa_get_error_flags()
     if flags:
