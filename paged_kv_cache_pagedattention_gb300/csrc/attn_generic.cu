@@ -54,7 +54,7 @@ __device__ __forceinline__ float kv_elem(const KvRow& r, int dd) {
 }
 
 template <int QDT, int KVDT>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128, 1)
     attn_generic_kernel(const AttnParams p, int only_multi_token) {
   using QE = Elem<QDT>;
   const int lane = threadIdx.x & 31;
@@ -111,9 +111,16 @@ __global__ void __launch_bounds__(128)
       } else {
         tile = (long long)phys * p.num_kv_heads + kvh;
         const KvRow kr = kv_row<KVDT>(p.k_cache, tile, p.block_size, d, tt % p.block_size);
-        // eight independent loads in flight, four accumulation chains
+        // 32 independent loads in flight per round, four accumulation chains
         float dot[4] = {0.f, 0.f, 0.f, 0.f};
         int dd = 0;
+        for (; dd + 32 <= d; dd += 32) {
+          float kv[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) kv[e] = kv_elem<KVDT>(kr, dd + e);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) dot[e & 3] = fmaf(q_s[dd + e], kv[e], dot[e & 3]);
+        }
         for (; dd + 8 <= d; dd += 8) {
           float kv[8];
 #pragma unroll
@@ -133,23 +140,36 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int i = 0; i < kGenericMaxPerLane; ++i) acc[i] *= alpha;
     const int n = min(32, t1 - tb);
-#pragma unroll 4
-    // lane j's V row, handed to every lane in turn
+    // lane j's V row, handed to every lane; eight rows at a time, so that the loads
+    // of eight keys are in flight together
     const KvRow my_v = tile >= 0 ? kv_row<KVDT>(p.v_cache, tile, p.block_size, d, tt % p.block_size)
                                  : KvRow{nullptr, nullptr};
-    for (int j = 0; j < n; ++j) {
-      const float pv = __shfl_sync(0xffffffffu, pj, j);
-      KvRow vr;
-      vr.row = reinterpret_cast<const uint8_t*>(
-          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(my_v.row), j));
-      if (vr.row == nullptr) continue;  // unreadable block (flagged above): no weight, not read
-      if constexpr (is_nvfp4<KVDT>())
-        vr.scales = reinterpret_cast<const uint8_t*>(
-            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(my_v.scales), j));
+    for (int j0 = 0; j0 < n; j0 += 8) {
+      float pv[8];
+      KvRow vr[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u;  // < 32
+        pv[u] = __shfl_sync(0xffffffffu, pj, j);
+        vr[u].row = reinterpret_cast<const uint8_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(my_v.row), j));
+        vr[u].scales = nullptr;
+        if constexpr (is_nvfp4<KVDT>())
+          vr[u].scales = reinterpret_cast<const uint8_t*>(
+              __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(my_v.scales), j));
+        // keys past the group, or in an unreadable block (flagged above): not read
+        if (j >= n) vr[u].row = nullptr;
+      }
 #pragma unroll
       for (int i = 0; i < kGenericMaxPerLane; ++i) {
         const int dd = lane + 32 * i;
-        if (dd < d) acc[i] = fmaf(pv, kv_elem<KVDT>(vr, dd), acc[i]);
+        if (dd < d) {
+          float v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v[u] = vr[u].row != nullptr ? kv_elem<KVDT>(vr[u], dd) : 0.f;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) acc[i] = fmaf(pv[u], v[u], acc[i]);
+        }
       }
     }
     m = m_new;
