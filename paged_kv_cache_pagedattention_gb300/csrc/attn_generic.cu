@@ -267,14 +267,26 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnParams p
           o.w = fmaf(a[u].w, w[u], o.w);
         }
       }
-      for (; j < np; ++j) {
-        const float2 v = ml[(long long)j * hq];
-        const float w = v.y > 0.f ? exp2f(v.x - M) : 0.f;
-        const float4 a = reinterpret_cast<const float4*>(acc + j * stride)[c];
-        o.x = fmaf(a.x, w, o.x);
-        o.y = fmaf(a.y, w, o.y);
-        o.z = fmaf(a.z, w, o.z);
-        o.w = fmaf(a.w, w, o.w);
+      if (j < np) {  // the last np - j < 8 partials: every load issued before the first use
+        float4 a[8];
+        float w[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          w[u] = 0.f;
+          a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (j + u < np) {
+            const float2 v = ml[(long long)(j + u) * hq];
+            w[u] = v.y > 0.f ? exp2f(v.x - M) : 0.f;
+            a[u] = reinterpret_cast<const float4*>(acc + (j + u) * stride)[c];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          o.x = fmaf(a[u].x, w[u], o.x);
+          o.y = fmaf(a[u].y, w[u], o.y);
+          o.z = fmaf(a[u].z, w[u], o.z);
+          o.w = fmaf(a[u].w, w[u], o.w);
+        }
       }
       out[4 * c + 0] = QE::from_float(o.x * inv);
       out[4 * c + 1] = QE::from_float(o.y * inv);
