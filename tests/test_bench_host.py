@@ -1,0 +1,51 @@
+"""Host-side arithmetic of the benchmark, on the CPU: the counts its JSON line
+reports are checked against closed forms and against brute-force enumeration."""
+
+import numpy as np
+
+import bench
+import workloads
+
+
+def _brute_pairs(b, window=0):
+    """Enumerate every (query, key) pair the attention scores."""
+    total = 0
+    qsl = b.query_start_loc
+    for r, n in enumerate(b.seq_lens):
+        n, q = int(n), int(qsl[r + 1] - qsl[r])
+        for j in range(q):
+            p = n - q + j
+            for t in range(n):
+                if b.causal and t > p:
+                    continue
+                if window and t < p - window + 1:
+                    continue
+                total += 1
+    return total
+
+
+def test_decode_pairs_are_the_context_tokens():
+    b = workloads.tiny()
+    assert bench.qk_pairs(b) == int(b.seq_lens.sum()) == 17 + 64 + 129 + 200
+    # a window of 32 keeps min(len, 32) keys per sequence
+    assert bench.qk_pairs(b, 32) == 17 + 32 + 32 + 32
+
+
+def test_chunk_pairs_closed_form_and_brute_force():
+    b = workloads.build("qk", 3, [70, 9, 33], [20, 1, 33], 8, 2, 64, 16, "bf16")
+    # a causal chunk of q tokens ending at n scores q (n - q + 1) + q (q - 1) / 2 pairs
+    want = sum(q * (n - q + 1) + q * (q - 1) // 2 for n, q in ((70, 20), (9, 1), (33, 33)))
+    assert bench.qk_pairs(b) == want == _brute_pairs(b)
+    for w in (1, 5, 40):
+        assert bench.qk_pairs(b, w) == _brute_pairs(b, w)
+
+
+def test_non_causal_rows_score_the_whole_context():
+    b = workloads.build("qk_nc", 4, [50, 12], [10, 12], 8, 2, 64, 16, "bf16", causal=False)
+    assert bench.qk_pairs(b) == 10 * 50 + 12 * 12 == _brute_pairs(b)
+
+
+def test_empty_requests_score_nothing():
+    b = workloads.build("qk_empty", 5, [10, 30], [0, 2], 8, 2, 64, 16, "bf16")
+    assert bench.qk_pairs(b) == 29 + 30 == _brute_pairs(b)
+    assert np.diff(b.query_start_loc).tolist() == [0, 2]
