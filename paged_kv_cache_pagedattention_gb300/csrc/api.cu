@@ -9,6 +9,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -32,28 +33,32 @@ int current_device() {
   return dev;
 }
 
+// Per-device lookups below are cached in atomics: host threads may call on the
+// same or different devices at once, and a repeated lookup stores the same value.
 unsigned* error_word() {
-  static unsigned* cache[kMaxDevices] = {};
+  static std::atomic<unsigned*> cache[kMaxDevices] = {};
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!cache[dev]) {
+  unsigned* w = cache[dev].load(std::memory_order_acquire);
+  if (!w) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_pa_error_word) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<unsigned*>(ptr);
+    w = static_cast<unsigned*>(ptr);
+    cache[dev].store(w, std::memory_order_release);
   }
-  return cache[dev];
+  return w;
 }
 
 int sm_count() {
-  static int cache[kMaxDevices] = {};
+  static std::atomic<int> cache[kMaxDevices] = {};
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return 148;
-  if (!cache[dev]) {
-    int n = 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return n;
 }
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
