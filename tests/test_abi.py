@@ -143,3 +143,19 @@ def test_nvfp4_host_validation_without_a_gpu(pa):
               None) == pa.PA_ERR_UNSUPPORTED                             # 72-byte tiles
     assert rc(fake, fake, fake, fake, fake, 3, 10, 2, 128, 16, pa.PA_BF16, pa.PA_NVFP4_PER_HEAD, None, None,
               None) == pa.PA_ERR_INVALID_ARG                             # scales missing
+
+
+def test_static_workspace_host_validation_without_a_gpu(pa):
+    """The no-workspace decode rejects bad sizes, and does nothing for an empty batch,
+    before it looks up its device array."""
+    lib = ctypes.CDLL(pa.LIB_PATH)
+    fn = lib.pa_decode_static_workspace
+    fn.restype, fn.argtypes = pa.SIGNATURES["pa_decode_static_workspace"]
+    fake = 1 << 20  # never dereferenced: the checks return first
+    args = [fake, fake, fake, fake, 10, fake, 4, fake, 2, 64, 8, 2, 128, 16, 0.1, pa.PA_BF16, pa.PA_BF16, None, None,
+            0, None]
+    assert fn(*args[:8], 0, *args[9:]) == pa.PA_OK                      # no sequences: nothing to do
+    assert fn(*args[:8], -1, *args[9:]) == pa.PA_ERR_INVALID_ARG         # negative batch
+    assert fn(*args[:13], 0, *args[14:]) == pa.PA_ERR_INVALID_ARG        # block size 0
+    assert fn(*args[:9], 0, *args[10:]) == pa.PA_ERR_INVALID_ARG         # max_seq_len 0
+    assert fn(*args[:19], -16, None) == pa.PA_ERR_INVALID_ARG            # negative partition size
