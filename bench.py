@@ -321,6 +321,12 @@ def qk_pairs(b, window: int = 0) -> int:
 
 # ----------------------------------------------------------------------------- oracle (CPU) arm
 
+# The oracle's sample: the first ORACLE_SAMPLE_TOKENS tokens of the workload's
+# median-length sequence, one decode query per worker process, each worker on its own
+# copy.  The main arm's cpu_baseline and the reference arm time this same sample.
+ORACLE_SAMPLE_TOKENS = 32768
+REFERENCE_BUDGET_S = 240.0
+
 _CPU_SAMPLE = {}
 
 
@@ -350,22 +356,16 @@ def _cpu_worker_run(_):
 class OracleSampler:
     """The fp64 oracle timed on host cores: W worker processes (spawned, one BLAS
     thread each), each running the oracle on one decode sequence with the
-    workload's head shape, dtype and block size (the median length, or its first
-    tokens when a time budget is given).  Rate = attended tokens / wall time."""
+    workload's head shape, dtype and block size: the first `tokens` tokens of the
+    median-length sequence.  Rate = attended tokens / wall time of a step."""
 
-    # oracle cost measured on one x86 core: about 3.3e5 (context token x query head)
-    # per second; sizes a sample to a time budget
-    TOKEN_HEADS_PER_CORE_SECOND = 3.3e5
-
-    def __init__(self, b, workers: int, budget_s: float | None = None):
+    def __init__(self, b, workers: int, tokens: int = ORACLE_SAMPLE_TOKENS):
         self.b = b
         self.workers = workers
         L = int(sorted(b.seq_lens)[len(b.seq_lens) // 2])  # median-length sequence
         self.full_length = L
-        if budget_s is not None:
-            L = min(L, max(256, int(self.TOKEN_HEADS_PER_CORE_SECOND / b.num_q_heads * budget_s)))
-        self.length = L
-        shape = (b.name, 11, L, b.num_q_heads, b.num_kv_heads, b.head_size, b.block_size, b.kv_dtype)
+        self.length = min(L, int(tokens))
+        shape = (b.name, 11, self.length, b.num_q_heads, b.num_kv_heads, b.head_size, b.block_size, b.kv_dtype)
         ctx = mp.get_context("spawn")
         env_keep = os.environ.get("OPENBLAS_NUM_THREADS")
         os.environ["OPENBLAS_NUM_THREADS"] = "1"
@@ -383,9 +383,9 @@ class OracleSampler:
         return tokens / wall, wall
 
     def describe(self):
-        which = ("the batch's median length" if self.length == self.full_length else
-                 f"the first {self.length} tokens of a median-length ({self.full_length}) sequence")
-        return (f"{self.workers} processes x 1 decode sequence of {self.length} tokens ({which}), "
+        which = ("the whole median-length sequence" if self.length == self.full_length else
+                 f"the first {self.length} tokens of a median-length ({self.full_length}-token) sequence")
+        return (f"{self.workers} processes x 1 decode query over {which}, "
                 f"{self.b.num_q_heads}/{self.b.num_kv_heads} heads, head {self.b.head_size}, "
                 f"{self.b.kv_dtype}, block {self.b.block_size}, per step")
 
@@ -404,9 +404,15 @@ def run_reference(args):
     if rank != 0:
         return 0
     b = make_workload(args.workload, BASE_SEEDS[args.workload])
-    # whole run (warm-up + timed steps) sized to about two minutes of oracle time
-    sampler = OracleSampler(b, cpu_workers(), budget_s=120.0 / (args.steps + args.warmup))
-    for _ in range(args.warmup):
+    sampler = OracleSampler(b, cpu_workers())
+    # The same sample as the main arm's cpu_baseline; shortened only when the whole
+    # run (warm-up + timed steps) would not end within the budget.
+    _, first = sampler.step()
+    if first * (args.steps + args.warmup) > REFERENCE_BUDGET_S:
+        tokens = max(256, int(sampler.length * REFERENCE_BUDGET_S / (first * (args.steps + args.warmup))))
+        sampler.close()
+        sampler = OracleSampler(b, cpu_workers(), tokens)
+    for _ in range(max(0, args.warmup - 1)):
         sampler.step()
     rates, walls = [], []
     for _ in range(args.steps):
@@ -428,20 +434,386 @@ def run_reference(args):
     return 0
 
 
-def workload_config(b, args):
+def workload_config(b, args, api=None):
+    if api is None:
+        api = ("pa_varlen_attn" if b.max_query_len > 1 else
+               "pa_decode" if (args.no_shared_prefix or not b.families) else "pa_decode_shared_prefix")
     return {"workload": b.name, "num_seqs": b.num_seqs, "total_context_tokens": int(sum(int(n) for n in b.seq_lens)),
             "max_seq_len": b.max_seq_len, "num_q_heads": b.num_q_heads, "num_kv_heads": b.num_kv_heads,
             "head_size": b.head_size, "block_size": b.block_size, "kv_dtype": b.kv_dtype,
             "q_dtype": b.q_dtype, "new_tokens_per_step": b.total_q,
             "partition_size": args.partition_size or "auto",
-            "decode_api": ("pa_varlen_attn" if b.max_query_len > 1 else
-                           "pa_decode" if (args.no_shared_prefix or not b.families) else "pa_decode_shared_prefix"),
+            "decode_api": api,
             "length_scale": args.length_scale,
             "sliding_window": args.window or None,
             "l2": "inputs larger than L2 (KV working set >> 129 MB)" if b.name != "tiny" else "tiny (fits L2)"}
 
 
 # ----------------------------------------------------------------------------- GPU arm
+
+def device_inputs(b, dev) -> dict:
+    """The batch's tensors on the device: caches, new K/V, slots, q, tables, lengths."""
+    import torch
+
+    import workloads
+
+    kc, vc = workloads.device_cache(b, dev)
+    T = workloads.bits_to_torch
+    scaled = b.kv_dtype in workloads.SCALED
+    d = {"kc": kc, "vc": vc, "key": T(b.key, b.src_dtype, dev), "val": T(b.value, b.src_dtype, dev),
+         "slots": torch.from_numpy(b.slot_mapping).to(dev), "q": T(b.q, b.q_dtype, dev),
+         "tables": torch.from_numpy(b.block_tables).to(dev), "lens": torch.from_numpy(b.seq_lens).to(dev),
+         "qsl": torch.from_numpy(b.query_start_loc).to(dev),
+         "ks": torch.tensor([b.k_scale], dtype=torch.float32, device=dev) if scaled else None,
+         "vs": torch.tensor([b.v_scale], dtype=torch.float32, device=dev) if scaled else None}
+    d["out"] = torch.empty_like(d["q"])
+    return d
+
+
+class Runner:
+    """One step of the hot path on a prepared batch: the scatter of the new tokens, then
+    the attention call of `mode` -- "varlen" (pa_varlen_attn), "shared"
+    (pa_decode_shared_prefix with the batch's fork groups) or "decode" (pa_decode,
+    windowed when `window` > 0)."""
+
+    def __init__(self, pa, b, d, dev, mode, part=0, window=0):
+        import torch
+
+        self.pa, self.b, self.d, self.dev = pa, b, d, dev
+        self.mode, self.part, self.window = mode, part, window
+        self.groups = prefix_groups(b) if mode == "shared" else None
+        if mode == "shared" and self.groups is None:
+            raise ValueError("shared-prefix mode needs a batch of fork families")
+        if mode == "varlen":
+            wsb = pa.pa_varlen_workspace_size(b.num_seqs, b.total_q, b.max_query_len, b.num_q_heads,
+                                              b.num_kv_heads, b.head_size, b.max_seq_len, b.block_size, part)
+        elif mode == "shared":
+            wsb = pa.pa_decode_shared_prefix_workspace_size(b.num_seqs, len(self.groups[1]), b.num_q_heads,
+                                                            b.num_kv_heads, b.head_size, b.max_seq_len,
+                                                            b.block_size, part)
+            self.gstart = torch.from_numpy(self.groups[0]).to(dev)
+            self.gshared = torch.from_numpy(self.groups[1]).to(dev)
+            self.max_group = int(max(self.groups[0][1:] - self.groups[0][:-1]))
+        else:
+            wsb = pa.pa_decode_workspace_size(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_size,
+                                              b.max_seq_len, b.block_size, part)
+        self.ws = pa.workspace_tensor(wsb, dev)
+
+    def inputs(self) -> list:
+        """The per-step inputs a caller copies in (the e2e leg's host-to-device bytes)."""
+        d = self.d
+        srcs = [d["q"], d["key"], d["val"], d["slots"], d["tables"], d["lens"]]
+        if self.mode == "varlen":
+            srcs.append(d["qsl"])
+        if self.mode == "shared":
+            srcs += [self.gstart, self.gshared]
+        return srcs
+
+    def step(self, srcs=None, out=None):
+        import torch
+
+        pa, b, d = self.pa, self.b, self.d
+        q, key, val, slots, tables, lens = (srcs or self.inputs())[:6]
+        out = d["out"] if out is None else out
+        stream = torch.cuda.current_stream(self.dev)  # the capture stream while a graph is recorded
+        pa.pa_reshape_and_cache(key, val, d["kc"], d["vc"], slots, d["ks"], d["vs"], stream)
+        if self.mode == "varlen":
+            qsl = srcs[6] if srcs else d["qsl"]
+            pa.pa_varlen_attn(out, q, d["kc"], d["vc"], tables, qsl, lens, b.max_query_len, b.max_seq_len, b.scale,
+                              self.ws, True, d["ks"], d["vs"], self.part, stream)
+        elif self.mode == "shared":
+            gs, gb = (srcs[-2], srcs[-1]) if srcs else (self.gstart, self.gshared)
+            pa.pa_decode_shared_prefix(out, q, d["kc"], d["vc"], tables, lens, b.max_seq_len, b.scale, self.ws,
+                                       gs, gb, self.max_group, d["ks"], d["vs"], self.part, stream)
+        else:
+            pa.pa_decode(out, q, d["kc"], d["vc"], tables, lens, b.max_seq_len, b.scale, self.ws, d["ks"], d["vs"],
+                         self.part, stream, window=self.window)
+
+
+def timed_regions(run, steps, stream, barrier, dev, min_total_ms):
+    """Milliseconds per step of K = `steps` calls of `run`, each region bracketed by a
+    barrier (and a device synchronise) on both sides and timed with CUDA events on
+    the launching stream, maximum over ranks.  The region is repeated until about
+    `min_total_ms` of device time has passed (so that a clock sampler running beside
+    it sees the GPU under load); returns the per-step times of every repeat."""
+    import torch
+
+    out = []
+    total = 0.0
+    while True:
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            run()
+        e1.record(stream)
+        barrier()
+        ms = max_over_ranks(e0.elapsed_time(e1), dev)
+        out.append(ms / steps)
+        total += ms
+        if total >= min_total_ms or len(out) >= 400:
+            return out
+
+
+def traced_eager(pa, run, steps, stream, barrier, dev):
+    """One eager K-step region with the library's event tracing on: milliseconds per
+    step, and per kernel kind (launches, total ms)."""
+    import torch
+
+    pa.pa_trace_read(0, reset=True)
+    pa.pa_trace_enable(True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        run()
+    e1.record(stream)
+    barrier()
+    pa.pa_trace_enable(False)
+    ms = max_over_ranks(e0.elapsed_time(e1), dev) / steps
+    return ms, {name: pa.pa_trace_read(k) for k, name in enumerate(pa.TRACE_KINDS)}
+
+
+def capture(run):
+    """The step captured once into a CUDA graph (the library's calls neither
+    synchronise nor allocate), returned as its replay function."""
+    import torch
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    return graph.replay
+
+
+def roofline_of(b, runner, trace, ms_per_step, args, window=0):
+    """Roofline of the dominant kernel (or fork-join span) of one measured workload."""
+    import workloads
+
+    nbytes = algorithmic_bytes(b, window)
+    n_att, ms_att = trace["attention"]
+    att_ms = ms_att / max(n_att, 1)
+    peak, peak_kind = measured_peaks()
+    kernel_ms = {k: (v[1] / v[0] if v[0] else 0.0) for k, v in trace.items()}
+    src = f"{peak_kind} MEASURED_PEAKS.json hbm_gbs"
+    if runner.mode == "shared":
+        # the shared-prefix tiles and the private-remainder decode run concurrently:
+        # their fork -> join span is the unit measured against HBM
+        sb = shared_split_bytes(b, runner.groups)
+        span_ms = kernel_ms.get("shared_span", 0.0)
+        achieved = nbytes["algorithmic"] / (span_ms / 1000.0) / 1e9 if span_ms else 0.0
+        logical_gbs = nbytes["logical_total"] / (span_ms / 1000.0) / 1e9 if span_ms else 0.0
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": profiled_traffic(args.workload, "shared_prefix_span"),
+                "kernel": "shared_prefix_tile_kernel || decode_mma_kernel (one fork-join span)",
+                "peak_source": src, "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                "byte_basis": "unique physical bytes: each shared prefix block counted once (the "
+                              "prefix-sharing decode reads it once per family)",
+                "algorithmic_bytes_per_launch": nbytes["algorithmic"],
+                "shared_kv_bytes": sb["shared"], "private_kv_bytes": sb["private"],
+                "logical_bytes_per_launch": nbytes["logical_total"],
+                "logical_kv_bytes_per_launch": nbytes["logical_kv"], "logical_gbs": logical_gbs,
+                "logical_over_peak": logical_gbs / peak,
+                "logical_note": "logical bytes (every sequence's whole context, shared blocks once per "
+                                "member) / span: above 1 because shared blocks are read once, not HBM bandwidth",
+                "kernel_ms": span_ms,
+                "overlapped_kernel_ms": {"shared_prefix_tile_kernel": kernel_ms.get("shared_prefix", 0.0),
+                                         "decode_mma_kernel": att_ms}}
+    if runner.mode == "decode":
+        achieved = nbytes["algorithmic"] / (att_ms / 1000.0) / 1e9
+        shared_blocks = nbytes["unique_kv"] != nbytes["logical_kv"]
+        line = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "kernel": "decode_mma_kernel" if b.kv_dtype != "f32" else "attn_generic_kernel",
+                "peak_source": src, "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                "byte_basis": ("unique physical bytes (shared blocks once; L2 serves the repeats)" if shared_blocks
+                               else "logical KV + q + out + block tables"),
+                "algorithmic_bytes_per_launch": nbytes["algorithmic"],
+                "logical_bytes_per_launch": nbytes["logical_total"],
+                "logical_kv_bytes_per_launch": nbytes["logical_kv"],
+                "logical_gbs": nbytes["logical_total"] / (att_ms / 1000.0) / 1e9,
+                "kernel_ms": att_ms, "merge_ms": kernel_ms.get("merge", 0.0),
+                "scatter_ms": kernel_ms.get("reshape_and_cache", 0.0)}
+        prof = "agentic_pa_decode" if shared_blocks else args.workload
+        line["traffic"] = profiled_traffic(prof)
+        return line
+    # varlen: the single-token rows (HBM-bound decode kernel) and the multi-token rows
+    # (tensor-bound prefill tiles) run concurrently: their fork -> join span is the
+    # unit, measured against HBM for all the bytes both must move, and against the
+    # tensor peak for the prefill FLOPs
+    vsplit = varlen_split(b)
+    span_ms = kernel_ms.get("varlen_span", 0.0)
+    qb = workloads.ELEM_BYTES[b.q_dtype]
+    pf_rows = int(sum(int(b.query_start_loc[r + 1] - b.query_start_loc[r]) for r in range(b.num_seqs)
+                      if int(b.query_start_loc[r + 1] - b.query_start_loc[r]) > 1))
+    span_bytes = vsplit["decode_bytes"] + vsplit["prefill_kv_bytes"] + 2 * pf_rows * b.num_q_heads * b.head_size * qb
+    achieved = span_bytes / (span_ms / 1000.0) / 1e9 if span_ms else 0.0
+    pf_tflops = vsplit["prefill_flops"] / (span_ms / 1000.0) / 1e12 if span_ms else 0.0
+    tpeak, tkind = measured_bf16_sustained()
+    kernel_name = "decode_mma_kernel || prefill_tc_kernel (one fork-join span)"
+    # per step: the prefill tiles launch twice when decode rows run beside them
+    n_span = max(trace["varlen_span"][0], 1)
+    overlapped = {"decode_mma_kernel": att_ms, "prefill_tc_kernel": trace["prefill_tiles"][1] / n_span}
+    traffic = profiled_traffic(args.workload, "varlen_span")
+    hbm_line = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic, "kernel": kernel_name, "peak_source": src,
+                "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                "algorithmic_bytes_per_launch": span_bytes, "kernel_ms": span_ms,
+                "overlapped_kernel_ms": overlapped}
+    tensor_line = {"bound": "tensor", "achieved": pf_tflops, "peak": tpeak, "unit": "TFLOP/s",
+                   "frac": pf_tflops / tpeak, "kernel": kernel_name, "kernel_ms": span_ms,
+                   "algorithmic_flops_per_launch": vsplit["prefill_flops"], "traffic": traffic,
+                   "peak_source": f"{tkind} MEASURED_PEAKS.json bf16_tflops_sustained",
+                   "overlapped_kernel_ms": overlapped}
+    # the binding resource: the larger of the two lower bounds on the span
+    main, other = ((hbm_line, tensor_line) if hbm_line["frac"] >= tensor_line["frac"] else (tensor_line, hbm_line))
+    return dict(main, secondary={k: v for k, v in other.items() if k != "overlapped_kernel_ms"})
+
+
+def e2e_pipelined(runner, steps, stream, barrier, dev, use_graph):
+    """The step end to end through the public API from pinned host memory, pipelined.
+
+    Every input of a step (q, new K/V, slots, block tables, lengths, query_start_loc,
+    prefix groups) sits in one pinned host buffer at 256-byte aligned offsets and
+    moves with one host-to-device copy; the output returns with one device-to-host
+    copy.  Two device input buffers and two outputs alternate between steps: a copy
+    stream moves step i+1's inputs in while step i computes, and step i's output out
+    while step i+1 computes.  Copy i+1 waits for step i-1 to finish with that input
+    buffer; step i+2 waits (through copy i+2, behind it on the copy stream) for
+    output i to have left.  Every copy of every step is inside the timed region."""
+    import torch
+
+    srcs = runner.inputs()
+    offs, total = [], 0
+    for t in srcs:
+        offs.append(total)
+        total += -(-t.numel() * t.element_size() // 256) * 256
+    hbuf = torch.empty(total, dtype=torch.uint8).pin_memory()
+
+    def carve(buf, t, o):
+        return buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+
+    for t, o in zip(srcs, offs):
+        carve(hbuf, t, o).copy_(t)
+    dbufs = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+    views = [[carve(db, t, o) for t, o in zip(srcs, offs)] for db in dbufs]
+    outs = [torch.empty_like(runner.d["out"]) for _ in range(2)]
+    houts = [torch.empty(outs[0].shape, dtype=outs[0].dtype).pin_memory() for _ in range(2)]
+    computes = [lambda p=p: runner.step(views[p], outs[p]) for p in range(2)]
+    launch, capture_error = "eager", None
+    if use_graph:
+        try:
+            computes = [capture(c) for c in computes]
+            launch = "cuda_graph_replay (compute) + copies on a second stream"
+        except RuntimeError as ex:  # time the eager step instead, and say why
+            capture_error = str(ex).splitlines()[0][:200]
+            torch.cuda.synchronize(dev)
+    cs = torch.cuda.Stream(dev)
+    h2d_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+
+    def run_k(k):
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            dbufs[0].copy_(hbuf, non_blocking=True)
+            h2d_done[0].record(cs)
+        for i in range(k):
+            c, n = i % 2, 1 - i % 2
+            if i + 1 < k:
+                with torch.cuda.stream(cs):
+                    cs.wait_event(comp_done[n])  # step i-1 is done with input buffer n
+                    dbufs[n].copy_(hbuf, non_blocking=True)
+                    h2d_done[n].record(cs)
+            stream.wait_event(h2d_done[c])
+            computes[c]()
+            comp_done[c].record(stream)
+            with torch.cuda.stream(cs):
+                cs.wait_event(comp_done[c])
+                houts[c].copy_(outs[c], non_blocking=True)
+        stream.wait_stream(cs)
+
+    run_k(3)  # warm-up (and first use of the copy stream)
+    barrier()
+    t0 = time.perf_counter()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    run_k(steps)
+    f1.record(stream)
+    barrier()
+    wall_ms = (time.perf_counter() - t0) * 1000.0
+    e2e_ms = max_over_ranks(max(f0.elapsed_time(f1), wall_ms), dev) / steps
+    # the copied inputs are the device-resident ones: the output read back must equal
+    # the device-resident step's
+    torch.cuda.synchronize(dev)
+    runner.step()
+    torch.cuda.synchronize(dev)
+    same = bool(torch.equal(houts[(steps - 1) % 2], runner.d["out"].cpu()))
+    line = {"ms_per_step": e2e_ms, "h2d_bytes_per_step": total,
+            "d2h_bytes_per_step": houts[0].numel() * houts[0].element_size(),
+            "copies_per_step": {"h2d": 1, "d2h": 1}, "step_launch": launch, "pipelined": True,
+            "output_equals_device_step": same}
+    if capture_error:
+        line["capture_error"] = capture_error
+    return line
+
+
+def measure(pa, b, d, dev, mode, args, stream, barrier, steps, warmup, min_total_ms, window=0, e2e=False):
+    """Warm-up, one traced eager K-step region, then repeated graph-replayed K-step
+    regions (eager with --no-graph); the roofline of the dominant kernel."""
+    runner = Runner(pa, b, d, dev, mode, args.partition_size, window)
+    for _ in range(warmup):
+        runner.step()
+    torch_sync(dev)
+    flags = pa.pa_get_error_flags()
+    if flags:
+        raise RuntimeError(f"{b.name}: device error flags {flags:#x} during warm-up")
+    ms_eager, trace = traced_eager(pa, runner.step, steps, stream, barrier, dev)
+    run = runner.step
+    if not args.no_graph:
+        run = capture(runner.step)
+        for _ in range(3):
+            run()
+    per_step = timed_regions(run, steps, stream, barrier, dev, min_total_ms)
+    ms = statistics.median(per_step)
+    res = {"runner": runner, "trace": trace, "ms_per_step": ms, "ms_per_step_eager": ms_eager,
+           "repeats": len(per_step), "ms_per_step_min": min(per_step), "ms_per_step_max": max(per_step),
+           "step_launch": "eager" if args.no_graph else "cuda_graph_replay",
+           "launches": sum(n for name, (n, _) in trace.items() if not name.endswith("_span"))}
+    res["roofline"] = roofline_of(b, runner, trace, ms, args, window)
+    if e2e:
+        res["e2e"] = e2e_pipelined(runner, steps, stream, barrier, dev, not args.no_graph)
+    flags = pa.pa_get_error_flags()
+    if flags:
+        raise RuntimeError(f"{b.name}: device error flags {flags:#x} during the timed region")
+    return res
+
+
+def torch_sync(dev):
+    import torch
+
+    torch.cuda.synchronize(dev)
+
+
+# The other configurations of the path, measured in the same run as the headline:
+# (entry name, workload, attention call).
+CONFIG_LEGS = (("tiny", "tiny", "decode"), ("llama", "llama", "decode"), ("mixed", "mixed", "varlen"),
+               ("fp8", "fp8", "decode"), ("agentic_pa_decode", "agentic", "decode"))
+
+
+def compact(res, b, window=0) -> dict:
+    """The fields of one measured configuration that the bench line reports."""
+    rl = res["roofline"]
+    ctx = int(sum(window_tokens(b, window)))
+    keep = ("bound", "achieved", "peak", "unit", "frac", "kernel", "kernel_ms", "byte_basis", "traffic",
+            "algorithmic_bytes_per_launch", "algorithmic_flops_per_launch", "logical_gbs", "merge_ms", "scatter_ms",
+            "overlapped_kernel_ms")
+    out = {"workload": b.name, "decode_api": {"decode": "pa_decode", "varlen": "pa_varlen_attn",
+                                              "shared": "pa_decode_shared_prefix"}[res["runner"].mode],
+           "ms_per_step": res["ms_per_step"], "ms_per_step_eager": res["ms_per_step_eager"],
+           "timed_repeats": res["repeats"], "value": ctx / (res["ms_per_step"] / 1000.0), "unit": UNIT,
+           "gpu_launches": res["launches"], "roofline": {k: rl[k] for k in keep if k in rl}}
+    if "secondary" in rl:
+        out["roofline"]["secondary"] = {k: rl["secondary"][k] for k in keep if k in rl["secondary"]}
+    return out
+
 
 def run_ours(args):
     import torch
@@ -454,69 +826,22 @@ def run_ours(args):
     dev = torch.device("cuda", local_rank)
 
     import paged_kv_cache_pagedattention_gb300 as pa
-    import workloads
 
     b = make_workload(args.workload, rank_seed(BASE_SEEDS[args.workload], rank), args.length_scale)
     varlen = b.max_query_len > 1
-    kc, vc = workloads.device_cache(b, dev)
-    T = workloads.bits_to_torch
-    key, val = T(b.key, b.src_dtype, dev), T(b.value, b.src_dtype, dev)
-    slots = torch.from_numpy(b.slot_mapping).to(dev)
-    q = T(b.q, b.q_dtype, dev)
-    tables = torch.from_numpy(b.block_tables).to(dev)
-    lens = torch.from_numpy(b.seq_lens).to(dev)
-    qsl = torch.from_numpy(b.query_start_loc).to(dev)
-    scaled = b.kv_dtype in workloads.SCALED
-    ks = torch.tensor([b.k_scale], dtype=torch.float32, device=dev) if scaled else None
-    vs = torch.tensor([b.v_scale], dtype=torch.float32, device=dev) if scaled else None
-    out = torch.empty_like(q)
-    part = args.partition_size
-    if varlen:
-        wsb = pa.pa_varlen_workspace_size(b.num_seqs, b.total_q, b.max_query_len, b.num_q_heads, b.num_kv_heads,
-                                          b.head_size, b.max_seq_len, b.block_size, part)
-    else:
-        wsb = pa.pa_decode_workspace_size(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_size, b.max_seq_len,
-                                          b.block_size, part)
     if args.window and varlen:
         raise SystemExit("--window applies to the decode workloads (llama, fp8, agentic)")
-    groups = None if (varlen or args.no_shared_prefix or args.window) else prefix_groups(b)
-    if groups is not None:
-        wsb = pa.pa_decode_shared_prefix_workspace_size(b.num_seqs, len(groups[1]), b.num_q_heads,
-                                                        b.num_kv_heads, b.head_size, b.max_seq_len,
-                                                        b.block_size, part)
-        gstart = torch.from_numpy(groups[0]).to(dev)
-        gshared = torch.from_numpy(groups[1]).to(dev)
-        max_group = int(max(groups[0][1:] - groups[0][:-1]))
-    ws = pa.workspace_tensor(wsb, dev)
-
-    def step(q_=q, key_=key, value_=val, slots_=slots, tables_=tables, lens_=lens, qsl_=qsl, out_=out,
-             gstart_=None, gshared_=None):
-        stream = torch.cuda.current_stream(dev)  # the capture stream while a graph is recorded
-        pa.pa_reshape_and_cache(key_, value_, kc, vc, slots_, ks, vs, stream)
-        if varlen:
-            pa.pa_varlen_attn(out_, q_, kc, vc, tables_, qsl_, lens_, b.max_query_len, b.max_seq_len, b.scale, ws,
-                              True, ks, vs, part, stream)
-        elif groups is not None:
-            pa.pa_decode_shared_prefix(out_, q_, kc, vc, tables_, lens_, b.max_seq_len, b.scale, ws,
-                                       gstart if gstart_ is None else gstart_,
-                                       gshared if gshared_ is None else gshared_, max_group, ks, vs, part, stream)
-        else:
-            pa.pa_decode(out_, q_, kc, vc, tables_, lens_, b.max_seq_len, b.scale, ws, ks, vs, part, stream,
-                         window=args.window)
+    mode = ("varlen" if varlen else
+            "shared" if (not args.no_shared_prefix and not args.window and prefix_groups(b) is not None) else
+            "decode")
+    stream = torch.cuda.current_stream(dev)
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    flags = pa.pa_get_error_flags()
-    if flags:
-        raise RuntimeError(f"device error flags {flags:#x} during warm-up")
-
-    # ---- timed region: exactly K steps, CUDA events on the launching stream
+    d = device_inputs(b, dev)
     bus = None
     try:
         bus = torch.cuda.get_device_properties(dev).pci_bus_id
@@ -525,213 +850,74 @@ def run_ours(args):
     sampler = ClockSampler(bus) if rank == 0 else None
     if sampler:
         sampler.start()
-    stream = torch.cuda.current_stream(dev)
-    pa.pa_trace_read(0, reset=True)
-    pa.pa_trace_enable(True)
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    barrier()
-    pa.pa_trace_enable(False)
-    ms_eager = max_over_ranks(e0.elapsed_time(e1), dev) / args.steps
-    trace = {name: pa.pa_trace_read(k) for k, name in enumerate(pa.TRACE_KINDS)}
-    ms_graph = None
-    if not args.no_graph:
-        # The same step captured once into a CUDA graph (the library's calls neither
-        # synchronise nor allocate) and replayed: K replays timed with CUDA events.
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step()
-        for _ in range(3):
-            graph.replay()
-        barrier()
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
-        g1.record(stream)
-        barrier()
-        ms_graph = max_over_ranks(g0.elapsed_time(g1), dev) / args.steps
+    head = measure(pa, b, d, dev, mode, args, stream, barrier, args.steps, args.warmup, args.min_timed_ms,
+                   window=args.window, e2e=not args.no_e2e)
     clocks = sampler.stop() if sampler else None
-    ms_per_step = ms_graph if ms_graph is not None else ms_eager
+    ms_per_step = head["ms_per_step"]
     ctx_tokens = int(sum(window_tokens(b, args.window)))
     tok_s = ctx_tokens * world / (ms_per_step / 1000.0)
     qk = qk_pairs(b, args.window)
-    # kernel launches: every traced kind but the fork-join spans (which wrap launches)
-    launches = sum(n for name, (n, _) in trace.items() if not name.endswith("_span"))
-
-    # ---- roofline of the dominant kernel
-    nbytes = algorithmic_bytes(b, args.window)
-    n_att, ms_att = trace["attention"]
-    att_ms = ms_att / max(n_att, 1)
-    peak, peak_kind = measured_peaks()
-    kernel_ms = {k: (v[1] / v[0] if v[0] else 0.0) for k, v in trace.items()}
-    if groups is not None:
-        # the shared-prefix tiles and the private-remainder decode run concurrently:
-        # their fork -> join span is the unit measured against HBM
-        sb = shared_split_bytes(b, groups)
-        span_ms = kernel_ms.get("shared_span", 0.0)
-        achieved = nbytes["algorithmic"] / (span_ms / 1000.0) / 1e9 if span_ms else 0.0
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                    "traffic": profiled_traffic(args.workload, "shared_prefix_span"),
-                    "kernel": "shared_prefix_tile_kernel || decode_mma_kernel (one fork-join span)",
-                    "peak_source": f"{peak_kind} MEASURED_PEAKS.json hbm_gbs",
-                    "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
-                    "algorithmic_bytes_per_launch": nbytes["algorithmic"],
-                    "shared_kv_bytes": sb["shared"], "private_kv_bytes": sb["private"],
-                    "logical_kv_bytes_per_launch": nbytes["logical_kv"],
-                    "logical_gbs": nbytes["logical_total"] / (span_ms / 1000.0) / 1e9 if span_ms else 0.0,
-                    "kernel_ms": span_ms,
-                    "overlapped_kernel_ms": {"shared_prefix_tile_kernel": kernel_ms.get("shared_prefix", 0.0),
-                                             "decode_mma_kernel": att_ms}}
-    elif not varlen:
-        achieved = nbytes["algorithmic"] / (att_ms / 1000.0) / 1e9
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                    "traffic": profiled_traffic(args.workload),
-                    "kernel": "decode_mma_kernel" if b.kv_dtype != "f32" else "attn_generic_kernel",
-                    "peak_source": f"{peak_kind} MEASURED_PEAKS.json hbm_gbs",
-                    "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
-                    "algorithmic_bytes_per_launch": nbytes["algorithmic"],
-                    "logical_kv_bytes_per_launch": nbytes["logical_kv"],
-                    "logical_gbs": nbytes["logical_total"] / (att_ms / 1000.0) / 1e9,
-                    "kernel_ms": att_ms}
-    else:
-        # the single-token rows (HBM-bound decode kernel) and the multi-token rows
-        # (tensor-bound prefill tiles) run concurrently: their fork -> join span is the
-        # unit, measured against HBM for all the bytes both must move, and against the
-        # tensor peak for the prefill FLOPs
-        vsplit = varlen_split(b)
-        span_ms = kernel_ms.get("varlen_span", 0.0)
-        qb = workloads.ELEM_BYTES[b.q_dtype]
-        pf_rows = int(sum(int(b.query_start_loc[r + 1] - b.query_start_loc[r]) for r in range(b.num_seqs)
-                          if int(b.query_start_loc[r + 1] - b.query_start_loc[r]) > 1))
-        span_bytes = vsplit["decode_bytes"] + vsplit["prefill_kv_bytes"] + 2 * pf_rows * b.num_q_heads * b.head_size * qb
-        achieved = span_bytes / (span_ms / 1000.0) / 1e9 if span_ms else 0.0
-        pf_tflops = vsplit["prefill_flops"] / (span_ms / 1000.0) / 1e12 if span_ms else 0.0
-        tpeak, tkind = measured_bf16_sustained()
-        kernel_name = "decode_mma_kernel || prefill_tc_kernel (one fork-join span)"
-        # per step: the prefill tiles launch twice when decode rows run beside them
-        n_span = max(trace["varlen_span"][0], 1)
-        overlapped = {"decode_mma_kernel": att_ms, "prefill_tc_kernel": trace["prefill_tiles"][1] / n_span}
-        hbm_line = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                    "traffic": profiled_traffic(args.workload, "varlen_span"), "kernel": kernel_name,
-                    "peak_source": f"{peak_kind} MEASURED_PEAKS.json hbm_gbs",
-                    "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
-                    "algorithmic_bytes_per_launch": span_bytes, "kernel_ms": span_ms,
-                    "overlapped_kernel_ms": overlapped}
-        tensor_line = {"bound": "tensor", "achieved": pf_tflops, "peak": tpeak, "unit": "TFLOP/s",
-                       "frac": pf_tflops / tpeak, "kernel": kernel_name, "kernel_ms": span_ms,
-                       "algorithmic_flops_per_launch": vsplit["prefill_flops"],
-                       "traffic": profiled_traffic(args.workload, "varlen_span"),
-                       "peak_source": f"{tkind} MEASURED_PEAKS.json bf16_tflops_sustained",
-                       "overlapped_kernel_ms": overlapped}
-        # the binding resource: the larger of the two lower bounds on the span
-        roofline, other = ((hbm_line, tensor_line) if hbm_line["frac"] >= tensor_line["frac"]
-                           else (tensor_line, hbm_line))
-        roofline = dict(roofline, secondary={k: v for k, v in other.items() if k != "overlapped_kernel_ms"})
-
-    # ---- end to end through the public API with host buffers (pinned), K steps.
-    # Every input of a step (q, new K/V, slots, block tables, lengths, query_start_loc,
-    # prefix groups) sits in one pinned host buffer, each at a 256-byte aligned offset,
-    # and moves with one host-to-device copy; the output comes back with one
-    # device-to-host copy.  The copies and the library calls are captured together
-    # and replayed as one CUDA graph per step (eager launches with --no-graph).
+    roofline = head["roofline"]
     e2e = None
-    if not args.no_e2e:
-        srcs = [q, key, val, slots, tables, lens] + ([qsl] if varlen else [])
-        if groups is not None:
-            srcs += [gstart, gshared]
-        offs, total = [], 0
-        for t in srcs:
-            offs.append(total)
-            total += -(-t.numel() * t.element_size() // 256) * 256
-        hbuf = torch.empty(total, dtype=torch.uint8).pin_memory()
-        dbuf = torch.empty(total, dtype=torch.uint8, device=dev)
+    if "e2e" in head:
+        e2e = dict(head["e2e"], value=ctx_tokens * world / (head["e2e"]["ms_per_step"] / 1000.0), unit=UNIT)
+    if clocks and clocks.get("sm_mhz"):
+        clocks["ms_per_step_x_median_sm_mhz"] = ms_per_step * clocks["sm_mhz"]
 
-        def carve(buf, t, o):
-            return buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
-
-        for t, o in zip(srcs, offs):
-            carve(hbuf, t, o).copy_(t)
-        dv = [carve(dbuf, t, o) for t, o in zip(srcs, offs)]
-        dq, dkey, dval, dslots, dtab, dlens = dv[:6]
-        dqsl = dv[6] if varlen else qsl
-        dgs, dgb = (dv[-2], dv[-1]) if groups is not None else (None, None)
-        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        h2d = total
-        d2h = hout.numel() * hout.element_size()
-
-        def e2e_step():
-            dbuf.copy_(hbuf, non_blocking=True)
-            step(dq, dkey, dval, dslots, dtab, dlens, dqsl, out, dgs, dgb)
-            hout.copy_(out, non_blocking=True)
-
-        run_e2e, e2e_launch, capture_error = e2e_step, "eager", None
-        if not args.no_graph:
-            try:
-                e2e_graph = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(e2e_graph):
-                    e2e_step()
-                run_e2e, e2e_launch = e2e_graph.replay, "cuda_graph_replay"
-            except RuntimeError as ex:  # time the eager step instead, and say why
-                capture_error = str(ex).splitlines()[0][:200]
-                torch.cuda.synchronize(dev)
-        for _ in range(max(3, args.warmup)):
-            run_e2e()
-        barrier()
-        t0 = time.perf_counter()
-        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        for _ in range(args.steps):
-            run_e2e()
-        f1.record(stream)
-        barrier()
-        wall_ms = (time.perf_counter() - t0) * 1000.0
-        e2e_ms = max_over_ranks(max(f0.elapsed_time(f1), wall_ms), dev) / args.steps
-        # the copied inputs are the device-resident ones: the output read back must equal
-        # the device-resident step's
-        torch.cuda.synchronize(dev)
-        step()
-        torch.cuda.synchronize(dev)
-        same = bool(torch.equal(hout, out.cpu()))
-        e2e = {"value": ctx_tokens * world / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "copies_per_step": {"h2d": 1, "d2h": 1},
-               "step_launch": e2e_launch, "output_equals_device_step": same}
-        if capture_error:
-            e2e["capture_error"] = capture_error
-
-    flags = pa.pa_get_error_flags()
-    if flags:
-        raise RuntimeError(f"device error flags {flags:#x} during the timed region")
+    # ---- every other configuration of the path, measured in this run (one GPU)
+    configs = None
+    if world == 1 and not args.no_configs and not args.window and args.length_scale == 1.0:
+        configs = {}
+        for name, wl, leg_mode in CONFIG_LEGS:
+            if wl == args.workload and leg_mode == mode:
+                continue  # the headline itself
+            # the headline's batch is reused; any other workload's tensors are freed after its leg
+            bb = b if wl == args.workload else make_workload(wl, BASE_SEEDS[wl])
+            dd = d if wl == args.workload else device_inputs(bb, dev)
+            res = measure(pa, bb, dd, dev, leg_mode, args, stream, barrier, args.steps, args.warmup,
+                          args.min_timed_ms / 4)
+            configs[name] = compact(res, bb)
+            del res, dd
+            torch.cuda.synchronize(dev)
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.window:
-        sampler_cpu = OracleSampler(b, cpu_workers(), budget_s=15.0)
-        rate, wall = sampler_cpu.step()
+        sampler_cpu = OracleSampler(b, cpu_workers())
+        rates, walls = [], []
+        for _ in range(3):
+            r, w = sampler_cpu.step()
+            rates.append(r)
+            walls.append(w)
         sampler_cpu.close()
-        cpu = {"value": rate, "unit": UNIT, "cores": sampler_cpu.workers, "kind": "oracle",
-               "sample": sampler_cpu.describe(), "wall_s": wall}
+        cpu = {"value": statistics.median(rates), "unit": UNIT, "cores": sampler_cpu.workers, "kind": "oracle",
+               "sample": sampler_cpu.describe() + " (median of 3 steps)", "wall_s": statistics.median(walls)}
 
     if world > 1:
         dist.barrier()
     if rank == 0:
+        trace = head["trace"]
+        kernel_ms = {k: (v[1] / v[0] if v[0] else 0.0) for k, v in trace.items()}
         line = {"metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16" if b.kv_dtype == "bf16" else b.kv_dtype,
                 "data": "synthetic (seeded N(0,1) values, seeded block placement)",
-                "config": workload_config(b, args),
-                "hbm_gbs": achieved,
+                "config": workload_config(b, args, {"varlen": "pa_varlen_attn", "shared": "pa_decode_shared_prefix",
+                                                    "decode": "pa_decode"}[mode]),
+                "hbm_gbs": roofline["achieved"] if roofline["unit"] == "GB/s" else
+                roofline.get("secondary", {}).get("achieved"),
                 "qk_pairs_per_step": qk, "qk_pairs_per_s": qk * world / (ms_per_step / 1000.0),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "step_launch": "cuda_graph_replay" if ms_graph is not None else "eager",
-                "ms_per_step_eager": ms_eager,
-                "gpu_launches": launches,
+                "step_launch": head["step_launch"],
+                "timed_repeats": head["repeats"],
+                "timed_repeats_note": "each repeat times exactly `steps` steps between barriers; ms_per_step "
+                                      "is the median over repeats",
+                "ms_per_step_min": head["ms_per_step_min"], "ms_per_step_max": head["ms_per_step_max"],
+                "ms_per_step_eager": head["ms_per_step_eager"],
+                "gpu_launches": head["launches"],
                 "launches_by_kernel": {k: v[0] for k, v in trace.items() if v[0] and not k.endswith("_span")},
                 "kernel_ms_by_kind": {k: v for k, v in kernel_ms.items() if v},
-                "clocks": clocks}
+                "clocks": clocks, "configs": configs}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -859,6 +1045,10 @@ def main(argv=None):
                     help="agentic: call pa_decode instead of pa_decode_shared_prefix")
     ap.add_argument("--op", choices=("attention", "copy_blocks"), default="attention",
                     help="copy_blocks: time the copy-on-write block copy alone")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="measure the headline workload only (skip the other configurations of the path)")
+    ap.add_argument("--min-timed-ms", type=float, default=1500.0,
+                    help="repeat the K-step timed region until about this much device time has passed")
     ap.add_argument("--length-scale", type=float, default=1.0,
                     help="shrink every sequence length (profiling captures only; 1.0 = the named workload)")
     args = ap.parse_args(argv)

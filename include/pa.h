@@ -22,14 +22,28 @@
  *             llm/landscape/lineages/inference-serving)
  *   [ARCH]    summary of a vLLM V1 architecture deep-dive
  *             (ai.youdonthavefriends.com, llm/ai/deep-analysis/2026/08/08/vllm-architecture)
+ *   [DSV41]   vLLM x DeepSeek-V4.1-Flash agentic throughput write-up (yaoyouai.cn)
  *
  * Conventions shared by every call
  * --------------------------------
  * Memory.  Every array argument is a DEVICE pointer owned by the caller, unless
- *   the argument says otherwise.  The library allocates nothing and keeps no
- *   per-call state; scratch memory is the caller's `workspace`, sized by the
+ *   the argument says otherwise.  The library allocates no device memory and keeps
+ *   no per-call state; scratch memory is the caller's `workspace`, sized by the
  *   matching *_workspace_size() query.  This follows [LINEAGE]'s rule that
  *   running out of memory is handled at admission, never while writing KV.
+ * Library state.  What the library does hold, once per device and for the life of
+ *   the process: one CUDA stream and two events, created by the first
+ *   pa_decode_shared_prefix call or pa_varlen_attn call with multi-token rows
+ *   (those calls run two kernels at once: they fork the second stream from
+ *   `stream` and join it back); two file-scope device symbols, the error word
+ *   (pa_get_error_flags) and the pa_decode_static_workspace array; and, on the
+ *   host, each kernel's shared-memory opt-in and occupancy figure, and the
+ *   tracing counters.
+ * Sizes and partitions.  The attention calls and their workspace queries take a
+ *   partition_size (0 = the default): split-K splits each context into partitions
+ *   of that many tokens, and the partition count sizes the workspace.  The default
+ *   depends on the number of (sequence, KV head) units and the SM count, which is
+ *   why the workspace queries also take num_kv_heads.
  * Streams.  All compute calls are asynchronous on `stream` (a cudaStream_t;
  *   NULL is the legacy default stream).  Calls on one stream run in issue order:
  *   write the new tokens with pa_reshape_and_cache, then attend.
@@ -101,6 +115,9 @@ typedef enum pa_status {
   PA_ERR_CUDA = 6         /* a CUDA runtime call or kernel launch failed */
 } pa_status;
 
+/* Element formats.  The first four are the formats of the serving path (queries and
+ * caches in fp32 / f16 / bf16, caches in FP8 e4m3); the rest are more KV formats:
+ * FP8 e5m2, one FP8 scale per KV head, and NVFP4 ([DSV41] "三、第二招"). */
 typedef enum pa_dtype {
   PA_F32 = 0,
   PA_F16 = 1,
@@ -119,6 +136,10 @@ typedef enum pa_dtype {
 #define PA_ERRFLAG_SEQ_LEN 0x4u     /* seq_len <= 0, > max_seq_len or > max_blocks_per_seq*block_size */
 #define PA_ERRFLAG_QUERY 0x8u       /* query_start_loc decreasing, q_len > seq_len or > max_query_len */
 #define PA_ERRFLAG_TIMEOUT 0x10u    /* a bounded wait for an asynchronous copy gave up */
+/* Diagnostic, not an error: pa_decode_shared_prefix met a member whose block-table
+ * entry differs from the group's first member on a block declared shared.  The
+ * output is unaffected: that member read its own block. */
+#define PA_ERRFLAG_SHARED_MISMATCH 0x20u
 
 /* Human-readable name of a status code.  Never NULL. */
 const char* pa_status_string(pa_status status);
@@ -198,6 +219,9 @@ int32_t pa_default_partition_size(int32_t num_seqs, int32_t num_kv_heads, int32_
  * Bytes of workspace pa_decode needs.  partition_size == 0 means the default
  * (pa_default_partition_size with the current device; pass num_kv_heads through
  * num_kv_heads).  Always >= 256: the first bytes hold internal bookkeeping.
+ * num_kv_heads and partition_size are parameters because the partition count
+ * sizes the workspace (one partial state per sequence, query head and partition)
+ * and the default partition size depends on sequences x KV heads.
  */
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                 int32_t head_size, int32_t max_seq_len, int32_t block_size,
@@ -223,6 +247,7 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t n
  *                  finite, else PA_ERR_INVALID_ARG (the same for every attention call).
  *                  FP8 scales (*k_scale, *v_scale) must be positive as well.
  *   partition_size 0 for the default, else a positive multiple of block_size
+ *                  (lets a caller force or tune split-K; the tests force it)
  *   workspace      device scratch of >= pa_decode_workspace_size(...) bytes,
  *                  256-byte aligned; contents need no initialisation
  * A sequence whose seq_len is out of range gets an all-zero output row and sets
@@ -284,9 +309,14 @@ size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_grou
  *   max_group_size     host bound on the members of any group, 1..8; groups larger
  *                      than the bound share nothing (still correct)
  *   the rest as pa_decode; workspace >= pa_decode_shared_prefix_workspace_size(...).
- * A member whose table disagrees with the group's first sequence on a block it is
- * declared to share sets PA_ERRFLAG_BLOCK_TABLE and that block is skipped for the
- * whole group.  Without a tensor-core path for the dtypes/shape (or with no groups)
+ * The declaration is a hint, checked block by block.  [AGENTIC] "統一分頁 + 共用池":
+ * shared blocks are copied on write, so a hint can be stale (a member already
+ * holds its own copy of a block) or wrong.  A member whose entry for a declared
+ * block names another physical block than the group's first sequence reads its own
+ * block (loaded separately, for that member alone), so the output is always that of
+ * pa_decode; the call sets the diagnostic PA_ERRFLAG_SHARED_MISMATCH.  Entries
+ * outside [0, num_blocks) are skipped and set PA_ERRFLAG_BLOCK_TABLE, as in
+ * pa_decode.  Without a tensor-core path for the dtypes/shape (or with no groups)
  * this is exactly pa_decode (with a workspace of the size above).
  * The shared-prefix and private-remainder kernels run at once: the call forks a
  * second stream of its own (created on the device's first call, with two events;
@@ -342,7 +372,10 @@ pa_status pa_decode_static_workspace(void* out, const void* q, const void* k_cac
 
 /*
  * Bytes of workspace pa_varlen_attn needs (>= 256).  Same partition_size rule
- * as pa_decode_workspace_size.
+ * as pa_decode_workspace_size.  The workspace holds the partial states of every
+ * row (single-token rows by the decode partition size, multi-token rows by
+ * partitions of >= 16384 tokens) and the plan of the prefill tiles, whose length
+ * follows total_q_tokens and the query heads per KV head.
  */
 size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t total_q_tokens, int32_t max_query_len,
                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
@@ -407,8 +440,9 @@ pa_status pa_varlen_attn_windowed(void* out, const void* q, const void* k_cache,
 /*
  * Read the device error word of the current device (host pointer `flags`),
  * after synchronising `stream`.  clear != 0 resets it to zero.  Returns
- * PA_ERR_BOUNDS if any PA_ERRFLAG_* other than TIMEOUT is set, PA_ERR_TIMEOUT
- * if only PA_ERRFLAG_TIMEOUT is set, PA_OK if none.
+ * PA_ERR_BOUNDS if any error bit other than TIMEOUT is set, PA_ERR_TIMEOUT if
+ * TIMEOUT is the only error bit set, PA_OK otherwise (no bit, or only the
+ * diagnostic PA_ERRFLAG_SHARED_MISMATCH; `flags` still reports it).
  */
 pa_status pa_get_error_flags(uint32_t* flags, int32_t clear, pa_stream_t stream);
 

@@ -37,6 +37,8 @@ PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3, PA_FP8_E5M2, PA_FP8_E4M3_PER_HEAD, PA_FP8_
     PA_NVFP4_PER_HEAD = range(9)
 PA_ERRFLAG_BLOCK_TABLE, PA_ERRFLAG_SLOT, PA_ERRFLAG_SEQ_LEN, PA_ERRFLAG_QUERY, PA_ERRFLAG_TIMEOUT = \
     0x1, 0x2, 0x4, 0x8, 0x10
+# diagnostic only: a declared shared block differed for some member (the output is unaffected)
+PA_ERRFLAG_SHARED_MISMATCH = 0x20
 
 # Names of the kernel kinds reported by pa_trace_read.
 TRACE_KINDS = ("reshape_and_cache", "attention", "merge", "varlen_plan", "prefill_tiles", "shared_prefix",

@@ -42,7 +42,10 @@ unsigned* error_word() {
   unsigned* w = cache[dev].load(std::memory_order_acquire);
   if (!w) {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_pa_error_word) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_pa_error_word) != cudaSuccess) {
+      (void)cudaGetLastError();  // consume it: a later launch check must not see it
+      return nullptr;
+    }
     w = static_cast<unsigned*>(ptr);
     cache[dev].store(w, std::memory_order_release);
   }
@@ -366,14 +369,14 @@ pa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Checks shared by pa_decode and pa_varlen_attn.
-pa_status check_attention_args(const void* out, const void* q, const void* k_cache, const void* v_cache,
-                               int32_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_seq,
-                               const int32_t* seq_lens, int32_t max_seq_len, int32_t num_q_heads,
-                               int32_t num_kv_heads, int32_t head_size, int32_t block_size,
-                               pa_dtype q_dtype, pa_dtype kv_dtype, const float* k_scale,
-                               const float* v_scale, int32_t partition_size, void* workspace) {
-  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !workspace) return PA_ERR_INVALID_ARG;
+// Checks shared by pa_decode and pa_varlen_attn, but for the workspace.
+pa_status check_attention_inputs(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                                 int32_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* seq_lens, int32_t max_seq_len, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                 pa_dtype q_dtype, pa_dtype kv_dtype, const float* k_scale,
+                                 const float* v_scale, int32_t partition_size) {
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PA_ERR_INVALID_ARG;
   if (num_blocks < 1 || max_blocks_per_seq < 1 || max_seq_len < 1 || num_q_heads < 1 || num_kv_heads < 1 ||
       head_size < 1 || block_size < 1)
     return PA_ERR_INVALID_ARG;
@@ -387,6 +390,22 @@ pa_status check_attention_args(const void* out, const void* q, const void* k_cac
   if (head_size > 256) return PA_ERR_UNSUPPORTED;
   if (num_kv_heads * ((num_q_heads / num_kv_heads + 7) / 8) > 65535) return PA_ERR_UNSUPPORTED;
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+// Checks shared by pa_decode and pa_varlen_attn.
+pa_status check_attention_args(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                               int32_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* seq_lens, int32_t max_seq_len, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                               pa_dtype q_dtype, pa_dtype kv_dtype, const float* k_scale,
+                               const float* v_scale, int32_t partition_size, void* workspace) {
+  const pa_status st = check_attention_inputs(out, q, k_cache, v_cache, num_blocks, block_tables,
+                                              max_blocks_per_seq, seq_lens, max_seq_len, num_q_heads,
+                                              num_kv_heads, head_size, block_size, q_dtype, kv_dtype, k_scale,
+                                              v_scale, partition_size);
+  if (st != PA_OK) return st;
+  if (!workspace) return PA_ERR_INVALID_ARG;
   if (!aligned(workspace, 256)) return PA_ERR_WORKSPACE;
   return PA_OK;
 }
@@ -423,6 +442,28 @@ AttnParams base_params(void* out, const void* q, const void* k_cache, const void
 }
 
 }  // namespace
+
+namespace pa {
+
+// The checks pa_decode makes on everything but the workspace, for entry points that
+// supply their own workspace (pa_decode_static_workspace), so that they report an
+// invalid argument before a size problem, as pa_decode does.
+pa_status check_decode_args(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                            int32_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            const int32_t* seq_lens, int32_t max_seq_len, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_size, int32_t block_size, float scale,
+                            pa_dtype q_dtype, pa_dtype kv_dtype, const float* k_scale, const float* v_scale,
+                            int32_t partition_size) {
+  const pa_status st = check_attention_inputs(out, q, k_cache, v_cache, num_blocks, block_tables,
+                                              max_blocks_per_seq, seq_lens, max_seq_len, num_q_heads,
+                                              num_kv_heads, head_size, block_size, q_dtype, base_dtype(kv_dtype),
+                                              k_scale, v_scale, partition_size);
+  if (st != PA_OK) return st;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+}  // namespace pa
 
 extern "C" {
 
@@ -844,8 +885,9 @@ pa_status pa_get_error_flags(uint32_t* flags, int32_t clear, pa_stream_t stream)
     if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
   }
   *flags = host;
-  if (host & ~PA_ERRFLAG_TIMEOUT) return PA_ERR_BOUNDS;
-  if (host & PA_ERRFLAG_TIMEOUT) return PA_ERR_TIMEOUT;
+  const unsigned errors = host & ~PA_ERRFLAG_SHARED_MISMATCH;  // the diagnostic bit is no error
+  if (errors & ~PA_ERRFLAG_TIMEOUT) return PA_ERR_BOUNDS;
+  if (errors & PA_ERRFLAG_TIMEOUT) return PA_ERR_TIMEOUT;
   return PA_OK;
 }
 

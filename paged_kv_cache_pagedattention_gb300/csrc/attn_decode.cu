@@ -12,6 +12,9 @@
 // here each shared (block, head) tile is loaded once and one warp per member
 // applies that member's query heads to it.  The members' private remainders run in
 // decode_mma_kernel from their first private token, and the merge combines both.
+// A member whose entry for a declared-shared block names another physical block
+// (a stale or wrong declaration) gets that block as a stage of its own, read by its
+// warp alone, so every member attends exactly its own blocks.
 //
 // Data movement.  Each (physical block, KV head) tile of K or V is contiguous in
 // HBM (block_size x head_size elements).  TMA bulk-tensor copies land a tile in
@@ -669,30 +672,58 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32)
     fence_mbar_init();
   }
   __syncthreads();
-  const int32_t* lead = p.block_tables + (long long)s0 * p.max_blocks_per_seq;
-
   if (warp == nm) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
+      const uint32_t all = (1u << nm) - 1u;
+      int gi = 0;  // stages issued so far
       for (int i = 0; i < nblocks; ++i) {
-        const int s = i % ST;
-        if (i >= ST && !mbar_wait_bounded(empty + s, ((i / ST) - 1) & 1)) {
-          flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-          break;  // the members time out on the full barrier and write nothing
-        }
         const int jb = b0 + i;
-        const int phys = lead[jb];
-        bool same = true;  // the members' tables must name the same physical block
-        for (int m = 1; m < nm; ++m)
-          same &= p.block_tables[(long long)(s0 + m) * p.max_blocks_per_seq + jb] == phys;
-        const bool valid = same && phys >= 0 && phys < p.num_blocks;
-        stage_ok[s] = valid;
-        if (!valid) {
-          flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
-          mbar_arrive(full + s);  // empty phase: the members skip this block
-        } else {
-          load_kv_tiles<KVDT, HEAD, BS>(smem + s * 2 * TB, p, &tmk, &tmv, kvh, phys, full + s);
+        // the common case, checked first: every member names the first member's block
+        const int lead = p.block_tables[(long long)s0 * p.max_blocks_per_seq + jb];
+        bool same = lead >= 0 && lead < p.num_blocks;
+        for (int m = 1; m < nm; ++m) same &= p.block_tables[(long long)(s0 + m) * p.max_blocks_per_seq + jb] == lead;
+        if (same) {
+          const int s = gi % ST;
+          if (gi >= ST && !mbar_wait_bounded(empty + s, ((gi / ST) - 1) & 1)) {
+            flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+            return;  // the members time out on the full barrier and write nothing
+          }
+          stage_ok[s] = (int)all | kStageLast;
+          load_kv_tiles<KVDT, HEAD, BS>(smem + s * 2 * TB, p, &tmk, &tmv, kvh, lead, full + s);
+          ++gi;
+          continue;
         }
+        // otherwise one stage per distinct physical block the members name, and an
+        // empty last stage when none is in range
+        int e[kMaxShareMembers];
+        load_share_entries(p, s0, nm, jb, e);
+        uint32_t done = 0, mask = 0;
+        int phys = 0;
+        int m = next_share_stage(p, e, nm, done, mask, phys);
+        if (m >= 0 && mask != all) flag_error(p.err, PA_ERRFLAG_SHARED_MISMATCH);
+        do {
+          uint32_t mask_n = 0;
+          int phys_n = 0, mn = -1;
+          if (m >= 0) {
+            done |= mask;
+            mn = next_share_stage(p, e, nm, done, mask_n, phys_n);
+          }
+          const int s = gi % ST;
+          if (gi >= ST && !mbar_wait_bounded(empty + s, ((gi / ST) - 1) & 1)) {
+            flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+            return;  // the members time out on the full barrier and write nothing
+          }
+          stage_ok[s] = (m >= 0 ? (int)mask : 0) | (mn < 0 ? kStageLast : 0);
+          if (m < 0)
+            mbar_arrive(full + s);  // empty phase: no member reads this block
+          else
+            load_kv_tiles<KVDT, HEAD, BS>(smem + s * 2 * TB, p, &tmk, &tmv, kvh, phys, full + s);
+          ++gi;
+          m = mn;
+          mask = mask_n;
+          phys = phys_n;
+        } while (m >= 0);
       }
     }
     return;
@@ -706,16 +737,23 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32)
   load_query<QDT, KVDT, HEAD>(p, seq, h0, nh, qb, cA, cB);
   WarpState<HEAD> w;
   w.init();
+  int gi = 0;  // stages consumed so far
   for (int i = 0; i < nblocks; ++i) {
-    const int s = i % ST;
-    const bool got = mbar_wait_bounded(full + s, (i / ST) & 1);
-    if (!__all_sync(0xffffffffu, got)) {
-      if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-      return;
+    bool last = false;
+    while (!last) {  // the block's stages; this member reads the one naming its block
+      const int s = gi % ST;
+      const bool got = mbar_wait_bounded(full + s, (gi / ST) & 1);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+        return;
+      }
+      const int rec = stage_ok[s];
+      last = (rec & kStageLast) != 0;
+      if ((rec >> warp) & 1) attend_block<QDT, KVDT, HEAD, BS>(smem + s * 2 * TB, BS, 0, qb, cA, cB, w);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
+      ++gi;
     }
-    if (stage_ok[s]) attend_block<QDT, KVDT, HEAD, BS>(smem + s * 2 * TB, BS, 0, qb, cA, cB, w);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty + s);
   }
 
   // ---- this member's partial state for partition z of its shared prefix
@@ -744,24 +782,6 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32)
     if (hA < nh) p.ws_ml[pi * p.num_q_heads + h0 + hA] = make_float2(w.mA, w.lA);
     if (hB < nh) p.ws_ml[pi * p.num_q_heads + h0 + hB] = make_float2(w.mB, w.lB);
   }
-}
-
-// Opt the kernel into `smem` bytes of dynamic shared memory, once per kernel and
-// device (one static per instantiation of this template, i.e. per kernel).
-template <auto kKernel>
-cudaError_t set_smem(int smem) {
-  static int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(kKernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) {
-      (void)cudaGetLastError();  // consume it: the caller reports the failure
-      return e;
-    }
-    configured_device = dev;
-  }
-  return cudaSuccess;
 }
 
 template <int QDT, int KVDT, int HEAD, int BS>

@@ -182,6 +182,11 @@ constexpr int prefill_smem_bytes() {
 // partial state at its sequence's shared partition z; the members' private tokens
 // are attended by the decode kernel and the merge combines both.
 //
+// The declaration is checked block by block: when a member's entry names another
+// physical block than the first member's (a stale share after copy-on-write, or a
+// wrong one), that block is loaded as a stage of its own and only that member's rows
+// read it (next_share_stage), so every member attends exactly its own blocks.
+//
 // The grid is persistent: as many CTAs as fit on the GPU at once, each taking work
 // items blockIdx.x, blockIdx.x + gridDim.x, ... (items of groups that share nothing,
 // or past a group's shared length, are skipped by every warp alike).  The ring's
@@ -246,33 +251,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == nwc) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      long long gi = 0;  // blocks issued so far, over all items
+      long long gi = 0;  // stages issued so far, over all items
       for (long long it = blockIdx.x; it < total; it += gridDim.x) {
         Item w;
         if (!decode_item(it, w)) continue;
-        const int32_t* lead = p.block_tables + (long long)w.s0 * p.max_blocks_per_seq;
-        for (int i = 0; i < w.nblocks; ++i, ++gi) {
-          const int s = (int)(gi % ST);
-          if (gi >= ST && !mbar_wait_bounded(empty + s, (uint32_t)((gi / ST) - 1) & 1)) {
-            flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-            return;  // the consumers time out on the full barrier and write nothing
-          }
+        const uint32_t all = (1u << w.nm) - 1u;
+        for (int i = 0; i < w.nblocks; ++i) {
           const int jb = w.b0 + i;
-          const int phys = lead[jb];
-          bool same = true;  // every member's table must name the same physical block
+          // the common case, checked first: every member names the first member's block
+          const int lead = p.block_tables[(long long)w.s0 * p.max_blocks_per_seq + jb];
+          bool same = lead >= 0 && lead < p.num_blocks;
           for (int m = 1; m < w.nm; ++m)
-            same &= p.block_tables[(long long)(w.s0 + m) * p.max_blocks_per_seq + jb] == phys;
-          const bool valid = same && phys >= 0 && phys < p.num_blocks;
-          stage_ok[s] = valid;
-          if (!valid) {
-            flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
-            mbar_arrive(full + s);  // empty phase: the block is skipped for the whole group
-          } else {
+            same &= p.block_tables[(long long)(w.s0 + m) * p.max_blocks_per_seq + jb] == lead;
+          if (same) {
+            const int s = (int)(gi % ST);
+            if (gi >= ST && !mbar_wait_bounded(empty + s, (uint32_t)((gi / ST) - 1) & 1)) {
+              flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+              return;  // the consumers time out on the full barrier and write nothing
+            }
+            stage_ok[s] = (int)all | kStageLast;
             uint8_t* st = smem + s * 2 * TB;
             mbar_arrive_expect_tx(full + s, 2 * TB);
-            tma_load_4d(st, &tmk, 0, w.kvh * BS, 0, phys, full + s);
-            tma_load_4d(st + TB, &tmv, 0, w.kvh * BS, 0, phys, full + s);
+            tma_load_4d(st, &tmk, 0, w.kvh * BS, 0, lead, full + s);
+            tma_load_4d(st + TB, &tmv, 0, w.kvh * BS, 0, lead, full + s);
+            ++gi;
+            continue;
           }
+          // otherwise one stage per distinct physical block the members name, and an
+          // empty last stage when none is in range
+          int e[kMaxShareMembers];
+          load_share_entries(p, w.s0, w.nm, jb, e);
+          uint32_t done = 0, mask = 0;
+          int phys = 0;
+          int m = next_share_stage(p, e, w.nm, done, mask, phys);
+          if (m >= 0 && mask != all) flag_error(p.err, PA_ERRFLAG_SHARED_MISMATCH);
+          do {
+            uint32_t mask_n = 0;
+            int phys_n = 0, mn = -1;
+            if (m >= 0) {
+              done |= mask;
+              mn = next_share_stage(p, e, w.nm, done, mask_n, phys_n);
+            }
+            const int s = (int)(gi % ST);
+            if (gi >= ST && !mbar_wait_bounded(empty + s, (uint32_t)((gi / ST) - 1) & 1)) {
+              flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+              return;  // the consumers time out on the full barrier and write nothing
+            }
+            stage_ok[s] = (m >= 0 ? (int)mask : 0) | (mn < 0 ? kStageLast : 0);
+            if (m < 0) {
+              mbar_arrive(full + s);  // empty phase: no member reads this block
+            } else {
+              uint8_t* st = smem + s * 2 * TB;
+              mbar_arrive_expect_tx(full + s, 2 * TB);
+              tma_load_4d(st, &tmk, 0, w.kvh * BS, 0, phys, full + s);
+              tma_load_4d(st + TB, &tmv, 0, w.kvh * BS, 0, phys, full + s);
+            }
+            ++gi;
+            m = mn;
+            mask = mask_n;
+            phys = phys_n;
+          } while (m >= 0);
         }
       }
     }
@@ -281,10 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ------------------------------------------------------------------ consumers
   const float c = p.scale * kLog2e;
-  long long gi = 0;  // blocks consumed so far, over all items
+  long long gi = 0;  // stages consumed so far, over all items
   for (long long it = blockIdx.x; it < total; it += gridDim.x) {
     Item w;
     if (!decode_item(it, w)) continue;
+    const uint32_t all = (1u << w.nm) - 1u;
     int rm[2], rn[2];
     bool rvalid[2];
     const uint32_t* qw[2];
@@ -301,18 +340,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const bool warp_active = (16 * warp) / gp < w.nm;
     const bool all_valid = __all_sync(0xffffffffu, rvalid[0] && rvalid[1]);
+    // members whose rows this warp holds
+    const int m_lo = (16 * warp) / gp, m_hi = min((16 * warp + 15) / gp, w.nm - 1);
+    const uint32_t warp_members = warp_active ? (((2u << m_hi) - 1u) & ~((1u << m_lo) - 1u)) : 0u;
     uint32_t qa[G::kKSteps][4];
     load_query_rows<HEAD>(qw[0], qw[1], qa);
     RowState<HEAD> st;
     st.init();
-    for (int i = 0; i < w.nblocks; ++i, ++gi) {
-      const int s = (int)(gi % ST);
+    // the common case: every stage is a whole block read by every member
+    int i = 0;
+    int s = 0, rec = 0;
+    for (; i < w.nblocks; ++i, ++gi) {
+      s = (int)(gi % ST);
       const bool got = mbar_wait_bounded(full + s, (uint32_t)(gi / ST) & 1);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
         return;
       }
-      if (warp_active && stage_ok[s]) {
+      rec = stage_ok[s];
+      if (rec != ((int)all | kStageLast)) break;  // the rest of the item takes the general path
+      if (warp_active) {
         const uint32_t kbase = smem_u32(smem + s * 2 * TB);
         float sc[G::kNTok][4];
         fa2_scores<QDT, HEAD, BS>(kbase, qa, sc);
@@ -327,6 +374,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + s);
+    }
+    // the general path, from the stage waited for above: each stage read by the
+    // members that name its block, a block ending on its last stage
+    while (i < w.nblocks) {
+      const uint32_t readers = (uint32_t)(rec & kStageMembers);
+      if (readers & warp_members) {
+        const bool r0 = rvalid[0] && ((readers >> rm[0]) & 1u);
+        const bool r1 = rvalid[1] && ((readers >> rm[1]) & 1u);
+        const uint32_t kbase = smem_u32(smem + s * 2 * TB);
+        float sc[G::kNTok][4];
+        fa2_scores<QDT, HEAD, BS>(kbase, qa, sc);
+#pragma unroll
+        for (int nt = 0; nt < G::kNTok; ++nt) {
+          if (!r0) sc[nt][0] = sc[nt][1] = -INFINITY;
+          if (!r1) sc[nt][2] = sc[nt][3] = -INFINITY;
+        }
+        fa2_softmax_pv<QDT, HEAD, BS>(kbase + TB, sc, c, BS, st);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
+      ++gi;
+      if (rec & kStageLast) ++i;
+      if (i == w.nblocks) break;
+      s = (int)(gi % ST);
+      const bool got = mbar_wait_bounded(full + s, (uint32_t)(gi / ST) & 1);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+        return;
+      }
+      rec = stage_ok[s];
     }
 
     // ---- each valid row's partial state for shared partition z
@@ -350,39 +427,45 @@ template <int QDT, int HEAD, int BS>
 cudaError_t launch_shared_t(const AttnParams& p, int grid_z, const CUtensorMap* tk, const CUtensorMap* tv,
                             cudaStream_t stream) {
   constexpr int smem = prefill_smem_bytes<HEAD, BS>();
-  auto kern = shared_prefix_tile_kernel<QDT, HEAD, BS>;
-  static int configured_device = -1;
-  static int resident = 0;  // CTAs of this kernel per SM at the block size used
-  static int resident_threads = 0;
+  constexpr auto kern = shared_prefix_tile_kernel<QDT, HEAD, BS>;
+  cudaError_t e = set_smem<kern>(smem);
+  if (e != cudaSuccess) return e;
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) {
-      (void)cudaGetLastError();  // consume it: the caller reports the failure
-      return e;
-    }
-    configured_device = dev;
-    resident_threads = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return cudaErrorInvalidDevice;
   }
   int gp = 1;
   while (gp < (p.group < 8 ? p.group : 8)) gp <<= 1;
   const int nwc = (p.max_group_size * gp + 15) / 16;
   const int threads = (nwc + 1) * 32;
-  if (resident_threads != threads) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess || n < 1) {
+  // Resident CTAs per SM at this block size, cached per device as one word
+  // (threads << 32 | CTAs) so that a host thread never pairs one call's thread count
+  // with another's CTA count.
+  static std::atomic<unsigned long long> occupancy[kMaxDevices] = {};
+  int resident = 0;
+  const bool tracked = dev >= 0 && dev < kMaxDevices;
+  if (tracked) {
+    const unsigned long long w = occupancy[dev].load(std::memory_order_relaxed);
+    if ((int)(w >> 32) == threads) resident = (int)(w & 0xffffffffu);
+  }
+  if (resident < 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kern, threads, smem) != cudaSuccess ||
+        resident < 1) {
       (void)cudaGetLastError();
-      n = 1;
+      resident = 1;
     }
-    resident = n;
-    resident_threads = threads;
+    if (tracked)
+      occupancy[dev].store(((unsigned long long)threads << 32) | (unsigned)resident, std::memory_order_relaxed);
   }
   int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
+    (void)cudaGetLastError();
+    sms = 1;
+  }
   const long long items = (long long)p.num_groups * p.num_kv_heads * p.num_head_groups * grid_z;
+  if (items <= 0) return cudaSuccess;  // no shared partition to attend
   const long long grid = std::min<long long>(items, (long long)resident * sms);
-  if (grid <= 0) return cudaSuccess;
   kern<<<static_cast<unsigned>(grid), threads, smem, stream>>>(p, *tk, *tv, grid_z);
   return cudaGetLastError();
 }

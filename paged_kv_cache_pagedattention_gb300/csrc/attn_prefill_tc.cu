@@ -860,18 +860,9 @@ cudaError_t launch_tc_t(const AttnParams& p, int num_items, int max_ctas, const 
                         const CUtensorMap* tv, cudaStream_t stream) {
   constexpr bool kCvt = is_scaled<KVDT>();
   constexpr int smem = TcGeom<HEAD, BS, kCvt, is_nvfp4<KVDT>()>::kSmem;
-  auto kern = prefill_tc_kernel<QDT, KVDT, HEAD, BS>;
-  static int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) {
-      (void)cudaGetLastError();  // consume it: the caller reports the failure
-      return e;
-    }
-    configured_device = dev;
-  }
+  constexpr auto kern = prefill_tc_kernel<QDT, KVDT, HEAD, BS>;
+  const cudaError_t e = set_smem<kern>(smem);
+  if (e != cudaSuccess) return e;
   const long long tiles = (long long)num_items * p.num_kv_heads * p.num_head_groups;
   const int grid = static_cast<int>(std::min<long long>(tiles, std::max(1, max_ctas)));
   kern<<<grid, threads_tc<kCvt>(), smem, stream>>>(p, *tk, *tv);

@@ -11,9 +11,37 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "pa_internal.h"
 
 namespace pa {
+
+// ---------------------------------------------------------------- host side
+
+constexpr int kMaxDevices = 64;
+
+// Opt kernel kKernel into `smem` bytes of dynamic shared memory on the current
+// device, once per device.  The per-device flags are atomics: host threads may
+// launch at once, and a repeated opt-in only repeats the same call.
+template <auto kKernel>
+cudaError_t set_smem(int smem) {
+  static std::atomic<bool> done[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return cudaErrorInvalidDevice;
+  }
+  const bool tracked = dev >= 0 && dev < kMaxDevices;
+  if (tracked && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kKernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();  // consume it: the caller reports the failure
+    return e;
+  }
+  if (tracked) done[dev].store(true, std::memory_order_release);
+  return cudaSuccess;
+}
 
 // ---------------------------------------------------------------- elements
 
@@ -404,6 +432,55 @@ __device__ __forceinline__ int group_shared_tokens(const AttnParams& p, int g, i
     sb = min(sb, len / p.block_size);
   }
   return sb > 0 ? sb * p.block_size : 0;
+}
+
+// Stages of one declared-shared block.  [AGENTIC] "統一分頁 + 共用池": blocks are
+// shared by reference count and copied on write, so a group's declaration can be
+// stale (a member already holds a private copy of a block) or simply wrong.  Each
+// distinct physical block that the members' entries name for logical block jb gets a
+// stage of its own, read only by the members that name it; in the common case every
+// member names the first member's block and there is one stage.  A stage record holds
+// the reading members in bits 0..7 and kStageLast on the block's last stage.
+constexpr int kStageLast = 0x100;
+constexpr int kStageMembers = 0xff;
+
+constexpr int kMaxShareMembers = 8;
+
+// The members' block-table entries for logical block jb of the group whose nm
+// (<= kMaxShareMembers) members start at sequence s0, loaded together (independent
+// loads, issued back to back); -1 past the last member.
+__device__ __forceinline__ void load_share_entries(const AttnParams& p, int s0, int nm, int jb,
+                                                   int (&e)[kMaxShareMembers]) {
+#pragma unroll
+  for (int m = 0; m < kMaxShareMembers; ++m)
+    e[m] = m < nm ? p.block_tables[(long long)(s0 + m) * p.max_blocks_per_seq + jb] : -1;
+}
+
+// The next stage of a block whose members' entries are `e`: the first member not in
+// `done` whose entry is a physical block in range, with `mask` the members not in
+// `done` that name the same block, and `phys` that block.  Returns that member, or -1
+// when every member is done.  Members met with an entry outside [0, num_blocks) join
+// `done` without a stage and flag PA_ERRFLAG_BLOCK_TABLE (those tokens are skipped, as
+// pa_decode skips them).
+__device__ __forceinline__ int next_share_stage(const AttnParams& p, const int (&e)[kMaxShareMembers], int nm,
+                                                uint32_t& done, uint32_t& mask, int& phys) {
+#pragma unroll
+  for (int m = 0; m < kMaxShareMembers; ++m) {
+    if (m >= nm || ((done >> m) & 1u)) continue;
+    if (e[m] < 0 || e[m] >= p.num_blocks) {
+      flag_error(p.err, PA_ERRFLAG_BLOCK_TABLE);
+      done |= 1u << m;
+      continue;
+    }
+    uint32_t mk = 0;
+#pragma unroll
+    for (int m2 = 0; m2 < kMaxShareMembers; ++m2)
+      if (m2 >= m && m2 < nm && !((done >> m2) & 1u) && e[m2] == e[m]) mk |= 1u << m2;
+    mask = mk;
+    phys = e[m];
+    return m;
+  }
+  return -1;
 }
 
 // Tokens at the start of sequence `seq` processed by the shared-prefix kernel.

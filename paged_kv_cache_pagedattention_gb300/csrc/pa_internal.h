@@ -95,6 +95,14 @@ struct CopyParams {
 
 cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
 
+// pa_decode's argument checks on everything but the workspace (api.cu).
+pa_status check_decode_args(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                            int32_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            const int32_t* seq_lens, int32_t max_seq_len, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_size, int32_t block_size, float scale,
+                            pa_dtype q_dtype, pa_dtype kv_dtype, const float* k_scale, const float* v_scale,
+                            int32_t partition_size);
+
 // Query tokens handled by one CTA of the tcgen05 prefill kernel.
 int prefill_tile_tokens(int group);
 

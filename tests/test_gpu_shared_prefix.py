@@ -84,13 +84,78 @@ def test_groups_larger_than_bound_share_nothing(pa):
     assert torch.equal(out, plain) or (out.double() - plain.double()).abs().max().item() < 1e-2
 
 
-def test_declared_share_that_is_not_shared_is_flagged(pa):
-    b = workloads.build("liar", 23, [200, 200, 64], [1] * 3, 16, 2, 128, 16, "bf16")
+def _unused_blocks(b, n, rng):
+    used = set(int(x) for x in b.block_tables.ravel() if x >= 0)
+    free = np.array([p for p in range(b.num_blocks) if p not in used], np.int64)
+    assert len(free) >= n
+    return [int(x) for x in rng.choice(free, size=n, replace=False)]
+
+
+def _repoint(b, seq, blocks, rng):
+    """Point `seq`'s entries for the given logical blocks at unused physical blocks (a
+    copy-on-write that the group declaration does not know about); the cache there
+    holds other values, so the output changes."""
+    for j, p in zip(blocks, _unused_blocks(b, len(blocks), rng)):
+        b.block_tables[seq, j] = p
+
+
+def _stale_parity(pa, b, starts, shared, partition_size, max_group=8):
+    """Values against the oracle, which reads every sequence's own table; the call sets
+    only the diagnostic bit."""
     db = DeviceBatch(b, DEV)
+    run_scatter(pa, db)
+    out = run_shared(pa, db, starts, shared, max_group, partition_size)
+    torch.cuda.synchronize()
+    assert pa.pa_get_error_flags() == pa.PA_ERRFLAG_SHARED_MISMATCH
+    k_ref, v_ref = oracle_scatter(b)
+    ref = oracle.paged_decode(b.q, b.q_dtype, k_ref, v_ref, b.kv_dtype, b.block_tables, b.seq_lens, b.block_size,
+                              b.scale, b.k_scale, b.v_scale)
+    compare(out, ref, b.kv_dtype, where=b.name)
+    plain = run_decode(pa, db, partition_size)
+    torch.cuda.synchronize()
+    assert (out.double() - plain.double()).abs().max().item() < 1e-2
+
+
+@pytest.mark.parametrize("part", [0, 64])
+def test_stale_and_wrong_share_declarations_bf16(pa, part):
+    """[AGENTIC] "統一分頁 + 共用池": shared blocks are copied on write, so a group's
+    declaration can be stale.  Family 0: one fork copied the last two declared blocks;
+    family 1: one fork copied a block in the middle and another fork the first; family
+    2: one fork shares nothing (every declared entry differs)."""
+    b = workloads.agentic(seed=7, host_cache=True, scale_lengths=1 / 400.0)
+    starts, shared = family_groups(b)
+    rng = np.random.default_rng(5)
+    f0, f1, f2 = b.families[0], b.families[1], b.families[2]
+    _repoint(b, f0[2], [int(shared[0]) - 2, int(shared[0]) - 1], rng)
+    _repoint(b, f1[4], [int(shared[1]) // 2], rng)
+    _repoint(b, f1[1], [0], rng)
+    _repoint(b, f2[3], list(range(int(shared[2]))), rng)
+    _stale_parity(pa, b, starts, shared, part)
+
+
+@pytest.mark.parametrize("kv", ["fp8_e4m3", "nvfp4"])
+def test_stale_share_declarations_scaled_caches(pa, kv):
+    """The member-warp shared-prefix kernel (FP8 and NVFP4 caches) under the same
+    stale and wrong declarations: a group of 3 declaring 5 shared blocks where the
+    last member copied blocks 1 and 4, and a group of 3 whose middle member shares
+    nothing."""
+    lens = [300, 300, 300, 260, 280, 290, 77]
+    shared_map = {1: (0, 5), 2: (0, 5), 4: (3, 5), 5: (3, 5)}
+    b = workloads.build("stale_" + kv, 25, lens, [1] * 7, 32, 8, 128, 32, kv, shared=shared_map)
+    rng = np.random.default_rng(6)
+    _repoint(b, 2, [1, 4], rng)
+    _repoint(b, 4, [0, 1, 2, 3, 4], rng)
+    starts = np.array([0, 3, 6, 7], np.int32)
+    shared = np.array([5, 5, 0], np.int32)
+    _stale_parity(pa, b, starts, shared, 64)
+
+
+def test_declared_share_that_is_not_shared(pa):
+    """Sequences 0 and 1 share nothing in truth but are declared to share 4 blocks."""
+    b = workloads.build("liar", 23, [200, 200, 64], [1] * 3, 16, 2, 128, 16, "bf16")
     starts = np.array([0, 2, 3], np.int32)
-    shared = np.array([4, 0], np.int32)  # sequences 0 and 1 share nothing in truth
-    run_shared(pa, db, starts, shared, 4, 64)
-    assert pa.pa_get_error_flags() & pa.PA_ERRFLAG_BLOCK_TABLE
+    shared = np.array([4, 0], np.int32)
+    _stale_parity(pa, b, starts, shared, 64, max_group=4)
 
 
 @pytest.mark.slow

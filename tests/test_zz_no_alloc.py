@@ -5,7 +5,8 @@ memory planner only provides the tensors it planned, a plug-in that must not cal
 cudaMalloc on the serving path).  This entry point takes inputs and outputs only
 and keeps its split-K scratch in a fixed array inside the library.  These tests
 call it through the C ABI (ctypes, no Python wrapper) and compare its output with
-pa_decode's, which uses a caller-provided workspace, on consecutive calls.
+pa_decode's, which uses a caller-provided workspace, on consecutive calls, and with
+the fp64 oracle.
 """
 
 import ctypes
@@ -16,8 +17,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
-from harness import TOL, TOL_FP8, DeviceBatch, run_decode
+from harness import TOL, TOL_FP8, DeviceBatch, compare, run_decode
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -78,6 +80,60 @@ def test_static_workspace_matches_decode_on_consecutive_calls(lib):
         torch.cuda.synchronize()
         assert pa.pa_get_error_flags() == 0
         _check_close(got, ref, b.kv_dtype)
+        # and with the oracle on the same cache contents (nothing was scattered)
+        expect = oracle.paged_decode(b.q, b.q_dtype, b.k_cache, b.v_cache, b.kv_dtype, b.block_tables,
+                                     b.seq_lens, b.block_size, b.scale, b.k_scale, b.v_scale)
+        compare(got, expect, b.kv_dtype, where=f"static workspace {b.name}")
+
+
+def test_static_workspace_coarsens_the_default_partitioning(lib):
+    """A few short sequences under a large max_seq_len hint with 64 query heads per KV
+    head: the default partitioning needs more partial states than the fixed array
+    holds, so the call doubles the partition size until they fit.  Checked against
+    pa_decode at the partition size the doubling reaches, and against the oracle."""
+    pa, fn = lib
+    b = workloads.build("nz4", 44, [100, 2000, 37, 5000], [1] * 4, 64, 1, 128, 16, "bf16")
+    db = DeviceBatch(b, DEV)
+    hint = 200000
+    cap = 32 << 20
+    need = lambda part: pa.pa_decode_workspace_size(b.num_seqs, 64, 1, 128, hint, 16, part)  # noqa: E731
+    part = pa.pa_default_partition_size(b.num_seqs, 1, hint, 16)
+    assert need(part) > cap  # the coarsening loop runs
+    while part < hint and need(part) > cap:
+        part *= 2
+    assert need(part) <= cap
+    out = torch.full_like(db.q, float("nan"))
+    st = fn(out.data_ptr(), db.q.data_ptr(), db.kc.data_ptr(), db.vc.data_ptr(), b.num_blocks,
+            db.tables.data_ptr(), b.max_blocks_per_seq, db.lens.data_ptr(), b.num_seqs, hint, 64, 1, 128, 16,
+            b.scale, pa.PA_BF16, pa.PA_BF16, None, None, 0, torch.cuda.current_stream().cuda_stream)
+    assert st == pa.PA_OK, pa.pa_status_string(st)
+    ref = torch.empty_like(db.q)
+    ws = pa.workspace_tensor(need(part), DEV)
+    pa.pa_decode(ref, db.q, db.kc, db.vc, db.tables, db.lens, hint, b.scale, ws, None, None, part)
+    torch.cuda.synchronize()
+    assert pa.pa_get_error_flags() == 0
+    _check_close(out, ref, b.kv_dtype)
+    expect = oracle.paged_decode(b.q, b.q_dtype, b.k_cache, b.v_cache, b.kv_dtype, b.block_tables, b.seq_lens,
+                                 b.block_size, b.scale)
+    compare(out, expect, b.kv_dtype, where="static workspace, coarsened")
+
+
+def test_static_workspace_reports_invalid_arguments_first(lib):
+    """Invalid arguments on a problem too large for the array give the argument error
+    (as pa_decode does), not PA_ERR_WORKSPACE."""
+    pa, fn = lib
+    b = workloads.build("nz5", 45, [40], [1], 8, 2, 128, 16, "bf16")
+    db = DeviceBatch(b, DEV)
+    s = torch.cuda.current_stream().cuda_stream
+    args = lambda hq, hkv, part: (db.q.data_ptr(), db.q.data_ptr(), db.kc.data_ptr(), db.vc.data_ptr(),  # noqa
+                                  b.num_blocks, db.tables.data_ptr(), b.max_blocks_per_seq, db.lens.data_ptr(),
+                                  4096, 100000, hq, hkv, 128, 16, b.scale, pa.PA_BF16, pa.PA_BF16, None, None,
+                                  part, s)
+    assert fn(*args(63, 8, 16)) == pa.PA_ERR_INVALID_ARG  # query heads not a multiple of KV heads
+    assert fn(*args(64, 8, 24)) == pa.PA_ERR_INVALID_ARG  # partition not a multiple of the block
+    assert fn(*args(64, 8, 16)) == pa.PA_ERR_WORKSPACE    # valid, but too large for the array
+    torch.cuda.synchronize()
+    assert pa.pa_get_error_flags() == 0
 
 
 def test_static_workspace_rejects_problems_beyond_its_size(lib):
