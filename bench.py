@@ -585,8 +585,9 @@ def capture(run):
     return graph.replay
 
 
-def roofline_of(b, runner, trace, ms_per_step, args, window=0):
-    """Roofline of the dominant kernel (or fork-join span) of one measured workload."""
+def roofline_of(b, runner, trace, ms_per_step, wl, window=0):
+    """Roofline of the dominant kernel (or fork-join span) of one measured workload
+    (`wl`: its workload key, which names its ncu summary under profiles/)."""
     import workloads
 
     nbytes = algorithmic_bytes(b, window)
@@ -603,7 +604,7 @@ def roofline_of(b, runner, trace, ms_per_step, args, window=0):
         achieved = nbytes["algorithmic"] / (span_ms / 1000.0) / 1e9 if span_ms else 0.0
         logical_gbs = nbytes["logical_total"] / (span_ms / 1000.0) / 1e9 if span_ms else 0.0
         return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profiled_traffic(args.workload, "shared_prefix_span"),
+                "traffic": profiled_traffic(wl, "shared_prefix_span"),
                 "kernel": "shared_prefix_tile_kernel || decode_mma_kernel (one fork-join span)",
                 "peak_source": src, "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
                 "byte_basis": "unique physical bytes: each shared prefix block counted once (the "
@@ -632,7 +633,7 @@ def roofline_of(b, runner, trace, ms_per_step, args, window=0):
                 "logical_gbs": nbytes["logical_total"] / (att_ms / 1000.0) / 1e9,
                 "kernel_ms": att_ms, "merge_ms": kernel_ms.get("merge", 0.0),
                 "scatter_ms": kernel_ms.get("reshape_and_cache", 0.0)}
-        prof = "agentic_pa_decode" if shared_blocks else args.workload
+        prof = wl + "_pa_decode" if shared_blocks else wl
         line["traffic"] = profiled_traffic(prof)
         return line
     # varlen: the single-token rows (HBM-bound decode kernel) and the multi-token rows
@@ -652,7 +653,7 @@ def roofline_of(b, runner, trace, ms_per_step, args, window=0):
     # per step: the prefill tiles launch twice when decode rows run beside them
     n_span = max(trace["varlen_span"][0], 1)
     overlapped = {"decode_mma_kernel": att_ms, "prefill_tc_kernel": trace["prefill_tiles"][1] / n_span}
-    traffic = profiled_traffic(args.workload, "varlen_span")
+    traffic = profiled_traffic(wl, "varlen_span")
     hbm_line = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic, "kernel": kernel_name, "peak_source": src,
                 "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
@@ -755,7 +756,7 @@ def e2e_pipelined(runner, steps, stream, barrier, dev, use_graph):
     return line
 
 
-def measure(pa, b, d, dev, mode, args, stream, barrier, steps, warmup, min_total_ms, window=0, e2e=False):
+def measure(pa, b, d, dev, mode, args, wl, stream, barrier, steps, warmup, min_total_ms, window=0, e2e=False):
     """Warm-up, one traced eager K-step region, then repeated graph-replayed K-step
     regions (eager with --no-graph); the roofline of the dominant kernel."""
     runner = Runner(pa, b, d, dev, mode, args.partition_size, window)
@@ -777,7 +778,7 @@ def measure(pa, b, d, dev, mode, args, stream, barrier, steps, warmup, min_total
            "repeats": len(per_step), "ms_per_step_min": min(per_step), "ms_per_step_max": max(per_step),
            "step_launch": "eager" if args.no_graph else "cuda_graph_replay",
            "launches": sum(n for name, (n, _) in trace.items() if not name.endswith("_span"))}
-    res["roofline"] = roofline_of(b, runner, trace, ms, args, window)
+    res["roofline"] = roofline_of(b, runner, trace, ms, wl, window)
     if e2e:
         res["e2e"] = e2e_pipelined(runner, steps, stream, barrier, dev, not args.no_graph)
     flags = pa.pa_get_error_flags()
@@ -850,7 +851,7 @@ def run_ours(args):
     sampler = ClockSampler(bus) if rank == 0 else None
     if sampler:
         sampler.start()
-    head = measure(pa, b, d, dev, mode, args, stream, barrier, args.steps, args.warmup, args.min_timed_ms,
+    head = measure(pa, b, d, dev, mode, args, args.workload, stream, barrier, args.steps, args.warmup, args.min_timed_ms,
                    window=args.window, e2e=not args.no_e2e)
     clocks = sampler.stop() if sampler else None
     ms_per_step = head["ms_per_step"]
@@ -874,7 +875,7 @@ def run_ours(args):
             # the headline's batch is reused; any other workload's tensors are freed after its leg
             bb = b if wl == args.workload else make_workload(wl, BASE_SEEDS[wl])
             dd = d if wl == args.workload else device_inputs(bb, dev)
-            res = measure(pa, bb, dd, dev, leg_mode, args, stream, barrier, args.steps, args.warmup,
+            res = measure(pa, bb, dd, dev, leg_mode, args, wl, stream, barrier, args.steps, args.warmup,
                           args.min_timed_ms / 4)
             configs[name] = compact(res, bb)
             del res, dd

@@ -220,10 +220,20 @@ def _sampled_full_size(pa, b, seqs):
     return compare(outs[0], ref, b.kv_dtype, rows=seqs, where=b.name)
 
 
+def _spread_by_length(b, n):
+    """n sequences spread evenly over the batch's length ranks, the shortest and the
+    longest included."""
+    order = np.argsort(b.seq_lens, kind="stable")
+    picks = np.unique(np.round(np.linspace(0, len(order) - 1, n)).astype(int))
+    return sorted(int(order[i]) for i in picks)
+
+
 @pytest.mark.slow
-def test_llama_full_size_sampled(pa):
+def test_llama_full_size_every_row(pa):
+    """Every one of the 64 sequences of the full-size Llama-shaped batch, with the
+    default partitioning the bench uses, against the oracle."""
     b = workloads.llama()
-    _sampled_full_size(pa, b, [0, 17, 63])
+    _sampled_full_size(pa, b, list(range(b.num_seqs)))
 
 
 @pytest.mark.slow
@@ -235,8 +245,13 @@ def test_agentic_full_size_sampled(pa):
 
 @pytest.mark.slow
 def test_fp8_full_size_sampled(pa):
+    """16 of the 256 sequences of the full-size FP8 batch, spread over the length range
+    from the shortest to the longest."""
     b = workloads.fp8()
-    _sampled_full_size(pa, b, [0, 100, 255])
+    seqs = _spread_by_length(b, 16)
+    lens = b.seq_lens[seqs]
+    assert len(seqs) == 16 and lens.min() == b.seq_lens.min() and lens.max() == b.seq_lens.max()
+    _sampled_full_size(pa, b, seqs)
 
 
 @pytest.mark.slow
