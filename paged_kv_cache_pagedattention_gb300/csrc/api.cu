@@ -196,7 +196,18 @@ struct SharedLayout {
 SharedLayout shared_layout(int num_seqs, int num_groups, int hq, int hkv, int d, int max_seq_len, int bs,
                            int requested) {
   SharedLayout L;
-  L.part = resolve_partition(requested, num_seqs, hkv, max_seq_len, bs);
+  // The private remainders: in a batch of forks most are short, so the private grid's
+  // real CTAs are far fewer than sequences x KV heads x partitions, and a sequence with
+  // a long private range (one that shares nothing) is streamed by few long CTAs, each
+  // bound by its own copies in flight.  Partitions of at most 2048 tokens give such a
+  // sequence twice the CTAs of the plain decode's 4096-token cap (agentic forks + one
+  // lone parent: span 0.3681 -> 0.3626 ms; with the earlier tile producer 1024 / 512
+  // tokens measured 0.380 / 0.440 ms against 0.364 for 2048: the short remainders'
+  // empty CTAs then dominate).
+  L.part = requested > 0 ? requested
+                         : resolve_partition(std::min(default_partition(num_seqs, hkv, max_seq_len, bs),
+                                                      round_up(2048, bs)),
+                                             num_seqs, hkv, max_seq_len, bs);
   // The shared-prefix tiles carry a whole group per CTA: ~8 partitions' worth of work
   // items per SM (the persistent tile kernel takes them in turn), and coarser
   // partitions halve the shared partials the merge reads (measured on the agentic

@@ -250,68 +250,97 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == nwc) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      long long gi = 0;  // stages issued so far, over all items
-      for (long long it = blockIdx.x; it < total; it += gridDim.x) {
-        Item w;
-        if (!decode_item(it, w)) continue;
-        const uint32_t all = (1u << w.nm) - 1u;
-        for (int i = 0; i < w.nblocks; ++i) {
-          const int jb = w.b0 + i;
-          // the common case, checked first: every member names the first member's block
-          const int lead = p.block_tables[(long long)w.s0 * p.max_blocks_per_seq + jb];
-          bool same = lead >= 0 && lead < p.num_blocks;
-          for (int m = 1; m < w.nm; ++m)
-            same &= p.block_tables[(long long)(w.s0 + m) * p.max_blocks_per_seq + jb] == lead;
-          if (same) {
+    // The whole warp reads the block-table entries, a window of 32 blocks at a time
+    // (lane j: block base + j, every member's entry, loads issued together), one window
+    // ahead; lane 0 issues the copies.  The members' entries must name the first
+    // member's block (checked per window); a block where they do not takes the
+    // per-member path (next_share_stage) on lane 0.
+    long long gi = 0;  // stages issued so far, over all items
+    // entries of one window: the first member's block, and whether every member names it
+    auto window = [&](const Item& w, int base, int& lead, bool& same) {
+      const int jb = w.b0 + base + lane;
+      lead = -1;
+      same = false;
+      if (base + lane < w.nblocks) {
+        int e[kMaxShareMembers];
+        load_share_entries(p, w.s0, w.nm, jb, e);
+        lead = e[0];
+        same = lead >= 0 && lead < p.num_blocks;
+#pragma unroll
+        for (int m = 1; m < kMaxShareMembers; ++m) same &= m >= w.nm || e[m] == lead;
+      }
+    };
+    for (long long it = blockIdx.x; it < total; it += gridDim.x) {
+      Item w;
+      if (!decode_item(it, w)) continue;
+      const uint32_t all = (1u << w.nm) - 1u;
+      int lead_cur, lead_next;
+      bool same_cur, same_next;
+      window(w, 0, lead_cur, same_cur);
+      window(w, 32, lead_next, same_next);
+      for (int i = 0; i < w.nblocks; ++i) {
+        if (i > 0 && (i & 31) == 0) {
+          lead_cur = lead_next;
+          same_cur = same_next;
+          window(w, i + 32, lead_next, same_next);
+        }
+        const int lead = __shfl_sync(0xffffffffu, lead_cur, i & 31);
+        const bool same = __shfl_sync(0xffffffffu, same_cur ? 1 : 0, i & 31) != 0;
+        int stop = 0;
+        if (lane == 0) {
+          if (same) {  // the common case: one stage, every member
             const int s = (int)(gi % ST);
             if (gi >= ST && !mbar_wait_bounded(empty + s, (uint32_t)((gi / ST) - 1) & 1)) {
               flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-              return;  // the consumers time out on the full barrier and write nothing
-            }
-            stage_ok[s] = (int)all | kStageLast;
-            uint8_t* st = smem + s * 2 * TB;
-            mbar_arrive_expect_tx(full + s, 2 * TB);
-            tma_load_4d(st, &tmk, 0, w.kvh * BS, 0, lead, full + s);
-            tma_load_4d(st + TB, &tmv, 0, w.kvh * BS, 0, lead, full + s);
-            ++gi;
-            continue;
-          }
-          // otherwise one stage per distinct physical block the members name, and an
-          // empty last stage when none is in range
-          int e[kMaxShareMembers];
-          load_share_entries(p, w.s0, w.nm, jb, e);
-          uint32_t done = 0, mask = 0;
-          int phys = 0;
-          int m = next_share_stage(p, e, w.nm, done, mask, phys);
-          if (m >= 0 && mask != all) flag_error(p.err, PA_ERRFLAG_SHARED_MISMATCH);
-          do {
-            uint32_t mask_n = 0;
-            int phys_n = 0, mn = -1;
-            if (m >= 0) {
-              done |= mask;
-              mn = next_share_stage(p, e, w.nm, done, mask_n, phys_n);
-            }
-            const int s = (int)(gi % ST);
-            if (gi >= ST && !mbar_wait_bounded(empty + s, (uint32_t)((gi / ST) - 1) & 1)) {
-              flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-              return;  // the consumers time out on the full barrier and write nothing
-            }
-            stage_ok[s] = (m >= 0 ? (int)mask : 0) | (mn < 0 ? kStageLast : 0);
-            if (m < 0) {
-              mbar_arrive(full + s);  // empty phase: no member reads this block
+              stop = 1;  // the consumers time out on the full barrier and write nothing
             } else {
+              stage_ok[s] = (int)all | kStageLast;
               uint8_t* st = smem + s * 2 * TB;
               mbar_arrive_expect_tx(full + s, 2 * TB);
-              tma_load_4d(st, &tmk, 0, w.kvh * BS, 0, phys, full + s);
-              tma_load_4d(st + TB, &tmv, 0, w.kvh * BS, 0, phys, full + s);
+              tma_load_4d(st, &tmk, 0, w.kvh * BS, 0, lead, full + s);
+              tma_load_4d(st + TB, &tmv, 0, w.kvh * BS, 0, lead, full + s);
+              ++gi;
             }
-            ++gi;
-            m = mn;
-            mask = mask_n;
-            phys = phys_n;
-          } while (m >= 0);
+          } else {
+            // one stage per distinct physical block the members name, and an empty
+            // last stage when none is in range
+            const int jb = w.b0 + i;
+            int e[kMaxShareMembers];
+            load_share_entries(p, w.s0, w.nm, jb, e);
+            uint32_t done = 0, mask = 0;
+            int phys = 0;
+            int m = next_share_stage(p, e, w.nm, done, mask, phys);
+            if (m >= 0 && mask != all) flag_error(p.err, PA_ERRFLAG_SHARED_MISMATCH);
+            do {
+              uint32_t mask_n = 0;
+              int phys_n = 0, mn = -1;
+              if (m >= 0) {
+                done |= mask;
+                mn = next_share_stage(p, e, w.nm, done, mask_n, phys_n);
+              }
+              const int s = (int)(gi % ST);
+              if (gi >= ST && !mbar_wait_bounded(empty + s, (uint32_t)((gi / ST) - 1) & 1)) {
+                flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+                stop = 1;
+                break;
+              }
+              stage_ok[s] = (m >= 0 ? (int)mask : 0) | (mn < 0 ? kStageLast : 0);
+              if (m < 0) {
+                mbar_arrive(full + s);  // empty phase: no member reads this block
+              } else {
+                uint8_t* st = smem + s * 2 * TB;
+                mbar_arrive_expect_tx(full + s, 2 * TB);
+                tma_load_4d(st, &tmk, 0, w.kvh * BS, 0, phys, full + s);
+                tma_load_4d(st + TB, &tmv, 0, w.kvh * BS, 0, phys, full + s);
+              }
+              ++gi;
+              m = mn;
+              mask = mask_n;
+              phys = phys_n;
+            } while (m >= 0);
+          }
         }
+        if (__shfl_sync(0xffffffffu, stop, 0)) return;
       }
     }
     return;

@@ -428,7 +428,10 @@ __device__ __forceinline__ int group_shared_tokens(const AttnParams& p, int g, i
   int sb = p.group_shared_blocks[g];
   for (int m = s0; m < s1; ++m) {
     const int len = p.seq_lens[m];
-    if (len < 1 || len > p.max_seq_len) return 0;
+    // an out-of-range length (flagged by the decode kernel) shares nothing, so no table
+    // entry past the row is ever read
+    if (len < 1 || len > p.max_seq_len || (long long)len > (long long)p.max_blocks_per_seq * p.block_size)
+      return 0;
     sb = min(sb, len / p.block_size);
   }
   return sb > 0 ? sb * p.block_size : 0;
