@@ -520,9 +520,14 @@ __global__ void __launch_bounds__(1024)
       if (rp.full_tiles + rp.last_tiles) {
         int kf = ex[1], kl = full_total + ex[2];
         const int row0 = p.query_start_loc[r];
-        for (int t0 = 0; t0 < rp.q_len; t0 += tile_tokens) {
-          const int np = tile_partitions(p, rp, t0, tile_tokens);
-          for (int z = 0; z < np; ++z) {
+        // partition-major: the row tiles that read one partition are listed (and so
+        // claimed) one after another, and read its K/V from L2 while it is there
+        const int last_t0 = (rp.q_len - 1) / tile_tokens * tile_tokens;
+        const int np_max = tile_partitions(p, rp, last_t0, tile_tokens);  // the most any row tile has
+        for (int z = 0; z < np_max; ++z) {
+          for (int t0 = 0; t0 < rp.q_len; t0 += tile_tokens) {
+            const int np = tile_partitions(p, rp, t0, tile_tokens);
+            if (z >= np) continue;
             const int k = z + 1 < np ? kf++ : kl++;
             if (k < max_work) work[k] = make_int4(r, row0 + t0, z, 0);
           }
