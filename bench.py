@@ -796,7 +796,8 @@ def torch_sync(dev):
 # The other configurations of the path, measured in the same run as the headline:
 # (entry name, workload, attention call).
 CONFIG_LEGS = (("tiny", "tiny", "decode"), ("llama", "llama", "decode"), ("mixed", "mixed", "varlen"),
-               ("fp8", "fp8", "decode"), ("agentic_pa_decode", "agentic", "decode"))
+               ("fp8", "fp8", "decode"), ("agentic_pa_decode", "agentic", "decode"),
+               ("mixed_fp8", "mixed_fp8", "varlen"), ("nvfp4", "nvfp4", "decode"))
 
 
 def compact(res, b, window=0) -> dict:
