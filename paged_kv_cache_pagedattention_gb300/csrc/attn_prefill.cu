@@ -154,6 +154,77 @@ __device__ __forceinline__ void fa2_softmax_pv(uint32_t vbase, float (&sc)[BS / 
   }
 }
 
+// Softmax and O += P V for two whole blocks at once (every token valid): one running-
+// max update for the 2 x block_size scores, then both blocks' PV products.  Twice the
+// independent MMA and exp2 work per step for the scheduler to interleave.
+template <int QDT, int HEAD, int BS>
+__device__ __forceinline__ void fa2_softmax_pv2(uint32_t vbase0, uint32_t vbase1, float (&sc)[2][BS / 8][4],
+                                                float c, RowState<HEAD>& st) {
+  using G = PrefillGeom<HEAD, BS>;
+  const int lane = threadIdx.x & 31;
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int b = 0; b < 2; ++b)
+#pragma unroll
+    for (int nt = 0; nt < G::kNTok; ++nt) {
+      mx[0] = fmaxf(mx[0], fmaxf(sc[b][nt][0], sc[b][nt][1]));
+      mx[1] = fmaxf(mx[1], fmaxf(sc[b][nt][2], sc[b][nt][3]));
+    }
+  mx[0] = warp_max_xor(mx[0], 1, 2) * c;
+  mx[1] = warp_max_xor(mx[1], 1, 2) * c;
+  if (__any_sync(0xffffffffu, mx[0] > st.m[0] + kRescaleSlack || mx[1] > st.m[1] + kRescaleSlack)) {
+    float al[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float nm = fmaxf(st.m[h], mx[h]);
+      al[h] = nm == -INFINITY ? 1.f : ex2_approx(st.m[h] - nm);
+      st.m[h] = nm;
+      st.l[h] *= al[h];
+    }
+#pragma unroll
+    for (int dn = 0; dn < G::kNDim; ++dn) {
+      st.acc[dn][0] *= al[0];
+      st.acc[dn][1] *= al[0];
+      st.acc[dn][2] *= al[1];
+      st.acc[dn][3] *= al[1];
+    }
+  }
+  const float u0 = st.m[0] == -INFINITY ? 0.f : st.m[0], u1 = st.m[1] == -INFINITY ? 0.f : st.m[1];
+  uint32_t pa[2][G::kNTok][2];
+  float add0 = 0.f, add1 = 0.f;
+#pragma unroll
+  for (int b = 0; b < 2; ++b)
+#pragma unroll
+    for (int nt = 0; nt < G::kNTok; ++nt) {
+      pa[b][nt][0] = pack2<QDT>(ex2_approx(fmaf(sc[b][nt][0], c, -u0)), ex2_approx(fmaf(sc[b][nt][1], c, -u0)));
+      pa[b][nt][1] = pack2<QDT>(ex2_approx(fmaf(sc[b][nt][2], c, -u1)), ex2_approx(fmaf(sc[b][nt][3], c, -u1)));
+      const float2 f0 = unpack2<QDT>(pa[b][nt][0]), f1 = unpack2<QDT>(pa[b][nt][1]);
+      add0 += f0.x + f0.y;
+      add1 += f1.x + f1.y;
+    }
+  st.l[0] += add0;
+  st.l[1] += add1;
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    const uint32_t vbase = b ? vbase1 : vbase0;
+#pragma unroll
+    for (int kt = 0; kt < BS / 16; ++kt) {
+#pragma unroll
+      for (int dp = 0; dp < G::kNDim / 2; ++dp) {
+        const int mi = lane >> 3;
+        const int tok = 16 * kt + (lane & 7) + 8 * (mi & 1);
+        const int chunk = 2 * dp + (mi >> 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_trans(vbase + G::off(tok, chunk), b0, b1, b2, b3);
+        mma_16816<QDT>(st.acc[2 * dp], pa[b][2 * kt][0], pa[b][2 * kt][1], pa[b][2 * kt + 1][0],
+                       pa[b][2 * kt + 1][1], b0, b1);
+        mma_16816<QDT>(st.acc[2 * dp + 1], pa[b][2 * kt][0], pa[b][2 * kt][1], pa[b][2 * kt + 1][0],
+                       pa[b][2 * kt + 1][1], b2, b3);
+      }
+    }
+  }
+}
+
 // A-operand fragments of two query rows (zero when the row pointer is null).
 template <int HEAD>
 __device__ __forceinline__ void load_query_rows(const uint32_t* q0, const uint32_t* q1, uint32_t (&qa)[HEAD / 16][4]) {
@@ -376,33 +447,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     load_query_rows<HEAD>(qw[0], qw[1], qa);
     RowState<HEAD> st;
     st.init();
-    // the common case: every stage is a whole block read by every member
+    // the common case: every stage is a whole block read by every member, taken two
+    // blocks at a time (one block when the item has one left, or when the next
+    // stage is not such a block)
+    const int fast = (int)all | kStageLast;
     int i = 0;
     int s = 0, rec = 0;
-    for (; i < w.nblocks; ++i, ++gi) {
-      s = (int)(gi % ST);
-      const bool got = mbar_wait_bounded(full + s, (uint32_t)(gi / ST) & 1);
-      if (!__all_sync(0xffffffffu, got)) {
-        if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
-        return;
+    bool have = false;  // stage s of block i waited for and rec read already
+    while (i < w.nblocks) {
+      if (!have) {
+        s = (int)(gi % ST);
+        const bool got = mbar_wait_bounded(full + s, (uint32_t)(gi / ST) & 1);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+          return;
+        }
+        rec = stage_ok[s];
       }
-      rec = stage_ok[s];
-      if (rec != ((int)all | kStageLast)) break;  // the rest of the item takes the general path
+      have = true;
+      if (rec != fast) break;  // the rest of the item takes the general path
+      int s1 = -1, rec1 = 0;
+      if (i + 1 < w.nblocks) {
+        s1 = (int)((gi + 1) % ST);
+        const bool got = mbar_wait_bounded(full + s1, (uint32_t)((gi + 1) / ST) & 1);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) flag_error(p.err, PA_ERRFLAG_TIMEOUT);
+          return;
+        }
+        rec1 = stage_ok[s1];
+      }
+      const bool two = s1 >= 0 && rec1 == fast;
       if (warp_active) {
         const uint32_t kbase = smem_u32(smem + s * 2 * TB);
-        float sc[G::kNTok][4];
-        fa2_scores<QDT, HEAD, BS>(kbase, qa, sc);
-        if (!all_valid) {  // padding rows (no member / head) take no part
+        if (two) {
+          const uint32_t kbase1 = smem_u32(smem + s1 * 2 * TB);
+          float sc[2][G::kNTok][4];
+          fa2_scores<QDT, HEAD, BS>(kbase, qa, sc[0]);
+          fa2_scores<QDT, HEAD, BS>(kbase1, qa, sc[1]);
+          if (!all_valid) {  // padding rows (no member / head) take no part
 #pragma unroll
-          for (int nt = 0; nt < G::kNTok; ++nt) {
-            if (!rvalid[0]) sc[nt][0] = sc[nt][1] = -INFINITY;
-            if (!rvalid[1]) sc[nt][2] = sc[nt][3] = -INFINITY;
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+              for (int nt = 0; nt < G::kNTok; ++nt) {
+                if (!rvalid[0]) sc[b][nt][0] = sc[b][nt][1] = -INFINITY;
+                if (!rvalid[1]) sc[b][nt][2] = sc[b][nt][3] = -INFINITY;
+              }
           }
+          fa2_softmax_pv2<QDT, HEAD, BS>(kbase + TB, kbase1 + TB, sc, c, st);
+        } else {
+          float sc[G::kNTok][4];
+          fa2_scores<QDT, HEAD, BS>(kbase, qa, sc);
+          if (!all_valid) {
+#pragma unroll
+            for (int nt = 0; nt < G::kNTok; ++nt) {
+              if (!rvalid[0]) sc[nt][0] = sc[nt][1] = -INFINITY;
+              if (!rvalid[1]) sc[nt][2] = sc[nt][3] = -INFINITY;
+            }
+          }
+          fa2_softmax_pv<QDT, HEAD, BS>(kbase + TB, sc, c, BS, st);
         }
-        fa2_softmax_pv<QDT, HEAD, BS>(kbase + TB, sc, c, BS, st);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty + s);
+      if (lane == 0) {
+        mbar_arrive(empty + s);
+        if (two) mbar_arrive(empty + s1);
+      }
+      if (two) {
+        i += 2;
+        gi += 2;
+        have = false;
+      } else {
+        i += 1;
+        gi += 1;
+        have = s1 >= 0;  // the next block's stage was waited for above
+        s = s1;
+        rec = rec1;
+      }
     }
     // the general path, from the stage waited for above: each stage read by the
     // members that name its block, a block ending on its last stage
