@@ -233,6 +233,46 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnParams p
   const long long base = row_partial_base(p, ri, row);
   const int hq = p.num_q_heads, d = p.head_size;
   const float2* ml = p.ws_ml + base * hq + head;  // partial j at ml[j * hq]
+  if (np <= 8 && (d & 3) == 0 && d <= 128) {
+    // A few partials: every load (each lane's four dimensions of every partial, and
+    // every partial's max and sum, the same for all lanes) issued at once, one trip
+    // to memory; each lane combines the maxima itself.
+    const int nv = d >> 2;
+    const float4* acc4 = reinterpret_cast<const float4*>(p.ws_acc + (base * hq + head) * d);
+    const long long stride4 = (long long)hq * nv;
+    float2 v[8];
+    float4 a[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      v[u] = make_float2(-INFINITY, 0.f);
+      a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (u < np) {
+        v[u] = ml[(long long)u * hq];
+        if (lane < nv) a[u] = acc4[u * stride4 + lane];
+      }
+    }
+    float M = -INFINITY, L = 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) combine_ml(M, L, v[u].x, v[u].y);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float w = v[u].y > 0.f ? exp2f(v[u].x - M) : 0.f;
+      o.x = fmaf(a[u].x, w, o.x);
+      o.y = fmaf(a[u].y, w, o.y);
+      o.z = fmaf(a[u].z, w, o.z);
+      o.w = fmaf(a[u].w, w, o.w);
+    }
+    if (lane < nv) {
+      typename QE::T* out = reinterpret_cast<typename QE::T*>(p.out) + ((long long)row * hq + head) * d;
+      out[4 * lane + 0] = QE::from_float(o.x * inv);
+      out[4 * lane + 1] = QE::from_float(o.y * inv);
+      out[4 * lane + 2] = QE::from_float(o.z * inv);
+      out[4 * lane + 3] = QE::from_float(o.w * inv);
+    }
+    return;
+  }
   float M = -INFINITY, L = 0.f;
   for (int j = lane; j < np; j += 32) {
     const float2 v = ml[(long long)j * hq];
