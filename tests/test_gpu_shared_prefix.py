@@ -198,3 +198,21 @@ def test_many_groups_more_items_than_ctas(pa, part):
         shared.append(nsh if size > 1 else 0)
     b = workloads.build("many_groups", 79, lens, [1] * len(lens), 16, 4, 128, 16, "bf16", shared=shared_map)
     _parity(pa, b, np.array(starts, np.int32), np.array(shared, np.int32), part, max_group=4)
+
+
+@pytest.mark.parametrize("offsets", [[1], [2], [0, 1], [3, 4], [6, 7], [5]], ids=lambda o: "at_" + "_".join(map(str, o)))
+def test_stale_block_at_each_position_of_a_block_pair(pa, offsets):
+    """The bf16 tiles take whole shared blocks two at a time; a block a member copied
+    on write (read as stages of its own) can fall first or second in a pair, or end
+    an item of odd length.  Groups of 3 over 8-block partitions (128 tokens), the
+    stale blocks at the given offsets of each partition of the last member."""
+    lens = [600, 600, 600, 555]
+    shared_map = {1: (0, 35), 2: (0, 35)}  # 35 blocks: the last partition holds 3
+    b = workloads.build("pair_" + "_".join(map(str, offsets)), 31, lens, [1] * 4, 16, 2, 128, 16, "bf16",
+                        shared=shared_map)
+    rng = np.random.default_rng(7)
+    stale = [8 * z + o for z in range(35 // 8 + 1) for o in offsets if 8 * z + o < 35]
+    _repoint(b, 2, stale, rng)
+    starts = np.array([0, 3, 4], np.int32)
+    shared = np.array([35, 0], np.int32)
+    _stale_parity(pa, b, starts, shared, 128)
