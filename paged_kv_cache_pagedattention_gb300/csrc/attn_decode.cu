@@ -71,8 +71,9 @@ struct DecodeGeom {
   // HBM: three stages keep four CTAs (16 warps) per SM within shared memory and the
   // 128-register cap; measured 1.065 -> 0.994 ms on the NVFP4 decode workload.
   // 16-bit tiles: two stages (3 CTAs per SM instead of 2): Llama decode 95.9 -> 92.8
-  // us, agentic span 0.384 -> 0.373 ms; FP8 keeps three.
-  static constexpr int kStages = kFp4 ? 3 : kTileBytes <= 4096 ? (kFp8 ? 3 : 2) : 2;
+  // us, agentic span 0.384 -> 0.373 ms; FP8 keeps three, four for 2 KB tiles (block 16:
+  // the CTA stays at 48 -> 64 KB, three per SM; FP8 mixed step 1.468 -> 1.454 ms).
+  static constexpr int kStages = kFp4 ? 3 : kTileBytes <= 4096 ? (kFp8 ? (kTileBytes <= 2048 ? 4 : 3) : 2) : 2;
   static constexpr int kSharedStages = kTileBytes <= 4096 ? 6 : 4;       // CTA ring (shared prefix)
   static_assert(kFp4 ? HEAD == 128 : kRowBytes % 128 == 0, "token rows must be whole 128-byte rows");
   static_assert(kTileBytes % 16 == 0, "tiles are whole 16-byte pieces");
