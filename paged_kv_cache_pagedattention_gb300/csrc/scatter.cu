@@ -25,6 +25,10 @@ __global__ void __launch_bounds__(256) scatter_copy_kernel(const ScatterParams p
     const long long t = u / per_token;
     const int rem = static_cast<int>(u - t * per_token);
     const int h = rem / pieces, c = rem % pieces;
+    // the source pieces do not depend on the slot: their loads go out with the slot's
+    const long long src = (t * p.num_kv_heads + h) * pieces + c;
+    const uint4 kv = reinterpret_cast<const uint4*>(p.key)[src];
+    const uint4 vv = reinterpret_cast<const uint4*>(p.value)[src];
     const long long slot = p.slot_mapping[t];
     if (slot < 0) continue;
     if (slot >= limit) {
@@ -32,10 +36,7 @@ __global__ void __launch_bounds__(256) scatter_copy_kernel(const ScatterParams p
       continue;
     }
     const long long blk = slot / p.block_size, off = slot % p.block_size;
-    const long long src = (t * p.num_kv_heads + h) * pieces + c;
     const long long dst = ((blk * p.num_kv_heads + h) * p.block_size + off) * pieces + c;
-    const uint4 kv = reinterpret_cast<const uint4*>(p.key)[src];
-    const uint4 vv = reinterpret_cast<const uint4*>(p.value)[src];
     reinterpret_cast<uint4*>(p.k_cache)[dst] = kv;
     reinterpret_cast<uint4*>(p.v_cache)[dst] = vv;
   }
@@ -62,16 +63,10 @@ __global__ void __launch_bounds__(256) scatter_fp8_kernel(const ScatterParams p)
     const long long t = u / per_token;
     const int rem = static_cast<int>(u - t * per_token);
     const int h = rem / pieces, c = rem % pieces;
+    // the codes do not depend on the slot: their loads go out with the slot's
     const long long slot = p.slot_mapping[t];
-    if (slot < 0) continue;
-    if (slot >= limit) {
-      flag_error(p.err, PA_ERRFLAG_SLOT);
-      continue;
-    }
     const float ks = p.k_scale[h * p.scale_stride], vs = p.v_scale[h * p.scale_stride];
-    const long long blk = slot / p.block_size, off = slot % p.block_size;
     const long long src = ((t * p.num_kv_heads + h) * p.head_size) + c * 16;
-    const long long dst = ((blk * p.num_kv_heads + h) * p.block_size + off) * p.head_size + c * 16;
     const typename SE::T* ksrc = reinterpret_cast<const typename SE::T*>(p.key) + src;
     const typename SE::T* vsrc = reinterpret_cast<const typename SE::T*>(p.value) + src;
     uint32_t kw[4], vw[4];
@@ -86,6 +81,13 @@ __global__ void __launch_bounds__(256) scatter_fp8_kernel(const ScatterParams p)
       kw[w] = kb;
       vw[w] = vb;
     }
+    if (slot < 0) continue;
+    if (slot >= limit) {
+      flag_error(p.err, PA_ERRFLAG_SLOT);
+      continue;
+    }
+    const long long blk = slot / p.block_size, off = slot % p.block_size;
+    const long long dst = ((blk * p.num_kv_heads + h) * p.block_size + off) * p.head_size + c * 16;
     reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.k_cache) + dst)[0] = make_uint4(kw[0], kw[1], kw[2], kw[3]);
     reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.v_cache) + dst)[0] = make_uint4(vw[0], vw[1], vw[2], vw[3]);
   }
@@ -144,7 +146,15 @@ __global__ void __launch_bounds__(256) scatter_nvfp4_kernel(const ScatterParams 
     const long long t = u / per_token;
     const int rem = static_cast<int>(u - t * per_token);
     const int h = rem / groups, g = rem % groups;
+    // the codes do not depend on the slot: their loads go out with the slot's
     const long long slot = p.slot_mapping[t];
+    const long long src = (t * p.num_kv_heads + h) * d + g * 16;
+    uint2 kcodes, vcodes;
+    uint8_t ksc, vsc;
+    quant_nvfp4_group<SRC>(reinterpret_cast<const typename SE::T*>(p.key) + src, p.k_scale[h * p.scale_stride],
+                           kcodes, ksc);
+    quant_nvfp4_group<SRC>(reinterpret_cast<const typename SE::T*>(p.value) + src, p.v_scale[h * p.scale_stride],
+                           vcodes, vsc);
     if (slot < 0) continue;
     if (slot >= limit) {
       flag_error(p.err, PA_ERRFLAG_SLOT);
@@ -152,20 +162,13 @@ __global__ void __launch_bounds__(256) scatter_nvfp4_kernel(const ScatterParams 
     }
     const long long blk = slot / bs;
     const int off = static_cast<int>(slot % bs);
-    const long long src = (t * p.num_kv_heads + h) * d + g * 16;
     const long long tbase = (blk * p.num_kv_heads + h) * tile;
     const long long code_at = tbase + off * (d / 2) + g * 8;
     const long long scale_at = tbase + (long long)bs * (d / 2) + off * (d / 16) + g;
-    uint2 codes;
-    uint8_t sc;
-    quant_nvfp4_group<SRC>(reinterpret_cast<const typename SE::T*>(p.key) + src, p.k_scale[h * p.scale_stride],
-                           codes, sc);
-    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.k_cache) + code_at) = codes;
-    static_cast<uint8_t*>(p.k_cache)[scale_at] = sc;
-    quant_nvfp4_group<SRC>(reinterpret_cast<const typename SE::T*>(p.value) + src, p.v_scale[h * p.scale_stride],
-                           codes, sc);
-    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.v_cache) + code_at) = codes;
-    static_cast<uint8_t*>(p.v_cache)[scale_at] = sc;
+    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.k_cache) + code_at) = kcodes;
+    static_cast<uint8_t*>(p.k_cache)[scale_at] = ksc;
+    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.v_cache) + code_at) = vcodes;
+    static_cast<uint8_t*>(p.v_cache)[scale_at] = vsc;
   }
 }
 
