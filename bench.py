@@ -797,7 +797,8 @@ def torch_sync(dev):
 # (entry name, workload, attention call).
 CONFIG_LEGS = (("tiny", "tiny", "decode"), ("llama", "llama", "decode"), ("mixed", "mixed", "varlen"),
                ("fp8", "fp8", "decode"), ("agentic_pa_decode", "agentic", "decode"),
-               ("mixed_fp8", "mixed_fp8", "varlen"), ("nvfp4", "nvfp4", "decode"))
+               ("mixed_fp8", "mixed_fp8", "varlen"), ("nvfp4", "nvfp4", "decode"),
+               ("fp8_e5m2", "fp8_e5m2", "decode"), ("mixed_nvfp4", "mixed_nvfp4", "varlen"))
 
 
 def compact(res, b, window=0) -> dict:
