@@ -49,3 +49,38 @@ def test_empty_requests_score_nothing():
     b = workloads.build("qk_empty", 5, [10, 30], [0, 2], 8, 2, 64, 16, "bf16")
     assert bench.qk_pairs(b) == 29 + 30 == _brute_pairs(b)
     assert np.diff(b.query_start_loc).tolist() == [0, 2]
+
+
+def test_byte_counts_of_the_agentic_forks():
+    """The headline's byte basis, from closed forms.  Forks share floor(0.96 * blocks)
+    whole blocks with their parent: the unique K/V tokens are each parent's whole context
+    plus each fork's private remainder; the shared-prefix split (each family's shared
+    prefix once, every sequence's private rest) covers exactly those bytes; the logical
+    bytes are every sequence's whole context."""
+    b = workloads.agentic(seed=2, host_cache=False, scale_lengths=1 / 300.0)
+    bs = b.block_size
+    kv_tok = 2 * b.num_kv_heads * b.head_size * workloads.ELEM_BYTES[b.kv_dtype]
+    unique = 0
+    for fam in b.families:
+        L = int(b.seq_lens[fam[0]])
+        if len(fam) == 1:
+            unique += L
+            continue
+        nshare = int(np.floor(0.96 * -(-L // bs)))
+        unique += L + (len(fam) - 1) * (L - nshare * bs)
+    assert bench.unique_kv_tokens(b) == unique
+    split = bench.shared_split_bytes(b, bench.prefix_groups(b))
+    assert split["shared"] + split["private"] == unique * kv_tok
+    nb = bench.algorithmic_bytes(b)
+    assert nb["unique_kv"] == unique * kv_tok
+    assert nb["logical_kv"] == int(b.seq_lens.sum()) * kv_tok
+    q_out = 2 * b.num_seqs * b.num_q_heads * b.head_size * workloads.ELEM_BYTES[b.q_dtype]
+    tables = 4 * sum(-(-int(n) // bs) for n in b.seq_lens) + 4 * b.num_seqs
+    assert nb["algorithmic"] == unique * kv_tok + q_out + tables
+    assert nb["logical_total"] == int(b.seq_lens.sum()) * kv_tok + q_out + tables
+
+
+def test_unique_bytes_without_sharing_are_the_logical_bytes():
+    b = workloads.build("noshare", 6, [100, 17, 64], [1, 1, 1], 8, 2, 64, 16, "bf16", host_cache=False)
+    nb = bench.algorithmic_bytes(b)
+    assert nb["unique_kv"] == nb["logical_kv"] == (100 + 17 + 64) * 2 * 2 * 64 * 2
